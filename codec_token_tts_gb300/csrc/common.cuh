@@ -1,0 +1,130 @@
+// Shared device helpers and kernel launch declarations of the tts_bb engine.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace ttsbb {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr int HID = 1024;      // hidden size
+constexpr int HD = 128;        // head dim
+constexpr int NQ = 16;         // query heads
+constexpr int NKV = 8;         // kv heads
+constexpr int QKV = (NQ + 2 * NKV) * HD;  // 4096 fused projection rows
+constexpr int KVB = 64;        // tokens per KV block
+
+// Device error word bits.
+enum : int { ERR_BAD_ID = 1, ERR_TIMEOUT = 2, ERR_KV_RANGE = 4 };
+
+__device__ __forceinline__ void set_err(int* err, int bit) {
+    if (err) atomicOr(err, bit);
+}
+
+__device__ __forceinline__ float bf2f(bf16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ bf16 f2bf(float x) { return __float2bfloat16_rn(x); }
+
+// 8 bf16 packed in a uint4 -> 8 floats
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Argmax packing: (order-preserving float bits << 32) | (~index), so a 64-bit
+// max picks the largest value and, among equal values, the lowest index.
+__device__ __forceinline__ unsigned long long pack_argmax(float v, int idx) {
+    uint32_t u = __float_as_uint(v);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
+}
+
+// ---------------------------------------------------------------- epilogues
+enum EpiMode : int {
+    EPI_STORE_F32 = 0,   // out_f32[t*ldo + n] = acc
+    EPI_STORE_BF16 = 1,  // out_bf16[t*ldo + n] = acc
+    EPI_ADD_F32 = 2,     // out_f32[t*ldo + n] += acc (residual)
+    EPI_SWIGLU = 3,      // rows interleaved gate/up: out_bf16[t*ldo + n/2] = silu(g)*u
+    EPI_LOGITS = 4,      // out_f32 (optional) + packed argmax per row (optional)
+    EPI_LOGITS_PERM = 5  // OmniVoice audio heads: out[((b*G + k)*R + s)*V + v]
+};
+
+struct Epi {
+    int mode;
+    void* out;
+    int ldo;
+    unsigned long long* amax;  // EPI_LOGITS: [T] packed argmax
+    int perm_rows;             // EPI_LOGITS_PERM: rows per batch (R)
+    int perm_vocab;            // V
+    int perm_groups;           // G
+};
+
+// ---------------------------------------------------------------- kernels
+struct TableSet {
+    const bf16* tab[16];
+    int rows[16];
+    int n;
+};
+
+// h[t] = embeds[t] (optional) + sum_k E_k[ids[t][k]] (ids[t][k] == -1 skipped)
+int launch_embed_codebooks(const TableSet& ts, const int32_t* ids, const bf16* embeds,
+                            float* h, int T, int* err, cudaStream_t st);
+// OmniVoice hybrid embedding; tokens t = b*S + s
+int launch_embed_omnivoice(const bf16* text, int text_vocab, const bf16* audio, int n_cb, int vocab,
+                            const int32_t* ids, const uint8_t* mask, float* h, int B, int S, int* err,
+                            cudaStream_t st);
+// y[t] = bf16(rmsnorm(h[src(t)]) * gamma); src(t) = (t / per) * stride + offset + t % per,
+// or, when last_len != nullptr, src(t) = t * stride + last_len[t] - 1.
+int launch_rmsnorm(const float* h, const bf16* gamma, bf16* y, int T, float eps, int per, int stride,
+                    int offset, const int32_t* last_len, cudaStream_t st);
+// Y = X W^T with epilogue; X [T][K] bf16, W [N][K] bf16. T small (<= 8).
+int launch_gemv(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st);
+// Y = X W^T with epilogue, tensor cores, any T.
+int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st);
+
+// Per-token q/k RMSNorm + RoPE; q -> qout [T][16][128] bf16; k, v -> paged pool.
+// Token t belongs to sequence t / tok_per_seq at position seq_start[seq] + t % tok_per_seq,
+// valid when t % tok_per_seq < seq_len[seq]. Block of (seq, j): page_table[seq_slot[seq]*mbps + j]
+// or, when page_table is null, seq*mbps + j.
+struct KVView {
+    bf16* pool;            // layer base: [blocks][2][8][64][128]
+    const int32_t* page_table;
+    const int32_t* seq_slot;
+    int mbps;              // blocks per slot row of the page table
+};
+int launch_qk_norm_rope_append(const float* qkv, const bf16* qn, const bf16* kn, const float* cos_t,
+                                const float* sin_t, float eps, bf16* qout, KVView kv, const int32_t* seq_start,
+                                const int32_t* seq_len, int tok_per_seq, int T, int* err, cudaStream_t st);
+// Decode attention, one query per sequence: split-K flash decode + combine.
+int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B, int max_len,
+                        float* part, bf16* out, int max_splits, cudaStream_t st);
+// Prefill / bidirectional attention over the paged view, tensor cores.
+// causal: query at position p sees keys <= p; else keys < key_len[seq].
+int launch_attn_prefill(const bf16* q, KVView kv, const int32_t* seq_start, const int32_t* seq_len,
+                         const int32_t* key_len, int causal, int B, int S, bf16* out, cudaStream_t st);
+// out[b * stride] = unpacked argmax
+int launch_argmax_finalize(const unsigned long long* amax, int32_t* out, int stride, int B, cudaStream_t st);
+
+}  // namespace ttsbb

@@ -1,0 +1,720 @@
+// Host engine and C ABI (include/tts_bb.h): weight ownership, the paged KV
+// block pool and page tables, per-call validation, and the layer schedule of
+// the backbone step (Talker / Code-Predictor prefill and decode, MaskGIT pass).
+#include <algorithm>
+#include <cstdarg>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "../../include/tts_bb.h"
+
+using namespace ttsbb;
+
+#define TTS_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+constexpr int MAX_B = 256;        // sequences per call (per-call arrays travel as kernel parameters)
+constexpr int MAX_UPD = 1024;     // page-table updates per setup launch
+constexpr int MAX_SPLITS = 64;    // decode attention splits
+
+// Per-call sequence description and page-table updates, passed by value.
+struct SetupArgs {
+    int B;
+    int n_upd;
+    int clear_amax;
+    int32_t slot[MAX_B];
+    int32_t start[MAX_B];
+    int32_t len[MAX_B];
+    int32_t key_len[MAX_B];
+    int32_t upd_idx[MAX_UPD];
+    int32_t upd_val[MAX_UPD];
+};
+
+__global__ void k_setup(SetupArgs a, int32_t* seq_slot, int32_t* seq_start, int32_t* seq_len, int32_t* key_len,
+                        int32_t* page_table, unsigned long long* amax) {
+    for (int i = threadIdx.x; i < a.B; i += blockDim.x) {
+        seq_slot[i] = a.slot[i];
+        seq_start[i] = a.start[i];
+        seq_len[i] = a.len[i];
+        key_len[i] = a.key_len[i];
+        if (a.clear_amax) amax[i] = 0ull;
+    }
+    for (int i = threadIdx.x; i < a.n_upd; i += blockDim.x) page_table[a.upd_idx[i]] = a.upd_val[i];
+}
+
+__global__ void k_kv_copy(bf16* pool, const int32_t* page_table, int slot, int mbps, int pos0, int n, bf16* k,
+                          bf16* v, int to_pool) {
+    // one CTA per token, 256 threads: 8 kv heads x 128 elements, 4 per thread for K and V
+    const int t = blockIdx.x;
+    const int pos = pos0 + t;
+    const int phys = page_table[(size_t)slot * mbps + pos / KVB];
+    for (int e = threadIdx.x; e < NKV * HD; e += blockDim.x) {
+        const int g = e / HD, d = e % HD;
+        const size_t pk = (((size_t)phys * 2 + 0) * NKV + g) * KVB * HD + (size_t)(pos % KVB) * HD + d;
+        const size_t pv = pk + (size_t)NKV * KVB * HD;
+        const size_t io = (size_t)t * NKV * HD + e;
+        if (to_pool) {
+            pool[pk] = k[io];
+            pool[pv] = v[io];
+        } else {
+            k[io] = pool[pk];
+            v[io] = pool[pv];
+        }
+    }
+}
+
+struct LayerW {
+    bf16 *in_norm, *wqkv, *qn, *kn, *wo, *post_norm, *wgu, *wd;
+};
+
+}  // namespace
+
+struct tts_bb {
+    tts_bb_config cfg;
+    cudaStream_t st = nullptr;
+    int dev = 0;
+    std::vector<void*> allocs;
+    std::vector<LayerW> L;
+    TableSet tabs{};
+    bf16* text = nullptr;
+    bf16* audio = nullptr;
+    bf16* final_norm = nullptr;
+    bf16* heads[TTS_BB_MAX_HEADS] = {};
+    float* cos_t = nullptr;
+    float* sin_t = nullptr;
+    int rope_len = 0;
+    // KV
+    bf16* pool = nullptr;
+    size_t layer_elems = 0;   // elements per layer of the pool
+    int kv_blocks = 0, mbps = 0;
+    int32_t* d_page_table = nullptr;
+    std::vector<int32_t> page_table;
+    std::vector<int> slot_len;
+    std::vector<int> free_blocks;
+    // scratch
+    int T_cap = 0;
+    float* h = nullptr;
+    bf16* y = nullptr;
+    float* qkv = nullptr;
+    bf16* q = nullptr;
+    bf16* ao = nullptr;
+    bf16* m = nullptr;
+    float* part = nullptr;
+    unsigned long long* amax = nullptr;
+    int32_t *seq_slot = nullptr, *seq_start = nullptr, *seq_len = nullptr, *key_len = nullptr;
+    bf16* mg_pool = nullptr;
+    size_t mg_pool_blocks = 0;
+    int* err = nullptr;
+    int* h_err = nullptr;
+    std::string last_error;
+    uint64_t launches = 0;
+    SetupArgs* setup = nullptr;  // host staging (large struct)
+};
+
+namespace {
+
+tts_bb_status fail(tts_bb* h, tts_bb_status s, const char* fmt, ...) __attribute__((format(printf, 3, 4)));
+tts_bb_status fail(tts_bb* h, tts_bb_status s, const char* fmt, ...) {
+    if (h) {
+        char buf[512];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        h->last_error = buf;
+    }
+    return s;
+}
+
+tts_bb_status cuda_fail(tts_bb* h, cudaError_t e, const char* what) {
+    return fail(h, e == cudaErrorMemoryAllocation ? TTS_BB_E_OOM : TTS_BB_E_CUDA, "%s: %s", what,
+                cudaGetErrorString(e));
+}
+
+template <typename T>
+cudaError_t dalloc(tts_bb* h, T** p, size_t n) {
+    void* v = nullptr;
+    const cudaError_t e = cudaMalloc(&v, std::max<size_t>(n, 1) * sizeof(T));
+    if (e == cudaSuccess) {
+        h->allocs.push_back(v);
+        *p = reinterpret_cast<T*>(v);
+    }
+    return e;
+}
+
+bool cfg_supported(const tts_bb_config& c, std::string& why) {
+    if (c.hidden != HID || c.n_q_heads != NQ || c.n_kv_heads != NKV || c.head_dim != HD) {
+        why = "kernels are built for hidden 1024, 16 q / 8 kv heads of 128";
+        return false;
+    }
+    if (c.ffn % 256 != 0 || c.ffn <= 0 || c.ffn > 3072) {
+        why = "ffn must be a positive multiple of 256, at most 3072";
+        return false;
+    }
+    return true;
+}
+
+tts_bb_status check_launch(tts_bb* h, const char* what) {
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(h, e, what);
+    return TTS_BB_OK;
+}
+
+// Read (and clear) the device error word; synchronises the stream.
+tts_bb_status read_err(tts_bb* h) {
+    cudaError_t e = cudaMemcpyAsync(h->h_err, h->err, sizeof(int), cudaMemcpyDeviceToHost, h->st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "stream");
+    const int v = *h->h_err;
+    if (v) {
+        cudaMemsetAsync(h->err, 0, sizeof(int), h->st);
+        cudaStreamSynchronize(h->st);
+        if (v & ERR_TIMEOUT) return fail(h, TTS_BB_E_DEVICE_TIMEOUT, "a device-side wait timed out");
+        if (v & ERR_BAD_ID) return fail(h, TTS_BB_E_BAD_ID, "a token id was outside its table (skipped)");
+        if (v & ERR_KV_RANGE) return fail(h, TTS_BB_E_INVALID, "a KV position had no block");
+    }
+    return TTS_BB_OK;
+}
+
+tts_bb_status finish(tts_bb* h) {
+    tts_bb_status s = check_launch(h, "kernel launch");
+    if (s != TTS_BB_OK) return s;
+    if (h->cfg.sync_errors) return read_err(h);
+    return TTS_BB_OK;
+}
+
+// Scratch for T tokens (grows on demand; only between calls).
+tts_bb_status ensure_scratch(tts_bb* h, int T) {
+    if (T <= h->T_cap) return TTS_BB_OK;
+    if (h->h) {
+        cudaStreamSynchronize(h->st);
+        void* olds[] = {h->h, h->y, h->qkv, h->q, h->ao, h->m};
+        for (void* p : olds) {
+            cudaFree(p);
+            h->allocs.erase(std::remove(h->allocs.begin(), h->allocs.end(), p), h->allocs.end());
+        }
+    }
+    cudaError_t e;
+    if ((e = dalloc(h, &h->h, (size_t)T * HID)) != cudaSuccess ||
+        (e = dalloc(h, &h->y, (size_t)T * HID)) != cudaSuccess ||
+        (e = dalloc(h, &h->qkv, (size_t)T * QKV)) != cudaSuccess ||
+        (e = dalloc(h, &h->q, (size_t)T * NQ * HD)) != cudaSuccess ||
+        (e = dalloc(h, &h->ao, (size_t)T * NQ * HD)) != cudaSuccess ||
+        (e = dalloc(h, &h->m, (size_t)T * h->cfg.ffn)) != cudaSuccess) {
+        h->T_cap = 0;
+        h->h = nullptr;
+        return cuda_fail(h, e, "scratch allocation");
+    }
+    h->T_cap = T;
+    return TTS_BB_OK;
+}
+
+void launch_setup(tts_bb* h, SetupArgs& a) {
+    k_setup<<<1, 256, 0, h->st>>>(a, h->seq_slot, h->seq_start, h->seq_len, h->key_len, h->d_page_table, h->amax);
+    h->launches++;
+}
+
+// The layer schedule shared by every mode. T tokens laid out as B sequences x
+// tok_per_seq positions; mode: 0 decode (query length 1), 1 causal prefill,
+// 2 bidirectional pass.
+void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView kv_base, size_t layer_stride) {
+    const tts_bb_config& c = h->cfg;
+    const int T = B * tok_per_seq;
+    for (int l = 0; l < c.n_layers; ++l) {
+        const LayerW& w = h->L[l];
+        KVView kv = kv_base;
+        kv.pool = kv_base.pool + (size_t)l * layer_stride;
+        h->launches += launch_rmsnorm(h->h, w.in_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st);
+        Epi e{};
+        e.mode = EPI_STORE_F32; e.out = h->qkv; e.ldo = QKV;
+        h->launches += launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st);
+        h->launches += launch_qk_norm_rope_append(h->qkv, w.qn, w.kn, h->cos_t, h->sin_t, c.rms_eps, h->q, kv,
+                                                  h->seq_start, h->seq_len, tok_per_seq, T, h->err, h->st);
+        if (mode == 0)
+            h->launches += launch_attn_decode(h->q, kv, h->seq_start, B, max_len, h->part, h->ao, MAX_SPLITS, h->st);
+        else
+            h->launches += launch_attn_prefill(h->q, kv, h->seq_start, h->seq_len, h->key_len, mode == 1, B,
+                                               tok_per_seq, h->ao, h->st);
+        e = Epi{};
+        e.mode = EPI_ADD_F32; e.out = h->h; e.ldo = HID;
+        h->launches += launch_gemm(h->ao, w.wo, T, HID, NQ * HD, e, h->st);
+        h->launches += launch_rmsnorm(h->h, w.post_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st);
+        e = Epi{};
+        e.mode = EPI_SWIGLU; e.out = h->m; e.ldo = c.ffn;
+        h->launches += launch_gemm(h->y, w.wgu, T, 2 * c.ffn, HID, e, h->st);
+        e = Epi{};
+        e.mode = EPI_ADD_F32; e.out = h->h; e.ldo = HID;
+        h->launches += launch_gemm(h->m, w.wd, T, HID, c.ffn, e, h->st);
+    }
+}
+
+// Final norm of B selected rows + head GEMM with logits / argmax.
+void run_head(tts_bb* h, int B, int per_seq, int head_idx, bool last_of_seq, float* logits_out, int32_t* argmax_out,
+              int argmax_stride) {
+    const tts_bb_config& c = h->cfg;
+    h->launches += launch_rmsnorm(h->h, h->final_norm, h->y, B, c.rms_eps, 1, per_seq, 0,
+                                  last_of_seq ? h->seq_len : nullptr, h->st);
+    Epi e{};
+    e.mode = EPI_LOGITS; e.out = logits_out; e.ldo = c.head_rows; e.amax = argmax_out ? h->amax : nullptr;
+    h->launches += launch_gemm(h->y, h->heads[head_idx], B, c.head_rows, HID, e, h->st);
+    if (argmax_out) h->launches += launch_argmax_finalize(h->amax, argmax_out, argmax_stride, B, h->st);
+}
+
+bool slots_ok(tts_bb* h, int B, const int32_t* slots) {
+    if (!slots) return false;
+    std::vector<char> seen(h->cfg.max_slots, 0);
+    for (int b = 0; b < B; ++b) {
+        if (slots[b] < 0 || slots[b] >= h->cfg.max_slots || seen[slots[b]]) return false;
+        seen[slots[b]] = 1;
+    }
+    return true;
+}
+
+// Reserve the blocks that growing each slot to new_len[b] needs; all or nothing.
+tts_bb_status grow_slots(tts_bb* h, int B, const int32_t* slots, const int* new_len, SetupArgs& a) {
+    int need = 0;
+    for (int b = 0; b < B; ++b) {
+        const int have = (h->slot_len[slots[b]] + KVB - 1) / KVB;
+        const int want = (new_len[b] + KVB - 1) / KVB;
+        need += std::max(0, want - have);
+    }
+    if (need > (int)h->free_blocks.size())
+        return fail(h, TTS_BB_E_OOM, "KV block pool exhausted: need %d blocks, %zu free", need, h->free_blocks.size());
+    a.n_upd = 0;
+    std::vector<std::pair<int, int>> upd;
+    for (int b = 0; b < B; ++b) {
+        const int s = slots[b];
+        const int have = (h->slot_len[s] + KVB - 1) / KVB;
+        const int want = (new_len[b] + KVB - 1) / KVB;
+        for (int j = have; j < want; ++j) {
+            const int blk = h->free_blocks.back();
+            h->free_blocks.pop_back();
+            h->page_table[(size_t)s * h->mbps + j] = blk;
+            upd.push_back({s * h->mbps + j, blk});
+        }
+    }
+    // updates beyond what one setup launch carries go in extra launches first
+    size_t i = 0;
+    while (upd.size() - i > (size_t)MAX_UPD) {
+        SetupArgs* ex = new SetupArgs();
+        ex->B = 0;
+        ex->n_upd = MAX_UPD;
+        for (int k = 0; k < MAX_UPD; ++k, ++i) { ex->upd_idx[k] = upd[i].first; ex->upd_val[k] = upd[i].second; }
+        launch_setup(h, *ex);
+        delete ex;
+    }
+    for (; i < upd.size(); ++i) {
+        a.upd_idx[a.n_upd] = upd[i].first;
+        a.upd_val[a.n_upd] = upd[i].second;
+        a.n_upd++;
+    }
+    return TTS_BB_OK;
+}
+
+}  // namespace
+
+// ============================================================== C ABI
+TTS_API void tts_bb_default_config(tts_bb_config* c) {
+    if (!c) return;
+    std::memset(c, 0, sizeof *c);
+    c->n_layers = 28;
+    c->hidden = 1024;
+    c->n_q_heads = 16;
+    c->n_kv_heads = 8;
+    c->head_dim = 128;
+    c->ffn = 3072;
+    c->rms_eps = 1e-6f;
+    c->rope_theta = 1e6f;
+    c->n_codebooks = 16;
+    c->codebook_rows[0] = 3072;
+    for (int k = 1; k < 16; ++k) c->codebook_rows[k] = 2048;
+    c->n_heads = 1;
+    c->head_rows = 3072;
+    c->max_slots = 64;
+    c->max_ctx = 4096;
+    c->max_batch = 64;
+    c->max_tokens = 4096;
+    c->sync_errors = 1;
+}
+
+TTS_API const char* tts_bb_version(void) { return "0.1.0 (sm_103a)"; }
+
+TTS_API const char* tts_bb_last_error(const tts_bb* h) { return h ? h->last_error.c_str() : "null handle"; }
+
+TTS_API uint64_t tts_bb_launch_count(const tts_bb* h) { return h ? h->launches : 0; }
+
+TTS_API void tts_bb_free(tts_bb* h) {
+    if (!h) return;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    cudaSetDevice(h->dev);
+    if (h->st) cudaStreamSynchronize(h->st);
+    else cudaDeviceSynchronize();
+    for (void* p : h->allocs) cudaFree(p);
+    if (h->h_err) cudaFreeHost(h->h_err);
+    delete h->setup;
+    cudaSetDevice(cur);
+    delete h;
+}
+
+TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weights* w, void* stream, tts_bb** out) {
+    if (out) *out = nullptr;
+    if (!cfg || !w || !out) return TTS_BB_E_INVALID;
+    const tts_bb_config& c = *cfg;
+    if (c.n_layers < 0 || c.n_layers > 256 || c.max_batch <= 0 || c.max_batch > MAX_B || c.max_tokens < 0 ||
+        c.max_slots < 0 || c.max_ctx < 0 || c.n_codebooks < 0 || c.n_codebooks > TTS_BB_MAX_CODEBOOKS ||
+        c.n_heads < 0 || c.n_heads > TTS_BB_MAX_HEADS || (c.n_heads > 0 && c.head_rows <= 0) || !(c.rms_eps > 0.f) ||
+        !(c.rope_theta > 1.f) || (c.max_slots > 0 && c.max_ctx <= 0) || c.kv_blocks < 0)
+        return TTS_BB_E_INVALID;
+    std::string why;
+    if (!cfg_supported(c, why)) return TTS_BB_E_UNSUPPORTED;
+    if ((c.n_layers > 0 && !w->layer) || !w->final_norm) return TTS_BB_E_INVALID;
+    for (int k = 0; k < c.n_codebooks; ++k)
+        if (!w->codebook[k] || c.codebook_rows[k] <= 0) return TTS_BB_E_INVALID;
+    const bool omni = c.text_vocab > 0 || c.audio_codebooks > 0;
+    if (omni && (c.text_vocab <= 0 || c.audio_codebooks <= 0 || c.audio_vocab <= 0 || !w->text_table ||
+                 !w->audio_table))
+        return TTS_BB_E_INVALID;
+    const int n_head_mats = omni ? (c.n_heads > 0 ? 1 : 0) : c.n_heads;
+    for (int j = 0; j < n_head_mats; ++j)
+        if (!w->head[j]) return TTS_BB_E_INVALID;
+    for (int l = 0; l < c.n_layers; ++l)
+        for (int r = 0; r < TTS_BB_LAYER_TENSORS; ++r)
+            if (!w->layer[l * TTS_BB_LAYER_TENSORS + r]) return TTS_BB_E_INVALID;
+
+    tts_bb* h = new tts_bb();
+    h->cfg = c;
+    h->st = reinterpret_cast<cudaStream_t>(stream);
+    cudaGetDevice(&h->dev);
+    h->setup = new SetupArgs();
+    auto bail = [&](tts_bb_status s) {
+        tts_bb_free(h);
+        return s;
+    };
+    cudaError_t e;
+    const size_t H = HID, F = c.ffn;
+    // weights: one allocation per tensor family
+    auto copy = [&](bf16* dst, const void* src, size_t n) {
+        return cudaMemcpy(dst, src, n * sizeof(bf16), cudaMemcpyDefault);
+    };
+    h->L.resize(c.n_layers);
+    for (int l = 0; l < c.n_layers; ++l) {
+        const void* const* t = w->layer + (size_t)l * TTS_BB_LAYER_TENSORS;
+        LayerW& lw = h->L[l];
+        bf16* blk = nullptr;
+        const size_t n = 3 * H + 2 * HD + (size_t)QKV * H + H * NQ * HD + 2 * F * H + H * F;
+        if ((e = dalloc(h, &blk, n)) != cudaSuccess) return bail(TTS_BB_E_OOM);
+        lw.in_norm = blk;
+        lw.post_norm = lw.in_norm + H;
+        lw.qn = lw.post_norm + H;
+        lw.kn = lw.qn + HD;
+        lw.wqkv = lw.kn + HD + H;  // keep 16-byte alignment
+        lw.wo = lw.wqkv + (size_t)QKV * H;
+        lw.wgu = lw.wo + H * NQ * HD;
+        lw.wd = lw.wgu + 2 * F * H;
+        if ((e = copy(lw.in_norm, t[TTS_BB_W_IN_NORM], H)) != cudaSuccess ||
+            (e = copy(lw.post_norm, t[TTS_BB_W_POST_NORM], H)) != cudaSuccess ||
+            (e = copy(lw.qn, t[TTS_BB_W_Q_NORM], HD)) != cudaSuccess ||
+            (e = copy(lw.kn, t[TTS_BB_W_K_NORM], HD)) != cudaSuccess ||
+            (e = copy(lw.wqkv, t[TTS_BB_W_Q], (size_t)NQ * HD * H)) != cudaSuccess ||
+            (e = copy(lw.wqkv + (size_t)NQ * HD * H, t[TTS_BB_W_K], (size_t)NKV * HD * H)) != cudaSuccess ||
+            (e = copy(lw.wqkv + (size_t)(NQ + NKV) * HD * H, t[TTS_BB_W_V], (size_t)NKV * HD * H)) != cudaSuccess ||
+            (e = copy(lw.wo, t[TTS_BB_W_O], H * NQ * HD)) != cudaSuccess ||
+            (e = copy(lw.wd, t[TTS_BB_W_DOWN], H * F)) != cudaSuccess)
+            return bail(cuda_fail(h, e, "weight copy"));
+        // gate/up interleaved by row: row 2i = gate_i, row 2i+1 = up_i
+        if ((e = cudaMemcpy2D(lw.wgu, 2 * H * sizeof(bf16), t[TTS_BB_W_GATE], H * sizeof(bf16), H * sizeof(bf16), F,
+                              cudaMemcpyDefault)) != cudaSuccess ||
+            (e = cudaMemcpy2D(lw.wgu + H, 2 * H * sizeof(bf16), t[TTS_BB_W_UP], H * sizeof(bf16), H * sizeof(bf16), F,
+                              cudaMemcpyDefault)) != cudaSuccess)
+            return bail(cuda_fail(h, e, "weight copy"));
+    }
+    h->tabs.n = c.n_codebooks;
+    for (int k = 0; k < c.n_codebooks; ++k) {
+        bf16* p = nullptr;
+        if ((e = dalloc(h, &p, (size_t)c.codebook_rows[k] * H)) != cudaSuccess) return bail(TTS_BB_E_OOM);
+        if ((e = copy(p, w->codebook[k], (size_t)c.codebook_rows[k] * H)) != cudaSuccess)
+            return bail(cuda_fail(h, e, "table copy"));
+        h->tabs.tab[k] = p;
+        h->tabs.rows[k] = c.codebook_rows[k];
+    }
+    if (omni) {
+        if ((e = dalloc(h, &h->text, (size_t)c.text_vocab * H)) != cudaSuccess ||
+            (e = dalloc(h, &h->audio, (size_t)c.audio_codebooks * c.audio_vocab * H)) != cudaSuccess)
+            return bail(TTS_BB_E_OOM);
+        if ((e = copy(h->text, w->text_table, (size_t)c.text_vocab * H)) != cudaSuccess ||
+            (e = copy(h->audio, w->audio_table, (size_t)c.audio_codebooks * c.audio_vocab * H)) != cudaSuccess)
+            return bail(cuda_fail(h, e, "table copy"));
+    }
+    if ((e = dalloc(h, &h->final_norm, H)) != cudaSuccess) return bail(TTS_BB_E_OOM);
+    if ((e = copy(h->final_norm, w->final_norm, H)) != cudaSuccess) return bail(cuda_fail(h, e, "norm copy"));
+    for (int j = 0; j < n_head_mats; ++j) {
+        const size_t rows = omni ? (size_t)c.n_heads * c.head_rows : (size_t)c.head_rows;
+        if ((e = dalloc(h, &h->heads[j], rows * H)) != cudaSuccess) return bail(TTS_BB_E_OOM);
+        if ((e = copy(h->heads[j], w->head[j], rows * H)) != cudaSuccess) return bail(cuda_fail(h, e, "head copy"));
+    }
+    // RoPE tables, computed in double on the host: angle = pos * theta^(-2i/128)
+    h->rope_len = std::max(std::max(c.max_ctx, c.max_tokens), 1);
+    {
+        std::vector<float> ct((size_t)h->rope_len * (HD / 2)), sn((size_t)h->rope_len * (HD / 2));
+        for (int p = 0; p < h->rope_len; ++p)
+            for (int i = 0; i < HD / 2; ++i) {
+                const double inv = std::pow((double)c.rope_theta, -2.0 * i / HD);
+                const double a = (double)p * inv;
+                ct[(size_t)p * (HD / 2) + i] = (float)std::cos(a);
+                sn[(size_t)p * (HD / 2) + i] = (float)std::sin(a);
+            }
+        if ((e = dalloc(h, &h->cos_t, ct.size())) != cudaSuccess || (e = dalloc(h, &h->sin_t, sn.size())) != cudaSuccess)
+            return bail(TTS_BB_E_OOM);
+        cudaMemcpy(h->cos_t, ct.data(), ct.size() * sizeof(float), cudaMemcpyHostToDevice);
+        cudaMemcpy(h->sin_t, sn.data(), sn.size() * sizeof(float), cudaMemcpyHostToDevice);
+    }
+    // KV pool [layer][block][K|V][8][64][128]
+    if (c.max_slots > 0) {
+        h->mbps = (c.max_ctx + KVB - 1) / KVB;
+        h->kv_blocks = c.kv_blocks > 0 ? c.kv_blocks : c.max_slots * h->mbps;
+        if (const char* cap = std::getenv("TTS_BB_MAX_BLOCKS")) h->kv_blocks = std::min(h->kv_blocks, std::atoi(cap));
+        h->layer_elems = (size_t)h->kv_blocks * 2 * NKV * KVB * HD;
+        if ((e = dalloc(h, &h->pool, h->layer_elems * c.n_layers)) != cudaSuccess) return bail(TTS_BB_E_OOM);
+        if ((e = dalloc(h, &h->d_page_table, (size_t)c.max_slots * h->mbps)) != cudaSuccess) return bail(TTS_BB_E_OOM);
+        h->page_table.assign((size_t)c.max_slots * h->mbps, -1);
+        cudaMemcpy(h->d_page_table, h->page_table.data(), h->page_table.size() * sizeof(int32_t),
+                   cudaMemcpyHostToDevice);
+        h->slot_len.assign(c.max_slots, 0);
+        h->free_blocks.resize(h->kv_blocks);
+        for (int i = 0; i < h->kv_blocks; ++i) h->free_blocks[i] = h->kv_blocks - 1 - i;  // pop_back gives 0, 1, ...
+    }
+    const int nb = std::max(c.max_batch, 1);
+    if ((e = dalloc(h, &h->part, (size_t)nb * NQ * MAX_SPLITS * (HD + 2))) != cudaSuccess ||
+        (e = dalloc(h, &h->amax, (size_t)std::max(nb, c.max_tokens))) != cudaSuccess ||
+        (e = dalloc(h, &h->seq_slot, MAX_B)) != cudaSuccess || (e = dalloc(h, &h->seq_start, MAX_B)) != cudaSuccess ||
+        (e = dalloc(h, &h->seq_len, MAX_B)) != cudaSuccess || (e = dalloc(h, &h->key_len, MAX_B)) != cudaSuccess ||
+        (e = dalloc(h, &h->err, 1)) != cudaSuccess)
+        return bail(TTS_BB_E_OOM);
+    if ((e = cudaMallocHost(&h->h_err, sizeof(int))) != cudaSuccess) return bail(TTS_BB_E_OOM);
+    cudaMemset(h->err, 0, sizeof(int));
+    tts_bb_status s = ensure_scratch(h, std::max(nb, std::max(c.max_tokens, 1)));
+    if (s != TTS_BB_OK) return bail(s);
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return bail(cuda_fail(h, e, "create"));
+    *out = h;
+    return TTS_BB_OK;
+}
+
+TTS_API int tts_bb_slot_len(const tts_bb* h, int slot) {
+    if (!h || slot < 0 || slot >= h->cfg.max_slots) return -1;
+    return h->slot_len[slot];
+}
+
+TTS_API tts_bb_status tts_bb_truncate(tts_bb* h, int slot, int len) {
+    if (!h) return TTS_BB_E_INVALID;
+    if (slot < 0 || slot >= h->cfg.max_slots) return fail(h, TTS_BB_E_INVALID, "slot %d out of range", slot);
+    if (len < 0 || len > h->slot_len[slot]) return fail(h, TTS_BB_E_INVALID, "truncate length %d invalid", len);
+    const int keep = (len + KVB - 1) / KVB, have = (h->slot_len[slot] + KVB - 1) / KVB;
+    for (int j = keep; j < have; ++j) {
+        int32_t& e = h->page_table[(size_t)slot * h->mbps + j];
+        h->free_blocks.push_back(e);
+        e = -1;
+    }
+    h->slot_len[slot] = len;
+    // the device copy of freed entries is not cleared: freed blocks are only
+    // reachable again after a new append rewrites the entry.
+    return TTS_BB_OK;
+}
+
+TTS_API tts_bb_status tts_bb_release(tts_bb* h, int slot) { return tts_bb_truncate(h, slot, 0); }
+
+TTS_API tts_bb_status tts_bb_sync(tts_bb* h) {
+    if (!h) return TTS_BB_E_INVALID;
+    return read_err(h);
+}
+
+TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots, const int32_t* kv_lens,
+                                         const int32_t* ids, int head_idx, float* logits_out, int32_t* argmax_out,
+                                         const tts_bb_opts* opts) {
+    if (!h) return TTS_BB_E_INVALID;
+    const tts_bb_config& c = h->cfg;
+    if (c.max_slots <= 0) return fail(h, TTS_BB_E_UNSUPPORTED, "handle has no KV cache");
+    if (B <= 0 || B > c.max_batch) return fail(h, TTS_BB_E_INVALID, "B=%d outside 1..%d", B, c.max_batch);
+    if (!slots_ok(h, B, slots)) return fail(h, TTS_BB_E_INVALID, "slots must be distinct and in range");
+    if (!kv_lens) return fail(h, TTS_BB_E_INVALID, "kv_lens is NULL");
+    const void* embeds = opts ? opts->embeds : nullptr;
+    if (!ids && !embeds) return fail(h, TTS_BB_E_INVALID, "need ids or embeds");
+    if (ids && c.n_codebooks == 0) return fail(h, TTS_BB_E_INVALID, "handle has no codebook tables");
+    if (head_idx >= c.n_heads || head_idx < -1) return fail(h, TTS_BB_E_INVALID, "head_idx %d out of range", head_idx);
+    if (head_idx < 0 && (logits_out || argmax_out)) return fail(h, TTS_BB_E_INVALID, "outputs need a head");
+    int max_len = 0;
+    std::vector<int> nl(B);
+    for (int b = 0; b < B; ++b) {
+        if (kv_lens[b] != h->slot_len[slots[b]])
+            return fail(h, TTS_BB_E_INVALID, "kv_lens[%d]=%d but slot %d holds %d tokens", b, kv_lens[b], slots[b],
+                        h->slot_len[slots[b]]);
+        if (kv_lens[b] + 1 > c.max_ctx) return fail(h, TTS_BB_E_INVALID, "slot %d would exceed max_ctx", slots[b]);
+        nl[b] = kv_lens[b] + 1;
+        max_len = std::max(max_len, nl[b]);
+    }
+    SetupArgs& a = *h->setup;
+    a.B = B;
+    a.clear_amax = argmax_out != nullptr;
+    tts_bb_status s = grow_slots(h, B, slots, nl.data(), a);
+    if (s != TTS_BB_OK) return s;
+    for (int b = 0; b < B; ++b) {
+        a.slot[b] = slots[b];
+        a.start[b] = kv_lens[b];
+        a.len[b] = 1;
+        a.key_len[b] = nl[b];
+        h->slot_len[slots[b]] = nl[b];
+    }
+    launch_setup(h, a);
+    h->launches += launch_embed_codebooks(h->tabs, ids, reinterpret_cast<const bf16*>(embeds), h->h, B, h->err, h->st);
+    KVView kv{h->pool, h->d_page_table, h->seq_slot, h->mbps};
+    run_layers(h, B, 1, 0, max_len, kv, h->layer_elems);
+    if (opts && opts->hidden_out)
+        cudaMemcpyAsync(opts->hidden_out, h->h, (size_t)B * HID * sizeof(float), cudaMemcpyDeviceToDevice, h->st);
+    if (head_idx >= 0 && (logits_out || argmax_out))
+        run_head(h, B, 1, head_idx, false, logits_out, argmax_out, opts && opts->argmax_stride ? opts->argmax_stride : 1);
+    return finish(h);
+}
+
+TTS_API tts_bb_status tts_bb_prefill(tts_bb* h, int B, int S, const int32_t* slots, const int32_t* lens,
+                                     const int32_t* ids, int head_idx, float* logits_out, int32_t* argmax_out,
+                                     const tts_bb_opts* opts) {
+    if (!h) return TTS_BB_E_INVALID;
+    const tts_bb_config& c = h->cfg;
+    if (c.max_slots <= 0) return fail(h, TTS_BB_E_UNSUPPORTED, "handle has no KV cache");
+    if (B <= 0 || B > c.max_batch || S <= 0 || (long)B * S > std::max(c.max_tokens, c.max_batch))
+        return fail(h, TTS_BB_E_INVALID, "B=%d S=%d outside the configured sizes", B, S);
+    if (!slots_ok(h, B, slots)) return fail(h, TTS_BB_E_INVALID, "slots must be distinct and in range");
+    if (!lens) return fail(h, TTS_BB_E_INVALID, "lens is NULL");
+    const void* embeds = opts ? opts->embeds : nullptr;
+    if (!ids && !embeds) return fail(h, TTS_BB_E_INVALID, "need ids or embeds");
+    if (ids && c.n_codebooks == 0) return fail(h, TTS_BB_E_INVALID, "handle has no codebook tables");
+    if (head_idx >= c.n_heads || head_idx < -1) return fail(h, TTS_BB_E_INVALID, "head_idx %d out of range", head_idx);
+    if (head_idx < 0 && (logits_out || argmax_out)) return fail(h, TTS_BB_E_INVALID, "outputs need a head");
+    std::vector<int> nl(B);
+    for (int b = 0; b < B; ++b) {
+        if (lens[b] < 1 || lens[b] > S) return fail(h, TTS_BB_E_INVALID, "lens[%d]=%d outside 1..%d", b, lens[b], S);
+        nl[b] = h->slot_len[slots[b]] + lens[b];
+        if (nl[b] > c.max_ctx) return fail(h, TTS_BB_E_INVALID, "slot %d would exceed max_ctx", slots[b]);
+    }
+    SetupArgs& a = *h->setup;
+    a.B = B;
+    a.clear_amax = argmax_out != nullptr;
+    tts_bb_status s = grow_slots(h, B, slots, nl.data(), a);
+    if (s != TTS_BB_OK) return s;
+    for (int b = 0; b < B; ++b) {
+        a.slot[b] = slots[b];
+        a.start[b] = h->slot_len[slots[b]];
+        a.len[b] = lens[b];
+        a.key_len[b] = nl[b];
+        h->slot_len[slots[b]] = nl[b];
+    }
+    launch_setup(h, a);
+    const int T = B * S;
+    h->launches += launch_embed_codebooks(h->tabs, ids, reinterpret_cast<const bf16*>(embeds), h->h, T, h->err, h->st);
+    KVView kv{h->pool, h->d_page_table, h->seq_slot, h->mbps};
+    run_layers(h, B, S, 1, 0, kv, h->layer_elems);
+    if (opts && opts->hidden_out)
+        cudaMemcpyAsync(opts->hidden_out, h->h, (size_t)T * HID * sizeof(float), cudaMemcpyDeviceToDevice, h->st);
+    if (head_idx >= 0 && (logits_out || argmax_out))
+        run_head(h, B, S, head_idx, true, logits_out, argmax_out, opts && opts->argmax_stride ? opts->argmax_stride : 1);
+    return finish(h);
+}
+
+TTS_API tts_bb_status tts_bb_maskgit_pass(tts_bb* h, int B, int S, const int32_t* ids, const uint8_t* audio_mask,
+                                          const int32_t* key_lens, int audio_start, float* logits_out,
+                                          const tts_bb_opts* opts) {
+    if (!h) return TTS_BB_E_INVALID;
+    const tts_bb_config& c = h->cfg;
+    if (!h->text || !h->audio) return fail(h, TTS_BB_E_UNSUPPORTED, "handle has no text/audio tables");
+    if (B <= 0 || B > c.max_batch || S <= 0 || (long)B * S > c.max_tokens)
+        return fail(h, TTS_BB_E_INVALID, "B=%d S=%d outside the configured sizes", B, S);
+    if (S > h->rope_len) return fail(h, TTS_BB_E_INVALID, "S=%d beyond the RoPE table", S);
+    if (!ids || !audio_mask) return fail(h, TTS_BB_E_INVALID, "ids and audio_mask are required");
+    if (audio_start < 0 || audio_start >= S) return fail(h, TTS_BB_E_INVALID, "audio_start %d outside 0..S-1", audio_start);
+    if (logits_out && c.n_heads <= 0) return fail(h, TTS_BB_E_INVALID, "handle has no audio heads");
+    if (key_lens)
+        for (int b = 0; b < B; ++b)
+            if (key_lens[b] < 1 || key_lens[b] > S) return fail(h, TTS_BB_E_INVALID, "key_lens[%d] outside 1..S", b);
+    const int bps = (S + KVB - 1) / KVB;
+    const size_t need_blocks = (size_t)B * bps;
+    if (need_blocks > h->mg_pool_blocks) {
+        if (h->mg_pool) {
+            cudaStreamSynchronize(h->st);
+            cudaFree(h->mg_pool);
+            h->allocs.erase(std::remove(h->allocs.begin(), h->allocs.end(), (void*)h->mg_pool), h->allocs.end());
+            h->mg_pool = nullptr;
+            h->mg_pool_blocks = 0;
+        }
+        cudaError_t e = dalloc(h, &h->mg_pool, need_blocks * 2 * NKV * KVB * HD);
+        if (e != cudaSuccess) return cuda_fail(h, e, "MaskGIT scratch");
+        h->mg_pool_blocks = need_blocks;
+    }
+    SetupArgs& a = *h->setup;
+    a.B = B;
+    a.n_upd = 0;
+    a.clear_amax = 0;
+    for (int b = 0; b < B; ++b) {
+        a.slot[b] = b;
+        a.start[b] = 0;
+        a.len[b] = S;
+        a.key_len[b] = key_lens ? key_lens[b] : S;
+    }
+    launch_setup(h, a);
+    h->launches += launch_embed_omnivoice(h->text, c.text_vocab, h->audio, c.audio_codebooks, c.audio_vocab, ids,
+                                          audio_mask, h->h, B, S, h->err, h->st);
+    KVView kv{h->mg_pool, nullptr, h->seq_slot, bps};
+    run_layers(h, B, S, 2, 0, kv, 0);
+    if (opts && opts->hidden_out)
+        cudaMemcpyAsync(opts->hidden_out, h->h, (size_t)B * S * HID * sizeof(float), cudaMemcpyDeviceToDevice, h->st);
+    if (logits_out) {
+        const int Sa = S - audio_start;
+        h->launches += launch_rmsnorm(h->h, h->final_norm, h->y, B * Sa, c.rms_eps, Sa, S, audio_start, nullptr, h->st);
+        Epi e{};
+        e.mode = EPI_LOGITS_PERM; e.out = logits_out; e.perm_rows = Sa; e.perm_vocab = c.head_rows;
+        e.perm_groups = c.n_heads;
+        h->launches += launch_gemm(h->y, h->heads[0], B * Sa, c.n_heads * c.head_rows, HID, e, h->st);
+    }
+    return finish(h);
+}
+
+TTS_API tts_bb_status tts_bb_debug_kv_read(tts_bb* h, int layer, int slot, int pos0, int n, void* k_out, void* v_out) {
+    if (!h) return TTS_BB_E_INVALID;
+    if (h->cfg.max_slots <= 0 || layer < 0 || layer >= h->cfg.n_layers || slot < 0 || slot >= h->cfg.max_slots ||
+        pos0 < 0 || n < 0 || pos0 + n > h->slot_len[slot] || !k_out || !v_out)
+        return fail(h, TTS_BB_E_INVALID, "debug_kv_read: bad arguments");
+    if (n == 0) return TTS_BB_OK;
+    k_kv_copy<<<n, 256, 0, h->st>>>(h->pool + (size_t)layer * h->layer_elems, h->d_page_table, slot, h->mbps, pos0, n,
+                                    reinterpret_cast<bf16*>(k_out), reinterpret_cast<bf16*>(v_out), 0);
+    h->launches++;
+    return finish(h);
+}
+
+TTS_API tts_bb_status tts_bb_debug_kv_write(tts_bb* h, int layer, int slot, int pos0, int n, const void* k,
+                                           const void* v) {
+    if (!h) return TTS_BB_E_INVALID;
+    if (h->cfg.max_slots <= 0 || layer < 0 || layer >= h->cfg.n_layers || slot < 0 || slot >= h->cfg.max_slots ||
+        pos0 < 0 || n < 0 || pos0 > h->slot_len[slot] || pos0 + n > h->cfg.max_ctx || !k || !v)
+        return fail(h, TTS_BB_E_INVALID, "debug_kv_write: bad arguments");
+    if (n == 0) return TTS_BB_OK;
+    const int new_len = std::max(h->slot_len[slot], pos0 + n);
+    SetupArgs& a = *h->setup;
+    a.B = 0;
+    a.clear_amax = 0;
+    int32_t s1[1] = {slot};
+    int nl[1] = {new_len};
+    tts_bb_status s = grow_slots(h, 1, s1, nl, a);
+    if (s != TTS_BB_OK) return s;
+    h->slot_len[slot] = new_len;
+    launch_setup(h, a);
+    k_kv_copy<<<n, 256, 0, h->st>>>(h->pool + (size_t)layer * h->layer_elems, h->d_page_table, slot, h->mbps, pos0, n,
+                                    const_cast<bf16*>(reinterpret_cast<const bf16*>(k)),
+                                    const_cast<bf16*>(reinterpret_cast<const bf16*>(v)), 1);
+    h->launches++;
+    return finish(h);
+}

@@ -1,0 +1,243 @@
+/*
+ * tts_bb.h — C ABI of the GB300 (sm_103a) engine for the forward step of the
+ * Qwen3-0.6B-shaped backbone that drives codec-token speech generation.
+ *
+ * The backbone (28 layers, hidden 1024, 16 query / 8 KV heads of 128, SwiGLU
+ * 3072, RMSNorm eps 1e-6, q/k RMSNorm before half-rotate RoPE theta 1e6) is the
+ * one described on "omnivoice-cpp docs/ARCHITECTURE.md" (GGUF layout;
+ * Component architecture, Qwen3 specifics) and "Qwen3-TTS ncnn port"
+ * (Tencent/ncnn discussion 6877; model structure, Talker and Code Predictor;
+ * single-token SDPA and host attention; mRoPE conclusion).
+ *
+ * Conventions follow the public C99 ABI of omnivoice-cpp (Public API and ABI
+ * guarantee): an opaque handle, a default-initialiser for the config struct,
+ * a negative status enum, caller-owned outputs, a version string. The header
+ * is plain C99; the library exports only tts_bb_* symbols.
+ *
+ * Pointers. Unless a parameter says otherwise:
+ *   - "device" arrays are CUDA device pointers (e.g. torch CUDA tensors) on
+ *     the device that was current at tts_bb_create; they must stay valid
+ *     until the work enqueued on the handle's stream has finished;
+ *   - "host" arrays are ordinary CPU memory read before the call returns.
+ * All compute calls are asynchronous on the handle's stream. Host-side
+ * argument errors return before anything is enqueued and change no state.
+ * Device-side errors (an out-of-range id) are latched in a device error word:
+ * with config.sync_errors = 1 every call ends by reading it (one stream
+ * synchronisation); with 0 the caller reads it with tts_bb_sync().
+ * A handle is not thread-safe: one host thread at a time.
+ */
+#ifndef TTS_BB_H
+#define TTS_BB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TTS_BB_VERSION_MAJOR 0
+#define TTS_BB_VERSION_MINOR 1
+#define TTS_BB_VERSION_PATCH 0
+
+#define TTS_BB_MAX_CODEBOOKS 16
+#define TTS_BB_MAX_HEADS 16
+#define TTS_BB_KV_BLOCK 64
+
+typedef struct tts_bb tts_bb; /* opaque engine handle */
+
+typedef enum {
+    TTS_BB_OK = 0,
+    TTS_BB_E_INVALID = -1,         /* bad argument; nothing was enqueued */
+    TTS_BB_E_UNSUPPORTED = -2,     /* valid C, shape this build does not run */
+    TTS_BB_E_CUDA = -3,            /* a CUDA runtime call failed */
+    TTS_BB_E_OOM = -4,             /* device memory or KV blocks exhausted */
+    TTS_BB_E_DEVICE_TIMEOUT = -5,  /* a bounded device-side wait ran out */
+    TTS_BB_E_BAD_ID = -6,          /* a token id was out of its table (it was skipped) */
+    TTS_BB_E_NOT_IMPLEMENTED = -7
+} tts_bb_status;
+
+/* Backbone and engine shape. Field names follow the Code Predictor config of
+ * "rightkit-qts 0.2.0" (Mode API: hidden_size, n_layers, heads, kv heads,
+ * intermediate_size, head_dim, rms_norm_eps, rope_theta, vocab_size). */
+typedef struct {
+    int n_layers;          /* 28 Talker / OmniVoice, 5 Code Predictor */
+    int hidden;            /* 1024 (only value this build runs) */
+    int n_q_heads;         /* 16 */
+    int n_kv_heads;        /* 8 */
+    int head_dim;          /* 128 */
+    int ffn;               /* 3072 */
+    float rms_eps;         /* 1e-6 */
+    float rope_theta;      /* 1e6 */
+    /* Input embedding: the codebook tables E_0..E_{n_codebooks-1} are summed
+     * (Qwen3-TTS ncnn port, model structure: the 16 embeddings of a frame are
+     * added to form the next Talker input). */
+    int n_codebooks;
+    int codebook_rows[TTS_BB_MAX_CODEBOOKS];
+    /* OmniVoice hybrid input (omnivoice-cpp, Component architecture): a text
+     * table of text_vocab rows and an audio table of audio_codebooks *
+     * audio_vocab rows. 0 = absent. */
+    int text_vocab;
+    int audio_codebooks;
+    int audio_vocab;
+    /* Output heads: n_heads bf16 matrices of [head_rows][hidden] (Talker 1 x
+     * 3072, Code Predictor 15 x 2048). For OmniVoice set n_heads = audio_codebooks
+     * and head_rows = audio_vocab: one [n_heads*head_rows][hidden] matrix
+     * (audio_heads) is passed in head[0]. 0 heads = hidden-state only. */
+    int n_heads;
+    int head_rows;
+    /* KV cache: paged, TTS_BB_KV_BLOCK tokens per block. */
+    int max_slots;         /* concurrent sequences (stream slots) */
+    int max_ctx;           /* longest sequence, tokens */
+    int kv_blocks;         /* physical blocks; 0 = max_slots * ceil(max_ctx / 64) */
+    int max_batch;         /* largest B of one call (scratch sizing) */
+    int max_tokens;        /* largest B*S of one prefill / MaskGIT call */
+    int sync_errors;       /* 1 = each call synchronises to report device errors */
+} tts_bb_config;
+
+/* Per-layer tensor roles (PyTorch (out, in) row-major, bf16). */
+enum {
+    TTS_BB_W_IN_NORM = 0,  /* [hidden]           input_layernorm */
+    TTS_BB_W_Q,            /* [heads*128][hidden] q_proj */
+    TTS_BB_W_K,            /* [kv*128][hidden]   k_proj */
+    TTS_BB_W_V,            /* [kv*128][hidden]   v_proj */
+    TTS_BB_W_Q_NORM,       /* [128]              q_norm */
+    TTS_BB_W_K_NORM,       /* [128]              k_norm */
+    TTS_BB_W_O,            /* [hidden][heads*128] o_proj */
+    TTS_BB_W_POST_NORM,    /* [hidden]           post_attention_layernorm */
+    TTS_BB_W_GATE,         /* [ffn][hidden]      gate_proj */
+    TTS_BB_W_UP,           /* [ffn][hidden]      up_proj */
+    TTS_BB_W_DOWN,         /* [hidden][ffn]      down_proj */
+    TTS_BB_LAYER_TENSORS
+};
+
+/* Weight pointers, bf16 bit patterns. Host or device memory (anything
+ * cudaMemcpy with cudaMemcpyDefault accepts). tts_bb_create copies them into
+ * engine-owned device memory (fusing q/k/v and interleaving gate/up), so the
+ * caller may free its copies once tts_bb_create has returned. */
+typedef struct {
+    const void* codebook[TTS_BB_MAX_CODEBOOKS]; /* [codebook_rows[k]][hidden] */
+    const void* text_table;                     /* [text_vocab][hidden] or NULL */
+    const void* audio_table;                    /* [audio_codebooks*audio_vocab][hidden] or NULL */
+    const void* const* layer;                   /* n_layers * TTS_BB_LAYER_TENSORS pointers */
+    const void* final_norm;                     /* [hidden] */
+    const void* head[TTS_BB_MAX_HEADS];         /* [head_rows][hidden] each */
+} tts_bb_weights;
+
+/* Optional per-call inputs and outputs. NULL options = all defaults. */
+typedef struct {
+    /* device bf16 [tokens][hidden], added to the codebook sum (the Code
+     * Predictor's Talker-hidden row, or a plain embedding input). */
+    const void* embeds;
+    /* device fp32 [tokens][hidden]: the residual after the last layer, before
+     * the final norm. */
+    float* hidden_out;
+    /* element stride between consecutive rows of argmax_out (0 = 1): lets a
+     * Talker / Code-Predictor loop write codes straight into the next frame's
+     * id matrix. */
+    int argmax_stride;
+} tts_bb_opts;
+
+/* Fill *cfg with the Qwen3-TTS Talker shape: 28 layers, 16 codebooks
+ * (E_0 3072 rows, E_1..E_15 2048 rows), one 3072-row head, 64 slots, 4096 ctx. */
+void tts_bb_default_config(tts_bb_config* cfg);
+
+/* Create an engine on the current CUDA device; `stream` is a cudaStream_t
+ * (NULL = the legacy default stream) on which every call of the handle runs.
+ * Allocates the weights, the KV block pool and scratch. Returns
+ * TTS_BB_E_INVALID for a bad config, TTS_BB_E_UNSUPPORTED for a shape the
+ * kernels are not built for, TTS_BB_E_OOM when device memory runs out. */
+tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weights* w,
+                            void* stream, tts_bb** out);
+
+/* Wait for the handle's work and free everything it owns. NULL is a no-op. */
+void tts_bb_free(tts_bb* h);
+
+/* Causal prefill (Qwen3-TTS ncnn port: prompt prefill fills the per-layer
+ * KV cache). Sequence b appends lens[b] tokens (1..S) to slot slots[b],
+ * starting at the slot's current length, so a prefill can extend a cache.
+ *   B, S      batch and padded length; B*S <= max_tokens, B <= max_batch
+ *   slots     host int32 [B], distinct, in [0, max_slots)
+ *   lens      host int32 [B], 1..S
+ *   ids       device int32 [B][S][n_codebooks]; -1 = no token from that
+ *             codebook at that position; NULL = embeddings only
+ *   head_idx  head applied to the last valid position of each row (-1 = none)
+ *   logits_out device fp32 [B][head_rows] or NULL
+ *   argmax_out device int32 [B] (stride opts->argmax_stride) or NULL; the
+ *             lowest index wins a tie
+ *   opts->embeds     [B][S][hidden]; opts->hidden_out [B][S][hidden]
+ * An out-of-table id is skipped and reported as TTS_BB_E_BAD_ID. */
+tts_bb_status tts_bb_prefill(tts_bb* h, int B, int S, const int32_t* slots, const int32_t* lens,
+                             const int32_t* ids, int head_idx, float* logits_out,
+                             int32_t* argmax_out, const tts_bb_opts* opts);
+
+/* One decode step, query length 1, for B sequences (Qwen3-TTS ncnn port,
+ * single-token SDPA and host attention: RoPE, KV append and GQA attention over
+ * the cache for a query of length 1).
+ *   slots    host int32 [B], distinct
+ *   kv_lens  host int32 [B]: tokens already cached in each slot; must equal
+ *            the engine's length for the slot (TTS_BB_E_INVALID otherwise).
+ *            The new token is written at position kv_lens[b] and attention
+ *            covers kv_lens[b] + 1 tokens.
+ *   ids      device int32 [B][n_codebooks] (-1 = absent) or NULL
+ *   logits_out / argmax_out as in tts_bb_prefill, one row per sequence
+ *   opts->embeds [B][hidden]; opts->hidden_out [B][hidden] */
+tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots, const int32_t* kv_lens,
+                                 const int32_t* ids, int head_idx, float* logits_out,
+                                 int32_t* argmax_out, const tts_bb_opts* opts);
+
+/* One full bidirectional MaskGIT pass without a KV cache (omnivoice-cpp,
+ * MaskGIT decoder: every step is a full prefill with non-causal attention;
+ * Component architecture: hybrid text/audio embedding and audio heads;
+ * Inner-loop optimisations: logits only over the audio window).
+ *   ids         device int32 [B][audio_codebooks][S] (text id on every row at
+ *               text positions, audio codes 0..audio_vocab-1 at audio positions)
+ *   audio_mask  device uint8 [B][S], 1 = audio position
+ *   key_lens    host int32 [B] (keys >= key_lens[b] are padding) or NULL = S
+ *   audio_start first position of the audio window, 0 <= audio_start < S
+ *   logits_out  device fp32 [B][n_heads][S - audio_start][head_rows]:
+ *               logits[b][k][s][v] = final_norm(x[b][audio_start+s]) . W[k*head_rows + v]
+ *   opts->hidden_out [B][S][hidden]
+ * Requires a handle with text and audio tables; B*S <= max_tokens. */
+tts_bb_status tts_bb_maskgit_pass(tts_bb* h, int B, int S, const int32_t* ids,
+                                  const uint8_t* audio_mask, const int32_t* key_lens,
+                                  int audio_start, float* logits_out, const tts_bb_opts* opts);
+
+/* Return the slot's KV blocks to the pool; its length becomes 0. */
+tts_bb_status tts_bb_release(tts_bb* h, int slot);
+
+/* Shorten a slot to `len` tokens (0 <= len <= current length); blocks past
+ * the new end go back to the pool. Positions >= len are rewritten by the next
+ * prefill or decode step. */
+tts_bb_status tts_bb_truncate(tts_bb* h, int slot, int len);
+
+/* Current cached length of a slot, or -1 for a bad handle or slot. */
+int tts_bb_slot_len(const tts_bb* h, int slot);
+
+/* Wait for the handle's stream and report (then clear) any latched device error. */
+tts_bb_status tts_bb_sync(tts_bb* h);
+
+/* Text of the last error on this handle (empty string if none). */
+const char* tts_bb_last_error(const tts_bb* h);
+
+/* "MAJOR.MINOR.PATCH (sm_103a)". */
+const char* tts_bb_version(void);
+
+/* Test hooks: read or write n tokens of one layer's cache of one slot,
+ * positions pos0..pos0+n-1, through the page table.
+ *   k, v  device bf16 [n][n_kv_heads][head_dim] (keys after q/k-norm and RoPE)
+ * tts_bb_debug_kv_write extends the slot to pos0+n if it was shorter
+ * (allocating blocks); pos0 must not exceed the current length. */
+tts_bb_status tts_bb_debug_kv_read(tts_bb* h, int layer, int slot, int pos0, int n,
+                                   void* k_out, void* v_out);
+tts_bb_status tts_bb_debug_kv_write(tts_bb* h, int layer, int slot, int pos0, int n,
+                                    const void* k, const void* v);
+
+/* Number of kernel launches the handle has enqueued since creation (a
+ * counter kept on the host; lets a caller count launches in a timed region). */
+uint64_t tts_bb_launch_count(const tts_bb* h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TTS_BB_H */

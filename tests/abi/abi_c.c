@@ -1,0 +1,52 @@
+/* Plain C99 consumer of include/tts_bb.h: built with -std=c99 -Wall -Werror
+ * -pedantic and run without a GPU. It calls every entry point through an
+ * early-return path (NULL handle or invalid arguments), so it checks that the
+ * header is valid C99 and that every declared symbol links and returns the
+ * documented status without touching a device. */
+#include <stdio.h>
+#include <string.h>
+#include "tts_bb.h"
+
+#define EXPECT(cond)                                              \
+    do {                                                          \
+        if (!(cond)) {                                            \
+            fprintf(stderr, "FAILED: %s (line %d)\n", #cond, __LINE__); \
+            return 1;                                             \
+        }                                                         \
+    } while (0)
+
+int main(void) {
+    tts_bb_config cfg;
+    tts_bb_weights w;
+    tts_bb_opts o;
+    tts_bb* h = NULL;
+    int32_t slots[1] = {0}, lens[1] = {1};
+    char k[16], v[16];
+    memset(&w, 0, sizeof w);
+    memset(&o, 0, sizeof o);
+    tts_bb_default_config(&cfg);
+    EXPECT(cfg.n_layers == 28 && cfg.hidden == 1024 && cfg.n_q_heads == 16 && cfg.n_kv_heads == 8);
+    EXPECT(cfg.head_dim == 128 && cfg.ffn == 3072 && cfg.n_codebooks == 16 && cfg.head_rows == 3072);
+    EXPECT(strncmp(tts_bb_version(), "0.1.0", 5) == 0);
+    EXPECT(tts_bb_create(NULL, &w, NULL, &h) == TTS_BB_E_INVALID && h == NULL);
+    EXPECT(tts_bb_create(&cfg, NULL, NULL, &h) == TTS_BB_E_INVALID);
+    EXPECT(tts_bb_create(&cfg, &w, NULL, NULL) == TTS_BB_E_INVALID);
+    cfg.hidden = 2048;
+    EXPECT(tts_bb_create(&cfg, &w, NULL, &h) == TTS_BB_E_UNSUPPORTED);
+    tts_bb_default_config(&cfg);
+    EXPECT(tts_bb_create(&cfg, &w, NULL, &h) == TTS_BB_E_INVALID); /* NULL weight pointers */
+    EXPECT(tts_bb_prefill(NULL, 1, 1, slots, lens, NULL, -1, NULL, NULL, &o) == TTS_BB_E_INVALID);
+    EXPECT(tts_bb_decode_step(NULL, 1, slots, lens, NULL, -1, NULL, NULL, NULL) == TTS_BB_E_INVALID);
+    EXPECT(tts_bb_maskgit_pass(NULL, 1, 1, NULL, NULL, NULL, 0, NULL, NULL) == TTS_BB_E_INVALID);
+    EXPECT(tts_bb_release(NULL, 0) == TTS_BB_E_INVALID);
+    EXPECT(tts_bb_truncate(NULL, 0, 0) == TTS_BB_E_INVALID);
+    EXPECT(tts_bb_slot_len(NULL, 0) == -1);
+    EXPECT(tts_bb_sync(NULL) == TTS_BB_E_INVALID);
+    EXPECT(tts_bb_debug_kv_read(NULL, 0, 0, 0, 1, k, v) == TTS_BB_E_INVALID);
+    EXPECT(tts_bb_debug_kv_write(NULL, 0, 0, 0, 1, k, v) == TTS_BB_E_INVALID);
+    EXPECT(tts_bb_launch_count(NULL) == 0);
+    EXPECT(strlen(tts_bb_last_error(NULL)) > 0);
+    tts_bb_free(NULL);
+    printf("abi_c: ok\n");
+    return 0;
+}

@@ -1,0 +1,302 @@
+"""GPU parity on small shapes: every kernel of the path through the C ABI,
+compared element by element with the fp64 oracle on the same seeded inputs.
+
+Shapes keep the real widths (hidden 1024, 16/8 heads of 128, SwiGLU 3072) with
+few layers, so the oracle finishes in seconds while the kernels still span
+several tiles and ragged tails.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+from tests.gpu_util import (HIDDEN_TOL, LOGIT_TOL, Engine, bf16_tensor_bits, check_logits_and_argmax,
+                            dev_bf16_bits, dev_i32, dev_u8, f32_zeros, i32_full, rel_err_rows)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def _i32(x):
+    return np.asarray(x, dtype=np.int32)
+
+
+def small_talker(n_layers=2):
+    return synth.ModelShape(n_layers=n_layers, codebook_rows=(3072,) + (2048,) * 15, n_heads_out=1, head_rows=3072)
+
+
+# ---------------------------------------------------------------- a1: gather-sum, bit-exact
+def integer_tables(shape, seed):
+    """Tables whose rows hold small integers: every sum of 16 rows is exact in fp32."""
+    r = synth.rng_for(seed, "int_tables")
+    tabs = []
+    for rows in shape.codebook_rows:
+        vals = r.integers(-8, 9, size=(rows, shape.hidden)).astype(np.float32)
+        tabs.append(synth.bf16_bits(vals))
+    return tabs
+
+
+def test_gather_sum_bit_exact():
+    shape = synth.ModelShape(n_layers=0, codebook_rows=(3072,) + (2048,) * 15, n_heads_out=1, head_rows=3072)
+    w = synth.model_weights(shape, 21, tables=integer_tables(shape, 21))
+    r = synth.rng_for(21, "ids")
+    B = 7
+    ids = synth.uniform_ids(r, shape.codebook_rows, B)
+    ids[1, 3] = -1
+    ids[2, :] = -1
+    ids[2, 15] = 2047
+    ids[3, 0] = 3071
+    emb = synth.bf16_bits(r.integers(-4, 5, size=(B, 1024)).astype(np.float32))
+    want = O.codebook_embed_sum(ids, [O.bf16_to_f64(t) for t in w.codebooks])
+    want_e = want + O.bf16_to_f64(emb)
+    with Engine(w, max_slots=8, max_ctx=64, max_batch=8) as e:
+        hid = f32_zeros(B, 1024)
+        m = e.m
+        m.tts_bb_decode_step(e.h, B, np.arange(B), np.zeros(B), dev_i32(ids), hidden_out=hid)
+        assert np.array_equal(hid.cpu().numpy().astype(np.float64), want)
+        hid2 = f32_zeros(B, 1024)
+        m.tts_bb_decode_step(e.h, B, np.arange(B), np.ones(B), dev_i32(ids), embeds=dev_bf16_bits(emb), hidden_out=hid2)
+        assert np.array_equal(hid2.cpu().numpy().astype(np.float64), want_e)
+        # an out-of-table id is skipped and reported
+        bad = ids.copy()
+        bad[4, 5] = 2048
+        hid3 = f32_zeros(B, 1024)
+        st = m.tts_bb_decode_step(e.h, B, np.arange(B), np.full(B, 2), dev_i32(bad), hidden_out=hid3, check=False)
+        assert st == m.E_BAD_ID
+        skip = bad.copy()
+        skip[4, 5] = -1
+        assert np.array_equal(hid3.cpu().numpy().astype(np.float64),
+                              O.codebook_embed_sum(skip, [O.bf16_to_f64(t) for t in w.codebooks]))
+
+
+# ---------------------------------------------------------------- head + argmax
+def test_head_argmax_ties_lowest_index():
+    """Rows of the head that are exact copies tie exactly; the lowest index wins."""
+    shape = synth.ModelShape(n_layers=0, codebook_rows=(64,), n_heads_out=1, head_rows=3072)
+    w = synth.model_weights(shape, 22, unit_gains=True)
+    head = w.heads[0].copy()
+    head[2000] = head[17]
+    head[2999] = head[17]
+    w.heads[0] = head
+    tab = w.codebooks[0].copy()
+    tab[0] = head[17]          # the input points along head row 17: it is the maximum, tied with 2000 and 2999
+    tab[1] = head[100]
+    w.codebooks = [tab]
+    m0 = O.Backbone(w, shape)
+    ids = np.array([[0], [1], [5]], np.int32)
+    B = len(ids)
+    with Engine(w, max_slots=4, max_ctx=64, max_batch=4) as e:
+        logits = f32_zeros(B, 3072)
+        am = i32_full(B)
+        e.m.tts_bb_decode_step(e.h, B, np.arange(B), np.zeros(B), dev_i32(ids), 0, logits, am)
+        g = logits.cpu().numpy()
+        gam = am.cpu().numpy()
+        o = m0.head_logits(O.codebook_embed_sum(ids, m0.codebooks), 0)
+        check_logits_and_argmax(g, o, gam, O.argmax_first(o), min_agree=1.0)
+        assert g[0, 17] == g[0, 2000] == g[0, 2999]
+        assert gam[0] == 17 and gam[1] == 100
+
+
+# ---------------------------------------------------------------- KV cache: bit-exact paging
+def test_kv_write_read_roundtrip_across_shuffled_blocks():
+    shape = small_talker(2)
+    w = synth.model_weights(shape, 23)
+    with Engine(w, max_slots=3, max_ctx=300, max_batch=3) as e:
+        m = e.m
+        lens = [130, 64, 257]
+        data = {}
+        # interleave writes so the physical blocks of each slot are scattered
+        for chunk in range(5):
+            for s in range(3):
+                a, b = chunk * 64, min(lens[s], (chunk + 1) * 64)
+                if a >= b:
+                    continue
+                for layer in (0, 1):
+                    k = synth.kv_values(23, f"k{s}.{layer}.{chunk}", b - a)
+                    v = synth.kv_values(23, f"v{s}.{layer}.{chunk}", b - a)
+                    m.tts_bb_debug_kv_write(e.h, layer, s, a, b - a, dev_bf16_bits(k), dev_bf16_bits(v))
+                    data[(s, layer, chunk)] = (k, v)
+        for s in range(3):
+            assert m.tts_bb_slot_len(e.h, s) == lens[s]
+            for layer in (0, 1):
+                kk = torch.zeros(lens[s], 8, 128, dtype=torch.bfloat16, device="cuda")
+                vv = torch.zeros_like(kk)
+                m.tts_bb_debug_kv_read(e.h, layer, s, 0, lens[s], kk, vv)
+                want_k = np.concatenate([data[(s, layer, c)][0] for c in range(5) if (s, layer, c) in data])
+                want_v = np.concatenate([data[(s, layer, c)][1] for c in range(5) if (s, layer, c) in data])
+                assert np.array_equal(bf16_tensor_bits(kk), want_k)
+                assert np.array_equal(bf16_tensor_bits(vv), want_v)
+        # truncate + release hand blocks back; a read past the end is rejected
+        m.tts_bb_truncate(e.h, 2, 100)
+        assert m.tts_bb_slot_len(e.h, 2) == 100
+        assert m.tts_bb_debug_kv_read(e.h, 0, 2, 90, 20, kk, vv, check=False) == m.E_INVALID
+        m.tts_bb_release(e.h, 0)
+        assert m.tts_bb_slot_len(e.h, 0) == 0
+
+
+# ---------------------------------------------------------------- one layer: prefill 64 + 16 decodes
+def test_one_layer_prefill_then_decode():
+    shape = synth.ONE_LAYER
+    w = synth.model_weights(shape, 0)
+    X = synth.normal_bf16(synth.rng_for(0, "X"), (80, 1024), 1.0)
+    m0 = O.Backbone(w, shape)
+    hp, hd = O.one_layer_run(m0, O.bf16_to_f64(X), 64)
+    cache = m0.new_cache()
+    m0.forward_cached(O.bf16_to_f64(X), np.arange(80), cache)
+    with Engine(w, max_slots=1, max_ctx=80, max_batch=1, max_tokens=64) as e:
+        m = e.m
+        Xd = dev_bf16_bits(X)
+        hid = f32_zeros(64, 1024)
+        m.tts_bb_prefill(e.h, 1, 64, [0], [64], None, embeds=Xd[:64], hidden_out=hid)
+        assert rel_err_rows(hid.cpu().numpy(), hp) <= HIDDEN_TOL
+        got = []
+        for t in range(64, 80):
+            h1 = f32_zeros(1, 1024)
+            m.tts_bb_decode_step(e.h, 1, [0], [t], None, embeds=Xd[t:t + 1], hidden_out=h1)
+            got.append(h1.cpu().numpy()[0])
+        err = rel_err_rows(np.array(got), hd)
+        assert err <= HIDDEN_TOL, err
+        # the cache holds k (after q/k norm + RoPE) and v of all 80 positions
+        kk = torch.zeros(80, 8, 128, dtype=torch.bfloat16, device="cuda")
+        vv = torch.zeros_like(kk)
+        m.tts_bb_debug_kv_read(e.h, 0, 0, 0, 80, kk, vv)
+        kg = kk.float().cpu().numpy()
+        vg = vv.float().cpu().numpy()
+        assert rel_err_rows(kg.reshape(80, -1), cache.k[0].reshape(80, -1)) <= HIDDEN_TOL
+        assert rel_err_rows(vg.reshape(80, -1), cache.v[0].reshape(80, -1)) <= HIDDEN_TOL
+
+
+# ---------------------------------------------------------------- Talker-shaped, teacher forced
+def test_talker_two_layers_teacher_forced():
+    shape = small_talker(2)
+    w = synth.model_weights(shape, 24)
+    m0 = O.Backbone(w, shape)
+    P, N = 16, 24
+    ids = synth.talker_prefill_ids(24, P)
+    rest = synth.uniform_ids(synth.rng_for(24, "rest"), shape.codebook_rows[1:], N)
+    cache = m0.new_cache()
+    hp, lg0, a0 = O.talker_prefill(m0, ids, cache)
+    hid_o, lg_o, am_o, fed = O.talker_decode_steps(m0, cache, a0, rest)
+    with Engine(w, max_slots=2, max_ctx=64, max_batch=2, max_tokens=64) as e:
+        m = e.m
+        logits = f32_zeros(1, 3072)
+        am = i32_full(1)
+        hid = f32_zeros(P, 1024)
+        m.tts_bb_prefill(e.h, 1, P, [1], [P], dev_i32(ids.reshape(1, P, 16)), 0, logits, am, hidden_out=hid)
+        assert rel_err_rows(hid.cpu().numpy(), hp) <= HIDDEN_TOL
+        check_logits_and_argmax(logits.cpu().numpy(), lg0[None], am.cpu().numpy(), [a0], min_agree=1.0)
+        gl, ga, gh = [], [], []
+        for t in range(N):
+            h1 = f32_zeros(1, 1024)
+            m.tts_bb_decode_step(e.h, 1, [1], [P + t], dev_i32(fed[t:t + 1]), 0, logits, am, hidden_out=h1)
+            gl.append(logits.cpu().numpy()[0]); ga.append(int(am.cpu().numpy()[0])); gh.append(h1.cpu().numpy()[0])
+        assert rel_err_rows(np.array(gh), hid_o) <= HIDDEN_TOL
+        check_logits_and_argmax(np.array(gl), lg_o, np.array(ga), am_o)
+
+
+# ---------------------------------------------------------------- ragged batches, chunked prefill, paging
+def test_ragged_prefill_chunks_and_batched_decode():
+    shape = small_talker(2)
+    w = synth.model_weights(shape, 25)
+    m0 = O.Backbone(w, shape)
+    r = synth.rng_for(25, "ragged")
+    B, S = 4, 70
+    lens1 = [70, 1, 33, 64]
+    lens2 = [5, 66, 1, 17]                       # second prefill chunk extends each cache
+    ids1 = synth.uniform_ids(r, shape.codebook_rows, B * S).reshape(B, S, 16)
+    ids2 = synth.uniform_ids(r, shape.codebook_rows, B * S).reshape(B, S, 16)
+    slots = [3, 0, 2, 1]
+    caches = [m0.new_cache() for _ in range(B)]
+    hs1 = m0.forward_cached_multi([O.codebook_embed_sum(ids1[b, :lens1[b]], m0.codebooks) for b in range(B)], caches)
+    hs2 = m0.forward_cached_multi([O.codebook_embed_sum(ids2[b, :lens2[b]], m0.codebooks) for b in range(B)], caches)
+    n_dec = 3
+    dec_ids = synth.uniform_ids(r, shape.codebook_rows, n_dec * B).reshape(n_dec, B, 16)
+    dec_h, dec_l = [], []
+    for t in range(n_dec):
+        hs = m0.forward_cached_multi([O.codebook_embed_sum(dec_ids[t, b:b + 1], m0.codebooks) for b in range(B)], caches)
+        dec_h.append(np.concatenate(hs))
+        dec_l.append(m0.head_logits(np.concatenate(hs), 0))
+    with Engine(w, max_slots=4, max_ctx=160, max_batch=4, max_tokens=B * S) as e:
+        m = e.m
+        for ids, lens, hs in ((ids1, lens1, hs1), (ids2, lens2, hs2)):
+            logits = f32_zeros(B, 3072)
+            am = i32_full(B)
+            hid = f32_zeros(B, S, 1024)
+            m.tts_bb_prefill(e.h, B, S, slots, lens, dev_i32(ids), 0, logits, am, hidden_out=hid)
+            g = hid.cpu().numpy()
+            for b in range(B):
+                assert rel_err_rows(g[b, :lens[b]], hs[b]) <= HIDDEN_TOL
+            ol = np.array([m0.head_logits(hs[b][-1:], 0)[0] for b in range(B)])
+            check_logits_and_argmax(logits.cpu().numpy(), ol, am.cpu().numpy(), O.argmax_first(ol), min_agree=0.75)
+        kv = [lens1[b] + lens2[b] for b in range(B)]
+        for t in range(n_dec):
+            logits = f32_zeros(B, 3072)
+            am = i32_full(B)
+            hid = f32_zeros(B, 1024)
+            m.tts_bb_decode_step(e.h, B, slots, kv, dev_i32(dec_ids[t]), 0, logits, am, hidden_out=hid)
+            assert rel_err_rows(hid.cpu().numpy(), dec_h[t]) <= HIDDEN_TOL
+            check_logits_and_argmax(logits.cpu().numpy(), dec_l[t], am.cpu().numpy(), O.argmax_first(dec_l[t]),
+                                    min_agree=0.75)
+            kv = [x + 1 for x in kv]
+        # a wrong kv_lens is rejected before anything runs
+        assert m.tts_bb_decode_step(e.h, B, slots, [x + 1 for x in kv], dev_i32(dec_ids[0]), check=False) == m.E_INVALID
+
+
+# ---------------------------------------------------------------- Code-Predictor-shaped frame
+def test_code_predictor_frame_small_batch():
+    shape = synth.ModelShape(n_layers=2, codebook_rows=(3072,) + (2048,) * 15, n_heads_out=15, head_rows=2048)
+    w = synth.model_weights(shape, 26)
+    m0 = O.Backbone(w, shape)
+    F = 3
+    r = synth.rng_for(26, "cp")
+    th = synth.normal_bf16(r, (F, 1024), 1.0)
+    code0 = r.integers(0, 3072, size=F)
+    ref = [O.code_predictor_frame(m0, O.bf16_to_f64(th[f]), int(code0[f])) for f in range(F)]
+    with Engine(w, max_slots=F, max_ctx=17, max_batch=F, max_tokens=2 * F) as e:
+        m = e.m
+        emb = np.zeros((F, 2, 1024), np.uint16)
+        emb[:, 0] = th
+        ids = -np.ones((F, 2, 16), np.int32)
+        ids[:, 1, 0] = code0
+        codes = i32_full(F * 16)
+        logits = f32_zeros(F, 2048)
+        codes2d = codes.view(F, 16)
+        m.tts_bb_prefill(e.h, F, 2, list(range(F)), [2] * F, dev_i32(ids), 0, logits, codes2d[:, 1],
+                         embeds=dev_bf16_bits(emb), argmax_stride=16)
+        gl = [logits.cpu().numpy().copy()]
+        for j in range(1, 15):
+            step_ids = -np.ones((F, 16), np.int32)
+            # teacher forcing: feed the oracle's code j
+            step_ids[:, j] = [ref[f][0][j - 1] for f in range(F)]
+            m.tts_bb_decode_step(e.h, F, list(range(F)), [j + 1] * F, dev_i32(step_ids), j, logits,
+                                 codes2d[:, j + 1] if j < 15 else None, argmax_stride=16)
+            gl.append(logits.cpu().numpy().copy())
+        gl = np.array(gl)                                  # [15, F, 2048]
+        got_codes = codes2d.cpu().numpy()[:, 1:16]
+        for f in range(F):
+            check_logits_and_argmax(gl[:, f], ref[f][1], got_codes[f], ref[f][0], min_agree=0.9)
+
+
+# ---------------------------------------------------------------- MaskGIT bidirectional pass
+def test_maskgit_pass_small_with_padding():
+    shape = synth.ModelShape(n_layers=2, text_vocab=4096, audio_codebooks=8, audio_vocab=1025, n_heads_out=8,
+                             head_rows=1025)
+    w = synth.model_weights(shape, 27)
+    m0 = O.Backbone(w, shape)
+    B, S, n_text = 2, 200, 56
+    ids, mask = synth.maskgit_inputs(27, 0, B=B, S=S, n_text=n_text, text_vocab=4096)
+    key_lens = np.array([200, 150], np.int32)
+    lo, ho = O.maskgit_pass(m0, ids, mask, n_text, key_lens=key_lens)
+    with Engine(w, max_slots=0, max_ctx=0, max_batch=B, max_tokens=B * S) as e:
+        m = e.m
+        logits = f32_zeros(B, 8, S - n_text, 1025)
+        hid = f32_zeros(B, S, 1024)
+        m.tts_bb_maskgit_pass(e.h, B, S, dev_i32(ids), dev_u8(mask), key_lens, n_text, logits, hidden_out=hid)
+        g = hid.cpu().numpy()
+        assert rel_err_rows(g[0], ho[0]) <= HIDDEN_TOL
+        assert rel_err_rows(g[1, :150], ho[1, :150]) <= HIDDEN_TOL
+        gl = logits.cpu().numpy()
+        err0 = np.max(np.abs(gl[0] - lo[0]))
+        err1 = np.max(np.abs(gl[1][:, :150 - n_text] - lo[1][:, :150 - n_text]))
+        assert max(err0, err1) <= LOGIT_TOL, (err0, err1)
