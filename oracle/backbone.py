@@ -219,33 +219,63 @@ class Backbone:
         return KVCache.empty(self.s.n_layers, self.s.n_kv_heads, self.s.head_dim)
 
     def layer(self, l: int, h: np.ndarray, pos: Sequence[int], cache: Optional[KVCache],
-              allowed: np.ndarray, keys_k: Optional[np.ndarray] = None,
-              keys_v: Optional[np.ndarray] = None):
-        """One decoder layer on h[T, hidden]; returns the new residual.
+              allowed: np.ndarray) -> np.ndarray:
+        """One decoder layer on one sequence h[T, hidden]; returns the new residual.
 
         With a cache, the new keys/values are appended (KV-cache append of the
         ncnn port's host attention) and attention runs over the whole cache.
         """
+        return self.layer_multi(l, [h], [pos], [cache], [allowed])[0]
+
+    def layer_multi(self, l: int, hs: List[np.ndarray], poss: List[Sequence[int]],
+                    caches: List[Optional[KVCache]], alloweds: List[np.ndarray]) -> List[np.ndarray]:
+        """The same layer applied to several independent sequences.
+
+        The projections are row-wise, so they run as one matrix product over
+        the rows of all sequences; norms, RoPE, the cache append and attention
+        run per sequence.
+        """
         s, lw = self.s, self.layers[l]
-        T = h.shape[0]
-        y = rms_norm(h, lw["in_norm"], s.rms_eps)
-        q = (y @ lw["wq"].T).reshape(T, s.n_q_heads, s.head_dim)
-        k = (y @ lw["wk"].T).reshape(T, s.n_kv_heads, s.head_dim)
-        v = (y @ lw["wv"].T).reshape(T, s.n_kv_heads, s.head_dim)
+        sizes = [h.shape[0] for h in hs]
+        cut = np.cumsum([0] + sizes)
+        H = np.concatenate(hs, axis=0)
+        N = H.shape[0]
+        y = rms_norm(H, lw["in_norm"], s.rms_eps)
+        q = (y @ lw["wq"].T).reshape(N, s.n_q_heads, s.head_dim)
+        k = (y @ lw["wk"].T).reshape(N, s.n_kv_heads, s.head_dim)
+        v = (y @ lw["wv"].T).reshape(N, s.n_kv_heads, s.head_dim)
         q = rms_norm(q, lw["q_norm"], s.rms_eps)       # per-head RMSNorm before RoPE
         k = rms_norm(k, lw["k_norm"], s.rms_eps)
-        q = rope_half_rotate(q, pos, s.rope_theta)
-        k = rope_half_rotate(k, pos, s.rope_theta)
-        if cache is not None:
-            cache.k[l] = np.concatenate([cache.k[l], k], axis=0)
-            cache.v[l] = np.concatenate([cache.v[l], v], axis=0)
-            K, V = cache.k[l], cache.v[l]
-        else:
-            K, V = k, v
-        o = attention_gqa(q, K, V, allowed).reshape(T, s.n_q_heads * s.head_dim)
-        h = h + o @ lw["wo"].T
-        y2 = rms_norm(h, lw["post_norm"], s.rms_eps)
-        return h + swiglu_mlp(y2, lw["wg"], lw["wu"], lw["wd"])
+        o = np.empty((N, s.n_q_heads * s.head_dim))
+        for i, (pos, cache, allowed) in enumerate(zip(poss, caches, alloweds)):
+            a, b = cut[i], cut[i + 1]
+            qi = rope_half_rotate(q[a:b], pos, s.rope_theta)
+            ki = rope_half_rotate(k[a:b], pos, s.rope_theta)
+            vi = v[a:b]
+            if cache is not None:
+                cache.k[l] = np.concatenate([cache.k[l], ki], axis=0)
+                cache.v[l] = np.concatenate([cache.v[l], vi], axis=0)
+                K, V = cache.k[l], cache.v[l]
+            else:
+                K, V = ki, vi
+            o[a:b] = attention_gqa(qi, K, V, allowed).reshape(b - a, -1)
+        H = H + o @ lw["wo"].T
+        y2 = rms_norm(H, lw["post_norm"], s.rms_eps)
+        H = H + swiglu_mlp(y2, lw["wg"], lw["wu"], lw["wd"])
+        return [H[cut[i]:cut[i + 1]] for i in range(len(hs))]
+
+    def forward_cached_multi(self, xs: List[np.ndarray], caches: List[KVCache]) -> List[np.ndarray]:
+        """Causal forward of several independent sequences, each extending its own cache."""
+        poss, alloweds = [], []
+        for x, c in zip(xs, caches):
+            L0 = len(c)
+            p = np.arange(L0, L0 + x.shape[0])
+            poss.append(p)
+            alloweds.append(causal_allowed(p, L0 + x.shape[0]))
+        hs = [np.asarray(x, dtype=np.float64) for x in xs]
+        for l in range(self.s.n_layers):
+            hs = self.layer_multi(l, hs, poss, caches, alloweds)
+        return hs
 
     def forward_cached(self, x: np.ndarray, pos: Sequence[int], cache: KVCache) -> np.ndarray:
         """Causal forward of T new tokens appended after the cache (prefill or decode).
