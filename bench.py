@@ -1,0 +1,412 @@
+#!/usr/bin/env python3
+"""Benchmark of the codec-token TTS backbone step on GB300 (one JSON line).
+
+Workload (default, ``talker_b1``): the 28-layer Qwen3-0.6B-shaped Talker at
+batch 1 — a 128-position prefill of 16 summed codebook embeddings, then decode
+steps with query length 1, a 3072-way codec head and the greedy argmax fed
+back on the device as the next codebook-0 id. One timed step = one decode step
+= one codec token. Positions cycle through 128..383 (256 decode steps per
+utterance, the slot is rewound to 128 between utterances), so the KV lengths
+seen are exactly those of a 128 + 256 generation.
+
+``--workload serving_b64``: 64 concurrent streams with ragged cached lengths
+uniform in [200, 2000], paged KV, one decode step per stream per call; one
+timed step = one call = 64 codec tokens.
+
+Inputs are synthetic (seeded bf16 N(0, 0.02) weights and uniform ids) and
+resident in HBM before the timed region. The 880 MB of weights streamed per
+step exceed the 129 MB L2, so no flush is needed between steps.
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
+workload (the oracle is the reference for this method; it is a deliberately
+slow, obviously correct program).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "codec tokens/s per GB300 (decode, batch 1 & 64); % of HBM roofline"
+UNIT = "codec tokens/s"
+P_PREFILL = 128
+N_DECODE = 256
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------- distributed (replicas only)
+def dist_setup(backend):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=ws)
+    return ws, rank, local
+
+
+def dist_barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(ws, x: float) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- workloads
+class TalkerB1:
+    """Talker batch 1: 128-position prefill, then decode steps at positions 128..383."""
+    name = "talker_b1"
+    seed = 1
+    B = 1
+
+    def __init__(self):
+        self.shape = synth.TALKER
+        self.w = synth.model_weights(self.shape, self.seed)
+        self.prefill_ids = synth.talker_prefill_ids(self.seed, P_PREFILL)
+        self.rest = synth.uniform_ids(synth.rng_for(self.seed, "decode_rest"), self.shape.codebook_rows[1:], N_DECODE)
+
+    def config(self):
+        return {"workload": "talker_b1: Qwen3-0.6B-shaped Talker, 28 layers, batch 1, 128-position prefill then "
+                            "decode at positions 128..383, 3072-way head, greedy id0 fed back",
+                "global_batch": 1, "seq_len": P_PREFILL + N_DECODE, "layers": 28,
+                "l2": "no flush: 880 MB of weights per step > 129 MB L2"}
+
+    def algorithmic_bytes_per_step(self, pos):
+        """Weights + 16 embedding rows + final norm + head, KV read (pos + 1 tokens) and write, logits."""
+        w = 28 * 31_461_888 + 16 * 2048 + 2048 + 3072 * 1024 * 2
+        return w + 114_688 * (pos + 1) + 114_688 + 3072 * 4
+
+
+class ServingB64:
+    """64 streams, ragged cached lengths U[200, 2000], one decode step per stream per call."""
+    name = "serving_b64"
+    seed = 2
+    B = 64
+
+    def __init__(self):
+        self.shape = synth.TALKER
+        self.w = synth.model_weights(self.shape, self.seed)
+        self.L0 = synth.ragged_lengths(self.seed, self.B, 200, 2000)
+
+    def config(self):
+        return {"workload": "serving_b64: 28-layer Talker, 64 streams, ragged KV lengths U[200,2000], paged KV "
+                            "(64-token blocks), one decode step per stream per call, 3072-way head",
+                "global_batch": 64, "seq_len": int(self.L0.max()), "layers": 28,
+                "l2": "no flush: 880 MB weights + ~10 GB KV per step > 129 MB L2"}
+
+
+def make_engine(wl, m, stream, max_ctx, max_batch, max_tokens, max_slots):
+    from tests.gpu_util import config_for, weights_for
+    cfg = config_for(wl.shape, max_slots=max_slots, max_ctx=max_ctx, max_batch=max_batch, max_tokens=max_tokens,
+                     sync_errors=0)
+    wref = weights_for(wl.w)
+    return m.tts_bb_create(cfg, wref, stream)
+
+
+# ---------------------------------------------------------------- our arm: talker_b1
+def run_talker_b1(args, ws, rank):
+    import torch
+    import codec_token_tts_gb300 as m
+    from tests.gpu_util import dev_i32
+
+    wl = TalkerB1()
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    h = make_engine(wl, m, stream.cuda_stream, P_PREFILL + N_DECODE, 1, P_PREFILL, 1)
+    n_all = max(args.steps, args.warmup) + 1
+    # ids for every decode step: column 0 is overwritten by the previous step's argmax
+    rest = np.tile(wl.rest, ((n_all + N_DECODE - 1) // N_DECODE, 1))[:n_all]
+    ids = np.concatenate([np.zeros((n_all, 1), np.int32), rest], axis=1)
+    ids_d = dev_i32(ids)
+    logits = torch.zeros(1, 3072, dtype=torch.float32, device="cuda")
+    pre_ids = dev_i32(wl.prefill_ids.reshape(1, P_PREFILL, 16))
+    first = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m.tts_bb_prefill(h, 1, P_PREFILL, [0], [P_PREFILL], pre_ids, 0, logits, first)
+    slot, kv = np.zeros(1, np.int32), np.zeros(1, np.int32)
+
+    def steps(n):
+        """n decode steps, rewinding to position 128 every 256 steps."""
+        for t in range(n):
+            pos = P_PREFILL + (t % N_DECODE)
+            if pos == P_PREFILL:
+                m.tts_bb_truncate(h, 0, P_PREFILL)
+                ids_d[t, 0:1].copy_(first)
+            kv[0] = pos
+            m.lib.tts_bb_decode_step(h, 1, slot.ctypes.data, kv.ctypes.data, ids_d[t].data_ptr(), 0,
+                                     logits.data_ptr(), ids_d[t + 1].data_ptr(), None)
+
+    steps(args.warmup)
+    m.tts_bb_sync(h)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or 0))
+    n0 = m.tts_bb_launch_count(h)
+    dist_barrier(ws)
+    torch.cuda.synchronize()
+    clocks.start()
+    ev0.record(stream)
+    steps(args.steps)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    dist_barrier(ws)
+    ms = ev0.elapsed_time(ev1)
+    launches = m.tts_bb_launch_count(h) - n0
+    m.tts_bb_sync(h)
+    ms_max = dist_max(ws, ms)
+
+    # profiled pass: per-kernel event times for the roofline of the dominant kernel
+    m.tts_bb_profile(h, True)
+    steps(min(args.steps, 2 * N_DECODE))
+    rep = m.tts_bb_profile_report(h)
+    m.tts_bb_profile(h, False)
+
+    # end to end through the public API with host buffers: per step, copy the
+    # ids from pinned host memory, run the step, read the argmax back
+    host_ids = torch.from_numpy(ids.copy()).pin_memory()
+    host_am = torch.zeros(1, dtype=torch.int32).pin_memory()
+    dev_row = torch.zeros(16, dtype=torch.int32, device="cuda")
+    dev_am = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m.tts_bb_truncate(h, 0, P_PREFILL)
+    first_host = int(first.cpu().item())
+    n_e2e = min(args.steps, 4 * N_DECODE)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    nxt = first_host
+    for t in range(n_e2e):
+        pos = P_PREFILL + (t % N_DECODE)
+        if pos == P_PREFILL:
+            m.tts_bb_truncate(h, 0, P_PREFILL)
+            nxt = first_host
+        host_ids[t, 0] = nxt
+        dev_row.copy_(host_ids[t], non_blocking=True)
+        kv[0] = pos
+        m.lib.tts_bb_decode_step(h, 1, slot.ctypes.data, kv.ctypes.data, dev_row.data_ptr(), 0, logits.data_ptr(),
+                                 dev_am.data_ptr(), None)
+        host_am.copy_(dev_am, non_blocking=True)
+        stream.synchronize()
+        nxt = int(host_am[0])
+    e2e_s = time.perf_counter() - t0
+    m.tts_bb_sync(h)
+    m.tts_bb_free(h)
+
+    tokens = args.steps * ws
+    value = tokens / (ms_max / 1e3)
+    pos_bytes = np.mean([wl.algorithmic_bytes_per_step(P_PREFILL + (t % N_DECODE)) for t in range(N_DECODE)])
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic", "config": dict(wl.config(), parallelism="replicas" if ws > 1 else "single"),
+        "hbm_step_roofline": {"algorithmic_bytes_per_step": pos_bytes,
+                              "achieved_gbs": pos_bytes / (ms_max / args.steps) / 1e6},
+        "clocks": clk, "gpu_launches": int(launches),
+        "e2e": {"value": n_e2e / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 16 * 4, "d2h_bytes_per_step": 4},
+        "kernel_profile": rep,
+    }
+    return res, wl
+
+
+def roofline_from_profile(rep, traffic=None):
+    pk, src = peaks()
+    ks = rep.get("kernels", [])
+    if not ks:
+        return None
+    top = max(ks, key=lambda k: k["ms"])
+    total = sum(k["ms"] for k in ks)
+    if top["flops"] and top["bytes"] and top["flops"] / max(top["bytes"], 1) > 300:
+        ach = top["flops"] / (top["ms"] / 1e3) / 1e12
+        peak = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+        return {"kernel": top["kind"], "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": traffic, "peak_source": f"{src} bf16_tflops_sustained",
+                "share": top["ms"] / total, "launches": top["launches"]}
+    ach = top["bytes"] / (top["ms"] / 1e3) / 1e9
+    peak = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    return {"kernel": top["kind"], "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+            "frac": ach / peak, "traffic": traffic, "peak_source": f"{src} hbm_gbs",
+            "bytes_per_launch": top["bytes"] / top["launches"], "share": top["ms"] / total,
+            "launches": top["launches"]}
+
+
+def measured_traffic(rep):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if one exists."""
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    ks = rep.get("kernels", [])
+    if not ks or not os.path.exists(tp):
+        return None
+    with open(tp) as f:
+        return json.load(f).get(max(ks, key=lambda k: k["ms"])["kind"])
+
+
+# ---------------------------------------------------------------- oracle timing (CPU baseline / reference arm)
+def oracle_talker_tokens_per_s(budget_s: float, max_steps: int):
+    """Time the fp64 oracle on decode steps of the talker_b1 workload (positions 128..)."""
+    import oracle as O
+    wl = TalkerB1()
+    t_setup = time.perf_counter()
+    mo = O.Backbone(wl.w, wl.shape)
+    cache = mo.new_cache()
+    _, _, a0 = O.talker_prefill(mo, wl.prefill_ids, cache)
+    setup_s = time.perf_counter() - t_setup
+    n = 0
+    t0 = time.perf_counter()
+    id0 = a0
+    while n < max_steps and (time.perf_counter() - t0) < budget_s:
+        _, _, am, _ = O.talker_decode_steps(mo, cache, id0, wl.rest[n:n + 1])
+        id0 = int(am[0])
+        n += 1
+    el = time.perf_counter() - t0
+    return n / el, n, el, setup_s
+
+
+def cpu_info():
+    return {"cores": os.cpu_count(), "blas_threads": os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get(
+        "OMP_NUM_THREADS") or "default (all cores)"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return None
+    budget = float(os.environ.get("TTS_BB_REF_BUDGET_S", "120"))
+    _ = oracle_talker_tokens_per_s(5.0, max(1, args.warmup)) if args.warmup else None
+    v, n, el, setup_s = oracle_talker_tokens_per_s(budget, args.steps)
+    ci = cpu_info()
+    wl_cfg = {"workload": "talker_b1: Qwen3-0.6B-shaped Talker, 28 layers, batch 1, 128-position prefill then "
+                          "decode at positions 128..383, 3072-way head, greedy id0 fed back",
+              "global_batch": 1, "seq_len": P_PREFILL + N_DECODE, "layers": 28}
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws, "steps": n,
+            "steps_requested": args.steps, "warmup": args.warmup, "ms_per_step": el / n * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": wl_cfg,
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": ci["cores"], "kind": "oracle",
+                             "sample": f"{n} decode steps from position 128 after the oracle's 128-position prefill "
+                                       f"({setup_s:.1f} s untimed setup), {ci['blas_threads']} BLAS threads"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2048)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="talker_b1", choices=["talker_b1"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    if args.impl == "reference":
+        ws, rank, _ = dist_setup("gloo")
+        res = run_reference(args, ws, rank)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
+
+    import torch
+    ws, rank, local = dist_setup("nccl")
+    torch.cuda.set_device(local)
+    from tests.gpu_util import build_lib
+    build_lib()
+    res, wl = run_talker_b1(args, ws, rank)
+    res["roofline"] = roofline_from_profile(res["kernel_profile"], measured_traffic(res["kernel_profile"]))
+    if rank == 0 and not args.no_cpu_baseline:
+        v, n, el, setup_s = oracle_talker_tokens_per_s(args.cpu_budget_s, 10_000)
+        ci = cpu_info()
+        res["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": ci["cores"], "kind": "oracle",
+                               "sample": f"{n} Talker decode steps from position 128 in {el:.1f} s after an untimed "
+                                         f"128-position prefill ({setup_s:.1f} s), {ci['blas_threads']} BLAS threads"}
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -75,6 +75,8 @@ def _load() -> C.CDLL:
         "tts_bb_debug_kv_read": (I, [P, I, I, I, I, P, P]),
         "tts_bb_debug_kv_write": (I, [P, I, I, I, I, P, P]),
         "tts_bb_launch_count": (C.c_uint64, [P]),
+        "tts_bb_profile": (I, [P, I]),
+        "tts_bb_profile_report": (C.c_char_p, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -87,7 +89,7 @@ lib = _load()
 EXPORTED = ("tts_bb_default_config", "tts_bb_create", "tts_bb_free", "tts_bb_prefill", "tts_bb_decode_step",
             "tts_bb_maskgit_pass", "tts_bb_release", "tts_bb_truncate", "tts_bb_slot_len", "tts_bb_sync",
             "tts_bb_last_error", "tts_bb_version", "tts_bb_debug_kv_read", "tts_bb_debug_kv_write",
-            "tts_bb_launch_count")
+            "tts_bb_launch_count", "tts_bb_profile", "tts_bb_profile_report")
 
 
 def _ptr(x) -> Optional[int]:
@@ -226,3 +228,12 @@ def tts_bb_debug_kv_write(h, layer: int, slot: int, pos0: int, n: int, k, v, che
 
 def tts_bb_launch_count(h) -> int:
     return int(lib.tts_bb_launch_count(h))
+
+
+def tts_bb_profile(h, on: bool) -> int:
+    return _check(h, lib.tts_bb_profile(h, 1 if on else 0))
+
+
+def tts_bb_profile_report(h) -> dict:
+    import json
+    return json.loads(lib.tts_bb_profile_report(h).decode())

@@ -115,6 +115,12 @@ struct tts_bb {
     std::string last_error;
     uint64_t launches = 0;
     SetupArgs* setup = nullptr;  // host staging (large struct)
+    // per-kernel timing (tts_bb_profile): events around every launch, by kernel kind
+    bool prof_on = false;
+    struct ProfRec { int kind; cudaEvent_t a, b; double bytes; double flops; };
+    std::vector<ProfRec> prof;
+    std::vector<cudaEvent_t> ev_pool;
+    std::string prof_json;
 };
 
 namespace {
@@ -189,6 +195,49 @@ tts_bb_status finish(tts_bb* h) {
     return TTS_BB_OK;
 }
 
+enum Kind { K_SETUP, K_EMBED, K_RMSNORM, K_GEMV, K_GEMM, K_QKROPE, K_ATTN_DECODE, K_ATTN_PREFILL, K_ARGMAX,
+            K_KVCOPY, K_NKINDS };
+const char* kind_name[K_NKINDS] = {"setup", "embed_gather", "rmsnorm", "gemv", "gemm_mma", "qk_norm_rope_append",
+                                   "attn_decode", "attn_prefill", "argmax", "kv_copy"};
+
+cudaEvent_t prof_event(tts_bb* h) {
+    if (!h->ev_pool.empty()) {
+        cudaEvent_t e = h->ev_pool.back();
+        h->ev_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+// Brackets the launches of one engine step with CUDA events when profiling is on,
+// and counts the kernels launched. bytes / flops: algorithmic work of the launch.
+struct Launch {
+    tts_bb* h;
+    int kind;
+    double bytes, flops;
+    cudaEvent_t a = nullptr;
+    Launch(tts_bb* h_, int kind_, double bytes_ = 0, double flops_ = 0) : h(h_), kind(kind_), bytes(bytes_), flops(flops_) {
+        if (h->prof_on) {
+            a = prof_event(h);
+            cudaEventRecord(a, h->st);
+        }
+    }
+    void operator+=(int n) { h->launches += n; }
+    ~Launch() {
+        if (a) {
+            cudaEvent_t b = prof_event(h);
+            cudaEventRecord(b, h->st);
+            h->prof.push_back({kind, a, b, bytes, flops});
+        }
+    }
+};
+
+double gemm_bytes(int T, int N, int K, int out_bytes) {
+    return 2.0 * N * K + 2.0 * T * K + (double)out_bytes * T * N;
+}
+
 // Scratch for T tokens (grows on demand; only between calls).
 tts_bb_status ensure_scratch(tts_bb* h, int T) {
     if (T <= h->T_cap) return TTS_BB_OK;
@@ -216,41 +265,48 @@ tts_bb_status ensure_scratch(tts_bb* h, int T) {
 }
 
 void launch_setup(tts_bb* h, SetupArgs& a) {
+    Launch L(h, K_SETUP);
     k_setup<<<1, 256, 0, h->st>>>(a, h->seq_slot, h->seq_start, h->seq_len, h->key_len, h->d_page_table, h->amax);
-    h->launches++;
+    L += 1;
 }
 
 // The layer schedule shared by every mode. T tokens laid out as B sequences x
 // tok_per_seq positions; mode: 0 decode (query length 1), 1 causal prefill,
 // 2 bidirectional pass.
-void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView kv_base, size_t layer_stride) {
+void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView kv_base, size_t layer_stride,
+                double kv_read_bytes = 0, double attn_flops = 0) {
     const tts_bb_config& c = h->cfg;
     const int T = B * tok_per_seq;
     for (int l = 0; l < c.n_layers; ++l) {
         const LayerW& w = h->L[l];
         KVView kv = kv_base;
         kv.pool = kv_base.pool + (size_t)l * layer_stride;
-        h->launches += launch_rmsnorm(h->h, w.in_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st);
+        const int gk = T <= 8 ? K_GEMV : K_GEMM;
+        const double norm_bytes = T * (4.0 + 2.0) * HID + 2.0 * HID;
+        { Launch L(h, K_RMSNORM, norm_bytes); L += launch_rmsnorm(h->h, w.in_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st); }
         Epi e{};
         e.mode = EPI_STORE_F32; e.out = h->qkv; e.ldo = QKV;
-        h->launches += launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st);
-        h->launches += launch_qk_norm_rope_append(h->qkv, w.qn, w.kn, h->cos_t, h->sin_t, c.rms_eps, h->q, kv,
-                                                  h->seq_start, h->seq_len, tok_per_seq, T, h->err, h->st);
-        if (mode == 0)
-            h->launches += launch_attn_decode(h->q, kv, h->seq_start, B, max_len, h->part, h->ao, MAX_SPLITS, h->st);
-        else
-            h->launches += launch_attn_prefill(h->q, kv, h->seq_start, h->seq_len, h->key_len, mode == 1, B,
-                                               tok_per_seq, h->ao, h->st);
+        { Launch L(h, gk, gemm_bytes(T, QKV, HID, 4), 2.0 * T * QKV * HID); L += launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st); }
+        { Launch L(h, K_QKROPE, T * (4.0 * QKV + 2.0 * QKV));
+          L += launch_qk_norm_rope_append(h->qkv, w.qn, w.kn, h->cos_t, h->sin_t, c.rms_eps, h->q, kv,
+                                          h->seq_start, h->seq_len, tok_per_seq, T, h->err, h->st); }
+        if (mode == 0) {
+            Launch L(h, K_ATTN_DECODE, kv_read_bytes + T * (2.0 * NQ * HD * 2), 4.0 * NQ * HD * (kv_read_bytes / (2.0 * NKV * HD * 2)));
+            L += launch_attn_decode(h->q, kv, h->seq_start, B, max_len, h->part, h->ao, MAX_SPLITS, h->st);
+        } else {
+            Launch L(h, K_ATTN_PREFILL, 0, attn_flops);
+            L += launch_attn_prefill(h->q, kv, h->seq_start, h->seq_len, h->key_len, mode == 1, B, tok_per_seq, h->ao, h->st);
+        }
         e = Epi{};
         e.mode = EPI_ADD_F32; e.out = h->h; e.ldo = HID;
-        h->launches += launch_gemm(h->ao, w.wo, T, HID, NQ * HD, e, h->st);
-        h->launches += launch_rmsnorm(h->h, w.post_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st);
+        { Launch L(h, gk, gemm_bytes(T, HID, NQ * HD, 8), 2.0 * T * HID * NQ * HD); L += launch_gemm(h->ao, w.wo, T, HID, NQ * HD, e, h->st); }
+        { Launch L(h, K_RMSNORM, norm_bytes); L += launch_rmsnorm(h->h, w.post_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st); }
         e = Epi{};
         e.mode = EPI_SWIGLU; e.out = h->m; e.ldo = c.ffn;
-        h->launches += launch_gemm(h->y, w.wgu, T, 2 * c.ffn, HID, e, h->st);
+        { Launch L(h, gk, gemm_bytes(T, 2 * c.ffn, HID, 1), 2.0 * T * 2 * c.ffn * HID); L += launch_gemm(h->y, w.wgu, T, 2 * c.ffn, HID, e, h->st); }
         e = Epi{};
         e.mode = EPI_ADD_F32; e.out = h->h; e.ldo = HID;
-        h->launches += launch_gemm(h->m, w.wd, T, HID, c.ffn, e, h->st);
+        { Launch L(h, gk, gemm_bytes(T, HID, c.ffn, 8), 2.0 * T * HID * c.ffn); L += launch_gemm(h->m, w.wd, T, HID, c.ffn, e, h->st); }
     }
 }
 
@@ -258,12 +314,13 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
 void run_head(tts_bb* h, int B, int per_seq, int head_idx, bool last_of_seq, float* logits_out, int32_t* argmax_out,
               int argmax_stride) {
     const tts_bb_config& c = h->cfg;
-    h->launches += launch_rmsnorm(h->h, h->final_norm, h->y, B, c.rms_eps, 1, per_seq, 0,
-                                  last_of_seq ? h->seq_len : nullptr, h->st);
+    { Launch L(h, K_RMSNORM, B * 6.0 * HID + 2.0 * HID);
+      L += launch_rmsnorm(h->h, h->final_norm, h->y, B, c.rms_eps, 1, per_seq, 0, last_of_seq ? h->seq_len : nullptr, h->st); }
     Epi e{};
     e.mode = EPI_LOGITS; e.out = logits_out; e.ldo = c.head_rows; e.amax = argmax_out ? h->amax : nullptr;
-    h->launches += launch_gemm(h->y, h->heads[head_idx], B, c.head_rows, HID, e, h->st);
-    if (argmax_out) h->launches += launch_argmax_finalize(h->amax, argmax_out, argmax_stride, B, h->st);
+    { Launch L(h, B <= 8 ? K_GEMV : K_GEMM, gemm_bytes(B, c.head_rows, HID, logits_out ? 4 : 0), 2.0 * B * c.head_rows * HID);
+      L += launch_gemm(h->y, h->heads[head_idx], B, c.head_rows, HID, e, h->st); }
+    if (argmax_out) { Launch L(h, K_ARGMAX); L += launch_argmax_finalize(h->amax, argmax_out, argmax_stride, B, h->st); }
 }
 
 bool slots_ok(tts_bb* h, int B, const int32_t* slots) {
@@ -358,6 +415,8 @@ TTS_API void tts_bb_free(tts_bb* h) {
     else cudaDeviceSynchronize();
     for (void* p : h->allocs) cudaFree(p);
     if (h->h_err) cudaFreeHost(h->h_err);
+    for (auto& r : h->prof) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
+    for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
     delete h->setup;
     cudaSetDevice(cur);
     delete h;
@@ -571,9 +630,14 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
         h->slot_len[slots[b]] = nl[b];
     }
     launch_setup(h, a);
-    h->launches += launch_embed_codebooks(h->tabs, ids, reinterpret_cast<const bf16*>(embeds), h->h, B, h->err, h->st);
+    {
+        Launch L(h, K_EMBED, B * (4.0 * HID + (ids ? 2.0 * HID * c.n_codebooks : 0) + (embeds ? 2.0 * HID : 0)));
+        L += launch_embed_codebooks(h->tabs, ids, reinterpret_cast<const bf16*>(embeds), h->h, B, h->err, h->st);
+    }
     KVView kv{h->pool, h->d_page_table, h->seq_slot, h->mbps};
-    run_layers(h, B, 1, 0, max_len, kv, h->layer_elems);
+    double kv_bytes = 0;
+    for (int b = 0; b < B; ++b) kv_bytes += (double)nl[b] * 2 * NKV * HD * 2;
+    run_layers(h, B, 1, 0, max_len, kv, h->layer_elems, kv_bytes);
     if (opts && opts->hidden_out)
         cudaMemcpyAsync(opts->hidden_out, h->h, (size_t)B * HID * sizeof(float), cudaMemcpyDeviceToDevice, h->st);
     if (head_idx >= 0 && (logits_out || argmax_out))
@@ -616,9 +680,15 @@ TTS_API tts_bb_status tts_bb_prefill(tts_bb* h, int B, int S, const int32_t* slo
     }
     launch_setup(h, a);
     const int T = B * S;
-    h->launches += launch_embed_codebooks(h->tabs, ids, reinterpret_cast<const bf16*>(embeds), h->h, T, h->err, h->st);
+    {
+        Launch L(h, K_EMBED, T * (4.0 * HID + (ids ? 2.0 * HID * c.n_codebooks : 0) + (embeds ? 2.0 * HID : 0)));
+        L += launch_embed_codebooks(h->tabs, ids, reinterpret_cast<const bf16*>(embeds), h->h, T, h->err, h->st);
+    }
     KVView kv{h->pool, h->d_page_table, h->seq_slot, h->mbps};
-    run_layers(h, B, S, 1, 0, kv, h->layer_elems);
+    double aflops = 0;   // causal: query j of a row sees start + j + 1 keys
+    for (int b = 0; b < B; ++b)
+        aflops += 4.0 * NQ * HD * ((double)lens[b] * a.start[b] + 0.5 * (double)lens[b] * (lens[b] + 1));
+    run_layers(h, B, S, 1, 0, kv, h->layer_elems, 0, aflops);
     if (opts && opts->hidden_out)
         cudaMemcpyAsync(opts->hidden_out, h->h, (size_t)T * HID * sizeof(float), cudaMemcpyDeviceToDevice, h->st);
     if (head_idx >= 0 && (logits_out || argmax_out))
@@ -666,19 +736,27 @@ TTS_API tts_bb_status tts_bb_maskgit_pass(tts_bb* h, int B, int S, const int32_t
         a.key_len[b] = key_lens ? key_lens[b] : S;
     }
     launch_setup(h, a);
-    h->launches += launch_embed_omnivoice(h->text, c.text_vocab, h->audio, c.audio_codebooks, c.audio_vocab, ids,
-                                          audio_mask, h->h, B, S, h->err, h->st);
+    {
+        Launch L(h, K_EMBED);
+        L += launch_embed_omnivoice(h->text, c.text_vocab, h->audio, c.audio_codebooks, c.audio_vocab, ids, audio_mask,
+                                    h->h, B, S, h->err, h->st);
+    }
     KVView kv{h->mg_pool, nullptr, h->seq_slot, bps};
-    run_layers(h, B, S, 2, 0, kv, 0);
+    double aflops = 0;
+    for (int b = 0; b < B; ++b) aflops += 4.0 * NQ * HD * (double)S * a.key_len[b];
+    run_layers(h, B, S, 2, 0, kv, 0, 0, aflops);
     if (opts && opts->hidden_out)
         cudaMemcpyAsync(opts->hidden_out, h->h, (size_t)B * S * HID * sizeof(float), cudaMemcpyDeviceToDevice, h->st);
     if (logits_out) {
         const int Sa = S - audio_start;
-        h->launches += launch_rmsnorm(h->h, h->final_norm, h->y, B * Sa, c.rms_eps, Sa, S, audio_start, nullptr, h->st);
+        { Launch L(h, K_RMSNORM, B * Sa * 6.0 * HID);
+          L += launch_rmsnorm(h->h, h->final_norm, h->y, B * Sa, c.rms_eps, Sa, S, audio_start, nullptr, h->st); }
         Epi e{};
         e.mode = EPI_LOGITS_PERM; e.out = logits_out; e.perm_rows = Sa; e.perm_vocab = c.head_rows;
         e.perm_groups = c.n_heads;
-        h->launches += launch_gemm(h->y, h->heads[0], B * Sa, c.n_heads * c.head_rows, HID, e, h->st);
+        const int N = c.n_heads * c.head_rows;
+        Launch L(h, B * Sa <= 8 ? K_GEMV : K_GEMM, gemm_bytes(B * Sa, N, HID, 4), 2.0 * B * Sa * N * HID);
+        L += launch_gemm(h->y, h->heads[0], B * Sa, N, HID, e, h->st);
     }
     return finish(h);
 }
@@ -689,9 +767,12 @@ TTS_API tts_bb_status tts_bb_debug_kv_read(tts_bb* h, int layer, int slot, int p
         pos0 < 0 || n < 0 || pos0 + n > h->slot_len[slot] || !k_out || !v_out)
         return fail(h, TTS_BB_E_INVALID, "debug_kv_read: bad arguments");
     if (n == 0) return TTS_BB_OK;
-    k_kv_copy<<<n, 256, 0, h->st>>>(h->pool + (size_t)layer * h->layer_elems, h->d_page_table, slot, h->mbps, pos0, n,
-                                    reinterpret_cast<bf16*>(k_out), reinterpret_cast<bf16*>(v_out), 0);
-    h->launches++;
+    {
+        Launch L(h, K_KVCOPY);
+        k_kv_copy<<<n, 256, 0, h->st>>>(h->pool + (size_t)layer * h->layer_elems, h->d_page_table, slot, h->mbps, pos0, n,
+                                        reinterpret_cast<bf16*>(k_out), reinterpret_cast<bf16*>(v_out), 0);
+        L += 1;
+    }
     return finish(h);
 }
 
@@ -712,9 +793,51 @@ TTS_API tts_bb_status tts_bb_debug_kv_write(tts_bb* h, int layer, int slot, int 
     if (s != TTS_BB_OK) return s;
     h->slot_len[slot] = new_len;
     launch_setup(h, a);
-    k_kv_copy<<<n, 256, 0, h->st>>>(h->pool + (size_t)layer * h->layer_elems, h->d_page_table, slot, h->mbps, pos0, n,
-                                    const_cast<bf16*>(reinterpret_cast<const bf16*>(k)),
-                                    const_cast<bf16*>(reinterpret_cast<const bf16*>(v)), 1);
-    h->launches++;
+    {
+        Launch L(h, K_KVCOPY);
+        k_kv_copy<<<n, 256, 0, h->st>>>(h->pool + (size_t)layer * h->layer_elems, h->d_page_table, slot, h->mbps, pos0, n,
+                                        const_cast<bf16*>(reinterpret_cast<const bf16*>(k)),
+                                        const_cast<bf16*>(reinterpret_cast<const bf16*>(v)), 1);
+        L += 1;
+    }
     return finish(h);
+}
+
+TTS_API tts_bb_status tts_bb_profile(tts_bb* h, int on) {
+    if (!h) return TTS_BB_E_INVALID;
+    cudaStreamSynchronize(h->st);
+    for (auto& r : h->prof) {
+        h->ev_pool.push_back(r.a);
+        h->ev_pool.push_back(r.b);
+    }
+    h->prof.clear();
+    h->prof_on = on != 0;
+    return TTS_BB_OK;
+}
+
+TTS_API const char* tts_bb_profile_report(tts_bb* h) {
+    if (!h) return "{}";
+    cudaStreamSynchronize(h->st);
+    double ms[K_NKINDS] = {}, bytes[K_NKINDS] = {}, flops[K_NKINDS] = {};
+    long n[K_NKINDS] = {};
+    for (const auto& r : h->prof) {
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess) ms[r.kind] += t;
+        bytes[r.kind] += r.bytes;
+        flops[r.kind] += r.flops;
+        n[r.kind]++;
+    }
+    std::string j = "{\"kernels\": [";
+    bool first = true;
+    for (int k = 0; k < K_NKINDS; ++k) {
+        if (!n[k]) continue;
+        char buf[320];
+        snprintf(buf, sizeof buf, "%s{\"kind\": \"%s\", \"launches\": %ld, \"ms\": %.6f, \"bytes\": %.0f, \"flops\": %.0f}",
+                 first ? "" : ", ", kind_name[k], n[k], ms[k], bytes[k], flops[k]);
+        j += buf;
+        first = false;
+    }
+    j += "]}";
+    h->prof_json = j;
+    return h->prof_json.c_str();
 }

@@ -237,6 +237,17 @@ tts_bb_status tts_bb_debug_kv_write(tts_bb* h, int layer, int slot, int pos0, in
  * counter kept on the host; lets a caller count launches in a timed region). */
 uint64_t tts_bb_launch_count(const tts_bb* h);
 
+/* Per-kernel timing. tts_bb_profile(h, 1) clears the record and brackets
+ * every later kernel launch of the handle with CUDA events on its stream;
+ * tts_bb_profile(h, 0) stops. tts_bb_profile_report waits for the stream and
+ * returns a JSON summary {"kernels": [{"kind", "launches", "ms", "bytes",
+ * "flops"}]}: per kernel kind, the launches, their summed event time and
+ * their algorithmic bytes and flops. The string stays valid until the next
+ * report or tts_bb_free. The events add a little time between launches, so
+ * time a clean run without profiling. */
+tts_bb_status tts_bb_profile(tts_bb* h, int on);
+const char* tts_bb_profile_report(tts_bb* h);
+
 #ifdef __cplusplus
 }
 #endif

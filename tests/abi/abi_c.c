@@ -45,6 +45,8 @@ int main(void) {
     EXPECT(tts_bb_debug_kv_read(NULL, 0, 0, 0, 1, k, v) == TTS_BB_E_INVALID);
     EXPECT(tts_bb_debug_kv_write(NULL, 0, 0, 0, 1, k, v) == TTS_BB_E_INVALID);
     EXPECT(tts_bb_launch_count(NULL) == 0);
+    EXPECT(tts_bb_profile(NULL, 1) == TTS_BB_E_INVALID);
+    EXPECT(strcmp(tts_bb_profile_report(NULL), "{}") == 0);
     EXPECT(strlen(tts_bb_last_error(NULL)) > 0);
     tts_bb_free(NULL);
     printf("abi_c: ok\n");
