@@ -77,6 +77,7 @@ def _load() -> C.CDLL:
         "tts_bb_launch_count": (C.c_uint64, [P]),
         "tts_bb_profile": (I, [P, I]),
         "tts_bb_profile_report": (C.c_char_p, [P]),
+        "tts_bb_gqa_decode_attention_static": (I, [P, P, P, I, P, I, I, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -89,7 +90,8 @@ lib = _load()
 EXPORTED = ("tts_bb_default_config", "tts_bb_create", "tts_bb_free", "tts_bb_prefill", "tts_bb_decode_step",
             "tts_bb_maskgit_pass", "tts_bb_release", "tts_bb_truncate", "tts_bb_slot_len", "tts_bb_sync",
             "tts_bb_last_error", "tts_bb_version", "tts_bb_debug_kv_read", "tts_bb_debug_kv_write",
-            "tts_bb_launch_count", "tts_bb_profile", "tts_bb_profile_report")
+            "tts_bb_launch_count", "tts_bb_profile", "tts_bb_profile_report",
+            "tts_bb_gqa_decode_attention_static")
 
 
 def _ptr(x) -> Optional[int]:
@@ -237,3 +239,11 @@ def tts_bb_profile(h, on: bool) -> int:
 def tts_bb_profile_report(h) -> dict:
     import json
     return json.loads(lib.tts_bb_profile_report(h).decode())
+
+
+def tts_bb_gqa_decode_attention_static(q, kv_pool, page_table, blocks_per_seq: int, positions, B: int,
+                                       max_position: int, out, stream: int = 0) -> int:
+    """Decode attention on caller buffers with the library's fixed scratch (allocates nothing)."""
+    return lib.tts_bb_gqa_decode_attention_static(_ptr(q), _ptr(kv_pool), _ptr(page_table), blocks_per_seq,
+                                                  _ptr(positions), B, max_position, _ptr(out),
+                                                  C.c_void_p(stream or None))

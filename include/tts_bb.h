@@ -248,6 +248,43 @@ uint64_t tts_bb_launch_count(const tts_bb* h);
 tts_bb_status tts_bb_profile(tts_bb* h, int on);
 const char* tts_bb_profile_report(tts_bb* h);
 
+/* Decode attention that allocates nothing (the pages have no counterpart: it
+ * exists for callers of this library that may not call cudaMalloc — a plug-in
+ * whose host framework owns every device allocation, work recorded during
+ * CUDA stream capture where cudaMalloc is not allowed, or a real-time audio
+ * thread that must not block in the allocator).
+ *
+ * It runs the same split-K GQA flash-decode kernels as tts_bb_decode_step on
+ * the caller's own buffers; the split partials go to a fixed array in device
+ * memory that is part of the library (TTS_BB_STATIC_ATTN_MAX_B x 16 heads x
+ * TTS_BB_STATIC_ATTN_MAX_SPLITS x 130 floats = 4.26 MB, held by every GPU that
+ * loads the library until the process exits). No cudaMalloc or cudaFree, no
+ * allocating library call.
+ *   q           device bf16 [B][16][128]: queries after q-norm and RoPE
+ *   kv_pool     device bf16 blocks [n][2][8][64][128]: block p holds K then V
+ *               of 64 positions for the 8 KV heads (the engine's pool layout)
+ *   page_table  device int32 [B][blocks_per_seq]: physical block of each
+ *               64-token block of sequence b
+ *   positions   device int32 [B]: position of the query token of sequence b;
+ *               its K/V must already be in the pool, attention covers
+ *               positions 0..positions[b]
+ *   max_position the largest value in positions (host int)
+ *   out         device bf16 [B][16][128]
+ *   stream      cudaStream_t (NULL = legacy default stream)
+ * Returns TTS_BB_E_INVALID for NULL pointers, B outside
+ * 1..TTS_BB_STATIC_ATTN_MAX_B or a max_position the page table cannot hold;
+ * TTS_BB_E_CUDA if a launch fails. The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current:
+ * make that first call before any stream capture. Every call shares the
+ * array and overwrites all the partials it reads, so nothing needs clearing
+ * between calls; calls that overlap on the GPU (other streams, other host
+ * threads) race on it and must be serialised by the caller. */
+#define TTS_BB_STATIC_ATTN_MAX_B 64
+#define TTS_BB_STATIC_ATTN_MAX_SPLITS 8
+tts_bb_status tts_bb_gqa_decode_attention_static(const void* q, const void* kv_pool, const int32_t* page_table,
+                                                 int blocks_per_seq, const int32_t* positions, int B,
+                                                 int max_position, void* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

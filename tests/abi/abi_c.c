@@ -48,6 +48,9 @@ int main(void) {
     EXPECT(tts_bb_profile(NULL, 1) == TTS_BB_E_INVALID);
     EXPECT(strcmp(tts_bb_profile_report(NULL), "{}") == 0);
     EXPECT(strlen(tts_bb_last_error(NULL)) > 0);
+    EXPECT(tts_bb_gqa_decode_attention_static(NULL, NULL, NULL, 1, NULL, 1, 0, NULL, NULL) == TTS_BB_E_INVALID);
+    EXPECT(tts_bb_gqa_decode_attention_static(k, k, slots, 1, slots, TTS_BB_STATIC_ATTN_MAX_B + 1, 0, v, NULL) ==
+           TTS_BB_E_INVALID);
     tts_bb_free(NULL);
     printf("abi_c: ok\n");
     return 0;
