@@ -11,6 +11,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "mega.cuh"
 #include "../../include/tts_bb.h"
 
 using namespace ttsbb;
@@ -121,6 +122,20 @@ struct tts_bb {
     std::vector<ProfRec> prof;
     std::vector<cudaEvent_t> ev_pool;
     std::string prof_json;
+    // persistent small-batch decode step
+    int mega_grid = 0;                 // 0 = not available on this device
+    unsigned long long* mega_bar = nullptr;
+    int* mega_abort = nullptr;
+    float* mega_part = nullptr;
+    unsigned long long bar_base = 0;
+    MegaArgs* mega = nullptr;          // per-handle constant fields filled at create
+    unsigned long long* mega_trace = nullptr;   // phase stamps while profiling
+    std::vector<double> phase_us;      // summed per-phase mean-over-CTA durations over traced layers
+    std::vector<double> phase_max_us;  // summed per-phase max-over-CTA durations
+    long phase_n = 0;                  // traced layers
+    double unit_us[3] = {0, 0, 0};     // attention unit sub-phases (CTAs with a unit)
+    double ring_wait_us = 0, ring_wait_max_us = 0;  // weight-ring waits per layer (mean, max over CTAs)
+    long unit_n = 0;
 };
 
 namespace {
@@ -180,6 +195,11 @@ tts_bb_status read_err(tts_bb* h) {
     const int v = *h->h_err;
     if (v) {
         cudaMemsetAsync(h->err, 0, sizeof(int), h->st);
+        if ((v & ERR_TIMEOUT) && h->mega_bar) {  // restart the persistent step's barrier state
+            cudaMemsetAsync(h->mega_bar, 0, sizeof(unsigned long long), h->st);
+            cudaMemsetAsync(h->mega_abort, 0, sizeof(int), h->st);
+            h->bar_base = 0;
+        }
         cudaStreamSynchronize(h->st);
         if (v & ERR_TIMEOUT) return fail(h, TTS_BB_E_DEVICE_TIMEOUT, "a device-side wait timed out");
         if (v & ERR_BAD_ID) return fail(h, TTS_BB_E_BAD_ID, "a token id was outside its table (skipped)");
@@ -196,9 +216,9 @@ tts_bb_status finish(tts_bb* h) {
 }
 
 enum Kind { K_SETUP, K_EMBED, K_RMSNORM, K_GEMV, K_GEMM, K_QKROPE, K_ATTN_DECODE, K_ATTN_PREFILL, K_ARGMAX,
-            K_KVCOPY, K_NKINDS };
+            K_KVCOPY, K_MEGA, K_NKINDS };
 const char* kind_name[K_NKINDS] = {"setup", "embed_gather", "rmsnorm", "gemv", "gemm_mma", "qk_norm_rope_append",
-                                   "attn_decode", "attn_prefill", "argmax", "kv_copy"};
+                                   "attn_decode", "attn_prefill", "argmax", "kv_copy", "decode_step_persistent"};
 
 cudaEvent_t prof_event(tts_bb* h) {
     if (!h->ev_pool.empty()) {
@@ -418,6 +438,7 @@ TTS_API void tts_bb_free(tts_bb* h) {
     for (auto& r : h->prof) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
     for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
     delete h->setup;
+    delete h->mega;
     cudaSetDevice(cur);
     delete h;
 }
@@ -560,6 +581,46 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
     cudaMemset(h->err, 0, sizeof(int));
     tts_bb_status s = ensure_scratch(h, std::max(nb, std::max(c.max_tokens, 1)));
     if (s != TTS_BB_OK) return bail(s);
+    // persistent decode step: barrier counter, abort flag, block partials, constant arguments
+    if (c.max_slots > 0 && c.n_layers >= 1 && c.n_layers <= mk::MAXL && c.max_ctx <= 64 * KVB && (c.n_heads == 0 || c.head_rows % 2 == 0) && c.text_vocab == 0) {
+        h->mega_grid = mega_max_grid();
+        cudaGetLastError();
+        if (h->mega_grid > 0) {
+            if ((e = dalloc(h, &h->mega_bar, 1)) != cudaSuccess || (e = dalloc(h, &h->mega_abort, 1)) != cudaSuccess ||
+                (e = dalloc(h, &h->mega_part, (size_t)mk::MAXB * NQ * h->mbps * PART_STRIDE)) != cudaSuccess)
+                return bail(TTS_BB_E_OOM);
+            cudaMemset(h->mega_bar, 0, sizeof(unsigned long long));
+            cudaMemset(h->mega_abort, 0, sizeof(int));
+            MegaArgs* ma = new MegaArgs();
+            std::memset(ma, 0, sizeof *ma);
+            for (int l = 0; l < c.n_layers; ++l) {
+                const LayerW& lw = h->L[l];
+                ma->L[l] = {lw.in_norm, lw.wqkv, lw.qn, lw.kn, lw.wo, lw.post_norm, lw.wgu, lw.wd};
+            }
+            ma->tabs = h->tabs;
+            ma->final_norm = h->final_norm;
+            ma->head_rows = c.head_rows;
+            ma->pool = h->pool;
+            ma->layer_elems = h->layer_elems;
+            ma->page_table = h->d_page_table;
+            ma->mbps = h->mbps;
+            ma->h = h->h;
+            ma->qkv = h->qkv;
+            ma->m = h->m;
+            ma->part = h->mega_part;
+            ma->nblk_max = h->mbps;
+            ma->amax = h->amax;
+            ma->bar = h->mega_bar;
+            ma->abort_flag = h->mega_abort;
+            ma->err = h->err;
+            ma->cos_t = h->cos_t;
+            ma->sin_t = h->sin_t;
+            ma->eps = c.rms_eps;
+            ma->n_layers = c.n_layers;
+            ma->ffn = c.ffn;
+            h->mega = ma;
+        }
+    }
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return bail(cuda_fail(h, e, "create"));
     *out = h;
     return TTS_BB_OK;
@@ -628,6 +689,95 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
         a.len[b] = 1;
         a.key_len[b] = nl[b];
         h->slot_len[slots[b]] = nl[b];
+    }
+    const char* path = std::getenv("TTS_BB_DECODE_PATH");
+    const bool want_head = head_idx >= 0 && (logits_out || argmax_out);
+    if (h->mega && B <= mk::MAXB && !(path && std::strcmp(path, "multi") == 0)) {
+        MegaArgs ma = *h->mega;
+        ma.ids = ids;
+        ma.embeds = reinterpret_cast<const bf16*>(embeds);
+        ma.head = want_head ? h->heads[head_idx] : nullptr;
+        ma.logits = want_head ? logits_out : nullptr;
+        ma.argmax_out = want_head ? argmax_out : nullptr;
+        ma.argmax_stride = opts && opts->argmax_stride ? opts->argmax_stride : 1;
+        ma.B = B;
+        for (int b = 0; b < B; ++b) {
+            ma.slot[b] = slots[b];
+            ma.pos[b] = kv_lens[b];
+        }
+        ma.n_upd = a.n_upd;
+        for (int i = 0; i < a.n_upd; ++i) {
+            ma.upd_idx[i] = a.upd_idx[i];
+            ma.upd_val[i] = a.upd_val[i];
+        }
+        ma.bar_base = h->bar_base;
+        ma.trace = nullptr;
+        if (h->prof_on) {
+            if (!h->mega_trace &&
+                dalloc(h, &h->mega_trace, (size_t)h->mega_grid * mk::MAXL * 16) != cudaSuccess)
+                return fail(h, TTS_BB_E_OOM, "trace buffer");
+            if (h->phase_n == 0 && h->unit_n == 0)
+                cudaMemsetAsync(h->mega_trace, 0, (size_t)h->mega_grid * mk::MAXL * 16 * 8, h->st);
+            ma.trace = h->mega_trace;
+        }
+        double kvb = 0;
+        for (int b = 0; b < B; ++b) kvb += (double)nl[b] * 2 * NKV * HD * 2 * c.n_layers;
+        const double wbytes = (double)c.n_layers * 2.0 * HID * (QKV + NQ * HD + 3.0 * c.ffn) +
+                              (ma.head ? 2.0 * c.head_rows * HID : 0);
+        {
+            Launch L(h, K_MEGA, wbytes + kvb, 2.0 * B * wbytes / 2);
+            const cudaError_t e = launch_decode_mega(ma, h->mega_grid, h->st);
+            if (e != cudaSuccess) return cuda_fail(h, e, "persistent decode step launch");
+            L += 1;
+        }
+        h->bar_base += (unsigned long long)mega_barriers(c.n_layers, ma.head != nullptr, ma.argmax_out != nullptr) *
+                       (unsigned long long)h->mega_grid;
+        if (ma.trace) {  // fold this launch's phase stamps into the profile (synchronises)
+            const int NS = 16, G = h->mega_grid, NL = c.n_layers;
+            std::vector<unsigned long long> st((size_t)G * NL * NS, 0ull);
+            cudaMemcpyAsync(st.data(), h->mega_trace, st.size() * 8, cudaMemcpyDeviceToHost, h->st);
+            cudaStreamSynchronize(h->st);
+            if (h->phase_us.empty()) { h->phase_us.assign(12, 0.0); h->phase_max_us.assign(12, 0.0); }
+            for (int l = 0; l < NL; ++l) {
+                for (int i = 0; i < 12; ++i) {
+                    if (i == 11 && l + 1 >= NL) continue;
+                    double sum = 0, mx = 0;
+                    for (int g = 0; g < G; ++g) {
+                        const unsigned long long* r = &st[((size_t)g * NL + l) * NS];
+                        const unsigned long long nxt = (i == 11) ? st[((size_t)g * NL + l + 1) * NS] : r[i + 1];
+                        const double d = (double)(nxt - r[i]) * 1e-3;
+                        sum += d;
+                        mx = d > mx ? d : mx;
+                    }
+                    h->phase_us[i] += sum / G;
+                    h->phase_max_us[i] += mx;
+                }
+                for (int g = 0; g < G; ++g) {
+                    const unsigned long long* r = &st[((size_t)g * NL + l) * NS];
+                    if (r[12] && r[13] && r[14] && r[12] >= r[2]) {
+                        h->unit_us[0] += (double)(r[12] - r[2]) * 1e-3;
+                        h->unit_us[1] += (double)(r[13] - r[12]) * 1e-3;
+                        h->unit_us[2] += (double)(r[14] - r[13]) * 1e-3;
+                        h->unit_n++;
+                    }
+                }
+            }
+            for (int l = 0; l < NL; ++l) {
+                double sum = 0, mx = 0;
+                for (int g = 0; g < G; ++g) {
+                    const double w = (double)st[((size_t)g * NL + l) * NS + 15] * 1e-3;
+                    sum += w;
+                    mx = w > mx ? w : mx;
+                }
+                h->ring_wait_us += sum / G;
+                h->ring_wait_max_us += mx;
+            }
+            h->phase_n += NL;
+            cudaMemsetAsync(h->mega_trace, 0, st.size() * 8, h->st);
+        }
+        if (opts && opts->hidden_out)
+            cudaMemcpyAsync(opts->hidden_out, h->h, (size_t)B * HID * sizeof(float), cudaMemcpyDeviceToDevice, h->st);
+        return finish(h);
     }
     launch_setup(h, a);
     {
@@ -811,6 +961,12 @@ TTS_API tts_bb_status tts_bb_profile(tts_bb* h, int on) {
         h->ev_pool.push_back(r.b);
     }
     h->prof.clear();
+    h->phase_us.clear();
+    h->phase_max_us.clear();
+    h->phase_n = 0;
+    h->unit_n = 0;
+    h->unit_us[0] = h->unit_us[1] = h->unit_us[2] = 0;
+    h->ring_wait_us = h->ring_wait_max_us = 0;
     h->prof_on = on != 0;
     return TTS_BB_OK;
 }
@@ -837,7 +993,33 @@ TTS_API const char* tts_bb_profile_report(tts_bb* h) {
         j += buf;
         first = false;
     }
-    j += "]}";
+    j += "]";
+    if (h->phase_n > 0) {
+        static const char* names[12] = {"norm_qkv", "barrier_after_qkv", "attention", "barrier_after_attention",
+                                        "merge_attention", "o_proj", "barrier_after_o", "gate_up",
+                                        "barrier_after_gate_up", "down", "barrier_after_down", "next_layer_start"};
+        j += ", \"persistent_phases_us_per_layer\": {";
+        for (int i = 0; i < 12; ++i) {
+            char buf[160];
+            snprintf(buf, sizeof buf, "%s\"%s\": {\"mean\": %.3f, \"max\": %.3f}", i ? ", " : "", names[i],
+                     h->phase_us[i] / h->phase_n, h->phase_max_us[i] / h->phase_n);
+            j += buf;
+        }
+        j += "}";
+        {
+            char buf[160];
+            snprintf(buf, sizeof buf, ", \"ring_wait_us_per_layer\": {\"mean\": %.3f, \"max\": %.3f}",
+                     h->ring_wait_us / h->phase_n, h->ring_wait_max_us / h->phase_n);
+            j += buf;
+        }
+        if (h->unit_n) {
+            char buf[200];
+            snprintf(buf, sizeof buf, ", \"attention_unit_us\": {\"stage_q_kv\": %.3f, \"scores_pv\": %.3f, \"merge\": %.3f}",
+                     h->unit_us[0] / h->unit_n, h->unit_us[1] / h->unit_n, h->unit_us[2] / h->unit_n);
+            j += buf;
+        }
+    }
+    j += "}";
     h->prof_json = j;
     return h->prof_json.c_str();
 }
