@@ -24,6 +24,8 @@ __device__ __forceinline__ void set_err(int* err, int bit) {
 
 __device__ __forceinline__ float bf2f(bf16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ bf16 f2bf(float x) { return __float2bfloat16_rn(x); }
+// Low bf16 part of a value whose high part is f2bf(x): hi + lo carries ~16 mantissa bits.
+__device__ __forceinline__ bf16 f2bf_lo(float x) { return __float2bfloat16_rn(x - __bfloat162float(__float2bfloat16_rn(x))); }
 
 // 8 bf16 packed in a uint4 -> 8 floats
 __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
@@ -79,6 +81,7 @@ struct Epi {
     int perm_rows;             // EPI_LOGITS_PERM: rows per batch (R)
     int perm_vocab;            // V
     int perm_groups;           // G
+    void* out_lo;              // EPI_SWIGLU: optional bf16 low part (value - bf16(value))
 };
 
 // ---------------------------------------------------------------- kernels
@@ -96,13 +99,17 @@ int launch_embed_omnivoice(const bf16* text, int text_vocab, const bf16* audio, 
                             const int32_t* ids, const uint8_t* mask, float* h, int B, int S, int* err,
                             cudaStream_t st);
 // y[t] = bf16(rmsnorm(h[src(t)]) * gamma); src(t) = (t / per) * stride + offset + t % per,
-// or, when last_len != nullptr, src(t) = t * stride + last_len[t] - 1.
+// or, when last_len != nullptr, src(t) = t * stride + last_len[t] - 1. y_lo (optional) gets the
+// low bf16 parts, value - bf16(value).
 int launch_rmsnorm(const float* h, const bf16* gamma, bf16* y, int T, float eps, int per, int stride,
-                    int offset, const int32_t* last_len, cudaStream_t st);
+                    int offset, const int32_t* last_len, cudaStream_t st, bf16* y_lo = nullptr);
 // Y = X W^T with epilogue; X [T][K] bf16, W [N][K] bf16. T small (<= 8).
-int launch_gemv(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st);
+// X_lo (optional): low bf16 parts of the activations; the products use X + X_lo.
+int launch_gemv(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st,
+                const bf16* X_lo = nullptr);
 // Y = X W^T with epilogue, tensor cores, any T.
-int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st);
+int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st,
+                const bf16* X_lo = nullptr);
 
 // Per-token q/k RMSNorm + RoPE; q -> qout [T][16][128] bf16; k, v -> paged pool.
 // Token t belongs to sequence t / tok_per_seq at position seq_start[seq] + t % tok_per_seq,
@@ -119,7 +126,7 @@ int launch_qk_norm_rope_append(const float* qkv, const bf16* qn, const bf16* kn,
                                 const int32_t* seq_len, int tok_per_seq, int T, int* err, cudaStream_t st);
 // Decode attention, one query per sequence: split-K flash decode + combine.
 int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B, int max_len,
-                        float* part, bf16* out, int max_splits, cudaStream_t st);
+                        float* part, bf16* out, int max_splits, cudaStream_t st, bf16* out_lo = nullptr);
 // Prefill / bidirectional attention over the paged view, tensor cores.
 // causal: query at position p sees keys <= p; else keys < key_len[seq].
 int launch_attn_prefill(const bf16* q, KVView kv, const int32_t* seq_start, const int32_t* seq_len,

@@ -106,6 +106,7 @@ struct tts_bb {
     bf16* q = nullptr;
     bf16* ao = nullptr;
     bf16* m = nullptr;
+    bf16 *y_lo = nullptr, *ao_lo = nullptr, *m_lo = nullptr;  // low bf16 parts (decode)
     float* part = nullptr;
     unsigned long long* amax = nullptr;
     int32_t *seq_slot = nullptr, *seq_start = nullptr, *seq_len = nullptr, *key_len = nullptr;
@@ -127,6 +128,7 @@ struct tts_bb {
     unsigned long long* mega_bar = nullptr;
     int* mega_abort = nullptr;
     float* mega_part = nullptr;
+    float* mega_m = nullptr;
     unsigned long long bar_base = 0;
     MegaArgs* mega = nullptr;          // per-handle constant fields filled at create
     unsigned long long* mega_trace = nullptr;   // phase stamps while profiling
@@ -263,7 +265,7 @@ tts_bb_status ensure_scratch(tts_bb* h, int T) {
     if (T <= h->T_cap) return TTS_BB_OK;
     if (h->h) {
         cudaStreamSynchronize(h->st);
-        void* olds[] = {h->h, h->y, h->qkv, h->q, h->ao, h->m};
+        void* olds[] = {h->h, h->y, h->qkv, h->q, h->ao, h->m, h->y_lo, h->ao_lo, h->m_lo};
         for (void* p : olds) {
             cudaFree(p);
             h->allocs.erase(std::remove(h->allocs.begin(), h->allocs.end(), p), h->allocs.end());
@@ -275,7 +277,10 @@ tts_bb_status ensure_scratch(tts_bb* h, int T) {
         (e = dalloc(h, &h->qkv, (size_t)T * QKV)) != cudaSuccess ||
         (e = dalloc(h, &h->q, (size_t)T * NQ * HD)) != cudaSuccess ||
         (e = dalloc(h, &h->ao, (size_t)T * NQ * HD)) != cudaSuccess ||
-        (e = dalloc(h, &h->m, (size_t)T * h->cfg.ffn)) != cudaSuccess) {
+        (e = dalloc(h, &h->m, (size_t)T * h->cfg.ffn)) != cudaSuccess ||
+        (e = dalloc(h, &h->y_lo, (size_t)T * HID)) != cudaSuccess ||
+        (e = dalloc(h, &h->ao_lo, (size_t)T * NQ * HD)) != cudaSuccess ||
+        (e = dalloc(h, &h->m_lo, (size_t)T * h->cfg.ffn)) != cudaSuccess) {
         h->T_cap = 0;
         h->h = nullptr;
         return cuda_fail(h, e, "scratch allocation");
@@ -302,44 +307,50 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         KVView kv = kv_base;
         kv.pool = kv_base.pool + (size_t)l * layer_stride;
         const int gk = T <= 8 ? K_GEMV : K_GEMM;
+        // decode carries GEMM inputs as bf16 high + low parts (weights are read
+        // once either way); prefill / bidirectional passes use plain bf16
+        const bool split = mode == 0;
+        bf16* ylo = split ? h->y_lo : nullptr;
+        bf16* aolo = split ? h->ao_lo : nullptr;
+        bf16* mlo = split ? h->m_lo : nullptr;
         const double norm_bytes = T * (4.0 + 2.0) * HID + 2.0 * HID;
-        { Launch L(h, K_RMSNORM, norm_bytes); L += launch_rmsnorm(h->h, w.in_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st); }
+        { Launch L(h, K_RMSNORM, norm_bytes); L += launch_rmsnorm(h->h, w.in_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st, ylo); }
         Epi e{};
         e.mode = EPI_STORE_F32; e.out = h->qkv; e.ldo = QKV;
-        { Launch L(h, gk, gemm_bytes(T, QKV, HID, 4), 2.0 * T * QKV * HID); L += launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st); }
+        { Launch L(h, gk, gemm_bytes(T, QKV, HID, 4), 2.0 * T * QKV * HID); L += launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st, ylo); }
         { Launch L(h, K_QKROPE, T * (4.0 * QKV + 2.0 * QKV));
           L += launch_qk_norm_rope_append(h->qkv, w.qn, w.kn, h->cos_t, h->sin_t, c.rms_eps, h->q, kv,
                                           h->seq_start, h->seq_len, tok_per_seq, T, h->err, h->st); }
         if (mode == 0) {
             Launch L(h, K_ATTN_DECODE, kv_read_bytes + T * (2.0 * NQ * HD * 2), 4.0 * NQ * HD * (kv_read_bytes / (2.0 * NKV * HD * 2)));
-            L += launch_attn_decode(h->q, kv, h->seq_start, B, max_len, h->part, h->ao, MAX_SPLITS, h->st);
+            L += launch_attn_decode(h->q, kv, h->seq_start, B, max_len, h->part, h->ao, MAX_SPLITS, h->st, aolo);
         } else {
             Launch L(h, K_ATTN_PREFILL, 0, attn_flops);
             L += launch_attn_prefill(h->q, kv, h->seq_start, h->seq_len, h->key_len, mode == 1, B, tok_per_seq, h->ao, h->st);
         }
         e = Epi{};
         e.mode = EPI_ADD_F32; e.out = h->h; e.ldo = HID;
-        { Launch L(h, gk, gemm_bytes(T, HID, NQ * HD, 8), 2.0 * T * HID * NQ * HD); L += launch_gemm(h->ao, w.wo, T, HID, NQ * HD, e, h->st); }
-        { Launch L(h, K_RMSNORM, norm_bytes); L += launch_rmsnorm(h->h, w.post_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st); }
+        { Launch L(h, gk, gemm_bytes(T, HID, NQ * HD, 8), 2.0 * T * HID * NQ * HD); L += launch_gemm(h->ao, w.wo, T, HID, NQ * HD, e, h->st, aolo); }
+        { Launch L(h, K_RMSNORM, norm_bytes); L += launch_rmsnorm(h->h, w.post_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st, ylo); }
         e = Epi{};
-        e.mode = EPI_SWIGLU; e.out = h->m; e.ldo = c.ffn;
-        { Launch L(h, gk, gemm_bytes(T, 2 * c.ffn, HID, 1), 2.0 * T * 2 * c.ffn * HID); L += launch_gemm(h->y, w.wgu, T, 2 * c.ffn, HID, e, h->st); }
+        e.mode = EPI_SWIGLU; e.out = h->m; e.ldo = c.ffn; e.out_lo = mlo;
+        { Launch L(h, gk, gemm_bytes(T, 2 * c.ffn, HID, 1), 2.0 * T * 2 * c.ffn * HID); L += launch_gemm(h->y, w.wgu, T, 2 * c.ffn, HID, e, h->st, ylo); }
         e = Epi{};
         e.mode = EPI_ADD_F32; e.out = h->h; e.ldo = HID;
-        { Launch L(h, gk, gemm_bytes(T, HID, c.ffn, 8), 2.0 * T * HID * c.ffn); L += launch_gemm(h->m, w.wd, T, HID, c.ffn, e, h->st); }
-    }
+        { Launch L(h, gk, gemm_bytes(T, HID, c.ffn, 8), 2.0 * T * HID * c.ffn); L += launch_gemm(h->m, w.wd, T, HID, c.ffn, e, h->st, mlo); }    }
 }
 
 // Final norm of B selected rows + head GEMM with logits / argmax.
 void run_head(tts_bb* h, int B, int per_seq, int head_idx, bool last_of_seq, float* logits_out, int32_t* argmax_out,
-              int argmax_stride) {
+              int argmax_stride, bool split = false) {
     const tts_bb_config& c = h->cfg;
+    bf16* ylo = split ? h->y_lo : nullptr;
     { Launch L(h, K_RMSNORM, B * 6.0 * HID + 2.0 * HID);
-      L += launch_rmsnorm(h->h, h->final_norm, h->y, B, c.rms_eps, 1, per_seq, 0, last_of_seq ? h->seq_len : nullptr, h->st); }
+      L += launch_rmsnorm(h->h, h->final_norm, h->y, B, c.rms_eps, 1, per_seq, 0, last_of_seq ? h->seq_len : nullptr, h->st, ylo); }
     Epi e{};
     e.mode = EPI_LOGITS; e.out = logits_out; e.ldo = c.head_rows; e.amax = argmax_out ? h->amax : nullptr;
     { Launch L(h, B <= 8 ? K_GEMV : K_GEMM, gemm_bytes(B, c.head_rows, HID, logits_out ? 4 : 0), 2.0 * B * c.head_rows * HID);
-      L += launch_gemm(h->y, h->heads[head_idx], B, c.head_rows, HID, e, h->st); }
+      L += launch_gemm(h->y, h->heads[head_idx], B, c.head_rows, HID, e, h->st, ylo); }
     if (argmax_out) { Launch L(h, K_ARGMAX); L += launch_argmax_finalize(h->amax, argmax_out, argmax_stride, B, h->st); }
 }
 
@@ -587,7 +598,8 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
         cudaGetLastError();
         if (h->mega_grid > 0) {
             if ((e = dalloc(h, &h->mega_bar, 1)) != cudaSuccess || (e = dalloc(h, &h->mega_abort, 1)) != cudaSuccess ||
-                (e = dalloc(h, &h->mega_part, (size_t)mk::MAXB * NQ * h->mbps * PART_STRIDE)) != cudaSuccess)
+                (e = dalloc(h, &h->mega_part, (size_t)mk::MAXB * NQ * h->mbps * PART_STRIDE)) != cudaSuccess ||
+                (e = dalloc(h, &h->mega_m, (size_t)mk::MAXB * c.ffn)) != cudaSuccess)
                 return bail(TTS_BB_E_OOM);
             cudaMemset(h->mega_bar, 0, sizeof(unsigned long long));
             cudaMemset(h->mega_abort, 0, sizeof(int));
@@ -606,7 +618,7 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
             ma->mbps = h->mbps;
             ma->h = h->h;
             ma->qkv = h->qkv;
-            ma->m = h->m;
+            ma->m = h->mega_m;
             ma->part = h->mega_part;
             ma->nblk_max = h->mbps;
             ma->amax = h->amax;
@@ -791,7 +803,8 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
     if (opts && opts->hidden_out)
         cudaMemcpyAsync(opts->hidden_out, h->h, (size_t)B * HID * sizeof(float), cudaMemcpyDeviceToDevice, h->st);
     if (head_idx >= 0 && (logits_out || argmax_out))
-        run_head(h, B, 1, head_idx, false, logits_out, argmax_out, opts && opts->argmax_stride ? opts->argmax_stride : 1);
+        run_head(h, B, 1, head_idx, false, logits_out, argmax_out, opts && opts->argmax_stride ? opts->argmax_stride : 1,
+                 true);
     return finish(h);
 }
 

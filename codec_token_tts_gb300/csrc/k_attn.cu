@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(128) k_attn_decode(const bf16* __restrict__ q,
 
 // grid B*16, 128 threads: merge the splits of one (sequence, head) in split order.
 __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ part, int n_splits,
-                                                      bf16* __restrict__ out) {
+                                                      bf16* __restrict__ out, bf16* __restrict__ out_lo) {
     const int bh = blockIdx.x, d = threadIdx.x;
     const float* p = part + (size_t)bh * n_splits * (HD + 2);
     float M = -INFINITY;
@@ -148,11 +148,13 @@ __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ 
         l += p[s * (HD + 2) + HD + 1] * f;
         o += p[s * (HD + 2) + d] * f;
     }
-    out[(size_t)bh * HD + d] = f2bf(l > 0.f ? o / l : 0.f);
+    const float r = l > 0.f ? o / l : 0.f;
+    out[(size_t)bh * HD + d] = f2bf(r);
+    if (out_lo) out_lo[(size_t)bh * HD + d] = f2bf_lo(r);
 }
 
 int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B, int max_len, float* part,
-                        bf16* out, int max_splits, cudaStream_t st) {
+                        bf16* out, int max_splits, cudaStream_t st, bf16* out_lo) {
     if (B <= 0) return 0;
     const int nblk = (max_len + KVB - 1) / KVB;
     int splits = (2 * 152 + B * NKV - 1) / (B * NKV);
@@ -160,7 +162,7 @@ int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B
     const int bps = (nblk + splits - 1) / splits;
     splits = (nblk + bps - 1) / bps;
     k_attn_decode<<<dim3(splits, NKV, B), 128, 0, st>>>(q, kv, seq_start, bps, splits, part);
-    k_attn_combine<<<B * NQ, 128, 0, st>>>(part, splits, out);
+    k_attn_combine<<<B * NQ, 128, 0, st>>>(part, splits, out, out_lo);
     return 2;
 }
 

@@ -23,7 +23,7 @@ constexpr int NT = NCT + 32;            // + one producer warp
 constexpr int RING = 176 * 1024;        // weight ring bytes
 constexpr int NSLOT = 16;               // chunks in flight at most
 constexpr int CHUNK = 32 * 1024;        // bytes per chunk (whole rows)
-constexpr int XS_BYTES = MAXB * 3072 * 2;
+constexpr int XS_BYTES = MAXB * 3072 * 4;   // fp32 activations
 constexpr int MAXSPLIT = 64;            // cache blocks per sequence (4096 tokens)
 constexpr int NSTAMP = 16;              // trace stamps per layer
 constexpr int ATT_FLOATS = (NCW * (2 * HD + 4) + 2 * HD) > (MAXB * NQ * MAXSPLIT) ? (NCW * (2 * HD + 4) + 2 * HD)
@@ -158,7 +158,7 @@ struct Ring {
 
 // ---------------------------------------------------------------- consumer pieces
 // xs[b][0..1023] = bf16(rmsnorm(src[b]) * gamma); warp b does row b.
-__device__ __forceinline__ void stage_norm(const MegaArgs& a, const float* src, const bf16* gamma, bf16* xs) {
+__device__ __forceinline__ void stage_norm(const MegaArgs& a, const float* src, const bf16* gamma, float* xs) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp < a.B) {
         const float4* row = reinterpret_cast<const float4*>(src + (size_t)warp * HID);
@@ -175,14 +175,9 @@ __device__ __forceinline__ void stage_norm(const MegaArgs& a, const float* src, 
         for (int i = 0; i < 8; ++i) {
             const int e = (i * 32 + lane) * 4;
             const uint2 gr = *reinterpret_cast<const uint2*>(gamma + e);
-            __nv_bfloat162 p0 = __floats2bfloat162_rn(v[i].x * r * __uint_as_float(gr.x << 16),
-                                                      v[i].y * r * __uint_as_float(gr.x & 0xFFFF0000u));
-            __nv_bfloat162 p1 = __floats2bfloat162_rn(v[i].z * r * __uint_as_float(gr.y << 16),
-                                                      v[i].w * r * __uint_as_float(gr.y & 0xFFFF0000u));
-            uint2 o;
-            o.x = *reinterpret_cast<uint32_t*>(&p0);
-            o.y = *reinterpret_cast<uint32_t*>(&p1);
-            *reinterpret_cast<uint2*>(xs + (size_t)warp * HID + e) = o;
+            *reinterpret_cast<float4*>(xs + (size_t)warp * HID + e) =
+                make_float4(v[i].x * r * __uint_as_float(gr.x << 16), v[i].y * r * __uint_as_float(gr.x & 0xFFFF0000u),
+                            v[i].z * r * __uint_as_float(gr.y << 16), v[i].w * r * __uint_as_float(gr.y & 0xFFFF0000u));
         }
     }
 }
@@ -230,7 +225,7 @@ __device__ __forceinline__ void stage_embed(const MegaArgs& a, float* hs) {
 // Warp w takes rows 2w and 2w+1 of each chunk (a gate/up pair for SwiGLU).
 template <int B>
 __device__ __forceinline__ void consume_op(const MegaArgs& a, int l, int o, Ring& ring, unsigned char* ring_mem,
-                                           uint64_t* full, uint64_t* empty, const bf16* xs) {
+                                           uint64_t* full, uint64_t* empty, const float* xs) {
     const OpDesc d = op_desc(a, l, o);
     int r0, r1;
     cta_rows(d.N, blockIdx.x, gridDim.x, r0, r1);
@@ -263,7 +258,12 @@ __device__ __forceinline__ void consume_op(const MegaArgs& a, int l, int o, Ring
                 const int col = (i * 32 + lane) * 8;
                 float xf[B][8];
 #pragma unroll
-                for (int b = 0; b < B; ++b) unpack8(*reinterpret_cast<const uint4*>(xs + b * d.K + col), xf[b]);
+                for (int b = 0; b < B; ++b) {
+                    const float4 x0 = *reinterpret_cast<const float4*>(xs + b * d.K + col);
+                    const float4 x1 = *reinterpret_cast<const float4*>(xs + b * d.K + col + 4);
+                    xf[b][0] = x0.x; xf[b][1] = x0.y; xf[b][2] = x0.z; xf[b][3] = x0.w;
+                    xf[b][4] = x1.x; xf[b][5] = x1.y; xf[b][6] = x1.z; xf[b][7] = x1.w;
+                }
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
                     if (lr0 + rr >= nr) break;
@@ -306,7 +306,7 @@ __device__ __forceinline__ void consume_op(const MegaArgs& a, int l, int o, Ring
                         if (lr0 + 1 < nr) a.qkv[(size_t)b * QKV + row + 1] = acc[1][b];
                     } else if (o == 2) {
                         const float g = acc[0][b], u = acc[1][b];
-                        a.m[(size_t)b * a.ffn + row / 2] = f2bf(g / (1.f + __expf(-g)) * u);
+                        a.m[(size_t)b * a.ffn + row / 2] = g / (1.f + __expf(-g)) * u;
                     } else {  // o_proj / down: residual add (each row has one owner)
                         float* hr = a.h + (size_t)b * HID + row;
                         hr[0] = __ldcg(hr) + acc[0][b];
@@ -467,7 +467,7 @@ __device__ __forceinline__ void attn_unit(const MegaArgs& a, int l, int b, int g
 // First the per-block weights w_j = 2^(m_j - M) / sum_j l_j 2^(m_j - M) go to
 // shared memory (one thread per (b, h)); then every thread combines float4
 // slices with all block loads issued before any is used.
-__device__ __forceinline__ void stage_attn_out(const MegaArgs& a, bf16* xs, float* wsm) {
+__device__ __forceinline__ void stage_attn_out(const MegaArgs& a, float* xs, float* wsm) {
     const int nb_max = a.nblk_max;
     for (int t = threadIdx.x; t < a.B * NQ; t += mk::NCT) {
         const int b = t / NQ, h = t % NQ;
@@ -505,11 +505,7 @@ __device__ __forceinline__ void stage_attn_out(const MegaArgs& a, bf16* xs, floa
                     acc.x += w * v[jj].x; acc.y += w * v[jj].y; acc.z += w * v[jj].z; acc.w += w * v[jj].w;
                 }
         }
-        __nv_bfloat162 p0 = __floats2bfloat162_rn(acc.x, acc.y), p1 = __floats2bfloat162_rn(acc.z, acc.w);
-        uint2 o;
-        o.x = *reinterpret_cast<uint32_t*>(&p0);
-        o.y = *reinterpret_cast<uint32_t*>(&p1);
-        *reinterpret_cast<uint2*>(xs + (size_t)bh * HD + e4 * 4) = o;
+        *reinterpret_cast<float4*>(xs + (size_t)bh * HD + e4 * 4) = acc;
     }
 }
 
@@ -518,7 +514,7 @@ template <int B>
 __global__ void __launch_bounds__(mk::NT, 1) k_decode_mega(const __grid_constant__ MegaArgs a) {
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* ring_mem = smem;
-    bf16* xs = reinterpret_cast<bf16*>(smem + mk::RING);
+    float* xs = reinterpret_cast<float*>(smem + mk::RING);
     float* att = reinterpret_cast<float*>(smem + mk::RING + mk::XS_BYTES);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + mk::RING + mk::XS_BYTES + mk::ATT_FLOATS * 4);
     uint64_t* empty = full + mk::NSLOT;
@@ -603,7 +599,7 @@ __global__ void __launch_bounds__(mk::NT, 1) k_decode_mega(const __grid_constant
         // ---- QKV
         if (l == 0) {
             // embedding sum -> global h (CTA 0) and every CTA's normed input
-            float* hrow = reinterpret_cast<float*>(xs + B * 1024);  // scratch after the bf16 input rows
+            float* hrow = xs + B * 1024;  // scratch after the input rows
             stage_embed(a, hrow);
             named_sync();
             // norm from the smem copy
@@ -613,7 +609,7 @@ __global__ void __launch_bounds__(mk::NT, 1) k_decode_mega(const __grid_constant
                 ss = warp_sum(ss);
                 const float r = rsqrtf(ss * (1.f / HID) + a.eps);
                 for (int c = lane; c < HID; c += 32)
-                    xs[warp * HID + c] = f2bf(hrow[warp * HID + c] * r * bf2f(a.L[0].in_norm[c]));
+                    xs[warp * HID + c] = hrow[warp * HID + c] * r * bf2f(a.L[0].in_norm[c]);
             }
         } else {
             stage_norm(a, a.h, a.L[l].in_norm, xs);
@@ -652,8 +648,8 @@ __global__ void __launch_bounds__(mk::NT, 1) k_decode_mega(const __grid_constant
         grid_sync(a, bk);
         STAMP(9);
         // ---- down + residual
-        for (int t = threadIdx.x; t < B * a.ffn / 8; t += mk::NCT)
-            reinterpret_cast<uint4*>(xs)[t] = __ldcg(reinterpret_cast<const uint4*>(a.m) + t);
+        for (int t = threadIdx.x; t < B * a.ffn / 4; t += mk::NCT)
+            reinterpret_cast<float4*>(xs)[t] = __ldcg(reinterpret_cast<const float4*>(a.m) + t);
         named_sync();
         consume_op<B>(a, l, 3, ring, ring_mem, full, empty, xs);
         STAMP(10);
@@ -704,8 +700,6 @@ cudaError_t launch_decode_mega(const MegaArgs& a, int grid, cudaStream_t st) {
     switch (a.B) {
         case 1: return launch_b<1>(a, grid, st);
         case 2: return launch_b<2>(a, grid, st);
-        case 3: return launch_b<3>(a, grid, st);
-        case 4: return launch_b<4>(a, grid, st);
         default: return cudaErrorInvalidValue;
     }
 }

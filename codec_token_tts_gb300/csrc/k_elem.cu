@@ -99,7 +99,8 @@ int launch_embed_omnivoice(const bf16* text, int text_vocab, const bf16* audio, 
 // y = h * rsqrt(mean(h^2) + eps) * gamma; fp32 residual in, bf16 out. One warp per row.
 __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ h, const bf16* __restrict__ gamma,
                                                  bf16* __restrict__ y, int T, float eps, int per, int stride,
-                                                 int offset, const int32_t* __restrict__ last_len) {
+                                                 int offset, const int32_t* __restrict__ last_len,
+                                                 bf16* __restrict__ y_lo) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= T) return;
@@ -122,19 +123,27 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ h, co
         const uint2 gr = *reinterpret_cast<const uint2*>(gamma + e);
         const float g0 = __uint_as_float(gr.x << 16), g1 = __uint_as_float(gr.x & 0xFFFF0000u);
         const float g2 = __uint_as_float(gr.y << 16), g3 = __uint_as_float(gr.y & 0xFFFF0000u);
-        __nv_bfloat162 a = __floats2bfloat162_rn(v[i].x * r * g0, v[i].y * r * g1);
-        __nv_bfloat162 b = __floats2bfloat162_rn(v[i].z * r * g2, v[i].w * r * g3);
+        const float f0 = v[i].x * r * g0, f1 = v[i].y * r * g1, f2 = v[i].z * r * g2, f3 = v[i].w * r * g3;
+        __nv_bfloat162 a = __floats2bfloat162_rn(f0, f1);
+        __nv_bfloat162 b = __floats2bfloat162_rn(f2, f3);
         uint2 o;
         o.x = *reinterpret_cast<uint32_t*>(&a);
         o.y = *reinterpret_cast<uint32_t*>(&b);
         *reinterpret_cast<uint2*>(y + (size_t)t * HID + e) = o;
+        if (y_lo) {
+            __nv_bfloat162 al = __halves2bfloat162(f2bf_lo(f0), f2bf_lo(f1));
+            __nv_bfloat162 bl = __halves2bfloat162(f2bf_lo(f2), f2bf_lo(f3));
+            o.x = *reinterpret_cast<uint32_t*>(&al);
+            o.y = *reinterpret_cast<uint32_t*>(&bl);
+            *reinterpret_cast<uint2*>(y_lo + (size_t)t * HID + e) = o;
+        }
     }
 }
 
 int launch_rmsnorm(const float* h, const bf16* gamma, bf16* y, int T, float eps, int per, int stride, int offset,
-                    const int32_t* last_len, cudaStream_t st) {
+                    const int32_t* last_len, cudaStream_t st, bf16* y_lo) {
     if (T <= 0) return 0;
-    k_rmsnorm<<<(T + 7) / 8, 256, 0, st>>>(h, gamma, y, T, eps, per, stride, offset, last_len);
+    k_rmsnorm<<<(T + 7) / 8, 256, 0, st>>>(h, gamma, y, T, eps, per, stride, offset, last_len, y_lo);
     return 1;
 }
 

@@ -52,15 +52,18 @@ __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsig
 // streams 16-byte chunks l, l+32, ... of each weight row; X sits in shared
 // memory. ROWS = 2 keeps a gate/up pair in one warp for the SwiGLU epilogue.
 template <int T, int ROWS>
-__global__ void __launch_bounds__(256) k_gemv(const bf16* __restrict__ X, const bf16* __restrict__ W, int N, int K,
-                                              Epi e) {
+__global__ void __launch_bounds__(256) k_gemv(const bf16* __restrict__ X, const bf16* __restrict__ X_lo,
+                                              const bf16* __restrict__ W, int N, int K, Epi e) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     bf16* xs = reinterpret_cast<bf16*>(smem_raw);
+    bf16* xl = xs + (size_t)T * K;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // stage X [T][K]
+    // stage X [T][K] (and its low parts)
     const int nchunk = T * K / 8;
-    for (int i = tid; i < nchunk; i += 256)
+    for (int i = tid; i < nchunk; i += 256) {
         reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(X)[i];
+        if (X_lo) reinterpret_cast<uint4*>(xl)[i] = reinterpret_cast<const uint4*>(X_lo)[i];
+    }
     __syncthreads();
 
     const int row0 = (blockIdx.x * 8 + warp) * ROWS;
@@ -93,6 +96,12 @@ __global__ void __launch_bounds__(256) k_gemv(const bf16* __restrict__ X, const 
             for (int t = 0; t < T; ++t) {
                 float xf[8];
                 unpack8(reinterpret_cast<const uint4*>(xs + (size_t)t * K + c * 256)[lane], xf);
+                if (X_lo) {
+                    float lf[8];
+                    unpack8(reinterpret_cast<const uint4*>(xl + (size_t)t * K + c * 256)[lane], lf);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) xf[j] += lf[j];
+                }
 #pragma unroll
                 for (int r = 0; r < ROWS; ++r) {
                     float wf[8];
@@ -119,7 +128,9 @@ __global__ void __launch_bounds__(256) k_gemv(const bf16* __restrict__ X, const 
 #pragma unroll
                     for (int r = 0; r + 1 < ROWS; r += 2) {
                         const float g = acc[r][t], u = acc[r + 1][t];
-                        reinterpret_cast<bf16*>(e.out)[(size_t)t * e.ldo + (row0 + r) / 2] = f2bf(silu(g) * u);
+                        const float mv = silu(g) * u;
+                        reinterpret_cast<bf16*>(e.out)[(size_t)t * e.ldo + (row0 + r) / 2] = f2bf(mv);
+                        if (e.out_lo) reinterpret_cast<bf16*>(e.out_lo)[(size_t)t * e.ldo + (row0 + r) / 2] = f2bf_lo(mv);
                     }
                 }
         }
@@ -142,27 +153,27 @@ __global__ void __launch_bounds__(256) k_gemv(const bf16* __restrict__ X, const 
 }
 
 template <int T>
-static void gemv_t(const bf16* X, const bf16* W, int N, int K, const Epi& e, cudaStream_t st) {
-    const size_t smem = (size_t)T * K * sizeof(bf16);
+static void gemv_t(const bf16* X, const bf16* X_lo, const bf16* W, int N, int K, const Epi& e, cudaStream_t st) {
+    const size_t smem = (size_t)(X_lo ? 2 : 1) * T * K * sizeof(bf16);
     static bool attr_set = false;
     if (!attr_set) {
-        cudaFuncSetAttribute(k_gemv<T, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 8 * 3072 * 2);
+        cudaFuncSetAttribute(k_gemv<T, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 8 * 3072 * 2);
         attr_set = true;
     }
     const int rows_per_cta = 16;
-    k_gemv<T, 2><<<(N + rows_per_cta - 1) / rows_per_cta, 256, smem, st>>>(X, W, N, K, e);
+    k_gemv<T, 2><<<(N + rows_per_cta - 1) / rows_per_cta, 256, smem, st>>>(X, X_lo, W, N, K, e);
 }
 
-int launch_gemv(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st) {
+int launch_gemv(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st, const bf16* X_lo) {
     switch (T) {
-        case 1: gemv_t<1>(X, W, N, K, e, st); break;
-        case 2: gemv_t<2>(X, W, N, K, e, st); break;
-        case 3: gemv_t<3>(X, W, N, K, e, st); break;
-        case 4: gemv_t<4>(X, W, N, K, e, st); break;
-        case 5: gemv_t<5>(X, W, N, K, e, st); break;
-        case 6: gemv_t<6>(X, W, N, K, e, st); break;
-        case 7: gemv_t<7>(X, W, N, K, e, st); break;
-        case 8: gemv_t<8>(X, W, N, K, e, st); break;
+        case 1: gemv_t<1>(X, X_lo, W, N, K, e, st); break;
+        case 2: gemv_t<2>(X, X_lo, W, N, K, e, st); break;
+        case 3: gemv_t<3>(X, X_lo, W, N, K, e, st); break;
+        case 4: gemv_t<4>(X, X_lo, W, N, K, e, st); break;
+        case 5: gemv_t<5>(X, X_lo, W, N, K, e, st); break;
+        case 6: gemv_t<6>(X, X_lo, W, N, K, e, st); break;
+        case 7: gemv_t<7>(X, X_lo, W, N, K, e, st); break;
+        case 8: gemv_t<8>(X, X_lo, W, N, K, e, st); break;
         default: return 0;
     }
     return 1;
@@ -176,6 +187,7 @@ namespace gm {
 constexpr int BM = 128, BN = 128, BK = 32, LDS = BK + 8, STAGES = 4;
 constexpr int TILE_A = BM * LDS, TILE_B = BN * LDS;
 constexpr int SMEM = STAGES * (TILE_A + TILE_B) * 2;
+constexpr int SMEM_SPLIT = STAGES * (2 * TILE_A + TILE_B) * 2;
 }  // namespace gm
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool pred) {
@@ -200,12 +212,17 @@ __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, const uint
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-__global__ void __launch_bounds__(256) k_gemm_mma(const bf16* __restrict__ X, const bf16* __restrict__ W, int T, int N,
-                                                  int K, Epi e) {
+// SPLIT: the activations come as bf16 high + low parts; a second MMA per
+// k-step adds the low part (weights are read once, so this is free when the
+// GEMM streams weights at small T).
+template <bool SPLIT>
+__global__ void __launch_bounds__(256) k_gemm_mma(const bf16* __restrict__ X, const bf16* __restrict__ X_lo,
+                                                  const bf16* __restrict__ W, int T, int N, int K, Epi e) {
     using namespace gm;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     bf16* sA = reinterpret_cast<bf16*>(smem_raw);
     bf16* sB = sA + STAGES * TILE_A;
+    bf16* sL = sB + STAGES * TILE_B;  // low parts (SPLIT only)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wm = warp >> 1, wn = warp & 1;
     const int n0 = blockIdx.x * BN, t0 = blockIdx.y * BM;
@@ -220,6 +237,8 @@ __global__ void __launch_bounds__(256) k_gemm_mma(const bf16* __restrict__ X, co
             const int tr = t0 + r, nr = n0 + r;
             cp_async16(sA + stage * TILE_A + r * LDS + col, X + (size_t)min(tr, T - 1) * K + k0 + col, tr < T);
             cp_async16(sB + stage * TILE_B + r * LDS + col, W + (size_t)min(nr, N - 1) * K + k0 + col, nr < N);
+            if (SPLIT)
+                cp_async16(sL + stage * TILE_A + r * LDS + col, X_lo + (size_t)min(tr, T - 1) * K + k0 + col, tr < T);
         }
     };
 
@@ -264,6 +283,21 @@ __global__ void __launch_bounds__(256) k_gemm_mma(const bf16* __restrict__ X, co
                     mma16816(acc[i][2 * j], af[i], &bfr[j][0]);
                     mma16816(acc[i][2 * j + 1], af[i], &bfr[j][2]);
                 }
+            if (SPLIT) {
+                const bf16* l_s = sL + (kt % STAGES) * TILE_A;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int r = wm * 32 + i * 16 + (lane & 15);
+                    ldmatrix_x4(af[i], l_s + r * LDS + kk + (lane >> 4) * 8);
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        mma16816(acc[i][2 * j], af[i], &bfr[j][0]);
+                        mma16816(acc[i][2 * j + 1], af[i], &bfr[j][2]);
+                    }
+            }
         }
     }
     cp_async_wait<0>();
@@ -281,7 +315,9 @@ __global__ void __launch_bounds__(256) k_gemm_mma(const bf16* __restrict__ X, co
                 const float v0 = acc[i][j][hr * 2], v1 = acc[i][j][hr * 2 + 1];
                 if (t < T && n < N) {
                     if (e.mode == EPI_SWIGLU) {
-                        reinterpret_cast<bf16*>(e.out)[(size_t)t * e.ldo + n / 2] = f2bf(silu(v0) * v1);
+                        const float mv = silu(v0) * v1;
+                        reinterpret_cast<bf16*>(e.out)[(size_t)t * e.ldo + n / 2] = f2bf(mv);
+                        if (e.out_lo) reinterpret_cast<bf16*>(e.out_lo)[(size_t)t * e.ldo + n / 2] = f2bf_lo(mv);
                     } else {
                         epi_one(e, t, n, v0);
                         if (n + 1 < N) epi_one(e, t, n + 1, v1);
@@ -300,16 +336,20 @@ __global__ void __launch_bounds__(256) k_gemm_mma(const bf16* __restrict__ X, co
         }
 }
 
-int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st) {
+int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st, const bf16* X_lo) {
     if (T <= 0) return 0;
-    if (T <= 8) return launch_gemv(X, W, T, N, K, e, st);
+    if (T <= 8) return launch_gemv(X, W, T, N, K, e, st, X_lo);
     static bool attr_set = false;
     if (!attr_set) {
-        cudaFuncSetAttribute(k_gemm_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, gm::SMEM);
+        cudaFuncSetAttribute(k_gemm_mma<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, gm::SMEM);
+        cudaFuncSetAttribute(k_gemm_mma<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, gm::SMEM_SPLIT);
         attr_set = true;
     }
     dim3 grid((N + gm::BN - 1) / gm::BN, (T + gm::BM - 1) / gm::BM);
-    k_gemm_mma<<<grid, 256, gm::SMEM, st>>>(X, W, T, N, K, e);
+    if (X_lo)
+        k_gemm_mma<true><<<grid, 256, gm::SMEM_SPLIT, st>>>(X, X_lo, W, T, N, K, e);
+    else
+        k_gemm_mma<false><<<grid, 256, gm::SMEM, st>>>(X, nullptr, W, T, N, K, e);
     return 1;
 }
 

@@ -5,7 +5,7 @@
 namespace ttsbb {
 
 namespace mk {
-constexpr int MAXB = 4;    // largest batch the persistent step runs
+constexpr int MAXB = 2;    // largest batch the persistent step runs (fp32 activations in shared memory)
 constexpr int MAXL = 32;   // layers
 }  // namespace mk
 
@@ -40,7 +40,7 @@ struct MegaArgs {
     int upd_val[mk::MAXB];
     float* h;                  // [B][HID] residual (fp32)
     float* qkv;                // [B][QKV]
-    bf16* m;                   // [B][ffn]
+    float* m;                  // [B][ffn] SwiGLU output (fp32)
     float* part;               // [B][16][nblk_max][PART_STRIDE]
     int nblk_max;
     unsigned long long* amax;  // [B]

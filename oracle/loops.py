@@ -22,7 +22,7 @@ import numpy as np
 
 from .backbone import Backbone, KVCache, argmax_first, codebook_embed_sum, omnivoice_embed
 
-__all__ = ["talker_prefill", "talker_decode_steps", "code_predictor_frame",
+__all__ = ["talker_prefill", "talker_decode_steps", "code_predictor_frame", "code_predictor_frames",
            "maskgit_pass", "one_layer_run", "cp_position_ids"]
 
 
@@ -98,6 +98,34 @@ def code_predictor_frame(m: Backbone, talker_hidden: np.ndarray, code0: int,
         lg = m.head_logits(h, j)[0]
         codes.append(int(argmax_first(lg))); logits.append(lg); hidden.append(h[0])
     return np.array(codes, np.int32), np.array(logits), np.array(hidden)
+
+
+def code_predictor_frames(m: Backbone, talker_hidden: np.ndarray, code0: np.ndarray,
+                          forced: Optional[np.ndarray] = None):
+    """code_predictor_frame for F independent frames at once (same steps; the
+    row-wise projections of the frames share one matrix product).
+    talker_hidden[F, H], code0[F], forced[F, 15] or None.
+    Returns (codes[F, 15], logits[F, 15, rows])."""
+    F = len(code0)
+    n_cb = len(m.codebooks)
+    caches = [m.new_cache() for _ in range(F)]
+    xs = []
+    for f in range(F):
+        x1 = codebook_embed_sum(cp_position_ids(n_cb, 0, int(code0[f]))[None, :], m.codebooks)
+        xs.append(np.concatenate([np.asarray(talker_hidden[f], np.float64)[None, :], x1]))
+    hs = m.forward_cached_multi(xs, caches)
+    last = np.stack([h[-1] for h in hs])
+    lg = m.head_logits(last, 0)
+    codes = [argmax_first(lg)]
+    logits = [lg]
+    for j in range(1, 15):
+        prev = forced[:, j - 1] if forced is not None else codes[-1]
+        xs = [codebook_embed_sum(cp_position_ids(n_cb, j, int(prev[f]))[None, :], m.codebooks) for f in range(F)]
+        hs = m.forward_cached_multi(xs, caches)
+        lg = m.head_logits(np.concatenate(hs), j)
+        codes.append(argmax_first(lg))
+        logits.append(lg)
+    return np.stack(codes, axis=1).astype(np.int32), np.stack(logits, axis=1)
 
 
 def maskgit_pass(m: Backbone, ids: np.ndarray, audio_mask: np.ndarray, audio_start: int,

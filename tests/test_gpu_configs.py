@@ -1,0 +1,205 @@
+"""GPU parity at the full sizes of the five workloads, in the launch
+configuration the benchmark times, against the fp64 oracle.
+
+Where the fp64 oracle cannot run the whole workload in seconds, it runs a
+stated sample: every test names it. Teacher forcing: the GPU is fed the
+oracle's own greedy ids, so every compared step sees identical inputs.
+"""
+import concurrent.futures as cf
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+from tests.gpu_util import (HIDDEN_TOL, LOGIT_TOL, Engine, check_logits_and_argmax, dev_bf16_bits, dev_i32,
+                            dev_u8, f32_zeros, i32_full, rel_err_rows)
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+def report(name, **kw):
+    print(f"[{name}] " + " ".join(f"{k}={v}" for k, v in kw.items()))
+
+
+# ---------------------------------------------------------------- one layer, 64 + 16 (seed 0)
+# (covered at full size by tests/test_gpu_small.py::test_one_layer_prefill_then_decode)
+
+
+# ---------------------------------------------------------------- Talker batch 1: 128 prefill + 256 decode (seed 1)
+def test_talker_batch1_full():
+    """Whole workload: 28 layers, 128-position prefill, 256 decode steps, every step compared."""
+    seed = 1
+    w = synth.model_weights(synth.TALKER, seed)
+    m0 = O.Backbone(w, synth.TALKER)
+    ids = synth.talker_prefill_ids(seed, 128)
+    rest = synth.uniform_ids(synth.rng_for(seed, "decode_rest"), synth.TALKER.codebook_rows[1:], 256)
+    cache = m0.new_cache()
+    hp, lg0, a0 = O.talker_prefill(m0, ids, cache)
+    hid_o, lg_o, am_o, fed = O.talker_decode_steps(m0, cache, a0, rest)
+    with Engine(w, max_slots=1, max_ctx=384, max_batch=1, max_tokens=128) as e:
+        m = e.m
+        logits = f32_zeros(1, 3072)
+        am = i32_full(1)
+        hid = f32_zeros(128, 1024)
+        m.tts_bb_prefill(e.h, 1, 128, [0], [128], dev_i32(ids.reshape(1, 128, 16)), 0, logits, am, hidden_out=hid)
+        assert rel_err_rows(hid.cpu().numpy(), hp) <= HIDDEN_TOL
+        check_logits_and_argmax(logits.cpu().numpy(), lg0[None], am.cpu().numpy(), [a0], min_agree=0.0)
+        fed_d = dev_i32(fed)
+        L = torch.zeros(256, 3072, dtype=torch.float32, device="cuda")
+        A = torch.zeros(256, dtype=torch.int32, device="cuda")
+        H = torch.zeros(256, 1024, dtype=torch.float32, device="cuda")
+        for t in range(256):                 # teacher forced: the oracle's id rows
+            m.tts_bb_decode_step(e.h, 1, [0], [128 + t], fed_d[t:t + 1], 0, L[t:t + 1], A[t:t + 1],
+                                 hidden_out=H[t:t + 1])
+        herr = rel_err_rows(H.cpu().numpy(), hid_o)
+        err, agree, agree_u = check_logits_and_argmax(L.cpu().numpy(), lg_o, A.cpu().numpy(), am_o)
+        assert herr <= HIDDEN_TOL
+        report("talker_b1", hidden_rel=f"{herr:.2e}", logit_abs=f"{err:.2e}", argmax_raw=agree,
+               argmax_unique=agree_u)
+        # free-running on the device: argmax written straight into the next id row
+        m.tts_bb_truncate(e.h, 0, 128)
+        ids_d = dev_i32(np.concatenate([np.zeros((257, 1), np.int32), np.vstack([rest, rest[:1]])], axis=1))
+        ids_d[0, 0] = a0
+        for t in range(256):
+            m.tts_bb_decode_step(e.h, 1, [0], [128 + t], ids_d[t:t + 1], 0, None, ids_d[t + 1, 0:1])
+        free = ids_d[1:, 0].cpu().numpy()
+        div = np.nonzero(free != am_o)[0]
+        report("talker_b1_free_running", first_divergence=int(div[0]) if len(div) else None)
+
+
+# ---------------------------------------------------------------- serving: 64 streams, ragged KV (seed 2)
+def _kv_for(seed, b, layer, n):
+    k = synth.kv_values(seed, f"serve_k{b}.{layer}", n)
+    v = synth.kv_values(seed, f"serve_v{b}.{layer}", n)
+    return k, v
+
+
+def test_serving_batch64_full():
+    """64 streams with cached lengths U[200, 2000] (synthetic K/V written through the page table),
+    8 decode steps for all 64 streams; the oracle follows 8 streams (shortest, longest, 6 more)."""
+    seed, B, steps = 2, 64, 8
+    w = synth.model_weights(synth.TALKER, seed)
+    L0 = synth.ragged_lengths(seed, B, 200, 2000)
+    order = np.argsort(L0)
+    sample = sorted({int(order[0]), int(order[-1])} | set(int(x) for x in order[np.linspace(1, B - 2, 6).astype(int)]))
+    slots = synth.block_permutation(seed, B)          # stream b lives in slot slots[b]
+    m0 = O.Backbone(w, synth.TALKER)
+    caches = {b: m0.new_cache() for b in sample}
+    with Engine(w, max_slots=B, max_ctx=2000 + steps, max_batch=B, max_tokens=B) as e:
+        m = e.m
+        # cached K/V, written layer by layer in interleaved stream order (scattered blocks)
+        with cf.ThreadPoolExecutor(8) as ex:
+            for layer in range(28):
+                kvs = list(ex.map(lambda b: _kv_for(seed, b, layer, int(L0[b])), range(B)))
+                for b in range(B):
+                    k, v = kvs[b]
+                    m.tts_bb_debug_kv_write(e.h, layer, int(slots[b]), 0, int(L0[b]), dev_bf16_bits(k),
+                                            dev_bf16_bits(v))
+                    if b in caches:
+                        caches[b].k[layer] = O.bf16_to_f64(k)
+                        caches[b].v[layer] = O.bf16_to_f64(v)
+        r = synth.rng_for(seed, "serve_ids")
+        ids = synth.uniform_ids(r, synth.TALKER.codebook_rows, steps * B).reshape(steps, B, 16)
+        kv = L0.copy()
+        worst_h, worst_l, agrees = 0.0, 0.0, []
+        for t in range(steps):
+            xs = [O.codebook_embed_sum(ids[t, b:b + 1], m0.codebooks) for b in sample]
+            hs = m0.forward_cached_multi(xs, [caches[b] for b in sample])
+            ho = np.concatenate(hs)
+            lo = m0.head_logits(ho, 0)
+            ao = O.argmax_first(lo)
+            logits = f32_zeros(B, 3072)
+            am = i32_full(B)
+            hid = f32_zeros(B, 1024)
+            m.tts_bb_decode_step(e.h, B, slots, kv, dev_i32(ids[t]), 0, logits, am, hidden_out=hid)
+            g = hid.cpu().numpy()[sample]
+            worst_h = max(worst_h, rel_err_rows(g, ho))
+            err, agree, _ = check_logits_and_argmax(logits.cpu().numpy()[sample], lo, am.cpu().numpy()[sample], ao,
+                                                    min_agree=0.0)
+            worst_l = max(worst_l, err)
+            agrees.append(agree)
+            if t + 1 < steps:                 # teacher forcing for the followed streams
+                for i, b in enumerate(sample):
+                    ids[t + 1, b, 0] = ao[i]
+            kv = kv + 1
+        assert worst_h <= HIDDEN_TOL
+        report("serving_b64", sample=sample, hidden_rel=f"{worst_h:.2e}", logit_abs=f"{worst_l:.2e}",
+               argmax_raw=float(np.mean(agrees)))
+        # paging: the appended tokens sit behind the synthetic prefix, which is unchanged
+        b = sample[0]
+        n = int(L0[b]) + steps
+        kk = torch.zeros(n, 8, 128, dtype=torch.bfloat16, device="cuda")
+        vv = torch.zeros_like(kk)
+        m.tts_bb_debug_kv_read(e.h, 5, int(slots[b]), 0, n, kk, vv)
+        k5, _ = _kv_for(seed, b, 5, int(L0[b]))
+        from tests.gpu_util import bf16_tensor_bits
+        assert np.array_equal(bf16_tensor_bits(kk)[:int(L0[b])], k5)
+        assert rel_err_rows(kk.float().cpu().numpy()[int(L0[b]):].reshape(steps, -1),
+                            caches[b].k[5][int(L0[b]):].reshape(steps, -1)) <= HIDDEN_TOL
+
+
+# ---------------------------------------------------------------- Code Predictor: 256 frames x 15 steps (seed 3)
+def test_code_predictor_256_frames_full():
+    """256 frames run on the GPU (2-token prefill + 14 decode calls, heads 0..14); the oracle follows 16 frames."""
+    seed, F = 3, 256
+    w = synth.model_weights(synth.CODE_PREDICTOR, seed)
+    m0 = O.Backbone(w, synth.CODE_PREDICTOR)
+    r = synth.rng_for(seed, "cp_inputs")
+    th = synth.normal_bf16(r, (F, 1024), 1.0)
+    code0 = r.integers(0, 3072, size=F).astype(np.int32)
+    sample = list(range(0, F, 16))
+    codes_o, logits_o = O.code_predictor_frames(m0, O.bf16_to_f64(th[sample]), code0[sample])
+    with Engine(w, max_slots=F, max_ctx=17, max_batch=F, max_tokens=2 * F) as e:
+        m = e.m
+        emb = np.zeros((F, 2, 1024), np.uint16)
+        emb[:, 0] = th
+        ids = -np.ones((F, 2, 16), np.int32)
+        ids[:, 1, 0] = code0
+        codes = i32_full(F * 16).view(F, 16)
+        logits = f32_zeros(F, 2048)
+        slots = list(range(F))
+        m.tts_bb_prefill(e.h, F, 2, slots, [2] * F, dev_i32(ids), 0, logits, codes[:, 1],
+                         embeds=dev_bf16_bits(emb), argmax_stride=16)
+        gl = [logits.cpu().numpy()[sample]]
+        forced = np.zeros((F, 15), np.int32)
+        forced[sample] = codes_o
+        for j in range(1, 15):
+            step = -np.ones((F, 16), np.int32)
+            prev = codes[:, j].cpu().numpy()
+            prev[sample] = codes_o[:, j - 1]                 # teacher forcing on the followed frames
+            step[:, j] = prev
+            m.tts_bb_decode_step(e.h, F, slots, [j + 1] * F, dev_i32(step), j, logits, codes[:, j + 1],
+                                 argmax_stride=16)
+            gl.append(logits.cpu().numpy()[sample])
+        gl = np.stack(gl, axis=1)                             # [16, 15, 2048]
+        got = codes.cpu().numpy()[sample][:, 1:16]
+        err, agree, agree_u = check_logits_and_argmax(gl.reshape(-1, 2048), logits_o.reshape(-1, 2048),
+                                                      got.reshape(-1), codes_o.reshape(-1))
+        report("code_predictor", frames=F, followed=len(sample), logit_abs=f"{err:.2e}", argmax_raw=agree,
+               argmax_unique=agree_u)
+
+
+# ---------------------------------------------------------------- MaskGIT: B=8, S=1024 (seed 4)
+@pytest.mark.parametrize("step", [0, 31])
+def test_maskgit_pass_full(step):
+    """One bidirectional pass of the 28-layer OmniVoice LM over B=8 x 1024 (256 text + 768 audio);
+    the oracle computes rows 0 and 7 completely (rows are independent)."""
+    seed = 4
+    w = synth.model_weights(synth.OMNIVOICE, seed)
+    ids, mask = synth.maskgit_inputs(seed, step)
+    m0 = O.Backbone(w, synth.OMNIVOICE)
+    rows = [0, 7]
+    lo, ho = O.maskgit_pass(m0, ids, mask, 256, rows=rows)
+    with Engine(w, max_slots=0, max_ctx=0, max_batch=8, max_tokens=8 * 1024) as e:
+        logits = f32_zeros(8, 8, 768, 1025)
+        hid = f32_zeros(8, 1024, 1024)
+        e.m.tts_bb_maskgit_pass(e.h, 8, 1024, dev_i32(ids), dev_u8(mask), None, 256, logits, hidden_out=hid)
+        g = hid.cpu().numpy()[rows]
+        gl = logits.cpu().numpy()[rows]
+        herr = max(rel_err_rows(g[i], ho[i]) for i in range(len(rows)))
+        lerr = float(np.max(np.abs(gl - lo)))
+        report(f"maskgit_step{step}", hidden_rel=f"{herr:.2e}", logit_abs=f"{lerr:.2e}")
+        assert herr <= HIDDEN_TOL
+        assert lerr <= LOGIT_TOL

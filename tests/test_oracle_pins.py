@@ -297,3 +297,18 @@ def test_talker_prefill_then_decode_matches_longer_prefill(tiny):
     hid, _, _, _ = O.talker_decode_steps(tiny, cache, int(ids[6, 0]), ids[6:, 1:],
                                          forced_id0=ids[6:, 0])
     assert np.allclose(hid, h_all[6:], rtol=1e-11, atol=1e-12)
+
+
+def test_batched_code_predictor_frames_match_single_frames():
+    w = synth.model_weights(synth.ModelShape(
+        n_layers=1, hidden=64, n_q_heads=4, n_kv_heads=2, head_dim=16, ffn=96,
+        codebook_rows=(40,) * 16, n_heads_out=15, head_rows=40), 17)
+    m = O.Backbone(w, w.shape)
+    rng = np.random.default_rng(17)
+    th = rng.normal(size=(3, 64))
+    c0 = np.array([1, 39, 7])
+    codes, logits = O.code_predictor_frames(m, th, c0)
+    for f in range(3):
+        c1, l1, _ = O.code_predictor_frame(m, th[f], int(c0[f]))
+        assert np.array_equal(codes[f], c1)
+        assert np.allclose(logits[f], l1, rtol=1e-11, atol=1e-12)
