@@ -290,6 +290,119 @@ def run_talker_b1(args, ws, rank):
     return res, wl
 
 
+def fill_kv_random(m, h, L0, slots, n_layers, seed):
+    """Synthetic cached K/V (bf16 N(0,1), the scale of normed keys) for every stream, written
+    through the page table; generated on the device (their values do not affect timing)."""
+    import torch
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    for layer in range(n_layers):
+        for b in range(len(L0)):
+            n = int(L0[b])
+            k = torch.randn(n, 8, 128, generator=g, device="cuda").to(torch.bfloat16)
+            v = torch.randn(n, 8, 128, generator=g, device="cuda").to(torch.bfloat16)
+            m.tts_bb_debug_kv_write(h, layer, int(slots[b]), 0, n, k, v)
+    m.tts_bb_sync(h)
+
+
+def run_serving_b64(steps, warmup):
+    """64 streams, ragged cached lengths U[200, 2000], one decode step per stream per call."""
+    import torch
+    import codec_token_tts_gb300 as m
+    from tests.gpu_util import dev_i32
+    wl = ServingB64()
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    h = make_engine(wl, m, stream.cuda_stream, 2000 + steps + warmup + 1, wl.B, wl.B, wl.B)
+    slots = synth.block_permutation(wl.seed, wl.B)
+    fill_kv_random(m, h, wl.L0, slots, 28, wl.seed)
+    ids = synth.uniform_ids(synth.rng_for(wl.seed, "serve_ids"), wl.shape.codebook_rows, (steps + warmup + 1) * wl.B)
+    ids_d = dev_i32(ids.reshape(steps + warmup + 1, wl.B, 16))
+    logits = torch.zeros(wl.B, 3072, dtype=torch.float32, device="cuda")
+    sl = np.ascontiguousarray(slots, np.int32)
+    kv = np.ascontiguousarray(wl.L0, np.int32).copy()
+
+    def run(n, t0):
+        for t in range(t0, t0 + n):
+            # greedy ids written into the next step's codebook-0 column (stride 16)
+            m.lib.tts_bb_decode_step(h, wl.B, sl.ctypes.data, kv.ctypes.data, ids_d[t].data_ptr(), 0,
+                                     logits.data_ptr(), ids_d[t + 1, :, 0].data_ptr(),
+                                     m._opts(None, None, 16))
+            kv[:] += 1
+
+    run(warmup, 0)
+    m.tts_bb_sync(h)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    run(steps, warmup)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    st = m.tts_bb_sync(h, check=False)
+    # profiled steps for the roofline of the dominant kernel
+    m.tts_bb_profile(h, True)
+    kv0 = kv.copy()
+    for b in range(wl.B):
+        m.tts_bb_truncate(h, int(slots[b]), int(wl.L0[b]) + warmup)
+    kv[:] = wl.L0 + warmup
+    run(min(steps, 8), warmup)
+    rep = m.tts_bb_profile_report(h)
+    m.tts_bb_profile(h, False)
+    m.tts_bb_free(h)
+    kv_bytes = 114_688 * float(np.sum(wl.L0 + warmup + steps / 2 + 1))
+    step_bytes = 28 * 31_461_888 + 64 * 16 * 2048 + 3072 * 1024 * 2 + kv_bytes + 64 * 114_688
+    return {"workload": wl.config()["workload"], "value": wl.B / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+            "steps": steps, "status": st, "algorithmic_bytes_per_step": step_bytes,
+            "hbm_frac_of_measured": step_bytes / (ms / 1e3) / 1e9 / peaks()[0]["hbm_gbs"],
+            "roofline": roofline_from_profile(rep), "kernel_profile": rep}
+
+
+def run_maskgit(steps, warmup):
+    """OmniVoice MaskGIT pass: B=8 x S=1024 (256 text + 768 audio), 28 bidirectional layers, audio heads."""
+    import torch
+    import codec_token_tts_gb300 as m
+    from tests.gpu_util import config_for, dev_i32, dev_u8, weights_for
+    seed = 4
+    w = synth.model_weights(synth.OMNIVOICE, seed)
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    cfg = config_for(synth.OMNIVOICE, max_slots=0, max_ctx=0, max_batch=8, max_tokens=8192, sync_errors=0)
+    h = m.tts_bb_create(cfg, weights_for(w), stream.cuda_stream)
+    passes = [synth.maskgit_inputs(seed, s) for s in range(4)]
+    ids_d = [dev_i32(p[0]) for p in passes]
+    mask_d = [dev_u8(p[1]) for p in passes]
+    logits = torch.zeros(8, 8, 768, 1025, dtype=torch.float32, device="cuda")
+
+    def run(n):
+        for i in range(n):
+            m.tts_bb_maskgit_pass(h, 8, 1024, ids_d[i % 4], mask_d[i % 4], None, 256, logits, check=False)
+
+    run(warmup)
+    m.tts_bb_sync(h)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    run(steps)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    st = m.tts_bb_sync(h, check=False)
+    m.tts_bb_profile(h, True)
+    run(2)
+    rep = m.tts_bb_profile_report(h)
+    m.tts_bb_profile(h, False)
+    m.tts_bb_free(h)
+    flops = 2 * 8192 * 15_728_640 * 28 + 4 * 8 * 16 * 1024 ** 2 * 128 * 28 + 2 * 8 * 768 * 8200 * 1024
+    pk = peaks()[0]
+    return {"workload": "maskgit: OmniVoice LM pass, 28 layers, B=8 x S=1024 (256 text + 768 audio), bidirectional, "
+                        "8 x 1025 audio heads over the 768 audio positions",
+            "value": 1e3 / ms, "unit": "passes/s", "ms_per_pass": ms, "steps": steps, "status": st,
+            "tflops": flops / (ms / 1e3) / 1e12, "flop_per_pass": flops,
+            "tensor_frac_of_measured_sustained": flops / (ms / 1e3) / 1e12 / pk["bf16_tflops_sustained"],
+            "roofline": roofline_from_profile(rep), "kernel_profile": rep}
+
+
 def roofline_from_profile(rep, traffic=None):
     pk, src = peaks()
     ks = rep.get("kernels", [])
@@ -297,7 +410,7 @@ def roofline_from_profile(rep, traffic=None):
         return None
     top = max(ks, key=lambda k: k["ms"])
     total = sum(k["ms"] for k in ks)
-    if top["flops"] and top["bytes"] and top["flops"] / max(top["bytes"], 1) > 300:
+    if top["flops"] and (not top["bytes"] or top["flops"] / max(top["bytes"], 1) > 300):
         ach = top["flops"] / (top["ms"] / 1e3) / 1e12
         peak = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
         return {"kernel": top["kind"], "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
@@ -377,6 +490,7 @@ def main():
     ap.add_argument("--workload", default="talker_b1", choices=["talker_b1"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
+    ap.add_argument("--no-secondary", action="store_true", help="skip the batch-64 serving and MaskGIT lines")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -395,6 +509,8 @@ def main():
     build_lib()
     res, wl = run_talker_b1(args, ws, rank)
     res["roofline"] = roofline_from_profile(res["kernel_profile"], measured_traffic(res["kernel_profile"]))
+    if not args.no_secondary:
+        res["also"] = {"serving_b64": run_serving_b64(64, 4), "maskgit": run_maskgit(8, 3)}
     if rank == 0 and not args.no_cpu_baseline:
         v, n, el, setup_s = oracle_talker_tokens_per_s(args.cpu_budget_s, 10_000)
         ci = cpu_info()

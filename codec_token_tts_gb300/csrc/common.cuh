@@ -108,8 +108,12 @@ int launch_rmsnorm(const float* h, const bf16* gamma, bf16* y, int T, float eps,
 int launch_gemv(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st,
                 const bf16* X_lo = nullptr);
 // Y = X W^T with epilogue, tensor cores, any T.
+// Plain bf16 activations with T > 8 run on tcgen05 (k_gemm_tc.cu); split
+// activations (X_lo) run on mma.sync with a second MMA per k-step.
 int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st,
-                const bf16* X_lo = nullptr);
+                const bf16* X_lo = nullptr, int* err = nullptr);
+int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, int* err, cudaStream_t st);
+bool gemm_tc_available();
 
 // Per-token q/k RMSNorm + RoPE; q -> qout [T][16][128] bf16; k, v -> paged pool.
 // Token t belongs to sequence t / tok_per_seq at position seq_start[seq] + t % tok_per_seq,

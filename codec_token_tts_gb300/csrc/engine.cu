@@ -218,9 +218,10 @@ tts_bb_status finish(tts_bb* h) {
 }
 
 enum Kind { K_SETUP, K_EMBED, K_RMSNORM, K_GEMV, K_GEMM, K_QKROPE, K_ATTN_DECODE, K_ATTN_PREFILL, K_ARGMAX,
-            K_KVCOPY, K_MEGA, K_NKINDS };
-const char* kind_name[K_NKINDS] = {"setup", "embed_gather", "rmsnorm", "gemv", "gemm_mma", "qk_norm_rope_append",
-                                   "attn_decode", "attn_prefill", "argmax", "kv_copy", "decode_step_persistent"};
+            K_KVCOPY, K_MEGA, K_GEMM_TC, K_NKINDS };
+const char* kind_name[K_NKINDS] = {"setup", "embed_gather", "rmsnorm", "gemv", "gemm_mma_split", "qk_norm_rope_append",
+                                   "attn_decode", "attn_prefill", "argmax", "kv_copy", "decode_step_persistent",
+                                   "gemm_tcgen05"};
 
 cudaEvent_t prof_event(tts_bb* h) {
     if (!h->ev_pool.empty()) {
@@ -306,7 +307,7 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         const LayerW& w = h->L[l];
         KVView kv = kv_base;
         kv.pool = kv_base.pool + (size_t)l * layer_stride;
-        const int gk = T <= 8 ? K_GEMV : K_GEMM;
+        const int gk = T <= 8 ? K_GEMV : (mode == 0 ? K_GEMM : K_GEMM_TC);
         // decode carries GEMM inputs as bf16 high + low parts (weights are read
         // once either way); prefill / bidirectional passes use plain bf16
         const bool split = mode == 0;
@@ -317,7 +318,7 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         { Launch L(h, K_RMSNORM, norm_bytes); L += launch_rmsnorm(h->h, w.in_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st, ylo); }
         Epi e{};
         e.mode = EPI_STORE_F32; e.out = h->qkv; e.ldo = QKV;
-        { Launch L(h, gk, gemm_bytes(T, QKV, HID, 4), 2.0 * T * QKV * HID); L += launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st, ylo); }
+        { Launch L(h, gk, gemm_bytes(T, QKV, HID, 4), 2.0 * T * QKV * HID); L += launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st, ylo, h->err); }
         { Launch L(h, K_QKROPE, T * (4.0 * QKV + 2.0 * QKV));
           L += launch_qk_norm_rope_append(h->qkv, w.qn, w.kn, h->cos_t, h->sin_t, c.rms_eps, h->q, kv,
                                           h->seq_start, h->seq_len, tok_per_seq, T, h->err, h->st); }
@@ -330,14 +331,15 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         }
         e = Epi{};
         e.mode = EPI_ADD_F32; e.out = h->h; e.ldo = HID;
-        { Launch L(h, gk, gemm_bytes(T, HID, NQ * HD, 8), 2.0 * T * HID * NQ * HD); L += launch_gemm(h->ao, w.wo, T, HID, NQ * HD, e, h->st, aolo); }
+        { Launch L(h, gk, gemm_bytes(T, HID, NQ * HD, 8), 2.0 * T * HID * NQ * HD); L += launch_gemm(h->ao, w.wo, T, HID, NQ * HD, e, h->st, aolo, h->err); }
         { Launch L(h, K_RMSNORM, norm_bytes); L += launch_rmsnorm(h->h, w.post_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st, ylo); }
         e = Epi{};
         e.mode = EPI_SWIGLU; e.out = h->m; e.ldo = c.ffn; e.out_lo = mlo;
-        { Launch L(h, gk, gemm_bytes(T, 2 * c.ffn, HID, 1), 2.0 * T * 2 * c.ffn * HID); L += launch_gemm(h->y, w.wgu, T, 2 * c.ffn, HID, e, h->st, ylo); }
+        { Launch L(h, gk, gemm_bytes(T, 2 * c.ffn, HID, 1), 2.0 * T * 2 * c.ffn * HID); L += launch_gemm(h->y, w.wgu, T, 2 * c.ffn, HID, e, h->st, ylo, h->err); }
         e = Epi{};
         e.mode = EPI_ADD_F32; e.out = h->h; e.ldo = HID;
-        { Launch L(h, gk, gemm_bytes(T, HID, c.ffn, 8), 2.0 * T * HID * c.ffn); L += launch_gemm(h->m, w.wd, T, HID, c.ffn, e, h->st, mlo); }    }
+        { Launch L(h, gk, gemm_bytes(T, HID, c.ffn, 8), 2.0 * T * HID * c.ffn); L += launch_gemm(h->m, w.wd, T, HID, c.ffn, e, h->st, mlo, h->err); }
+    }
 }
 
 // Final norm of B selected rows + head GEMM with logits / argmax.
@@ -349,8 +351,8 @@ void run_head(tts_bb* h, int B, int per_seq, int head_idx, bool last_of_seq, flo
       L += launch_rmsnorm(h->h, h->final_norm, h->y, B, c.rms_eps, 1, per_seq, 0, last_of_seq ? h->seq_len : nullptr, h->st, ylo); }
     Epi e{};
     e.mode = EPI_LOGITS; e.out = logits_out; e.ldo = c.head_rows; e.amax = argmax_out ? h->amax : nullptr;
-    { Launch L(h, B <= 8 ? K_GEMV : K_GEMM, gemm_bytes(B, c.head_rows, HID, logits_out ? 4 : 0), 2.0 * B * c.head_rows * HID);
-      L += launch_gemm(h->y, h->heads[head_idx], B, c.head_rows, HID, e, h->st, ylo); }
+    { Launch L(h, B <= 8 ? K_GEMV : (split ? K_GEMM : K_GEMM_TC), gemm_bytes(B, c.head_rows, HID, logits_out ? 4 : 0), 2.0 * B * c.head_rows * HID);
+      L += launch_gemm(h->y, h->heads[head_idx], B, c.head_rows, HID, e, h->st, ylo, h->err); }
     if (argmax_out) { Launch L(h, K_ARGMAX); L += launch_argmax_finalize(h->amax, argmax_out, argmax_stride, B, h->st); }
 }
 
@@ -918,8 +920,8 @@ TTS_API tts_bb_status tts_bb_maskgit_pass(tts_bb* h, int B, int S, const int32_t
         e.mode = EPI_LOGITS_PERM; e.out = logits_out; e.perm_rows = Sa; e.perm_vocab = c.head_rows;
         e.perm_groups = c.n_heads;
         const int N = c.n_heads * c.head_rows;
-        Launch L(h, B * Sa <= 8 ? K_GEMV : K_GEMM, gemm_bytes(B * Sa, N, HID, 4), 2.0 * B * Sa * N * HID);
-        L += launch_gemm(h->y, h->heads[0], B * Sa, N, HID, e, h->st);
+        Launch L(h, B * Sa <= 8 ? K_GEMV : K_GEMM_TC, gemm_bytes(B * Sa, N, HID, 4), 2.0 * B * Sa * N * HID);
+        L += launch_gemm(h->y, h->heads[0], B * Sa, N, HID, e, h->st, nullptr, h->err);
     }
     return finish(h);
 }

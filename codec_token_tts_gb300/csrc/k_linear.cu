@@ -336,9 +336,14 @@ __global__ void __launch_bounds__(256) k_gemm_mma(const bf16* __restrict__ X, co
         }
 }
 
-int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st, const bf16* X_lo) {
+int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st, const bf16* X_lo,
+                int* err) {
     if (T <= 0) return 0;
     if (T <= 8) return launch_gemv(X, W, T, N, K, e, st, X_lo);
+    if (!X_lo && gemm_tc_available()) {
+        const int n = launch_gemm_tc(X, W, T, N, K, e, err, st);
+        if (n) return n;
+    }
     static bool attr_set = false;
     if (!attr_set) {
         cudaFuncSetAttribute(k_gemm_mma<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, gm::SMEM);
