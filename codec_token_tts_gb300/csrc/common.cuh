@@ -108,10 +108,19 @@ int launch_rmsnorm(const float* h, const bf16* gamma, bf16* y, int T, float eps,
 int launch_gemv(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st,
                 const bf16* X_lo = nullptr);
 // Y = X W^T with epilogue, tensor cores, any T.
+// Split-K workspace for the small-batch GEMM: fp32 partial tiles and one
+// arrival counter per 64-feature tile (zero between launches).
+struct SplitK {
+    float* part;
+    size_t part_elems;
+    int* ctr;
+    int n_ctr;
+};
 // Plain bf16 activations with T > 8 run on tcgen05 (k_gemm_tc.cu); split
-// activations (X_lo) run on mma.sync with a second MMA per k-step.
+// activations (X_lo) with T <= 256 run on the split-K mma.sync kernel when a
+// workspace is given, else on the tiled mma.sync kernel with a second MMA per k-step.
 int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st,
-                const bf16* X_lo = nullptr, int* err = nullptr);
+                const bf16* X_lo = nullptr, int* err = nullptr, const SplitK* sk = nullptr);
 int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, int* err, cudaStream_t st);
 bool gemm_tc_available();
 

@@ -107,6 +107,7 @@ struct tts_bb {
     bf16* ao = nullptr;
     bf16* m = nullptr;
     bf16 *y_lo = nullptr, *ao_lo = nullptr, *m_lo = nullptr;  // low bf16 parts (decode)
+    SplitK sk{};                        // split-K workspace of the decode-batch GEMM
     float* part = nullptr;
     unsigned long long* amax = nullptr;
     int32_t *seq_slot = nullptr, *seq_start = nullptr, *seq_len = nullptr, *key_len = nullptr;
@@ -314,11 +315,12 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         bf16* ylo = split ? h->y_lo : nullptr;
         bf16* aolo = split ? h->ao_lo : nullptr;
         bf16* mlo = split ? h->m_lo : nullptr;
+        const SplitK* skp = split && h->sk.part ? &h->sk : nullptr;
         const double norm_bytes = T * (4.0 + 2.0) * HID + 2.0 * HID;
         { Launch L(h, K_RMSNORM, norm_bytes); L += launch_rmsnorm(h->h, w.in_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st, ylo); }
         Epi e{};
         e.mode = EPI_STORE_F32; e.out = h->qkv; e.ldo = QKV;
-        { Launch L(h, gk, gemm_bytes(T, QKV, HID, 4), 2.0 * T * QKV * HID); L += launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st, ylo, h->err); }
+        { Launch L(h, gk, gemm_bytes(T, QKV, HID, 4), 2.0 * T * QKV * HID); L += launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st, ylo, h->err, skp); }
         { Launch L(h, K_QKROPE, T * (4.0 * QKV + 2.0 * QKV));
           L += launch_qk_norm_rope_append(h->qkv, w.qn, w.kn, h->cos_t, h->sin_t, c.rms_eps, h->q, kv,
                                           h->seq_start, h->seq_len, tok_per_seq, T, h->err, h->st); }
@@ -331,14 +333,14 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         }
         e = Epi{};
         e.mode = EPI_ADD_F32; e.out = h->h; e.ldo = HID;
-        { Launch L(h, gk, gemm_bytes(T, HID, NQ * HD, 8), 2.0 * T * HID * NQ * HD); L += launch_gemm(h->ao, w.wo, T, HID, NQ * HD, e, h->st, aolo, h->err); }
+        { Launch L(h, gk, gemm_bytes(T, HID, NQ * HD, 8), 2.0 * T * HID * NQ * HD); L += launch_gemm(h->ao, w.wo, T, HID, NQ * HD, e, h->st, aolo, h->err, skp); }
         { Launch L(h, K_RMSNORM, norm_bytes); L += launch_rmsnorm(h->h, w.post_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st, ylo); }
         e = Epi{};
         e.mode = EPI_SWIGLU; e.out = h->m; e.ldo = c.ffn; e.out_lo = mlo;
-        { Launch L(h, gk, gemm_bytes(T, 2 * c.ffn, HID, 1), 2.0 * T * 2 * c.ffn * HID); L += launch_gemm(h->y, w.wgu, T, 2 * c.ffn, HID, e, h->st, ylo, h->err); }
+        { Launch L(h, gk, gemm_bytes(T, 2 * c.ffn, HID, 1), 2.0 * T * 2 * c.ffn * HID); L += launch_gemm(h->y, w.wgu, T, 2 * c.ffn, HID, e, h->st, ylo, h->err, skp); }
         e = Epi{};
         e.mode = EPI_ADD_F32; e.out = h->h; e.ldo = HID;
-        { Launch L(h, gk, gemm_bytes(T, HID, c.ffn, 8), 2.0 * T * HID * c.ffn); L += launch_gemm(h->m, w.wd, T, HID, c.ffn, e, h->st, mlo, h->err); }
+        { Launch L(h, gk, gemm_bytes(T, HID, c.ffn, 8), 2.0 * T * HID * c.ffn); L += launch_gemm(h->m, w.wd, T, HID, c.ffn, e, h->st, mlo, h->err, skp); }
     }
 }
 
@@ -352,7 +354,8 @@ void run_head(tts_bb* h, int B, int per_seq, int head_idx, bool last_of_seq, flo
     Epi e{};
     e.mode = EPI_LOGITS; e.out = logits_out; e.ldo = c.head_rows; e.amax = argmax_out ? h->amax : nullptr;
     { Launch L(h, B <= 8 ? K_GEMV : (split ? K_GEMM : K_GEMM_TC), gemm_bytes(B, c.head_rows, HID, logits_out ? 4 : 0), 2.0 * B * c.head_rows * HID);
-      L += launch_gemm(h->y, h->heads[head_idx], B, c.head_rows, HID, e, h->st, ylo, h->err); }
+      L += launch_gemm(h->y, h->heads[head_idx], B, c.head_rows, HID, e, h->st, ylo, h->err,
+                        split && h->sk.part ? &h->sk : nullptr); }
     if (argmax_out) { Launch L(h, K_ARGMAX); L += launch_argmax_finalize(h->amax, argmax_out, argmax_stride, B, h->st); }
 }
 
@@ -591,6 +594,16 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
         (e = dalloc(h, &h->err, 1)) != cudaSuccess)
         return bail(TTS_BB_E_OOM);
     if ((e = cudaMallocHost(&h->h_err, sizeof(int))) != cudaSuccess) return bail(TTS_BB_E_OOM);
+    if (c.max_batch > 8) {  // K splits x N, largest over the decode GEMMs, for K slices of 256 / token-tiles
+        const int mt = c.max_batch <= 64 ? 1 : (c.max_batch <= 128 ? 2 : 4);
+        const size_t ks_n = std::max(std::max((size_t)(HID * mt / 256) * 2 * c.ffn, (size_t)(NQ * HD * mt / 256) * HID),
+                                     std::max((size_t)(c.ffn * mt / 256) * HID, (size_t)(HID * mt / 256) * QKV));
+        h->sk.part_elems = std::max(ks_n, (size_t)(HID * mt / 256) * std::max(c.head_rows, 1)) * c.max_batch;
+        h->sk.n_ctr = 256;
+        if ((e = dalloc(h, &h->sk.part, h->sk.part_elems)) != cudaSuccess || (e = dalloc(h, &h->sk.ctr, 256)) != cudaSuccess)
+            return bail(TTS_BB_E_OOM);
+        cudaMemset(h->sk.ctr, 0, 256 * sizeof(int));
+    }
     cudaMemset(h->err, 0, sizeof(int));
     tts_bb_status s = ensure_scratch(h, std::max(nb, std::max(c.max_tokens, 1)));
     if (s != TTS_BB_OK) return bail(s);

@@ -50,11 +50,14 @@ __global__ void __launch_bounds__(128) k_attn_decode(const bf16* __restrict__ q,
         const bf16* vb = kv_tile(kv, b, j, 1, g);
         const int key0 = j * KVB + warp * 16;
         float d[32];  // d[h*16 + kk]
-        uint2 kr[16];
+        uint2 kr[16], vr[16];
+        // K and V of the warp's 16 keys are independent of the scores: issue all loads at once
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk)
-            kr[kk] = (key0 + kk < L) ? *reinterpret_cast<const uint2*>(kb + (size_t)(warp * 16 + kk) * HD + lane * 4)
-                                     : make_uint2(0u, 0u);
+        for (int kk = 0; kk < 16; ++kk) {
+            const bool ok = key0 + kk < L;
+            kr[kk] = ok ? *reinterpret_cast<const uint2*>(kb + (size_t)(warp * 16 + kk) * HD + lane * 4) : make_uint2(0u, 0u);
+            vr[kk] = ok ? *reinterpret_cast<const uint2*>(vb + (size_t)(warp * 16 + kk) * HD + lane * 4) : make_uint2(0u, 0u);
+        }
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
             const float k0 = __uint_as_float(kr[kk].x << 16), k1 = __uint_as_float(kr[kk].x & 0xFFFF0000u);
@@ -97,10 +100,9 @@ __global__ void __launch_bounds__(128) k_attn_decode(const bf16* __restrict__ q,
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
             const float p0 = __shfl_sync(0xffffffffu, p, kk), p1 = __shfl_sync(0xffffffffu, p, 16 + kk);
-            if (key0 + kk < L) {
-                const uint2 vr = *reinterpret_cast<const uint2*>(vb + (size_t)(warp * 16 + kk) * HD + lane * 4);
-                const float v0 = __uint_as_float(vr.x << 16), v1 = __uint_as_float(vr.x & 0xFFFF0000u);
-                const float v2 = __uint_as_float(vr.y << 16), v3 = __uint_as_float(vr.y & 0xFFFF0000u);
+            {
+                const float v0 = __uint_as_float(vr[kk].x << 16), v1 = __uint_as_float(vr[kk].x & 0xFFFF0000u);
+                const float v2 = __uint_as_float(vr[kk].y << 16), v3 = __uint_as_float(vr[kk].y & 0xFFFF0000u);
                 o0[0] += p0 * v0; o0[1] += p0 * v1; o0[2] += p0 * v2; o0[3] += p0 * v3;
                 o1[0] += p1 * v0; o1[1] += p1 * v1; o1[2] += p1 * v2; o1[3] += p1 * v3;
             }
@@ -157,7 +159,7 @@ int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B
                         bf16* out, int max_splits, cudaStream_t st, bf16* out_lo) {
     if (B <= 0) return 0;
     const int nblk = (max_len + KVB - 1) / KVB;
-    int splits = (2 * 152 + B * NKV - 1) / (B * NKV);
+    int splits = (8 * 152 + B * NKV - 1) / (B * NKV);   // aim for ~8 CTAs per SM
     splits = max(1, min(splits, min(nblk, max_splits)));
     const int bps = (nblk + splits - 1) / splits;
     splits = (nblk + bps - 1) / bps;

@@ -336,10 +336,182 @@ __global__ void __launch_bounds__(256) k_gemm_mma(const bf16* __restrict__ X, co
         }
 }
 
+// ---------------------------------------------------------------- split-K GEMM for decode batches
+// Y[T][N] = (X + X_lo)[T][K] W[N][K]^T for 8 < T <= 256. CTA (n-tile, k-split)
+// owns a 64-feature x KC slice of W and the matching T x KC activations: it
+// issues every load of its slice at once (one round trip), computes a
+// 64 x T partial on mma.sync (both activation parts), writes it to the
+// workspace, and the last CTA to arrive at the n-tile's counter sums the K
+// splits in index order and applies the epilogue (deterministic; it also
+// re-arms the counter for the next launch). KC = 256 / MT keeps the
+// activation chunk at 64 KB whatever T is.
+namespace sk {
+constexpr int BN = 64, LDS_PAD = 8, MAXT = 256;
+}  // namespace sk
+
+template <int MT>  // token tiles of 64; KC = 256 / MT
+__global__ void __launch_bounds__(256) k_gemm_splitk(const bf16* __restrict__ X, const bf16* __restrict__ X_lo,
+                                                     const bf16* __restrict__ W, int T, int N, int K, Epi e,
+                                                     float* __restrict__ part, int* __restrict__ ctr) {
+    using namespace sk;
+    constexpr int KC = 256 / MT, LDS = KC + LDS_PAD, TP = MT * 64;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    bf16* sW = reinterpret_cast<bf16*>(smem_raw);  // [64][LDS]
+    bf16* sA = sW + BN * LDS;                        // [TP][LDS]
+    bf16* sL = sA + TP * LDS;                        // [TP][LDS]
+    __shared__ int last_s;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wm = warp >> 1, wn = warp & 1;  // 4 x 2 warps: rows wm*16 (+64 per token tile), cols wn*32
+    const int n0 = blockIdx.x * BN, kc0 = blockIdx.y * KC;
+    const int KS = gridDim.y;
+    constexpr int CPR = KC / 8;  // 16-byte chunks per row
+
+    for (int c = tid; c < BN * CPR; c += 256) {
+        const int r = c / CPR, col = (c % CPR) * 8;
+        cp_async16(sW + r * LDS + col, W + (size_t)(n0 + r) * K + kc0 + col, true);
+    }
+    for (int c = tid; c < TP * CPR; c += 256) {
+        const int r = c / CPR, col = (c % CPR) * 8;
+        const size_t src = (size_t)min(r, T - 1) * K + kc0 + col;
+        cp_async16(sA + r * LDS + col, X + src, r < T);
+        cp_async16(sL + r * LDS + col, X_lo + src, r < T);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+
+    float acc[MT][4][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[mt][j][q] = 0.f;
+#pragma unroll 4
+    for (int kk = 0; kk < KC; kk += 16) {
+        uint32_t bfr[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int r = wn * 32 + j * 16 + (lane & 7) + ((lane >> 4) << 3);
+            ldmatrix_x4(bfr[j], sW + r * LDS + kk + ((lane >> 3) & 1) * 8);
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            uint32_t af[4], lf[4];
+            const int r = mt * 64 + wm * 16 + (lane & 15);
+            ldmatrix_x4(af, sA + r * LDS + kk + (lane >> 4) * 8);
+            ldmatrix_x4(lf, sL + r * LDS + kk + (lane >> 4) * 8);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                mma16816(acc[mt][2 * j], af, &bfr[j][0]);
+                mma16816(acc[mt][2 * j + 1], af, &bfr[j][2]);
+                mma16816(acc[mt][2 * j], lf, &bfr[j][0]);
+                mma16816(acc[mt][2 * j + 1], lf, &bfr[j][2]);
+            }
+        }
+    }
+    // partial tile -> workspace part[ks][t][n]
+    float* pk = part + (size_t)blockIdx.y * T * N;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            const int t = mt * 64 + wm * 16 + (lane >> 2) + hr * 8;
+            if (t >= T) continue;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int n = n0 + wn * 32 + j * 8 + (lane & 3) * 2;
+                *reinterpret_cast<float2*>(pk + (size_t)t * N + n) = make_float2(acc[mt][j][hr * 2], acc[mt][j][hr * 2 + 1]);
+            }
+        }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const int old = atomicAdd(ctr + blockIdx.x, 1);
+        last_s = (old == KS - 1);
+        if (last_s) ctr[blockIdx.x] = 0;  // re-arm for the next launch
+    }
+    __syncthreads();
+    if (!last_s) return;
+    __threadfence();
+    // last CTA: thread -> (t, 4 features); the K splits are summed in index
+    // order, four splits' loads in flight at a time; then the epilogue
+    for (int idx = tid; idx < T * (BN / 4); idx += 256) {
+        const int t = idx / (BN / 4), n = n0 + (idx % (BN / 4)) * 4;
+        const float* src = part + (size_t)t * N + n;
+        const size_t sstride = (size_t)T * N;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        int s = 0;
+        for (; s + 4 <= KS; s += 4) {
+            float4 p[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) p[u] = __ldcg(reinterpret_cast<const float4*>(src + (s + u) * sstride));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) { v.x += p[u].x; v.y += p[u].y; v.z += p[u].z; v.w += p[u].w; }
+        }
+        for (; s < KS; ++s) {
+            const float4 p = __ldcg(reinterpret_cast<const float4*>(src + s * sstride));
+            v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
+        }
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+        if (e.mode == EPI_SWIGLU) {
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {
+                const float mv = silu(vv[u]) * vv[u + 1];
+                reinterpret_cast<bf16*>(e.out)[(size_t)t * e.ldo + (n + u) / 2] = f2bf(mv);
+                if (e.out_lo) reinterpret_cast<bf16*>(e.out_lo)[(size_t)t * e.ldo + (n + u) / 2] = f2bf_lo(mv);
+            }
+        } else {
+            unsigned long long best = 0ull;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                epi_one(e, t, n + u, vv[u]);
+                const unsigned long long pk = pack_argmax(vv[u], n + u);
+                best = pk > best ? pk : best;
+            }
+            if (e.mode == EPI_LOGITS && e.amax) atomicMax(e.amax + t, best);
+        }
+    }
+}
+
+template <int MT>
+static constexpr int splitk_smem() {
+    return (sk::BN + 2 * MT * 64) * (256 / MT + sk::LDS_PAD) * 2;
+}
+
+static int launch_splitk(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N, int K, const Epi& e,
+                         const SplitK& w, cudaStream_t st) {
+    using namespace sk;
+    if (T > MAXT || N % BN != 0 || N / BN > w.n_ctr) return 0;
+    const int MT = T <= 64 ? 1 : (T <= 128 ? 2 : 4);
+    const int KC = 256 / MT;
+    if (K % KC != 0) return 0;
+    const int KS = K / KC;
+    if ((size_t)KS * T * N > w.part_elems) return 0;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_gemm_splitk<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, splitk_smem<1>());
+        cudaFuncSetAttribute(k_gemm_splitk<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, splitk_smem<2>());
+        cudaFuncSetAttribute(k_gemm_splitk<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, splitk_smem<4>());
+        attr = true;
+    }
+    dim3 grid(N / BN, KS);
+    switch (MT) {
+        case 1: k_gemm_splitk<1><<<grid, 256, splitk_smem<1>(), st>>>(X, X_lo, W, T, N, K, e, w.part, w.ctr); break;
+        case 2: k_gemm_splitk<2><<<grid, 256, splitk_smem<2>(), st>>>(X, X_lo, W, T, N, K, e, w.part, w.ctr); break;
+        default: k_gemm_splitk<4><<<grid, 256, splitk_smem<4>(), st>>>(X, X_lo, W, T, N, K, e, w.part, w.ctr); break;
+    }
+    return 1;
+}
+
 int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st, const bf16* X_lo,
-                int* err) {
+                int* err, const SplitK* skw) {
     if (T <= 0) return 0;
     if (T <= 8) return launch_gemv(X, W, T, N, K, e, st, X_lo);
+    if (X_lo && skw) {
+        const int n = launch_splitk(X, X_lo, W, T, N, K, e, *skw, st);
+        if (n) return n;
+    }
     if (!X_lo && gemm_tc_available()) {
         const int n = launch_gemm_tc(X, W, T, N, K, e, err, st);
         if (n) return n;
