@@ -50,11 +50,15 @@ __global__ void k_setup(SetupArgs a, int32_t* seq_slot, int32_t* seq_start, int3
 }
 
 __global__ void k_kv_copy(bf16* pool, const int32_t* page_table, int slot, int mbps, int pos0, int n, bf16* k,
-                          bf16* v, int to_pool) {
+                          bf16* v, int to_pool, int n_blocks, int* err) {
     // one CTA per token, 256 threads: 8 kv heads x 128 elements, 4 per thread for K and V
     const int t = blockIdx.x;
     const int pos = pos0 + t;
     const int phys = page_table[(size_t)slot * mbps + pos / KVB];
+    if (phys < 0 || phys >= n_blocks) {  // no block behind this position: report, touch nothing
+        if (threadIdx.x == 0) set_err(err, ERR_KV_RANGE);
+        return;
+    }
     for (int e = threadIdx.x; e < NKV * HD; e += blockDim.x) {
         const int g = e / HD, d = e % HD;
         const size_t pk = (((size_t)phys * 2 + 0) * NKV + g) * KVB * HD + (size_t)(pos % KVB) * HD + d;
@@ -126,19 +130,22 @@ struct tts_bb {
     std::string prof_json;
     // persistent small-batch decode step
     int mega_grid = 0;                 // 0 = not available on this device
-    unsigned long long* mega_bar = nullptr;
     int* mega_abort = nullptr;
     float* mega_part = nullptr;
     float* mega_m = nullptr;
-    unsigned long long bar_base = 0;
+    unsigned long long* ll_xbuf = nullptr;   // exchange words
+    unsigned long long* ll_amax = nullptr;   // [MAXB], re-armed by the kernel
+    unsigned int* ll_done = nullptr;
+    uint32_t ep_base = 1;
     MegaArgs* mega = nullptr;          // per-handle constant fields filled at create
     unsigned long long* mega_trace = nullptr;   // phase stamps while profiling
     std::vector<double> phase_us;      // summed per-phase mean-over-CTA durations over traced layers
     std::vector<double> phase_max_us;  // summed per-phase max-over-CTA durations
     long phase_n = 0;                  // traced layers
-    double unit_us[3] = {0, 0, 0};     // attention unit sub-phases (CTAs with a unit)
-    double ring_wait_us = 0, ring_wait_max_us = 0;  // weight-ring waits per layer (mean, max over CTAs)
-    long unit_n = 0;
+    std::vector<double> sub_us;        // gate/up sub-phases
+    double unit_split[2] = {0, 0};
+    long unit_split_n[2] = {0, 0};
+    long sub_n = 0;
 };
 
 namespace {
@@ -198,10 +205,10 @@ tts_bb_status read_err(tts_bb* h) {
     const int v = *h->h_err;
     if (v) {
         cudaMemsetAsync(h->err, 0, sizeof(int), h->st);
-        if ((v & ERR_TIMEOUT) && h->mega_bar) {  // restart the persistent step's barrier state
-            cudaMemsetAsync(h->mega_bar, 0, sizeof(unsigned long long), h->st);
+        if ((v & ERR_TIMEOUT) && h->mega_abort) {  // re-arm the persistent step after an abort
             cudaMemsetAsync(h->mega_abort, 0, sizeof(int), h->st);
-            h->bar_base = 0;
+            cudaMemsetAsync(h->ll_amax, 0, mk::MAXB * sizeof(unsigned long long), h->st);
+            cudaMemsetAsync(h->ll_done, 0, sizeof(unsigned int), h->st);
         }
         cudaStreamSynchronize(h->st);
         if (v & ERR_TIMEOUT) return fail(h, TTS_BB_E_DEVICE_TIMEOUT, "a device-side wait timed out");
@@ -609,15 +616,22 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
     if (s != TTS_BB_OK) return bail(s);
     // persistent decode step: barrier counter, abort flag, block partials, constant arguments
     if (c.max_slots > 0 && c.n_layers >= 1 && c.n_layers <= mk::MAXL && c.max_ctx <= 64 * KVB && (c.n_heads == 0 || c.head_rows % 2 == 0) && c.text_vocab == 0) {
-        h->mega_grid = mega_max_grid();
+        h->mega_grid = ll_max_grid();
         cudaGetLastError();
+        if (const char* g = std::getenv("TTS_BB_DECODE_CTAS"))  // tuning knob: CTAs of the persistent step
+            h->mega_grid = std::max(0, std::min(h->mega_grid, std::atoi(g)));
         if (h->mega_grid > 0) {
-            if ((e = dalloc(h, &h->mega_bar, 1)) != cudaSuccess || (e = dalloc(h, &h->mega_abort, 1)) != cudaSuccess ||
+            const size_t xw = ll_xbuf_words(h->mbps);
+            if ((e = dalloc(h, &h->mega_abort, 1)) != cudaSuccess ||
                 (e = dalloc(h, &h->mega_part, (size_t)mk::MAXB * NQ * h->mbps * PART_STRIDE)) != cudaSuccess ||
-                (e = dalloc(h, &h->mega_m, (size_t)mk::MAXB * c.ffn)) != cudaSuccess)
+                (e = dalloc(h, &h->mega_m, (size_t)mk::MAXB * c.ffn)) != cudaSuccess ||
+                (e = dalloc(h, &h->ll_xbuf, xw)) != cudaSuccess || (e = dalloc(h, &h->ll_amax, mk::MAXB)) != cudaSuccess ||
+                (e = dalloc(h, &h->ll_done, 1)) != cudaSuccess)
                 return bail(TTS_BB_E_OOM);
-            cudaMemset(h->mega_bar, 0, sizeof(unsigned long long));
             cudaMemset(h->mega_abort, 0, sizeof(int));
+            cudaMemset(h->ll_xbuf, 0, xw * sizeof(unsigned long long));
+            cudaMemset(h->ll_amax, 0, mk::MAXB * sizeof(unsigned long long));
+            cudaMemset(h->ll_done, 0, sizeof(unsigned int));
             MegaArgs* ma = new MegaArgs();
             std::memset(ma, 0, sizeof *ma);
             for (int l = 0; l < c.n_layers; ++l) {
@@ -636,9 +650,10 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
             ma->m = h->mega_m;
             ma->part = h->mega_part;
             ma->nblk_max = h->mbps;
-            ma->amax = h->amax;
-            ma->bar = h->mega_bar;
+            ma->amax = h->ll_amax;
             ma->abort_flag = h->mega_abort;
+            ma->xbuf = h->ll_xbuf;
+            ma->done = h->ll_done;
             ma->err = h->err;
             ma->cos_t = h->cos_t;
             ma->sin_t = h->sin_t;
@@ -737,13 +752,14 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
             ma.upd_idx[i] = a.upd_idx[i];
             ma.upd_val[i] = a.upd_val[i];
         }
-        ma.bar_base = h->bar_base;
+        ma.ep_base = h->ep_base;
+        for (int b = 0; b < B; ++b) ma.last_phys[b] = h->page_table[(size_t)slots[b] * h->mbps + kv_lens[b] / KVB];
         ma.trace = nullptr;
         if (h->prof_on) {
             if (!h->mega_trace &&
                 dalloc(h, &h->mega_trace, (size_t)h->mega_grid * mk::MAXL * 16) != cudaSuccess)
                 return fail(h, TTS_BB_E_OOM, "trace buffer");
-            if (h->phase_n == 0 && h->unit_n == 0)
+            if (h->phase_n == 0)
                 cudaMemsetAsync(h->mega_trace, 0, (size_t)h->mega_grid * mk::MAXL * 16 * 8, h->st);
             ma.trace = h->mega_trace;
         }
@@ -753,25 +769,24 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
                               (ma.head ? 2.0 * c.head_rows * HID : 0);
         {
             Launch L(h, K_MEGA, wbytes + kvb, 2.0 * B * wbytes / 2);
-            const cudaError_t e = launch_decode_mega(ma, h->mega_grid, h->st);
+            const cudaError_t e = launch_decode_ll(ma, h->mega_grid, h->st);
             if (e != cudaSuccess) return cuda_fail(h, e, "persistent decode step launch");
             L += 1;
         }
-        h->bar_base += (unsigned long long)mega_barriers(c.n_layers, ma.head != nullptr, ma.argmax_out != nullptr) *
-                       (unsigned long long)h->mega_grid;
+        h->ep_base += ll_epochs_per_launch(c.n_layers);
         if (ma.trace) {  // fold this launch's phase stamps into the profile (synchronises)
-            const int NS = 16, G = h->mega_grid, NL = c.n_layers;
+            const int NS = 16, NP = 10, G = h->mega_grid, NL = c.n_layers;
             std::vector<unsigned long long> st((size_t)G * NL * NS, 0ull);
             cudaMemcpyAsync(st.data(), h->mega_trace, st.size() * 8, cudaMemcpyDeviceToHost, h->st);
             cudaStreamSynchronize(h->st);
-            if (h->phase_us.empty()) { h->phase_us.assign(12, 0.0); h->phase_max_us.assign(12, 0.0); }
-            for (int l = 0; l < NL; ++l) {
-                for (int i = 0; i < 12; ++i) {
-                    if (i == 11 && l + 1 >= NL) continue;
+            if (h->phase_us.empty()) { h->phase_us.assign(NP, 0.0); h->phase_max_us.assign(NP, 0.0); }
+            for (int l = 0; l < NL; ++l)
+                for (int i = 0; i < NP; ++i) {
+                    if (i == NP - 1 && l + 1 >= NL) continue;
                     double sum = 0, mx = 0;
                     for (int g = 0; g < G; ++g) {
                         const unsigned long long* r = &st[((size_t)g * NL + l) * NS];
-                        const unsigned long long nxt = (i == 11) ? st[((size_t)g * NL + l + 1) * NS] : r[i + 1];
+                        const unsigned long long nxt = (i == NP - 1) ? st[((size_t)g * NL + l + 1) * NS] : r[i + 1];
                         const double d = (double)(nxt - r[i]) * 1e-3;
                         sum += d;
                         mx = d > mx ? d : mx;
@@ -779,26 +794,27 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
                     h->phase_us[i] += sum / G;
                     h->phase_max_us[i] += mx;
                 }
+            // gate/up sub-phases (stamps 6, 10..14): ring wait, math, reduce + store of chunk 0; wait, math of chunk 1
+            if (h->sub_us.empty()) h->sub_us.assign(5, 0.0);
+            for (int l = 0; l < NL; ++l)
                 for (int g = 0; g < G; ++g) {
                     const unsigned long long* r = &st[((size_t)g * NL + l) * NS];
-                    if (r[12] && r[13] && r[14] && r[12] >= r[2]) {
-                        h->unit_us[0] += (double)(r[12] - r[2]) * 1e-3;
-                        h->unit_us[1] += (double)(r[13] - r[12]) * 1e-3;
-                        h->unit_us[2] += (double)(r[14] - r[13]) * 1e-3;
-                        h->unit_n++;
-                    }
+                    if (!r[10] || !r[14]) continue;
+                    h->sub_us[0] += (r[10] - r[6]) * 1e-3;
+                    h->sub_us[1] += (r[11] - r[10]) * 1e-3;
+                    h->sub_us[2] += (r[12] - r[11]) * 1e-3;
+                    h->sub_us[3] += (r[13] - r[12]) * 1e-3;
+                    h->sub_us[4] += (r[14] - r[13]) * 1e-3;
+                    h->sub_n++;
                 }
-            }
-            for (int l = 0; l < NL; ++l) {
-                double sum = 0, mx = 0;
+            // attention-unit phase (stamps 2 -> 3) split by whether the CTA ran a unit
+            for (int l = 0; l < NL; ++l)
                 for (int g = 0; g < G; ++g) {
-                    const double w = (double)st[((size_t)g * NL + l) * NS + 15] * 1e-3;
-                    sum += w;
-                    mx = w > mx ? w : mx;
+                    const unsigned long long* r = &st[((size_t)g * NL + l) * NS];
+                    const int k = r[15] ? 1 : 0;
+                    h->unit_split[k] += (r[3] - r[2]) * 1e-3;
+                    h->unit_split_n[k]++;
                 }
-                h->ring_wait_us += sum / G;
-                h->ring_wait_max_us += mx;
-            }
             h->phase_n += NL;
             cudaMemsetAsync(h->mega_trace, 0, st.size() * 8, h->st);
         }
@@ -948,7 +964,8 @@ TTS_API tts_bb_status tts_bb_debug_kv_read(tts_bb* h, int layer, int slot, int p
     {
         Launch L(h, K_KVCOPY);
         k_kv_copy<<<n, 256, 0, h->st>>>(h->pool + (size_t)layer * h->layer_elems, h->d_page_table, slot, h->mbps, pos0, n,
-                                        reinterpret_cast<bf16*>(k_out), reinterpret_cast<bf16*>(v_out), 0);
+                                        reinterpret_cast<bf16*>(k_out), reinterpret_cast<bf16*>(v_out), 0, h->kv_blocks,
+                                        h->err);
         L += 1;
     }
     return finish(h);
@@ -975,7 +992,7 @@ TTS_API tts_bb_status tts_bb_debug_kv_write(tts_bb* h, int layer, int slot, int 
         Launch L(h, K_KVCOPY);
         k_kv_copy<<<n, 256, 0, h->st>>>(h->pool + (size_t)layer * h->layer_elems, h->d_page_table, slot, h->mbps, pos0, n,
                                         const_cast<bf16*>(reinterpret_cast<const bf16*>(k)),
-                                        const_cast<bf16*>(reinterpret_cast<const bf16*>(v)), 1);
+                                        const_cast<bf16*>(reinterpret_cast<const bf16*>(v)), 1, h->kv_blocks, h->err);
         L += 1;
     }
     return finish(h);
@@ -992,9 +1009,10 @@ TTS_API tts_bb_status tts_bb_profile(tts_bb* h, int on) {
     h->phase_us.clear();
     h->phase_max_us.clear();
     h->phase_n = 0;
-    h->unit_n = 0;
-    h->unit_us[0] = h->unit_us[1] = h->unit_us[2] = 0;
-    h->ring_wait_us = h->ring_wait_max_us = 0;
+    h->sub_us.clear();
+    h->sub_n = 0;
+    h->unit_split[0] = h->unit_split[1] = 0;
+    h->unit_split_n[0] = h->unit_split_n[1] = 0;
     h->prof_on = on != 0;
     return TTS_BB_OK;
 }
@@ -1023,27 +1041,29 @@ TTS_API const char* tts_bb_profile_report(tts_bb* h) {
     }
     j += "]";
     if (h->phase_n > 0) {
-        static const char* names[12] = {"norm_qkv", "barrier_after_qkv", "attention", "barrier_after_attention",
-                                        "merge_attention", "o_proj", "barrier_after_o", "gate_up",
-                                        "barrier_after_gate_up", "down", "barrier_after_down", "next_layer_start"};
+        static const char* names[10] = {"wait_h_norm", "qkv", "attention_units", "wait_partials_merge", "o_proj",
+                                        "wait_h_norm2", "gate_up_swiglu", "wait_m", "down", "to_next_layer"};
         j += ", \"persistent_phases_us_per_layer\": {";
-        for (int i = 0; i < 12; ++i) {
+        for (int i = 0; i < 10; ++i) {
             char buf[160];
             snprintf(buf, sizeof buf, "%s\"%s\": {\"mean\": %.3f, \"max\": %.3f}", i ? ", " : "", names[i],
                      h->phase_us[i] / h->phase_n, h->phase_max_us[i] / h->phase_n);
             j += buf;
         }
         j += "}";
-        {
-            char buf[160];
-            snprintf(buf, sizeof buf, ", \"ring_wait_us_per_layer\": {\"mean\": %.3f, \"max\": %.3f}",
-                     h->ring_wait_us / h->phase_n, h->ring_wait_max_us / h->phase_n);
+        if (h->unit_split_n[0] + h->unit_split_n[1]) {
+            char buf[200];
+            snprintf(buf, sizeof buf, ", \"attention_phase_us\": {\"ctas_without_unit\": %.3f, \"ctas_with_units\": %.3f, \"share_with\": %.3f}",
+                     h->unit_split_n[0] ? h->unit_split[0] / h->unit_split_n[0] : 0.0,
+                     h->unit_split_n[1] ? h->unit_split[1] / h->unit_split_n[1] : 0.0,
+                     (double)h->unit_split_n[1] / (h->unit_split_n[0] + h->unit_split_n[1]));
             j += buf;
         }
-        if (h->unit_n) {
-            char buf[200];
-            snprintf(buf, sizeof buf, ", \"attention_unit_us\": {\"stage_q_kv\": %.3f, \"scores_pv\": %.3f, \"merge\": %.3f}",
-                     h->unit_us[0] / h->unit_n, h->unit_us[1] / h->unit_n, h->unit_us[2] / h->unit_n);
+        if (h->sub_n) {
+            char buf[256];
+            snprintf(buf, sizeof buf, ", \"gate_up_chunks_us\": {\"wait0\": %.3f, \"math0\": %.3f, \"reduce_store0\": %.3f, "
+                     "\"wait1\": %.3f, \"math1\": %.3f}", h->sub_us[0] / h->sub_n, h->sub_us[1] / h->sub_n,
+                     h->sub_us[2] / h->sub_n, h->sub_us[3] / h->sub_n, h->sub_us[4] / h->sub_n);
             j += buf;
         }
     }

@@ -1,0 +1,883 @@
+// Persistent small-batch decode step (B <= 2) with flag-in-data exchanges.
+//
+// One cooperative launch, one CTA per SM, runs the whole 28-layer step. Each
+// CTA owns fixed row slices of every weight matrix; a producer warp streams
+// them (cp.async.bulk + mbarriers) into a shared-memory ring that runs ahead
+// of the eight consumer warps. Between the dependent phases of a layer the
+// CTAs exchange vectors through global memory in 8-byte words that carry the
+// value and an epoch tag together: a reader polls the words it needs until
+// every tag shows the current epoch, so one exchange costs one write-to-read
+// latency instead of a grid barrier plus a read round trip. Per layer:
+//   h (all rows)  -> norm -> QKV rows          -> q/k/v words
+//   q/k/v of one KV head group -> attention unit (one cache block) -> partial words
+//   all partials  -> merge -> o_proj rows       -> own residual rows -> h words
+//   h (all rows)  -> norm -> gate/up rows       -> SwiGLU words
+//   SwiGLU (all)  -> down rows                  -> own residual rows -> h words
+// Exchange buffers alternate by layer parity; epochs grow monotonically across
+// launches (the host passes the base), so stale words never match. Each CTA
+// keeps its own residual rows on chip. Every wait is bounded: on timeout the
+// kernel raises the error word and a shared abort flag, after which all waits
+// return at once and the kernel runs to its end.
+#include "mega.cuh"
+
+namespace ttsbb {
+
+namespace ll {
+constexpr int NCW = 8;
+constexpr int NCT = NCW * 32;
+constexpr int NT = NCT + 32;
+constexpr int RING = 176 * 1024;
+constexpr int NSLOT = 16;
+constexpr int CHUNK = 32 * 1024;
+constexpr int XS_FLOATS = mk::MAXB * 3072;
+constexpr int OWN_MAX = 32;                 // own residual rows per CTA (>= ceil(1024 / G) rounded to pairs)
+constexpr int MAXSPLIT = 64;                // cache blocks per sequence (4096 tokens)
+constexpr int ATT_UNIT = NCW * (2 * HD + 4) + 2 * HD;
+constexpr int ATT_MERGE = 2 * mk::MAXB * NQ * MAXSPLIT;
+constexpr int ATT_FLOATS = ATT_UNIT > ATT_MERGE ? ATT_UNIT : ATT_MERGE;
+constexpr int SMEM = RING + XS_FLOATS * 4 + mk::MAXB * OWN_MAX * 4 + ATT_FLOATS * 4 + 2 * NSLOT * 8 + 64;
+constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
+}  // namespace ll
+
+// ---------------------------------------------------------------- small PTX helpers
+__device__ __forceinline__ uint32_t l_su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ unsigned long long l_time() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void l_mbar_init(uint64_t* b, int count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(l_su32(b)), "r"(count));
+}
+__device__ __forceinline__ bool l_mbar_try(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(l_su32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void l_named_sync() { asm volatile("bar.sync 1, %0;" ::"n"(ll::NCT) : "memory"); }
+
+__device__ __forceinline__ bool l_aborted(const MegaArgs& a) { return *reinterpret_cast<volatile int*>(a.abort_flag) != 0; }
+__device__ __forceinline__ void l_raise(const MegaArgs& a) {
+    set_err(a.err, ERR_TIMEOUT);
+    atomicExch(a.abort_flag, 1);
+}
+
+__device__ __forceinline__ bool l_mbar_wait(uint64_t* b, uint32_t parity, const MegaArgs& a) {
+    if (l_mbar_try(b, parity)) return true;
+    const unsigned long long t0 = l_time();
+    for (uint32_t i = 0;; ++i) {
+        if (l_mbar_try(b, parity)) return true;
+        if ((i & 63) == 63) {
+            if (l_aborted(a)) return false;
+            if (l_time() - t0 > ll::TIMEOUT_NS) { l_raise(a); return false; }
+        }
+    }
+}
+
+// 8-byte exchange word: low 32 bits the float, high 32 bits the epoch.
+__device__ __forceinline__ void ll_put(unsigned long long* p, float v, uint32_t ep) {
+    const unsigned long long w = ((unsigned long long)ep << 32) | (unsigned long long)__float_as_uint(v);
+    asm volatile("st.global.cg.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ unsigned long long ll_ld(const unsigned long long* p) {
+    unsigned long long w;
+    asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+__device__ __forceinline__ void ll_ld2(const unsigned long long* p, unsigned long long& w0, unsigned long long& w1) {
+    asm volatile("ld.global.cg.v2.u64 {%0, %1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(p) : "memory");
+}
+// Wait until words w[0..n) (loaded from p[0..n)) all carry epoch ep: the
+// caller issues every load first, so one exchange costs one round trip;
+// stale words are reloaded individually (bounded).
+template <int N>
+__device__ __forceinline__ void ll_settle(unsigned long long (&w)[N], const unsigned long long* const (&p)[N], uint32_t ep,
+                                          const MegaArgs& a) {
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < N; ++i) ok &= (uint32_t)(w[i] >> 32) == ep;
+    if (ok) return;
+    // Back off, then watch one stale word only (thousands of threads poll the
+    // same lines: keep the request rate low so the writers' stores get through);
+    // once it turns, reload every word that was stale.
+    const unsigned long long t0 = l_time();
+    for (uint32_t it = 0;; ++it) {
+        __nanosleep(it < 4 ? 128 : 256);
+        int first = -1;
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (first < 0 && (uint32_t)(w[i] >> 32) != ep) first = i;
+        unsigned long long probe = 0;
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (i == first) probe = ll_ld(p[i]);
+        if ((uint32_t)(probe >> 32) == ep) {
+            ok = true;
+#pragma unroll
+            for (int i = 0; i < N; ++i)
+                if ((uint32_t)(w[i] >> 32) != ep) {
+                    w[i] = ll_ld(p[i]);
+                    ok &= (uint32_t)(w[i] >> 32) == ep;
+                }
+            if (ok) return;
+        }
+        if ((it & 15) == 15) {
+            if (l_aborted(a)) return;
+            if (l_time() - t0 > ll::TIMEOUT_NS) { l_raise(a); return; }
+        }
+    }
+}
+__device__ __forceinline__ float ll_val(unsigned long long w) { return __uint_as_float((uint32_t)w); }
+
+// ---------------------------------------------------------------- schedule (same as the producer)
+struct LOp {
+    const bf16* W;
+    int N, K;
+};
+__device__ __forceinline__ LOp l_op(const MegaArgs& a, int l, int o) {
+    if (l == a.n_layers) return {a.head, a.head_rows, HID};
+    const MegaLayer& L = a.L[l];
+    switch (o) {
+        case 0: return {L.wqkv, QKV, HID};
+        case 1: return {L.wo, HID, NQ * HD};
+        case 2: return {L.wgu, 2 * a.ffn, HID};
+        default: return {L.wd, HID, a.ffn};
+    }
+}
+__device__ __forceinline__ void l_rows(int N, int c, int G, int& r0, int& r1) {
+    const long pairs = N / 2;
+    r0 = (int)(pairs * c / G) * 2;
+    r1 = (int)(pairs * (c + 1) / G) * 2;
+}
+__device__ __forceinline__ int l_rpc(int K) {
+    int r = ll::CHUNK / (K * 2);
+    r &= ~1;
+    return r < 2 ? 2 : (r > 16 ? 16 : r);
+}
+struct LRing {
+    unsigned long long head = 0;
+    uint32_t k = 0;
+    __device__ __forceinline__ uint32_t place(uint32_t bytes) {
+        uint32_t p = (uint32_t)(head % ll::RING);
+        if (p + bytes > (uint32_t)ll::RING) {
+            head += ll::RING - p;
+            p = 0;
+        }
+        head += bytes;
+        return p;
+    }
+};
+
+// Exchange buffers inside MegaArgs::xbuf (unsigned long long words):
+//   h : [2][MAXB][HID]     q/k/v : [2][MAXB][QKV]     m : [2][MAXB][3072]
+//   part : [2][MAXB][16][nblk_max][132]
+struct XBufs {
+    unsigned long long *h, *q, *m, *p;
+};
+__device__ __forceinline__ XBufs l_bufs(const MegaArgs& a) {
+    XBufs x;
+    x.h = a.xbuf;
+    x.q = x.h + 2 * mk::MAXB * HID;
+    x.m = x.q + 2 * mk::MAXB * QKV;
+    x.p = x.m + 2 * mk::MAXB * 3072;
+    return x;
+}
+
+// Epoch of each exchange: h version v (0 = layer-0 input, 2l+1 after o_proj, 2l+2 after down).
+__device__ __forceinline__ uint32_t ep_h(const MegaArgs& a, int v) { return a.ep_base + 3u * (uint32_t)v; }
+__device__ __forceinline__ uint32_t ep_q(const MegaArgs& a, int l) { return a.ep_base + 6u * (uint32_t)l + 1u; }
+__device__ __forceinline__ uint32_t ep_p(const MegaArgs& a, int l) { return a.ep_base + 6u * (uint32_t)l + 2u; }
+__device__ __forceinline__ uint32_t ep_m(const MegaArgs& a, int l) { return a.ep_base + 6u * (uint32_t)l + 4u; }
+
+// ---------------------------------------------------------------- consumer pieces
+// xs[b][k] = rmsnorm(h_v[b]) * gamma, h read from the exchange words of version v.
+__device__ __forceinline__ void l_stage_norm(const MegaArgs& a, const unsigned long long* hx, uint32_t ep,
+                                             const bf16* gamma, float* xs, float* red) {
+    const int t = threadIdx.x;
+    // thread t: elements 4t..4t+3 of each token row (B <= 2: all loads issued before any check)
+    unsigned long long w[2 * 4];
+    const unsigned long long* p[2 * 4];
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p[b * 4 + e] = hx + (size_t)min(b, a.B - 1) * HID + t * 4 + e;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        ll_ld2(p[b * 4], w[b * 4], w[b * 4 + 1]);
+        ll_ld2(p[b * 4 + 2], w[b * 4 + 2], w[b * 4 + 3]);
+    }
+    ll_settle(w, p, ep, a);
+    const uint2 gr = *reinterpret_cast<const uint2*>(gamma + t * 4);
+    const float g4[4] = {__uint_as_float(gr.x << 16), __uint_as_float(gr.x & 0xFFFF0000u),
+                         __uint_as_float(gr.y << 16), __uint_as_float(gr.y & 0xFFFF0000u)};
+    for (int b = 0; b < a.B; ++b) {
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float v = ll_val(w[b * 4 + e]);
+            ss += v * v;
+            xs[b * HID + t * 4 + e] = v * g4[e];
+        }
+        ss = warp_sum(ss);
+        if ((t & 31) == 0) red[b * ll::NCW + (t >> 5)] = ss;
+    }
+    l_named_sync();
+    for (int b = 0; b < a.B; ++b) {
+        float ss = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < ll::NCW; ++wi) ss += red[b * ll::NCW + wi];
+        const float r = rsqrtf(ss * (1.f / HID) + a.eps);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) xs[b * HID + t * 4 + e] *= r;
+    }
+}
+
+// Partial dot products of weight rows lr0, lr0+1 (of a chunk in shared
+// memory) with the staged activations: lane holds 16-byte column vectors
+// lane, lane+32, ...; NV vectors per lane. All shared loads of a row are
+// issued before its FMAs, which run as 4 independent chains per row.
+template <int B, int NV>
+__device__ __forceinline__ void l_rows_dot(const bf16* wc, const float* xs, int K, int lr0, int nr, int lane,
+                                           float (&acc)[2][B]) {
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int b = 0; b < B; ++b) acc[rr][b] = 0.f;
+    if (lr0 >= nr) return;
+    const bool two = lr0 + 1 < nr;
+    float part[2][B][4];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int b = 0; b < B; ++b)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) part[rr][b][q] = 0.f;
+    constexpr int U = NV < 4 ? NV : 4;
+#pragma unroll
+    for (int i0 = 0; i0 < NV; i0 += U) {
+        uint4 w[2][U];
+        float4 x[B][U][2];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int col = ((i0 + u) * 32 + lane) * 8;
+            w[0][u] = *reinterpret_cast<const uint4*>(wc + (size_t)lr0 * K + col);
+            w[1][u] = two ? *reinterpret_cast<const uint4*>(wc + (size_t)(lr0 + 1) * K + col) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                x[b][u][0] = *reinterpret_cast<const float4*>(xs + b * K + col);
+                x[b][u][1] = *reinterpret_cast<const float4*>(xs + b * K + col + 4);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                float wf[8];
+                unpack8(w[rr][u], wf);
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    const float xf[8] = {x[b][u][0].x, x[b][u][0].y, x[b][u][0].z, x[b][u][0].w,
+                                         x[b][u][1].x, x[b][u][1].y, x[b][u][1].z, x[b][u][1].w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) part[rr][b][j & 3] = fmaf(wf[j], xf[j], part[rr][b][j & 3]);
+                }
+            }
+    }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int b = 0; b < B; ++b) acc[rr][b] = (part[rr][b][0] + part[rr][b][1]) + (part[rr][b][2] + part[rr][b][3]);
+}
+
+// Consume this CTA's chunks of one op; results go to `sink` per (b, row, value).
+template <int B, typename Sink>
+__device__ __forceinline__ void l_consume(const MegaArgs& a, int l, int o, LRing& ring, unsigned char* ring_mem,
+                                          uint64_t* full, uint64_t* empty, const float* xs, Sink sink) {
+    const LOp d = l_op(a, l, o);
+    int r0, r1;
+    l_rows(d.N, blockIdx.x, gridDim.x, r0, r1);
+    const int rpc = l_rpc(d.K);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nv = d.K / 256;
+    const bool sub = a.trace && o == 2 && l < a.n_layers && threadIdx.x == 0;
+    unsigned long long* st = sub ? a.trace + ((size_t)blockIdx.x * a.n_layers + l) * 16 : nullptr;
+    int ci = 0;
+    for (int rc = r0; rc < r1; rc += rpc, ++ci) {
+        const int nr = min(rpc, r1 - rc);
+        const uint32_t bytes = (uint32_t)nr * d.K * 2;
+        const uint32_t p = ring.place(bytes);
+        const uint32_t slot = ring.k % ll::NSLOT, par = (ring.k / ll::NSLOT) & 1;
+        ring.k++;
+        l_mbar_wait(full + slot, par, a);
+        if (sub && ci < 2) st[10 + 3 * ci] = l_time();
+        const bf16* wc = reinterpret_cast<const bf16*>(ring_mem + p);
+        float acc[2][B];
+        const int lr0 = 2 * warp;
+        if (d.K == 1024)
+            l_rows_dot<B, 4>(wc, xs, d.K, lr0, nr, lane, acc);
+        else if (d.K == 2048)
+            l_rows_dot<B, 8>(wc, xs, d.K, lr0, nr, lane, acc);
+        else
+            l_rows_dot<B, 12>(wc, xs, d.K, lr0, nr, lane, acc);
+        __syncwarp();
+        if (sub && ci < 2) st[11 + 3 * ci] = l_time();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(l_su32(empty + slot)) : "memory");
+        if (lr0 < nr) {
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                for (int b = 0; b < B; ++b) acc[rr][b] = warp_sum(acc[rr][b]);
+            if (lane == 0) {
+#pragma unroll
+                for (int b = 0; b < B; ++b) sink(b, rc + lr0, acc[0][b], (lr0 + 1 < nr), acc[1][b], r0);
+            }
+        }
+        if (sub && ci == 0) st[12] = l_time();
+    }
+}
+
+// q/k RMSNorm + RoPE of one head, 4 elements per lane (RoPE partner lane ^ 16);
+// g4 = the lane's 4 gains, c4 / s4 = its 4 cos / sin table entries.
+__device__ __forceinline__ void l_norm_rope4(float* v, const float* g4, const float4& c4, const float4& s4,
+                                             const MegaArgs& a, int lane) {
+    const float ss = warp_sum(v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3]);
+    const float r = rsqrtf(ss * (1.f / HD) + a.eps);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = v[e] * r * g4[e];
+    float p[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) p[e] = __shfl_xor_sync(0xffffffffu, v[e], 16);
+    const float ct[4] = {c4.x, c4.y, c4.z, c4.w}, st[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = (lane < 16) ? (v[e] * ct[e] - p[e] * st[e]) : (v[e] * ct[e] + p[e] * st[e]);
+}
+__device__ __forceinline__ void l_gain4(const bf16* gamma, int lane, float* g4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(gamma + lane * 4);
+    g4[0] = __uint_as_float(u.x << 16); g4[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    g4[2] = __uint_as_float(u.y << 16); g4[3] = __uint_as_float(u.y & 0xFFFF0000u);
+}
+
+// Attention unit (b, g, block j): K/V of the block's old keys are loaded
+// before the q/k/v words are polled; the owner of the last block also appends
+// the new token. Writes the block's softmax partial words for heads 2g, 2g+1.
+__device__ __forceinline__ void l_attn_unit(const MegaArgs& a, const XBufs& X, int l, int b, int g, int j, float* att) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pos = a.pos[b], L = pos + 1;
+    const int nblk = (L + KVB - 1) / KVB;
+    const bool last = (j == nblk - 1);
+    const int phys = last ? a.last_phys[b] : __ldcg(a.page_table + (size_t)a.slot[b] * a.mbps + j);
+    bf16* kb = a.pool + (size_t)l * a.layer_elems + ((size_t)phys * 2 * NKV + g) * KVB * HD;
+    bf16* vb = kb + (size_t)NKV * KVB * HD;
+    // old keys of this warp (keys 8w..8w+7 of the block), loaded ahead of the q/k/v exchange
+    const int key0 = j * KVB + warp * 8;
+    uint2 kr[8], vr[8];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const bool ok = key0 + kk < pos;  // the new token (position pos) comes from the exchange
+        kr[kk] = ok ? __ldcg(reinterpret_cast<const uint2*>(kb + (size_t)(warp * 8 + kk) * HD + lane * 4)) : make_uint2(0u, 0u);
+        vr[kk] = ok ? __ldcg(reinterpret_cast<const uint2*>(vb + (size_t)(warp * 8 + kk) * HD + lane * 4)) : make_uint2(0u, 0u);
+    }
+    float* sq = att + ll::NCW * (2 * HD + 4);  // [2][HD] scaled queries
+    const unsigned long long* qx = X.q + ((size_t)(l & 1) * mk::MAXB + b) * QKV;
+    const uint32_t eq = ep_q(a, l);
+    __shared__ uint2 newk[HD / 4], newv[HD / 4];
+    // inputs that do not depend on the exchange: gains and this position's RoPE entries
+    float g4[4];
+    l_gain4(warp < 2 ? a.L[l].qn : a.L[l].kn, lane, g4);
+    const float4 c4 = *reinterpret_cast<const float4*>(a.cos_t + (size_t)pos * (HD / 2) + (lane & 15) * 4);
+    const float4 s4 = *reinterpret_cast<const float4*>(a.sin_t + (size_t)pos * (HD / 2) + (lane & 15) * 4);
+    auto poll4 = [&](const unsigned long long* src, float* v) {
+        unsigned long long w[4];
+        const unsigned long long* p[4] = {src, src + 1, src + 2, src + 3};
+        ll_ld2(src, w[0], w[1]);
+        ll_ld2(src + 2, w[2], w[3]);
+        ll_settle(w, p, eq, a);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = ll_val(w[e]);
+    };
+    if (warp < 2) {
+        float v[4];
+        poll4(qx + (2 * g + warp) * HD + lane * 4, v);
+        l_norm_rope4(v, g4, c4, s4, a, lane);
+        const float sc = rsqrtf((float)HD) * 1.4426950408889634f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sq[warp * HD + lane * 4 + e] = v[e] * sc;
+    } else if (warp == 2 && last) {
+        float v[4];
+        poll4(qx + NQ * HD + g * HD + lane * 4, v);
+        l_norm_rope4(v, g4, c4, s4, a, lane);
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]), p1 = __floats2bfloat162_rn(v[2], v[3]);
+        uint2 o;
+        o.x = *reinterpret_cast<uint32_t*>(&p0);
+        o.y = *reinterpret_cast<uint32_t*>(&p1);
+        *reinterpret_cast<uint2*>(kb + (size_t)(pos % KVB) * HD + lane * 4) = o;
+        newk[lane] = o;
+    } else if (warp == 3 && last) {
+        float v[4];
+        poll4(qx + NQ * HD + NKV * HD + g * HD + lane * 4, v);
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]), p1 = __floats2bfloat162_rn(v[2], v[3]);
+        uint2 o;
+        o.x = *reinterpret_cast<uint32_t*>(&p0);
+        o.y = *reinterpret_cast<uint32_t*>(&p1);
+        *reinterpret_cast<uint2*>(vb + (size_t)(pos % KVB) * HD + lane * 4) = o;
+        newv[lane] = o;
+    }
+    l_named_sync();
+    if (last && key0 <= pos && pos < key0 + 8) {  // this warp holds the new token's slot
+        kr[pos - key0] = newk[lane];
+        vr[pos - key0] = newv[lane];
+    }
+    float q0[4], q1[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) { q0[e] = sq[lane * 4 + e]; q1[e] = sq[HD + lane * 4 + e]; }
+    float d[16];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const float k0 = __uint_as_float(kr[kk].x << 16), k1 = __uint_as_float(kr[kk].x & 0xFFFF0000u);
+        const float k2 = __uint_as_float(kr[kk].y << 16), k3 = __uint_as_float(kr[kk].y & 0xFFFF0000u);
+        d[kk] = q0[0] * k0 + q0[1] * k1 + q0[2] * k2 + q0[3] * k3;
+        d[8 + kk] = q1[0] * k0 + q1[1] * k1 + q1[2] * k2 + q1[3] * k3;
+    }
+#pragma unroll
+    for (int s = 8; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = upper ? d[i] : d[i + s];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, s);
+            d[i] = (upper ? d[i + s] : d[i]) + recv;
+        }
+    }
+    d[0] += __shfl_xor_sync(0xffffffffu, d[0], 16);
+    const int kk0 = lane & 7;
+    const float score = (key0 + kk0 < L) ? d[0] : -INFINITY;
+    float mx = score;
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    const float pr = (mx == -INFINITY) ? 0.f : exp2f(score - mx);
+    float ps = pr;
+    ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+    ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+    ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+    const float m0 = __shfl_sync(0xffffffffu, mx, 0), m1 = __shfl_sync(0xffffffffu, mx, 8);
+    const float l0 = __shfl_sync(0xffffffffu, ps, 0), l1 = __shfl_sync(0xffffffffu, ps, 8);
+    float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k2 = 0; k2 < 8; ++k2) {
+        const float p0 = __shfl_sync(0xffffffffu, pr, k2), p1 = __shfl_sync(0xffffffffu, pr, 8 + k2);
+        const float v0 = __uint_as_float(vr[k2].x << 16), v1 = __uint_as_float(vr[k2].x & 0xFFFF0000u);
+        const float v2 = __uint_as_float(vr[k2].y << 16), v3 = __uint_as_float(vr[k2].y & 0xFFFF0000u);
+        o0[0] += p0 * v0; o0[1] += p0 * v1; o0[2] += p0 * v2; o0[3] += p0 * v3;
+        o1[0] += p1 * v0; o1[1] += p1 * v1; o1[2] += p1 * v2; o1[3] += p1 * v3;
+    }
+    float* wml = att + warp * (2 * HD + 4);
+    if (lane == 0) { wml[2 * HD] = m0; wml[2 * HD + 1] = l0; wml[2 * HD + 2] = m1; wml[2 * HD + 3] = l1; }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) { wml[lane * 4 + e] = o0[e]; wml[HD + lane * 4 + e] = o1[e]; }
+    l_named_sync();
+    {
+        const int t = threadIdx.x, h2 = t >> 7, e = t & 127;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < ll::NCW; ++w) M = fmaxf(M, att[w * (2 * HD + 4) + 2 * HD + 2 * h2]);
+        float lsum = 0.f, acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < ll::NCW; ++w) {
+            const float* ww = att + w * (2 * HD + 4);
+            const float mw = ww[2 * HD + 2 * h2];
+            const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+            lsum += ww[2 * HD + 2 * h2 + 1] * f;
+            acc += ww[h2 * HD + e] * f;
+        }
+        unsigned long long* dst =
+            X.p + ((((size_t)(l & 1) * mk::MAXB + b) * NQ + 2 * g + h2) * a.nblk_max + j) * PART_STRIDE;
+        const uint32_t ep = ep_p(a, l);
+        ll_put(dst + e, acc, ep);
+        if (e == 0) { ll_put(dst + HD, M, ep); ll_put(dst + HD + 1, lsum, ep); }
+    }
+    l_named_sync();
+}
+
+// xs[b][h*128 + e] = merge of the block partial words of (b, h) in block order.
+// Thread (b, h, 4 outputs) loads, for up to 8 blocks at a time, the block's
+// running max / sum and its 4 outputs together, waits once, and combines.
+__device__ __forceinline__ void l_stage_attn(const MegaArgs& a, const XBufs& X, int l, float* xs) {
+    const uint32_t ep = ep_p(a, l);
+    const unsigned long long* base = X.p + (size_t)(l & 1) * mk::MAXB * NQ * a.nblk_max * PART_STRIDE;
+    const int nbm = a.nblk_max;
+    for (int t = threadIdx.x; t < a.B * NQ * (HD / 4); t += ll::NCT) {
+        const int bh = t / (HD / 4), e4 = (t % (HD / 4)) * 4;
+        const int b = bh / NQ;
+        const int nblk = (a.pos[b] + 1 + KVB - 1) / KVB;
+        float M = -INFINITY, lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j0 = 0; j0 < nblk; j0 += 8) {
+            unsigned long long w[8 * 6];
+            const unsigned long long* p[8 * 6];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int j = min(j0 + jj, nblk - 1);
+                const unsigned long long* rec = base + ((size_t)bh * nbm + j) * PART_STRIDE;
+                p[jj * 6 + 0] = rec + HD;
+                p[jj * 6 + 1] = rec + HD + 1;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) p[jj * 6 + 2 + e] = rec + e4 + e;
+                ll_ld2(rec + HD, w[jj * 6 + 0], w[jj * 6 + 1]);
+                ll_ld2(rec + e4, w[jj * 6 + 2], w[jj * 6 + 3]);
+                ll_ld2(rec + e4 + 2, w[jj * 6 + 4], w[jj * 6 + 5]);
+            }
+            ll_settle(w, p, ep, a);
+            // online merge of these blocks (same result as max-then-sum, block order kept)
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                if (j0 + jj >= nblk) break;
+                const float mj = ll_val(w[jj * 6]), lj = ll_val(w[jj * 6 + 1]);
+                const float Mn = fmaxf(M, mj);
+                const float fo = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
+                const float fj = (mj == -INFINITY) ? 0.f : exp2f(mj - Mn);
+                lsum = lsum * fo + lj * fj;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] = acc[e] * fo + ll_val(w[jj * 6 + 2 + e]) * fj;
+                M = Mn;
+            }
+        }
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) xs[bh * HD + e4 + e] = acc[e] * inv;
+    }
+}
+
+// ---------------------------------------------------------------- the kernel
+template <int B>
+__global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__ MegaArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    unsigned char* ring_mem = smem;
+    float* xs = reinterpret_cast<float*>(smem + ll::RING);
+    float* hown = xs + ll::XS_FLOATS;                         // [B][OWN_MAX]
+    float* att = hown + mk::MAXB * ll::OWN_MAX;
+    uint64_t* full = reinterpret_cast<uint64_t*>(att + ll::ATT_FLOATS);
+    uint64_t* empty = full + ll::NSLOT;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < ll::NSLOT; ++i) {
+            l_mbar_init(full + i, 1);
+            l_mbar_init(empty + i, ll::NCW);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == ll::NCW) {
+        // ------------------------------------------------ producer: weight stream
+        if (lane == 0) {
+            LRing ring;
+            unsigned long long ends[ll::NSLOT];
+            unsigned long long tail = 0;
+            uint32_t consumed = 0;
+            bool ok = true;
+            for (int l = 0; l <= a.n_layers && ok; ++l) {
+                const int nops = (l == a.n_layers) ? (a.head ? 1 : 0) : 4;
+                for (int o = 0; o < nops && ok; ++o) {
+                    const LOp d = l_op(a, l, o);
+                    int r0, r1;
+                    l_rows(d.N, blockIdx.x, gridDim.x, r0, r1);
+                    const int rpc = l_rpc(d.K);
+                    for (int rc = r0; rc < r1 && ok; rc += rpc) {
+                        const int nr = min(rpc, r1 - rc);
+                        const uint32_t bytes = (uint32_t)nr * d.K * 2;
+                        const uint32_t k = ring.k;
+                        const uint32_t p = ring.place(bytes);
+                        while (ok && (k - consumed >= (uint32_t)ll::NSLOT ||
+                                      ring.head - tail > (unsigned long long)ll::RING)) {
+                            const uint32_t s = consumed % ll::NSLOT;
+                            ok = l_mbar_wait(empty + s, (consumed / ll::NSLOT) & 1, a);
+                            if (ok) { tail = ends[s]; ++consumed; }
+                        }
+                        if (!ok) break;
+                        const uint32_t slot = k % ll::NSLOT;
+                        ends[slot] = ring.head;
+                        ring.k++;
+                        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(l_su32(full + slot)),
+                                     "r"(bytes)
+                                     : "memory");
+                        asm volatile(
+                            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                                l_su32(ring_mem + p)),
+                            "l"(d.W + (size_t)rc * d.K), "r"(bytes), "r"(l_su32(full + slot))
+                            : "memory");
+                    }
+                }
+            }
+            while (consumed < ring.k) {  // every copy must land before the CTA leaves
+                const uint32_t s = consumed % ll::NSLOT;
+                if (ok) {
+                    if (!l_mbar_wait(empty + s, (consumed / ll::NSLOT) & 1, a)) ok = false;
+                } else {
+                    const unsigned long long t0 = l_time();
+                    while (!l_mbar_try(full + s, (consumed / ll::NSLOT) & 1) && l_time() - t0 < ll::TIMEOUT_NS) {
+                    }
+                }
+                ++consumed;
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumers
+    const XBufs X = l_bufs(a);
+    LRing ring;
+    int own0, own1;
+    l_rows(HID, blockIdx.x, gridDim.x, own0, own1);
+    const int t = threadIdx.x;
+#define LSTAMP(i)                                                                                 \
+    do {                                                                                          \
+        if (a.trace && t == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * 16 + (i)] = l_time(); \
+    } while (0)
+
+    // page-table entries of blocks opened by this step (read by later launches)
+    if (blockIdx.x == 0 && t < a.n_upd) const_cast<int32_t*>(a.page_table)[a.upd_idx[t]] = a.upd_val[t];
+    // layer-0 input: every CTA sums the embeddings itself; own rows are kept
+    for (int b = 0; b < B; ++b) {
+        for (int c = t * 4; c < HID; c += ll::NCT * 4) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            if (a.embeds) {
+                const uint2 u = *reinterpret_cast<const uint2*>(a.embeds + (size_t)b * HID + c);
+                acc[0] = __uint_as_float(u.x << 16); acc[1] = __uint_as_float(u.x & 0xFFFF0000u);
+                acc[2] = __uint_as_float(u.y << 16); acc[3] = __uint_as_float(u.y & 0xFFFF0000u);
+            }
+            if (a.ids) {
+                for (int k = 0; k < a.tabs.n; ++k) {
+                    const int id = a.ids[b * a.tabs.n + k];
+                    if (id == -1) continue;
+                    if (id < -1 || id >= a.tabs.rows[k]) {
+                        if (blockIdx.x == 0 && c == 0) set_err(a.err, ERR_BAD_ID);
+                        continue;
+                    }
+                    const uint2 u = *reinterpret_cast<const uint2*>(a.tabs.tab[k] + (size_t)id * HID + c);
+                    acc[0] += __uint_as_float(u.x << 16); acc[1] += __uint_as_float(u.x & 0xFFFF0000u);
+                    acc[2] += __uint_as_float(u.y << 16); acc[3] += __uint_as_float(u.y & 0xFFFF0000u);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                xs[b * HID + c + e] = acc[e];
+                if (c + e >= own0 && c + e < own1) hown[b * ll::OWN_MAX + (c + e - own0)] = acc[e];
+            }
+        }
+    }
+    l_named_sync();
+    // norm of the layer-0 input straight from shared memory
+    {
+        float* red = att;
+        for (int b = 0; b < B; ++b) {
+            float ss = 0.f;
+            for (int c = t; c < HID; c += ll::NCT) ss += xs[b * HID + c] * xs[b * HID + c];
+            ss = warp_sum(ss);
+            if (lane == 0) red[b * ll::NCW + warp] = ss;
+        }
+        l_named_sync();
+        for (int b = 0; b < B; ++b) {
+            float ss = 0.f;
+#pragma unroll
+            for (int w = 0; w < ll::NCW; ++w) ss += red[b * ll::NCW + w];
+            const float r = rsqrtf(ss * (1.f / HID) + a.eps);
+            for (int c = t; c < HID; c += ll::NCT) xs[b * HID + c] *= r * bf2f(a.L[0].in_norm[c]);
+        }
+    }
+    l_named_sync();
+
+    for (int l = 0; l < a.n_layers; ++l) {
+        LSTAMP(0);
+        unsigned long long* hx_prev = X.h + (size_t)((2 * l) & 1) * mk::MAXB * HID;
+        if (l > 0) {
+            l_stage_norm(a, hx_prev, ep_h(a, 2 * l), a.L[l].in_norm, xs, att);
+            l_named_sync();
+        }
+        LSTAMP(1);
+        // ---- QKV rows -> q/k/v words
+        {
+            unsigned long long* qx = X.q + (size_t)(l & 1) * mk::MAXB * QKV;
+            const uint32_t eq = ep_q(a, l);
+            l_consume<B>(a, l, 0, ring, ring_mem, full, empty, xs,
+                         [&](int b, int row, float v0, bool two, float v1, int) {
+                             ll_put(qx + (size_t)b * QKV + row, v0, eq);
+                             if (two) ll_put(qx + (size_t)b * QKV + row + 1, v1, eq);
+                         });
+        }
+        LSTAMP(2);
+        // ---- attention units
+        {
+            int u = 0;
+            for (int b = 0; b < B; ++b) {
+                const int nblk = (a.pos[b] + 1 + KVB - 1) / KVB;
+                for (int g = 0; g < NKV; ++g)
+                    for (int j = 0; j < nblk; ++j, ++u)
+                        if (u % (int)gridDim.x == (int)blockIdx.x) {
+                            l_attn_unit(a, X, l, b, g, j, att);
+                            if (a.trace && t == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * 16 + 15] += 1;
+                        }
+            }
+        }
+        LSTAMP(3);
+        // ---- merge + o_proj + residual (own rows) -> h words (version 2l+1)
+        l_stage_attn(a, X, l, xs);
+        l_named_sync();
+        LSTAMP(4);
+        l_consume<B>(a, l, 1, ring, ring_mem, full, empty, xs,
+                     [&](int b, int row, float v0, bool two, float v1, int r0) {
+                         hown[b * ll::OWN_MAX + row - r0] += v0;
+                         if (two) hown[b * ll::OWN_MAX + row + 1 - r0] += v1;
+                     });
+        l_named_sync();
+        {
+            unsigned long long* hx = X.h + (size_t)((2 * l + 1) & 1) * mk::MAXB * HID;
+            const uint32_t eh = ep_h(a, 2 * l + 1);
+            for (int i = t; i < B * (own1 - own0); i += ll::NCT) {
+                const int b = i / (own1 - own0), r = i % (own1 - own0);
+                ll_put(hx + (size_t)b * HID + own0 + r, hown[b * ll::OWN_MAX + r], eh);
+            }
+        }
+        LSTAMP(5);
+        // ---- gate/up + SwiGLU -> m words
+        l_stage_norm(a, X.h + (size_t)((2 * l + 1) & 1) * mk::MAXB * HID, ep_h(a, 2 * l + 1), a.L[l].post_norm, xs, att);
+        l_named_sync();
+        LSTAMP(6);
+        {
+            unsigned long long* mx = X.m + (size_t)(l & 1) * mk::MAXB * 3072;
+            const uint32_t em = ep_m(a, l);
+            l_consume<B>(a, l, 2, ring, ring_mem, full, empty, xs,
+                         [&](int b, int row, float g, bool, float u, int) {
+                             ll_put(mx + (size_t)b * 3072 + row / 2, g / (1.f + __expf(-g)) * u, em);
+                         });
+        }
+        LSTAMP(7);
+        // ---- down + residual (own rows) -> h words (version 2l+2)
+        {
+            const unsigned long long* mx = X.m + (size_t)(l & 1) * mk::MAXB * 3072;
+            const uint32_t em = ep_m(a, l);
+            // thread t: 12 consecutive values of each row (ffn 3072 / 256 threads), all loads first
+            for (int b = 0; b < B; ++b) {
+                unsigned long long w[12];
+                const unsigned long long* p[12];
+                const int c0 = t * 12;
+#pragma unroll
+                for (int e = 0; e < 12; e += 2) {
+                    p[e] = mx + (size_t)b * 3072 + min(c0 + e, a.ffn - 2);
+                    p[e + 1] = p[e] + 1;
+                    ll_ld2(p[e], w[e], w[e + 1]);
+                }
+                ll_settle(w, p, em, a);
+#pragma unroll
+                for (int e = 0; e < 12; ++e)
+                    if (c0 + e < a.ffn) xs[b * a.ffn + c0 + e] = ll_val(w[e]);
+            }
+        }
+        l_named_sync();
+        LSTAMP(8);
+        l_consume<B>(a, l, 3, ring, ring_mem, full, empty, xs,
+                     [&](int b, int row, float v0, bool two, float v1, int r0) {
+                         hown[b * ll::OWN_MAX + row - r0] += v0;
+                         if (two) hown[b * ll::OWN_MAX + row + 1 - r0] += v1;
+                     });
+        l_named_sync();
+        {
+            unsigned long long* hx = X.h + (size_t)((2 * l + 2) & 1) * mk::MAXB * HID;
+            const uint32_t eh = ep_h(a, 2 * l + 2);
+            for (int i = t; i < B * (own1 - own0); i += ll::NCT) {
+                const int b = i / (own1 - own0), r = i % (own1 - own0);
+                ll_put(hx + (size_t)b * HID + own0 + r, hown[b * ll::OWN_MAX + r], eh);
+                if (l == a.n_layers - 1) a.h[(size_t)b * HID + own0 + r] = hown[b * ll::OWN_MAX + r];
+            }
+        }
+        LSTAMP(9);
+    }
+#undef LSTAMP
+    // ---- final norm + head + argmax
+    if (a.head) {
+        const int vl = 2 * a.n_layers;
+        l_stage_norm(a, X.h + (size_t)(vl & 1) * mk::MAXB * HID, ep_h(a, vl), a.final_norm, xs, att);
+        l_named_sync();
+        __shared__ unsigned long long best_s[mk::MAXB];
+        if (t < B) best_s[t] = 0ull;
+        l_named_sync();
+        l_consume<B>(a, a.n_layers, 0, ring, ring_mem, full, empty, xs,
+                     [&](int b, int row, float v0, bool two, float v1, int) {
+                         if (a.logits) {
+                             a.logits[(size_t)b * a.head_rows + row] = v0;
+                             if (two) a.logits[(size_t)b * a.head_rows + row + 1] = v1;
+                         }
+                         unsigned long long pk = pack_argmax(v0, row);
+                         if (two) {
+                             const unsigned long long p1 = pack_argmax(v1, row + 1);
+                             pk = p1 > pk ? p1 : pk;
+                         }
+                         atomicMax(best_s + b, pk);
+                     });
+        l_named_sync();
+        if (a.argmax_out) {
+            __shared__ int last_s;
+            if (t == 0) {
+                for (int b = 0; b < B; ++b) atomicMax(a.amax + b, best_s[b]);
+                __threadfence();
+                const unsigned int old = atomicAdd(a.done, 1u);
+                last_s = (old == gridDim.x - 1);
+            }
+            l_named_sync();
+            if (last_s && t < B) {
+                __threadfence();
+                const unsigned long long best = atomicExch(a.amax + t, 0ull);  // read and re-arm for the next step
+                a.argmax_out[(size_t)t * a.argmax_stride] = (int32_t)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+            }
+            if (last_s && t == 0) atomicExch(a.done, 0u);
+        }
+    }
+}
+
+int ll_smem_bytes() { return ll::SMEM; }
+uint32_t ll_epochs_per_launch(int n_layers) { return 6u * (uint32_t)n_layers + 8u; }
+
+template <int B>
+static cudaError_t ll_launch_b(const MegaArgs& a, int grid, cudaStream_t st) {
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_decode_ll<B>, cudaFuncAttributeMaxDynamicSharedMemorySize, ll::SMEM);
+        attr = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(ll::NT);
+    cfg.dynamicSmemBytes = ll::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_decode_ll<B>, a);
+}
+
+cudaError_t launch_decode_ll(const MegaArgs& a, int grid, cudaStream_t st) {
+    switch (a.B) {
+        case 1: return ll_launch_b<1>(a, grid, st);
+        case 2: return ll_launch_b<2>(a, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+int ll_max_grid() {
+    int dev = 0, sms = 0, per = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaFuncSetAttribute(k_decode_ll<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, ll::SMEM);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_decode_ll<1>, ll::NT, ll::SMEM);
+    // own residual rows per CTA must fit OWN_MAX
+    if (per < 1 || (HID / 2 + sms - 1) / sms * 2 > ll::OWN_MAX) return 0;
+    return sms;
+}
+
+}  // namespace ttsbb

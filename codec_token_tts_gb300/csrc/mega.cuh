@@ -1,4 +1,4 @@
-// Persistent small-batch decode step (k_decode_mega.cu): argument block and launch API.
+// Persistent small-batch decode step (k_decode_ll.cu): argument block and launch API.
 #pragma once
 #include "common.cuh"
 
@@ -44,22 +44,27 @@ struct MegaArgs {
     float* part;               // [B][16][nblk_max][PART_STRIDE]
     int nblk_max;
     unsigned long long* amax;  // [B]
-    unsigned long long* bar;   // grid barrier counter (monotonic)
-    unsigned long long bar_base;
     int* abort_flag;
     int* err;
     const float* cos_t;
     const float* sin_t;
     float eps;
     int B, n_layers, ffn;
-    unsigned long long* trace; // optional: [grid][n_layers][12] globaltimer stamps of CTA phases
+    unsigned long long* trace; // optional: [grid][n_layers][16] globaltimer stamps of CTA phases
+    // flag-in-data exchange (k_decode_ll.cu)
+    unsigned long long* xbuf;  // exchange words (value | epoch << 32), zero-initialised
+    uint32_t ep_base;          // first epoch of this launch (grows by ll_epochs_per_launch)
+    int last_phys[mk::MAXB];   // physical block holding each sequence's new token
+    unsigned int* done;        // CTAs finished with the head (last one publishes the argmax)
 };
 
 // Launch one decode step on `grid` CTAs (cooperative: all co-resident or an error).
-cudaError_t launch_decode_mega(const MegaArgs& a, int grid, cudaStream_t st);
-// Grid barriers one launch performs; the host advances MegaArgs::bar_base by this times grid.
-int mega_barriers(int n_layers, bool head, bool argmax);
-// Largest cooperative grid (one CTA per SM), 0 if the kernel cannot run here.
-int mega_max_grid();
+cudaError_t launch_decode_ll(const MegaArgs& a, int grid, cudaStream_t st);
+int ll_max_grid();
+uint32_t ll_epochs_per_launch(int n_layers);
+// Exchange words the flag-in-data step needs for mbps cache blocks per sequence.
+inline size_t ll_xbuf_words(int mbps) {
+    return 2ull * mk::MAXB * (HID + QKV + 3072) + 2ull * mk::MAXB * NQ * (size_t)mbps * PART_STRIDE;
+}
 
 }  // namespace ttsbb
