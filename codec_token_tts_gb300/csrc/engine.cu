@@ -142,10 +142,8 @@ struct tts_bb {
     std::vector<double> phase_us;      // summed per-phase mean-over-CTA durations over traced layers
     std::vector<double> phase_max_us;  // summed per-phase max-over-CTA durations
     long phase_n = 0;                  // traced layers
-    std::vector<double> sub_us;        // gate/up sub-phases
     double unit_split[2] = {0, 0};
     long unit_split_n[2] = {0, 0};
-    long sub_n = 0;
 };
 
 namespace {
@@ -619,7 +617,7 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
         h->mega_grid = ll_max_grid();
         cudaGetLastError();
         if (const char* g = std::getenv("TTS_BB_DECODE_CTAS"))  // tuning knob: CTAs of the persistent step
-            h->mega_grid = std::max(0, std::min(h->mega_grid, std::atoi(g)));
+            h->mega_grid = std::max(std::min(h->mega_grid, LL_MIN_GRID), std::min(h->mega_grid, std::atoi(g)));
         if (h->mega_grid > 0) {
             const size_t xw = ll_xbuf_words(h->mbps);
             if ((e = dalloc(h, &h->mega_abort, 1)) != cudaSuccess ||
@@ -793,19 +791,6 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
                     }
                     h->phase_us[i] += sum / G;
                     h->phase_max_us[i] += mx;
-                }
-            // gate/up sub-phases (stamps 6, 10..14): ring wait, math, reduce + store of chunk 0; wait, math of chunk 1
-            if (h->sub_us.empty()) h->sub_us.assign(5, 0.0);
-            for (int l = 0; l < NL; ++l)
-                for (int g = 0; g < G; ++g) {
-                    const unsigned long long* r = &st[((size_t)g * NL + l) * NS];
-                    if (!r[10] || !r[14]) continue;
-                    h->sub_us[0] += (r[10] - r[6]) * 1e-3;
-                    h->sub_us[1] += (r[11] - r[10]) * 1e-3;
-                    h->sub_us[2] += (r[12] - r[11]) * 1e-3;
-                    h->sub_us[3] += (r[13] - r[12]) * 1e-3;
-                    h->sub_us[4] += (r[14] - r[13]) * 1e-3;
-                    h->sub_n++;
                 }
             // attention-unit phase (stamps 2 -> 3) split by whether the CTA ran a unit
             for (int l = 0; l < NL; ++l)
@@ -1009,8 +994,6 @@ TTS_API tts_bb_status tts_bb_profile(tts_bb* h, int on) {
     h->phase_us.clear();
     h->phase_max_us.clear();
     h->phase_n = 0;
-    h->sub_us.clear();
-    h->sub_n = 0;
     h->unit_split[0] = h->unit_split[1] = 0;
     h->unit_split_n[0] = h->unit_split_n[1] = 0;
     h->prof_on = on != 0;
@@ -1057,13 +1040,6 @@ TTS_API const char* tts_bb_profile_report(tts_bb* h) {
                      h->unit_split_n[0] ? h->unit_split[0] / h->unit_split_n[0] : 0.0,
                      h->unit_split_n[1] ? h->unit_split[1] / h->unit_split_n[1] : 0.0,
                      (double)h->unit_split_n[1] / (h->unit_split_n[0] + h->unit_split_n[1]));
-            j += buf;
-        }
-        if (h->sub_n) {
-            char buf[256];
-            snprintf(buf, sizeof buf, ", \"gate_up_chunks_us\": {\"wait0\": %.3f, \"math0\": %.3f, \"reduce_store0\": %.3f, "
-                     "\"wait1\": %.3f, \"math1\": %.3f}", h->sub_us[0] / h->sub_n, h->sub_us[1] / h->sub_n,
-                     h->sub_us[2] / h->sub_n, h->sub_us[3] / h->sub_n, h->sub_us[4] / h->sub_n);
             j += buf;
         }
     }

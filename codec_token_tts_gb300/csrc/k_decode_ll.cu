@@ -66,6 +66,27 @@ __device__ __forceinline__ void l_raise(const MegaArgs& a) {
     atomicExch(a.abort_flag, 1);
 }
 
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the
+// phase completes or the hint (ns) elapses, leaving issue slots to the consumers.
+__device__ __forceinline__ bool l_mbar_try_sleep(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(l_su32(b)), "r"(parity), "r"(20000u)
+        : "memory");
+    return ok != 0;
+}
+// Producer-side bounded wait (sleeping between checks).
+__device__ __forceinline__ bool l_mbar_wait_sleep(uint64_t* b, uint32_t parity, const MegaArgs& a) {
+    if (l_mbar_try(b, parity)) return true;
+    const unsigned long long t0 = l_time();
+    for (;;) {
+        if (l_mbar_try_sleep(b, parity)) return true;
+        if (l_aborted(a)) return false;
+        if (l_time() - t0 > ll::TIMEOUT_NS) { l_raise(a); return false; }
+    }
+}
 __device__ __forceinline__ bool l_mbar_wait(uint64_t* b, uint32_t parity, const MegaArgs& a) {
     if (l_mbar_try(b, parity)) return true;
     const unsigned long long t0 = l_time();
@@ -149,9 +170,9 @@ __device__ __forceinline__ LOp l_op(const MegaArgs& a, int l, int o) {
     }
 }
 __device__ __forceinline__ void l_rows(int N, int c, int G, int& r0, int& r1) {
-    const long pairs = N / 2;
-    r0 = (int)(pairs * c / G) * 2;
-    r1 = (int)(pairs * (c + 1) / G) * 2;
+    const unsigned pairs = (unsigned)N / 2;  // pairs * (c + 1) < 2^32 for every shape here
+    r0 = (int)(pairs * (unsigned)c / (unsigned)G) * 2;
+    r1 = (int)(pairs * (unsigned)(c + 1) / (unsigned)G) * 2;
 }
 __device__ __forceinline__ int l_rpc(int K) {
     int r = ll::CHUNK / (K * 2);
@@ -294,6 +315,10 @@ __device__ __forceinline__ void l_rows_dot(const bf16* wc, const float* xs, int 
 }
 
 // Consume this CTA's chunks of one op; results go to `sink` per (b, row, value).
+// The op's chunks (at most MAXC) are waited for first; then warp w takes row
+// pairs w, w+8, ... across all chunks with all its loads in flight, and the
+// chunks are released once every warp is done with them.
+constexpr int MAXC = 4;  // chunks per op per CTA: holds for grids >= 96 CTAs (gate/up 6144 rows: <= 64 rows = 4 chunks)
 template <int B, typename Sink>
 __device__ __forceinline__ void l_consume(const MegaArgs& a, int l, int o, LRing& ring, unsigned char* ring_mem,
                                           uint64_t* full, uint64_t* empty, const float* xs, Sink sink) {
@@ -302,42 +327,40 @@ __device__ __forceinline__ void l_consume(const MegaArgs& a, int l, int o, LRing
     l_rows(d.N, blockIdx.x, gridDim.x, r0, r1);
     const int rpc = l_rpc(d.K);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nv = d.K / 256;
-    const bool sub = a.trace && o == 2 && l < a.n_layers && threadIdx.x == 0;
-    unsigned long long* st = sub ? a.trace + ((size_t)blockIdx.x * a.n_layers + l) * 16 : nullptr;
-    int ci = 0;
-    for (int rc = r0; rc < r1; rc += rpc, ++ci) {
+    uint32_t off[MAXC], slots[MAXC];
+    int nc = 0;
+    for (int rc = r0; rc < r1 && nc < MAXC; rc += rpc, ++nc) {
         const int nr = min(rpc, r1 - rc);
-        const uint32_t bytes = (uint32_t)nr * d.K * 2;
-        const uint32_t p = ring.place(bytes);
-        const uint32_t slot = ring.k % ll::NSLOT, par = (ring.k / ll::NSLOT) & 1;
+        off[nc] = ring.place((uint32_t)nr * d.K * 2);
+        slots[nc] = ring.k;
         ring.k++;
-        l_mbar_wait(full + slot, par, a);
-        if (sub && ci < 2) st[10 + 3 * ci] = l_time();
-        const bf16* wc = reinterpret_cast<const bf16*>(ring_mem + p);
-        float acc[2][B];
-        const int lr0 = 2 * warp;
-        if (d.K == 1024)
-            l_rows_dot<B, 4>(wc, xs, d.K, lr0, nr, lane, acc);
-        else if (d.K == 2048)
-            l_rows_dot<B, 8>(wc, xs, d.K, lr0, nr, lane, acc);
-        else
-            l_rows_dot<B, 12>(wc, xs, d.K, lr0, nr, lane, acc);
-        __syncwarp();
-        if (sub && ci < 2) st[11 + 3 * ci] = l_time();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(l_su32(empty + slot)) : "memory");
-        if (lr0 < nr) {
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-                for (int b = 0; b < B; ++b) acc[rr][b] = warp_sum(acc[rr][b]);
-            if (lane == 0) {
-#pragma unroll
-                for (int b = 0; b < B; ++b) sink(b, rc + lr0, acc[0][b], (lr0 + 1 < nr), acc[1][b], r0);
-            }
-        }
-        if (sub && ci == 0) st[12] = l_time();
     }
+    for (int c = 0; c < nc; ++c) l_mbar_wait(full + slots[c] % ll::NSLOT, (slots[c] / ll::NSLOT) & 1, a);
+    const int npairs = (r1 - r0) / 2;
+    for (int pr = warp; pr < npairs; pr += ll::NCW) {
+        const int lrow = 2 * pr;                   // row within the CTA's slice
+        const int c = lrow / rpc, rin = lrow - c * rpc;
+        const bf16* wc = reinterpret_cast<const bf16*>(ring_mem + off[c]);
+        float acc[2][B];
+        if (d.K == 1024)
+            l_rows_dot<B, 4>(wc, xs, d.K, rin, rin + 2, lane, acc);
+        else if (d.K == 2048)
+            l_rows_dot<B, 8>(wc, xs, d.K, rin, rin + 2, lane, acc);
+        else
+            l_rows_dot<B, 12>(wc, xs, d.K, rin, rin + 2, lane, acc);
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+            for (int b = 0; b < B; ++b) acc[rr][b] = warp_sum(acc[rr][b]);
+        if (lane == 0) {
+#pragma unroll
+            for (int b = 0; b < B; ++b) sink(b, r0 + lrow, acc[0][b], true, acc[1][b], r0);
+        }
+    }
+    __syncwarp();
+    if (lane == 0)
+        for (int c = 0; c < nc; ++c)
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(l_su32(empty + slots[c] % ll::NSLOT)) : "memory");
 }
 
 // q/k RMSNorm + RoPE of one head, 4 elements per lane (RoPE partner lane ^ 16);
@@ -515,11 +538,11 @@ __device__ __forceinline__ void l_stage_attn(const MegaArgs& a, const XBufs& X, 
         const int b = bh / NQ;
         const int nblk = (a.pos[b] + 1 + KVB - 1) / KVB;
         float M = -INFINITY, lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int j0 = 0; j0 < nblk; j0 += 8) {
-            unsigned long long w[8 * 6];
-            const unsigned long long* p[8 * 6];
+        for (int j0 = 0; j0 < nblk; j0 += 4) {
+            unsigned long long w[4 * 6];
+            const unsigned long long* p[4 * 6];
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
+            for (int jj = 0; jj < 4; ++jj) {
                 const int j = min(j0 + jj, nblk - 1);
                 const unsigned long long* rec = base + ((size_t)bh * nbm + j) * PART_STRIDE;
                 p[jj * 6 + 0] = rec + HD;
@@ -533,7 +556,7 @@ __device__ __forceinline__ void l_stage_attn(const MegaArgs& a, const XBufs& X, 
             ll_settle(w, p, ep, a);
             // online merge of these blocks (same result as max-then-sum, block order kept)
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
+            for (int jj = 0; jj < 4; ++jj) {
                 if (j0 + jj >= nblk) break;
                 const float mj = ll_val(w[jj * 6]), lj = ll_val(w[jj * 6 + 1]);
                 const float Mn = fmaxf(M, mj);
@@ -595,7 +618,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
                         while (ok && (k - consumed >= (uint32_t)ll::NSLOT ||
                                       ring.head - tail > (unsigned long long)ll::RING)) {
                             const uint32_t s = consumed % ll::NSLOT;
-                            ok = l_mbar_wait(empty + s, (consumed / ll::NSLOT) & 1, a);
+                            ok = l_mbar_wait_sleep(empty + s, (consumed / ll::NSLOT) & 1, a);
                             if (ok) { tail = ends[s]; ++consumed; }
                         }
                         if (!ok) break;
@@ -616,7 +639,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
             while (consumed < ring.k) {  // every copy must land before the CTA leaves
                 const uint32_t s = consumed % ll::NSLOT;
                 if (ok) {
-                    if (!l_mbar_wait(empty + s, (consumed / ll::NSLOT) & 1, a)) ok = false;
+                    if (!l_mbar_wait_sleep(empty + s, (consumed / ll::NSLOT) & 1, a)) ok = false;
                 } else {
                     const unsigned long long t0 = l_time();
                     while (!l_mbar_try(full + s, (consumed / ll::NSLOT) & 1) && l_time() - t0 < ll::TIMEOUT_NS) {
@@ -633,6 +656,10 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
     LRing ring;
     int own0, own1;
     l_rows(HID, blockIdx.x, gridDim.x, own0, own1);
+    const int nblk0 = (a.pos[0] + 1 + KVB - 1) / KVB;
+    const int nblk1 = B > 1 ? (a.pos[B > 1 ? 1 : 0] + 1 + KVB - 1) / KVB : 0;
+    const int units_b0 = NKV * nblk0;
+    const int n_units = units_b0 + NKV * nblk1;
     const int t = threadIdx.x;
 #define LSTAMP(i)                                                                                 \
     do {                                                                                          \
@@ -710,18 +737,14 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
                          });
         }
         LSTAMP(2);
-        // ---- attention units
-        {
-            int u = 0;
-            for (int b = 0; b < B; ++b) {
-                const int nblk = (a.pos[b] + 1 + KVB - 1) / KVB;
-                for (int g = 0; g < NKV; ++g)
-                    for (int j = 0; j < nblk; ++j, ++u)
-                        if (u % (int)gridDim.x == (int)blockIdx.x) {
-                            l_attn_unit(a, X, l, b, g, j, att);
-                            if (a.trace && t == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * 16 + 15] += 1;
-                        }
-            }
+        // ---- attention units: unit u = (b, g, j) in order; CTA c takes u = c, c + G, ...
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+            int b = 0, r = u;
+            if (B > 1 && r >= units_b0) { b = 1; r -= units_b0; }
+            const int nblk = b == 0 ? nblk0 : nblk1;
+            const int g = r / nblk, j = r - g * nblk;
+            l_attn_unit(a, X, l, b, g, j, att);
+            if (a.trace && t == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * 16 + 15] += 1;
         }
         LSTAMP(3);
         // ---- merge + o_proj + residual (own rows) -> h words (version 2l+1)
@@ -839,6 +862,8 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
 }
 
 int ll_smem_bytes() { return ll::SMEM; }
+static_assert((3072 * 2 + LL_MIN_GRID - 1) / LL_MIN_GRID <= 16 * MAXC, "gate/up slice exceeds MAXC chunks");
+static_assert((3072 * 2 + LL_MIN_GRID - 1) / LL_MIN_GRID * 2 * HID <= ll::RING, "gate/up slice exceeds the ring");
 uint32_t ll_epochs_per_launch(int n_layers) { return 6u * (uint32_t)n_layers + 8u; }
 
 template <int B>
@@ -875,8 +900,8 @@ int ll_max_grid() {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaFuncSetAttribute(k_decode_ll<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, ll::SMEM);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_decode_ll<1>, ll::NT, ll::SMEM);
-    // own residual rows per CTA must fit OWN_MAX
-    if (per < 1 || (HID / 2 + sms - 1) / sms * 2 > ll::OWN_MAX) return 0;
+    // one op's chunks must fit the ring and MAXC at once, own residual rows must fit OWN_MAX
+    if (per < 1 || sms < LL_MIN_GRID || (HID / 2 + sms - 1) / sms * 2 > ll::OWN_MAX) return 0;
     return sms;
 }
 

@@ -61,6 +61,7 @@ struct MegaArgs {
 // Launch one decode step on `grid` CTAs (cooperative: all co-resident or an error).
 cudaError_t launch_decode_ll(const MegaArgs& a, int grid, cudaStream_t st);
 int ll_max_grid();
+constexpr int LL_MIN_GRID = 96;  // smallest grid whose per-CTA op slices fit the weight ring
 uint32_t ll_epochs_per_launch(int n_layers);
 // Exchange words the flag-in-data step needs for mbps cache blocks per sequence.
 inline size_t ll_xbuf_words(int mbps) {
