@@ -144,6 +144,8 @@ struct tts_bb {
     long phase_n = 0;                  // traced layers
     double unit_split[2] = {0, 0};
     long unit_split_n[2] = {0, 0};
+    double ring_wait[2] = {0, 0};      // persistent step: weight-ring waits inside gate/up and down
+    long ring_wait_n = 0;
 };
 
 namespace {
@@ -613,7 +615,7 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
     tts_bb_status s = ensure_scratch(h, std::max(nb, std::max(c.max_tokens, 1)));
     if (s != TTS_BB_OK) return bail(s);
     // persistent decode step: barrier counter, abort flag, block partials, constant arguments
-    if (c.max_slots > 0 && c.n_layers >= 1 && c.n_layers <= mk::MAXL && c.max_ctx <= 64 * KVB && (c.n_heads == 0 || c.head_rows % 2 == 0) && c.text_vocab == 0) {
+    if (c.max_slots > 0 && c.n_layers >= 1 && c.n_layers <= mk::MAXL && c.max_ctx <= 64 * KVB && c.ffn == 3072 && (c.n_heads == 0 || (c.head_rows % 2 == 0 && c.head_rows <= 6144)) && c.text_vocab == 0) {
         h->mega_grid = ll_max_grid();
         cudaGetLastError();
         if (const char* g = std::getenv("TTS_BB_DECODE_CTAS"))  // tuning knob: CTAs of the persistent step
@@ -755,10 +757,10 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
         ma.trace = nullptr;
         if (h->prof_on) {
             if (!h->mega_trace &&
-                dalloc(h, &h->mega_trace, (size_t)h->mega_grid * mk::MAXL * 16) != cudaSuccess)
+                dalloc(h, &h->mega_trace, (size_t)h->mega_grid * mk::MAXL * TRACE_STRIDE) != cudaSuccess)
                 return fail(h, TTS_BB_E_OOM, "trace buffer");
             if (h->phase_n == 0)
-                cudaMemsetAsync(h->mega_trace, 0, (size_t)h->mega_grid * mk::MAXL * 16 * 8, h->st);
+                cudaMemsetAsync(h->mega_trace, 0, (size_t)h->mega_grid * mk::MAXL * TRACE_STRIDE * 8, h->st);
             ma.trace = h->mega_trace;
         }
         double kvb = 0;
@@ -773,7 +775,7 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
         }
         h->ep_base += ll_epochs_per_launch(c.n_layers);
         if (ma.trace) {  // fold this launch's phase stamps into the profile (synchronises)
-            const int NS = 16, NP = 10, G = h->mega_grid, NL = c.n_layers;
+            const int NS = TRACE_STRIDE, NP = 10, G = h->mega_grid, NL = c.n_layers;
             std::vector<unsigned long long> st((size_t)G * NL * NS, 0ull);
             cudaMemcpyAsync(st.data(), h->mega_trace, st.size() * 8, cudaMemcpyDeviceToHost, h->st);
             cudaStreamSynchronize(h->st);
@@ -792,6 +794,15 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
                     h->phase_us[i] += sum / G;
                     h->phase_max_us[i] += mx;
                 }
+            // ring waits inside gate/up (stamps 6 -> 10) and down (8 -> 11)
+            for (int l = 0; l < NL; ++l)
+                for (int g = 0; g < G; ++g) {
+                    const unsigned long long* r = &st[((size_t)g * NL + l) * NS];
+                    if (!r[10] || !r[11]) continue;
+                    h->ring_wait[0] += (r[10] - r[6]) * 1e-3;
+                    h->ring_wait[1] += (r[11] - r[8]) * 1e-3;
+                    h->ring_wait_n++;
+                }
             // attention-unit phase (stamps 2 -> 3) split by whether the CTA ran a unit
             for (int l = 0; l < NL; ++l)
                 for (int g = 0; g < G; ++g) {
@@ -801,6 +812,12 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
                     h->unit_split_n[k]++;
                 }
             h->phase_n += NL;
+            if (const char* dump = std::getenv("TTS_BB_TRACE_DUMP")) {  // raw stamps of the latest launch
+                if (FILE* f = std::fopen(dump, "wb")) {
+                    std::fwrite(st.data(), 8, st.size(), f);
+                    std::fclose(f);
+                }
+            }
             cudaMemsetAsync(h->mega_trace, 0, st.size() * 8, h->st);
         }
         if (opts && opts->hidden_out)
@@ -996,6 +1013,8 @@ TTS_API tts_bb_status tts_bb_profile(tts_bb* h, int on) {
     h->phase_n = 0;
     h->unit_split[0] = h->unit_split[1] = 0;
     h->unit_split_n[0] = h->unit_split_n[1] = 0;
+    h->ring_wait[0] = h->ring_wait[1] = 0;
+    h->ring_wait_n = 0;
     h->prof_on = on != 0;
     return TTS_BB_OK;
 }
@@ -1040,6 +1059,12 @@ TTS_API const char* tts_bb_profile_report(tts_bb* h) {
                      h->unit_split_n[0] ? h->unit_split[0] / h->unit_split_n[0] : 0.0,
                      h->unit_split_n[1] ? h->unit_split[1] / h->unit_split_n[1] : 0.0,
                      (double)h->unit_split_n[1] / (h->unit_split_n[0] + h->unit_split_n[1]));
+            j += buf;
+        }
+        if (h->ring_wait_n) {
+            char buf[160];
+            snprintf(buf, sizeof buf, ", \"ring_wait_us\": {\"gate_up\": %.3f, \"down\": %.3f}",
+                     h->ring_wait[0] / h->ring_wait_n, h->ring_wait[1] / h->ring_wait_n);
             j += buf;
         }
     }

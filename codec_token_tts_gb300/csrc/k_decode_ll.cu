@@ -35,7 +35,8 @@ constexpr int MAXSPLIT = 64;                // cache blocks per sequence (4096 t
 constexpr int ATT_UNIT = NCW * (2 * HD + 4) + 2 * HD;
 constexpr int ATT_MERGE = 2 * mk::MAXB * NQ * MAXSPLIT;
 constexpr int ATT_FLOATS = ATT_UNIT > ATT_MERGE ? ATT_UNIT : ATT_MERGE;
-constexpr int SMEM = RING + XS_FLOATS * 4 + mk::MAXB * OWN_MAX * 4 + ATT_FLOATS * 4 + 2 * NSLOT * 8 + 64;
+constexpr int PART_FLOATS = NCW * 64 * mk::MAXB;  // per-warp partial sums of one op ([KS][64 rows][B])
+constexpr int SMEM = RING + XS_FLOATS * 4 + mk::MAXB * OWN_MAX * 4 + ATT_FLOATS * 4 + PART_FLOATS * 4 + 2 * NSLOT * 8 + 64;
 constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
 }  // namespace ll
 
@@ -122,30 +123,17 @@ __device__ __forceinline__ void ll_settle(unsigned long long (&w)[N], const unsi
 #pragma unroll
     for (int i = 0; i < N; ++i) ok &= (uint32_t)(w[i] >> 32) == ep;
     if (ok) return;
-    // Back off, then watch one stale word only (thousands of threads poll the
-    // same lines: keep the request rate low so the writers' stores get through);
-    // once it turns, reload every word that was stale.
+    // Reissue every stale word each round (one round trip per check; the
+    // whole exchange is a few KB per CTA, so the L2 request rate stays low).
     const unsigned long long t0 = l_time();
     for (uint32_t it = 0;; ++it) {
-        __nanosleep(it < 4 ? 128 : 256);
-        int first = -1;
 #pragma unroll
         for (int i = 0; i < N; ++i)
-            if (first < 0 && (uint32_t)(w[i] >> 32) != ep) first = i;
-        unsigned long long probe = 0;
+            if ((uint32_t)(w[i] >> 32) != ep) w[i] = ll_ld(p[i]);
+        ok = true;
 #pragma unroll
-        for (int i = 0; i < N; ++i)
-            if (i == first) probe = ll_ld(p[i]);
-        if ((uint32_t)(probe >> 32) == ep) {
-            ok = true;
-#pragma unroll
-            for (int i = 0; i < N; ++i)
-                if ((uint32_t)(w[i] >> 32) != ep) {
-                    w[i] = ll_ld(p[i]);
-                    ok &= (uint32_t)(w[i] >> 32) == ep;
-                }
-            if (ok) return;
-        }
+        for (int i = 0; i < N; ++i) ok &= (uint32_t)(w[i] >> 32) == ep;
+        if (ok) return;
         if ((it & 15) == 15) {
             if (l_aborted(a)) return;
             if (l_time() - t0 > ll::TIMEOUT_NS) { l_raise(a); return; }
@@ -174,10 +162,9 @@ __device__ __forceinline__ void l_rows(int N, int c, int G, int& r0, int& r1) {
     r0 = (int)(pairs * (unsigned)c / (unsigned)G) * 2;
     r1 = (int)(pairs * (unsigned)(c + 1) / (unsigned)G) * 2;
 }
-__device__ __forceinline__ int l_rpc(int K) {
-    int r = ll::CHUNK / (K * 2);
-    r &= ~1;
-    return r < 2 ? 2 : (r > 16 ? 16 : r);
+// weight rows per ring chunk for a K-column matrix (even, 2..16)
+__host__ __device__ constexpr int l_rpc(int K) {
+    return ((ll::CHUNK / (K * 2)) & ~1) < 2 ? 2 : (((ll::CHUNK / (K * 2)) & ~1) > 16 ? 16 : ((ll::CHUNK / (K * 2)) & ~1));
 }
 struct LRing {
     unsigned long long head = 0;
@@ -194,19 +181,27 @@ struct LRing {
 };
 
 // Exchange buffers inside MegaArgs::xbuf (unsigned long long words):
-//   h : [2][MAXB][HID]     q/k/v : [2][MAXB][QKV]     m : [2][MAXB][3072]
+//   h : [2][XR][MAXB][HID]   q/k/v : [2][MAXB][QKV]   m : [2][XR][MAXB][3072]
 //   part : [2][MAXB][16][nblk_max][132]
+// Every CTA reads all of h and m, so their writers store XR copies and CTA c
+// reads copy c % XR: fewer readers per L2 line, and a shorter exchange.
 struct XBufs {
     unsigned long long *h, *q, *m, *p;
 };
 __device__ __forceinline__ XBufs l_bufs(const MegaArgs& a) {
     XBufs x;
     x.h = a.xbuf;
-    x.q = x.h + 2 * mk::MAXB * HID;
+    x.q = x.h + 2 * LL_XR * mk::MAXB * HID;
     x.m = x.q + 2 * mk::MAXB * QKV;
-    x.p = x.m + 2 * mk::MAXB * 3072;
+    x.p = x.m + 2 * LL_XR * mk::MAXB * 3072;
     return x;
 }
+constexpr size_t XH_REP = (size_t)mk::MAXB * HID, XM_REP = (size_t)mk::MAXB * 3072;
+// h version v: base of the copies, and the copy this CTA reads
+__device__ __forceinline__ unsigned long long* xh_base(const XBufs& X, int v) { return X.h + (size_t)(v & 1) * LL_XR * XH_REP; }
+__device__ __forceinline__ unsigned long long* xh_mine(const XBufs& X, int v) { return xh_base(X, v) + (blockIdx.x % LL_XR) * XH_REP; }
+__device__ __forceinline__ unsigned long long* xm_base(const XBufs& X, int l) { return X.m + (size_t)(l & 1) * LL_XR * XM_REP; }
+__device__ __forceinline__ unsigned long long* xm_mine(const XBufs& X, int l) { return xm_base(X, l) + (blockIdx.x % LL_XR) * XM_REP; }
 
 // Epoch of each exchange: h version v (0 = layer-0 input, 2l+1 after o_proj, 2l+2 after down).
 __device__ __forceinline__ uint32_t ep_h(const MegaArgs& a, int v) { return a.ep_base + 3u * (uint32_t)v; }
@@ -216,18 +211,19 @@ __device__ __forceinline__ uint32_t ep_m(const MegaArgs& a, int l) { return a.ep
 
 // ---------------------------------------------------------------- consumer pieces
 // xs[b][k] = rmsnorm(h_v[b]) * gamma, h read from the exchange words of version v.
+template <int B>
 __device__ __forceinline__ void l_stage_norm(const MegaArgs& a, const unsigned long long* hx, uint32_t ep,
                                              const bf16* gamma, float* xs, float* red) {
     const int t = threadIdx.x;
-    // thread t: elements 4t..4t+3 of each token row (B <= 2: all loads issued before any check)
-    unsigned long long w[2 * 4];
-    const unsigned long long* p[2 * 4];
+    // thread t: elements 4t..4t+3 of each token row (all loads issued before any check)
+    unsigned long long w[B * 4];
+    const unsigned long long* p[B * 4];
 #pragma unroll
-    for (int b = 0; b < 2; ++b)
+    for (int b = 0; b < B; ++b)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) p[b * 4 + e] = hx + (size_t)min(b, a.B - 1) * HID + t * 4 + e;
+        for (int e = 0; e < 4; ++e) p[b * 4 + e] = hx + (size_t)b * HID + t * 4 + e;
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < B; ++b) {
         ll_ld2(p[b * 4], w[b * 4], w[b * 4 + 1]);
         ll_ld2(p[b * 4 + 2], w[b * 4 + 2], w[b * 4 + 3]);
     }
@@ -235,132 +231,150 @@ __device__ __forceinline__ void l_stage_norm(const MegaArgs& a, const unsigned l
     const uint2 gr = *reinterpret_cast<const uint2*>(gamma + t * 4);
     const float g4[4] = {__uint_as_float(gr.x << 16), __uint_as_float(gr.x & 0xFFFF0000u),
                          __uint_as_float(gr.y << 16), __uint_as_float(gr.y & 0xFFFF0000u)};
-    for (int b = 0; b < a.B; ++b) {
+    float v[B][4];
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
         float ss = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float v = ll_val(w[b * 4 + e]);
-            ss += v * v;
-            xs[b * HID + t * 4 + e] = v * g4[e];
+            v[b][e] = ll_val(w[b * 4 + e]);
+            ss += v[b][e] * v[b][e];
         }
         ss = warp_sum(ss);
         if ((t & 31) == 0) red[b * ll::NCW + (t >> 5)] = ss;
     }
     l_named_sync();
-    for (int b = 0; b < a.B; ++b) {
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
         float ss = 0.f;
 #pragma unroll
         for (int wi = 0; wi < ll::NCW; ++wi) ss += red[b * ll::NCW + wi];
         const float r = rsqrtf(ss * (1.f / HID) + a.eps);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) xs[b * HID + t * 4 + e] *= r;
+        *reinterpret_cast<float4*>(xs + b * HID + t * 4) =
+            make_float4(v[b][0] * g4[0] * r, v[b][1] * g4[1] * r, v[b][2] * g4[2] * r, v[b][3] * g4[3] * r);
     }
 }
 
-// Partial dot products of weight rows lr0, lr0+1 (of a chunk in shared
-// memory) with the staged activations: lane holds 16-byte column vectors
-// lane, lane+32, ...; NV vectors per lane. All shared loads of a row are
-// issued before its FMAs, which run as 4 independent chains per row.
-template <int B, int NV>
-__device__ __forceinline__ void l_rows_dot(const bf16* wc, const float* xs, int K, int lr0, int nr, int lane,
-                                           float (&acc)[2][B]) {
+// Warp-wide sums of N values at once (N a power of two <= 32): exchange
+// halves, then fold the remaining lane bits. Afterwards lane l holds in v[0]
+// the total of value (l & (N - 1)); N - 1 + 5 - log2(N) shuffles in all.
+template <int N>
+__device__ __forceinline__ void l_multi_reduce(float (&v)[N], int lane) {
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr)
+    for (int s = N / 2; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
 #pragma unroll
-        for (int b = 0; b < B; ++b) acc[rr][b] = 0.f;
-    if (lr0 >= nr) return;
-    const bool two = lr0 + 1 < nr;
-    float part[2][B][4];
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-        for (int b = 0; b < B; ++b)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) part[rr][b][q] = 0.f;
-    constexpr int U = NV < 4 ? NV : 4;
-#pragma unroll
-    for (int i0 = 0; i0 < NV; i0 += U) {
-        uint4 w[2][U];
-        float4 x[B][U][2];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int col = ((i0 + u) * 32 + lane) * 8;
-            w[0][u] = *reinterpret_cast<const uint4*>(wc + (size_t)lr0 * K + col);
-            w[1][u] = two ? *reinterpret_cast<const uint4*>(wc + (size_t)(lr0 + 1) * K + col) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int b = 0; b < B; ++b) {
-                x[b][u][0] = *reinterpret_cast<const float4*>(xs + b * K + col);
-                x[b][u][1] = *reinterpret_cast<const float4*>(xs + b * K + col + 4);
-            }
+        for (int i = 0; i < s; ++i) {
+            const float send = upper ? v[i] : v[i + s];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, s);
+            v[i] = (upper ? v[i + s] : v[i]) + recv;
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                float wf[8];
-                unpack8(w[rr][u], wf);
-#pragma unroll
-                for (int b = 0; b < B; ++b) {
-                    const float xf[8] = {x[b][u][0].x, x[b][u][0].y, x[b][u][0].z, x[b][u][0].w,
-                                         x[b][u][1].x, x[b][u][1].y, x[b][u][1].z, x[b][u][1].w};
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) part[rr][b][j & 3] = fmaf(wf[j], xf[j], part[rr][b][j & 3]);
-                }
-            }
     }
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-        for (int b = 0; b < B; ++b) acc[rr][b] = (part[rr][b][0] + part[rr][b][1]) + (part[rr][b][2] + part[rr][b][3]);
+    for (int s = N; s < 32; s <<= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], s);
 }
 
-// Consume this CTA's chunks of one op; results go to `sink` per (b, row, value).
-// The op's chunks (at most MAXC) are waited for first; then warp w takes row
-// pairs w, w+8, ... across all chunks with all its loads in flight, and the
-// chunks are released once every warp is done with them.
+// Consume this CTA's chunks of one op: rows r0..r1 of a K-column matrix,
+// results to `sink(b, row, v_row, true, v_row+1, r0)` per even row.
+// The eight warps form 8/KS row groups of KS warps each. A group's warps
+// split the columns (K/KS each; a lane reads 4 consecutive bf16 in every
+// 128), keep the activations of their columns in registers for the whole op,
+// and take rows rg, rg + RG, ... four at a time, reduced across lanes with one
+// multi-value butterfly. Partial sums go to `part`; after a barrier, threads
+// add the KS partials of each row pair in order and call the sink. Callers
+// put a barrier between consecutive calls (the partial buffer is reused).
 constexpr int MAXC = 4;  // chunks per op per CTA: holds for grids >= 96 CTAs (gate/up 6144 rows: <= 64 rows = 4 chunks)
-template <int B, typename Sink>
+constexpr int PART_ROWS = 64;  // most rows of one op in one CTA (grids >= 96 CTAs, N <= 6144)
+template <int B, int K, int KS, typename Sink>
 __device__ __forceinline__ void l_consume(const MegaArgs& a, int l, int o, LRing& ring, unsigned char* ring_mem,
-                                          uint64_t* full, uint64_t* empty, const float* xs, Sink sink) {
-    const LOp d = l_op(a, l, o);
+                                          uint64_t* full, uint64_t* empty, const float* xs, float* part, int stamp,
+                                          Sink sink) {
+    constexpr int RG = ll::NCW / KS, KW = K / KS, NV = KW / 128, RPC = l_rpc(K);
+    static_assert(KW % 128 == 0 && ll::NCW % KS == 0, "column split must be a multiple of 128");
+    const LOp d = l_op(a, l, o);  // d.K == K (checked by the host for every op)
     int r0, r1;
     l_rows(d.N, blockIdx.x, gridDim.x, r0, r1);
-    const int rpc = l_rpc(d.K);
+    const int R = r1 - r0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint32_t off[MAXC], slots[MAXC];
+    const int rg = warp / KS, ks = warp - rg * KS;
+    // ring chunks of this op, in the producer's order
+    uint32_t off[MAXC] = {0u, 0u, 0u, 0u};
+    const uint32_t slot0 = ring.k;
     int nc = 0;
-    for (int rc = r0; rc < r1 && nc < MAXC; rc += rpc, ++nc) {
-        const int nr = min(rpc, r1 - rc);
-        off[nc] = ring.place((uint32_t)nr * d.K * 2);
-        slots[nc] = ring.k;
+    for (int rc = 0; rc < R && nc < MAXC; rc += RPC, ++nc) {
+        const uint32_t bytes = (uint32_t)min(RPC, R - rc) * K * 2;
+        const uint32_t p = ring.place(bytes);
+#pragma unroll
+        for (int c = 0; c < MAXC; ++c)
+            if (c == nc) off[c] = p;
         ring.k++;
     }
-    for (int c = 0; c < nc; ++c) l_mbar_wait(full + slots[c] % ll::NSLOT, (slots[c] / ll::NSLOT) & 1, a);
-    const int npairs = (r1 - r0) / 2;
-    for (int pr = warp; pr < npairs; pr += ll::NCW) {
-        const int lrow = 2 * pr;                   // row within the CTA's slice
-        const int c = lrow / rpc, rin = lrow - c * rpc;
-        const bf16* wc = reinterpret_cast<const bf16*>(ring_mem + off[c]);
-        float acc[2][B];
-        if (d.K == 1024)
-            l_rows_dot<B, 4>(wc, xs, d.K, rin, rin + 2, lane, acc);
-        else if (d.K == 2048)
-            l_rows_dot<B, 8>(wc, xs, d.K, rin, rin + 2, lane, acc);
-        else
-            l_rows_dot<B, 12>(wc, xs, d.K, rin, rin + 2, lane, acc);
+    // activations of this warp's columns (loaded before the weights are waited for)
+    float xr[B][NV][4];
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr)
+    for (int b = 0; b < B; ++b)
 #pragma unroll
-            for (int b = 0; b < B; ++b) acc[rr][b] = warp_sum(acc[rr][b]);
-        if (lane == 0) {
+        for (int v = 0; v < NV; ++v) {
+            const float4 x4 = *reinterpret_cast<const float4*>(xs + b * K + ks * KW + v * 128 + lane * 4);
+            xr[b][v][0] = x4.x; xr[b][v][1] = x4.y; xr[b][v][2] = x4.z; xr[b][v][3] = x4.w;
+        }
+    for (int c = 0; c < nc; ++c) l_mbar_wait(full + (slot0 + c) % ll::NSLOT, ((slot0 + c) / ll::NSLOT) & 1, a);
+    if (stamp >= 0 && a.trace && threadIdx.x == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + stamp] = l_time();
+    const int col0 = (ks * KW + lane * 4) * 2;  // byte offset of the lane's first column in a row
+    for (int i0 = rg; i0 < R; i0 += 4 * RG) {
+        float acc[4 * B];
 #pragma unroll
-            for (int b = 0; b < B; ++b) sink(b, r0 + lrow, acc[0][b], true, acc[1][b], r0);
+        for (int f = 0; f < 4 * B; ++f) acc[f] = 0.f;
+        uint2 w[4][NV];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int row = i0 + q * RG;
+            const int c = row / RPC, rin = row - c * RPC;
+            const uint32_t base = c == 0 ? off[0] : c == 1 ? off[1] : c == 2 ? off[2] : off[3];
+            const unsigned char* wp = ring_mem + base + (size_t)rin * K * 2 + col0;
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+                w[q][v] = row < R ? *reinterpret_cast<const uint2*>(wp + v * 256) : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const float w0 = __uint_as_float(w[q][v].x << 16), w1 = __uint_as_float(w[q][v].x & 0xFFFF0000u);
+                const float w2 = __uint_as_float(w[q][v].y << 16), w3 = __uint_as_float(w[q][v].y & 0xFFFF0000u);
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    float t = acc[q * B + b];
+                    t = fmaf(w0, xr[b][v][0], t);
+                    t = fmaf(w1, xr[b][v][1], t);
+                    t = fmaf(w2, xr[b][v][2], t);
+                    t = fmaf(w3, xr[b][v][3], t);
+                    acc[q * B + b] = t;
+                }
+            }
+        l_multi_reduce<4 * B>(acc, lane);
+        if (lane < 4 * B) {
+            const int q = lane / B, b = lane - q * B, row = i0 + q * RG;
+            if (row < R) part[(ks * PART_ROWS + row) * B + b] = acc[0];
         }
     }
     __syncwarp();
+    if (stamp >= 0 && a.trace && lane == 0)  // per-warp finish: slots 16 + 8 * (stamp - 10) + warp
+        a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + 16 + 8 * (stamp - 10) + warp] = l_time();
     if (lane == 0)
         for (int c = 0; c < nc; ++c)
-            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(l_su32(empty + slots[c] % ll::NSLOT)) : "memory");
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(l_su32(empty + (slot0 + c) % ll::NSLOT)) : "memory");
+    l_named_sync();
+    for (int i = threadIdx.x; i < (R / 2) * B; i += ll::NCT) {
+        const int pr = i / B, b = i - pr * B, row = 2 * pr;
+        float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+            v0 += part[(k * PART_ROWS + row) * B + b];
+            v1 += part[(k * PART_ROWS + row + 1) * B + b];
+        }
+        sink(b, r0 + row, v0, true, v1, r0);
+    }
 }
 
 // q/k RMSNorm + RoPE of one head, 4 elements per lane (RoPE partner lane ^ 16);
@@ -582,7 +596,8 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
     float* xs = reinterpret_cast<float*>(smem + ll::RING);
     float* hown = xs + ll::XS_FLOATS;                         // [B][OWN_MAX]
     float* att = hown + mk::MAXB * ll::OWN_MAX;
-    uint64_t* full = reinterpret_cast<uint64_t*>(att + ll::ATT_FLOATS);
+    float* part = att + ll::ATT_FLOATS;
+    uint64_t* full = reinterpret_cast<uint64_t*>(part + ll::PART_FLOATS);
     uint64_t* empty = full + ll::NSLOT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -663,7 +678,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
     const int t = threadIdx.x;
 #define LSTAMP(i)                                                                                 \
     do {                                                                                          \
-        if (a.trace && t == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * 16 + (i)] = l_time(); \
+        if (a.trace && t == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + (i)] = l_time(); \
     } while (0)
 
     // page-table entries of blocks opened by this step (read by later launches)
@@ -720,9 +735,13 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
 
     for (int l = 0; l < a.n_layers; ++l) {
         LSTAMP(0);
-        unsigned long long* hx_prev = X.h + (size_t)((2 * l) & 1) * mk::MAXB * HID;
+        if (a.trace && t == 0 && l == 0) {
+            uint32_t smid;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+            a.trace[(size_t)blockIdx.x * a.n_layers * TRACE_STRIDE + 12] = smid;
+        }
         if (l > 0) {
-            l_stage_norm(a, hx_prev, ep_h(a, 2 * l), a.L[l].in_norm, xs, att);
+            l_stage_norm<B>(a, xh_mine(X, 2 * l), ep_h(a, 2 * l), a.L[l].in_norm, xs, att);
             l_named_sync();
         }
         LSTAMP(1);
@@ -730,7 +749,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
         {
             unsigned long long* qx = X.q + (size_t)(l & 1) * mk::MAXB * QKV;
             const uint32_t eq = ep_q(a, l);
-            l_consume<B>(a, l, 0, ring, ring_mem, full, empty, xs,
+            l_consume<B, HID, 1>(a, l, 0, ring, ring_mem, full, empty, xs, part, -1,
                          [&](int b, int row, float v0, bool two, float v1, int) {
                              ll_put(qx + (size_t)b * QKV + row, v0, eq);
                              if (two) ll_put(qx + (size_t)b * QKV + row + 1, v1, eq);
@@ -744,77 +763,84 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
             const int nblk = b == 0 ? nblk0 : nblk1;
             const int g = r / nblk, j = r - g * nblk;
             l_attn_unit(a, X, l, b, g, j, att);
-            if (a.trace && t == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * 16 + 15] += 1;
+            if (a.trace && t == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + 15] += 1;
         }
         LSTAMP(3);
         // ---- merge + o_proj + residual (own rows) -> h words (version 2l+1)
         l_stage_attn(a, X, l, xs);
         l_named_sync();
         LSTAMP(4);
-        l_consume<B>(a, l, 1, ring, ring_mem, full, empty, xs,
+        l_consume<B, NQ * HD, 8>(a, l, 1, ring, ring_mem, full, empty, xs, part, -1,
                      [&](int b, int row, float v0, bool two, float v1, int r0) {
                          hown[b * ll::OWN_MAX + row - r0] += v0;
                          if (two) hown[b * ll::OWN_MAX + row + 1 - r0] += v1;
                      });
         l_named_sync();
         {
-            unsigned long long* hx = X.h + (size_t)((2 * l + 1) & 1) * mk::MAXB * HID;
+            unsigned long long* hx = xh_base(X, 2 * l + 1);
             const uint32_t eh = ep_h(a, 2 * l + 1);
-            for (int i = t; i < B * (own1 - own0); i += ll::NCT) {
-                const int b = i / (own1 - own0), r = i % (own1 - own0);
-                ll_put(hx + (size_t)b * HID + own0 + r, hown[b * ll::OWN_MAX + r], eh);
+            const int n = B * (own1 - own0);
+            for (int i = t; i < LL_XR * n; i += ll::NCT) {
+                const int rep = i / n, k = i - rep * n, b = k / (own1 - own0), r = k - b * (own1 - own0);
+                ll_put(hx + rep * XH_REP + (size_t)b * HID + own0 + r, hown[b * ll::OWN_MAX + r], eh);
             }
         }
         LSTAMP(5);
         // ---- gate/up + SwiGLU -> m words
-        l_stage_norm(a, X.h + (size_t)((2 * l + 1) & 1) * mk::MAXB * HID, ep_h(a, 2 * l + 1), a.L[l].post_norm, xs, att);
+        l_stage_norm<B>(a, xh_mine(X, 2 * l + 1), ep_h(a, 2 * l + 1), a.L[l].post_norm, xs, att);
         l_named_sync();
         LSTAMP(6);
         {
-            unsigned long long* mx = X.m + (size_t)(l & 1) * mk::MAXB * 3072;
+            unsigned long long* mx = xm_base(X, l);
             const uint32_t em = ep_m(a, l);
-            l_consume<B>(a, l, 2, ring, ring_mem, full, empty, xs,
+            l_consume<B, HID, 1>(a, l, 2, ring, ring_mem, full, empty, xs, part, 10,
                          [&](int b, int row, float g, bool, float u, int) {
-                             ll_put(mx + (size_t)b * 3072 + row / 2, g / (1.f + __expf(-g)) * u, em);
+                             const float m = g / (1.f + __expf(-g)) * u;
+#pragma unroll
+                             for (int rep = 0; rep < LL_XR; ++rep) ll_put(mx + rep * XM_REP + (size_t)b * 3072 + row / 2, m, em);
                          });
         }
         LSTAMP(7);
         // ---- down + residual (own rows) -> h words (version 2l+2)
         {
-            const unsigned long long* mx = X.m + (size_t)(l & 1) * mk::MAXB * 3072;
+            const unsigned long long* mx = xm_mine(X, l);
             const uint32_t em = ep_m(a, l);
-            // thread t: 12 consecutive values of each row (ffn 3072 / 256 threads), all loads first
-            for (int b = 0; b < B; ++b) {
-                unsigned long long w[12];
-                const unsigned long long* p[12];
-                const int c0 = t * 12;
+            // thread t: 12 consecutive values of each row (3072 / 256 threads), all loads first
+            unsigned long long w[B * 12];
+            const unsigned long long* p[B * 12];
+            const int c0 = t * 12;
+#pragma unroll
+            for (int b = 0; b < B; ++b)
 #pragma unroll
                 for (int e = 0; e < 12; e += 2) {
-                    p[e] = mx + (size_t)b * 3072 + min(c0 + e, a.ffn - 2);
-                    p[e + 1] = p[e] + 1;
-                    ll_ld2(p[e], w[e], w[e + 1]);
+                    p[b * 12 + e] = mx + (size_t)b * 3072 + c0 + e;
+                    p[b * 12 + e + 1] = p[b * 12 + e] + 1;
+                    ll_ld2(p[b * 12 + e], w[b * 12 + e], w[b * 12 + e + 1]);
                 }
-                ll_settle(w, p, em, a);
+            ll_settle(w, p, em, a);
 #pragma unroll
-                for (int e = 0; e < 12; ++e)
-                    if (c0 + e < a.ffn) xs[b * a.ffn + c0 + e] = ll_val(w[e]);
-            }
+            for (int b = 0; b < B; ++b)
+#pragma unroll
+                for (int e = 0; e < 12; e += 4)
+                    *reinterpret_cast<float4*>(xs + b * 3072 + c0 + e) =
+                        make_float4(ll_val(w[b * 12 + e]), ll_val(w[b * 12 + e + 1]), ll_val(w[b * 12 + e + 2]), ll_val(w[b * 12 + e + 3]));
         }
         l_named_sync();
         LSTAMP(8);
-        l_consume<B>(a, l, 3, ring, ring_mem, full, empty, xs,
+        l_consume<B, 3072, 8>(a, l, 3, ring, ring_mem, full, empty, xs, part, 11,
                      [&](int b, int row, float v0, bool two, float v1, int r0) {
                          hown[b * ll::OWN_MAX + row - r0] += v0;
                          if (two) hown[b * ll::OWN_MAX + row + 1 - r0] += v1;
                      });
         l_named_sync();
         {
-            unsigned long long* hx = X.h + (size_t)((2 * l + 2) & 1) * mk::MAXB * HID;
+            unsigned long long* hx = xh_base(X, 2 * l + 2);
             const uint32_t eh = ep_h(a, 2 * l + 2);
-            for (int i = t; i < B * (own1 - own0); i += ll::NCT) {
-                const int b = i / (own1 - own0), r = i % (own1 - own0);
-                ll_put(hx + (size_t)b * HID + own0 + r, hown[b * ll::OWN_MAX + r], eh);
-                if (l == a.n_layers - 1) a.h[(size_t)b * HID + own0 + r] = hown[b * ll::OWN_MAX + r];
+            const int n = B * (own1 - own0);
+            for (int i = t; i < LL_XR * n; i += ll::NCT) {
+                const int rep = i / n, k = i - rep * n, b = k / (own1 - own0), r = k - b * (own1 - own0);
+                ll_put(hx + rep * XH_REP + (size_t)b * HID + own0 + r, hown[b * ll::OWN_MAX + r], eh);
+                if (l == a.n_layers - 1 && rep == 0) a.h[(size_t)b * HID + own0 + r] = hown[b * ll::OWN_MAX + r];
             }
         }
         LSTAMP(9);
@@ -823,12 +849,12 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
     // ---- final norm + head + argmax
     if (a.head) {
         const int vl = 2 * a.n_layers;
-        l_stage_norm(a, X.h + (size_t)(vl & 1) * mk::MAXB * HID, ep_h(a, vl), a.final_norm, xs, att);
+        l_stage_norm<B>(a, xh_mine(X, vl), ep_h(a, vl), a.final_norm, xs, att);
         l_named_sync();
         __shared__ unsigned long long best_s[mk::MAXB];
         if (t < B) best_s[t] = 0ull;
         l_named_sync();
-        l_consume<B>(a, a.n_layers, 0, ring, ring_mem, full, empty, xs,
+        l_consume<B, HID, 1>(a, a.n_layers, 0, ring, ring_mem, full, empty, xs, part, -1,
                      [&](int b, int row, float v0, bool two, float v1, int) {
                          if (a.logits) {
                              a.logits[(size_t)b * a.head_rows + row] = v0;
@@ -864,6 +890,8 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
 int ll_smem_bytes() { return ll::SMEM; }
 static_assert((3072 * 2 + LL_MIN_GRID - 1) / LL_MIN_GRID <= 16 * MAXC, "gate/up slice exceeds MAXC chunks");
 static_assert((3072 * 2 + LL_MIN_GRID - 1) / LL_MIN_GRID * 2 * HID <= ll::RING, "gate/up slice exceeds the ring");
+static_assert((3072 * 2 + LL_MIN_GRID - 1) / LL_MIN_GRID <= PART_ROWS && PART_ROWS * mk::MAXB * ll::NCW <= ll::PART_FLOATS,
+              "one op's rows exceed the partial buffer");
 uint32_t ll_epochs_per_launch(int n_layers) { return 6u * (uint32_t)n_layers + 8u; }
 
 template <int B>
