@@ -59,6 +59,16 @@ __device__ __forceinline__ bool l_mbar_try(uint64_t* b, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking test of a phase (cheaper than try_wait when it has completed).
+__device__ __forceinline__ bool l_mbar_test(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(l_su32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ void l_named_sync() { asm volatile("bar.sync 1, %0;" ::"n"(ll::NCT) : "memory"); }
 
 __device__ __forceinline__ bool l_aborted(const MegaArgs& a) { return *reinterpret_cast<volatile int*>(a.abort_flag) != 0; }
@@ -89,7 +99,7 @@ __device__ __forceinline__ bool l_mbar_wait_sleep(uint64_t* b, uint32_t parity, 
     }
 }
 __device__ __forceinline__ bool l_mbar_wait(uint64_t* b, uint32_t parity, const MegaArgs& a) {
-    if (l_mbar_try(b, parity)) return true;
+    if (l_mbar_test(b, parity)) return true;
     const unsigned long long t0 = l_time();
     for (uint32_t i = 0;; ++i) {
         if (l_mbar_try(b, parity)) return true;
@@ -140,6 +150,28 @@ __device__ __forceinline__ void ll_settle(unsigned long long (&w)[N], const unsi
         }
     }
 }
+// ll_settle with the address of word i computed by addr(i) instead of stored.
+template <int N, typename Addr>
+__device__ __forceinline__ void ll_settle_f(unsigned long long (&w)[N], Addr addr, uint32_t ep, const MegaArgs& a) {
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < N; ++i) ok &= (uint32_t)(w[i] >> 32) == ep;
+    if (ok) return;
+    const unsigned long long t0 = l_time();
+    for (uint32_t it = 0;; ++it) {
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if ((uint32_t)(w[i] >> 32) != ep) w[i] = ll_ld(addr(i));
+        ok = true;
+#pragma unroll
+        for (int i = 0; i < N; ++i) ok &= (uint32_t)(w[i] >> 32) == ep;
+        if (ok) return;
+        if ((it & 15) == 15) {
+            if (l_aborted(a)) return;
+            if (l_time() - t0 > ll::TIMEOUT_NS) { l_raise(a); return; }
+        }
+    }
+}
 __device__ __forceinline__ float ll_val(unsigned long long w) { return __uint_as_float((uint32_t)w); }
 
 // ---------------------------------------------------------------- schedule (same as the producer)
@@ -167,14 +199,16 @@ __host__ __device__ constexpr int l_rpc(int K) {
     return ((ll::CHUNK / (K * 2)) & ~1) < 2 ? 2 : (((ll::CHUNK / (K * 2)) & ~1) > 16 ? 16 : ((ll::CHUNK / (K * 2)) & ~1));
 }
 struct LRing {
-    unsigned long long head = 0;
-    uint32_t k = 0;
+    unsigned long long head = 0;  // bytes placed so far, including skipped ring tails
+    uint32_t pos = 0;             // offset of the next placement in the ring
+    uint32_t k = 0;               // chunks placed so far
     __device__ __forceinline__ uint32_t place(uint32_t bytes) {
-        uint32_t p = (uint32_t)(head % ll::RING);
-        if (p + bytes > (uint32_t)ll::RING) {
-            head += ll::RING - p;
-            p = 0;
+        if (pos + bytes > (uint32_t)ll::RING) {
+            head += ll::RING - pos;
+            pos = 0;
         }
+        const uint32_t p = pos;
+        pos += bytes;
         head += bytes;
         return p;
     }
@@ -182,9 +216,10 @@ struct LRing {
 
 // Exchange buffers inside MegaArgs::xbuf (unsigned long long words):
 //   h : [2][XR][MAXB][HID]   q/k/v : [2][MAXB][QKV]   m : [2][XR][MAXB][3072]
-//   part : [2][MAXB][16][nblk_max][132]
-// Every CTA reads all of h and m, so their writers store XR copies and CTA c
-// reads copy c % XR: fewer readers per L2 line, and a shorter exchange.
+//   part : [2][XR][MAXB][16][nblk_max][132]
+// Every CTA reads all of h, m and the attention partials, so their writers
+// store XR copies and CTA c reads copy c % XR: fewer readers per L2 line, and
+// a shorter exchange.
 struct XBufs {
     unsigned long long *h, *q, *m, *p;
 };
@@ -202,6 +237,10 @@ __device__ __forceinline__ unsigned long long* xh_base(const XBufs& X, int v) { 
 __device__ __forceinline__ unsigned long long* xh_mine(const XBufs& X, int v) { return xh_base(X, v) + (blockIdx.x % LL_XR) * XH_REP; }
 __device__ __forceinline__ unsigned long long* xm_base(const XBufs& X, int l) { return X.m + (size_t)(l & 1) * LL_XR * XM_REP; }
 __device__ __forceinline__ unsigned long long* xm_mine(const XBufs& X, int l) { return xm_base(X, l) + (blockIdx.x % LL_XR) * XM_REP; }
+__device__ __forceinline__ size_t xp_rep(const MegaArgs& a) { return (size_t)mk::MAXB * NQ * a.nblk_max * PART_STRIDE; }
+__device__ __forceinline__ unsigned long long* xp_base(const MegaArgs& a, const XBufs& X, int l) {
+    return X.p + (size_t)(l & 1) * LL_XRP * xp_rep(a);
+}
 
 // Epoch of each exchange: h version v (0 = layer-0 input, 2l+1 after o_proj, 2l+2 after down).
 __device__ __forceinline__ uint32_t ep_h(const MegaArgs& a, int v) { return a.ep_base + 3u * (uint32_t)v; }
@@ -215,22 +254,19 @@ template <int B>
 __device__ __forceinline__ void l_stage_norm(const MegaArgs& a, const unsigned long long* hx, uint32_t ep,
                                              const bf16* gamma, float* xs, float* red) {
     const int t = threadIdx.x;
-    // thread t: elements 4t..4t+3 of each token row (all loads issued before any check)
+    // thread t: elements 2t, 2t+1 and 512+2t, 512+2t+1 of each token row, so
+    // a warp's 16-byte loads cover 512 contiguous bytes (all loads issued before any check)
     unsigned long long w[B * 4];
-    const unsigned long long* p[B * 4];
-#pragma unroll
-    for (int b = 0; b < B; ++b)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) p[b * 4 + e] = hx + (size_t)b * HID + t * 4 + e;
 #pragma unroll
     for (int b = 0; b < B; ++b) {
-        ll_ld2(p[b * 4], w[b * 4], w[b * 4 + 1]);
-        ll_ld2(p[b * 4 + 2], w[b * 4 + 2], w[b * 4 + 3]);
+        ll_ld2(hx + (size_t)b * HID + 2 * t, w[b * 4], w[b * 4 + 1]);
+        ll_ld2(hx + (size_t)b * HID + 512 + 2 * t, w[b * 4 + 2], w[b * 4 + 3]);
     }
-    ll_settle(w, p, ep, a);
-    const uint2 gr = *reinterpret_cast<const uint2*>(gamma + t * 4);
-    const float g4[4] = {__uint_as_float(gr.x << 16), __uint_as_float(gr.x & 0xFFFF0000u),
-                         __uint_as_float(gr.y << 16), __uint_as_float(gr.y & 0xFFFF0000u)};
+    ll_settle_f(w, [&](int i) { return hx + (size_t)(i >> 2) * HID + ((i & 2) ? 512 : 0) + 2 * t + (i & 1); }, ep, a);
+    const uint32_t g0 = *reinterpret_cast<const uint32_t*>(gamma + 2 * t);
+    const uint32_t g1 = *reinterpret_cast<const uint32_t*>(gamma + 512 + 2 * t);
+    const float g4[4] = {__uint_as_float(g0 << 16), __uint_as_float(g0 & 0xFFFF0000u),
+                         __uint_as_float(g1 << 16), __uint_as_float(g1 & 0xFFFF0000u)};
     float v[B][4];
 #pragma unroll
     for (int b = 0; b < B; ++b) {
@@ -250,8 +286,8 @@ __device__ __forceinline__ void l_stage_norm(const MegaArgs& a, const unsigned l
 #pragma unroll
         for (int wi = 0; wi < ll::NCW; ++wi) ss += red[b * ll::NCW + wi];
         const float r = rsqrtf(ss * (1.f / HID) + a.eps);
-        *reinterpret_cast<float4*>(xs + b * HID + t * 4) =
-            make_float4(v[b][0] * g4[0] * r, v[b][1] * g4[1] * r, v[b][2] * g4[2] * r, v[b][3] * g4[3] * r);
+        *reinterpret_cast<float2*>(xs + b * HID + 2 * t) = make_float2(v[b][0] * g4[0] * r, v[b][1] * g4[1] * r);
+        *reinterpret_cast<float2*>(xs + b * HID + 512 + 2 * t) = make_float2(v[b][2] * g4[2] * r, v[b][3] * g4[3] * r);
     }
 }
 
@@ -286,15 +322,13 @@ __device__ __forceinline__ void l_multi_reduce(float (&v)[N], int lane) {
 constexpr int MAXC = 4;  // chunks per op per CTA: holds for grids >= 96 CTAs (gate/up 6144 rows: <= 64 rows = 4 chunks)
 constexpr int PART_ROWS = 64;  // most rows of one op in one CTA (grids >= 96 CTAs, N <= 6144)
 template <int B, int K, int KS, typename Sink>
-__device__ __forceinline__ void l_consume(const MegaArgs& a, int l, int o, LRing& ring, unsigned char* ring_mem,
+__device__ __forceinline__ void l_consume(const MegaArgs& a, int l, int2 rows, LRing& ring, unsigned char* ring_mem,
                                           uint64_t* full, uint64_t* empty, const float* xs, float* part, int stamp,
                                           Sink sink) {
     constexpr int RG = ll::NCW / KS, KW = K / KS, NV = KW / 128, RPC = l_rpc(K);
     static_assert(KW % 128 == 0 && ll::NCW % KS == 0, "column split must be a multiple of 128");
-    const LOp d = l_op(a, l, o);  // d.K == K (checked by the host for every op)
-    int r0, r1;
-    l_rows(d.N, blockIdx.x, gridDim.x, r0, r1);
-    const int R = r1 - r0;
+    // rows = this CTA's slice [r0, r1) of the op (l_rows); K is the op's column count (the host checks both)
+    const int r0 = rows.x, R = rows.y - rows.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rg = warp / KS, ks = warp - rg * KS;
     // ring chunks of this op, in the producer's order
@@ -531,61 +565,74 @@ __device__ __forceinline__ void l_attn_unit(const MegaArgs& a, const XBufs& X, i
             lsum += ww[2 * HD + 2 * h2 + 1] * f;
             acc += ww[h2 * HD + e] * f;
         }
-        unsigned long long* dst =
-            X.p + ((((size_t)(l & 1) * mk::MAXB + b) * NQ + 2 * g + h2) * a.nblk_max + j) * PART_STRIDE;
+        unsigned long long* dst = xp_base(a, X, l) + (((size_t)b * NQ + 2 * g + h2) * a.nblk_max + j) * PART_STRIDE;
         const uint32_t ep = ep_p(a, l);
-        ll_put(dst + e, acc, ep);
-        if (e == 0) { ll_put(dst + HD, M, ep); ll_put(dst + HD + 1, lsum, ep); }
+        const size_t rs = xp_rep(a);
+#pragma unroll
+        for (int rep = 0; rep < LL_XRP; ++rep) {
+            ll_put(dst + rep * rs + e, acc, ep);
+            if (e == 0) { ll_put(dst + rep * rs + HD, M, ep); ll_put(dst + rep * rs + HD + 1, lsum, ep); }
+        }
     }
     l_named_sync();
 }
 
 // xs[b][h*128 + e] = merge of the block partial words of (b, h) in block order.
-// Thread (b, h, 4 outputs) loads, for up to 8 blocks at a time, the block's
-// running max / sum and its 4 outputs together, waits once, and combines.
+// Thread t owns E outputs of one (b, h), as E/4 groups of 4 spaced HD/(E/4)
+// apart (so a warp's loads stay contiguous); per round it loads, for J
+// blocks at once, each block's running max / sum and its outputs, waits
+// once, and folds them in (online, block order kept).
+template <int B>
 __device__ __forceinline__ void l_stage_attn(const MegaArgs& a, const XBufs& X, int l, float* xs) {
+    constexpr int E = B * NQ * HD / ll::NCT;  // outputs per thread
+    constexpr int G4 = E / 4, GS = HD / G4;   // groups of 4 outputs, their spacing
+    constexpr int J = B == 1 ? 4 : 2;         // cache blocks per poll round
+    constexpr int W = 2 + E;                  // words per block
+    constexpr int TPH = HD / E;               // threads per (b, h)
     const uint32_t ep = ep_p(a, l);
-    const unsigned long long* base = X.p + (size_t)(l & 1) * mk::MAXB * NQ * a.nblk_max * PART_STRIDE;
-    const int nbm = a.nblk_max;
-    for (int t = threadIdx.x; t < a.B * NQ * (HD / 4); t += ll::NCT) {
-        const int bh = t / (HD / 4), e4 = (t % (HD / 4)) * 4;
-        const int b = bh / NQ;
-        const int nblk = (a.pos[b] + 1 + KVB - 1) / KVB;
-        float M = -INFINITY, lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int j0 = 0; j0 < nblk; j0 += 4) {
-            unsigned long long w[4 * 6];
-            const unsigned long long* p[4 * 6];
+    const int t = threadIdx.x, bh = t / TPH, e0 = (t - bh * TPH) * 4, b = bh / NQ;
+    const unsigned long long* base =
+        xp_base(a, X, l) + (blockIdx.x % LL_XRP) * xp_rep(a) + (size_t)bh * a.nblk_max * PART_STRIDE;
+    const int nblk = (a.pos[b] + 1 + KVB - 1) / KVB;
+    float M = -INFINITY, lsum = 0.f, acc[E];
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int j = min(j0 + jj, nblk - 1);
-                const unsigned long long* rec = base + ((size_t)bh * nbm + j) * PART_STRIDE;
-                p[jj * 6 + 0] = rec + HD;
-                p[jj * 6 + 1] = rec + HD + 1;
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    for (int j0 = 0; j0 < nblk; j0 += J) {
+        unsigned long long w[J * W];
+        auto addr = [&](int i) {
+            const int jj = i / W, k = i - jj * W;
+            const unsigned long long* rec = base + (size_t)min(j0 + jj, nblk - 1) * PART_STRIDE;
+            return k < 2 ? rec + HD + k : rec + e0 + ((k - 2) >> 2) * GS + ((k - 2) & 3);
+        };
 #pragma unroll
-                for (int e = 0; e < 4; ++e) p[jj * 6 + 2 + e] = rec + e4 + e;
-                ll_ld2(rec + HD, w[jj * 6 + 0], w[jj * 6 + 1]);
-                ll_ld2(rec + e4, w[jj * 6 + 2], w[jj * 6 + 3]);
-                ll_ld2(rec + e4 + 2, w[jj * 6 + 4], w[jj * 6 + 5]);
-            }
-            ll_settle(w, p, ep, a);
-            // online merge of these blocks (same result as max-then-sum, block order kept)
+        for (int jj = 0; jj < J; ++jj) {
+            const unsigned long long* rec = base + (size_t)min(j0 + jj, nblk - 1) * PART_STRIDE;
+            ll_ld2(rec + HD, w[jj * W], w[jj * W + 1]);
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                if (j0 + jj >= nblk) break;
-                const float mj = ll_val(w[jj * 6]), lj = ll_val(w[jj * 6 + 1]);
-                const float Mn = fmaxf(M, mj);
-                const float fo = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
-                const float fj = (mj == -INFINITY) ? 0.f : exp2f(mj - Mn);
-                lsum = lsum * fo + lj * fj;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[e] = acc[e] * fo + ll_val(w[jj * 6 + 2 + e]) * fj;
-                M = Mn;
+            for (int g = 0; g < G4; ++g) {
+                ll_ld2(rec + e0 + g * GS, w[jj * W + 2 + 4 * g], w[jj * W + 3 + 4 * g]);
+                ll_ld2(rec + e0 + g * GS + 2, w[jj * W + 4 + 4 * g], w[jj * W + 5 + 4 * g]);
             }
         }
-        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        ll_settle_f(w, addr, ep, a);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) xs[bh * HD + e4 + e] = acc[e] * inv;
+        for (int jj = 0; jj < J; ++jj) {
+            if (j0 + jj >= nblk) break;
+            const float mj = ll_val(w[jj * W]), lj = ll_val(w[jj * W + 1]);
+            const float Mn = fmaxf(M, mj);
+            const float fo = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
+            const float fj = (mj == -INFINITY) ? 0.f : exp2f(mj - Mn);
+            lsum = lsum * fo + lj * fj;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = acc[e] * fo + ll_val(w[jj * W + 2 + e]) * fj;
+            M = Mn;
+        }
     }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+#pragma unroll
+    for (int g = 0; g < G4; ++g)
+        *reinterpret_cast<float4*>(xs + bh * HD + e0 + g * GS) =
+            make_float4(acc[4 * g] * inv, acc[4 * g + 1] * inv, acc[4 * g + 2] * inv, acc[4 * g + 3] * inv);
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -638,6 +685,8 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
                         }
                         if (!ok) break;
                         const uint32_t slot = k % ll::NSLOT;
+                        if (a.trace && rc == r0 && l < a.n_layers && (o == 2 || o == 3))  // issue time of the op's first chunk
+                            a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + 11 + o] = l_time();
                         ends[slot] = ring.head;
                         ring.k++;
                         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(l_su32(full + slot)),
@@ -671,6 +720,13 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
     LRing ring;
     int own0, own1;
     l_rows(HID, blockIdx.x, gridDim.x, own0, own1);
+    // this CTA's row slices of every op (the same for all layers)
+    int2 rows_qkv, rows_o, rows_gu, rows_d, rows_head;
+    l_rows(QKV, blockIdx.x, gridDim.x, rows_qkv.x, rows_qkv.y);
+    l_rows(HID, blockIdx.x, gridDim.x, rows_o.x, rows_o.y);
+    l_rows(2 * 3072, blockIdx.x, gridDim.x, rows_gu.x, rows_gu.y);
+    rows_d = rows_o;
+    l_rows(a.head_rows, blockIdx.x, gridDim.x, rows_head.x, rows_head.y);
     const int nblk0 = (a.pos[0] + 1 + KVB - 1) / KVB;
     const int nblk1 = B > 1 ? (a.pos[B > 1 ? 1 : 0] + 1 + KVB - 1) / KVB : 0;
     const int units_b0 = NKV * nblk0;
@@ -749,7 +805,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
         {
             unsigned long long* qx = X.q + (size_t)(l & 1) * mk::MAXB * QKV;
             const uint32_t eq = ep_q(a, l);
-            l_consume<B, HID, 1>(a, l, 0, ring, ring_mem, full, empty, xs, part, -1,
+            l_consume<B, HID, 1>(a, l, rows_qkv, ring, ring_mem, full, empty, xs, part, -1,
                          [&](int b, int row, float v0, bool two, float v1, int) {
                              ll_put(qx + (size_t)b * QKV + row, v0, eq);
                              if (two) ll_put(qx + (size_t)b * QKV + row + 1, v1, eq);
@@ -767,10 +823,10 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
         }
         LSTAMP(3);
         // ---- merge + o_proj + residual (own rows) -> h words (version 2l+1)
-        l_stage_attn(a, X, l, xs);
+        l_stage_attn<B>(a, X, l, xs);
         l_named_sync();
         LSTAMP(4);
-        l_consume<B, NQ * HD, 8>(a, l, 1, ring, ring_mem, full, empty, xs, part, -1,
+        l_consume<B, NQ * HD, 8>(a, l, rows_o, ring, ring_mem, full, empty, xs, part, -1,
                      [&](int b, int row, float v0, bool two, float v1, int r0) {
                          hown[b * ll::OWN_MAX + row - r0] += v0;
                          if (two) hown[b * ll::OWN_MAX + row + 1 - r0] += v1;
@@ -793,7 +849,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
         {
             unsigned long long* mx = xm_base(X, l);
             const uint32_t em = ep_m(a, l);
-            l_consume<B, HID, 1>(a, l, 2, ring, ring_mem, full, empty, xs, part, 10,
+            l_consume<B, HID, 1>(a, l, rows_gu, ring, ring_mem, full, empty, xs, part, 10,
                          [&](int b, int row, float g, bool, float u, int) {
                              const float m = g / (1.f + __expf(-g)) * u;
 #pragma unroll
@@ -805,29 +861,24 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
         {
             const unsigned long long* mx = xm_mine(X, l);
             const uint32_t em = ep_m(a, l);
-            // thread t: 12 consecutive values of each row (3072 / 256 threads), all loads first
+            // thread t: values 512k + 2t, 512k + 2t + 1 (k < 6) of each row, so a warp's
+            // 16-byte loads cover 512 contiguous bytes; all loads first
             unsigned long long w[B * 12];
-            const unsigned long long* p[B * 12];
-            const int c0 = t * 12;
 #pragma unroll
             for (int b = 0; b < B; ++b)
 #pragma unroll
-                for (int e = 0; e < 12; e += 2) {
-                    p[b * 12 + e] = mx + (size_t)b * 3072 + c0 + e;
-                    p[b * 12 + e + 1] = p[b * 12 + e] + 1;
-                    ll_ld2(p[b * 12 + e], w[b * 12 + e], w[b * 12 + e + 1]);
-                }
-            ll_settle(w, p, em, a);
+                for (int k = 0; k < 6; ++k) ll_ld2(mx + (size_t)b * 3072 + 512 * k + 2 * t, w[b * 12 + 2 * k], w[b * 12 + 2 * k + 1]);
+            ll_settle_f(w, [&](int i) { return mx + (size_t)(i / 12) * 3072 + 512 * ((i % 12) >> 1) + 2 * t + (i & 1); }, em, a);
 #pragma unroll
             for (int b = 0; b < B; ++b)
 #pragma unroll
-                for (int e = 0; e < 12; e += 4)
-                    *reinterpret_cast<float4*>(xs + b * 3072 + c0 + e) =
-                        make_float4(ll_val(w[b * 12 + e]), ll_val(w[b * 12 + e + 1]), ll_val(w[b * 12 + e + 2]), ll_val(w[b * 12 + e + 3]));
+                for (int k = 0; k < 6; ++k)
+                    *reinterpret_cast<float2*>(xs + b * 3072 + 512 * k + 2 * t) =
+                        make_float2(ll_val(w[b * 12 + 2 * k]), ll_val(w[b * 12 + 2 * k + 1]));
         }
         l_named_sync();
         LSTAMP(8);
-        l_consume<B, 3072, 8>(a, l, 3, ring, ring_mem, full, empty, xs, part, 11,
+        l_consume<B, 3072, 8>(a, l, rows_d, ring, ring_mem, full, empty, xs, part, 11,
                      [&](int b, int row, float v0, bool two, float v1, int r0) {
                          hown[b * ll::OWN_MAX + row - r0] += v0;
                          if (two) hown[b * ll::OWN_MAX + row + 1 - r0] += v1;
@@ -854,7 +905,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
         __shared__ unsigned long long best_s[mk::MAXB];
         if (t < B) best_s[t] = 0ull;
         l_named_sync();
-        l_consume<B, HID, 1>(a, a.n_layers, 0, ring, ring_mem, full, empty, xs, part, -1,
+        l_consume<B, HID, 1>(a, a.n_layers, rows_head, ring, ring_mem, full, empty, xs, part, -1,
                      [&](int b, int row, float v0, bool two, float v1, int) {
                          if (a.logits) {
                              a.logits[(size_t)b * a.head_rows + row] = v0;

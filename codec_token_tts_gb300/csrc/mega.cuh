@@ -62,12 +62,13 @@ struct MegaArgs {
 cudaError_t launch_decode_ll(const MegaArgs& a, int grid, cudaStream_t st);
 int ll_max_grid();
 constexpr int LL_MIN_GRID = 96;   // smallest grid whose per-CTA op slices fit the weight ring
-constexpr int TRACE_STRIDE = 32;  // profiling stamps per (CTA, layer)
+constexpr int TRACE_STRIDE = 40;  // profiling stamps per (CTA, layer)
 constexpr int LL_XR = 8;          // replicas of the h and SwiGLU exchange vectors (readers spread over them)
+constexpr int LL_XRP = 8;         // replicas of the attention partials
 uint32_t ll_epochs_per_launch(int n_layers);
 // Exchange words the flag-in-data step needs for mbps cache blocks per sequence.
 inline size_t ll_xbuf_words(int mbps) {
-    return 2ull * mk::MAXB * (LL_XR * HID + QKV + LL_XR * 3072) + 2ull * mk::MAXB * NQ * (size_t)mbps * PART_STRIDE;
+    return 2ull * mk::MAXB * (LL_XR * HID + QKV + LL_XR * 3072) + 2ull * LL_XRP * mk::MAXB * NQ * (size_t)mbps * PART_STRIDE;
 }
 
 }  // namespace ttsbb
