@@ -28,15 +28,16 @@ constexpr int NCT = NCW * 32;
 constexpr int NT = NCT + 32;
 constexpr int RING = 176 * 1024;
 constexpr int NSLOT = 16;
-constexpr int CHUNK = 32 * 1024;
-constexpr int XS_FLOATS = mk::MAXB * 3072;
+constexpr int CHUNK = 34 * 1024;             // ring chunk budget: 16 padded rows of K = 1024
+constexpr int ROW_PAD = 32;                  // bytes after each weight row in the ring (conflict-free fragment loads)
+constexpr int XF_BYTES = mk::MAXB * 3072 * 2 * 2;  // staged activations: bf16 high + low part per value
 constexpr int OWN_MAX = 32;                 // own residual rows per CTA (>= ceil(1024 / G) rounded to pairs)
 constexpr int MAXSPLIT = 64;                // cache blocks per sequence (4096 tokens)
 constexpr int ATT_UNIT = NCW * (2 * HD + 4) + 2 * HD;
 constexpr int ATT_MERGE = 2 * mk::MAXB * NQ * MAXSPLIT;
 constexpr int ATT_FLOATS = ATT_UNIT > ATT_MERGE ? ATT_UNIT : ATT_MERGE;
 constexpr int PART_FLOATS = NCW * 64 * mk::MAXB;  // per-warp partial sums of one op ([KS][64 rows][B])
-constexpr int SMEM = RING + XS_FLOATS * 4 + mk::MAXB * OWN_MAX * 4 + ATT_FLOATS * 4 + PART_FLOATS * 4 + 2 * NSLOT * 8 + 64;
+constexpr int SMEM = RING + XF_BYTES + mk::MAXB * OWN_MAX * 4 + ATT_FLOATS * 4 + PART_FLOATS * 4 + 2 * NSLOT * 8 + 64;
 constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
 }  // namespace ll
 
@@ -194,9 +195,10 @@ __device__ __forceinline__ void l_rows(int N, int c, int G, int& r0, int& r1) {
     r0 = (int)(pairs * (unsigned)c / (unsigned)G) * 2;
     r1 = (int)(pairs * (unsigned)(c + 1) / (unsigned)G) * 2;
 }
-// weight rows per ring chunk for a K-column matrix (even, 2..16)
+// weight rows per ring chunk for a K-column matrix (even, 2..16), rows padded by ROW_PAD
 __host__ __device__ constexpr int l_rpc(int K) {
-    return ((ll::CHUNK / (K * 2)) & ~1) < 2 ? 2 : (((ll::CHUNK / (K * 2)) & ~1) > 16 ? 16 : ((ll::CHUNK / (K * 2)) & ~1));
+    return ((ll::CHUNK / (K * 2 + ll::ROW_PAD)) & ~1) < 2 ? 2
+         : (((ll::CHUNK / (K * 2 + ll::ROW_PAD)) & ~1) > 16 ? 16 : ((ll::CHUNK / (K * 2 + ll::ROW_PAD)) & ~1));
 }
 struct LRing {
     unsigned long long head = 0;  // bytes placed so far, including skipped ring tails
@@ -249,10 +251,40 @@ __device__ __forceinline__ uint32_t ep_p(const MegaArgs& a, int l) { return a.ep
 __device__ __forceinline__ uint32_t ep_m(const MegaArgs& a, int l) { return a.ep_base + 6u * (uint32_t)l + 4u; }
 
 // ---------------------------------------------------------------- consumer pieces
-// xs[b][k] = rmsnorm(h_v[b]) * gamma, h read from the exchange words of version v.
+// Staged activations for the tensor-core matrix-vector products: value x of
+// token b, column k of a K-column operand is kept as x ~= hi + lo (two bf16,
+// so the products keep ~16 mantissa bits) in the column order of the mma
+// fragments: 16-column step, lane quad (4 columns), part (hi, lo), element.
+__device__ __forceinline__ int xf_idx(int K, int b, int k, int part) {
+    return b * K * 2 + (k >> 4) * 32 + ((k >> 2) & 3) * 8 + part * 4 + (k & 3);
+}
+__device__ __forceinline__ uint32_t xf_split2(float v0, float v1, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+// columns k, k+1 (k even)
+__device__ __forceinline__ void xf_put2(bf16* xf, int K, int b, int k, float v0, float v1) {
+    uint32_t lo;
+    const uint32_t hi = xf_split2(v0, v1, lo);
+    *reinterpret_cast<uint32_t*>(xf + xf_idx(K, b, k, 0)) = hi;
+    *reinterpret_cast<uint32_t*>(xf + xf_idx(K, b, k, 1)) = lo;
+}
+// columns k..k+3 (k a multiple of 4)
+__device__ __forceinline__ void xf_put4(bf16* xf, int K, int b, int k, float v0, float v1, float v2, float v3) {
+    uint2 hi, lo;
+    hi.x = xf_split2(v0, v1, lo.x);
+    hi.y = xf_split2(v2, v3, lo.y);
+    *reinterpret_cast<uint2*>(xf + xf_idx(K, b, k, 0)) = hi;
+    *reinterpret_cast<uint2*>(xf + xf_idx(K, b, k, 1)) = lo;
+}
+
+// xf[b][k] = rmsnorm(h_v[b]) * gamma (staged), h read from the exchange words of version v.
 template <int B>
 __device__ __forceinline__ void l_stage_norm(const MegaArgs& a, const unsigned long long* hx, uint32_t ep,
-                                             const bf16* gamma, float* xs, float* red) {
+                                             const bf16* gamma, bf16* xf, float* red) {
     const int t = threadIdx.x;
     // thread t: elements 2t, 2t+1 and 512+2t, 512+2t+1 of each token row, so
     // a warp's 16-byte loads cover 512 contiguous bytes (all loads issued before any check)
@@ -286,110 +318,128 @@ __device__ __forceinline__ void l_stage_norm(const MegaArgs& a, const unsigned l
 #pragma unroll
         for (int wi = 0; wi < ll::NCW; ++wi) ss += red[b * ll::NCW + wi];
         const float r = rsqrtf(ss * (1.f / HID) + a.eps);
-        *reinterpret_cast<float2*>(xs + b * HID + 2 * t) = make_float2(v[b][0] * g4[0] * r, v[b][1] * g4[1] * r);
-        *reinterpret_cast<float2*>(xs + b * HID + 512 + 2 * t) = make_float2(v[b][2] * g4[2] * r, v[b][3] * g4[3] * r);
+        xf_put2(xf, HID, b, 2 * t, v[b][0] * g4[0] * r, v[b][1] * g4[1] * r);
+        xf_put2(xf, HID, b, 512 + 2 * t, v[b][2] * g4[2] * r, v[b][3] * g4[3] * r);
     }
 }
 
-// Warp-wide sums of N values at once (N a power of two <= 32): exchange
-// halves, then fold the remaining lane bits. Afterwards lane l holds in v[0]
-// the total of value (l & (N - 1)); N - 1 + 5 - log2(N) shuffles in all.
-template <int N>
-__device__ __forceinline__ void l_multi_reduce(float (&v)[N], int lane) {
+__device__ __forceinline__ void l_mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                      uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The k-loop of l_consume: the warp's NK column steps over TT tiles (TT and
+// LASTHI fixed at compile time, so the loads carry no branch and schedule
+// freely). LASTHI = the last tile's rows 8..15 hold rows of the slice (else
+// they are zero and not loaded).
+template <int B, int MAXT, int NK, int TT, bool LASTHI>
+__device__ __forceinline__ void l_mma_loop(float (&d)[MAXT][2][4], const int (&ra)[MAXT][2], const unsigned char* ring_mem,
+                                           const bf16* xb, uint32_t bmask) {
+    static_assert(NK % 2 == 0 && TT <= MAXT, "column steps per warp must be even");
 #pragma unroll
-    for (int s = N / 2; s >= 1; s >>= 1) {
-        const bool upper = (lane & s) != 0;
+    for (int tt = 0; tt < MAXT; ++tt)
 #pragma unroll
-        for (int i = 0; i < s; ++i) {
-            const float send = upper ? v[i] : v[i + s];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, s);
-            v[i] = (upper ? v[i + s] : v[i]) + recv;
+        for (int q = 0; q < 2; ++q) d[tt][q][0] = d[tt][q][1] = d[tt][q][2] = d[tt][q][3] = 0.f;
+#pragma unroll 4
+    for (int s = 0; s < NK; ++s) {
+        uint2 bv = *reinterpret_cast<const uint2*>(xb + s * 32);
+        bv.x &= bmask;
+        bv.y &= bmask;
+#pragma unroll
+        for (int tt = 0; tt < TT; ++tt) {
+            const uint2 lo = *reinterpret_cast<const uint2*>(ring_mem + ra[tt][0] + s * 32);
+            const uint2 hi = (LASTHI || tt + 1 < TT) ? *reinterpret_cast<const uint2*>(ring_mem + ra[tt][1] + s * 32)
+                                                    : make_uint2(0u, 0u);
+            l_mma(d[tt][s & 1], lo.x, hi.x, lo.y, hi.y, bv.x, bv.y);
         }
     }
-#pragma unroll
-    for (int s = N; s < 32; s <<= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], s);
+}
+template <int B, int MAXT, int NK, int TT>
+__device__ __forceinline__ void l_mma_dispatch(float (&d)[MAXT][2][4], const int (&ra)[MAXT][2], const unsigned char* ring_mem,
+                                               const bf16* xb, uint32_t bmask, int T, bool lasthi) {
+    if constexpr (TT <= MAXT) {
+        if (T == TT) {
+            if (lasthi) l_mma_loop<B, MAXT, NK, TT, true>(d, ra, ring_mem, xb, bmask);
+            else l_mma_loop<B, MAXT, NK, TT, false>(d, ra, ring_mem, xb, bmask);
+        } else {
+            l_mma_dispatch<B, MAXT, NK, TT + 1>(d, ra, ring_mem, xb, bmask, T, lasthi);
+        }
+    }
 }
 
 // Consume this CTA's chunks of one op: rows r0..r1 of a K-column matrix,
 // results to `sink(b, row, v_row, true, v_row+1, r0)` per even row.
-// The eight warps form 8/KS row groups of KS warps each. A group's warps
-// split the columns (K/KS each; a lane reads 4 consecutive bf16 in every
-// 128), keep the activations of their columns in registers for the whole op,
-// and take rows rg, rg + RG, ... four at a time, reduced across lanes with one
-// multi-value butterfly. Partial sums go to `part`; after a barrier, threads
-// add the KS partials of each row pair in order and call the sink. Callers
-// put a barrier between consecutive calls (the partial buffer is reused).
-constexpr int MAXC = 4;  // chunks per op per CTA: holds for grids >= 96 CTAs (gate/up 6144 rows: <= 64 rows = 4 chunks)
+// Tensor cores (m16n8k16, bf16 in, fp32 accumulate): the rows form 16-row
+// tiles (A, from the ring, rows padded so fragment loads are conflict-free);
+// the staged activations are the B operand, column 2b the high and 2b+1 the
+// low part of token b. Columns are permuted consistently in A and B so each
+// thread's fragment is one 8-byte load: within every 16 columns, the four
+// k-slots of lane quad t are the columns 4t..4t+3. Warp w takes columns
+// [w K/8, (w+1) K/8) of every tile; its partial sums go to `part` and, after a
+// barrier, threads add the eight partials of each row pair in order and call
+// the sink. Callers put a barrier between consecutive calls (the partial
+// buffer is reused).
+constexpr int MAXC = 4;        // chunks per op per CTA: holds for grids >= 96 CTAs (gate/up 6144 rows: <= 64 rows = 4 chunks)
 constexpr int PART_ROWS = 64;  // most rows of one op in one CTA (grids >= 96 CTAs, N <= 6144)
-template <int B, int K, int KS, typename Sink>
+template <int B, int K, int MAXT, typename Sink>
 __device__ __forceinline__ void l_consume(const MegaArgs& a, int l, int2 rows, LRing& ring, unsigned char* ring_mem,
-                                          uint64_t* full, uint64_t* empty, const float* xs, float* part, int stamp,
+                                          uint64_t* full, uint64_t* empty, const bf16* xf, float* part, int stamp,
                                           Sink sink) {
-    constexpr int RG = ll::NCW / KS, KW = K / KS, NV = KW / 128, RPC = l_rpc(K);
-    static_assert(KW % 128 == 0 && ll::NCW % KS == 0, "column split must be a multiple of 128");
+    // MAXT = most 16-row tiles of this op in one CTA (grids >= LL_MIN_GRID)
+    constexpr int RPC = l_rpc(K), RS = K * 2 + ll::ROW_PAD, NK = K / ll::NCW / 16;
+    static_assert(MAXT * 16 <= PART_ROWS, "tiles exceed the partial buffer");
+    static_assert(K % (ll::NCW * 16) == 0, "columns must split into 16-column steps per warp");
     // rows = this CTA's slice [r0, r1) of the op (l_rows); K is the op's column count (the host checks both)
-    const int r0 = rows.x, R = rows.y - rows.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rg = warp / KS, ks = warp - rg * KS;
+    const int r0 = rows.x, R = rows.y - rows.x, T = (R + 15) >> 4;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
     // ring chunks of this op, in the producer's order
     uint32_t off[MAXC] = {0u, 0u, 0u, 0u};
     const uint32_t slot0 = ring.k;
     int nc = 0;
     for (int rc = 0; rc < R && nc < MAXC; rc += RPC, ++nc) {
-        const uint32_t bytes = (uint32_t)min(RPC, R - rc) * K * 2;
-        const uint32_t p = ring.place(bytes);
+        const uint32_t p = ring.place((uint32_t)min(RPC, R - rc) * RS);
 #pragma unroll
         for (int c = 0; c < MAXC; ++c)
             if (c == nc) off[c] = p;
         ring.k++;
     }
-    // activations of this warp's columns (loaded before the weights are waited for)
-    float xr[B][NV][4];
+    // ring byte offsets of this thread's A rows (16 t + g and 16 t + g + 8); rows past the
+    // slice read row R - 1 instead (their results are dropped), so the loads need no branch
+    int ra[MAXT][2];
 #pragma unroll
-    for (int b = 0; b < B; ++b)
+    for (int tt = 0; tt < MAXT; ++tt)
 #pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            const float4 x4 = *reinterpret_cast<const float4*>(xs + b * K + ks * KW + v * 128 + lane * 4);
-            xr[b][v][0] = x4.x; xr[b][v][1] = x4.y; xr[b][v][2] = x4.z; xr[b][v][3] = x4.w;
+        for (int h = 0; h < 2; ++h) {
+            const int i = min(16 * tt + g + 8 * h, R - 1), c = i / RPC, rin = i - c * RPC;
+            const uint32_t base = c == 0 ? off[0] : c == 1 ? off[1] : c == 2 ? off[2] : off[3];
+            ra[tt][h] = (int)(base + (uint32_t)rin * RS) + (warp * NK * 16 + tq * 4) * 2;
         }
     for (int c = 0; c < nc; ++c) l_mbar_wait(full + (slot0 + c) % ll::NSLOT, ((slot0 + c) / ll::NSLOT) & 1, a);
     if (stamp >= 0 && a.trace && threadIdx.x == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + stamp] = l_time();
-    const int col0 = (ks * KW + lane * 4) * 2;  // byte offset of the lane's first column in a row
-    for (int i0 = rg; i0 < R; i0 += 4 * RG) {
-        float acc[4 * B];
+    // two accumulator sets per tile (even / odd column steps) halve the mma dependency chain
+    float d[MAXT][2][4];
+    // B fragment: lanes g < 2B carry token g / 2 (high part for even g, low for odd); the others
+    // load a valid address and are masked to zero
+    const int gb = min(g, 2 * B - 1);
+    const bf16* xb = xf + (gb >> 1) * K * 2 + (gb & 1) * 4 + tq * 8 + warp * NK * 32;
+    const uint32_t bmask = g < 2 * B ? 0xffffffffu : 0u;
 #pragma unroll
-        for (int f = 0; f < 4 * B; ++f) acc[f] = 0.f;
-        uint2 w[4][NV];
+    for (int tt = 0; tt < MAXT; ++tt)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int row = i0 + q * RG;
-            const int c = row / RPC, rin = row - c * RPC;
-            const uint32_t base = c == 0 ? off[0] : c == 1 ? off[1] : c == 2 ? off[2] : off[3];
-            const unsigned char* wp = ring_mem + base + (size_t)rin * K * 2 + col0;
+        for (int q = 0; q < 2; ++q) d[tt][q][0] = d[tt][q][1] = d[tt][q][2] = d[tt][q][3] = 0.f;
+    // tile count and whether the last tile's rows 8..15 hold rows of the slice, chosen once
+    l_mma_dispatch<B, MAXT, NK, 1>(d, ra, ring_mem, xb, bmask, T, R > 16 * (T - 1) + 8);
+    // thread (g, tq < B) holds rows 16 t + g (d0 + d1) and 16 t + g + 8 (d2 + d3) of token tq
+    if (tq < B) {
 #pragma unroll
-            for (int v = 0; v < NV; ++v)
-                w[q][v] = row < R ? *reinterpret_cast<const uint2*>(wp + v * 256) : make_uint2(0u, 0u);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int v = 0; v < NV; ++v) {
-                const float w0 = __uint_as_float(w[q][v].x << 16), w1 = __uint_as_float(w[q][v].x & 0xFFFF0000u);
-                const float w2 = __uint_as_float(w[q][v].y << 16), w3 = __uint_as_float(w[q][v].y & 0xFFFF0000u);
-#pragma unroll
-                for (int b = 0; b < B; ++b) {
-                    float t = acc[q * B + b];
-                    t = fmaf(w0, xr[b][v][0], t);
-                    t = fmaf(w1, xr[b][v][1], t);
-                    t = fmaf(w2, xr[b][v][2], t);
-                    t = fmaf(w3, xr[b][v][3], t);
-                    acc[q * B + b] = t;
-                }
-            }
-        l_multi_reduce<4 * B>(acc, lane);
-        if (lane < 4 * B) {
-            const int q = lane / B, b = lane - q * B, row = i0 + q * RG;
-            if (row < R) part[(ks * PART_ROWS + row) * B + b] = acc[0];
+        for (int tt = 0; tt < MAXT; ++tt) {
+            const int i = 16 * tt + g;
+            if (i < R) part[(warp * PART_ROWS + i) * B + tq] = (d[tt][0][0] + d[tt][0][1]) + (d[tt][1][0] + d[tt][1][1]);
+            if (i + 8 < R) part[(warp * PART_ROWS + i + 8) * B + tq] = (d[tt][0][2] + d[tt][0][3]) + (d[tt][1][2] + d[tt][1][3]);
         }
     }
     __syncwarp();
@@ -403,7 +453,7 @@ __device__ __forceinline__ void l_consume(const MegaArgs& a, int l, int2 rows, L
         const int pr = i / B, b = i - pr * B, row = 2 * pr;
         float v0 = 0.f, v1 = 0.f;
 #pragma unroll
-        for (int k = 0; k < KS; ++k) {
+        for (int k = 0; k < ll::NCW; ++k) {
             v0 += part[(k * PART_ROWS + row) * B + b];
             v1 += part[(k * PART_ROWS + row + 1) * B + b];
         }
@@ -498,6 +548,7 @@ __device__ __forceinline__ void l_attn_unit(const MegaArgs& a, const XBufs& X, i
         newv[lane] = o;
     }
     l_named_sync();
+    if (a.trace && threadIdx.x == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + 36] = l_time();
     if (last && key0 <= pos && pos < key0 + 8) {  // this warp holds the new token's slot
         kr[pos - key0] = newk[lane];
         vr[pos - key0] = newv[lane];
@@ -565,6 +616,7 @@ __device__ __forceinline__ void l_attn_unit(const MegaArgs& a, const XBufs& X, i
             lsum += ww[2 * HD + 2 * h2 + 1] * f;
             acc += ww[h2 * HD + e] * f;
         }
+        if (a.trace && threadIdx.x == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + 37] = l_time();
         unsigned long long* dst = xp_base(a, X, l) + (((size_t)b * NQ + 2 * g + h2) * a.nblk_max + j) * PART_STRIDE;
         const uint32_t ep = ep_p(a, l);
         const size_t rs = xp_rep(a);
@@ -577,16 +629,16 @@ __device__ __forceinline__ void l_attn_unit(const MegaArgs& a, const XBufs& X, i
     l_named_sync();
 }
 
-// xs[b][h*128 + e] = merge of the block partial words of (b, h) in block order.
+// xf[b][h*128 + e] (staged) = merge of the block partial words of (b, h) in block order.
 // Thread t owns E outputs of one (b, h), as E/4 groups of 4 spaced HD/(E/4)
 // apart (so a warp's loads stay contiguous); per round it loads, for J
 // blocks at once, each block's running max / sum and its outputs, waits
 // once, and folds them in (online, block order kept).
 template <int B>
-__device__ __forceinline__ void l_stage_attn(const MegaArgs& a, const XBufs& X, int l, float* xs) {
+__device__ __forceinline__ void l_stage_attn(const MegaArgs& a, const XBufs& X, int l, bf16* xf) {
     constexpr int E = B * NQ * HD / ll::NCT;  // outputs per thread
     constexpr int G4 = E / 4, GS = HD / G4;   // groups of 4 outputs, their spacing
-    constexpr int J = B == 1 ? 4 : 2;         // cache blocks per poll round
+    constexpr int J = B == 1 ? 3 : 2;         // cache blocks per poll round
     constexpr int W = 2 + E;                  // words per block
     constexpr int TPH = HD / E;               // threads per (b, h)
     const uint32_t ep = ep_p(a, l);
@@ -631,8 +683,8 @@ __device__ __forceinline__ void l_stage_attn(const MegaArgs& a, const XBufs& X, 
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll
     for (int g = 0; g < G4; ++g)
-        *reinterpret_cast<float4*>(xs + bh * HD + e0 + g * GS) =
-            make_float4(acc[4 * g] * inv, acc[4 * g + 1] * inv, acc[4 * g + 2] * inv, acc[4 * g + 3] * inv);
+        xf_put4(xf, NQ * HD, b, (bh - b * NQ) * HD + e0 + g * GS, acc[4 * g] * inv, acc[4 * g + 1] * inv,
+                acc[4 * g + 2] * inv, acc[4 * g + 3] * inv);
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -640,8 +692,8 @@ template <int B>
 __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__ MegaArgs a) {
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* ring_mem = smem;
-    float* xs = reinterpret_cast<float*>(smem + ll::RING);
-    float* hown = xs + ll::XS_FLOATS;                         // [B][OWN_MAX]
+    bf16* xf = reinterpret_cast<bf16*>(smem + ll::RING);     // staged activations of the current op
+    float* hown = reinterpret_cast<float*>(smem + ll::RING + ll::XF_BYTES);  // [B][OWN_MAX]
     float* att = hown + mk::MAXB * ll::OWN_MAX;
     float* part = att + ll::ATT_FLOATS;
     uint64_t* full = reinterpret_cast<uint64_t*>(part + ll::PART_FLOATS);
@@ -672,11 +724,12 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
                     int r0, r1;
                     l_rows(d.N, blockIdx.x, gridDim.x, r0, r1);
                     const int rpc = l_rpc(d.K);
+                    const uint32_t rs = (uint32_t)d.K * 2 + ll::ROW_PAD;  // ring row stride
                     for (int rc = r0; rc < r1 && ok; rc += rpc) {
                         const int nr = min(rpc, r1 - rc);
                         const uint32_t bytes = (uint32_t)nr * d.K * 2;
                         const uint32_t k = ring.k;
-                        const uint32_t p = ring.place(bytes);
+                        const uint32_t p = ring.place((uint32_t)nr * rs);
                         while (ok && (k - consumed >= (uint32_t)ll::NSLOT ||
                                       ring.head - tail > (unsigned long long)ll::RING)) {
                             const uint32_t s = consumed % ll::NSLOT;
@@ -692,11 +745,12 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
                         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(l_su32(full + slot)),
                                      "r"(bytes)
                                      : "memory");
-                        asm volatile(
-                            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                                l_su32(ring_mem + p)),
-                            "l"(d.W + (size_t)rc * d.K), "r"(bytes), "r"(l_su32(full + slot))
-                            : "memory");
+                        for (int i = 0; i < nr; ++i)  // one copy per row: rows land ROW_PAD bytes apart
+                            asm volatile(
+                                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                                    l_su32(ring_mem + p + (uint32_t)i * rs)),
+                                "l"(d.W + (size_t)(rc + i) * d.K), "r"((uint32_t)d.K * 2), "r"(l_su32(full + slot))
+                                : "memory");
                     }
                 }
             }
@@ -739,7 +793,9 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
 
     // page-table entries of blocks opened by this step (read by later launches)
     if (blockIdx.x == 0 && t < a.n_upd) const_cast<int32_t*>(a.page_table)[a.upd_idx[t]] = a.upd_val[t];
-    // layer-0 input: every CTA sums the embeddings itself; own rows are kept
+    // layer-0 input: every CTA sums the embeddings itself (fp32 in the attention
+    // scratch); own rows are kept
+    float* xs = att;
     for (int b = 0; b < B; ++b) {
         for (int c = t * 4; c < HID; c += ll::NCT * 4) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -771,7 +827,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
     l_named_sync();
     // norm of the layer-0 input straight from shared memory
     {
-        float* red = att;
+        float* red = part;
         for (int b = 0; b < B; ++b) {
             float ss = 0.f;
             for (int c = t; c < HID; c += ll::NCT) ss += xs[b * HID + c] * xs[b * HID + c];
@@ -784,7 +840,9 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
 #pragma unroll
             for (int w = 0; w < ll::NCW; ++w) ss += red[b * ll::NCW + w];
             const float r = rsqrtf(ss * (1.f / HID) + a.eps);
-            for (int c = t; c < HID; c += ll::NCT) xs[b * HID + c] *= r * bf2f(a.L[0].in_norm[c]);
+            for (int c = 2 * t; c < HID; c += 2 * ll::NCT)
+                xf_put2(xf, HID, b, c, xs[b * HID + c] * r * bf2f(a.L[0].in_norm[c]),
+                        xs[b * HID + c + 1] * r * bf2f(a.L[0].in_norm[c + 1]));
         }
     }
     l_named_sync();
@@ -797,7 +855,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
             a.trace[(size_t)blockIdx.x * a.n_layers * TRACE_STRIDE + 12] = smid;
         }
         if (l > 0) {
-            l_stage_norm<B>(a, xh_mine(X, 2 * l), ep_h(a, 2 * l), a.L[l].in_norm, xs, att);
+            l_stage_norm<B>(a, xh_mine(X, 2 * l), ep_h(a, 2 * l), a.L[l].in_norm, xf, att);
             l_named_sync();
         }
         LSTAMP(1);
@@ -805,7 +863,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
         {
             unsigned long long* qx = X.q + (size_t)(l & 1) * mk::MAXB * QKV;
             const uint32_t eq = ep_q(a, l);
-            l_consume<B, HID, 1>(a, l, rows_qkv, ring, ring_mem, full, empty, xs, part, -1,
+            l_consume<B, HID, (QKV + LL_MIN_GRID - 1) / LL_MIN_GRID / 16 + 1>(a, l, rows_qkv, ring, ring_mem, full, empty, xf, part, -1,
                          [&](int b, int row, float v0, bool two, float v1, int) {
                              ll_put(qx + (size_t)b * QKV + row, v0, eq);
                              if (two) ll_put(qx + (size_t)b * QKV + row + 1, v1, eq);
@@ -823,10 +881,10 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
         }
         LSTAMP(3);
         // ---- merge + o_proj + residual (own rows) -> h words (version 2l+1)
-        l_stage_attn<B>(a, X, l, xs);
+        l_stage_attn<B>(a, X, l, xf);
         l_named_sync();
         LSTAMP(4);
-        l_consume<B, NQ * HD, 8>(a, l, rows_o, ring, ring_mem, full, empty, xs, part, -1,
+        l_consume<B, NQ * HD, 1>(a, l, rows_o, ring, ring_mem, full, empty, xf, part, -1,
                      [&](int b, int row, float v0, bool two, float v1, int r0) {
                          hown[b * ll::OWN_MAX + row - r0] += v0;
                          if (two) hown[b * ll::OWN_MAX + row + 1 - r0] += v1;
@@ -843,13 +901,13 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
         }
         LSTAMP(5);
         // ---- gate/up + SwiGLU -> m words
-        l_stage_norm<B>(a, xh_mine(X, 2 * l + 1), ep_h(a, 2 * l + 1), a.L[l].post_norm, xs, att);
+        l_stage_norm<B>(a, xh_mine(X, 2 * l + 1), ep_h(a, 2 * l + 1), a.L[l].post_norm, xf, att);
         l_named_sync();
         LSTAMP(6);
         {
             unsigned long long* mx = xm_base(X, l);
             const uint32_t em = ep_m(a, l);
-            l_consume<B, HID, 1>(a, l, rows_gu, ring, ring_mem, full, empty, xs, part, 10,
+            l_consume<B, HID, 4>(a, l, rows_gu, ring, ring_mem, full, empty, xf, part, 10,
                          [&](int b, int row, float g, bool, float u, int) {
                              const float m = g / (1.f + __expf(-g)) * u;
 #pragma unroll
@@ -873,12 +931,11 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
             for (int b = 0; b < B; ++b)
 #pragma unroll
                 for (int k = 0; k < 6; ++k)
-                    *reinterpret_cast<float2*>(xs + b * 3072 + 512 * k + 2 * t) =
-                        make_float2(ll_val(w[b * 12 + 2 * k]), ll_val(w[b * 12 + 2 * k + 1]));
+                    xf_put2(xf, 3072, b, 512 * k + 2 * t, ll_val(w[b * 12 + 2 * k]), ll_val(w[b * 12 + 2 * k + 1]));
         }
         l_named_sync();
         LSTAMP(8);
-        l_consume<B, 3072, 8>(a, l, rows_d, ring, ring_mem, full, empty, xs, part, 11,
+        l_consume<B, 3072, 1>(a, l, rows_d, ring, ring_mem, full, empty, xf, part, 11,
                      [&](int b, int row, float v0, bool two, float v1, int r0) {
                          hown[b * ll::OWN_MAX + row - r0] += v0;
                          if (two) hown[b * ll::OWN_MAX + row + 1 - r0] += v1;
@@ -900,12 +957,12 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
     // ---- final norm + head + argmax
     if (a.head) {
         const int vl = 2 * a.n_layers;
-        l_stage_norm<B>(a, xh_mine(X, vl), ep_h(a, vl), a.final_norm, xs, att);
+        l_stage_norm<B>(a, xh_mine(X, vl), ep_h(a, vl), a.final_norm, xf, att);
         l_named_sync();
         __shared__ unsigned long long best_s[mk::MAXB];
         if (t < B) best_s[t] = 0ull;
         l_named_sync();
-        l_consume<B, HID, 1>(a, a.n_layers, rows_head, ring, ring_mem, full, empty, xs, part, -1,
+        l_consume<B, HID, 4>(a, a.n_layers, rows_head, ring, ring_mem, full, empty, xf, part, -1,
                      [&](int b, int row, float v0, bool two, float v1, int) {
                          if (a.logits) {
                              a.logits[(size_t)b * a.head_rows + row] = v0;
@@ -939,8 +996,12 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
 }
 
 int ll_smem_bytes() { return ll::SMEM; }
-static_assert((3072 * 2 + LL_MIN_GRID - 1) / LL_MIN_GRID <= 16 * MAXC, "gate/up slice exceeds MAXC chunks");
-static_assert((3072 * 2 + LL_MIN_GRID - 1) / LL_MIN_GRID * 2 * HID <= ll::RING, "gate/up slice exceeds the ring");
+static_assert((3072 * 2 + LL_MIN_GRID - 1) / LL_MIN_GRID <= l_rpc(HID) * MAXC, "gate/up slice exceeds MAXC chunks");
+static_assert((3072 * 2 + LL_MIN_GRID - 1) / LL_MIN_GRID * (2 * HID + ll::ROW_PAD) <= ll::RING, "gate/up slice exceeds the ring");
+static_assert(l_rpc(HID) == 16 && l_rpc(NQ * HD) == 8 && l_rpc(3072) == 4, "ring chunk shapes");
+// tile counts at the call sites: o_proj and down slices fit one tile, gate/up and the head four
+static_assert((HID / 2 + LL_MIN_GRID - 1) / LL_MIN_GRID * 2 <= 16 && (3072 + LL_MIN_GRID - 1) / LL_MIN_GRID * 2 <= 64,
+              "op slices exceed their tile counts");
 static_assert((3072 * 2 + LL_MIN_GRID - 1) / LL_MIN_GRID <= PART_ROWS && PART_ROWS * mk::MAXB * ll::NCW <= ll::PART_FLOATS,
               "one op's rows exceed the partial buffer");
 uint32_t ll_epochs_per_launch(int n_layers) { return 6u * (uint32_t)n_layers + 8u; }

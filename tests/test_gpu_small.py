@@ -195,6 +195,28 @@ def test_talker_two_layers_teacher_forced():
         check_logits_and_argmax(np.array(gl), lg_o, np.array(ga), am_o)
 
 
+def test_decode_path_selection():
+    """Decode batches of one or two run as a single persistent launch; larger
+    batches take the multi-kernel path (guards against a silent fallback)."""
+    shape = small_talker(2)
+    w = synth.model_weights(shape, 25)
+    ids = synth.talker_prefill_ids(25, 8)
+    with Engine(w, max_slots=4, max_ctx=64, max_batch=4, max_tokens=64) as e:
+        m = e.m
+        m.tts_bb_prefill(e.h, 3, 8, [0, 1, 2], [8, 8, 8], dev_i32(np.stack([ids] * 3)))
+        lens = [8, 8, 8]
+        for B, want in ((1, True), (2, True), (3, False)):
+            m.tts_bb_profile(e.h, True)
+            m.tts_bb_decode_step(e.h, B, list(range(B)), lens[:B], dev_i32(ids[:B].copy()))
+            lens[:B] = [x + 1 for x in lens[:B]]
+            kinds = {k["kind"]: k["launches"] for k in m.tts_bb_profile_report(e.h)["kernels"]}
+            m.tts_bb_profile(e.h, False)
+            if want:
+                assert kinds == {"decode_step_persistent": 1}, (B, kinds)
+            else:
+                assert "decode_step_persistent" not in kinds and kinds, (B, kinds)
+
+
 # ---------------------------------------------------------------- ragged batches, chunked prefill, paging
 def test_ragged_prefill_chunks_and_batched_decode():
     shape = small_talker(2)
