@@ -424,14 +424,30 @@ def roofline_from_profile(rep, traffic=None):
             "launches": top["launches"]}
 
 
+# DRAM bytes (read + write) per launch of a kernel, from the ncu capture summarised under
+# profiles/ (decode_ll_talker_b1.md). Valid only while the kernel's sources are the ones that
+# were captured: the sha256 of the listed files must match, else the bench reports null.
+MEASURED_TRAFFIC = {
+    "decode_step_persistent": {"files": ("k_decode_ll.cu", "mega.cuh", "common.cuh"),
+                               "sha256": "d2b66b9605a035e2e1d08130240a2cafeb5e6ffe3be179a4a5bbd2a478b97496",
+                               "bytes_per_launch": 908.317184e6},
+}
+
+
 def measured_traffic(rep):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if one exists."""
-    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch of the dominant kernel from a capture of its current sources, or None."""
+    import hashlib
     ks = rep.get("kernels", [])
-    if not ks or not os.path.exists(tp):
+    if not ks:
         return None
-    with open(tp) as f:
-        return json.load(f).get(max(ks, key=lambda k: k["ms"])["kind"])
+    rec = MEASURED_TRAFFIC.get(max(ks, key=lambda k: k["ms"])["kind"])
+    if rec is None:
+        return None
+    h = hashlib.sha256()
+    for f in rec["files"]:
+        with open(os.path.join(ROOT, "codec_token_tts_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return rec["bytes_per_launch"] if h.hexdigest() == rec["sha256"] else None
 
 
 # ---------------------------------------------------------------- oracle timing (CPU baseline / reference arm)

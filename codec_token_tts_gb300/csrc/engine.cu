@@ -131,8 +131,6 @@ struct tts_bb {
     // persistent small-batch decode step
     int mega_grid = 0;                 // 0 = not available on this device
     int* mega_abort = nullptr;
-    float* mega_part = nullptr;
-    float* mega_m = nullptr;
     unsigned long long* ll_xbuf = nullptr;   // exchange words
     unsigned long long* ll_amax = nullptr;   // [MAXB], re-armed by the kernel
     unsigned int* ll_done = nullptr;
@@ -614,7 +612,7 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
     cudaMemset(h->err, 0, sizeof(int));
     tts_bb_status s = ensure_scratch(h, std::max(nb, std::max(c.max_tokens, 1)));
     if (s != TTS_BB_OK) return bail(s);
-    // persistent decode step: barrier counter, abort flag, block partials, constant arguments
+    // persistent decode step: abort flag, exchange words, argmax words, constant arguments
     if (c.max_slots > 0 && c.n_layers >= 1 && c.n_layers <= mk::MAXL && c.max_ctx <= 64 * KVB && c.ffn == 3072 && (c.n_heads == 0 || (c.head_rows % 2 == 0 && c.head_rows <= 6144)) && c.text_vocab == 0) {
         h->mega_grid = ll_max_grid();
         cudaGetLastError();
@@ -623,8 +621,6 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
         if (h->mega_grid > 0) {
             const size_t xw = ll_xbuf_words(h->mbps);
             if ((e = dalloc(h, &h->mega_abort, 1)) != cudaSuccess ||
-                (e = dalloc(h, &h->mega_part, (size_t)mk::MAXB * NQ * h->mbps * PART_STRIDE)) != cudaSuccess ||
-                (e = dalloc(h, &h->mega_m, (size_t)mk::MAXB * c.ffn)) != cudaSuccess ||
                 (e = dalloc(h, &h->ll_xbuf, xw)) != cudaSuccess || (e = dalloc(h, &h->ll_amax, mk::MAXB)) != cudaSuccess ||
                 (e = dalloc(h, &h->ll_done, 1)) != cudaSuccess)
                 return bail(TTS_BB_E_OOM);
@@ -647,8 +643,6 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
             ma->mbps = h->mbps;
             ma->h = h->h;
             ma->qkv = h->qkv;
-            ma->m = h->mega_m;
-            ma->part = h->mega_part;
             ma->nblk_max = h->mbps;
             ma->amax = h->ll_amax;
             ma->abort_flag = h->mega_abort;

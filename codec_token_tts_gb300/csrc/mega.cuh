@@ -40,8 +40,6 @@ struct MegaArgs {
     int upd_val[mk::MAXB];
     float* h;                  // [B][HID] residual (fp32)
     float* qkv;                // [B][QKV]
-    float* m;                  // [B][ffn] SwiGLU output (fp32)
-    float* part;               // [B][16][nblk_max][PART_STRIDE]
     int nblk_max;
     unsigned long long* amax;  // [B]
     int* abort_flag;
