@@ -117,11 +117,15 @@ struct SplitK {
     int n_ctr;
 };
 // Plain bf16 activations with T > 8 run on tcgen05 (k_gemm_tc.cu); split
-// activations (X_lo) with T <= 256 run on the split-K mma.sync kernel when a
-// workspace is given, else on the tiled mma.sync kernel with a second MMA per k-step.
+// activations (X_lo) with 8 < T <= 128 run on the swap-AB cluster split-K
+// tcgen05 kernel (k_gemm_tc.cu), with T <= 256 on the split-K mma.sync kernel
+// when a workspace is given, else on the tiled mma.sync kernel with a second
+// MMA per k-step.
 int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st,
                 const bf16* X_lo = nullptr, int* err = nullptr, const SplitK* sk = nullptr);
 int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, int* err, cudaStream_t st);
+int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N, int K, const Epi& e, int* err,
+                    cudaStream_t st);
 bool gemm_tc_available();
 
 // Per-token q/k RMSNorm + RoPE; q -> qout [T][16][128] bf16; k, v -> paged pool.

@@ -13,6 +13,10 @@
 // Every mbarrier wait is bounded; on timeout the CTA raises the error word,
 // stops issuing work, waits (bounded) for its copies in flight, frees TMEM and
 // returns.
+#include <algorithm>
+#include <mutex>
+#include <unordered_map>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -297,6 +301,296 @@ __global__ void __launch_bounds__(tc::NT, 1)
     }
 }
 
+// ---------------------------------------------------------------- decode batches (8 < T <= 128)
+// Y = (X_hi + X_lo) W^T for a handful of tokens, weights streamed once. The
+// roles swap so the weights fill the 128-row M side: A = a 128-row tile of W,
+// B = the tokens' high parts (rows 0..TB-1) stacked on their low parts
+// (rows TB..2TB-1), N = 2 TB. The S CTAs of one thread-block cluster split K
+// for one 128-row tile; each sums hi + lo per token into its shared memory.
+// After a cluster barrier, CTA r owns tokens [r T / S, (r+1) T / S): every
+// CTA pushes each peer's token slice of its partial with one bulk copy into
+// that peer's receive buffer (completion on the peer's mbarrier); the owner
+// adds the S partials in rank order (deterministic) and applies the epilogue,
+// one thread per output feature.
+namespace tcd {
+constexpr int BM = 128, BK = 64, STAGES = 4, NT = 192;
+constexpr int MAXTB = 128;                          // padded tokens per launch
+constexpr int A_BYTES = BM * BK * 2;                // 16 KB
+constexpr int STAGE = A_BYTES + 2 * MAXTB * BK * 2; // 48 KB
+constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+constexpr int MAXS = 16;
+static_assert((2 * MAXTB + MAXS) * BM * 4 <= STAGES * STAGE, "partials and receive buffer must fit the stages");
+}  // namespace tcd
+constexpr unsigned long long TIMEOUT_NS_TCD = tc::TIMEOUT_NS;
+
+// Address of `local` in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(s_addr(local)), "r"(rank));
+    return remote;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Epilogue arguments held in registers (the kernel's Epi lives in local
+// memory; stores through its generic pointers would force reloads).
+struct TcdOut {
+    float* __restrict__ f32;          // STORE / ADD / LOGITS output (LOGITS: may be null)
+    bf16* __restrict__ hi;            // SWIGLU output
+    bf16* __restrict__ lo;            // SWIGLU low part (may be null)
+    unsigned long long* __restrict__ amax;
+    int ldo;
+};
+
+// Sum, in rank order, the S partials of tokens [t0, t1) (this CTA's own
+// partial in `red`, the peers' in `recv`) and apply the epilogue. Epilogue
+// warp w takes tokens t0 + w, t0 + w + 4, ...; lane l takes the four features
+// n0 + 4l .. 4l + 3 (vector loads and stores; a gate/up pair stays in one lane).
+template <int MODE>
+__device__ __forceinline__ void tcd_reduce(const TcdOut o, const float* __restrict__ red, const float* __restrict__ recv,
+                                           int t0, int t1, uint32_t S, uint32_t r, int n0, int N, int w, int lane) {
+    constexpr int BM = tcd::BM;
+    const int nt_all = t1 - t0, f = lane * 4, n = n0 + f;
+    for (int t = t0 + w; t < t1; t += 4) {
+        const int tl = t - t0;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int p0 = 0; p0 < (int)S; p0 += 4) {
+            float4 x[4];
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                const int p = min(p0 + pp, (int)S - 1);
+                const float* src = p == (int)r ? red + (size_t)t * BM + f : recv + ((size_t)p * nt_all + tl) * BM + f;
+                x[pp] = *reinterpret_cast<const float4*>(src);
+            }
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp)
+                if (p0 + pp < (int)S) { v.x += x[pp].x; v.y += x[pp].y; v.z += x[pp].z; v.w += x[pp].w; }
+        }
+        const size_t row = (size_t)t * o.ldo;
+        if (MODE == EPI_STORE_F32 || MODE == EPI_ADD_F32) {
+            float* dst = o.f32 + row + n;
+            if (n + 4 <= N) {
+                if (MODE == EPI_ADD_F32) {
+                    const float4 h = *reinterpret_cast<const float4*>(dst);
+                    v.x += h.x; v.y += h.y; v.z += h.z; v.w += h.w;
+                }
+                *reinterpret_cast<float4*>(dst) = v;
+            } else {
+                const float vv[4] = {v.x, v.y, v.z, v.w};
+                for (int j = 0; j < 4 && n + j < N; ++j) dst[j] = (MODE == EPI_ADD_F32 ? dst[j] : 0.f) + vv[j];
+            }
+        } else if (MODE == EPI_SWIGLU) {  // features (2i, 2i+1) = (gate_i, up_i)
+            if (n + 4 <= N) {
+                const float m0 = silu_tc(v.x) * v.y, m1 = silu_tc(v.z) * v.w;
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(m0, m1);
+                *reinterpret_cast<__nv_bfloat162*>(o.hi + row + n / 2) = h2;
+                if (o.lo) *reinterpret_cast<__nv_bfloat162*>(o.lo + row + n / 2) = __halves2bfloat162(f2bf_lo(m0), f2bf_lo(m1));
+            } else if (n + 2 <= N) {
+                const float m0 = silu_tc(v.x) * v.y;
+                o.hi[row + n / 2] = f2bf(m0);
+                if (o.lo) o.lo[row + n / 2] = f2bf_lo(m0);
+            }
+        } else {  // EPI_LOGITS
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+            unsigned long long best = 0ull;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (n + j < N) {
+                    if (o.f32) o.f32[row + n + j] = vv[j];
+                    const unsigned long long pk = pack_argmax(vv[j], n + j);
+                    best = pk > best ? pk : best;
+                }
+#pragma unroll
+            for (int sh = 16; sh >= 1; sh >>= 1) {
+                const unsigned long long x = __shfl_xor_sync(0xffffffffu, best, sh);
+                best = x > best ? x : best;
+            }
+            if (lane == 0 && o.amax && best) atomicMax(o.amax + t, best);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(tcd::NT, 1)
+    k_gemm_tcd(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmXh,
+               const __grid_constant__ CUtensorMap tmXl, int T, int TB, int N, int K, const __grid_constant__ Epi e,
+               int* err) {
+    using namespace tcd;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE);
+    uint64_t* empty = full + STAGES;
+    uint64_t* accf = empty + STAGES;
+    uint64_t* recvb = accf + 1;  // peers' slices of this CTA's tokens have landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recvb + 1);
+    volatile int* abort_s = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // over the stages once the MMAs are done: this CTA's partial sums [TB][128], then the
+    // receive buffer [S][tokens of this CTA][128]
+    float* red = reinterpret_cast<float*>(smem);
+    float* recv = red + MAXTB * BM;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t S, r;
+    asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(S));
+    asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    const int n0 = (int)(blockIdx.x / S) * BM;
+    const int KT = K / BK, kb0 = (int)(r * KT / S), nk = (int)((r + 1) * KT / S) - kb0;
+    const uint32_t b_bytes = 2u * TB * BK * 2, ncols = 2u * TB;
+    const uint32_t tcols = ncols <= 32 ? 32 : ncols <= 64 ? 64 : ncols <= 128 ? 128 : 256;
+    // kind::f16, D f32, A/B bf16 K-major, N = 2 TB, M = 128
+    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((ncols >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            tc_mbar_init(full + s, 1);
+            tc_mbar_init(empty + s, 1);
+        }
+        tc_mbar_init(accf, 1);
+        tc_mbar_init(recvb, 1);
+        *abort_s = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(s_addr(tmem_slot)),
+                     "r"(tcols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {  // TMA producer
+            int issued = 0;
+            for (int i = 0; i < nk; ++i) {
+                const int s = i % STAGES;
+                if (i >= STAGES && !tc_wait(empty + s, ((i / STAGES) - 1) & 1, abort_s)) {
+                    *abort_s = 1;
+                    break;
+                }
+                unsigned char* st = smem + s * STAGE;
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(full + s)),
+                             "r"((uint32_t)A_BYTES + b_bytes)
+                             : "memory");
+                const int kx = (kb0 + i) * BK;
+                tma_load_2d(st, &tmW, kx, n0, full + s);
+                tma_load_2d(st + A_BYTES, &tmXh, kx, 0, full + s);
+                tma_load_2d(st + A_BYTES + TB * BK * 2, &tmXl, kx, 0, full + s);
+                ++issued;
+            }
+            if (*abort_s) {
+                for (int i = 0; i < issued; ++i) {
+                    const unsigned long long t0 = g_time();
+                    while (!tc_mbar_try(full + i % STAGES, (i / STAGES) & 1) && g_time() - t0 < TIMEOUT_NS_TCD) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // MMA issuer
+            for (int i = 0; i < nk; ++i) {
+                const int s = i % STAGES;
+                if (!tc_wait(full + s, (i / STAGES) & 1, abort_s)) {
+                    *abort_s = 1;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t a0 = s_addr(smem + s * STAGE), b0 = a0 + A_BYTES;
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k) {
+                    const uint64_t ad = sw128_desc(a0 + k * 32), bd = sw128_desc(b0 + k * 32);
+                    const uint32_t acc = (i | k) ? 1u : 0u;
+                    asm volatile(
+                        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem),
+                        "l"(ad), "l"(bd), "r"(idesc), "r"(acc));
+                }
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                    s_addr(empty + s))
+                             : "memory");
+            }
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                s_addr(accf))
+                         : "memory");
+        }
+    } else {
+        // partial sums: thread = feature q * 32 + lane; column c < TB is token c's high part, TB + c its low part
+        const int q = warp & 3, f = q * 32 + lane;
+        const bool ok = tc_wait(accf, 0, abort_s) && !*abort_s;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (ok) {
+            for (int c = 0; c < TB; c += 16) {
+                uint32_t hi[16], lo[16];
+                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c;
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+                    "[%16];"
+                    : "=r"(hi[0]), "=r"(hi[1]), "=r"(hi[2]), "=r"(hi[3]), "=r"(hi[4]), "=r"(hi[5]), "=r"(hi[6]),
+                      "=r"(hi[7]), "=r"(hi[8]), "=r"(hi[9]), "=r"(hi[10]), "=r"(hi[11]), "=r"(hi[12]), "=r"(hi[13]),
+                      "=r"(hi[14]), "=r"(hi[15])
+                    : "r"(ta));
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+                    "[%16];"
+                    : "=r"(lo[0]), "=r"(lo[1]), "=r"(lo[2]), "=r"(lo[3]), "=r"(lo[4]), "=r"(lo[5]), "=r"(lo[6]),
+                      "=r"(lo[7]), "=r"(lo[8]), "=r"(lo[9]), "=r"(lo[10]), "=r"(lo[11]), "=r"(lo[12]), "=r"(lo[13]),
+                      "=r"(lo[14]), "=r"(lo[15])
+                    : "r"(ta + (uint32_t)TB));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                for (int j = 0; j < 16; ++j) red[(c + j) * BM + f] = __uint_as_float(hi[j]) + __uint_as_float(lo[j]);
+            }
+        } else if (lane == 0 && q == 0) {
+            set_err(err, ERR_TIMEOUT);
+        }
+    }
+    // tokens owned by CTA q: [tok(q), tok(q + 1))
+    auto tok = [&](uint32_t q) { return (int)(q * (uint32_t)T / S); };
+    const int t0 = tok(r), t1 = tok(r + 1);
+    if (threadIdx.x == 0)  // expect the S - 1 peers' slices of this CTA's tokens
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(recvb)),
+                     "r"((uint32_t)((S - 1) * (t1 - t0) * BM * 4))
+                     : "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    cluster_sync_all();  // every CTA's partials are in its shared memory, every receive barrier armed
+    if (threadIdx.x == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // partials written by threads -> bulk copy reads
+        for (uint32_t q = 0; q < S; ++q) {
+            const int a0 = tok(q), a1 = tok(q + 1);
+            if (q == r || a1 == a0) continue;
+            // my partial of q's tokens -> q's receive slot r
+            const uint32_t dst = dsmem_addr(recv + (size_t)r * (a1 - a0) * BM, q);
+            const uint32_t bar = dsmem_addr(recvb, q);
+            asm volatile(
+                "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                "r"(s_addr(red + (size_t)a0 * BM)), "r"((uint32_t)((a1 - a0) * BM * 4)), "r"(bar)
+                : "memory");
+        }
+    }
+    if (warp >= 2) {
+        const bool got = t1 == t0 || S == 1 || tc_wait(recvb, 0, abort_s);
+        if (!got && lane == 0 && warp == 2) set_err(err, ERR_TIMEOUT);
+        TcdOut o;
+        o.f32 = reinterpret_cast<float*>(e.out);
+        o.hi = reinterpret_cast<bf16*>(e.out);
+        o.lo = reinterpret_cast<bf16*>(e.out_lo);
+        o.amax = e.amax;
+        o.ldo = e.ldo;
+        const int w = warp - 2;
+        switch (e.mode) {
+            case EPI_STORE_F32: tcd_reduce<EPI_STORE_F32>(o, red, recv, t0, t1, S, r, n0, N, w, lane); break;
+            case EPI_ADD_F32: tcd_reduce<EPI_ADD_F32>(o, red, recv, t0, t1, S, r, n0, N, w, lane); break;
+            case EPI_SWIGLU: tcd_reduce<EPI_SWIGLU>(o, red, recv, t0, t1, S, r, n0, N, w, lane); break;
+            default: tcd_reduce<EPI_LOGITS>(o, red, recv, t0, t1, S, r, n0, N, w, lane); break;
+        }
+    }
+    cluster_sync_all();  // peers are done reading this CTA's partials
+    if (warp == 1) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tcols));
+    }
+}
+
 // ---------------------------------------------------------------- host side
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -312,7 +606,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D bf16 tensor [rows][K] (K contiguous), box [box_rows][64], 128-byte swizzle.
-static bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
+static bool encode_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
@@ -324,7 +618,99 @@ static bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Encoded maps are cached by (base, rows, K, box rows): weights never move and
+// the engine's activation buffers are fixed, so a decode step re-encodes
+// nothing. The cache is per process and guarded by a mutex; a full cache
+// is cleared (maps are cheap to re-encode).
+static bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
+    struct Key {
+        const void* base;
+        int rows, K, box;
+        bool operator==(const Key& o) const { return base == o.base && rows == o.rows && K == o.K && box == o.box; }
+    };
+    struct KeyHash {
+        size_t operator()(const Key& k) const {
+            size_t h = std::hash<const void*>()(k.base);
+            h ^= (size_t)k.rows * 0x9E3779B97F4A7C15ull + (size_t)k.K * 0xC2B2AE3D27D4EB4Full + (size_t)k.box;
+            return h;
+        }
+    };
+    static std::mutex mu;
+    static std::unordered_map<Key, CUtensorMap, KeyHash> cache;
+    const Key key{base, rows, K, box_rows};
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            *m = it->second;
+            return true;
+        }
+    }
+    if (!encode_map(m, base, rows, K, box_rows)) return false;
+    std::lock_guard<std::mutex> g(mu);
+    if (cache.size() > 4096) cache.clear();
+    cache.emplace(key, *m);
+    return true;
+}
+
 bool gemm_tc_available() { return encode_fn() != nullptr; }
+
+// X_lo-carrying GEMM for 8 < T <= 128 tokens on tcgen05 (swap-AB, cluster
+// split-K). Returns the number of kernels launched (0 if unsupported).
+int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N, int K, const Epi& e, int* err,
+                    cudaStream_t st) {
+    if (T <= 0 || T > tcd::MAXTB || N <= 0 || K % tcd::BK != 0 || !X_lo) return 0;
+    if (e.mode != EPI_STORE_F32 && e.mode != EPI_ADD_F32 && e.mode != EPI_SWIGLU && e.mode != EPI_LOGITS) return 0;
+    const int TB = (T + 15) / 16 * 16;
+    CUtensorMap mw, mh, ml;
+    if (!make_map(&mw, W, N, K, tcd::BM) || !make_map(&mh, X, T, K, TB) || !make_map(&ml, X_lo, T, K, TB)) return 0;
+    // clusters of each size that fit at once (1 CTA per SM): S is chosen so all clusters run in one wave
+    static const int cand[] = {1, 2, 3, 4, 6, 8, 12, 16};
+    static int fit[8] = {-1};
+    if (fit[0] < 0) {
+        cudaFuncSetAttribute(k_gemm_tcd, cudaFuncAttributeMaxDynamicSharedMemorySize, tcd::SMEM);
+        const bool nonport = cudaFuncSetAttribute(k_gemm_tcd, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+        for (int i = 0; i < 8; ++i) {
+            fit[i] = 0;
+            if (cand[i] > 8 && !nonport) continue;
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(cand[i]);
+            q.blockDim = dim3(tcd::NT);
+            q.dynamicSmemBytes = tcd::SMEM;
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = cand[i];
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            q.attrs = qa;
+            q.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tcd, &q) == cudaSuccess) fit[i] = n;
+        }
+        cudaGetLastError();
+    }
+    const int tiles = (N + tcd::BM - 1) / tcd::BM, KT = K / tcd::BK;
+    int S = 1, best = 0;
+    for (int i = 0; i < 8; ++i)  // the most CTAs whose clusters all fit in one wave
+        if (cand[i] <= KT && tiles <= fit[i] && tiles * cand[i] > best) {
+            best = tiles * cand[i];
+            S = cand[i];
+        }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles * S);
+    cfg.blockDim = dim3(tcd::NT);
+    cfg.dynamicSmemBytes = tcd::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = S;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_gemm_tcd, mw, mh, ml, T, TB, N, K, e, err) == cudaSuccess ? 1 : 0;
+}
+
 
 // Y = X W^T on tcgen05. Requires K % 64 == 0, 16-byte aligned X and W rows.
 // Returns the number of kernels launched (0 if the shape is not supported).

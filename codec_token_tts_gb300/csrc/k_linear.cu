@@ -508,6 +508,10 @@ int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e,
                 int* err, const SplitK* skw) {
     if (T <= 0) return 0;
     if (T <= 8) return launch_gemv(X, W, T, N, K, e, st, X_lo);
+    if (X_lo && T <= 128 && gemm_tc_available()) {
+        const int n = launch_gemm_tcd(X, X_lo, W, T, N, K, e, err, st);
+        if (n) return n;
+    }
     if (X_lo && skw) {
         const int n = launch_splitk(X, X_lo, W, T, N, K, e, *skw, st);
         if (n) return n;
