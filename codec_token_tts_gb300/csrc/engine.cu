@@ -49,6 +49,57 @@ __global__ void k_setup(SetupArgs a, int32_t* seq_slot, int32_t* seq_start, int3
     for (int i = threadIdx.x; i < a.n_upd; i += blockDim.x) page_table[a.upd_idx[i]] = a.upd_val[i];
 }
 
+// Per-call state of a decode step replayed from a CUDA graph: the setup
+// arguments and the caller's pointers, refreshed by one host-to-device copy
+// before each replay, so every captured launch keeps fixed parameters.
+struct StepBlock {
+    SetupArgs a;
+    const int32_t* ids;      // [B][n_codebooks] or null
+    const bf16* embeds;      // [B][HID] or null
+    float* logits_out;       // [B][head_rows] or null
+    int32_t* argmax_out;     // stride argmax_stride, or null
+    int argmax_stride;
+    float* hidden_out;       // [B][HID] or null
+};
+
+// Graph-step setup: block 0 does k_setup's work from the step block; block b
+// copies token b's ids / embeddings into the engine's fixed input buffers.
+__global__ void k_step_setup(const StepBlock* __restrict__ sb, int n_cb, int32_t* seq_slot, int32_t* seq_start,
+                             int32_t* seq_len, int32_t* key_len, int32_t* page_table, unsigned long long* amax,
+                             int32_t* ids_buf, bf16* emb_buf) {
+    const SetupArgs& a = sb->a;
+    const int b = blockIdx.x;
+    if (b == 0) {
+        for (int i = threadIdx.x; i < a.B; i += blockDim.x) {
+            seq_slot[i] = a.slot[i];
+            seq_start[i] = a.start[i];
+            seq_len[i] = a.len[i];
+            key_len[i] = a.key_len[i];
+            if (a.clear_amax) amax[i] = 0ull;
+        }
+        for (int i = threadIdx.x; i < a.n_upd; i += blockDim.x) page_table[a.upd_idx[i]] = a.upd_val[i];
+    }
+    if (b < a.B) {
+        if (ids_buf && sb->ids)
+            for (int k = threadIdx.x; k < n_cb; k += blockDim.x) ids_buf[b * n_cb + k] = sb->ids[(size_t)b * n_cb + k];
+        if (emb_buf && sb->embeds)
+            for (int i = threadIdx.x; i < HID; i += blockDim.x) emb_buf[(size_t)b * HID + i] = sb->embeds[(size_t)b * HID + i];
+    }
+}
+
+// Graph-step outputs: block b copies token b's logits, argmax and final hidden
+// state to the caller's pointers from the step block.
+__global__ void k_step_publish(const StepBlock* __restrict__ sb, const float* logits, int rows,
+                               const unsigned long long* amax, const float* hid) {
+    const int b = blockIdx.x;
+    if (logits && sb->logits_out)
+        for (int i = threadIdx.x; i < rows; i += blockDim.x) sb->logits_out[(size_t)b * rows + i] = logits[(size_t)b * rows + i];
+    if (amax && sb->argmax_out && threadIdx.x == 0)
+        sb->argmax_out[(size_t)b * sb->argmax_stride] = (int32_t)(0xFFFFFFFFu - (uint32_t)(amax[b] & 0xFFFFFFFFull));
+    if (hid && sb->hidden_out)
+        for (int i = threadIdx.x; i < HID; i += blockDim.x) sb->hidden_out[(size_t)b * HID + i] = hid[(size_t)b * HID + i];
+}
+
 __global__ void k_kv_copy(bf16* pool, const int32_t* page_table, int slot, int mbps, int pos0, int n, bf16* k,
                           bf16* v, int to_pool, int n_blocks, int* err) {
     // one CTA per token, 256 threads: 8 kv heads x 128 elements, 4 per thread for K and V
@@ -144,6 +195,25 @@ struct tts_bb {
     long unit_split_n[2] = {0, 0};
     double ring_wait[2] = {0, 0};      // persistent step: weight-ring waits inside gate/up and down
     long ring_wait_n = 0;
+    // multi-kernel decode steps replayed from CUDA graphs
+    static constexpr int RING = 8;
+    bool graphs_on = false;
+    StepBlock* d_step = nullptr;       // device step block (read by the captured setup / publish)
+    StepBlock* h_ring = nullptr;       // pinned staging, RING entries
+    cudaEvent_t ring_ev[RING] = {};
+    bool ring_used[RING] = {};
+    int ring_i = 0;
+    int32_t* ids_buf = nullptr;        // [max_batch][n_codebooks]
+    bf16* emb_buf = nullptr;           // [max_batch][HID]
+    float* logits_buf = nullptr;       // [max_batch][head_rows]
+    struct DecodeGraph {
+        int key[7];
+        int seen = 0;                  // calls with this key (the first runs eagerly)
+        cudaGraphExec_t exec = nullptr;
+        uint64_t n_kernels = 0;
+        bool bad = false;              // capture failed: stay eager
+    };
+    std::vector<DecodeGraph> graphs;
 };
 
 namespace {
@@ -351,7 +421,7 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
 
 // Final norm of B selected rows + head GEMM with logits / argmax.
 void run_head(tts_bb* h, int B, int per_seq, int head_idx, bool last_of_seq, float* logits_out, int32_t* argmax_out,
-              int argmax_stride, bool split = false) {
+              int argmax_stride, bool split = false, bool finalize = true) {
     const tts_bb_config& c = h->cfg;
     bf16* ylo = split ? h->y_lo : nullptr;
     { Launch L(h, K_RMSNORM, B * 6.0 * HID + 2.0 * HID);
@@ -361,7 +431,7 @@ void run_head(tts_bb* h, int B, int per_seq, int head_idx, bool last_of_seq, flo
     { Launch L(h, B <= 8 ? K_GEMV : (split ? (B <= 128 ? K_GEMM_TCD : K_GEMM) : K_GEMM_TC), gemm_bytes(B, c.head_rows, HID, logits_out ? 4 : 0), 2.0 * B * c.head_rows * HID);
       L += launch_gemm(h->y, h->heads[head_idx], B, c.head_rows, HID, e, h->st, ylo, h->err,
                         split && h->sk.part ? &h->sk : nullptr); }
-    if (argmax_out) { Launch L(h, K_ARGMAX); L += launch_argmax_finalize(h->amax, argmax_out, argmax_stride, B, h->st); }
+    if (argmax_out && finalize) { Launch L(h, K_ARGMAX); L += launch_argmax_finalize(h->amax, argmax_out, argmax_stride, B, h->st); }
 }
 
 bool slots_ok(tts_bb* h, int B, const int32_t* slots) {
@@ -415,6 +485,83 @@ tts_bb_status grow_slots(tts_bb* h, int B, const int32_t* slots, const int* new_
     return TTS_BB_OK;
 }
 
+// Enqueue the multi-kernel decode step of the captured graph for this call's
+// shape (B, head, which inputs and outputs), capturing it on the key's second
+// call (the first runs eagerly, so every launcher's one-time setup has run).
+// Per-call state travels in the step block; returns false to run eagerly.
+bool decode_step_graph(tts_bb* h, int B, int head_idx, const int32_t* ids, const void* embeds, float* logits_out,
+                       int32_t* argmax_out, int argmax_stride, float* hidden_out, const SetupArgs& a,
+                       tts_bb_status& st) {
+    const tts_bb_config& c = h->cfg;
+    const bool want_head = head_idx >= 0 && (logits_out || argmax_out);
+    const int key[7] = {B, want_head ? head_idx : -1, ids != nullptr, embeds != nullptr, logits_out != nullptr,
+                        argmax_out != nullptr, hidden_out != nullptr};
+    tts_bb::DecodeGraph* g = nullptr;
+    for (auto& x : h->graphs)
+        if (std::memcmp(x.key, key, sizeof key) == 0) g = &x;
+    if (!g) {
+        h->graphs.emplace_back();
+        g = &h->graphs.back();
+        std::memcpy(g->key, key, sizeof key);
+    }
+    if (g->bad || g->seen++ == 0) return false;
+    // stage this call's state: wait until the ring entry's previous copy has been consumed
+    const int i = h->ring_i;
+    h->ring_i = (i + 1) % tts_bb::RING;
+    if (h->ring_used[i]) cudaEventSynchronize(h->ring_ev[i]);
+    StepBlock& sb = h->h_ring[i];
+    std::memcpy(&sb.a, &a, sizeof(SetupArgs));
+    sb.ids = ids;
+    sb.embeds = reinterpret_cast<const bf16*>(embeds);
+    sb.logits_out = logits_out;
+    sb.argmax_out = argmax_out;
+    sb.argmax_stride = argmax_stride;
+    sb.hidden_out = hidden_out;
+    if (!g->exec) {
+        const uint64_t before = h->launches;
+        cudaGraph_t graph = nullptr;
+        bool ok = cudaStreamBeginCapture(h->st, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+        if (ok) {
+            k_step_setup<<<B, 256, 0, h->st>>>(h->d_step, c.n_codebooks, h->seq_slot, h->seq_start, h->seq_len,
+                                                h->key_len, h->d_page_table, h->amax, ids ? h->ids_buf : nullptr,
+                                                embeds ? h->emb_buf : nullptr);
+            h->launches += 1;
+            h->launches += launch_embed_codebooks(h->tabs, ids ? h->ids_buf : nullptr, embeds ? h->emb_buf : nullptr,
+                                                  h->h, B, h->err, h->st);
+            KVView kv{h->pool, h->d_page_table, h->seq_slot, h->mbps};
+            run_layers(h, B, 1, 0, c.max_ctx, kv, h->layer_elems, 0);  // attention grid sized for max_ctx
+            if (want_head)
+                run_head(h, B, 1, head_idx, false, logits_out ? h->logits_buf : nullptr, argmax_out, 1, true, false);
+            k_step_publish<<<B, 256, 0, h->st>>>(h->d_step, want_head && logits_out ? h->logits_buf : nullptr,
+                                                  c.head_rows, want_head && argmax_out ? h->amax : nullptr,
+                                                  hidden_out ? h->h : nullptr);
+            h->launches += 1;
+            ok = cudaStreamEndCapture(h->st, &graph) == cudaSuccess && graph;
+        }
+        if (ok) ok = cudaGraphInstantiate(&g->exec, graph, 0) == cudaSuccess;
+        if (graph) cudaGraphDestroy(graph);
+        g->n_kernels = h->launches - before;
+        h->launches = before;
+        if (!ok) {
+            cudaGetLastError();
+            g->bad = true;
+            g->exec = nullptr;
+            return false;
+        }
+    }
+    cudaError_t e = cudaMemcpyAsync(h->d_step, &sb, sizeof(StepBlock), cudaMemcpyHostToDevice, h->st);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ring_ev[i], h->st);
+    h->ring_used[i] = true;
+    if (e == cudaSuccess) e = cudaGraphLaunch(g->exec, h->st);
+    if (e != cudaSuccess) {
+        st = cuda_fail(h, e, "decode step graph");
+        return true;
+    }
+    h->launches += g->n_kernels;
+    st = finish(h);
+    return true;
+}
+
 }  // namespace
 
 // ============================================================== C ABI
@@ -454,6 +601,11 @@ TTS_API void tts_bb_free(tts_bb* h) {
     cudaSetDevice(h->dev);
     if (h->st) cudaStreamSynchronize(h->st);
     else cudaDeviceSynchronize();
+    for (auto& g : h->graphs)
+        if (g.exec) cudaGraphExecDestroy(g.exec);
+    for (int i = 0; i < tts_bb::RING; ++i)
+        if (h->ring_ev[i]) cudaEventDestroy(h->ring_ev[i]);
+    if (h->h_ring) cudaFreeHost(h->h_ring);
     for (void* p : h->allocs) cudaFree(p);
     if (h->h_err) cudaFreeHost(h->h_err);
     for (auto& r : h->prof) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
@@ -608,6 +760,18 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
         if ((e = dalloc(h, &h->sk.part, h->sk.part_elems)) != cudaSuccess || (e = dalloc(h, &h->sk.ctr, 256)) != cudaSuccess)
             return bail(TTS_BB_E_OOM);
         cudaMemset(h->sk.ctr, 0, 256 * sizeof(int));
+    }
+    if (c.max_slots > 0) {  // graph-replayed decode steps: step block, staging ring, fixed input / output buffers
+        const char* gv = std::getenv("TTS_BB_GRAPHS");
+        h->graphs_on = !(gv && std::strcmp(gv, "0") == 0);
+        if ((e = dalloc(h, &h->d_step, 1)) != cudaSuccess ||
+            (e = dalloc(h, &h->ids_buf, (size_t)c.max_batch * std::max(c.n_codebooks, 1))) != cudaSuccess ||
+            (e = dalloc(h, &h->emb_buf, (size_t)c.max_batch * HID)) != cudaSuccess ||
+            (e = dalloc(h, &h->logits_buf, (size_t)c.max_batch * std::max(c.head_rows, 1))) != cudaSuccess ||
+            cudaMallocHost(&h->h_ring, tts_bb::RING * sizeof(StepBlock)) != cudaSuccess)
+            return bail(TTS_BB_E_OOM);
+        for (int i = 0; i < tts_bb::RING; ++i)
+            if (cudaEventCreateWithFlags(&h->ring_ev[i], cudaEventDisableTiming) != cudaSuccess) return bail(TTS_BB_E_CUDA);
     }
     cudaMemset(h->err, 0, sizeof(int));
     tts_bb_status s = ensure_scratch(h, std::max(nb, std::max(c.max_tokens, 1)));
@@ -817,6 +981,13 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
         if (opts && opts->hidden_out)
             cudaMemcpyAsync(opts->hidden_out, h->h, (size_t)B * HID * sizeof(float), cudaMemcpyDeviceToDevice, h->st);
         return finish(h);
+    }
+    if (h->graphs_on && !h->prof_on) {
+        tts_bb_status gs = TTS_BB_OK;
+        if (decode_step_graph(h, B, head_idx, ids, embeds, logits_out, argmax_out,
+                              opts && opts->argmax_stride ? opts->argmax_stride : 1, opts ? opts->hidden_out : nullptr, a,
+                              gs))
+            return gs;
     }
     launch_setup(h, a);
     {
