@@ -78,6 +78,7 @@ def _load() -> C.CDLL:
         "tts_bb_profile": (I, [P, I]),
         "tts_bb_profile_report": (C.c_char_p, [P]),
         "tts_bb_gqa_decode_attention_static": (I, [P, P, P, I, P, I, I, P, P]),
+        "tts_bb_debug_fault": (I, [P, I, C.c_int64]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -91,7 +92,7 @@ EXPORTED = ("tts_bb_default_config", "tts_bb_create", "tts_bb_free", "tts_bb_pre
             "tts_bb_maskgit_pass", "tts_bb_release", "tts_bb_truncate", "tts_bb_slot_len", "tts_bb_sync",
             "tts_bb_last_error", "tts_bb_version", "tts_bb_debug_kv_read", "tts_bb_debug_kv_write",
             "tts_bb_launch_count", "tts_bb_profile", "tts_bb_profile_report",
-            "tts_bb_gqa_decode_attention_static")
+            "tts_bb_gqa_decode_attention_static", "tts_bb_debug_fault")
 
 
 def _ptr(x) -> Optional[int]:
@@ -239,6 +240,14 @@ def tts_bb_profile(h, on: bool) -> int:
 def tts_bb_profile_report(h) -> dict:
     import json
     return json.loads(lib.tts_bb_profile_report(h).decode())
+
+
+DEBUG_WAIT_LIMIT_NS, DEBUG_STALL_NEXT_STEP = 1, 2
+
+
+def tts_bb_debug_fault(h, what: int, arg: int = 0) -> int:
+    """Failure-handling test hook (see include/tts_bb.h); returns the status."""
+    return lib.tts_bb_debug_fault(h, what, int(arg))
 
 
 def tts_bb_gqa_decode_attention_static(q, kv_pool, page_table, blocks_per_seq: int, positions, B: int,

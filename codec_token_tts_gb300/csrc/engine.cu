@@ -214,6 +214,10 @@ struct tts_bb {
         bool bad = false;              // capture failed: stay eager
     };
     std::vector<DecodeGraph> graphs;
+    // failure-handling test hooks (tts_bb_debug_fault, TTS_BB_FAIL_ALLOC_AT)
+    unsigned long n_allocs = 0;
+    unsigned long long wait_limit_ns = 2000000000ull;
+    int stall_next = 0;
 };
 
 namespace {
@@ -236,8 +240,16 @@ tts_bb_status cuda_fail(tts_bb* h, cudaError_t e, const char* what) {
                 cudaGetErrorString(e));
 }
 
+// TTS_BB_FAIL_ALLOC_AT=n: the n-th device allocation of a handle fails (test hook).
+inline bool alloc_fault(tts_bb* h) {
+    const char* v = std::getenv("TTS_BB_FAIL_ALLOC_AT");
+    const long at = v ? std::atol(v) : 0L;
+    return at > 0 && (long)++h->n_allocs == at;
+}
+
 template <typename T>
 cudaError_t dalloc(tts_bb* h, T** p, size_t n) {
+    if (alloc_fault(h)) return cudaErrorMemoryAllocation;
     void* v = nullptr;
     const cudaError_t e = cudaMalloc(&v, std::max<size_t>(n, 1) * sizeof(T));
     if (e == cudaSuccess) {
@@ -594,6 +606,21 @@ TTS_API const char* tts_bb_last_error(const tts_bb* h) { return h ? h->last_erro
 
 TTS_API uint64_t tts_bb_launch_count(const tts_bb* h) { return h ? h->launches : 0; }
 
+TTS_API tts_bb_status tts_bb_debug_fault(tts_bb* h, int what, int64_t arg) {
+    if (!h) return TTS_BB_E_INVALID;
+    switch (what) {
+        case TTS_BB_DEBUG_WAIT_LIMIT_NS:
+            if (arg < 1000000 || arg > 10000000000LL) return fail(h, TTS_BB_E_INVALID, "wait limit %lld ns outside 1e6..1e10", (long long)arg);
+            h->wait_limit_ns = (unsigned long long)arg;
+            return TTS_BB_OK;
+        case TTS_BB_DEBUG_STALL_NEXT_STEP:
+            h->stall_next = 1;
+            return TTS_BB_OK;
+        default:
+            return fail(h, TTS_BB_E_INVALID, "unknown debug hook %d", what);
+    }
+}
+
 TTS_API void tts_bb_free(tts_bb* h) {
     if (!h) return;
     int cur = 0;
@@ -868,7 +895,6 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
     if (ids && c.n_codebooks == 0) return fail(h, TTS_BB_E_INVALID, "handle has no codebook tables");
     if (head_idx >= c.n_heads || head_idx < -1) return fail(h, TTS_BB_E_INVALID, "head_idx %d out of range", head_idx);
     if (head_idx < 0 && (logits_out || argmax_out)) return fail(h, TTS_BB_E_INVALID, "outputs need a head");
-    int max_len = 0;
     std::vector<int> nl(B);
     for (int b = 0; b < B; ++b) {
         if (kv_lens[b] != h->slot_len[slots[b]])
@@ -876,7 +902,6 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
                         h->slot_len[slots[b]]);
         if (kv_lens[b] + 1 > c.max_ctx) return fail(h, TTS_BB_E_INVALID, "slot %d would exceed max_ctx", slots[b]);
         nl[b] = kv_lens[b] + 1;
-        max_len = std::max(max_len, nl[b]);
     }
     SetupArgs& a = *h->setup;
     a.B = B;
@@ -911,6 +936,9 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
             ma.upd_val[i] = a.upd_val[i];
         }
         ma.ep_base = h->ep_base;
+        ma.timeout_ns = h->wait_limit_ns;
+        ma.debug_stall = h->stall_next;
+        h->stall_next = 0;
         for (int b = 0; b < B; ++b) ma.last_phys[b] = h->page_table[(size_t)slots[b] * h->mbps + kv_lens[b] / KVB];
         ma.trace = nullptr;
         if (h->prof_on) {
@@ -997,7 +1025,9 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
     KVView kv{h->pool, h->d_page_table, h->seq_slot, h->mbps};
     double kv_bytes = 0;
     for (int b = 0; b < B; ++b) kv_bytes += (double)nl[b] * 2 * NKV * HD * 2;
-    run_layers(h, B, 1, 0, max_len, kv, h->layer_elems, kv_bytes);
+    // attention splits are sized for max_ctx here as in the graph-replayed step, so a step's
+    // summation order (and result) does not depend on which of the two ran
+    run_layers(h, B, 1, 0, c.max_ctx, kv, h->layer_elems, kv_bytes);
     if (opts && opts->hidden_out)
         cudaMemcpyAsync(opts->hidden_out, h->h, (size_t)B * HID * sizeof(float), cudaMemcpyDeviceToDevice, h->st);
     if (head_idx >= 0 && (logits_out || argmax_out))

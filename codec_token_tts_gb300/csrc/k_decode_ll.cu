@@ -15,9 +15,9 @@
 //   SwiGLU (all)  -> down rows                  -> own residual rows -> h words
 // Exchange buffers alternate by layer parity; epochs grow monotonically across
 // launches (the host passes the base), so stale words never match. Each CTA
-// keeps its own residual rows on chip. Every wait is bounded: on timeout the
-// kernel raises the error word and a shared abort flag, after which all waits
-// return at once and the kernel runs to its end.
+// keeps its own residual rows on chip. Every wait is bounded (timeout_ns): on
+// timeout the kernel raises the error word and a shared abort flag, after
+// which all waits return at once and the kernel runs to its end.
 #include "mega.cuh"
 
 namespace ttsbb {
@@ -38,7 +38,6 @@ constexpr int ATT_MERGE = 2 * mk::MAXB * NQ * MAXSPLIT;
 constexpr int ATT_FLOATS = ATT_UNIT > ATT_MERGE ? ATT_UNIT : ATT_MERGE;
 constexpr int PART_FLOATS = NCW * 64 * mk::MAXB;  // per-warp partial sums of one op ([KS][64 rows][B])
 constexpr int SMEM = RING + XF_BYTES + mk::MAXB * OWN_MAX * 4 + ATT_FLOATS * 4 + PART_FLOATS * 4 + 2 * NSLOT * 8 + 64;
-constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
 }  // namespace ll
 
 // ---------------------------------------------------------------- small PTX helpers
@@ -96,7 +95,7 @@ __device__ __forceinline__ bool l_mbar_wait_sleep(uint64_t* b, uint32_t parity, 
     for (;;) {
         if (l_mbar_try_sleep(b, parity)) return true;
         if (l_aborted(a)) return false;
-        if (l_time() - t0 > ll::TIMEOUT_NS) { l_raise(a); return false; }
+        if (l_time() - t0 > a.timeout_ns) { l_raise(a); return false; }
     }
 }
 __device__ __forceinline__ bool l_mbar_wait(uint64_t* b, uint32_t parity, const MegaArgs& a) {
@@ -106,7 +105,7 @@ __device__ __forceinline__ bool l_mbar_wait(uint64_t* b, uint32_t parity, const 
         if (l_mbar_try(b, parity)) return true;
         if ((i & 63) == 63) {
             if (l_aborted(a)) return false;
-            if (l_time() - t0 > ll::TIMEOUT_NS) { l_raise(a); return false; }
+            if (l_time() - t0 > a.timeout_ns) { l_raise(a); return false; }
         }
     }
 }
@@ -147,7 +146,7 @@ __device__ __forceinline__ void ll_settle(unsigned long long (&w)[N], const unsi
         if (ok) return;
         if ((it & 15) == 15) {
             if (l_aborted(a)) return;
-            if (l_time() - t0 > ll::TIMEOUT_NS) { l_raise(a); return; }
+            if (l_time() - t0 > a.timeout_ns) { l_raise(a); return; }
         }
     }
 }
@@ -169,7 +168,7 @@ __device__ __forceinline__ void ll_settle_f(unsigned long long (&w)[N], Addr add
         if (ok) return;
         if ((it & 15) == 15) {
             if (l_aborted(a)) return;
-            if (l_time() - t0 > ll::TIMEOUT_NS) { l_raise(a); return; }
+            if (l_time() - t0 > a.timeout_ns) { l_raise(a); return; }
         }
     }
 }
@@ -760,7 +759,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
                     if (!l_mbar_wait_sleep(empty + s, (consumed / ll::NSLOT) & 1, a)) ok = false;
                 } else {
                     const unsigned long long t0 = l_time();
-                    while (!l_mbar_try(full + s, (consumed / ll::NSLOT) & 1) && l_time() - t0 < ll::TIMEOUT_NS) {
+                    while (!l_mbar_try(full + s, (consumed / ll::NSLOT) & 1) && l_time() - t0 < a.timeout_ns) {
                     }
                 }
                 ++consumed;
@@ -890,7 +889,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
                          if (two) hown[b * ll::OWN_MAX + row + 1 - r0] += v1;
                      });
         l_named_sync();
-        {
+        if (!(a.debug_stall && l == 0 && blockIdx.x == 0)) {  // (test hook: withhold CTA 0's words once)
             unsigned long long* hx = xh_base(X, 2 * l + 1);
             const uint32_t eh = ep_h(a, 2 * l + 1);
             const int n = B * (own1 - own0);

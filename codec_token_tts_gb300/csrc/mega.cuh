@@ -54,6 +54,8 @@ struct MegaArgs {
     uint32_t ep_base;          // first epoch of this launch (grows by ll_epochs_per_launch)
     int last_phys[mk::MAXB];   // physical block holding each sequence's new token
     unsigned int* done;        // CTAs finished with the head (last one publishes the argmax)
+    unsigned long long timeout_ns;  // bound of every wait (exchange polls, ring slots)
+    int debug_stall;           // test hook: CTA 0 withholds one exchange, so every wait runs out
 };
 
 // Launch one decode step on `grid` CTAs (cooperative: all co-resident or an error).

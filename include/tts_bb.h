@@ -233,6 +233,22 @@ tts_bb_status tts_bb_debug_kv_read(tts_bb* h, int layer, int slot, int pos0, int
 tts_bb_status tts_bb_debug_kv_write(tts_bb* h, int layer, int slot, int pos0, int n,
                                     const void* k, const void* v);
 
+/* Test hooks for failure handling (the pages have no counterpart; SURVEY's
+ * failure-detection contract asks that device waits be forced to run out
+ * without faulting the GPU).
+ *   what = TTS_BB_DEBUG_WAIT_LIMIT_NS: every wait of the persistent decode
+ *          step (exchange polls, weight-ring slots) gives up after arg ns
+ *          (default 2e9; arg in 1e6 .. 1e10, else TTS_BB_E_INVALID).
+ *   what = TTS_BB_DEBUG_STALL_NEXT_STEP: the next persistent decode step
+ *          (batch <= 2) withholds one CTA's exchange words, so every CTA's
+ *          wait runs out; that step returns TTS_BB_E_DEVICE_TIMEOUT (its
+ *          outputs are undefined) and the handle stays usable. arg unused.
+ * Returns TTS_BB_E_INVALID for a null handle or an unknown `what`. The
+ * environment variable TTS_BB_FAIL_ALLOC_AT=n makes the n-th device
+ * allocation of a handle being created fail (creation returns TTS_BB_E_OOM). */
+enum { TTS_BB_DEBUG_WAIT_LIMIT_NS = 1, TTS_BB_DEBUG_STALL_NEXT_STEP = 2 };
+tts_bb_status tts_bb_debug_fault(tts_bb* h, int what, int64_t arg);
+
 /* Number of kernel launches the handle has enqueued since creation (a
  * counter kept on the host; lets a caller count launches in a timed region). */
 uint64_t tts_bb_launch_count(const tts_bb* h);
