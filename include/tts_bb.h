@@ -233,9 +233,8 @@ tts_bb_status tts_bb_debug_kv_read(tts_bb* h, int layer, int slot, int pos0, int
 tts_bb_status tts_bb_debug_kv_write(tts_bb* h, int layer, int slot, int pos0, int n,
                                     const void* k, const void* v);
 
-/* Test hooks for failure handling (the pages have no counterpart; SURVEY's
- * failure-detection contract asks that device waits be forced to run out
- * without faulting the GPU).
+/* Test hooks for failure handling (no counterpart on the pages): they force
+ * device-side waits to run out without faulting the GPU.
  *   what = TTS_BB_DEBUG_WAIT_LIMIT_NS: every wait of the persistent decode
  *          step (exchange polls, weight-ring slots) gives up after arg ns
  *          (default 2e9; arg in 1e6 .. 1e10, else TTS_BB_E_INVALID).
