@@ -403,6 +403,70 @@ def run_maskgit(steps, warmup):
             "roofline": roofline_from_profile(rep), "kernel_profile": rep}
 
 
+def run_code_predictor(steps, warmup):
+    """Code Predictor, 256 frames at once: a 2-token prefill (Talker hidden state + code 0, head 0)
+    then 14 decode calls with heads 1..14; one step = the 15 codes of every frame."""
+    import torch
+    import codec_token_tts_gb300 as m
+    from tests.gpu_util import config_for, dev_bf16_bits, dev_i32, weights_for
+    seed, F = 3, 256
+    w = synth.model_weights(synth.CODE_PREDICTOR, seed)
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    cfg = config_for(synth.CODE_PREDICTOR, max_slots=F, max_ctx=17, max_batch=F, max_tokens=2 * F, sync_errors=0)
+    h = m.tts_bb_create(cfg, weights_for(w), stream.cuda_stream)
+    r = synth.rng_for(seed, "cp_inputs")
+    th = synth.normal_bf16(r, (F, 1024), 1.0)
+    code0 = r.integers(0, 3072, size=F).astype(np.int32)
+    emb = np.zeros((F, 2, 1024), np.uint16)
+    emb[:, 0] = th
+    ids = -np.ones((F, 2, 16), np.int32)
+    ids[:, 1, 0] = code0
+    emb_d, ids_d = dev_bf16_bits(emb), dev_i32(ids)
+    codes = torch.full((F, 16), -1, dtype=torch.int32, device="cuda")
+    # step ids: column j carries code j (written by the previous call's argmax), -1 elsewhere
+    steps_ids = torch.full((15, F, 16), -1, dtype=torch.int32, device="cuda")
+    logits = torch.zeros(F, 2048, dtype=torch.float32, device="cuda")
+    slots = np.arange(F, dtype=np.int32)
+
+    def frame_batch():
+        m.tts_bb_prefill(h, F, 2, slots, [2] * F, ids_d, 0, None, steps_ids[1, :, 1], embeds=emb_d,
+                         argmax_stride=16, check=False)
+        for j in range(1, 15):
+            nxt = steps_ids[j + 1, :, j + 1] if j + 1 < 15 else codes[:, 15]
+            m.tts_bb_decode_step(h, F, slots, [j + 1] * F, steps_ids[j], j, None, nxt, argmax_stride=16, check=False)
+        for s in slots:
+            m.lib.tts_bb_release(h, int(s))
+
+    for _ in range(warmup):
+        frame_batch()
+    m.tts_bb_sync(h)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(steps):
+        frame_batch()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    st = m.tts_bb_sync(h, check=False)
+    m.tts_bb_profile(h, True)
+    frame_batch()
+    rep = m.tts_bb_profile_report(h)
+    m.tts_bb_profile(h, False)
+    m.tts_bb_free(h)
+    # per call: 5 layers + final norm + one 2048 x 1024 head; KV read 20,480 B per cached token per frame
+    per_call = 5 * 31_461_888 + 2048 + 2048 * 1024 * 2
+    kv = sum(20_480 * F * (j + 1) for j in range(1, 15))
+    step_bytes = 15 * per_call + kv + F * 2 * 2048 * 2
+    return {"workload": "code_predictor: 5-layer Code Predictor, 256 frames at once, 2-token prefill + 14 decode "
+                        "calls (heads 0..14), greedy codes fed back",
+            "value": F * 15 / (ms / 1e3), "unit": "codebook tokens/s", "ms_per_step": ms, "steps": steps,
+            "status": st, "algorithmic_bytes_per_step": step_bytes,
+            "hbm_frac_of_measured": step_bytes / (ms / 1e3) / 1e9 / peaks()[0]["hbm_gbs"],
+            "roofline": roofline_from_profile(rep), "kernel_profile": rep}
+
+
 def roofline_from_profile(rep, traffic=None):
     pk, src = peaks()
     ks = rep.get("kernels", [])
@@ -463,6 +527,7 @@ def oracle_talker_tokens_per_s(budget_s: float, max_steps: int):
     n = 0
     t0 = time.perf_counter()
     id0 = a0
+    max_steps = min(max_steps, len(wl.rest))  # the workload's decode positions (128..383)
     while n < max_steps and (time.perf_counter() - t0) < budget_s:
         _, _, am, _ = O.talker_decode_steps(mo, cache, id0, wl.rest[n:n + 1])
         id0 = int(am[0])
@@ -506,7 +571,7 @@ def main():
     ap.add_argument("--workload", default="talker_b1", choices=["talker_b1"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
-    ap.add_argument("--no-secondary", action="store_true", help="skip the batch-64 serving and MaskGIT lines")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the batch-64 serving, MaskGIT and Code Predictor lines")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -526,7 +591,8 @@ def main():
     res, wl = run_talker_b1(args, ws, rank)
     res["roofline"] = roofline_from_profile(res["kernel_profile"], measured_traffic(res["kernel_profile"]))
     if not args.no_secondary:
-        res["also"] = {"serving_b64": run_serving_b64(64, 4), "maskgit": run_maskgit(8, 3)}
+        res["also"] = {"serving_b64": run_serving_b64(64, 4), "maskgit": run_maskgit(8, 3),
+                       "code_predictor": run_code_predictor(16, 3)}
     if rank == 0 and not args.no_cpu_baseline:
         v, n, el, setup_s = oracle_talker_tokens_per_s(args.cpu_budget_s, 10_000)
         ci = cpu_info()

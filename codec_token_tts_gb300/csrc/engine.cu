@@ -395,7 +395,7 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         const LayerW& w = h->L[l];
         KVView kv = kv_base;
         kv.pool = kv_base.pool + (size_t)l * layer_stride;
-        const int gk = T <= 8 ? K_GEMV : (mode == 0 ? (T <= 128 ? K_GEMM_TCD : K_GEMM) : K_GEMM_TC);
+        const int gk = T <= 8 ? K_GEMV : (mode == 0 ? (T <= 256 ? K_GEMM_TCD : K_GEMM) : K_GEMM_TC);
         // decode carries GEMM inputs as bf16 high + low parts (weights are read
         // once either way); prefill / bidirectional passes use plain bf16
         const bool split = mode == 0;
@@ -440,7 +440,7 @@ void run_head(tts_bb* h, int B, int per_seq, int head_idx, bool last_of_seq, flo
       L += launch_rmsnorm(h->h, h->final_norm, h->y, B, c.rms_eps, 1, per_seq, 0, last_of_seq ? h->seq_len : nullptr, h->st, ylo); }
     Epi e{};
     e.mode = EPI_LOGITS; e.out = logits_out; e.ldo = c.head_rows; e.amax = argmax_out ? h->amax : nullptr;
-    { Launch L(h, B <= 8 ? K_GEMV : (split ? (B <= 128 ? K_GEMM_TCD : K_GEMM) : K_GEMM_TC), gemm_bytes(B, c.head_rows, HID, logits_out ? 4 : 0), 2.0 * B * c.head_rows * HID);
+    { Launch L(h, B <= 8 ? K_GEMV : (split ? (B <= 256 ? K_GEMM_TCD : K_GEMM) : K_GEMM_TC), gemm_bytes(B, c.head_rows, HID, logits_out ? 4 : 0), 2.0 * B * c.head_rows * HID);
       L += launch_gemm(h->y, h->heads[head_idx], B, c.head_rows, HID, e, h->st, ylo, h->err,
                         split && h->sk.part ? &h->sk : nullptr); }
     if (argmax_out && finalize) { Launch L(h, K_ARGMAX); L += launch_argmax_finalize(h->amax, argmax_out, argmax_stride, B, h->st); }
