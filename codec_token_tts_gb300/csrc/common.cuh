@@ -84,6 +84,31 @@ struct Epi {
     void* out_lo;              // EPI_SWIGLU: optional bf16 low part (value - bf16(value))
 };
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Kernels of the step chain are launched with programmatic stream
+// serialization: a kernel may be dispatched while its predecessor finishes,
+// runs only setup that reads no upstream results, then waits in pdl_wait()
+// until the predecessor has completed and its writes are visible. pdl_trigger()
+// lets the next kernel of the chain be dispatched early (it launches only once
+// every CTA of this grid is running). Both are no-ops without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- kernels
 struct TableSet {
     const bf16* tab[16];

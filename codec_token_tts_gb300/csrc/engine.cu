@@ -39,6 +39,8 @@ struct SetupArgs {
 
 __global__ void k_setup(SetupArgs a, int32_t* seq_slot, int32_t* seq_start, int32_t* seq_len, int32_t* key_len,
                         int32_t* page_table, unsigned long long* amax) {
+    pdl_wait();  // upstream results are read below
+    pdl_trigger();
     for (int i = threadIdx.x; i < a.B; i += blockDim.x) {
         seq_slot[i] = a.slot[i];
         seq_start[i] = a.start[i];
@@ -67,6 +69,8 @@ struct StepBlock {
 __global__ void k_step_setup(const StepBlock* __restrict__ sb, int n_cb, int32_t* seq_slot, int32_t* seq_start,
                              int32_t* seq_len, int32_t* key_len, int32_t* page_table, unsigned long long* amax,
                              int32_t* ids_buf, bf16* emb_buf) {
+    pdl_wait();  // upstream results are read below
+    pdl_trigger();
     const SetupArgs& a = sb->a;
     const int b = blockIdx.x;
     if (b == 0) {
@@ -91,6 +95,8 @@ __global__ void k_step_setup(const StepBlock* __restrict__ sb, int n_cb, int32_t
 // state to the caller's pointers from the step block.
 __global__ void k_step_publish(const StepBlock* __restrict__ sb, const float* logits, int rows,
                                const unsigned long long* amax, const float* hid) {
+    pdl_wait();  // upstream results are read below
+    pdl_trigger();
     const int b = blockIdx.x;
     if (logits && sb->logits_out)
         for (int i = threadIdx.x; i < rows; i += blockDim.x) sb->logits_out[(size_t)b * rows + i] = logits[(size_t)b * rows + i];
@@ -380,7 +386,7 @@ tts_bb_status ensure_scratch(tts_bb* h, int T) {
 
 void launch_setup(tts_bb* h, SetupArgs& a) {
     Launch L(h, K_SETUP);
-    k_setup<<<1, 256, 0, h->st>>>(a, h->seq_slot, h->seq_start, h->seq_len, h->key_len, h->d_page_table, h->amax);
+    launch_pdl(k_setup, 1, 256, 0, h->st, a, h->seq_slot, h->seq_start, h->seq_len, h->key_len, h->d_page_table, h->amax);
     L += 1;
 }
 
@@ -534,7 +540,7 @@ bool decode_step_graph(tts_bb* h, int B, int head_idx, const int32_t* ids, const
         cudaGraph_t graph = nullptr;
         bool ok = cudaStreamBeginCapture(h->st, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
         if (ok) {
-            k_step_setup<<<B, 256, 0, h->st>>>(h->d_step, c.n_codebooks, h->seq_slot, h->seq_start, h->seq_len,
+            launch_pdl(k_step_setup, B, 256, 0, h->st, h->d_step, c.n_codebooks, h->seq_slot, h->seq_start, h->seq_len,
                                                 h->key_len, h->d_page_table, h->amax, ids ? h->ids_buf : nullptr,
                                                 embeds ? h->emb_buf : nullptr);
             h->launches += 1;
@@ -544,7 +550,7 @@ bool decode_step_graph(tts_bb* h, int B, int head_idx, const int32_t* ids, const
             run_layers(h, B, 1, 0, c.max_ctx, kv, h->layer_elems, 0);  // attention grid sized for max_ctx
             if (want_head)
                 run_head(h, B, 1, head_idx, false, logits_out ? h->logits_buf : nullptr, argmax_out, 1, true, false);
-            k_step_publish<<<B, 256, 0, h->st>>>(h->d_step, want_head && logits_out ? h->logits_buf : nullptr,
+            launch_pdl(k_step_publish, B, 256, 0, h->st, h->d_step, want_head && logits_out ? h->logits_buf : nullptr,
                                                   c.head_rows, want_head && argmax_out ? h->amax : nullptr,
                                                   hidden_out ? h->h : nullptr);
             h->launches += 1;

@@ -25,6 +25,8 @@ __device__ __forceinline__ const bf16* kv_tile(const KVView& kv, int seq, int j,
 __global__ void __launch_bounds__(128) k_attn_decode(const bf16* __restrict__ q, KVView kv,
                                                      const int32_t* __restrict__ seq_start, int bps,
                                                      int n_splits, float* __restrict__ part) {
+    pdl_wait();  // upstream results are read below
+    pdl_trigger();
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int L = seq_start[b] + 1;                 // keys incl. the token just appended
@@ -139,6 +141,8 @@ __global__ void __launch_bounds__(128) k_attn_decode(const bf16* __restrict__ q,
 // grid B*16, 128 threads: merge the splits of one (sequence, head) in split order.
 __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ part, int n_splits,
                                                       bf16* __restrict__ out, bf16* __restrict__ out_lo) {
+    pdl_wait();  // upstream results are read below
+    pdl_trigger();
     const int bh = blockIdx.x, d = threadIdx.x;
     const float* p = part + (size_t)bh * n_splits * (HD + 2);
     float M = -INFINITY;
@@ -165,8 +169,8 @@ int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B
     splits = max(1, min(splits, min(nblk, max_splits)));
     const int bps = (nblk + splits - 1) / splits;
     splits = (nblk + bps - 1) / bps;
-    k_attn_decode<<<dim3(splits, NKV, B), 128, 0, st>>>(q, kv, seq_start, bps, splits, part);
-    k_attn_combine<<<B * NQ, 128, 0, st>>>(part, splits, out, out_lo);
+    launch_pdl(k_attn_decode, dim3(splits, NKV, B), 128, 0, st, q, kv, seq_start, bps, splits, part);
+    launch_pdl(k_attn_combine, B * NQ, 128, 0, st, part, splits, out, out_lo);
     return 2;
 }
 
@@ -210,6 +214,8 @@ __global__ void __launch_bounds__(256) k_attn_prefill(const bf16* __restrict__ q
                                                       const int32_t* __restrict__ seq_len,
                                                       const int32_t* __restrict__ key_len, int causal, int S,
                                                       bf16* __restrict__ out) {
+    pdl_wait();  // upstream results are read below
+    pdl_trigger();
     using namespace fa;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     bf16* sQ = reinterpret_cast<bf16*>(smem_raw);
@@ -378,7 +384,7 @@ int launch_attn_prefill(const bf16* q, KVView kv, const int32_t* seq_start, cons
         attr_set = true;
     }
     dim3 grid((S + fa::BQ - 1) / fa::BQ, NKV, B);
-    k_attn_prefill<<<grid, 256, fa::SMEM, st>>>(q, kv, seq_start, seq_len, key_len, causal, S, out);
+    launch_pdl(k_attn_prefill, grid, 256, fa::SMEM, st, q, kv, seq_start, seq_len, key_len, causal, S, out);
     return 1;
 }
 

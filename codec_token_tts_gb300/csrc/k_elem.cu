@@ -13,6 +13,8 @@ namespace ttsbb {
 __global__ void __launch_bounds__(128) k_embed_codebooks(TableSet ts, const int32_t* __restrict__ ids,
                                                          const bf16* __restrict__ embeds,
                                                          float* __restrict__ h, int* err) {
+    pdl_wait();  // upstream results are read below
+    pdl_trigger();
     const int t = blockIdx.x;
     const int c = threadIdx.x * 8;
     float acc[8];
@@ -44,7 +46,7 @@ __global__ void __launch_bounds__(128) k_embed_codebooks(TableSet ts, const int3
 int launch_embed_codebooks(const TableSet& ts, const int32_t* ids, const bf16* embeds, float* h, int T,
                             int* err, cudaStream_t st) {
     if (T <= 0) return 0;
-    k_embed_codebooks<<<T, 128, 0, st>>>(ts, ids, embeds, h, err);
+    launch_pdl(k_embed_codebooks, T, 128, 0, st, ts, ids, embeds, h, err);
     return 1;
 }
 
@@ -56,6 +58,8 @@ __global__ void __launch_bounds__(128) k_embed_omnivoice(const bf16* __restrict_
                                                          const int32_t* __restrict__ ids,
                                                          const uint8_t* __restrict__ mask,
                                                          float* __restrict__ h, int S, int* err) {
+    pdl_wait();  // upstream results are read below
+    pdl_trigger();
     const int t = blockIdx.x;
     const int b = t / S, s = t % S;
     const int c = threadIdx.x * 8;
@@ -91,7 +95,7 @@ int launch_embed_omnivoice(const bf16* text, int text_vocab, const bf16* audio, 
                             const int32_t* ids, const uint8_t* mask, float* h, int B, int S, int* err,
                             cudaStream_t st) {
     if (B * S <= 0) return 0;
-    k_embed_omnivoice<<<B * S, 128, 0, st>>>(text, text_vocab, audio, n_cb, vocab, ids, mask, h, S, err);
+    launch_pdl(k_embed_omnivoice, B * S, 128, 0, st, text, text_vocab, audio, n_cb, vocab, ids, mask, h, S, err);
     return 1;
 }
 
@@ -101,6 +105,8 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ h, co
                                                  bf16* __restrict__ y, int T, float eps, int per, int stride,
                                                  int offset, const int32_t* __restrict__ last_len,
                                                  bf16* __restrict__ y_lo) {
+    pdl_wait();  // upstream results are read below
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= T) return;
@@ -143,7 +149,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ h, co
 int launch_rmsnorm(const float* h, const bf16* gamma, bf16* y, int T, float eps, int per, int stride, int offset,
                     const int32_t* last_len, cudaStream_t st, bf16* y_lo) {
     if (T <= 0) return 0;
-    k_rmsnorm<<<(T + 7) / 8, 256, 0, st>>>(h, gamma, y, T, eps, per, stride, offset, last_len, y_lo);
+    launch_pdl(k_rmsnorm, (T + 7) / 8, 256, 0, st, h, gamma, y, T, eps, per, stride, offset, last_len, y_lo);
     return 1;
 }
 
@@ -159,6 +165,8 @@ __global__ void __launch_bounds__(256) k_qk_norm_rope_append(
     const float* __restrict__ cos_t, const float* __restrict__ sin_t, float eps, bf16* __restrict__ qout,
     KVView kv, const int32_t* __restrict__ seq_start, const int32_t* __restrict__ seq_len, int tok_per_seq,
     int* err) {
+    pdl_wait();  // upstream results are read below
+    pdl_trigger();
     const int t = blockIdx.x;
     const int seq = t / tok_per_seq, s = t % tok_per_seq;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -230,20 +238,22 @@ int launch_qk_norm_rope_append(const float* qkv, const bf16* qn, const bf16* kn,
                                 const float* sin_t, float eps, bf16* qout, KVView kv, const int32_t* seq_start,
                                 const int32_t* seq_len, int tok_per_seq, int T, int* err, cudaStream_t st) {
     if (T <= 0) return 0;
-    k_qk_norm_rope_append<<<T, 256, 0, st>>>(qkv, qn, kn, cos_t, sin_t, eps, qout, kv, seq_start, seq_len,
+    launch_pdl(k_qk_norm_rope_append, T, 256, 0, st, qkv, qn, kn, cos_t, sin_t, eps, qout, kv, seq_start, seq_len,
                                              tok_per_seq, err);
     return 1;
 }
 
 // ---------------------------------------------------------------- argmax
 __global__ void k_argmax_finalize(const unsigned long long* __restrict__ amax, int32_t* out, int stride, int B) {
+    pdl_wait();  // upstream results are read below
+    pdl_trigger();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b < B) out[(size_t)b * stride] = (int32_t)(0xFFFFFFFFu - (uint32_t)(amax[b] & 0xFFFFFFFFull));
 }
 
 int launch_argmax_finalize(const unsigned long long* amax, int32_t* out, int stride, int B, cudaStream_t st) {
     if (B <= 0) return 0;
-    k_argmax_finalize<<<(B + 127) / 128, 128, 0, st>>>(amax, out, stride, B);
+    launch_pdl(k_argmax_finalize, (B + 127) / 128, 128, 0, st, amax, out, stride, B);
     return 1;
 }
 

@@ -205,6 +205,8 @@ __global__ void __launch_bounds__(tc::NT, 1)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();  // barriers and TMEM are set up; activations (and the output) come from upstream kernels
+    pdl_trigger();
 
     if (warp == 0) {
         // ---------------- TMA producer
@@ -458,9 +460,21 @@ __global__ void __launch_bounds__(tcd::NT, 1)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
+    pdl_trigger();
+    if (!(warp == 0 && lane == 0)) pdl_wait();  // activations (and the output) come from upstream kernels
 
     if (warp == 0) {
         if (lane == 0) {  // TMA producer
+            // the weights do not depend on upstream kernels: the first stages' weight tiles are
+            // requested before waiting for them, the activation tiles after
+            const int pre = nk < STAGES ? nk : STAGES;
+            for (int i = 0; i < pre; ++i) {
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(full + i)),
+                             "r"((uint32_t)A_BYTES + b_bytes)
+                             : "memory");
+                tma_load_2d(smem + i * STAGE, &tmW, (kb0 + i) * BK, n0, full + i);
+            }
+            pdl_wait();
             int issued = 0;
             for (int i = 0; i < nk; ++i) {
                 const int s = i % STAGES;
@@ -469,15 +483,18 @@ __global__ void __launch_bounds__(tcd::NT, 1)
                     break;
                 }
                 unsigned char* st = smem + s * STAGE;
-                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(full + s)),
-                             "r"((uint32_t)A_BYTES + b_bytes)
-                             : "memory");
                 const int kx = (kb0 + i) * BK;
-                tma_load_2d(st, &tmW, kx, n0, full + s);
+                if (i >= pre) {
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(full + s)),
+                                 "r"((uint32_t)A_BYTES + b_bytes)
+                                 : "memory");
+                    tma_load_2d(st, &tmW, kx, n0, full + s);
+                }
                 tma_load_2d(st + A_BYTES, &tmXh, kx, 0, full + s);
                 tma_load_2d(st + A_BYTES + TB * BK * 2, &tmXl, kx, 0, full + s);
                 ++issued;
             }
+            if (*abort_s && issued < pre) issued = pre;  // weight tiles already requested must land too
             if (*abort_s) {
                 for (int i = 0; i < issued; ++i) {
                     const unsigned long long t0 = g_time();
@@ -701,13 +718,15 @@ int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N
     cfg.blockDim = dim3(tcd::NT);
     cfg.dynamicSmemBytes = tcd::SMEM;
     cfg.stream = st;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = S;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, k_gemm_tcd, mw, mh, ml, T, TB, N, K, e, err) == cudaSuccess ? 1 : 0;
 }
 
@@ -724,7 +743,7 @@ int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi&
         attr = true;
     }
     dim3 grid((N + tc::BN - 1) / tc::BN, (T + tc::BM - 1) / tc::BM);
-    k_gemm_tc<<<grid, tc::NT, tc::SMEM, st>>>(ma, mb, T, N, K, e, err);
+    launch_pdl(k_gemm_tc, grid, tc::NT, tc::SMEM, st, ma, mb, T, N, K, e, err);
     return 1;
 }
 

@@ -56,6 +56,8 @@ __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsig
 template <int T, int ROWS>
 __global__ void __launch_bounds__(256) k_gemv(const bf16* __restrict__ X, const bf16* __restrict__ X_lo,
                                               const bf16* __restrict__ W, int N, int K, Epi e) {
+    pdl_wait();  // upstream results are read below
+    pdl_trigger();
     extern __shared__ __align__(16) unsigned char smem_raw[];
     bf16* xs = reinterpret_cast<bf16*>(smem_raw);
     bf16* xl = xs + (size_t)T * K;
@@ -163,7 +165,7 @@ static void gemv_t(const bf16* X, const bf16* X_lo, const bf16* W, int N, int K,
         attr_set = true;
     }
     const int rows_per_cta = 16;
-    k_gemv<T, 2><<<(N + rows_per_cta - 1) / rows_per_cta, 256, smem, st>>>(X, X_lo, W, N, K, e);
+    launch_pdl(k_gemv<T, 2>, (N + rows_per_cta - 1) / rows_per_cta, 256, smem, st, X, X_lo, W, N, K, e);
 }
 
 int launch_gemv(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st, const bf16* X_lo) {
@@ -220,6 +222,8 @@ __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, const uint
 template <bool SPLIT>
 __global__ void __launch_bounds__(256) k_gemm_mma(const bf16* __restrict__ X, const bf16* __restrict__ X_lo,
                                                   const bf16* __restrict__ W, int T, int N, int K, Epi e) {
+    pdl_wait();  // upstream results are read below
+    pdl_trigger();
     using namespace gm;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     bf16* sA = reinterpret_cast<bf16*>(smem_raw);
@@ -355,6 +359,8 @@ template <int MT>  // token tiles of 64; KC = 256 / MT
 __global__ void __launch_bounds__(256) k_gemm_splitk(const bf16* __restrict__ X, const bf16* __restrict__ X_lo,
                                                      const bf16* __restrict__ W, int T, int N, int K, Epi e,
                                                      float* __restrict__ part, int* __restrict__ ctr) {
+    pdl_wait();  // upstream results are read below
+    pdl_trigger();
     using namespace sk;
     constexpr int KC = 256 / MT, LDS = KC + LDS_PAD, TP = MT * 64;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -499,9 +505,9 @@ static int launch_splitk(const bf16* X, const bf16* X_lo, const bf16* W, int T, 
     }
     dim3 grid(N / BN, KS);
     switch (MT) {
-        case 1: k_gemm_splitk<1><<<grid, 256, splitk_smem<1>(), st>>>(X, X_lo, W, T, N, K, e, w.part, w.ctr); break;
-        case 2: k_gemm_splitk<2><<<grid, 256, splitk_smem<2>(), st>>>(X, X_lo, W, T, N, K, e, w.part, w.ctr); break;
-        default: k_gemm_splitk<4><<<grid, 256, splitk_smem<4>(), st>>>(X, X_lo, W, T, N, K, e, w.part, w.ctr); break;
+        case 1: launch_pdl(k_gemm_splitk<1>, grid, 256, splitk_smem<1>(), st, X, X_lo, W, T, N, K, e, w.part, w.ctr); break;
+        case 2: launch_pdl(k_gemm_splitk<2>, grid, 256, splitk_smem<2>(), st, X, X_lo, W, T, N, K, e, w.part, w.ctr); break;
+        default: launch_pdl(k_gemm_splitk<4>, grid, 256, splitk_smem<4>(), st, X, X_lo, W, T, N, K, e, w.part, w.ctr); break;
     }
     return 1;
 }
@@ -542,9 +548,9 @@ int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e,
     }
     dim3 grid((N + gm::BN - 1) / gm::BN, (T + gm::BM - 1) / gm::BM);
     if (X_lo)
-        k_gemm_mma<true><<<grid, 256, gm::SMEM_SPLIT, st>>>(X, X_lo, W, T, N, K, e);
+        launch_pdl(k_gemm_mma<true>, grid, 256, gm::SMEM_SPLIT, st, X, X_lo, W, T, N, K, e);
     else
-        k_gemm_mma<false><<<grid, 256, gm::SMEM, st>>>(X, nullptr, W, T, N, K, e);
+        launch_pdl(k_gemm_mma<false>, grid, 256, gm::SMEM, st, X, (const bf16*)nullptr, W, T, N, K, e);
     return 1;
 }
 
