@@ -1,18 +1,21 @@
 // Dense Y = X W^T on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
-// One CTA computes a 128-token x 256-feature tile: a producer thread loads
+// Persistent: one CTA per SM walks the 128-token x 256-feature output tiles
+// (tile = blockIdx.x, + gridDim.x, ...). A producer thread loads
 // 128-byte-swizzled K-slices of X (128 x 64) and W (256 x 64) with TMA into a
-// 4-stage shared-memory ring; one thread issues tcgen05.mma (M=128, N=256,
-// K=16, bf16 in, fp32 accumulate) into a TMEM accumulator and commits each
-// stage back to the producer through an mbarrier; four epilogue warps read
-// the accumulator with tcgen05.ld (each warp owns its 32-lane quarter of
-// TMEM = 32 token rows) and apply the same fused epilogues as the other
-// linear kernels (fp32 store, residual add, SwiGLU over interleaved gate/up
-// columns, logits + argmax, permuted audio-head logits).
+// 4-stage shared-memory ring that runs on across tiles; one thread issues
+// tcgen05.mma (M=128, N=256, K=16, bf16 in, fp32 accumulate) into one of two
+// TMEM accumulators (2 x 256 columns) and commits each stage back to the
+// producer through an mbarrier; four epilogue warps drain the other
+// accumulator with tcgen05.ld (each warp owns its 32-lane quarter of TMEM =
+// 32 token rows) while the next tile accumulates, applying the same fused
+// epilogues as the other linear kernels (fp32 store, residual add, SwiGLU
+// over interleaved gate/up columns, logits + argmax, permuted audio-head
+// logits).
 //
 // Every mbarrier wait is bounded; on timeout the CTA raises the error word,
-// stops issuing work, waits (bounded) for its copies in flight, frees TMEM and
-// returns.
+// stops issuing work, waits (bounded) for its copies and MMAs in flight,
+// frees TMEM and returns.
 #include <algorithm>
 #include <mutex>
 #include <unordered_map>
@@ -30,7 +33,7 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
-constexpr int TMEM_COLS = 256;
+constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 constexpr int NT = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-5 epilogue
 constexpr unsigned long long TIMEOUT_NS = 1000000000ull;
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (7-9 = 1),
@@ -172,7 +175,7 @@ __device__ __forceinline__ void tc_epilogue16(const Epi& e, int t, int n0, int N
 
 __global__ void __launch_bounds__(tc::NT, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int T, int N, int K,
-              Epi e, int* err) {
+              const __grid_constant__ Epi e, int* err) {
     using namespace tc;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -180,19 +183,24 @@ __global__ void __launch_bounds__(tc::NT, 1)
     unsigned char* sB = smem + STAGES * A_BYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
     uint64_t* empty = full + STAGES;
-    uint64_t* accf = empty + STAGES;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+    uint64_t* accf = empty + STAGES;  // [2] accumulator ready (MMA -> epilogue)
+    uint64_t* acce = accf + 2;        // [2] accumulator drained (epilogue -> MMA), 4 warp arrivals
+    uint64_t* fin = acce + 2;         // every MMA issued by this CTA has completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
     volatile int* abort_s = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
-    const int KT = K / BK;
+    const int MT = (T + BM - 1) / BM, NTL = (N + BN - 1) / BN, tiles = MT * NTL, KT = K / BK;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             tc_mbar_init(full + s, 1);
             tc_mbar_init(empty + s, 1);
         }
-        tc_mbar_init(accf, 1);
+        for (int i = 0; i < 2; ++i) {
+            tc_mbar_init(accf + i, 1);
+            tc_mbar_init(acce + i, 4);
+        }
+        tc_mbar_init(fin, 1);
         *abort_s = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -209,72 +217,97 @@ __global__ void __launch_bounds__(tc::NT, 1)
     pdl_trigger();
 
     if (warp == 0) {
-        // ---------------- TMA producer
-        if (lane == 0) {
-            int issued = 0;
-            for (int kt = 0; kt < KT; ++kt) {
-                const int s = kt % STAGES;
-                if (kt >= STAGES && !tc_wait(empty + s, ((kt / STAGES) - 1) & 1, abort_s)) {
-                    *abort_s = 1;
-                    break;
+        if (lane == 0) {  // ---------------- TMA producer: the stage ring runs on across tiles
+            uint32_t g = 0;  // k-blocks issued
+            for (int tile = blockIdx.x; tile < tiles && !*abort_s; tile += gridDim.x) {
+                const int m0 = (tile % MT) * BM, n0 = (tile / MT) * BN;
+                for (int kt = 0; kt < KT; ++kt, ++g) {
+                    const int s = g % STAGES;
+                    if (g >= STAGES && !tc_wait(empty + s, ((g / STAGES) - 1) & 1, abort_s)) {
+                        *abort_s = 1;
+                        break;
+                    }
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(full + s)),
+                                 "r"(STAGE_BYTES)
+                                 : "memory");
+                    tma_load_2d(sA + s * A_BYTES, &tmA, kt * BK, m0, full + s);
+                    tma_load_2d(sB + s * B_BYTES, &tmB, kt * BK, n0, full + s);
                 }
-                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(full + s)),
-                             "r"(STAGE_BYTES)
-                             : "memory");
-                tma_load_2d(sA + s * A_BYTES, &tmA, kt * BK, m0, full + s);
-                tma_load_2d(sB + s * B_BYTES, &tmB, kt * BK, n0, full + s);
-                ++issued;
             }
-            if (*abort_s) {  // let every issued copy land before the CTA can exit
-                for (int kt = 0; kt < issued; ++kt) {
+            if (*abort_s) {  // let the copies in flight (the last STAGES issued) land before the CTA can exit
+                for (uint32_t i = g > (uint32_t)STAGES ? g - STAGES : 0; i < g; ++i) {
                     const unsigned long long t0 = g_time();
-                    while (!tc_mbar_try(full + kt % STAGES, (kt / STAGES) & 1) && g_time() - t0 < TIMEOUT_NS) {
+                    while (!tc_mbar_try(full + i % STAGES, (i / STAGES) & 1) && g_time() - t0 < TIMEOUT_NS) {
                     }
                 }
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
+        if (lane == 0) {  // ---------------- MMA issuer
+            uint32_t g = 0;  // k-blocks consumed
+            int it = 0;      // tiles of this CTA
             bool ok = true;
-            for (int kt = 0; kt < KT && ok; ++kt) {
-                const int s = kt % STAGES;
-                if (!tc_wait(full + s, (kt / STAGES) & 1, abort_s)) {
+            for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++it) {
+                const int buf = it & 1;
+                if (it >= 2 && !tc_wait(acce + buf, ((it >> 1) - 1) & 1, abort_s)) {  // epilogue drained it
                     *abort_s = 1;
                     ok = false;
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t a0 = s_addr(sA + s * A_BYTES), b0 = s_addr(sB + s * B_BYTES);
+                const uint32_t d = tmem + (uint32_t)(buf * BN);
+                for (int kt = 0; kt < KT; ++kt, ++g) {
+                    const int s = g % STAGES;
+                    if (!tc_wait(full + s, (g / STAGES) & 1, abort_s)) {
+                        *abort_s = 1;
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t a0 = s_addr(sA + s * A_BYTES), b0 = s_addr(sB + s * B_BYTES);
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k) {
-                    const uint64_t ad = sw128_desc(a0 + k * 32), bd = sw128_desc(b0 + k * 32);
-                    const uint32_t acc = (kt | k) ? 1u : 0u;
-                    asm volatile(
-                        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-                        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem),
-                        "l"(ad), "l"(bd), "r"(IDESC), "r"(acc));
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t ad = sw128_desc(a0 + k * 32), bd = sw128_desc(b0 + k * 32);
+                        const uint32_t acc = (kt | k) ? 1u : 0u;
+                        asm volatile(
+                            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                            " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+                            "l"(ad), "l"(bd), "r"(IDESC), "r"(acc));
+                    }
+                    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                        s_addr(empty + s))
+                                 : "memory");
                 }
+                if (!ok) break;
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                    s_addr(empty + s))
+                    s_addr(accf + buf))
                              : "memory");
             }
-            // accumulator complete (or abandoned): wake the epilogue either way
-            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                s_addr(accf))
+            // every MMA issued so far completes before TMEM may be freed
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(s_addr(fin))
                          : "memory");
+            const unsigned long long t0 = g_time();
+            while (!tc_mbar_try(fin, 0) && g_time() - t0 < TIMEOUT_NS) {
+            }
         }
     } else {
-        // ---------------- epilogue: warp w reads TMEM lanes 32 * (w % 4) ..
+        // ---------------- epilogue: warp w reads TMEM lanes 32 * (w % 4) .. of the tile's accumulator
         const int q = warp & 3;
-        const bool ok = tc_wait(accf, 0, abort_s) && !*abort_s;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const int t = m0 + q * 32 + lane;
-        unsigned long long best = 0ull;
-        if (ok) {
+        int it = 0;
+        for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++it) {
+            const int buf = it & 1;
+            if (!tc_wait(accf + buf, (it >> 1) & 1, abort_s) || *abort_s) {
+                if (lane == 0 && q == 0) set_err(err, ERR_TIMEOUT);
+                *abort_s = 1;
+                break;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const int m0 = (tile % MT) * BM, n0 = (tile / MT) * BN;
+            const int t = m0 + q * 32 + lane;
+            unsigned long long best = 0ull;
             for (int c = 0; c < BN; c += 16) {
                 uint32_t r[16];
-                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c;
+                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c);
                 asm volatile(
                     "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
                     "[%16];"
@@ -291,8 +324,9 @@ __global__ void __launch_bounds__(tc::NT, 1)
                 }
             }
             if (e.mode == EPI_LOGITS && e.amax && t < T && best) atomicMax(e.amax + t, best);
-        } else if (lane == 0 && q == 0) {
-            set_err(err, ERR_TIMEOUT);
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(s_addr(acce + buf)) : "memory");
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -742,8 +776,14 @@ int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi&
         cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM);
         attr = true;
     }
-    dim3 grid((N + tc::BN - 1) / tc::BN, (T + tc::BM - 1) / tc::BM);
-    launch_pdl(k_gemm_tc, grid, tc::NT, tc::SMEM, st, ma, mb, T, N, K, e, err);
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    const int tiles = ((N + tc::BN - 1) / tc::BN) * ((T + tc::BM - 1) / tc::BM);
+    launch_pdl(k_gemm_tc, std::min(tiles, sms), tc::NT, tc::SMEM, st, ma, mb, T, N, K, e, err);
     return 1;
 }
 
