@@ -572,9 +572,20 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--no-secondary", action="store_true", help="skip the batch-64 serving, MaskGIT and Code Predictor lines")
+    ap.add_argument("--only", choices=["serving_b64", "maskgit", "code_predictor"],
+                    help="run one secondary workload alone (--steps / --warmup apply) and print its line; a profiling aid")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.only:
+        import torch
+        from tests.gpu_util import build_lib
+        torch.cuda.set_device(0)
+        build_lib()
+        fn = {"serving_b64": run_serving_b64, "maskgit": run_maskgit, "code_predictor": run_code_predictor}[args.only]
+        r = fn(args.steps, args.warmup)
+        print(json.dumps({k: v for k, v in r.items() if k != "kernel_profile"}), flush=True)
+        return
 
     if args.impl == "reference":
         ws, rank, _ = dist_setup("gloo")
