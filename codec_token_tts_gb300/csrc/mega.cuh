@@ -63,8 +63,11 @@ cudaError_t launch_decode_ll(const MegaArgs& a, int grid, cudaStream_t st);
 int ll_max_grid();
 constexpr int LL_MIN_GRID = 96;   // smallest grid whose per-CTA op slices fit the weight ring
 constexpr int TRACE_STRIDE = 40;  // profiling stamps per (CTA, layer)
-constexpr int LL_XR = 8;          // replicas of the h and SwiGLU exchange vectors (readers spread over them)
-constexpr int LL_XRP = 8;         // replicas of the attention partials
+// Replicas of the h and SwiGLU exchange vectors and of the attention partials (readers spread over
+// them, writers store every copy). Measured at batch 1 on 128 CTAs (tokens/s, h/SwiGLU : partials):
+// 1:1 2001, 2:2 2072, 4:4 2091, 4:2 2092, 8:8 2027, 16:8 2036, 16:16 1994.
+constexpr int LL_XR = 4;
+constexpr int LL_XRP = 4;
 uint32_t ll_epochs_per_launch(int n_layers);
 // Exchange words the flag-in-data step needs for mbps cache blocks per sequence.
 inline size_t ll_xbuf_words(int mbps) {
