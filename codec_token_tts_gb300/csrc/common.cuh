@@ -152,6 +152,8 @@ int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi&
 int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N, int K, const Epi& e, int* err,
                     cudaStream_t st);
 bool gemm_tc_available();
+int launch_attn_bidir_tc(const bf16* q, const bf16* pool, size_t pool_blocks, int bps, const int32_t* key_len, int B,
+                         int S, bf16* out, int* err, cudaStream_t st);
 
 // Per-token q/k RMSNorm + RoPE; q -> qout [T][16][128] bf16; k, v -> paged pool.
 // Token t belongs to sequence t / tok_per_seq at position seq_start[seq] + t % tok_per_seq,

@@ -173,6 +173,7 @@ struct tts_bb {
     unsigned long long* amax = nullptr;
     int32_t *seq_slot = nullptr, *seq_start = nullptr, *seq_len = nullptr, *key_len = nullptr;
     bf16* mg_pool = nullptr;
+    bool attn_bidir_tc = false;  // bidirectional attention on tcgen05 (else the mma.sync flash kernel)
     size_t mg_pool_blocks = 0;
     int* err = nullptr;
     int* h_err = nullptr;
@@ -312,10 +313,10 @@ tts_bb_status finish(tts_bb* h) {
 }
 
 enum Kind { K_SETUP, K_EMBED, K_RMSNORM, K_GEMV, K_GEMM, K_QKROPE, K_ATTN_DECODE, K_ATTN_PREFILL, K_ARGMAX,
-            K_KVCOPY, K_MEGA, K_GEMM_TC, K_GEMM_TCD, K_NKINDS };
+            K_KVCOPY, K_MEGA, K_GEMM_TC, K_GEMM_TCD, K_ATTN_BIDIR_TC, K_NKINDS };
 const char* kind_name[K_NKINDS] = {"setup", "embed_gather", "rmsnorm", "gemv", "gemm_mma_split", "qk_norm_rope_append",
                                    "attn_decode", "attn_prefill", "argmax", "kv_copy", "decode_step_persistent",
-                                   "gemm_tcgen05", "gemm_tcgen05_decode"};
+                                   "gemm_tcgen05", "gemm_tcgen05_decode", "attn_bidir_tcgen05"};
 
 cudaEvent_t prof_event(tts_bb* h) {
     if (!h->ev_pool.empty()) {
@@ -397,6 +398,8 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
                 double kv_read_bytes = 0, double attn_flops = 0) {
     const tts_bb_config& c = h->cfg;
     const int T = B * tok_per_seq;
+    // the bidirectional pass keeps K / V in its own pool (no page table), which the tcgen05 kernel reads by TMA
+    const bool bidir_tc = mode == 2 && h->attn_bidir_tc;
     for (int l = 0; l < c.n_layers; ++l) {
         const LayerW& w = h->L[l];
         KVView kv = kv_base;
@@ -417,7 +420,10 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         { Launch L(h, K_QKROPE, T * (4.0 * QKV + 2.0 * QKV));
           L += launch_qk_norm_rope_append(h->qkv, w.qn, w.kn, h->cos_t, h->sin_t, c.rms_eps, h->q, kv,
                                           h->seq_start, h->seq_len, tok_per_seq, T, h->err, h->st); }
-        if (mode == 0) {
+        if (bidir_tc) {
+            Launch L(h, K_ATTN_BIDIR_TC, 0, attn_flops);
+            L += launch_attn_bidir_tc(h->q, kv.pool, h->mg_pool_blocks, kv.mbps, h->key_len, B, tok_per_seq, h->ao, h->err, h->st);
+        } else if (mode == 0) {
             Launch L(h, K_ATTN_DECODE, kv_read_bytes + T * (2.0 * NQ * HD * 2), 4.0 * NQ * HD * (kv_read_bytes / (2.0 * NKV * HD * 2)));
             L += launch_attn_decode(h->q, kv, h->seq_start, B, max_len, h->part, h->ao, MAX_SPLITS, h->st, aolo);
         } else {
@@ -794,6 +800,10 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
             return bail(TTS_BB_E_OOM);
         cudaMemset(h->sk.ctr, 0, 256 * sizeof(int));
     }
+    {
+        const char* av = std::getenv("TTS_BB_BIDIR_ATTN");  // "mma": the mma.sync flash kernel for the bidirectional pass
+        h->attn_bidir_tc = gemm_tc_available() && !(av && std::strcmp(av, "mma") == 0);
+    }
     if (c.max_slots > 0) {  // graph-replayed decode steps: step block, staging ring, fixed input / output buffers
         const char* gv = std::getenv("TTS_BB_GRAPHS");
         h->graphs_on = !(gv && std::strcmp(gv, "0") == 0);
@@ -1123,6 +1133,9 @@ TTS_API tts_bb_status tts_bb_maskgit_pass(tts_bb* h, int B, int S, const int32_t
             h->mg_pool_blocks = 0;
         }
         cudaError_t e = dalloc(h, &h->mg_pool, need_blocks * 2 * NKV * KVB * HD);
+        if (e != cudaSuccess) return cuda_fail(h, e, "MaskGIT scratch");
+        // keys past a sequence's end are masked (probability 0) but still multiplied: keep them finite
+        e = cudaMemsetAsync(h->mg_pool, 0, need_blocks * 2 * NKV * KVB * HD * sizeof(bf16), h->st);
         if (e != cudaSuccess) return cuda_fail(h, e, "MaskGIT scratch");
         h->mg_pool_blocks = need_blocks;
     }

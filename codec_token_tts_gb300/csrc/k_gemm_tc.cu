@@ -642,6 +642,331 @@ __global__ void __launch_bounds__(tcd::NT, 1)
     }
 }
 
+// ---------------------------------------------------------------- bidirectional attention on tcgen05
+// Flash attention for the MaskGIT pass (no mask but per-sequence key lengths).
+// A CTA takes 64 queries of the two query heads of one KV head: 128 rows
+// (rows 0..63 head 2g, 64..127 head 2g+1) of Q, loaded once into shared
+// memory in the 128-byte-swizzled K-major layout. Per tile of 128 keys (two
+// cache blocks) a producer thread loads K and V [128 keys][128 dims] with TMA
+// into a 2-stage ring; the MMA thread computes S = Q K^T into one of two TMEM
+// buffers (M = N = K = 128, K-major operands) and, once the softmax warps
+// have written P, O += P V into a TMEM accumulator (V read MN-major, as the
+// cache stores it). Four softmax warps (thread = row) read a whole S row
+// into registers, take its max in the base-2 domain and write
+// P = exp2(s - m) as bf16 into one of two shared-memory buffers (swizzled,
+// the A operand of P V), keeping the row sum. The running max m moves only
+// when a tile's max exceeds it by more than 8, and then O (TMEM) and the sum
+// are rescaled, so P stays <= 2^8 and the result is exact up to rounding;
+// with P double-buffered the softmax of tile j + 1 runs while the tensor
+// cores do P V of tile j. Every wait is bounded.
+namespace at {
+constexpr int BQ = 64, ROWS = 128, BKV = 128, NT = 192, STAGES = 2;
+constexpr int CHUNK = ROWS * 128;                 // 128 rows x 128 B, 128-byte swizzled
+constexpr int Q_OFF = 0, K_OFF = 2 * CHUNK, V_OFF = K_OFF + STAGES * 2 * CHUNK, P_OFF = V_OFF + STAGES * 2 * CHUNK;
+constexpr int BAR_OFF = P_OFF + 2 * 2 * CHUNK;    // 224 KB
+constexpr int SMEM = BAR_OFF + 256 + 1024;
+constexpr int TMEM_COLS = 512;                    // S buffers at 0, 128; O at 256
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+constexpr uint32_t IDESC_PV = IDESC | (1u << 16);  // B (V) MN-major
+// V stage: [cache block i][dims 64c .. 64c+63][64 keys x 128 B]: MN-major atoms of 64 dims x 8 keys,
+// 1024 B apart along the keys (stride offset), 8 KB apart along the dims (leading offset)
+constexpr uint32_t V_LBO = 8192, V_SBO = 1024;
+constexpr unsigned long long TIMEOUT_NS = 1000000000ull;
+}  // namespace at
+static_assert(at::SMEM <= 232448, "shared memory per CTA");
+
+// byte offset of 16-byte piece c of row r in a 128-byte-swizzled chunk
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+// MN-major 128-byte-swizzled operand descriptor with explicit leading / stride offsets
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// 32 lanes x 32 columns of 32 bit from TMEM (no wait: tm_wait_ld before use)
+__device__ __forceinline__ void tm_ld32_nw(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tm_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tm_st32(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void at_mma(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+        "l"(ad), "l"(bd), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void at_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(s_addr(bar)) : "memory");
+}
+// hardware base-2 exponential (approximate, flushes denormals); ex2(-inf) = 0
+__device__ __forceinline__ float at_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// grid (ceil(S / 64), 8, B), 192 threads. q [B*S][16][128] bf16; pool: K and V tiles [64][128] per
+// (block, KV head), [blocks][K, V][8][64][128], blocks of sequence b at b * bps; out [B*S][16][128] bf16.
+__global__ void __launch_bounds__(at::NT, 1)
+    k_attn_bidir_tc(const __grid_constant__ CUtensorMap tmKV, const bf16* __restrict__ q,
+                    const int32_t* __restrict__ key_len, int S, int bps, bf16* __restrict__ out, int* err) {
+    using namespace at;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+    uint64_t* kv_empty = kv_full + STAGES;
+    uint64_t* s_full = kv_empty + STAGES;  // [2] S buffer j & 1 written
+    uint64_t* p_full = s_full + 2;         // [2] P buffer j & 1 written (4 softmax-warp arrivals)
+    uint64_t* o_done = p_full + 2;         // [2] P V of a tile using P buffer j & 1 complete
+    uint64_t* fin = o_done + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
+    volatile int* abort_s = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const int qt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            tc_mbar_init(kv_full + i, 1);
+            tc_mbar_init(kv_empty + i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc_mbar_init(s_full + i, 1);
+            tc_mbar_init(p_full + i, 4);
+            tc_mbar_init(o_done + i, 1);
+        }
+        tc_mbar_init(fin, 1);
+        *abort_s = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(s_addr(tmem_slot)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    pdl_wait();  // q and the K / V tiles come from upstream kernels
+    pdl_trigger();
+    // Q rows -> shared memory, swizzled (rows past the sequence are zero)
+    for (int i = threadIdx.x; i < ROWS * 16; i += NT) {
+        const int r = i >> 4, pc = i & 15, c = pc >> 3, piece = pc & 7;
+        const int sq = qt * BQ + (r & 63), head = 2 * g + (r >> 6);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (sq < S) v = *reinterpret_cast<const uint4*>(q + (((size_t)b * S + sq) * NQ + head) * HD + c * 64 + piece * 8);
+        *reinterpret_cast<uint4*>(smem + Q_OFF + c * CHUNK + sw128_off(r, piece)) = v;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q (generic writes) -> tensor core reads
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot;
+    const int L = key_len[b];
+    const int nt = (L + BKV - 1) / BKV;
+
+    if (warp == 0) {
+        if (lane == 0) {  // ---------------- TMA producer: K and V of each 128-key tile
+            int issued = 0;
+            for (int j = 0; j < nt; ++j) {
+                const int st = j % STAGES;
+                if (j >= STAGES && !tc_wait(kv_empty + st, ((j / STAGES) - 1) & 1, abort_s)) {
+                    *abort_s = 1;
+                    break;
+                }
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(kv_full + st)),
+                             "r"((uint32_t)(4 * CHUNK))
+                             : "memory");
+                for (int i = 0; i < 2; ++i) {
+                    const int phys = b * bps + 2 * j + i;  // past the sequence: masked keys (or zero fill)
+                    const int krow = ((phys * 2 + 0) * NKV + g) * KVB, vrow = ((phys * 2 + 1) * NKV + g) * KVB;
+                    for (int c = 0; c < 2; ++c) {
+                        tma_load_2d(smem + K_OFF + st * 2 * CHUNK + c * CHUNK + i * (CHUNK / 2), &tmKV, c * 64, krow,
+                                    kv_full + st);
+                        tma_load_2d(smem + V_OFF + st * 2 * CHUNK + i * CHUNK + c * (CHUNK / 2), &tmKV, c * 64, vrow,
+                                    kv_full + st);
+                    }
+                }
+                ++issued;
+            }
+            if (*abort_s)
+                for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j) {
+                    const unsigned long long t0 = g_time();
+                    while (!tc_mbar_try(kv_full + j % STAGES, (j / STAGES) & 1) && g_time() - t0 < TIMEOUT_NS) {
+                    }
+                }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---------------- MMA issuer
+            const uint32_t q0 = s_addr(smem + Q_OFF);
+            auto issue_s = [&](int j) {  // S_j = Q K_j^T into buffer j & 1
+                const int st = j % STAGES;
+                const uint32_t k0 = s_addr(smem + K_OFF + st * 2 * CHUNK), d = tmem + (uint32_t)((j & 1) * 128);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (uint32_t)((kk >> 2) * CHUNK + (kk & 3) * 32);
+                    at_mma(d, sw128_desc(q0 + off), sw128_desc(k0 + off), IDESC, kk ? 1u : 0u);
+                }
+                at_commit(s_full + (j & 1));
+            };
+            bool ok = nt > 0 && tc_wait(kv_full, 0, abort_s);
+            if (ok) {
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                issue_s(0);
+            }
+            for (int j = 0; j < nt && ok; ++j) {
+                if (j + 1 < nt) {  // S buffer (j+1) & 1 was read by the softmax of tile j - 1 (p_full waited)
+                    if (!tc_wait(kv_full + (j + 1) % STAGES, ((j + 1) / STAGES) & 1, abort_s)) { ok = false; break; }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    issue_s(j + 1);
+                }
+                if (!tc_wait(p_full + (j & 1), (j >> 1) & 1, abort_s)) { ok = false; break; }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const int st = j % STAGES;
+                const uint32_t p0 = s_addr(smem + P_OFF + (j & 1) * 2 * CHUNK), v0 = s_addr(smem + V_OFF + st * 2 * CHUNK);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step: P chunk kk >> 2, V block kk >> 2, 8-key groups 2 (kk & 3)
+                    const uint64_t ad = sw128_desc(p0 + (uint32_t)((kk >> 2) * CHUNK + (kk & 3) * 32));
+                    const uint64_t bd = sw128_desc_mn(v0 + (uint32_t)((kk >> 2) * CHUNK + (kk & 3) * 2048), V_LBO, V_SBO);
+                    at_mma(tmem + 256, ad, bd, IDESC_PV, (j | kk) ? 1u : 0u);
+                }
+                at_commit(o_done + (j & 1));
+                at_commit(kv_empty + st);
+            }
+            if (!ok) *abort_s = 1;
+            at_commit(fin);
+            const unsigned long long t0 = g_time();
+            while (!tc_mbar_try(fin, 0) && g_time() - t0 < TIMEOUT_NS) {
+            }
+        }
+    } else {
+        // ---------------- softmax + epilogue: thread = row (TMEM lane)
+        const int qd = warp & 3, r = qd * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
+        const float sc = rsqrtf((float)HD) * 1.4426950408889634f;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nt && ok; ++j) {
+            if (!tc_wait(s_full + (j & 1), (j >> 1) & 1, abort_s)) { ok = false; break; }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            uint32_t v[128];
+            const uint32_t sb = lane_base + (uint32_t)((j & 1) * 128);
+            tm_ld32_nw(sb, v);
+            tm_ld32_nw(sb + 32, v + 32);
+            tm_ld32_nw(sb + 64, v + 64);
+            tm_ld32_nw(sb + 96, v + 96);
+            tm_wait_ld();
+            const int kvalid = L - j * BKV;  // keys of this tile below the sequence's key length
+            if (kvalid < BKV) {
+#pragma unroll
+                for (int x = 0; x < 128; ++x)
+                    if (x >= kvalid) v[x] = 0xFF800000u;  // -inf
+            }
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int x = 0; x < 128; ++x) m4[x & 3] = fmaxf(m4[x & 3], __uint_as_float(v[x]));
+            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sc;
+            float alpha = 1.f;
+            const bool move = mx > m_used + 8.f;
+            if (move) {
+                alpha = (m_used == -INFINITY) ? 0.f : at_ex2(m_used - mx);
+                m_used = mx;
+            }
+            // P buffer j & 1 was read by P V of tile j - 2
+            if (j >= 2 && !tc_wait(o_done + (j & 1), ((j - 2) >> 1) & 1, abort_s)) { ok = false; break; }
+            if (move && j >= 1) {  // rescale O once P V of tile j - 1 is in it
+                if (!tc_wait(o_done + ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_s)) { ok = false; break; }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t o[32];
+                    tm_ld32_nw(lane_base + 256 + ch * 32, o);
+                    tm_wait_ld();
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+                    tm_st32(lane_base + 256 + ch * 32, o);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            }
+            l *= alpha;
+            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+            unsigned char* pbase = smem + P_OFF + (j & 1) * 2 * CHUNK;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int x = 0; x < 32; x += 2) {
+                    const float p0 = at_ex2(fmaf(__uint_as_float(v[ch * 32 + x]), sc, -m_used));
+                    const float p1 = at_ex2(fmaf(__uint_as_float(v[ch * 32 + x + 1]), sc, -m_used));
+                    l4[(x >> 1) & 3] += p0 + p1;
+                    __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                    pk[x >> 1] = *reinterpret_cast<uint32_t*>(&h2);
+                }
+                // keys ch*32 .. ch*32+31: key chunk ch >> 1, pieces (ch & 1) * 4 .. + 3 of row r
+                unsigned char* prow = pbase + (ch >> 1) * CHUNK;
+#pragma unroll
+                for (int pp = 0; pp < 4; ++pp)
+                    *reinterpret_cast<uint4*>(prow + sw128_off(r, (ch & 1) * 4 + pp)) =
+                        make_uint4(pk[4 * pp], pk[4 * pp + 1], pk[4 * pp + 2], pk[4 * pp + 3]);
+            }
+            l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P (generic writes) -> tensor core reads
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(s_addr(p_full + (j & 1))) : "memory");
+        }
+        if (ok && nt > 0 && tc_wait(o_done + ((nt - 1) & 1), ((nt - 1) >> 1) & 1, abort_s)) {
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const int sq = qt * BQ + (r & 63), head = 2 * g + (r >> 6);
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t o[32];
+                tm_ld32_nw(lane_base + 256 + ch * 32, o);
+                tm_wait_ld();
+                if (sq < S) {
+                    bf16* dst = out + (((size_t)b * S + sq) * NQ + head) * HD + ch * 32;
+#pragma unroll
+                    for (int x = 0; x < 32; x += 8) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            __nv_bfloat162 a2 = __floats2bfloat162_rn(__uint_as_float(o[x + 2 * u]) * inv,
+                                                                      __uint_as_float(o[x + 2 * u + 1]) * inv);
+                            w[u] = *reinterpret_cast<uint32_t*>(&a2);
+                        }
+                        *reinterpret_cast<uint4*>(dst + x) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+        } else if (lane == 0 && qd == 0) {
+            set_err(err, ERR_TIMEOUT);
+            *abort_s = 1;
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 1) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+    }
+}
+
 // ---------------------------------------------------------------- host side
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -706,8 +1031,24 @@ static bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_
 
 bool gemm_tc_available() { return encode_fn() != nullptr; }
 
-// X_lo-carrying GEMM for 8 < T <= 128 tokens on tcgen05 (swap-AB, cluster
-// split-K). Returns the number of kernels launched (0 if unsupported).
+// Bidirectional attention of the MaskGIT pass on tcgen05 (no page table: sequence b's blocks at
+// b * bps). Returns launches (0 = not available).
+int launch_attn_bidir_tc(const bf16* q, const bf16* pool, size_t pool_blocks, int bps, const int32_t* key_len, int B,
+                         int S, bf16* out, int* err, cudaStream_t st) {
+    if (B <= 0 || S <= 0 || !gemm_tc_available()) return 0;
+    const size_t rows = pool_blocks * 2 * NKV * KVB;  // [rows][128]: K and V tiles of every (block, KV head)
+    if (rows > (size_t)INT32_MAX) return 0;
+    CUtensorMap mkv;
+    if (!make_map(&mkv, pool, (int)rows, HD, KVB)) return 0;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_attn_bidir_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, at::SMEM);
+        attr = true;
+    }
+    dim3 grid((S + at::BQ - 1) / at::BQ, NKV, B);
+    return launch_pdl(k_attn_bidir_tc, grid, at::NT, at::SMEM, st, mkv, q, key_len, S, bps, out, err) == cudaSuccess ? 1 : 0;
+}
+
 int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N, int K, const Epi& e, int* err,
                     cudaStream_t st) {
     if (T <= 0 || T > tcd::MAXTB || N <= 0 || K % tcd::BK != 0 || !X_lo) return 0;

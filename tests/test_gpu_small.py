@@ -301,24 +301,37 @@ def test_code_predictor_frame_small_batch():
 
 
 # ---------------------------------------------------------------- MaskGIT bidirectional pass
-def test_maskgit_pass_small_with_padding():
+@pytest.mark.parametrize("attn", ["tcgen05", "mma"])
+@pytest.mark.parametrize("key_lens", [(200, 150), (70, 129)])
+def test_maskgit_pass_small_with_padding(attn, key_lens, monkeypatch):
+    """Bidirectional pass with padded sequences on both attention kernels: the
+    tcgen05 one (128-key tiles: a tile with one valid key at 129, one shorter
+    than a cache block at 70) and the mma.sync flash kernel."""
+    if attn == "mma":
+        monkeypatch.setenv("TTS_BB_BIDIR_ATTN", "mma")
     shape = synth.ModelShape(n_layers=2, text_vocab=4096, audio_codebooks=8, audio_vocab=1025, n_heads_out=8,
                              head_rows=1025)
     w = synth.model_weights(shape, 27)
     m0 = O.Backbone(w, shape)
     B, S, n_text = 2, 200, 56
     ids, mask = synth.maskgit_inputs(27, 0, B=B, S=S, n_text=n_text, text_vocab=4096)
-    key_lens = np.array([200, 150], np.int32)
+    key_lens = np.array(key_lens, np.int32)
     lo, ho = O.maskgit_pass(m0, ids, mask, n_text, key_lens=key_lens)
     with Engine(w, max_slots=0, max_ctx=0, max_batch=B, max_tokens=B * S) as e:
         m = e.m
         logits = f32_zeros(B, 8, S - n_text, 1025)
         hid = f32_zeros(B, S, 1024)
+        m.tts_bb_profile(e.h, True)
         m.tts_bb_maskgit_pass(e.h, B, S, dev_i32(ids), dev_u8(mask), key_lens, n_text, logits, hidden_out=hid)
+        kinds = {k["kind"] for k in m.tts_bb_profile_report(e.h)["kernels"]}
+        m.tts_bb_profile(e.h, False)
+        assert ("attn_bidir_tcgen05" in kinds) == (attn == "tcgen05"), kinds
+        assert ("attn_prefill" in kinds) == (attn == "mma"), kinds
         g = hid.cpu().numpy()
-        assert rel_err_rows(g[0], ho[0]) <= HIDDEN_TOL
-        assert rel_err_rows(g[1, :150], ho[1, :150]) <= HIDDEN_TOL
         gl = logits.cpu().numpy()
-        err0 = np.max(np.abs(gl[0] - lo[0]))
-        err1 = np.max(np.abs(gl[1][:, :150 - n_text] - lo[1][:, :150 - n_text]))
-        assert max(err0, err1) <= LOGIT_TOL, (err0, err1)
+        for b in range(B):
+            kl = int(key_lens[b])
+            assert rel_err_rows(g[b, :kl], ho[b, :kl]) <= HIDDEN_TOL, b
+            if kl > n_text:
+                err = np.max(np.abs(gl[b][:, :kl - n_text] - lo[b][:, :kl - n_text]))
+                assert err <= LOGIT_TOL, (b, err)
