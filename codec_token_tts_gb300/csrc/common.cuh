@@ -16,7 +16,7 @@ constexpr int QKV = (NQ + 2 * NKV) * HD;  // 4096 fused projection rows
 constexpr int KVB = 64;        // tokens per KV block
 
 // Device error word bits.
-enum : int { ERR_BAD_ID = 1, ERR_TIMEOUT = 2, ERR_KV_RANGE = 4 };
+enum : int { ERR_BAD_ID = 1, ERR_TIMEOUT = 2, ERR_KV_RANGE = 4, ERR_LAYOUT = 8 };
 
 __device__ __forceinline__ void set_err(int* err, int bit) {
     if (err) atomicOr(err, bit);

@@ -173,7 +173,8 @@ struct tts_bb {
     unsigned long long* amax = nullptr;
     int32_t *seq_slot = nullptr, *seq_start = nullptr, *seq_len = nullptr, *key_len = nullptr;
     bf16* mg_pool = nullptr;
-    bool attn_bidir_tc = false;  // bidirectional attention on tcgen05 (else the mma.sync flash kernel)
+    bool attn_bidir_tc = false;
+    int l2_prefetch = 1;         // persistent step: next-layer weight rows prefetched into L2  // bidirectional attention on tcgen05 (else the mma.sync flash kernel)
     size_t mg_pool_blocks = 0;
     int* err = nullptr;
     int* h_err = nullptr;
@@ -301,6 +302,7 @@ tts_bb_status read_err(tts_bb* h) {
         if (v & ERR_TIMEOUT) return fail(h, TTS_BB_E_DEVICE_TIMEOUT, "a device-side wait timed out");
         if (v & ERR_BAD_ID) return fail(h, TTS_BB_E_BAD_ID, "a token id was outside its table (skipped)");
         if (v & ERR_KV_RANGE) return fail(h, TTS_BB_E_INVALID, "a KV position had no block");
+        if (v & ERR_LAYOUT) return fail(h, TTS_BB_E_CUDA, "a kernel's shared memory was not 1 KB aligned");
     }
     return TTS_BB_OK;
 }
@@ -827,6 +829,7 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
         // so no CTA carries an extra row pair into the critical path: measured faster than all 152 SMs
         // (2040 vs 1911 tokens/s at batch 1) and than every grid from 96 to 144 tried.
         if (h->mega_grid >= 128) h->mega_grid = 128;
+        if (const char* pf = std::getenv("TTS_BB_L2_PREFETCH")) h->l2_prefetch = std::atoi(pf) != 0;
         if (const char* g = std::getenv("TTS_BB_DECODE_CTAS"))  // tuning knob: CTAs of the persistent step
             h->mega_grid = std::max(std::min(ll_max_grid(), LL_MIN_GRID), std::min(ll_max_grid(), std::atoi(g)));
         if (h->mega_grid > 0) {
@@ -958,6 +961,7 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
         ma.ep_base = h->ep_base;
         ma.timeout_ns = h->wait_limit_ns;
         ma.debug_stall = h->stall_next;
+        ma.l2_prefetch = h->l2_prefetch;
         h->stall_next = 0;
         for (int b = 0; b < B; ++b) ma.last_phys[b] = h->page_table[(size_t)slots[b] * h->mbps + kv_lens[b] / KVB];
         ma.trace = nullptr;

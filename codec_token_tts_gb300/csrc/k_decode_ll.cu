@@ -722,6 +722,19 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
                     const LOp d = l_op(a, l, o);
                     int r0, r1;
                     l_rows(d.N, blockIdx.x, gridDim.x, r0, r1);
+                    // this CTA's rows of the same op one layer ahead (the head after the last layer)
+                    // -> L2, so HBM keeps streaming while the ring is full and ring copies hit L2
+                    if (a.l2_prefetch && (l + 1 < a.n_layers || (l + 1 == a.n_layers && a.head && o == 0))) {
+                        const LOp nx = l_op(a, l + 1, o);
+                        int p0, p1;
+                        l_rows(nx.N, blockIdx.x, gridDim.x, p0, p1);
+                        const char* src = reinterpret_cast<const char*>(nx.W + (size_t)p0 * nx.K);
+                        const uint32_t total = (uint32_t)(p1 - p0) * (uint32_t)nx.K * 2u;
+                        for (uint32_t off = 0; off < total; off += 16384u)
+                            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src + off),
+                                         "r"(min(16384u, total - off))
+                                         : "memory");
+                    }
                     const int rpc = l_rpc(d.K);
                     const uint32_t rs = (uint32_t)d.K * 2 + ll::ROW_PAD;  // ring row stride
                     for (int rc = r0; rc < r1 && ok; rc += rpc) {

@@ -651,20 +651,23 @@ __global__ void __launch_bounds__(tcd::NT, 1)
 // into a 2-stage ring; the MMA thread computes S = Q K^T into one of two TMEM
 // buffers (M = N = K = 128, K-major operands) and, once the softmax warps
 // have written P, O += P V into a TMEM accumulator (V read MN-major, as the
-// cache stores it). Four softmax warps (thread = row) read a whole S row
-// into registers, take its max in the base-2 domain and write
-// P = exp2(s - m) as bf16 into one of two shared-memory buffers (swizzled,
-// the A operand of P V), keeping the row sum. The running max m moves only
-// when a tile's max exceeds it by more than 8, and then O (TMEM) and the sum
+// cache stores it). Eight softmax warps, two per row quarter (TMEM lanes),
+// each take 64 of a tile's 128 columns: a thread reads its half row into
+// registers, the two halves exchange their maxima through shared memory,
+// and each writes P = exp2(s - m) as bf16 into its half of one of two
+// shared-memory buffers (swizzled, the A operand of P V), keeping its own
+// partial row sum. The running max m moves only when a tile's max exceeds it
+// by more than 8, and then O (TMEM, each half its 64 columns) and the sums
 // are rescaled, so P stays <= 2^8 and the result is exact up to rounding;
 // with P double-buffered the softmax of tile j + 1 runs while the tensor
 // cores do P V of tile j. Every wait is bounded.
 namespace at {
-constexpr int BQ = 64, ROWS = 128, BKV = 128, NT = 192, STAGES = 2;
+constexpr int BQ = 64, ROWS = 128, BKV = 128, NT = 320, STAGES = 2;
 constexpr int CHUNK = ROWS * 128;                 // 128 rows x 128 B, 128-byte swizzled
 constexpr int Q_OFF = 0, K_OFF = 2 * CHUNK, V_OFF = K_OFF + STAGES * 2 * CHUNK, P_OFF = V_OFF + STAGES * 2 * CHUNK;
-constexpr int BAR_OFF = P_OFF + 2 * 2 * CHUNK;    // 224 KB
-constexpr int SMEM = BAR_OFF + 256 + 1024;
+constexpr int BAR_OFF = P_OFF + 2 * 2 * CHUNK;    // 224 KB of tiles, then barriers
+constexpr int PM_OFF = BAR_OFF + 256;             // [2 tile parities][2 halves][128 rows] fp32 row maxima
+constexpr int SMEM = PM_OFF + 2 * 2 * ROWS * 4;   // the tiles start the (1 KB-aligned) dynamic shared memory
 constexpr int TMEM_COLS = 512;                    // S buffers at 0, 128; O at 256
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 constexpr uint32_t IDESC_PV = IDESC | (1u << 16);  // B (V) MN-major
@@ -726,33 +729,41 @@ __device__ __forceinline__ float at_ex2(float x) {
     return y;
 }
 
-// grid (ceil(S / 64), 8, B), 192 threads. q [B*S][16][128] bf16; pool: K and V tiles [64][128] per
+// grid (ceil(S / 64), 8, B), 320 threads. q [B*S][16][128] bf16; pool: K and V tiles [64][128] per
 // (block, KV head), [blocks][K, V][8][64][128], blocks of sequence b at b * bps; out [B*S][16][128] bf16.
 __global__ void __launch_bounds__(at::NT, 1)
     k_attn_bidir_tc(const __grid_constant__ CUtensorMap tmKV, const bf16* __restrict__ q,
                     const int32_t* __restrict__ key_len, int S, int bps, bf16* __restrict__ out, int* err) {
     using namespace at;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
-    uint64_t* kv_empty = kv_full + STAGES;
-    uint64_t* s_full = kv_empty + STAGES;  // [2] S buffer j & 1 written
-    uint64_t* p_full = s_full + 2;         // [2] P buffer j & 1 written (4 softmax-warp arrivals)
+    extern __shared__ __align__(1024) unsigned char smem[];
+    if (s_addr(smem) & 1023u) {  // the swizzled tiles need a 1 KB-aligned base
+        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) set_err(err, ERR_LAYOUT);
+        return;
+    }
+    uint64_t* k_full = reinterpret_cast<uint64_t*>(smem + BAR_OFF);  // [STAGES] K of a tile landed
+    uint64_t* k_empty = k_full + STAGES;   // [STAGES] S of the tile done (K stage free)
+    uint64_t* v_full = k_empty + STAGES;   // [STAGES] V of a tile landed
+    uint64_t* v_empty = v_full + STAGES;   // [STAGES] P V of the tile done (V stage free)
+    uint64_t* s_full = v_empty + STAGES;   // [2] S buffer j & 1 written
+    uint64_t* p_full = s_full + 2;         // [2] P buffer j & 1 written (8 softmax-warp arrivals)
     uint64_t* o_done = p_full + 2;         // [2] P V of a tile using P buffer j & 1 complete
     uint64_t* fin = o_done + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
     volatile int* abort_s = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* pm = reinterpret_cast<float*>(smem + PM_OFF);
     const int qt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            tc_mbar_init(kv_full + i, 1);
-            tc_mbar_init(kv_empty + i, 1);
+            tc_mbar_init(k_full + i, 1);
+            tc_mbar_init(k_empty + i, 1);
+            tc_mbar_init(v_full + i, 1);
+            tc_mbar_init(v_empty + i, 1);
         }
         for (int i = 0; i < 2; ++i) {
             tc_mbar_init(s_full + i, 1);
-            tc_mbar_init(p_full + i, 4);
+            tc_mbar_init(p_full + i, 8);
             tc_mbar_init(o_done + i, 1);
         }
         tc_mbar_init(fin, 1);
@@ -766,13 +777,23 @@ __global__ void __launch_bounds__(at::NT, 1)
     }
     pdl_wait();  // q and the K / V tiles come from upstream kernels
     pdl_trigger();
-    // Q rows -> shared memory, swizzled (rows past the sequence are zero)
-    for (int i = threadIdx.x; i < ROWS * 16; i += NT) {
-        const int r = i >> 4, pc = i & 15, c = pc >> 3, piece = pc & 7;
-        const int sq = qt * BQ + (r & 63), head = 2 * g + (r >> 6);
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (sq < S) v = *reinterpret_cast<const uint4*>(q + (((size_t)b * S + sq) * NQ + head) * HD + c * 64 + piece * 8);
-        *reinterpret_cast<uint4*>(smem + Q_OFF + c * CHUNK + sw128_off(r, piece)) = v;
+    // Q rows -> shared memory, swizzled (rows past the sequence are zero); all loads first
+    {
+        constexpr int NQL = (ROWS * 16 + NT - 1) / NT;
+        uint4 qv[NQL];
+#pragma unroll
+        for (int k = 0; k < NQL; ++k) {
+            const int i = threadIdx.x + k * NT, r = (i >> 4) & (ROWS - 1), pc = i & 15;
+            const int sq = qt * BQ + (r & 63), head = 2 * g + (r >> 6);
+            qv[k] = make_uint4(0u, 0u, 0u, 0u);
+            if (i < ROWS * 16 && sq < S)
+                qv[k] = *reinterpret_cast<const uint4*>(q + (((size_t)b * S + sq) * NQ + head) * HD + pc * 8);
+        }
+#pragma unroll
+        for (int k = 0; k < NQL; ++k) {
+            const int i = threadIdx.x + k * NT, r = (i >> 4) & (ROWS - 1), pc = i & 15;
+            if (i < ROWS * 16) *reinterpret_cast<uint4*>(smem + Q_OFF + (pc >> 3) * CHUNK + sw128_off(r, pc & 7)) = qv[k];
+        }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q (generic writes) -> tensor core reads
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -783,25 +804,27 @@ __global__ void __launch_bounds__(at::NT, 1)
     const int nt = (L + BKV - 1) / BKV;
 
     if (warp == 0) {
-        if (lane == 0) {  // ---------------- TMA producer: K and V of each 128-key tile
+        if (lane < 2) {  // ---------------- TMA producers: lane 0 K, lane 1 V of each 128-key tile
+            const int which = lane;
+            uint64_t* full = which ? v_full : k_full;
+            uint64_t* empty = which ? v_empty : k_empty;
             int issued = 0;
             for (int j = 0; j < nt; ++j) {
                 const int st = j % STAGES;
-                if (j >= STAGES && !tc_wait(kv_empty + st, ((j / STAGES) - 1) & 1, abort_s)) {
+                if (j >= STAGES && !tc_wait(empty + st, ((j / STAGES) - 1) & 1, abort_s)) {
                     *abort_s = 1;
                     break;
                 }
-                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(kv_full + st)),
-                             "r"((uint32_t)(4 * CHUNK))
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(full + st)),
+                             "r"((uint32_t)(2 * CHUNK))
                              : "memory");
                 for (int i = 0; i < 2; ++i) {
                     const int phys = b * bps + 2 * j + i;  // past the sequence: masked keys (or zero fill)
-                    const int krow = ((phys * 2 + 0) * NKV + g) * KVB, vrow = ((phys * 2 + 1) * NKV + g) * KVB;
+                    const int row = ((phys * 2 + which) * NKV + g) * KVB;
                     for (int c = 0; c < 2; ++c) {
-                        tma_load_2d(smem + K_OFF + st * 2 * CHUNK + c * CHUNK + i * (CHUNK / 2), &tmKV, c * 64, krow,
-                                    kv_full + st);
-                        tma_load_2d(smem + V_OFF + st * 2 * CHUNK + i * CHUNK + c * (CHUNK / 2), &tmKV, c * 64, vrow,
-                                    kv_full + st);
+                        // K stage: [dims chunk c][keys 64i ..]; V stage: [cache block i][dims chunk c]
+                        const int off = which ? i * CHUNK + c * (CHUNK / 2) : c * CHUNK + i * (CHUNK / 2);
+                        tma_load_2d(smem + (which ? V_OFF : K_OFF) + st * 2 * CHUNK + off, &tmKV, c * 64, row, full + st);
                     }
                 }
                 ++issued;
@@ -809,7 +832,7 @@ __global__ void __launch_bounds__(at::NT, 1)
             if (*abort_s)
                 for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j) {
                     const unsigned long long t0 = g_time();
-                    while (!tc_mbar_try(kv_full + j % STAGES, (j / STAGES) & 1) && g_time() - t0 < TIMEOUT_NS) {
+                    while (!tc_mbar_try(full + j % STAGES, (j / STAGES) & 1) && g_time() - t0 < TIMEOUT_NS) {
                     }
                 }
         }
@@ -825,19 +848,21 @@ __global__ void __launch_bounds__(at::NT, 1)
                     at_mma(d, sw128_desc(q0 + off), sw128_desc(k0 + off), IDESC, kk ? 1u : 0u);
                 }
                 at_commit(s_full + (j & 1));
+                at_commit(k_empty + st);
             };
-            bool ok = nt > 0 && tc_wait(kv_full, 0, abort_s);
+            bool ok = nt > 0 && tc_wait(k_full, 0, abort_s);
             if (ok) {
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 issue_s(0);
             }
             for (int j = 0; j < nt && ok; ++j) {
                 if (j + 1 < nt) {  // S buffer (j+1) & 1 was read by the softmax of tile j - 1 (p_full waited)
-                    if (!tc_wait(kv_full + (j + 1) % STAGES, ((j + 1) / STAGES) & 1, abort_s)) { ok = false; break; }
+                    if (!tc_wait(k_full + (j + 1) % STAGES, ((j + 1) / STAGES) & 1, abort_s)) { ok = false; break; }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                     issue_s(j + 1);
                 }
                 if (!tc_wait(p_full + (j & 1), (j >> 1) & 1, abort_s)) { ok = false; break; }
+                if (!tc_wait(v_full + j % STAGES, (j / STAGES) & 1, abort_s)) { ok = false; break; }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const int st = j % STAGES;
                 const uint32_t p0 = s_addr(smem + P_OFF + (j & 1) * 2 * CHUNK), v0 = s_addr(smem + V_OFF + st * 2 * CHUNK);
@@ -848,7 +873,7 @@ __global__ void __launch_bounds__(at::NT, 1)
                     at_mma(tmem + 256, ad, bd, IDESC_PV, (j | kk) ? 1u : 0u);
                 }
                 at_commit(o_done + (j & 1));
-                at_commit(kv_empty + st);
+                at_commit(v_empty + st);
             }
             if (!ok) *abort_s = 1;
             at_commit(fin);
@@ -857,32 +882,46 @@ __global__ void __launch_bounds__(at::NT, 1)
             }
         }
     } else {
-        // ---------------- softmax + epilogue: thread = row (TMEM lane)
-        const int qd = warp & 3, r = qd * 32 + lane;
+        // ---------------- softmax + epilogue: thread = row (TMEM lane), half = 64 of the 128 columns
+        const int qd = warp & 3, r = qd * 32 + lane, half = (warp - 2) >> 2;
         const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
+        const uint32_t cbase = (uint32_t)(half * 64);
         const float sc = rsqrtf((float)HD) * 1.4426950408889634f;
         float m_used = -INFINITY, l = 0.f;
+        // the two warps of a row quarter meet at a named barrier once per tile and twice after the
+        // loop; after a failed wait a warp keeps meeting them (skipping the work), so neither can hang
         bool ok = true;
-        for (int j = 0; j < nt && ok; ++j) {
-            if (!tc_wait(s_full + (j & 1), (j >> 1) & 1, abort_s)) { ok = false; break; }
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            uint32_t v[128];
-            const uint32_t sb = lane_base + (uint32_t)((j & 1) * 128);
-            tm_ld32_nw(sb, v);
-            tm_ld32_nw(sb + 32, v + 32);
-            tm_ld32_nw(sb + 64, v + 64);
-            tm_ld32_nw(sb + 96, v + 96);
-            tm_wait_ld();
-            const int kvalid = L - j * BKV;  // keys of this tile below the sequence's key length
-            if (kvalid < BKV) {
+        auto wait_u = [&](uint64_t* bar, uint32_t par) {  // warp-uniform bounded wait
+            if (ok) ok = __all_sync(0xffffffffu, tc_wait(bar, par, abort_s));
+            if (!ok && lane == 0) *abort_s = 1;
+        };
+        for (int j = 0; j < nt; ++j) {
+            uint32_t v[64];
+            float mh = -INFINITY;
+            const int kvalid = L - j * BKV - half * 64;  // keys of this half below the sequence's key length
+            wait_u(s_full + (j & 1), (j >> 1) & 1);
+            if (ok) {
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t sb = lane_base + (uint32_t)((j & 1) * 128) + cbase;
+                tm_ld32_nw(sb, v);
+                tm_ld32_nw(sb + 32, v + 32);
+                tm_wait_ld();
+                if (kvalid < 64) {
 #pragma unroll
-                for (int x = 0; x < 128; ++x)
-                    if (x >= kvalid) v[x] = 0xFF800000u;  // -inf
+                    for (int x = 0; x < 64; ++x)
+                        if (x >= kvalid) v[x] = 0xFF800000u;  // -inf
+                }
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int x = 0; x < 64; ++x) m4[x & 3] = fmaxf(m4[x & 3], __uint_as_float(v[x]));
+                mh = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             }
-            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int x = 0; x < 128; ++x) m4[x & 3] = fmaxf(m4[x & 3], __uint_as_float(v[x]));
-            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sc;
+            // row max over both halves (a half may be fully masked: -inf)
+            float* pmj = pm + (j & 1) * 2 * ROWS;
+            pmj[half * ROWS + r] = mh;
+            asm volatile("bar.sync %0, 64;" ::"r"(1 + qd) : "memory");
+            const float mx = fmaxf(pmj[r], pmj[ROWS + r]) * sc;
+            if (!ok) continue;
             float alpha = 1.f;
             const bool move = mx > m_used + 8.f;
             if (move) {
@@ -890,25 +929,29 @@ __global__ void __launch_bounds__(at::NT, 1)
                 m_used = mx;
             }
             // P buffer j & 1 was read by P V of tile j - 2
-            if (j >= 2 && !tc_wait(o_done + (j & 1), ((j - 2) >> 1) & 1, abort_s)) { ok = false; break; }
-            if (move && j >= 1) {  // rescale O once P V of tile j - 1 is in it
-                if (!tc_wait(o_done + ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_s)) { ok = false; break; }
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t o[32];
-                    tm_ld32_nw(lane_base + 256 + ch * 32, o);
-                    tm_wait_ld();
+            if (j >= 2) wait_u(o_done + (j & 1), ((j - 2) >> 1) & 1);
+            if (ok && move && j >= 1) {  // rescale this half of O once P V of tile j - 1 is in it
+                wait_u(o_done + ((j - 1) & 1), ((j - 1) >> 1) & 1);
+                if (ok) {
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    for (int ch = 0; ch < 2; ++ch) {
+                        uint32_t o[32];
+                        tm_ld32_nw(lane_base + 256 + cbase + ch * 32, o);
+                        tm_wait_ld();
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-                    tm_st32(lane_base + 256 + ch * 32, o);
+                        for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+                        tm_st32(lane_base + 256 + cbase + ch * 32, o);
+                    }
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
+            if (!ok) continue;
             l *= alpha;
             float l4[4] = {0.f, 0.f, 0.f, 0.f};
-            unsigned char* pbase = smem + P_OFF + (j & 1) * 2 * CHUNK;
+            // this half's keys are key chunk `half` of the P buffer (64 keys = one 128-byte row)
+            unsigned char* prow = smem + P_OFF + (j & 1) * 2 * CHUNK + half * CHUNK;
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
+            for (int ch = 0; ch < 2; ++ch) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int x = 0; x < 32; x += 2) {
@@ -918,11 +961,9 @@ __global__ void __launch_bounds__(at::NT, 1)
                     __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
                     pk[x >> 1] = *reinterpret_cast<uint32_t*>(&h2);
                 }
-                // keys ch*32 .. ch*32+31: key chunk ch >> 1, pieces (ch & 1) * 4 .. + 3 of row r
-                unsigned char* prow = pbase + (ch >> 1) * CHUNK;
 #pragma unroll
                 for (int pp = 0; pp < 4; ++pp)
-                    *reinterpret_cast<uint4*>(prow + sw128_off(r, (ch & 1) * 4 + pp)) =
+                    *reinterpret_cast<uint4*>(prow + sw128_off(r, ch * 4 + pp)) =
                         make_uint4(pk[4 * pp], pk[4 * pp + 1], pk[4 * pp + 2], pk[4 * pp + 3]);
             }
             l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
@@ -931,16 +972,23 @@ __global__ void __launch_bounds__(at::NT, 1)
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(s_addr(p_full + (j & 1))) : "memory");
         }
-        if (ok && nt > 0 && tc_wait(o_done + ((nt - 1) & 1), ((nt - 1) >> 1) & 1, abort_s)) {
+        // row sum over both halves (through the max buffer of parity nt & 1, free once both passed tile nt - 1)
+        float* ls = pm + (nt & 1) * 2 * ROWS;
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + qd) : "memory");  // both halves done with every max buffer read
+        ls[half * ROWS + r] = ok ? l : 0.f;
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + qd) : "memory");
+        l = ls[r] + ls[ROWS + r];
+        if (nt > 0) wait_u(o_done + ((nt - 1) & 1), ((nt - 1) >> 1) & 1);
+        if (ok && nt > 0) {
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const int sq = qt * BQ + (r & 63), head = 2 * g + (r >> 6);
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            for (int ch = 0; ch < 4; ++ch) {
+            for (int ch = 0; ch < 2; ++ch) {
                 uint32_t o[32];
-                tm_ld32_nw(lane_base + 256 + ch * 32, o);
+                tm_ld32_nw(lane_base + 256 + cbase + ch * 32, o);
                 tm_wait_ld();
                 if (sq < S) {
-                    bf16* dst = out + (((size_t)b * S + sq) * NQ + head) * HD + ch * 32;
+                    bf16* dst = out + (((size_t)b * S + sq) * NQ + head) * HD + cbase + ch * 32;
 #pragma unroll
                     for (int x = 0; x < 32; x += 8) {
                         uint32_t w[4];
@@ -954,7 +1002,7 @@ __global__ void __launch_bounds__(at::NT, 1)
                     }
                 }
             }
-        } else if (lane == 0 && qd == 0) {
+        } else if (lane == 0) {
             set_err(err, ERR_TIMEOUT);
             *abort_s = 1;
         }

@@ -56,6 +56,7 @@ struct MegaArgs {
     unsigned int* done;        // CTAs finished with the head (last one publishes the argmax)
     unsigned long long timeout_ns;  // bound of every wait (exchange polls, ring slots)
     int debug_stall;           // test hook: CTA 0 withholds one exchange, so every wait runs out
+    int l2_prefetch;           // producer prefetches its next-layer weight rows into L2
 };
 
 // Launch one decode step on `grid` CTAs (cooperative: all co-resident or an error).
