@@ -18,9 +18,12 @@ Sources (page title, section):
   * "rightkit-qts 0.2.0" (docs.rs) — Mode API (Code Predictor config fields,
     identity input projection for 0.6B, talker-wide embeddings), Synthetic
     tests (cached / recompute equivalence).
+  * "omnivoice-cpp docs/ARCHITECTURE.md", MaskGIT decoder — the greedy token
+    update of one refinement step (maskgit_update.py).
 
 Every function computes its plain definition in float64; matrix products use
 numpy's ``@``. No blocking, fusion or reordering beyond the definitions.
 """
 from .backbone import *  # noqa: F401,F403
 from .loops import *  # noqa: F401,F403
+from .maskgit_update import *  # noqa: F401,F403
