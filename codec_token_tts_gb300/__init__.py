@@ -79,6 +79,8 @@ def _load() -> C.CDLL:
         "tts_bb_profile_report": (C.c_char_p, [P]),
         "tts_bb_gqa_decode_attention_static": (I, [P, P, P, I, P, I, I, P, P]),
         "tts_bb_debug_fault": (I, [P, I, C.c_int64]),
+        "tts_bb_maskgit_update": (I, [P, I, I, P, I, I, I, P, I, I, I, I, C.c_float, C.c_float]),
+        "tts_bb_maskgit_schedule": (I, [I, I, C.c_double, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -92,7 +94,8 @@ EXPORTED = ("tts_bb_default_config", "tts_bb_create", "tts_bb_free", "tts_bb_pre
             "tts_bb_maskgit_pass", "tts_bb_release", "tts_bb_truncate", "tts_bb_slot_len", "tts_bb_sync",
             "tts_bb_last_error", "tts_bb_version", "tts_bb_debug_kv_read", "tts_bb_debug_kv_write",
             "tts_bb_launch_count", "tts_bb_profile", "tts_bb_profile_report",
-            "tts_bb_gqa_decode_attention_static", "tts_bb_debug_fault")
+            "tts_bb_gqa_decode_attention_static", "tts_bb_debug_fault", "tts_bb_maskgit_update",
+            "tts_bb_maskgit_schedule")
 
 
 def _ptr(x) -> Optional[int]:
@@ -198,6 +201,22 @@ def tts_bb_maskgit_pass(h, B: int, S: int, ids, audio_mask, key_lens=None, audio
     st = lib.tts_bb_maskgit_pass(h, B, S, _ptr(ids), _ptr(audio_mask), _ptr(kl), audio_start, _ptr(logits_out),
                                  _opts(None, hidden_out, 0))
     return _check(h, st) if check else st
+
+
+def tts_bb_maskgit_update(h, n_items: int, T: int, logits, S_logits: int, cond_pos0: int, uncond_pos0: int, ids,
+                          S_ids: int, cond_ids_pos0: int, uncond_ids_pos0: int, n_unmask: int,
+                          cfg_scale: float = 2.0, layer_penalty: float = 5.0, check: bool = True) -> int:
+    st = lib.tts_bb_maskgit_update(h, n_items, T, _ptr(logits), S_logits, cond_pos0, uncond_pos0, _ptr(ids), S_ids,
+                                   cond_ids_pos0, uncond_ids_pos0, n_unmask, cfg_scale, layer_penalty)
+    return _check(h, st) if check else st
+
+
+def tts_bb_maskgit_schedule(num_step: int, n_total: int, t_shift: float = 0.1) -> np.ndarray:
+    out = np.zeros(num_step, np.int32)
+    st = lib.tts_bb_maskgit_schedule(num_step, n_total, t_shift, _ptr(out))
+    if st != OK:
+        raise TtsBbError(st, "tts_bb_maskgit_schedule: bad arguments")
+    return out
 
 
 def tts_bb_release(h, slot: int, check: bool = True) -> int:

@@ -152,6 +152,12 @@ int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi&
 int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N, int K, const Epi& e, int* err,
                     cudaStream_t st);
 bool gemm_tc_available();
+// MaskGIT greedy update (k_maskgit.cu): two launches
+int launch_maskgit_update(const float* logits, int n_items, int K, int T, int V, int S_log, int cond_pos0,
+                          int uncond_pos0, int32_t* ids, int S_ids, int cond_ids_pos0, int uncond_ids_pos0,
+                          int mask_id, float cfg, float penalty, int n_unmask, unsigned long long* keys, int32_t* pred,
+                          cudaStream_t st);
+int mg_max_vocab();
 int launch_attn_bidir_tc(const bf16* q, const bf16* pool, size_t pool_blocks, int bps, const int32_t* key_len, int B,
                          int S, bf16* out, int* err, cudaStream_t st);
 

@@ -174,6 +174,9 @@ struct tts_bb {
     int32_t *seq_slot = nullptr, *seq_start = nullptr, *seq_len = nullptr, *key_len = nullptr;
     bf16* mg_pool = nullptr;
     bool attn_bidir_tc = false;
+    unsigned long long* mg_keys = nullptr;  // MaskGIT update scratch: a key and a prediction per cell
+    int32_t* mg_pred = nullptr;
+    size_t mg_cells = 0;
     int l2_prefetch = 1;         // persistent step: next-layer weight rows prefetched into L2  // bidirectional attention on tcgen05 (else the mma.sync flash kernel)
     size_t mg_pool_blocks = 0;
     int* err = nullptr;
@@ -315,10 +318,10 @@ tts_bb_status finish(tts_bb* h) {
 }
 
 enum Kind { K_SETUP, K_EMBED, K_RMSNORM, K_GEMV, K_GEMM, K_QKROPE, K_ATTN_DECODE, K_ATTN_PREFILL, K_ARGMAX,
-            K_KVCOPY, K_MEGA, K_GEMM_TC, K_GEMM_TCD, K_ATTN_BIDIR_TC, K_NKINDS };
+            K_KVCOPY, K_MEGA, K_GEMM_TC, K_GEMM_TCD, K_ATTN_BIDIR_TC, K_MG_UPDATE, K_NKINDS };
 const char* kind_name[K_NKINDS] = {"setup", "embed_gather", "rmsnorm", "gemv", "gemm_mma_split", "qk_norm_rope_append",
                                    "attn_decode", "attn_prefill", "argmax", "kv_copy", "decode_step_persistent",
-                                   "gemm_tcgen05", "gemm_tcgen05_decode", "attn_bidir_tcgen05"};
+                                   "gemm_tcgen05", "gemm_tcgen05_decode", "attn_bidir_tcgen05", "maskgit_update"};
 
 cudaEvent_t prof_event(tts_bb* h) {
     if (!h->ev_pool.empty()) {
@@ -1177,6 +1180,56 @@ TTS_API tts_bb_status tts_bb_maskgit_pass(tts_bb* h, int B, int S, const int32_t
         L += launch_gemm(h->y, h->heads[0], B * Sa, N, HID, e, h->st, nullptr, h->err);
     }
     return finish(h);
+}
+
+TTS_API tts_bb_status tts_bb_maskgit_update(tts_bb* h, int n_items, int T, const float* logits, int S_logits,
+                                            int cond_pos0, int uncond_pos0, int32_t* ids, int S_ids,
+                                            int cond_ids_pos0, int uncond_ids_pos0, int n_unmask, float cfg_scale,
+                                            float layer_penalty) {
+    if (!h) return TTS_BB_E_INVALID;
+    const tts_bb_config& c = h->cfg;
+    if (c.n_heads <= 0 || c.head_rows < 2 || c.head_rows > mg_max_vocab())
+        return fail(h, TTS_BB_E_INVALID, "maskgit_update needs audio heads of 2..%d ids", mg_max_vocab());
+    if (n_items < 1 || T < 1 || n_unmask < 0 || !logits || !ids)
+        return fail(h, TTS_BB_E_INVALID, "maskgit_update: bad sizes or NULL buffers");
+    if (cond_pos0 < 0 || uncond_pos0 < 0 || cond_pos0 + T > S_logits || uncond_pos0 + T > S_logits)
+        return fail(h, TTS_BB_E_INVALID, "maskgit_update: logits windows outside S_logits=%d", S_logits);
+    if (cond_ids_pos0 < 0 || uncond_ids_pos0 < 0 || cond_ids_pos0 + T > S_ids || uncond_ids_pos0 + T > S_ids)
+        return fail(h, TTS_BB_E_INVALID, "maskgit_update: id windows outside S_ids=%d", S_ids);
+    const size_t cells = (size_t)n_items * c.n_heads * T;
+    if (cells > (size_t)INT32_MAX / 2) return fail(h, TTS_BB_E_INVALID, "maskgit_update: too many cells");
+    if (cells > h->mg_cells) {
+        cudaStreamSynchronize(h->st);
+        for (void* p : {(void*)h->mg_keys, (void*)h->mg_pred})
+            if (p) {
+                cudaFree(p);
+                h->allocs.erase(std::remove(h->allocs.begin(), h->allocs.end(), p), h->allocs.end());
+            }
+        h->mg_keys = nullptr;
+        h->mg_pred = nullptr;
+        h->mg_cells = 0;
+        cudaError_t e = dalloc(h, &h->mg_keys, cells);
+        if (e == cudaSuccess) e = dalloc(h, &h->mg_pred, cells);
+        if (e != cudaSuccess) return cuda_fail(h, e, "MaskGIT update scratch");
+        h->mg_cells = cells;
+    }
+    {
+        Launch L(h, K_MG_UPDATE, (double)cells * 2.0 * c.head_rows * 4.0);
+        L += launch_maskgit_update(logits, n_items, c.n_heads, T, c.head_rows, S_logits, cond_pos0, uncond_pos0, ids,
+                                   S_ids, cond_ids_pos0, uncond_ids_pos0, c.head_rows - 1, cfg_scale, layer_penalty,
+                                   n_unmask, h->mg_keys, h->mg_pred, h->st);
+    }
+    return finish(h);
+}
+
+TTS_API tts_bb_status tts_bb_maskgit_schedule(int num_step, int n_total, double t_shift, int32_t* counts) {
+    if (num_step < 1 || n_total < 0 || !(t_shift > 0.0) || !counts) return TTS_BB_E_INVALID;
+    auto tp = [&](int i) {
+        const double t = (double)i / (double)num_step;
+        return t_shift * t / (t_shift * t + (1.0 - t));
+    };
+    for (int i = 0; i < num_step; ++i) counts[i] = (int32_t)std::ceil((double)n_total * (tp(i + 1) - tp(i)));
+    return TTS_BB_OK;
 }
 
 TTS_API tts_bb_status tts_bb_debug_kv_read(tts_bb* h, int layer, int slot, int pos0, int n, void* k_out, void* v_out) {

@@ -1,0 +1,187 @@
+// MaskGIT greedy update of one refinement step, on the device ("omnivoice-cpp
+// docs/ARCHITECTURE.md", MaskGIT decoder; class and position temperatures 0).
+//
+// k_mg_score — one warp per target cell (item i, codebook k, position t):
+//   z = c + s (c - u) over the audio vocabulary (float32, one rounding per
+//   operation: no fused multiply-add, so the argmax is reproducible), its
+//   log-sum-exp, pred = argmax over the ids other than the mask id (lowest
+//   id on ties), score = z[pred] - lse - k * penalty. A cell whose current
+//   id is not the mask id gets key 0 (never taken); a masked cell gets the
+//   unique key (order(score) << 32) | (2^32 - 1 - flat), flat = k T + t, so
+//   a larger key is a higher score, then a lower flat index.
+// k_mg_select — one CTA per item: the n = min(n_unmask, masked cells)
+//   largest keys are found by a most-significant-digit radix select (8 bits
+//   per pass, counts in shared memory) and their cells take pred in both the
+//   conditional and the unconditional id rows.
+#include "common.cuh"
+
+namespace ttsbb {
+
+namespace mg {
+constexpr int MAXV_LANE = 33;  // vocabulary up to 32 * 33 = 1056 ids
+constexpr int SELECT_NT = 1024;
+}  // namespace mg
+
+__device__ __forceinline__ unsigned long long mg_key(float score, int flat) {
+    if (!(score == score)) return 0ull;  // NaN: never taken
+    const uint32_t b = __float_as_uint(score);
+    const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)flat);
+}
+
+// grid ceil(n_items K T / 8), 256 threads
+__global__ void __launch_bounds__(256) k_mg_score(const float* __restrict__ logits, int n_items, int K, int T, int V,
+                                                  int S_log, int cond_pos0, int uncond_pos0,
+                                                  const int32_t* __restrict__ ids, int S_ids, int cond_ids_pos0,
+                                                  int mask_id, float cfg, float penalty,
+                                                  unsigned long long* __restrict__ keys, int32_t* __restrict__ pred) {
+    pdl_wait();  // the logits come from the pass
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long cell = (long)blockIdx.x * 8 + warp;
+    const long KT = (long)K * T;
+    if (cell >= (long)n_items * KT) return;
+    const int i = (int)(cell / KT), r = (int)(cell % KT), k = r / T, t = r % T;
+    const float* c = logits + (((size_t)i * K + k) * S_log + cond_pos0 + t) * V;
+    const float* u = logits + (((size_t)(n_items + i) * K + k) * S_log + uncond_pos0 + t) * V;
+    float z[mg::MAXV_LANE];
+    float mx = -INFINITY, best = -INFINITY;
+    int bi = 0x7FFFFFFF;
+#pragma unroll
+    for (int j = 0; j < mg::MAXV_LANE; ++j) {
+        const int v = lane + 32 * j;
+        z[j] = -INFINITY;
+        if (v < V) {
+            const float cv = __ldg(c + v), uv = __ldg(u + v);
+            z[j] = __fadd_rn(cv, __fmul_rn(cfg, __fsub_rn(cv, uv)));
+            mx = fmaxf(mx, z[j]);
+            if (v != mask_id && (z[j] > best || bi == 0x7FFFFFFF)) {  // v grows with j: the first max stays
+                best = z[j];
+                bi = v;
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ob > best || (ob == best && oi < bi)) {
+            best = ob;
+            bi = oi;
+        }
+    }
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < mg::MAXV_LANE; ++j)
+        if (lane + 32 * j < V) sum += expf(z[j] - mx);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) {
+        const float lse = mx + logf(sum);
+        const float score = (best - lse) - (float)k * penalty;
+        const int cur = ids[((size_t)i * K + k) * S_ids + cond_ids_pos0 + t];
+        keys[cell] = cur == mask_id ? mg_key(score, r) : 0ull;
+        pred[cell] = bi;
+    }
+}
+
+// grid n_items, 1024 threads
+__global__ void __launch_bounds__(mg::SELECT_NT) k_mg_select(const unsigned long long* __restrict__ keys,
+                                                             const int32_t* __restrict__ pred, int n_items, int K,
+                                                             int T, int n_unmask, int32_t* __restrict__ ids, int S_ids,
+                                                             int cond_ids_pos0, int uncond_ids_pos0) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ int hist[256];
+    __shared__ int s_cnt[mg::SELECT_NT / 32];
+    __shared__ int s_sel, s_rem;
+    const int i = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int KT = K * T;
+    const unsigned long long* kp = keys + (size_t)i * KT;
+    // masked cells of this item
+    int cnt = 0;
+    for (int j = tid; j < KT; j += mg::SELECT_NT) cnt += kp[j] != 0ull;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (lane == 0) s_cnt[warp] = cnt;
+    __syncthreads();
+    if (tid == 0) {
+        int tot = 0;
+        for (int w = 0; w < mg::SELECT_NT / 32; ++w) tot += s_cnt[w];
+        s_rem = min(n_unmask, tot);
+    }
+    __syncthreads();
+    int rem = s_rem;
+    if (rem <= 0) return;
+    unsigned long long prefix = 0ull, pmask = 0ull;
+    for (int sh = 56; sh >= 0; sh -= 8) {
+        if (tid < 256) hist[tid] = 0;
+        __syncthreads();
+        for (int j = tid; j < KT; j += mg::SELECT_NT) {
+            const unsigned long long key = kp[j];
+            if (key != 0ull && (key & pmask) == prefix) atomicAdd(&hist[(int)((key >> sh) & 255ull)], 1);
+        }
+        __syncthreads();
+        if (warp == 0) {  // lane l holds digits 255 - 8l .. 248 - 8l (descending)
+            int cq[8], tot = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                cq[q] = hist[255 - 8 * lane - q];
+                tot += cq[q];
+            }
+            int incl = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const int excl = incl - tot;
+            const unsigned bal = __ballot_sync(0xffffffffu, excl < rem && rem <= incl);
+            if (lane == __ffs(bal) - 1) {
+                int cum = excl;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (cum + cq[q] >= rem) {
+                        s_sel = 255 - 8 * lane - q;
+                        s_rem = rem - cum;
+                        break;
+                    }
+                    cum += cq[q];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= (unsigned long long)s_sel << sh;
+        pmask |= 255ull << sh;
+        rem = s_rem;
+        __syncthreads();
+    }
+    // keys are unique: exactly the n largest are >= the n-th largest (prefix)
+    const int32_t* pp = pred + (size_t)i * KT;
+    for (int j = tid; j < KT; j += mg::SELECT_NT) {
+        const unsigned long long key = kp[j];
+        if (key != 0ull && key >= prefix) {
+            const int k = j / T, t = j - k * T, p = pp[j];
+            ids[((size_t)i * K + k) * S_ids + cond_ids_pos0 + t] = p;
+            ids[((size_t)(n_items + i) * K + k) * S_ids + uncond_ids_pos0 + t] = p;
+        }
+    }
+}
+
+int mg_max_vocab() { return 32 * mg::MAXV_LANE; }
+
+int launch_maskgit_update(const float* logits, int n_items, int K, int T, int V, int S_log, int cond_pos0,
+                          int uncond_pos0, int32_t* ids, int S_ids, int cond_ids_pos0, int uncond_ids_pos0,
+                          int mask_id, float cfg, float penalty, int n_unmask, unsigned long long* keys, int32_t* pred,
+                          cudaStream_t st) {
+    const long cells = (long)n_items * K * T;
+    if (cells <= 0) return 0;
+    launch_pdl(k_mg_score, (unsigned)((cells + 7) / 8), 256, 0, st, logits, n_items, K, T, V, S_log, cond_pos0,
+               uncond_pos0, (const int32_t*)ids, S_ids, cond_ids_pos0, mask_id, cfg, penalty, keys, pred);
+    launch_pdl(k_mg_select, n_items, mg::SELECT_NT, 0, st, (const unsigned long long*)keys, (const int32_t*)pred,
+               n_items, K, T, n_unmask, ids, S_ids, cond_ids_pos0, uncond_ids_pos0);
+    return 2;
+}
+
+}  // namespace ttsbb

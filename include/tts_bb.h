@@ -203,6 +203,44 @@ tts_bb_status tts_bb_maskgit_pass(tts_bb* h, int B, int S, const int32_t* ids,
                                   const uint8_t* audio_mask, const int32_t* key_lens,
                                   int audio_start, float* logits_out, const tts_bb_opts* opts);
 
+/* Greedy token update of one MaskGIT refinement step on the device
+ * (omnivoice-cpp, MaskGIT decoder, class and position temperatures 0). The
+ * batch of a pass holds n_items conditional rows (0..n_items-1) followed by
+ * their n_items unconditional rows (n_items..2 n_items-1). For every target
+ * cell (item i, codebook k < n_heads, position t < T):
+ *   z     = c + cfg_scale (c - u), float32, c the conditional and u the
+ *           unconditional logits of the cell (one rounding per operation)
+ *   pred  = argmax of z over the ids other than the mask id (head_rows - 1),
+ *           lowest id on ties
+ *   score = z[pred] - logsumexp(z over all head_rows ids) - k layer_penalty
+ * Cells whose current id (conditional row) is not the mask id are kept. Of
+ * the masked cells of each item, the min(n_unmask, masked) with the highest
+ * score (ties: lowest k T + t) take pred, written to the conditional and the
+ * unconditional rows.
+ *   logits  device fp32 [2 n_items][n_heads][S_logits][head_rows] (the
+ *           maskgit_pass output); the cell's logits sit at position
+ *           cond_pos0 + t (conditional rows) and uncond_pos0 + t
+ *           (unconditional rows)
+ *   ids     device int32 [2 n_items][n_heads][S_ids], updated in place at
+ *           positions cond_ids_pos0 + t and uncond_ids_pos0 + t
+ *   cfg_scale 2.0 and layer_penalty 5.0 on the page.
+ * Two kernel launches on the handle's stream; the scratch (12 bytes per cell)
+ * is allocated on the first call that needs more. TTS_BB_E_INVALID for
+ * windows outside their tensors, n_items < 1, T < 1, n_unmask < 0 or a
+ * handle without audio heads (or with more than 1056 ids per head). */
+tts_bb_status tts_bb_maskgit_update(tts_bb* h, int n_items, int T, const float* logits, int S_logits,
+                                    int cond_pos0, int uncond_pos0, int32_t* ids, int S_ids,
+                                    int cond_ids_pos0, int uncond_ids_pos0, int n_unmask,
+                                    float cfg_scale, float layer_penalty);
+
+/* Cells newly unmasked at each of num_step MaskGIT steps, host only:
+ * counts[i] = ceil(n_total (t'[i+1] - t'[i])) with t[i] = i / num_step
+ * shifted by t' = s t / (s t + (1 - t)), s = t_shift (0.1 on the page, whose
+ * time-step function is not printed: this shift is a reading). The counts sum
+ * to at least n_total. TTS_BB_E_INVALID for num_step < 1, n_total < 0,
+ * t_shift <= 0 or a NULL counts. */
+tts_bb_status tts_bb_maskgit_schedule(int num_step, int n_total, double t_shift, int32_t* counts);
+
 /* Return the slot's KV blocks to the pool; its length becomes 0. */
 tts_bb_status tts_bb_release(tts_bb* h, int slot);
 

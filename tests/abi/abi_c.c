@@ -51,6 +51,16 @@ int main(void) {
     EXPECT(tts_bb_gqa_decode_attention_static(NULL, NULL, NULL, 1, NULL, 1, 0, NULL, NULL) == TTS_BB_E_INVALID);
     EXPECT(tts_bb_gqa_decode_attention_static(k, k, slots, 1, slots, TTS_BB_STATIC_ATTN_MAX_B + 1, 0, v, NULL) ==
            TTS_BB_E_INVALID);
+    EXPECT(tts_bb_maskgit_update(NULL, 1, 1, NULL, 1, 0, 0, NULL, 1, 0, 0, 1, 2.0f, 5.0f) == TTS_BB_E_INVALID);
+    {
+        int32_t counts[32];
+        int32_t sum = 0;
+        int i;
+        EXPECT(tts_bb_maskgit_schedule(32, 6144, 0.1, counts) == TTS_BB_OK);
+        for (i = 0; i < 32; ++i) sum += counts[i];
+        EXPECT(sum >= 6144 && sum < 6144 + 32 && counts[0] < counts[31]);
+        EXPECT(tts_bb_maskgit_schedule(0, 10, 0.1, counts) == TTS_BB_E_INVALID);
+    }
     tts_bb_free(NULL);
     printf("abi_c: ok\n");
     return 0;

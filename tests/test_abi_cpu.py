@@ -65,3 +65,21 @@ def test_c99_consumer_compiles_and_runs(tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, env=env)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "abi_c: ok" in r.stdout
+
+
+def test_maskgit_schedule_matches_oracle():
+    """Host-only schedule of the library against the oracle's (same reading of
+    the shifted time steps); bad arguments are rejected."""
+    import numpy as np
+
+    import oracle as O
+    _lib()
+    import codec_token_tts_gb300 as m
+    for n_step, n_total, s in ((32, 6144, 0.1), (8, 100, 0.1), (1, 5, 0.1), (16, 2800, 0.1), (10, 1000, 1.0),
+                               (7, 0, 0.3)):
+        got = m.tts_bb_maskgit_schedule(n_step, n_total, s)
+        assert np.array_equal(got, O.maskgit_schedule(n_step, n_total, s)), (n_step, n_total, s)
+    buf = np.zeros(4, np.int32)
+    for args in ((0, 10, 0.1), (4, -1, 0.1), (4, 10, 0.0)):
+        assert m.lib.tts_bb_maskgit_schedule(*args, buf.ctypes.data) == m.E_INVALID
+    assert m.lib.tts_bb_maskgit_schedule(4, 10, 0.1, None) == m.E_INVALID

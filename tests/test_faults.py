@@ -32,6 +32,7 @@ def test_null_handle_is_rejected_everywhere():
     assert L.tts_bb_profile(None, 1) == m.E_INVALID
     assert L.tts_bb_debug_fault(None, m.DEBUG_STALL_NEXT_STEP, 0) == m.E_INVALID
     assert L.tts_bb_debug_kv_read(None, 0, 0, 0, 1, None, None) == m.E_INVALID
+    assert L.tts_bb_maskgit_update(None, 1, 1, buf, 1, 0, 0, buf, 1, 0, 0, 1, 2.0, 5.0) == m.E_INVALID
     assert L.tts_bb_launch_count(None) == 0
     L.tts_bb_free(None)  # no-op
 
