@@ -392,6 +392,7 @@ def run_maskgit(steps, warmup):
     run(2)
     rep = m.tts_bb_profile_report(h)
     m.tts_bb_profile(h, False)
+    refine = run_maskgit_refinement(m, h, seed, stream)
     m.tts_bb_free(h)
     flops = 2 * 8192 * 15_728_640 * 28 + 4 * 8 * 16 * 1024 ** 2 * 128 * 28 + 2 * 8 * 768 * 8200 * 1024
     pk = peaks()[0]
@@ -400,7 +401,65 @@ def run_maskgit(steps, warmup):
             "value": 1e3 / ms, "unit": "passes/s", "ms_per_pass": ms, "steps": steps, "status": st,
             "tflops": flops / (ms / 1e3) / 1e12, "flop_per_pass": flops,
             "tensor_frac_of_measured_sustained": flops / (ms / 1e3) / 1e12 / pk["bf16_tflops_sustained"],
-            "roofline": roofline_from_profile(rep), "kernel_profile": rep}
+            "roofline": roofline_from_profile(rep), "refinement": refine, "kernel_profile": rep}
+
+
+def run_maskgit_refinement(m, h, seed, stream, n_step=32):
+    """32 greedy refinement steps (pass + device update) of 4 items with CFG: rows 0-3 hold the
+    conditional prompts (256 text + 768 masked target frames), rows 4-7 the unconditional ones
+    (the 768 target frames alone, left-aligned, key_lens 768). Logits over all 1024 positions;
+    the update reads positions 256.. of the conditional rows and 0.. of the unconditional ones."""
+    import torch
+    from tests.gpu_util import dev_i32, dev_u8
+    n_items, S, n_text, V = 4, 1024, 256, 1025
+    T = S - n_text
+    ids0, mask0 = synth.maskgit_inputs(seed, 99)
+    ids0, mask0 = ids0.copy(), mask0.copy()
+    for i in range(n_items):
+        ids0[i, :, n_text:] = 1024
+        ids0[n_items + i, :, :T] = 1024
+        ids0[n_items + i, :, T:] = 0
+        mask0[n_items + i, :T] = 1
+        mask0[n_items + i, T:] = 0
+    key_lens = [S] * n_items + [T] * n_items
+    counts = [int(c) for c in m.tts_bb_maskgit_schedule(n_step, 8 * T, 0.1)]
+    init = dev_i32(ids0)
+    ids_d = init.clone()
+    mask_d = dev_u8(mask0)
+    logits = torch.zeros(2 * n_items, 8, S, V, dtype=torch.float32, device="cuda")
+
+    def refine():
+        ids_d.copy_(init)
+        for n in counts:
+            m.tts_bb_maskgit_pass(h, 2 * n_items, S, ids_d, mask_d, key_lens, 0, logits, check=False)
+            m.tts_bb_maskgit_update(h, n_items, T, logits, S, n_text, 0, ids_d, S, n_text, 0, n, check=False)
+
+    refine()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    refine()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    done = not bool((ids_d[:n_items, :, n_text:] == 1024).any().item())
+    m.tts_bb_profile(h, True)
+    refine()
+    rep = m.tts_bb_profile_report(h)
+    m.tts_bb_profile(h, False)
+    upd = [k for k in rep["kernels"] if k["kind"] == "maskgit_update"]
+    out = {"workload": f"{n_step}-step greedy MaskGIT refinement, 4 items x (cond + uncond) = 8 rows x 1024, "
+                       f"768 x 8 target cells per item, schedule shift 0.1",
+           "ms_per_refinement": ms, "ms_per_step": ms / n_step, "all_cells_unmasked": done}
+    if upd:
+        u = upd[0]
+        per = u["ms"] / n_step * 1e3
+        gbs = u["bytes"] / (u["ms"] / 1e3) / 1e9
+        out["update_us_per_step"] = per
+        out["update_roofline"] = {"kernel": "maskgit_update", "bound": "hbm", "achieved": gbs,
+                                  "peak": peaks()[0]["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks()[0]["hbm_gbs"],
+                                  "bytes_per_step": u["bytes"] / n_step}
+    return out
 
 
 def run_code_predictor(steps, warmup):

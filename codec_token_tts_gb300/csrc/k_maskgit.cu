@@ -44,22 +44,24 @@ __global__ void __launch_bounds__(256) k_mg_score(const float* __restrict__ logi
     const int i = (int)(cell / KT), r = (int)(cell % KT), k = r / T, t = r % T;
     const float* c = logits + (((size_t)i * K + k) * S_log + cond_pos0 + t) * V;
     const float* u = logits + (((size_t)(n_items + i) * K + k) * S_log + uncond_pos0 + t) * V;
-    float z[mg::MAXV_LANE];
+    // every load of the lane first (predicated, no branch between them), then the arithmetic
+    float z[mg::MAXV_LANE], uu[mg::MAXV_LANE];
+#pragma unroll
+    for (int j = 0; j < mg::MAXV_LANE; ++j) {
+        const int v = lane + 32 * j;
+        z[j] = v < V ? __ldg(c + v) : 0.f;
+        uu[j] = v < V ? __ldg(u + v) : 0.f;
+    }
     float mx = -INFINITY, best = -INFINITY;
     int bi = 0x7FFFFFFF;
 #pragma unroll
     for (int j = 0; j < mg::MAXV_LANE; ++j) {
         const int v = lane + 32 * j;
-        z[j] = -INFINITY;
-        if (v < V) {
-            const float cv = __ldg(c + v), uv = __ldg(u + v);
-            z[j] = __fadd_rn(cv, __fmul_rn(cfg, __fsub_rn(cv, uv)));
-            mx = fmaxf(mx, z[j]);
-            if (v != mask_id && (z[j] > best || bi == 0x7FFFFFFF)) {  // v grows with j: the first max stays
-                best = z[j];
-                bi = v;
-            }
-        }
+        z[j] = v < V ? __fadd_rn(z[j], __fmul_rn(cfg, __fsub_rn(z[j], uu[j]))) : -INFINITY;
+        mx = fmaxf(mx, z[j]);
+        const bool better = v < V && v != mask_id && (z[j] > best || bi == 0x7FFFFFFF);  // v grows with j
+        best = better ? z[j] : best;
+        bi = better ? v : bi;
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
@@ -118,9 +120,17 @@ __global__ void __launch_bounds__(mg::SELECT_NT) k_mg_select(const unsigned long
     for (int sh = 56; sh >= 0; sh -= 8) {
         if (tid < 256) hist[tid] = 0;
         __syncthreads();
-        for (int j = tid; j < KT; j += mg::SELECT_NT) {
-            const unsigned long long key = kp[j];
-            if (key != 0ull && (key & pmask) == prefix) atomicAdd(&hist[(int)((key >> sh) & 255ull)], 1);
+        // early digits are shared by most keys (scores of similar size): lanes with the same digit add
+        // once per warp, so a bin takes one shared-memory atomic per warp instead of one per key
+        for (int j0 = 0; j0 < KT; j0 += mg::SELECT_NT) {
+            const int j = j0 + tid;
+            int bin = -1;
+            if (j < KT) {
+                const unsigned long long key = kp[j];
+                if (key != 0ull && (key & pmask) == prefix) bin = (int)((key >> sh) & 255ull);
+            }
+            const unsigned same = __match_any_sync(0xffffffffu, bin);
+            if (bin >= 0 && lane == __ffs(same) - 1) atomicAdd(&hist[bin], __popc(same));
         }
         __syncthreads();
         if (warp == 0) {  // lane l holds digits 255 - 8l .. 248 - 8l (descending)
