@@ -9,6 +9,9 @@ Test infrastructure only. These follow the generation protocols on the pages:
     identity input projection for 0.6B, talker-wide embeddings).
   * MaskGIT full bidirectional pass (omnivoice-cpp ARCHITECTURE.md, MaskGIT
     decoder and Component architecture).
+  * The Talker -> Code Predictor frame loop (Qwen3-TTS ncnn port, model
+    structure: 16 codes per frame, their embeddings summed into the next
+    Talker input).
 
 All drivers support teacher forcing: pass the id stream to replay and the
 driver uses it instead of its own argmax, so a GPU run and the oracle see
@@ -23,7 +26,7 @@ import numpy as np
 from .backbone import Backbone, KVCache, argmax_first, codebook_embed_sum, omnivoice_embed
 
 __all__ = ["talker_prefill", "talker_decode_steps", "code_predictor_frame", "code_predictor_frames",
-           "maskgit_pass", "one_layer_run", "cp_position_ids"]
+           "maskgit_pass", "one_layer_run", "cp_position_ids", "talker_cp_frames"]
 
 
 def talker_prefill(m: Backbone, ids: np.ndarray, cache: KVCache):
@@ -126,6 +129,42 @@ def code_predictor_frames(m: Backbone, talker_hidden: np.ndarray, code0: np.ndar
         codes.append(argmax_first(lg))
         logits.append(lg)
     return np.stack(codes, axis=1).astype(np.int32), np.stack(logits, axis=1)
+
+
+def talker_cp_frames(talker: Backbone, cp: Backbone, cache: KVCache, first_codes: np.ndarray, n_frames: int,
+                     forced: Optional[np.ndarray] = None):
+    """The frame loop of the three-network protocol (Qwen3-TTS ncnn port, model
+    structure): per frame the Talker takes the sum of the previous frame's 16
+    codebook embeddings at its next position and predicts codebook 0 with the
+    3072-way head; the Code Predictor, with fresh state every frame, takes the
+    Talker's hidden state and code 0 and predicts codebooks 1..15; the frame's
+    16 codes are the next frame's Talker input.
+
+    Reading: the hidden state handed to the Code Predictor is the Talker's
+    last-layer output after its final norm (the vector its codec head reads).
+    first_codes[16]: the input of frame 0. forced[n_frames, 16] replays codes
+    (teacher forcing) as the next inputs. Returns (codes [n_frames, 16], Talker
+    logits [n_frames, rows], Code Predictor logits [n_frames, 15, rows],
+    hidden handed over [n_frames, H]).
+    """
+    codes_in = np.asarray(first_codes, np.int32)
+    out_codes, t_logits, c_logits, handed = [], [], [], []
+    for f in range(n_frames):
+        x = codebook_embed_sum(codes_in[None, :], talker.codebooks)
+        h = talker.forward_cached(x, [len(cache)], cache)
+        lg = talker.head_logits(h, 0)[0]
+        code0 = int(forced[f, 0]) if forced is not None else int(argmax_first(lg))
+        hidden = talker.final_norm(h)[0]
+        cp_codes, cp_lg, _ = code_predictor_frame(cp, hidden, code0, None if forced is None else forced[f, 1:])
+        frame = np.concatenate([[code0], cp_codes]).astype(np.int32)
+        if forced is not None:
+            frame = np.asarray(forced[f], np.int32)
+        out_codes.append(np.concatenate([[int(argmax_first(lg))], cp_codes]).astype(np.int32))
+        t_logits.append(lg)
+        c_logits.append(cp_lg)
+        handed.append(hidden)
+        codes_in = frame
+    return np.array(out_codes), np.array(t_logits), np.array(c_logits), np.array(handed)
 
 
 def maskgit_pass(m: Backbone, ids: np.ndarray, audio_mask: np.ndarray, audio_start: int,

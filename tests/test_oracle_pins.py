@@ -312,3 +312,52 @@ def test_batched_code_predictor_frames_match_single_frames():
         c1, l1, _ = O.code_predictor_frame(m, th[f], int(c0[f]))
         assert np.array_equal(codes[f], c1)
         assert np.allclose(logits[f], l1, rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------------------------- Talker -> Code Predictor frame loop
+def _frame_models(seed):
+    t_shape = synth.ModelShape(n_layers=2, hidden=64, n_q_heads=4, n_kv_heads=2, head_dim=16, ffn=96,
+                               codebook_rows=(48,) + (32,) * 15, n_heads_out=1, head_rows=48)
+    c_shape = synth.ModelShape(n_layers=1, hidden=64, n_q_heads=4, n_kv_heads=2, head_dim=16, ffn=96,
+                               codebook_rows=(48,) + (32,) * 15, n_heads_out=15, head_rows=32)
+    wt = synth.model_weights(t_shape, seed)
+    wc = synth.model_weights(c_shape, seed + 1)
+    wc.codebooks = wt.codebooks  # the Code Predictor's embeddings are the Talker's tables
+    return O.Backbone(wt, t_shape), O.Backbone(wc, c_shape)
+
+
+def test_frame_loop_composes_the_independent_drivers():
+    """The frame loop feeds the Talker exactly [code0, codes 1..15] of the previous
+    frame at the next position (checked against the Talker decode driver), and hands
+    the Code Predictor the final-normed hidden with fresh state each frame (checked
+    against the single-frame Code Predictor driver); teacher forcing with its own
+    codes replays it; the cache grows by one position per frame."""
+    talker, cp = _frame_models(21)
+    rng = np.random.default_rng(21)
+    ids = synth.uniform_ids(rng, (48,) + (32,) * 15, 5)
+    cache = talker.new_cache()
+    O.talker_prefill(talker, ids[:4], cache)
+    codes, t_lg, c_lg, handed = O.talker_cp_frames(talker, cp, cache, ids[4], 3)
+    assert len(cache) == 4 + 3
+    # Talker side: the decode driver fed with the same id rows
+    cache2 = talker.new_cache()
+    O.talker_prefill(talker, ids[:4], cache2)
+    rows = np.stack([ids[4], codes[0], codes[1]])
+    hid, lg2, _, fed = O.talker_decode_steps(talker, cache2, int(rows[0, 0]), rows[:, 1:], forced_id0=rows[:, 0])
+    assert np.array_equal(fed, rows)
+    assert np.allclose(lg2, t_lg, rtol=1e-11, atol=1e-12)
+    assert np.array_equal(codes[:, 0], O.argmax_first(t_lg))
+    # Code Predictor side: fresh frame from the normed hidden and code 0
+    for f in range(3):
+        assert np.allclose(handed[f], talker.final_norm(hid[f:f + 1])[0], rtol=1e-12, atol=1e-12)
+        c1, l1, _ = O.code_predictor_frame(cp, talker.final_norm(hid[f:f + 1])[0], int(codes[f, 0]))
+        assert np.array_equal(codes[f, 1:], c1)
+        assert np.allclose(c_lg[f], l1, rtol=1e-11, atol=1e-12)
+        # the un-normed hidden (a plausible slip) gives another frame
+        _, l_raw, _ = O.code_predictor_frame(cp, hid[f], int(codes[f, 0]))
+        assert not np.allclose(l_raw, l1, rtol=1e-6, atol=1e-6)
+    # teacher forcing with its own codes replays the free run
+    cache3 = talker.new_cache()
+    O.talker_prefill(talker, ids[:4], cache3)
+    codes3, t3, c3, _ = O.talker_cp_frames(talker, cp, cache3, ids[4], 3, forced=codes)
+    assert np.array_equal(codes3, codes) and np.allclose(t3, t_lg, atol=0) and np.allclose(c3, c_lg, atol=0)
