@@ -81,6 +81,7 @@ def _load() -> C.CDLL:
         "tts_bb_debug_fault": (I, [P, I, C.c_int64]),
         "tts_bb_maskgit_update": (I, [P, I, I, P, I, I, I, P, I, I, I, I, C.c_float, C.c_float]),
         "tts_bb_maskgit_schedule": (I, [I, I, C.c_double, P]),
+        "tts_bb_frame_step": (I, [P, P, I, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -95,7 +96,7 @@ EXPORTED = ("tts_bb_default_config", "tts_bb_create", "tts_bb_free", "tts_bb_pre
             "tts_bb_last_error", "tts_bb_version", "tts_bb_debug_kv_read", "tts_bb_debug_kv_write",
             "tts_bb_launch_count", "tts_bb_profile", "tts_bb_profile_report",
             "tts_bb_gqa_decode_attention_static", "tts_bb_debug_fault", "tts_bb_maskgit_update",
-            "tts_bb_maskgit_schedule")
+            "tts_bb_maskgit_schedule", "tts_bb_frame_step")
 
 
 def _ptr(x) -> Optional[int]:
@@ -209,6 +210,15 @@ def tts_bb_maskgit_update(h, n_items: int, T: int, logits, S_logits: int, cond_p
     st = lib.tts_bb_maskgit_update(h, n_items, T, _ptr(logits), S_logits, cond_pos0, uncond_pos0, _ptr(ids), S_ids,
                                    cond_ids_pos0, uncond_ids_pos0, n_unmask, cfg_scale, layer_penalty)
     return _check(h, st) if check else st
+
+
+def tts_bb_frame_step(talker, cp, B: int, slots, kv_lens, codes, talker_logits=None, check: bool = True) -> int:
+    sl, kl = _host_i32(slots), _host_i32(kv_lens)
+    st = lib.tts_bb_frame_step(talker, cp, B, _ptr(sl), _ptr(kl), _ptr(codes), _ptr(talker_logits))
+    if check and st != OK:
+        raise TtsBbError(st, (lib.tts_bb_last_error(talker) or b"").decode() + " / " +
+                         (lib.tts_bb_last_error(cp) or b"").decode())
+    return st
 
 
 def tts_bb_maskgit_schedule(num_step: int, n_total: int, t_shift: float = 0.1) -> np.ndarray:

@@ -106,6 +106,48 @@ __global__ void k_step_publish(const StepBlock* __restrict__ sb, const float* lo
         for (int i = threadIdx.x; i < HID; i += blockDim.x) sb->hidden_out[(size_t)b * HID + i] = hid[(size_t)b * HID + i];
 }
 
+// Frame loop, between the Talker step and the Code Predictor (Qwen3-TTS ncnn port, model
+// structure): row b of the Code Predictor's 2-token prefill gets the Talker's final-normed
+// hidden state (bf16) at position 0 and zero at position 1, whose ids carry code 0 alone; the id
+// rows of the 14 decode calls start at -1 (each call's argmax fills the next call's column).
+// grid B, 256 threads.
+__global__ void k_frame_prep(const float* __restrict__ hid, const bf16* __restrict__ gamma, float eps,
+                             const int32_t* __restrict__ code0, bf16* __restrict__ cp_emb, int32_t* __restrict__ cp_ids,
+                             int32_t* __restrict__ steps, int B) {
+    const int b = blockIdx.x, t = threadIdx.x;
+    __shared__ float red[8];
+    const float* x = hid + (size_t)b * HID;
+    float v[4], ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        v[e] = x[t + 256 * e];
+        ss += v[e] * v[e];
+    }
+    ss = warp_sum(ss);
+    if ((t & 31) == 0) red[t >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    const float r = rsqrtf(tot * (1.f / HID) + eps);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int c = t + 256 * e;
+        cp_emb[(size_t)b * 2 * HID + c] = f2bf(v[e] * r * bf2f(gamma[c]));
+        cp_emb[(size_t)b * 2 * HID + HID + c] = f2bf(0.f);
+    }
+    if (t < 32) cp_ids[(size_t)b * 32 + t] = t == 16 ? code0[b] : -1;
+    for (int i = t; i < 15 * 16; i += 256) steps[((size_t)(i >> 4) * B + b) * 16 + (i & 15)] = -1;
+}
+
+// codes[b] = [code 0, codes 1..14 from the decode calls' id rows, code 15 already in place]
+__global__ void k_frame_collect(const int32_t* __restrict__ code0, const int32_t* __restrict__ steps,
+                                int32_t* __restrict__ codes, int B) {
+    const int b = blockIdx.x, j = threadIdx.x;
+    if (j == 0) codes[(size_t)b * 16] = code0[b];
+    else if (j < 15) codes[(size_t)b * 16 + j] = steps[((size_t)j * B + b) * 16 + j];
+}
+
 __global__ void k_kv_copy(bf16* pool, const int32_t* page_table, int slot, int mbps, int pos0, int n, bf16* k,
                           bf16* v, int to_pool, int n_blocks, int* err) {
     // one CTA per token, 256 threads: 8 kv heads x 128 elements, 4 per thread for K and V
@@ -174,6 +216,14 @@ struct tts_bb {
     int32_t *seq_slot = nullptr, *seq_start = nullptr, *seq_len = nullptr, *key_len = nullptr;
     bf16* mg_pool = nullptr;
     bool attn_bidir_tc = false;
+    // frame-loop scratch (on the Code Predictor's handle): Talker hidden, code 0, prefill input,
+    // prefill ids, and the id rows of the 14 decode calls
+    float* fr_hid = nullptr;
+    int32_t* fr_code0 = nullptr;
+    bf16* fr_emb = nullptr;
+    int32_t* fr_ids = nullptr;
+    int32_t* fr_steps = nullptr;
+    int fr_cap = 0;
     unsigned long long* mg_keys = nullptr;  // MaskGIT update scratch: a key and a prediction per cell
     int32_t* mg_pred = nullptr;
     size_t mg_cells = 0;
@@ -318,10 +368,10 @@ tts_bb_status finish(tts_bb* h) {
 }
 
 enum Kind { K_SETUP, K_EMBED, K_RMSNORM, K_GEMV, K_GEMM, K_QKROPE, K_ATTN_DECODE, K_ATTN_PREFILL, K_ARGMAX,
-            K_KVCOPY, K_MEGA, K_GEMM_TC, K_GEMM_TCD, K_ATTN_BIDIR_TC, K_MG_UPDATE, K_NKINDS };
+            K_KVCOPY, K_MEGA, K_GEMM_TC, K_GEMM_TCD, K_ATTN_BIDIR_TC, K_MG_UPDATE, K_FRAME, K_NKINDS };
 const char* kind_name[K_NKINDS] = {"setup", "embed_gather", "rmsnorm", "gemv", "gemm_mma_split", "qk_norm_rope_append",
                                    "attn_decode", "attn_prefill", "argmax", "kv_copy", "decode_step_persistent",
-                                   "gemm_tcgen05", "gemm_tcgen05_decode", "attn_bidir_tcgen05", "maskgit_update"};
+                                   "gemm_tcgen05", "gemm_tcgen05_decode", "attn_bidir_tcgen05", "maskgit_update", "frame_glue"};
 
 cudaEvent_t prof_event(tts_bb* h) {
     if (!h->ev_pool.empty()) {
@@ -1180,6 +1230,77 @@ TTS_API tts_bb_status tts_bb_maskgit_pass(tts_bb* h, int B, int S, const int32_t
         L += launch_gemm(h->y, h->heads[0], B * Sa, N, HID, e, h->st, nullptr, h->err);
     }
     return finish(h);
+}
+
+TTS_API tts_bb_status tts_bb_frame_step(tts_bb* talker, tts_bb* cp, int B, const int32_t* slots,
+                                        const int32_t* kv_lens, int32_t* codes, float* talker_logits) {
+    if (!talker || !cp) return TTS_BB_E_INVALID;
+    const tts_bb_config &tc = talker->cfg, &cc = cp->cfg;
+    if (talker->st != cp->st) return fail(cp, TTS_BB_E_INVALID, "frame_step: both handles must share one stream");
+    if (tc.n_codebooks != 16 || cc.n_codebooks != 16 || tc.n_heads < 1 || cc.n_heads < 15)
+        return fail(cp, TTS_BB_E_INVALID, "frame_step: needs 16 codebooks, a Talker head and 15 predictor heads");
+    if (B < 1 || B > cc.max_slots || B > cc.max_batch || 2 * B > cc.max_tokens || cc.max_ctx < 16)
+        return fail(cp, TTS_BB_E_INVALID, "frame_step: B=%d does not fit the Code Predictor handle", B);
+    if (!codes || !slots || !kv_lens) return fail(talker, TTS_BB_E_INVALID, "frame_step: NULL codes, slots or kv_lens");
+    if (B > cp->fr_cap) {
+        cudaStreamSynchronize(cp->st);
+        for (void* p : {(void*)cp->fr_hid, (void*)cp->fr_code0, (void*)cp->fr_emb, (void*)cp->fr_ids, (void*)cp->fr_steps})
+            if (p) {
+                cudaFree(p);
+                cp->allocs.erase(std::remove(cp->allocs.begin(), cp->allocs.end(), p), cp->allocs.end());
+            }
+        cp->fr_hid = nullptr;
+        cp->fr_code0 = nullptr;
+        cp->fr_emb = nullptr;
+        cp->fr_ids = nullptr;
+        cp->fr_steps = nullptr;
+        cp->fr_cap = 0;
+        cudaError_t e = dalloc(cp, &cp->fr_hid, (size_t)B * HID);
+        if (e == cudaSuccess) e = dalloc(cp, &cp->fr_code0, (size_t)B);
+        if (e == cudaSuccess) e = dalloc(cp, &cp->fr_emb, (size_t)B * 2 * HID);
+        if (e == cudaSuccess) e = dalloc(cp, &cp->fr_ids, (size_t)B * 32);
+        if (e == cudaSuccess) e = dalloc(cp, &cp->fr_steps, (size_t)15 * B * 16);
+        if (e != cudaSuccess) return cuda_fail(cp, e, "frame-loop scratch");
+        cp->fr_cap = B;
+    }
+    std::vector<int32_t> cps(B), len2(B, 2), lens(B);
+    for (int b = 0; b < B; ++b) {
+        cps[b] = b;
+        if (cp->slot_len[b]) tts_bb_release(cp, b);  // a frame left behind by a failed call
+    }
+    // Talker: this frame's 16 codes at the next position -> code 0 and the hidden state
+    tts_bb_opts to{};
+    to.hidden_out = cp->fr_hid;
+    tts_bb_status st = tts_bb_decode_step(talker, B, slots, kv_lens, codes, 0, talker_logits, cp->fr_code0, &to);
+    if (st != TTS_BB_OK) return st;
+    {
+        Launch L(cp, K_FRAME);
+        k_frame_prep<<<B, 256, 0, cp->st>>>(cp->fr_hid, talker->final_norm, tc.rms_eps, cp->fr_code0, cp->fr_emb,
+                                            cp->fr_ids, cp->fr_steps, B);
+        L += 1;
+    }
+    // Code Predictor: 2-token prefill (head 0 -> code 1), then calls 1..14 (head j -> code j + 1)
+    tts_bb_opts po{};
+    po.embeds = cp->fr_emb;
+    po.argmax_stride = 16;
+    st = tts_bb_prefill(cp, B, 2, cps.data(), len2.data(), cp->fr_ids, 0, nullptr, cp->fr_steps + (size_t)1 * B * 16 + 1,
+                        &po);
+    for (int j = 1; j < 15 && st == TTS_BB_OK; ++j) {
+        for (int b = 0; b < B; ++b) lens[b] = j + 1;
+        tts_bb_opts dopt{};
+        dopt.argmax_stride = 16;
+        int32_t* dst = j < 14 ? cp->fr_steps + (size_t)(j + 1) * B * 16 + (j + 1) : codes + 15;
+        st = tts_bb_decode_step(cp, B, cps.data(), lens.data(), cp->fr_steps + (size_t)j * B * 16, j, nullptr, dst,
+                                &dopt);
+    }
+    if (st == TTS_BB_OK) {
+        Launch L(cp, K_FRAME);
+        k_frame_collect<<<B, 32, 0, cp->st>>>(cp->fr_code0, cp->fr_steps, codes, B);
+        L += 1;
+        st = finish(cp);
+    }
+    for (int b = 0; b < B; ++b) tts_bb_release(cp, b);
+    return st;
 }
 
 TTS_API tts_bb_status tts_bb_maskgit_update(tts_bb* h, int n_items, int T, const float* logits, int S_logits,

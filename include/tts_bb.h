@@ -203,6 +203,32 @@ tts_bb_status tts_bb_maskgit_pass(tts_bb* h, int B, int S, const int32_t* ids,
                                   const uint8_t* audio_mask, const int32_t* key_lens,
                                   int audio_start, float* logits_out, const tts_bb_opts* opts);
 
+/* One frame of the Talker -> Code Predictor loop (Qwen3-TTS ncnn port, model
+ * structure: the Talker predicts codebook 0 of each frame, the Code Predictor
+ * the other 15 in 15 autoregressive steps, and the frame's 16 embeddings
+ * summed are the Talker's next input), for B streams at once, greedy:
+ *   1. the Talker decodes `codes` (this frame's input, [B][16], -1 = absent)
+ *      at position kv_lens[b] of slot slots[b] (as tts_bb_decode_step), head 0
+ *      -> code 0, and its last-layer hidden state;
+ *   2. the Code Predictor runs a 2-token prefill in its slots 0..B-1: position
+ *      0 = the Talker hidden state after the Talker's final norm (bf16),
+ *      position 1 = E_0[code 0]; head 0 -> code 1; then calls j = 1..14 feed
+ *      E_j[code j] at position j + 1, head j -> code j + 1; its slots are
+ *      released afterwards;
+ *   3. codes[b] = the frame's 16 codes (the next frame's input).
+ *   talker, cp     handles on the same stream; cp has 16 codebooks (the
+ *                  Talker's tables), >= 15 heads, B <= max_slots, max_batch,
+ *                  2 B <= max_tokens, max_ctx >= 16
+ *   slots, kv_lens host int32 [B] for the Talker, as in tts_bb_decode_step
+ *   codes          device int32 [B][16], read then overwritten
+ *   talker_logits  device fp32 [B][Talker head_rows] or NULL
+ * Everything runs on the shared stream (about 2 + 16 launches and, for B > 2,
+ * graph replays); scratch is allocated on the first call that needs more.
+ * Errors as in tts_bb_decode_step / tts_bb_prefill (status of the first call
+ * that failed); TTS_BB_E_INVALID for handles that do not fit. */
+tts_bb_status tts_bb_frame_step(tts_bb* talker, tts_bb* cp, int B, const int32_t* slots,
+                                const int32_t* kv_lens, int32_t* codes, float* talker_logits);
+
 /* Greedy token update of one MaskGIT refinement step on the device
  * (omnivoice-cpp, MaskGIT decoder, class and position temperatures 0). The
  * batch of a pass holds n_items conditional rows (0..n_items-1) followed by
