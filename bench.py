@@ -526,6 +526,64 @@ def run_code_predictor(steps, warmup):
             "roofline": roofline_from_profile(rep), "kernel_profile": rep}
 
 
+def run_frame_loop(n_frames, warmup, B=1):
+    """Talker -> Code Predictor frame loop (tts_bb_frame_step), B streams: a 128-position Talker
+    prefill, then frames at positions 128.. (rewinding every 256 frames); one frame = the Talker
+    step (code 0) + the Code Predictor's 2-token prefill and 14 decode calls (codes 1..15)."""
+    import torch
+    import codec_token_tts_gb300 as m
+    from tests.gpu_util import config_for, dev_i32, weights_for
+    wt = synth.model_weights(synth.TALKER, 1)
+    wc = synth.model_weights(synth.CODE_PREDICTOR, 3)
+    wc.codebooks = wt.codebooks  # the Code Predictor embeds with the Talker's tables
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    ht = m.tts_bb_create(config_for(synth.TALKER, max_slots=B, max_ctx=P_PREFILL + N_DECODE, max_batch=B,
+                                    max_tokens=B * P_PREFILL, sync_errors=0), weights_for(wt), stream.cuda_stream)
+    hc = m.tts_bb_create(config_for(synth.CODE_PREDICTOR, max_slots=B, max_ctx=17, max_batch=B, max_tokens=2 * B,
+                                    sync_errors=0), weights_for(wc), stream.cuda_stream)
+    pre = np.stack([synth.talker_prefill_ids(1 + b, P_PREFILL + 1) for b in range(B)])
+    m.tts_bb_prefill(ht, B, P_PREFILL, list(range(B)), [P_PREFILL] * B, dev_i32(pre[:, :P_PREFILL]), -1, None, None)
+    first = dev_i32(pre[:, P_PREFILL])
+    codes = first.clone()
+    slots = np.arange(B, dtype=np.int32)
+    kv = np.zeros(B, np.int32)
+
+    def frames(n):
+        for t in range(n):
+            pos = P_PREFILL + (t % N_DECODE)
+            if pos == P_PREFILL:
+                for b in range(B):
+                    m.tts_bb_truncate(ht, b, P_PREFILL)
+                codes.copy_(first)
+            kv[:] = pos
+            m.lib.tts_bb_frame_step(ht, hc, B, slots.ctypes.data, kv.ctypes.data, codes.data_ptr(), None)
+
+    frames(warmup)
+    m.tts_bb_sync(ht)
+    m.tts_bb_sync(hc)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    frames(n_frames)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / n_frames
+    st = max(abs(m.tts_bb_sync(ht, check=False)), abs(m.tts_bb_sync(hc, check=False)))
+    m.tts_bb_free(hc)
+    m.tts_bb_free(ht)
+    # per frame: Talker weights + head + 16 embedding rows + KV read; 15 Code Predictor calls of
+    # 5 layers + one 2048-row head + their KV; position ~ the mean of 128..383
+    talker = 28 * 31_461_888 + 3072 * 1024 * 2 + 16 * 2048 + 2048 + 114_688 * (P_PREFILL + N_DECODE // 2)
+    cp = 15 * (5 * 31_461_888 + 2048 * 1024 * 2 + 2048 + 2048) + sum(20_480 * (j + 2) for j in range(15))
+    frame_bytes = talker + cp
+    return {"workload": f"frame_loop: Talker (28 layers) -> Code Predictor (5 layers, 15 codes) per frame, batch {B}, "
+                        f"positions 128..383, greedy codes fed back",
+            "value": B * 16 / (ms / 1e3), "unit": "codec tokens/s", "frames_per_s": B / (ms / 1e3),
+            "ms_per_frame": ms, "frames": n_frames, "status": st, "algorithmic_bytes_per_frame": frame_bytes,
+            "hbm_frac_of_measured": frame_bytes / (ms / 1e3) / 1e9 / peaks()[0]["hbm_gbs"]}
+
+
 def roofline_from_profile(rep, traffic=None):
     pk, src = peaks()
     ks = rep.get("kernels", [])
@@ -631,7 +689,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--no-secondary", action="store_true", help="skip the batch-64 serving, MaskGIT and Code Predictor lines")
-    ap.add_argument("--only", choices=["serving_b64", "maskgit", "code_predictor"],
+    ap.add_argument("--only", choices=["serving_b64", "maskgit", "code_predictor", "frame_loop"],
                     help="run one secondary workload alone (--steps / --warmup apply) and print its line; a profiling aid")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -641,7 +699,8 @@ def main():
         from tests.gpu_util import build_lib
         torch.cuda.set_device(0)
         build_lib()
-        fn = {"serving_b64": run_serving_b64, "maskgit": run_maskgit, "code_predictor": run_code_predictor}[args.only]
+        fn = {"serving_b64": run_serving_b64, "maskgit": run_maskgit, "code_predictor": run_code_predictor,
+              "frame_loop": run_frame_loop}[args.only]
         r = fn(args.steps, args.warmup)
         print(json.dumps({k: v for k, v in r.items() if k != "kernel_profile"}), flush=True)
         return
@@ -662,7 +721,7 @@ def main():
     res["roofline"] = roofline_from_profile(res["kernel_profile"], measured_traffic(res["kernel_profile"]))
     if not args.no_secondary:
         res["also"] = {"serving_b64": run_serving_b64(64, 4), "maskgit": run_maskgit(8, 3),
-                       "code_predictor": run_code_predictor(16, 3)}
+                       "code_predictor": run_code_predictor(16, 3), "frame_loop": run_frame_loop(64, 4)}
     if rank == 0 and not args.no_cpu_baseline:
         v, n, el, setup_s = oracle_talker_tokens_per_s(args.cpu_budget_s, 10_000)
         ci = cpu_info()
