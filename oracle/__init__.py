@@ -19,7 +19,8 @@ Sources (page title, section):
     identity input projection for 0.6B, talker-wide embeddings), Synthetic
     tests (cached / recompute equivalence).
   * "omnivoice-cpp docs/ARCHITECTURE.md", MaskGIT decoder — the greedy token
-    update of one refinement step (maskgit_update.py).
+    update of one refinement step (maskgit_update.py); Audio tokenizer
+    pipeline and RVQ codec — the decode of codes to frame features (rvq.py).
 
 Every function computes its plain definition in float64; matrix products use
 numpy's ``@``. No blocking, fusion or reordering beyond the definitions.
@@ -27,3 +28,4 @@ numpy's ``@``. No blocking, fusion or reordering beyond the definitions.
 from .backbone import *  # noqa: F401,F403
 from .loops import *  # noqa: F401,F403
 from .maskgit_update import *  # noqa: F401,F403
+from .rvq import *  # noqa: F401,F403
