@@ -82,6 +82,10 @@ def _load() -> C.CDLL:
         "tts_bb_maskgit_update": (I, [P, I, I, P, I, I, I, P, I, I, I, I, C.c_float, C.c_float]),
         "tts_bb_maskgit_schedule": (I, [I, I, C.c_double, P]),
         "tts_bb_frame_step": (I, [P, P, I, P, P, P, P]),
+        "tts_bb_rvq_create": (I, [I, I, I, I, C.POINTER(P), C.POINTER(P), C.POINTER(P), P, C.POINTER(P)]),
+        "tts_bb_rvq_decode": (I, [P, I, I, P, P]),
+        "tts_bb_rvq_sync": (I, [P]),
+        "tts_bb_rvq_free": (V, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -96,7 +100,8 @@ EXPORTED = ("tts_bb_default_config", "tts_bb_create", "tts_bb_free", "tts_bb_pre
             "tts_bb_last_error", "tts_bb_version", "tts_bb_debug_kv_read", "tts_bb_debug_kv_write",
             "tts_bb_launch_count", "tts_bb_profile", "tts_bb_profile_report",
             "tts_bb_gqa_decode_attention_static", "tts_bb_debug_fault", "tts_bb_maskgit_update",
-            "tts_bb_maskgit_schedule", "tts_bb_frame_step")
+            "tts_bb_maskgit_schedule", "tts_bb_frame_step", "tts_bb_rvq_create", "tts_bb_rvq_decode",
+            "tts_bb_rvq_sync", "tts_bb_rvq_free")
 
 
 def _ptr(x) -> Optional[int]:
@@ -219,6 +224,34 @@ def tts_bb_frame_step(talker, cp, B: int, slots, kv_lens, codes, talker_logits=N
         raise TtsBbError(st, (lib.tts_bb_last_error(talker) or b"").decode() + " / " +
                          (lib.tts_bb_last_error(cp) or b"").decode())
     return st
+
+
+def tts_bb_rvq_create(embed, proj_w, proj_b, stream=None):
+    """embed, proj_w, proj_b: lists (one per codebook) of device bf16 tensors [n][d], [out][d], [out]."""
+    K = len(embed)
+    n, d = int(embed[0].shape[0]), int(embed[0].shape[1])
+    out_dim = int(proj_w[0].shape[0])
+    arr = lambda xs: (C.c_void_p * K)(*[_ptr(x) for x in xs])
+    h = C.c_void_p()
+    st = lib.tts_bb_rvq_create(K, n, d, out_dim, arr(embed), arr(proj_w), arr(proj_b), stream, C.byref(h))
+    if st != OK:
+        raise TtsBbError(st, "tts_bb_rvq_create")
+    return h.value
+
+
+def tts_bb_rvq_decode(r, B: int, T: int, codes, out, check: bool = True) -> int:
+    st = lib.tts_bb_rvq_decode(r, B, T, _ptr(codes), _ptr(out))
+    if check and st != OK:
+        raise TtsBbError(st, "tts_bb_rvq_decode")
+    return st
+
+
+def tts_bb_rvq_sync(r) -> int:
+    return lib.tts_bb_rvq_sync(r)
+
+
+def tts_bb_rvq_free(r) -> None:
+    lib.tts_bb_rvq_free(r)
 
 
 def tts_bb_maskgit_schedule(num_step: int, n_total: int, t_shift: float = 0.1) -> np.ndarray:

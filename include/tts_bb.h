@@ -267,6 +267,31 @@ tts_bb_status tts_bb_maskgit_update(tts_bb* h, int n_items, int T, const float* 
  * t_shift <= 0 or a NULL counts. */
 tts_bb_status tts_bb_maskgit_schedule(int num_step, int n_total, double t_shift, int32_t* counts);
 
+/* RVQ codec decode (omnivoice-cpp, Audio tokenizer pipeline, Decode, and RVQ
+ * codec): codes of K codebooks -> out_dim frame features,
+ *   out[b][t] = sum_k ( embed_k[codes[b][k][t]] . proj_w_k^T + proj_b_k )
+ * with embed_k [codebook_size][dim] (codebook.embed), proj_w_k [out_dim][dim]
+ * (project_out.weight) and proj_b_k [out_dim] (project_out.bias), all device
+ * bf16 pointers, K of each; the OmniVoice codec has K = 8, 1024 x 64 tables and
+ * out_dim 1024. tts_bb_rvq_create copies them (the caller may free its copies)
+ * and returns TTS_BB_E_INVALID for NULL pointers or sizes outside
+ * 1 <= K <= 64, dim a multiple of 8 with K * dim a multiple of 64,
+ * TTS_BB_E_OOM, TTS_BB_E_UNSUPPORTED without tcgen05 tensor maps. */
+typedef struct tts_bb_rvq tts_bb_rvq;
+tts_bb_status tts_bb_rvq_create(int n_codebooks, int codebook_size, int dim, int out_dim,
+                                const void* const* embed, const void* const* proj_w,
+                                const void* const* proj_b, void* stream, tts_bb_rvq** out);
+/* codes device int32 [B][K][T]; out device fp32 [B][T][out_dim]. Asynchronous
+ * on the handle's stream (a gather kernel and one GEMM); a code outside
+ * 0..codebook_size-1 contributes nothing and is reported by tts_bb_rvq_sync as
+ * TTS_BB_E_BAD_ID. Scratch (K * dim bf16 per frame) grows on the first call
+ * that needs more. */
+tts_bb_status tts_bb_rvq_decode(tts_bb_rvq* r, int B, int T, const int32_t* codes, float* out);
+/* Wait for the handle's work; returns (and clears) a latched device error. */
+tts_bb_status tts_bb_rvq_sync(tts_bb_rvq* r);
+/* Wait and free. NULL is a no-op. */
+void tts_bb_rvq_free(tts_bb_rvq* r);
+
 /* Return the slot's KV blocks to the pool; its length becomes 0. */
 tts_bb_status tts_bb_release(tts_bb* h, int slot);
 
