@@ -394,6 +394,7 @@ def run_maskgit(steps, warmup):
     m.tts_bb_profile(h, False)
     refine = run_maskgit_refinement(m, h, seed, stream)
     m.tts_bb_free(h)
+    refine["rvq_decode"] = run_rvq_decode(m, stream)
     flops = 2 * 8192 * 15_728_640 * 28 + 4 * 8 * 16 * 1024 ** 2 * 128 * 28 + 2 * 8 * 768 * 8200 * 1024
     pk = peaks()[0]
     return {"workload": "maskgit: OmniVoice LM pass, 28 layers, B=8 x S=1024 (256 text + 768 audio), bidirectional, "
@@ -402,6 +403,38 @@ def run_maskgit(steps, warmup):
             "tflops": flops / (ms / 1e3) / 1e12, "flop_per_pass": flops,
             "tensor_frac_of_measured_sustained": flops / (ms / 1e3) / 1e12 / pk["bf16_tflops_sustained"],
             "roofline": roofline_from_profile(rep), "refinement": refine, "kernel_profile": rep}
+
+
+def run_rvq_decode(m, stream, B=4, T=768, reps=20):
+    """RVQ codec decode of a refinement's output: 4 items x 768 frames x 8 codebooks of 1024 x 64
+    (seeded bf16 tables) -> [4][768][1024] fp32 features."""
+    import torch
+    from tests.gpu_util import dev_bf16_bits, dev_i32
+    K, N, D, OUT = 8, 1024, 64, 1024
+    r = synth.rng_for(5, "rvq_tables")
+    e = [dev_bf16_bits(synth.normal_bf16(r, (N, D), 1.0)) for _ in range(K)]
+    w = [dev_bf16_bits(synth.normal_bf16(r, (OUT, D), 0.05)) for _ in range(K)]
+    b = [dev_bf16_bits(synth.normal_bf16(r, (OUT,), 0.1)) for _ in range(K)]
+    rv = m.tts_bb_rvq_create(e, w, b, stream.cuda_stream)
+    codes = dev_i32(synth.rng_for(5, "rvq_codes").integers(0, N, (B, K, T)))
+    out = torch.zeros(B, T, OUT, dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        m.tts_bb_rvq_decode(rv, B, T, codes, out)
+    st = m.tts_bb_rvq_sync(rv)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(reps):
+        m.tts_bb_rvq_decode(rv, B, T, codes, out)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    m.tts_bb_rvq_free(rv)
+    us = ev0.elapsed_time(ev1) / reps * 1e3
+    # codes read, gathered 64-d rows, packed weights read once, output written
+    nbytes = B * K * T * 4 + B * T * K * D * 2 + OUT * K * D * 2 + B * T * OUT * 4
+    return {"workload": f"RVQ decode: {B} x {T} frames x {K} codebooks (1024 x 64) -> {OUT}-d fp32",
+            "us_per_decode": us, "frames_per_s": B * T / (us / 1e6), "status": st,
+            "algorithmic_bytes": nbytes, "hbm_frac_of_measured": nbytes / (us / 1e6) / 1e9 / peaks()[0]["hbm_gbs"]}
 
 
 def run_maskgit_refinement(m, h, seed, stream, n_step=32):
