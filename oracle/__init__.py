@@ -20,7 +20,9 @@ Sources (page title, section):
     tests (cached / recompute equivalence).
   * "omnivoice-cpp docs/ARCHITECTURE.md", MaskGIT decoder — the greedy token
     update of one refinement step (maskgit_update.py); Audio tokenizer
-    pipeline and RVQ codec — the decode of codes to frame features (rvq.py).
+    pipeline and RVQ codec — the decode of codes to frame features (rvq.py);
+    DAC decoder block channels, Snake activation, ConvTranspose1d — the
+    decoder from frame features to audio (dac.py).
 
 Every function computes its plain definition in float64; matrix products use
 numpy's ``@``. No blocking, fusion or reordering beyond the definitions.
@@ -29,3 +31,4 @@ from .backbone import *  # noqa: F401,F403
 from .loops import *  # noqa: F401,F403
 from .maskgit_update import *  # noqa: F401,F403
 from .rvq import *  # noqa: F401,F403
+from .dac import *  # noqa: F401,F403
