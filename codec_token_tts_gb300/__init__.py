@@ -53,6 +53,18 @@ class TtsBbError(RuntimeError):
         self.status = status
 
 
+class tts_bb_dac_block(C.Structure):
+    _fields_ = [("alpha", C.c_void_p), ("up_w", C.c_void_p), ("up_b", C.c_void_p),
+                ("res_alpha1", C.c_void_p * 3), ("res_w1", C.c_void_p * 3), ("res_b1", C.c_void_p * 3),
+                ("res_alpha2", C.c_void_p * 3), ("res_w2", C.c_void_p * 3), ("res_b2", C.c_void_p * 3)]
+
+
+class tts_bb_dac_weights(C.Structure):
+    _fields_ = [("fc2_w", C.c_void_p), ("fc2_b", C.c_void_p), ("conv1_w", C.c_void_p), ("conv1_b", C.c_void_p),
+                ("block", tts_bb_dac_block * 5), ("final_alpha", C.c_void_p), ("conv2_w", C.c_void_p),
+                ("conv2_b", C.c_void_p)]
+
+
 def _load() -> C.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with codec_token_tts_gb300.build.build() "
@@ -86,6 +98,9 @@ def _load() -> C.CDLL:
         "tts_bb_rvq_decode": (I, [P, I, I, P, P]),
         "tts_bb_rvq_sync": (I, [P]),
         "tts_bb_rvq_free": (V, [P]),
+        "tts_bb_dac_create": (I, [C.POINTER(tts_bb_dac_weights), P, C.POINTER(P)]),
+        "tts_bb_dac_decode": (I, [P, I, I, P, P]),
+        "tts_bb_dac_free": (V, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -101,7 +116,7 @@ EXPORTED = ("tts_bb_default_config", "tts_bb_create", "tts_bb_free", "tts_bb_pre
             "tts_bb_launch_count", "tts_bb_profile", "tts_bb_profile_report",
             "tts_bb_gqa_decode_attention_static", "tts_bb_debug_fault", "tts_bb_maskgit_update",
             "tts_bb_maskgit_schedule", "tts_bb_frame_step", "tts_bb_rvq_create", "tts_bb_rvq_decode",
-            "tts_bb_rvq_sync", "tts_bb_rvq_free")
+            "tts_bb_rvq_sync", "tts_bb_rvq_free", "tts_bb_dac_create", "tts_bb_dac_decode", "tts_bb_dac_free")
 
 
 def _ptr(x) -> Optional[int]:
@@ -252,6 +267,36 @@ def tts_bb_rvq_sync(r) -> int:
 
 def tts_bb_rvq_free(r) -> None:
     lib.tts_bb_rvq_free(r)
+
+
+def tts_bb_dac_create(w: dict, stream=None):
+    """w: device fp32 tensors keyed like the oracle's dict (fc2_w, fc2_b, conv1_w, conv1_b,
+    blocks[i]{alpha, up_w, up_b, res[j]{alpha1, w1, b1, alpha2, w2, b2}}, final_alpha, conv2_w, conv2_b)."""
+    s = tts_bb_dac_weights()
+    for k in ("fc2_w", "fc2_b", "conv1_w", "conv1_b", "final_alpha", "conv2_w", "conv2_b"):
+        setattr(s, k, _ptr(w[k]))
+    for i, blk in enumerate(w["blocks"]):
+        bs = s.block[i]
+        bs.alpha, bs.up_w, bs.up_b = _ptr(blk["alpha"]), _ptr(blk["up_w"]), _ptr(blk["up_b"])
+        for j, ru in enumerate(blk["res"]):
+            bs.res_alpha1[j], bs.res_w1[j], bs.res_b1[j] = _ptr(ru["alpha1"]), _ptr(ru["w1"]), _ptr(ru["b1"])
+            bs.res_alpha2[j], bs.res_w2[j], bs.res_b2[j] = _ptr(ru["alpha2"]), _ptr(ru["w2"]), _ptr(ru["b2"])
+    h = C.c_void_p()
+    st = lib.tts_bb_dac_create(C.byref(s), stream, C.byref(h))
+    if st != OK:
+        raise TtsBbError(st, "tts_bb_dac_create")
+    return h.value
+
+
+def tts_bb_dac_decode(d, B: int, T: int, features, audio, check: bool = True) -> int:
+    st = lib.tts_bb_dac_decode(d, B, T, _ptr(features), _ptr(audio))
+    if check and st != OK:
+        raise TtsBbError(st, "tts_bb_dac_decode")
+    return st
+
+
+def tts_bb_dac_free(d) -> None:
+    lib.tts_bb_dac_free(d)
 
 
 def tts_bb_maskgit_schedule(num_step: int, n_total: int, t_shift: float = 0.1) -> np.ndarray:

@@ -292,6 +292,48 @@ tts_bb_status tts_bb_rvq_sync(tts_bb_rvq* r);
 /* Wait and free. NULL is a no-op. */
 void tts_bb_rvq_free(tts_bb_rvq* r);
 
+/* DAC decoder: frame features -> 24 kHz audio (omnivoice-cpp, Audio tokenizer
+ * pipeline, Decode; DAC decoder block channels; Snake activation;
+ * ConvTranspose1d): fc2 Linear 1024 -> 256, conv1 (256 -> 1024, k 7, pad 3),
+ * five blocks with ratios r = 8, 5, 4, 2, 3 and channels 1024 -> 512 -> 256 ->
+ * 128 -> 64 -> 32 (snake; ConvTranspose1d k 2r, stride r, padding ceil(r/2),
+ * output_padding r % 2; three residual units with dilations 1, 3, 9: snake,
+ * Conv1d k 7 pad 3d, snake, Conv1d k 1, add), snake, conv2 (32 -> 1, k 7,
+ * pad 3). Snake: y = x + sin(alpha x)^2 / (alpha + 1e-9), alpha per channel.
+ * Every convolution and the Linear have a bias. All weights are device fp32
+ * in PyTorch layouts; tts_bb_dac_create copies them. */
+typedef struct {
+    const float* alpha;          /* [IC] snake before the upsampling convolution */
+    const float* up_w;           /* [IC][OC][2r] ConvTranspose1d weight */
+    const float* up_b;           /* [OC] */
+    const float* res_alpha1[3];  /* [OC] */
+    const float* res_w1[3];      /* [OC][OC][7] */
+    const float* res_b1[3];      /* [OC] */
+    const float* res_alpha2[3];  /* [OC] */
+    const float* res_w2[3];      /* [OC][OC][1] */
+    const float* res_b2[3];      /* [OC] */
+} tts_bb_dac_block;
+typedef struct {
+    const float* fc2_w;          /* [256][1024] */
+    const float* fc2_b;          /* [256] */
+    const float* conv1_w;        /* [1024][256][7] */
+    const float* conv1_b;        /* [1024] */
+    tts_bb_dac_block block[5];
+    const float* final_alpha;    /* [32] */
+    const float* conv2_w;        /* [1][32][7] */
+    const float* conv2_b;        /* [1] */
+} tts_bb_dac_weights;
+typedef struct tts_bb_dac tts_bb_dac;
+/* TTS_BB_E_INVALID for a NULL pointer, TTS_BB_E_OOM when memory runs out. */
+tts_bb_status tts_bb_dac_create(const tts_bb_dac_weights* w, void* stream, tts_bb_dac** out);
+/* features device fp32 [B][T][1024] (the RVQ decode output); audio device fp32
+ * [B][960 T]. Asynchronous on the handle's stream (38 kernel launches); three
+ * activation buffers of 30720 T floats per item are allocated on the first
+ * call that needs more. TTS_BB_E_INVALID for bad sizes or NULL buffers. */
+tts_bb_status tts_bb_dac_decode(tts_bb_dac* d, int B, int T, const float* features, float* audio);
+/* Wait and free. NULL is a no-op. */
+void tts_bb_dac_free(tts_bb_dac* d);
+
 /* Return the slot's KV blocks to the pool; its length becomes 0. */
 tts_bb_status tts_bb_release(tts_bb* h, int slot);
 
