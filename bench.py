@@ -395,6 +395,7 @@ def run_maskgit(steps, warmup):
     refine = run_maskgit_refinement(m, h, seed, stream)
     m.tts_bb_free(h)
     refine["rvq_decode"] = run_rvq_decode(m, stream)
+    refine["dac_decode"] = run_dac_decode(m, stream)
     flops = 2 * 8192 * 15_728_640 * 28 + 4 * 8 * 16 * 1024 ** 2 * 128 * 28 + 2 * 8 * 768 * 8200 * 1024
     pk = peaks()[0]
     return {"workload": "maskgit: OmniVoice LM pass, 28 layers, B=8 x S=1024 (256 text + 768 audio), bidirectional, "
@@ -435,6 +436,65 @@ def run_rvq_decode(m, stream, B=4, T=768, reps=20):
     return {"workload": f"RVQ decode: {B} x {T} frames x {K} codebooks (1024 x 64) -> {OUT}-d fp32",
             "us_per_decode": us, "frames_per_s": B * T / (us / 1e6), "status": st,
             "algorithmic_bytes": nbytes, "hbm_frac_of_measured": nbytes / (us / 1e6) / 1e9 / peaks()[0]["hbm_gbs"]}
+
+
+def dac_flops_per_frame():
+    """FMA work of the DAC decoder per 25 Hz frame (2 flops per multiply-add)."""
+    ch, ratios = (1024, 512, 256, 128, 64, 32), (8, 5, 4, 2, 3)
+    f = 2 * 1024 * 256 + 2 * 256 * 1024 * 7
+    s = 1
+    for i, r in enumerate(ratios):
+        s *= r
+        ic, oc = ch[i], ch[i + 1]
+        f += s * (2 * ic * oc * 2 + 3 * (2 * oc * oc * 7 + 2 * oc * oc))
+    return f + 960 * 2 * 32 * 7
+
+
+def run_dac_decode(m, stream, B=4, T=768, reps=3):
+    """DAC decode of RVQ features: 4 items x 768 frames (30.7 s of 24 kHz audio each), seeded fp32
+    weights scaled by fan-in."""
+    import math
+    import torch
+    rng = np.random.default_rng(7)
+
+    def f(*shape, std):
+        return torch.from_numpy(rng.normal(0, std, shape).astype(np.float32)).cuda()
+
+    def u(n):
+        return torch.from_numpy(rng.uniform(0.5, 1.5, n).astype(np.float32)).cuda()
+
+    ch, ratios = (1024, 512, 256, 128, 64, 32), (8, 5, 4, 2, 3)
+    w = {"fc2_w": f(256, 1024, std=1 / 32), "fc2_b": f(256, std=0.05), "conv1_w": f(1024, 256, 7, std=1 / math.sqrt(1792)),
+         "conv1_b": f(1024, std=0.05), "final_alpha": u(32), "conv2_w": f(1, 32, 7, std=1 / math.sqrt(224)),
+         "conv2_b": f(1, std=0.05), "blocks": []}
+    for i, r in enumerate(ratios):
+        ic, oc = ch[i], ch[i + 1]
+        w["blocks"].append({"alpha": u(ic), "up_w": f(ic, oc, 2 * r, std=1 / math.sqrt(2 * ic)), "up_b": f(oc, std=0.05),
+                            "res": [{"alpha1": u(oc), "w1": f(oc, oc, 7, std=0.5 / math.sqrt(7 * oc)), "b1": f(oc, std=0.05),
+                                     "alpha2": u(oc), "w2": f(oc, oc, 1, std=0.5 / math.sqrt(oc)), "b2": f(oc, std=0.05)}
+                                    for _ in range(3)]})
+    d = m.tts_bb_dac_create(w, stream.cuda_stream)
+    feat = torch.from_numpy(rng.normal(0, 1, (B, T, 1024)).astype(np.float32)).cuda()
+    audio = torch.zeros(B, 960 * T, dtype=torch.float32, device="cuda")
+    m.tts_bb_dac_decode(d, B, T, feat, audio)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(reps):
+        m.tts_bb_dac_decode(d, B, T, feat, audio)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    finite = bool(torch.isfinite(audio).all().item())
+    m.tts_bb_dac_free(d)
+    ms = ev0.elapsed_time(ev1) / reps
+    flops = dac_flops_per_frame() * B * T
+    # fp32 FMA peak: 152 SMs x 128 lanes x 2 flops x 2.07 GHz (maximum SM clock)
+    peak = 152 * 128 * 2 * 2.07e9 / 1e12
+    tf = flops / (ms / 1e3) / 1e12
+    return {"workload": f"DAC decode: {B} items x {T} frames -> {B} x {960 * T} samples (24 kHz), fp32",
+            "ms_per_decode": ms, "audio_s_per_s": B * T / 25.0 / (ms / 1e3), "finite": finite,
+            "roofline": {"bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                         "peak_source": "fp32 FMA units x maximum SM clock", "flop_per_decode": flops}}
 
 
 def run_maskgit_refinement(m, h, seed, stream, n_step=32):
