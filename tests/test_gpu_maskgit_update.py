@@ -16,7 +16,7 @@ import pytest
 
 import oracle as O
 import synth
-from tests.gpu_util import Engine, LOGIT_TOL, dev_i32, dev_u8, f32_zeros
+from tests.gpu_util import Engine, dev_u8, f32_zeros
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
