@@ -777,6 +777,32 @@ __global__ void __launch_bounds__(at::NT, 1)
     }
     pdl_wait();  // q and the K / V tiles come from upstream kernels
     pdl_trigger();
+    const int L = key_len[b];
+    const int nt = (L + BKV - 1) / BKV;
+    // K and V tiles j of one stage: 2 cache blocks x 2 dims chunks of 64 x 64 each
+    auto issue_tile = [&](int which, int j) {
+        const int st = j % STAGES;
+        uint64_t* full = which ? v_full : k_full;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(full + st)),
+                     "r"((uint32_t)(2 * CHUNK))
+                     : "memory");
+        for (int i = 0; i < 2; ++i) {
+            const int phys = b * bps + 2 * j + i;  // past the sequence: masked keys (or zero fill)
+            const int row = ((phys * 2 + which) * NKV + g) * KVB;
+            for (int c = 0; c < 2; ++c) {
+                // K stage: [dims chunk c][keys 64i ..]; V stage: [cache block i][dims chunk c]
+                const int off = which ? i * CHUNK + c * (CHUNK / 2) : c * CHUNK + i * (CHUNK / 2);
+                tma_load_2d(smem + (which ? V_OFF : K_OFF) + st * 2 * CHUNK + off, &tmKV, c * 64, row, full + st);
+            }
+        }
+    };
+    // the first stages are requested by the thread that initialised the barriers, before Q is staged
+    const int pre = nt < STAGES ? nt : STAGES;
+    if (threadIdx.x == 0)
+        for (int j = 0; j < pre; ++j) {
+            issue_tile(0, j);
+            issue_tile(1, j);
+        }
     // Q rows -> shared memory, swizzled (rows past the sequence are zero); all loads first
     {
         constexpr int NQL = (ROWS * 16 + NT - 1) / NT;
@@ -800,33 +826,20 @@ __global__ void __launch_bounds__(at::NT, 1)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
-    const int L = key_len[b];
-    const int nt = (L + BKV - 1) / BKV;
 
     if (warp == 0) {
         if (lane < 2) {  // ---------------- TMA producers: lane 0 K, lane 1 V of each 128-key tile
             const int which = lane;
             uint64_t* full = which ? v_full : k_full;
             uint64_t* empty = which ? v_empty : k_empty;
-            int issued = 0;
-            for (int j = 0; j < nt; ++j) {
+            int issued = pre;
+            for (int j = pre; j < nt; ++j) {
                 const int st = j % STAGES;
-                if (j >= STAGES && !tc_wait(empty + st, ((j / STAGES) - 1) & 1, abort_s)) {
+                if (!tc_wait(empty + st, ((j / STAGES) - 1) & 1, abort_s)) {
                     *abort_s = 1;
                     break;
                 }
-                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(full + st)),
-                             "r"((uint32_t)(2 * CHUNK))
-                             : "memory");
-                for (int i = 0; i < 2; ++i) {
-                    const int phys = b * bps + 2 * j + i;  // past the sequence: masked keys (or zero fill)
-                    const int row = ((phys * 2 + which) * NKV + g) * KVB;
-                    for (int c = 0; c < 2; ++c) {
-                        // K stage: [dims chunk c][keys 64i ..]; V stage: [cache block i][dims chunk c]
-                        const int off = which ? i * CHUNK + c * (CHUNK / 2) : c * CHUNK + i * (CHUNK / 2);
-                        tma_load_2d(smem + (which ? V_OFF : K_OFF) + st * 2 * CHUNK + off, &tmKV, c * 64, row, full + st);
-                    }
-                }
+                issue_tile(which, j);
                 ++issued;
             }
             if (*abort_s)
