@@ -49,7 +49,7 @@ typedef struct tts_bb tts_bb; /* opaque engine handle */
 typedef enum {
     TTS_BB_OK = 0,
     TTS_BB_E_INVALID = -1,         /* bad argument; nothing was enqueued */
-    TTS_BB_E_UNSUPPORTED = -2,     /* valid C, shape this build does not run */
+    TTS_BB_E_UNSUPPORTED = -2,     /* valid C, a shape the kernels are not built for */
     TTS_BB_E_CUDA = -3,            /* a CUDA runtime call failed */
     TTS_BB_E_OOM = -4,             /* device memory or KV blocks exhausted */
     TTS_BB_E_DEVICE_TIMEOUT = -5,  /* a bounded device-side wait ran out */
@@ -62,7 +62,7 @@ typedef enum {
  * intermediate_size, head_dim, rms_norm_eps, rope_theta, vocab_size). */
 typedef struct {
     int n_layers;          /* 28 Talker / OmniVoice, 5 Code Predictor */
-    int hidden;            /* 1024 (only value this build runs) */
+    int hidden;            /* 1024 (the only value the kernels support) */
     int n_q_heads;         /* 16 */
     int n_kv_heads;        /* 8 */
     int head_dim;          /* 128 */
