@@ -63,8 +63,9 @@ def conv_transpose1d(x: np.ndarray, w: np.ndarray, b: np.ndarray, stride: int, p
     _, OC, K = w.shape
     T_out = (T - 1) * stride - 2 * pad + (K - 1) + out_pad + 1
     full = np.zeros((OC, (T - 1) * stride + K + out_pad))
-    for t in range(T):
-        full[:, t * stride:t * stride + K] += np.einsum("ic,iok->ok", x[:, t:t + 1], np.asarray(w, np.float64))
+    w = np.asarray(w, np.float64)
+    for k in range(K):  # tap k of every input sample t lands at t * stride + k
+        full[:, k:k + (T - 1) * stride + 1:stride] += w[:, :, k].T @ x
     y = full[:, pad:pad + T_out]
     return y + np.asarray(b, np.float64)[:, None]
 
