@@ -44,8 +44,9 @@ def to_device(w):
     return torch.from_numpy(np.ascontiguousarray(w)).cuda()
 
 
-@pytest.mark.parametrize("B,T", [(1, 1), (2, 5), (1, 7)])
+@pytest.mark.parametrize("B,T", [(1, 1), (2, 5), (1, 7), (1, 768)])
 def test_dac_matches_oracle(B, T):
+    """(1, 768) is one item of the bench's decode: 30.7 s of audio, every sample compared."""
     import codec_token_tts_gb300 as m
     w = dac_weights(71)
     feat = np.random.default_rng(72).normal(0, 1, (B, T, 1024)).astype(np.float32)

@@ -103,6 +103,16 @@ def test_update_matches_oracle(eng, n_unmask):
     _run_case(eng, logits, ids, n_items, T, S_log, 60, 0, S_ids, 100, 10, n_unmask)
 
 
+def test_update_full_size(eng):
+    """The shape the bench's refinement runs: 4 items x 8 codebooks x 768 target frames, logits over
+    all 1024 positions (conditional window at 256, unconditional at 0), the largest step of the
+    32-step schedule, 30 % of the cells already unmasked."""
+    n_items, T, S = 4, 768, 1024
+    n = int(O.maskgit_schedule(32, K * T, 0.1).max())
+    logits, ids = _inputs(11, n_items, T, S, S, cpos=256, upos=0, cidp=256, uidp=0)
+    _run_case(eng, logits, ids, n_items, T, S, 256, 0, S, 256, 0, n)
+
+
 def test_update_ties_take_lowest_index(eng):
     """Equal logits everywhere: every masked cell of a codebook ties, so the
     lowest positions of codebook 0 go first (scores fall by 5 per codebook)."""

@@ -45,8 +45,9 @@ def _run(m, e, w, b, codes):
         m.tts_bb_rvq_free(r)
 
 
-@pytest.mark.parametrize("B,T", [(1, 5), (3, 257)])
+@pytest.mark.parametrize("B,T", [(1, 5), (3, 257), (4, 768)])
 def test_rvq_exact_on_integer_tables(B, T):
+    """(4, 768) is the shape the bench times (a refinement's 4 items x 768 frames)."""
     import codec_token_tts_gb300 as m
     e, w, b = _tables(61, True)
     codes = synth.rng_for(61, f"codes{B}").integers(0, N, (B, K, T))
