@@ -83,3 +83,32 @@ def test_frame_step_rejects_mismatched_handles():
         assert m.tts_bb_frame_step(et.h, ec.h, 2, [0, 1], [0, 0], codes, check=False) == m.E_INVALID
         # a Talker used as the Code Predictor lacks the 15 heads
         assert m.tts_bb_frame_step(et.h, et.h, 1, [0], [0], codes, check=False) == m.E_INVALID
+
+
+def test_frame_loop_full_size():
+    """The bench's frame loop: 28-layer Talker (3072-row E_0 and head) and 5-layer Code Predictor,
+    batch 1, a 128-position prefill then 2 frames, against the teacher-forced oracle."""
+    wt = synth.model_weights(synth.TALKER, 1)
+    wc = synth.model_weights(synth.CODE_PREDICTOR, 3)
+    wc.codebooks = wt.codebooks
+    P, n_frames = 128, 2
+    pre = synth.talker_prefill_ids(1, P + 1)
+    with Engine(wt, max_slots=1, max_ctx=P + 8, max_batch=1, max_tokens=P) as et, \
+            Engine(wc, max_slots=1, max_ctx=17, max_batch=1, max_tokens=2) as ec:
+        m = et.m
+        m.tts_bb_prefill(et.h, 1, P, [0], [P], dev_i32(pre[None, :P]))
+        codes = dev_i32(pre[None, P])
+        logits = f32_zeros(1, 3072)
+        got_codes, got_logits = [], []
+        for f in range(n_frames):
+            m.tts_bb_frame_step(et.h, ec.h, 1, [0], [P + f], codes, logits)
+            got_codes.append(codes.cpu().numpy()[0].copy())
+            got_logits.append(logits.cpu().numpy()[0].copy())
+    got_codes, got_logits = np.array(got_codes), np.array(got_logits)
+    talker, cp = O.Backbone(wt, wt.shape), O.Backbone(wc, wc.shape)
+    cache = talker.new_cache()
+    O.talker_prefill(talker, pre[:P], cache)
+    o_codes, t_lg, c_lg, _ = O.talker_cp_frames(talker, cp, cache, pre[P], n_frames, forced=got_codes)
+    check_logits_and_argmax(got_logits, t_lg, got_codes[:, 0], o_codes[:, 0], min_agree=0.0)
+    for f in range(n_frames):
+        _check_cp_codes(got_codes[f, 1:], c_lg[f])
