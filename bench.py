@@ -245,15 +245,15 @@ def run_talker_b1(args, ws, rank):
     rep = m.tts_bb_profile_report(h)
     m.tts_bb_profile(h, False)
 
-    # end to end through the public API with host buffers: per step, copy the
-    # ids from pinned host memory, run the step, read the argmax back
-    host_ids = torch.from_numpy(ids.copy()).pin_memory()
-    host_am = torch.zeros(1, dtype=torch.int32).pin_memory()
-    dev_row = torch.zeros(16, dtype=torch.int32, device="cuda")
-    dev_am = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # end to end through the C ABI with host buffers: per step, the ids go from pinned host memory
+    # to the device, the step runs, and its argmax (the token fed back) comes back to the host
+    host_ids_t = torch.from_numpy(ids.copy()).pin_memory()
+    host_am_t = torch.zeros(1, dtype=torch.int32).pin_memory()
+    host_ids, host_am = host_ids_t.numpy(), host_am_t.numpy()
     m.tts_bb_truncate(h, 0, P_PREFILL)
     first_host = int(first.cpu().item())
     n_e2e = min(args.steps, 4 * N_DECODE)
+    row_bytes = host_ids.strides[0]
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     nxt = first_host
@@ -263,12 +263,9 @@ def run_talker_b1(args, ws, rank):
             m.tts_bb_truncate(h, 0, P_PREFILL)
             nxt = first_host
         host_ids[t, 0] = nxt
-        dev_row.copy_(host_ids[t], non_blocking=True)
         kv[0] = pos
-        m.lib.tts_bb_decode_step(h, 1, slot.ctypes.data, kv.ctypes.data, dev_row.data_ptr(), 0, logits.data_ptr(),
-                                 dev_am.data_ptr(), None)
-        host_am.copy_(dev_am, non_blocking=True)
-        stream.synchronize()
+        m.lib.tts_bb_decode_step_host(h, 1, slot.ctypes.data, kv.ctypes.data, host_ids.ctypes.data + t * row_bytes, 0,
+                                      host_am.ctypes.data, None)
         nxt = int(host_am[0])
     e2e_s = time.perf_counter() - t0
     m.tts_bb_sync(h)
@@ -284,7 +281,8 @@ def run_talker_b1(args, ws, rank):
         "hbm_step_roofline": {"algorithmic_bytes_per_step": pos_bytes,
                               "achieved_gbs": pos_bytes / (ms_max / args.steps) / 1e6},
         "clocks": clk, "gpu_launches": int(launches),
-        "e2e": {"value": n_e2e / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 16 * 4, "d2h_bytes_per_step": 4},
+        "e2e": {"value": n_e2e / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 16 * 4, "d2h_bytes_per_step": 4 + 4,
+                "path": "tts_bb_decode_step_host: ids H2D, step, argmax + error word D2H, one sync per step"},
         "kernel_profile": rep,
     }
     return res, wl

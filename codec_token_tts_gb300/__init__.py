@@ -94,6 +94,7 @@ def _load() -> C.CDLL:
         "tts_bb_maskgit_update": (I, [P, I, I, P, I, I, I, P, I, I, I, I, C.c_float, C.c_float]),
         "tts_bb_maskgit_schedule": (I, [I, I, C.c_double, P]),
         "tts_bb_frame_step": (I, [P, P, I, P, P, P, P]),
+        "tts_bb_decode_step_host": (I, [P, I, P, P, P, I, P, P]),
         "tts_bb_rvq_create": (I, [I, I, I, I, C.POINTER(P), C.POINTER(P), C.POINTER(P), P, C.POINTER(P)]),
         "tts_bb_rvq_decode": (I, [P, I, I, P, P]),
         "tts_bb_rvq_sync": (I, [P]),
@@ -116,7 +117,8 @@ EXPORTED = ("tts_bb_default_config", "tts_bb_create", "tts_bb_free", "tts_bb_pre
             "tts_bb_launch_count", "tts_bb_profile", "tts_bb_profile_report",
             "tts_bb_gqa_decode_attention_static", "tts_bb_debug_fault", "tts_bb_maskgit_update",
             "tts_bb_maskgit_schedule", "tts_bb_frame_step", "tts_bb_rvq_create", "tts_bb_rvq_decode",
-            "tts_bb_rvq_sync", "tts_bb_rvq_free", "tts_bb_dac_create", "tts_bb_dac_decode", "tts_bb_dac_free")
+            "tts_bb_rvq_sync", "tts_bb_rvq_free", "tts_bb_dac_create", "tts_bb_dac_decode", "tts_bb_dac_free",
+            "tts_bb_decode_step_host")
 
 
 def _ptr(x) -> Optional[int]:

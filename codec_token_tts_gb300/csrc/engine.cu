@@ -216,6 +216,9 @@ struct tts_bb {
     int32_t *seq_slot = nullptr, *seq_start = nullptr, *seq_len = nullptr, *key_len = nullptr;
     bf16* mg_pool = nullptr;
     bool attn_bidir_tc = false;
+    int32_t* hx_ids = nullptr;  // tts_bb_decode_step_host: device copies of the caller's host ids and argmax
+    int32_t* hx_am = nullptr;
+    float* hx_logits = nullptr;
     // frame-loop scratch (on the Code Predictor's handle): Talker hidden, code 0, prefill input,
     // prefill ids, and the id rows of the 14 decode calls
     float* fr_hid = nullptr;
@@ -1230,6 +1233,39 @@ TTS_API tts_bb_status tts_bb_maskgit_pass(tts_bb* h, int B, int S, const int32_t
         L += launch_gemm(h->y, h->heads[0], B * Sa, N, HID, e, h->st, nullptr, h->err);
     }
     return finish(h);
+}
+
+TTS_API tts_bb_status tts_bb_decode_step_host(tts_bb* h, int B, const int32_t* slots, const int32_t* kv_lens,
+                                              const int32_t* ids, int head_idx, int32_t* argmax_out,
+                                              float* logits_out) {
+    if (!h) return TTS_BB_E_INVALID;
+    const tts_bb_config& c = h->cfg;
+    if (!ids || c.n_codebooks <= 0) return fail(h, TTS_BB_E_INVALID, "decode_step_host needs host ids and codebook tables");
+    if (B <= 0 || B > c.max_batch) return fail(h, TTS_BB_E_INVALID, "B=%d outside 1..%d", B, c.max_batch);
+    const int rows = std::max(c.head_rows, 1);
+    if (!h->hx_ids) {
+        cudaError_t e = dalloc(h, &h->hx_ids, (size_t)c.max_batch * c.n_codebooks);
+        if (e == cudaSuccess) e = dalloc(h, &h->hx_am, (size_t)c.max_batch);
+        if (e == cudaSuccess) e = dalloc(h, &h->hx_logits, (size_t)c.max_batch * rows);
+        if (e != cudaSuccess) return cuda_fail(h, e, "host-buffer staging");
+    }
+    cudaError_t e = cudaMemcpyAsync(h->hx_ids, ids, (size_t)B * c.n_codebooks * sizeof(int32_t), cudaMemcpyHostToDevice,
+                                    h->st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "ids copy");
+    const bool sync_errors = h->cfg.sync_errors;
+    h->cfg.sync_errors = 0;  // one synchronisation at the end, below
+    const tts_bb_status st = tts_bb_decode_step(h, B, slots, kv_lens, h->hx_ids, head_idx,
+                                                logits_out ? h->hx_logits : nullptr, argmax_out ? h->hx_am : nullptr,
+                                                nullptr);
+    h->cfg.sync_errors = sync_errors;
+    if (st != TTS_BB_OK) return st;
+    if (argmax_out &&
+        (e = cudaMemcpyAsync(argmax_out, h->hx_am, (size_t)B * sizeof(int32_t), cudaMemcpyDeviceToHost, h->st)) != cudaSuccess)
+        return cuda_fail(h, e, "argmax copy");
+    if (logits_out && (e = cudaMemcpyAsync(logits_out, h->hx_logits, (size_t)B * rows * sizeof(float),
+                                           cudaMemcpyDeviceToHost, h->st)) != cudaSuccess)
+        return cuda_fail(h, e, "logits copy");
+    return read_err(h);  // the error word's copy and the one stream synchronisation
 }
 
 TTS_API tts_bb_status tts_bb_frame_step(tts_bb* talker, tts_bb* cp, int B, const int32_t* slots,

@@ -186,6 +186,17 @@ tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots, const i
                                  const int32_t* ids, int head_idx, float* logits_out,
                                  int32_t* argmax_out, const tts_bb_opts* opts);
 
+/* tts_bb_decode_step with HOST buffers, for a caller that keeps its ids and
+ * reads each step's tokens on the host (a streaming loop): copies ids (host
+ * int32 [B][n_codebooks], pinned for an asynchronous copy) to the device, runs
+ * the step, copies argmax_out (host int32 [B] or NULL) and logits_out (host
+ * fp32 [B][head_rows] or NULL) back, and returns once they have landed (one
+ * stream synchronisation, which also reads the device error word). Other
+ * arguments and errors as in tts_bb_decode_step. Device staging for max_batch
+ * rows is allocated on the first call. */
+tts_bb_status tts_bb_decode_step_host(tts_bb* h, int B, const int32_t* slots, const int32_t* kv_lens,
+                                      const int32_t* ids, int head_idx, int32_t* argmax_out, float* logits_out);
+
 /* One full bidirectional MaskGIT pass without a KV cache (omnivoice-cpp,
  * MaskGIT decoder: every step is a full prefill with non-causal attention;
  * Component architecture: hybrid text/audio embedding and audio heads;

@@ -52,6 +52,7 @@ int main(void) {
     EXPECT(tts_bb_gqa_decode_attention_static(k, k, slots, 1, slots, TTS_BB_STATIC_ATTN_MAX_B + 1, 0, v, NULL) ==
            TTS_BB_E_INVALID);
     EXPECT(tts_bb_frame_step(NULL, NULL, 1, NULL, NULL, NULL, NULL) == TTS_BB_E_INVALID);
+    EXPECT(tts_bb_decode_step_host(NULL, 1, NULL, NULL, NULL, 0, NULL, NULL) == TTS_BB_E_INVALID);
     {
         tts_bb_rvq* r = NULL;
         EXPECT(tts_bb_rvq_create(8, 1024, 64, 1024, NULL, NULL, NULL, NULL, &r) == TTS_BB_E_INVALID && r == NULL);

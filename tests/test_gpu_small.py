@@ -335,3 +335,39 @@ def test_maskgit_pass_small_with_padding(attn, key_lens, monkeypatch):
             if kl > n_text:
                 err = np.max(np.abs(gl[b][:, :kl - n_text] - lo[b][:, :kl - n_text]))
                 assert err <= LOGIT_TOL, (b, err)
+
+
+@pytest.mark.parametrize("B", [1, 3])
+def test_decode_step_host_buffers_match_device_buffers(B):
+    """tts_bb_decode_step_host (host ids in, host argmax / logits out, one synchronisation) returns
+    bit for bit what tts_bb_decode_step returns on device buffers (B = 1 persistent path, B = 3 graph
+    path), over a few greedy steps."""
+    import codec_token_tts_gb300 as tbm
+    shape = small_talker(2)
+    w = synth.model_weights(shape, 81)
+    ids = synth.talker_prefill_ids(81, 8)
+    rows = synth.uniform_ids(synth.rng_for(81, "rows"), shape.codebook_rows, 4)
+    runs = []
+    for host in (False, True):
+        with Engine(w, max_slots=B, max_ctx=32, max_batch=B, max_tokens=8 * B) as e:
+            m = e.m
+            m.tts_bb_prefill(e.h, B, 8, list(range(B)), [8] * B, dev_i32(np.stack([ids] * B)))
+            got = []
+            for t in range(4):
+                step = np.ascontiguousarray(np.stack([rows[t]] * B).astype(np.int32))
+                sl, kl = np.arange(B, dtype=np.int32), np.full(B, 8 + t, np.int32)
+                if host:
+                    am = np.zeros(B, np.int32)
+                    lg = np.zeros((B, 3072), np.float32)
+                    st = tbm.lib.tts_bb_decode_step_host(e.h, B, sl.ctypes.data, kl.ctypes.data, step.ctypes.data, 0,
+                                                         am.ctypes.data, lg.ctypes.data)
+                    assert st == tbm.OK
+                else:
+                    amd = i32_full(B)
+                    lgd = f32_zeros(B, 3072)
+                    m.tts_bb_decode_step(e.h, B, list(range(B)), list(kl), dev_i32(step), 0, lgd, amd)
+                    am, lg = amd.cpu().numpy(), lgd.cpu().numpy()
+                got.append((am.copy(), lg.copy()))
+            runs.append(got)
+    for (a0, l0), (a1, l1) in zip(*runs):
+        assert np.array_equal(a0, a1) and np.array_equal(l0, l1)
