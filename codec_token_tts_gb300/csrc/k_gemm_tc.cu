@@ -337,13 +337,16 @@ __global__ void __launch_bounds__(tc::NT, 1)
     }
 }
 
-// ---------------------------------------------------------------- decode batches (8 < T <= 128)
+// ---------------------------------------------------------------- decode batches (8 < T <= 256)
 // Y = (X_hi + X_lo) W^T for a handful of tokens, weights streamed once. The
 // roles swap so the weights fill the 128-row M side: A = a 128-row tile of W,
 // B = the tokens' high parts (rows 0..TB-1) stacked on their low parts
-// (rows TB..2TB-1), N = 2 TB. The S CTAs of one thread-block cluster split K
-// for one 128-row tile; each sums hi + lo per token into its shared memory.
-// After a cluster barrier, CTA r owns tokens [r T / S, (r+1) T / S): every
+// (rows TB..2TB-1), N = 2 TB. TB is at most 128 (N <= 256), so a grid row
+// takes one block of up to 128 tokens; a launch over 129..256 tokens has two
+// grid rows (or is issued as two launches, one per block). The S CTAs of one
+// thread-block cluster split K for one 128-row tile and one token block; each
+// sums hi + lo per token into its shared memory. After a cluster barrier,
+// CTA r owns the block's tokens [r T / S, (r+1) T / S): every
 // CTA pushes each peer's token slice of its partial with one bulk copy into
 // that peer's receive buffer (completion on the peer's mbarrier); the owner
 // adds the S partials in rank order (deterministic) and applies the epilogue,
@@ -449,8 +452,8 @@ __device__ __forceinline__ void tcd_reduce(const TcdOut o, const float* __restri
 
 __global__ void __launch_bounds__(tcd::NT, 1)
     k_gemm_tcd(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmXh,
-               const __grid_constant__ CUtensorMap tmXl, int T, int TB, int N, int K, const __grid_constant__ Epi e,
-               int* err) {
+               const __grid_constant__ CUtensorMap tmXl, int T, int TB, int tb_base, int N, int K,
+               const __grid_constant__ Epi e, int* err) {
     using namespace tcd;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -469,6 +472,8 @@ __global__ void __launch_bounds__(tcd::NT, 1)
     asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(S));
     asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     const int n0 = (int)(blockIdx.x / S) * BM;
+    // this CTA's tokens: [tb0, tb0 + Th), one block of up to MAXTB per grid row
+    const int tb0 = tb_base + (int)blockIdx.y * MAXTB, Th = min(T - tb0, MAXTB);
     const int KT = K / BK, kb0 = (int)(r * KT / S), nk = (int)((r + 1) * KT / S) - kb0;
     const uint32_t b_bytes = 2u * TB * BK * 2, ncols = 2u * TB;
     const uint32_t tcols = ncols <= 32 ? 32 : ncols <= 64 ? 64 : ncols <= 128 ? 128 : 256;
@@ -524,8 +529,8 @@ __global__ void __launch_bounds__(tcd::NT, 1)
                                  : "memory");
                     tma_load_2d(st, &tmW, kx, n0, full + s);
                 }
-                tma_load_2d(st + A_BYTES, &tmXh, kx, 0, full + s);
-                tma_load_2d(st + A_BYTES + TB * BK * 2, &tmXl, kx, 0, full + s);
+                tma_load_2d(st + A_BYTES, &tmXh, kx, tb0, full + s);
+                tma_load_2d(st + A_BYTES + TB * BK * 2, &tmXl, kx, tb0, full + s);
                 ++issued;
             }
             if (*abort_s && issued < pre) issued = pre;  // weight tiles already requested must land too
@@ -596,7 +601,7 @@ __global__ void __launch_bounds__(tcd::NT, 1)
         }
     }
     // tokens owned by CTA q: [tok(q), tok(q + 1))
-    auto tok = [&](uint32_t q) { return (int)(q * (uint32_t)T / S); };
+    auto tok = [&](uint32_t q) { return (int)(q * (uint32_t)Th / S); };
     const int t0 = tok(r), t1 = tok(r + 1);
     if (threadIdx.x == 0)  // expect the S - 1 peers' slices of this CTA's tokens
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(recvb)),
@@ -622,10 +627,11 @@ __global__ void __launch_bounds__(tcd::NT, 1)
         const bool got = t1 == t0 || S == 1 || tc_wait(recvb, 0, abort_s);
         if (!got && lane == 0 && warp == 2) set_err(err, ERR_TIMEOUT);
         TcdOut o;
-        o.f32 = reinterpret_cast<float*>(e.out);
-        o.hi = reinterpret_cast<bf16*>(e.out);
-        o.lo = reinterpret_cast<bf16*>(e.out_lo);
-        o.amax = e.amax;
+        const size_t orow = (size_t)tb0 * e.ldo;
+        o.f32 = e.out ? reinterpret_cast<float*>(e.out) + orow : nullptr;
+        o.hi = e.out ? reinterpret_cast<bf16*>(e.out) + orow : nullptr;
+        o.lo = e.out_lo ? reinterpret_cast<bf16*>(e.out_lo) + orow : nullptr;
+        o.amax = e.amax ? e.amax + tb0 : nullptr;
         o.ldo = e.ldo;
         const int w = warp - 2;
         switch (e.mode) {
@@ -1112,9 +1118,10 @@ int launch_attn_bidir_tc(const bf16* q, const bf16* pool, size_t pool_blocks, in
 
 int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N, int K, const Epi& e, int* err,
                     cudaStream_t st) {
-    if (T <= 0 || T > tcd::MAXTB || N <= 0 || K % tcd::BK != 0 || !X_lo) return 0;
+    if (T <= 0 || T > 2 * tcd::MAXTB || N <= 0 || K % tcd::BK != 0 || !X_lo) return 0;
     if (e.mode != EPI_STORE_F32 && e.mode != EPI_ADD_F32 && e.mode != EPI_SWIGLU && e.mode != EPI_LOGITS) return 0;
-    const int TB = (T + 15) / 16 * 16;
+    const int blocks = (T + tcd::MAXTB - 1) / tcd::MAXTB;  // token blocks of up to 128
+    const int TB = blocks > 1 ? tcd::MAXTB : (T + 15) / 16 * 16;
     CUtensorMap mw, mh, ml;
     if (!make_map(&mw, W, N, K, tcd::BM) || !make_map(&mh, X, T, K, TB) || !make_map(&ml, X_lo, T, K, TB)) return 0;
     // clusters of each size that fit at once (1 CTA per SM): S is chosen so all clusters run in one wave
@@ -1143,27 +1150,45 @@ int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N
         cudaGetLastError();
     }
     const int tiles = (N + tcd::BM - 1) / tcd::BM, KT = K / tcd::BK;
-    int S = 1, best = 0;
-    for (int i = 0; i < 8; ++i)  // the most CTAs whose clusters all fit in one wave
-        if (cand[i] <= KT && tiles <= fit[i] && tiles * cand[i] > best) {
-            best = tiles * cand[i];
-            S = cand[i];
-        }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(tiles * S);
-    cfg.blockDim = dim3(tcd::NT);
-    cfg.dynamicSmemBytes = tcd::SMEM;
-    cfg.stream = st;
-    cudaLaunchAttribute at[2];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = S;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_gemm_tcd, mw, mh, ml, T, TB, N, K, e, err) == cudaSuccess ? 1 : 0;
+    // the most CTAs whose clusters (one per weight tile and token block) all fit in one wave
+    auto pick = [&](int clusters, int& S) {
+        int best = 0;
+        S = 1;
+        for (int i = 0; i < 8; ++i)
+            if (cand[i] <= KT && clusters <= fit[i] && clusters * cand[i] > best) {
+                best = clusters * cand[i];
+                S = cand[i];
+            }
+        return best;
+    };
+    int S1 = 1, S2 = 1;
+    const int one = pick(tiles, S1);
+    // both token blocks in one launch when that keeps as many CTAs busy as a launch per block
+    const bool joint = blocks > 1 && pick(tiles * blocks, S2) >= one;
+    auto go = [&](int S, int rows, int tb_base) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(tiles * S, rows);
+        cfg.blockDim = dim3(tcd::NT);
+        cfg.dynamicSmemBytes = tcd::SMEM;
+        cfg.stream = st;
+        cudaLaunchAttribute at[2];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = S;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 2;
+        return cudaLaunchKernelEx(&cfg, k_gemm_tcd, mw, mh, ml, T, TB, tb_base, N, K, e, err) == cudaSuccess;
+    };
+    if (joint) return go(S2, blocks, 0) ? 1 : 0;
+    int n = 0;
+    for (int b = 0; b < blocks; ++b) {
+        if (!go(S1, 1, b * tcd::MAXTB)) return n;
+        ++n;
+    }
+    return n;
 }
 
 

@@ -517,19 +517,8 @@ int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e,
     if (T <= 0) return 0;
     if (T <= 8) return launch_gemv(X, W, T, N, K, e, st, X_lo);
     if (X_lo && T <= 256 && gemm_tc_available()) {
-        // up to 128 tokens per launch (N = 2T <= 256); a second launch takes tokens 128.. and
-        // streams the weights again (still far faster than the mma.sync split-K path)
-        int n = 0;
-        for (int t0 = 0; t0 < T; t0 += 128) {
-            Epi eh = e;
-            const size_t off = (size_t)t0 * e.ldo;
-            if (e.out) eh.out = e.mode == EPI_SWIGLU ? (void*)(static_cast<bf16*>(e.out) + off) : (void*)(static_cast<float*>(e.out) + off);
-            if (e.out_lo) eh.out_lo = static_cast<bf16*>(e.out_lo) + off;
-            if (e.amax) eh.amax = e.amax + t0;
-            const int k = launch_gemm_tcd(X + (size_t)t0 * K, X_lo + (size_t)t0 * K, W, std::min(128, T - t0), N, K, eh, err, st);
-            if (!k && t0 == 0) break;  // shape or epilogue not supported: use the paths below
-            n += k;
-        }
+        // up to 256 tokens as one or two 128-token blocks (N = 2 x block <= 256 per MMA)
+        const int n = launch_gemm_tcd(X, X_lo, W, T, N, K, e, err, st);
         if (n) return n;
     }
     if (X_lo && skw) {

@@ -300,6 +300,42 @@ def test_code_predictor_frame_small_batch():
             check_logits_and_argmax(gl[:, f], ref[f][1], got_codes[f], ref[f][0], min_agree=0.9)
 
 
+@pytest.mark.parametrize("F", [100, 150])
+def test_code_predictor_frames_over_128_tokens(F):
+    """Batches above 128 tokens run the decode GEMMs as two token blocks: F = 100 gives a 200-token
+    prefill (blocks of 128 + 72), F = 150 a 150-token decode (128 + 22). The GPU chains its own
+    codes through the argmax outputs; the oracle replays them."""
+    shape = synth.ModelShape(n_layers=2, codebook_rows=(3072,) + (2048,) * 15, n_heads_out=15, head_rows=2048)
+    w = synth.model_weights(shape, 27)
+    r = synth.rng_for(27, "cp_blocks")
+    th = synth.normal_bf16(r, (F, 1024), 1.0)
+    code0 = r.integers(0, 3072, size=F).astype(np.int32)
+    with Engine(w, max_slots=F, max_ctx=17, max_batch=F, max_tokens=2 * F) as e:
+        m = e.m
+        emb = np.zeros((F, 2, 1024), np.uint16)
+        emb[:, 0] = th
+        ids = -np.ones((F, 2, 16), np.int32)
+        ids[:, 1, 0] = code0
+        steps = i32_full(16 * F * 16, -1).view(16, F, 16)  # call j reads steps[j]; column j carries code j
+        logits = f32_zeros(F, 2048)
+        m.tts_bb_prefill(e.h, F, 2, list(range(F)), [2] * F, dev_i32(ids), 0, logits, steps[1, :, 1],
+                         embeds=dev_bf16_bits(emb), argmax_stride=16)
+        gl = [logits.cpu().numpy().copy()]
+        for j in range(1, 15):
+            m.tts_bb_decode_step(e.h, F, list(range(F)), [j + 1] * F, steps[j], j, logits, steps[j + 1, :, j + 1],
+                                 argmax_stride=16)
+            gl.append(logits.cpu().numpy().copy())
+        s = steps.cpu().numpy()
+    got_codes = np.stack([s[j + 1, :, j + 1] for j in range(15)], axis=1)  # [F, 15]: codes 1..15
+    gl = np.array(gl)                                                       # [15, F, 2048]
+    m0 = O.Backbone(w, shape)
+    o_codes, o_logits = O.code_predictor_frames(m0, O.bf16_to_f64(th), code0, forced=got_codes)
+    assert np.all((got_codes >= 0) & (got_codes < 2048))
+    # every row: logits within tolerance, flips only at oracle near-ties; raw agreement over all rows
+    check_logits_and_argmax(gl.transpose(1, 0, 2).reshape(-1, 2048), o_logits.reshape(-1, 2048),
+                            got_codes.reshape(-1), o_codes.reshape(-1))
+
+
 # ---------------------------------------------------------------- MaskGIT bidirectional pass
 @pytest.mark.parametrize("attn", ["tcgen05", "mma"])
 @pytest.mark.parametrize("key_lens", [(200, 150), (70, 129)])
