@@ -22,9 +22,12 @@ __device__ __forceinline__ const bf16* kv_tile(const KVView& kv, int seq, int j,
 // ---------------------------------------------------------------- decode
 // grid (n_splits, 8, B), 128 threads. Warp w takes keys 16w..16w+15 of every
 // block of the split; lane l holds head elements 4l..4l+3 of both query heads.
+// With one split the CTA writes the normalised output itself (what the
+// combine would compute: its weight for a single split is exactly 1).
 __global__ void __launch_bounds__(128) k_attn_decode(const bf16* __restrict__ q, KVView kv,
                                                      const int32_t* __restrict__ seq_start, int bps,
-                                                     int n_splits, float* __restrict__ part) {
+                                                     int n_splits, float* __restrict__ part,
+                                                     bf16* __restrict__ out, bf16* __restrict__ out_lo) {
     pdl_wait();  // upstream results are read below
     pdl_trigger();
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -131,6 +134,17 @@ __global__ void __launch_bounds__(128) k_attn_decode(const bf16* __restrict__ q,
         a += sm_o[w][hh][e0] * f;
         c += sm_o[w][hh][e0 + 1] * f;
     }
+    if (n_splits == 1) {
+        const size_t o = ((size_t)b * NQ + 2 * g + hh) * HD + e0;
+        const float r0 = l > 0.f ? a / l : 0.f, r1 = l > 0.f ? c / l : 0.f;
+        out[o] = f2bf(r0);
+        out[o + 1] = f2bf(r1);
+        if (out_lo) {
+            out_lo[o] = f2bf_lo(r0);
+            out_lo[o + 1] = f2bf_lo(r1);
+        }
+        return;
+    }
     // part layout per (b, head, split): [HD] o, then m, l
     float* dst = part + (((size_t)b * NQ + 2 * g + hh) * n_splits + split) * (HD + 2);
     dst[e0] = a;
@@ -169,7 +183,8 @@ int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B
     splits = max(1, min(splits, min(nblk, max_splits)));
     const int bps = (nblk + splits - 1) / splits;
     splits = (nblk + bps - 1) / bps;
-    launch_pdl(k_attn_decode, dim3(splits, NKV, B), 128, 0, st, q, kv, seq_start, bps, splits, part);
+    launch_pdl(k_attn_decode, dim3(splits, NKV, B), 128, 0, st, q, kv, seq_start, bps, splits, part, out, out_lo);
+    if (splits == 1) return 1;
     launch_pdl(k_attn_combine, B * NQ, 128, 0, st, part, splits, out, out_lo);
     return 2;
 }
