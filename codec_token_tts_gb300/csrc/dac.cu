@@ -260,8 +260,8 @@ TTS_API tts_bb_status tts_bb_dac_create(const tts_bb_dac_weights* w, void* strea
 
 TTS_API tts_bb_status tts_bb_dac_decode(tts_bb_dac* d, int B, int T, const float* features, float* audio) {
     if (!d || B < 1 || T < 1 || !features || !audio) return TTS_BB_E_INVALID;
-    if ((size_t)B * T * 960 > (size_t)INT32_MAX) return TTS_BB_E_INVALID;
-    // largest activation: 32 channels x 960 T (block 4) = 64 channels x 480 T... = 30720 T per item
+    if (B > 65535 || (size_t)B * T * 960 > (size_t)INT32_MAX) return TTS_BB_E_INVALID;  // grid z = B
+    // largest activation: block 4's output, 32 channels x 960 T samples = 30720 T floats per item
     const size_t need = (size_t)B * T * 30720;
     if (need > d->buf_elems) {
         cudaStreamSynchronize(d->st);

@@ -340,7 +340,8 @@ tts_bb_status tts_bb_dac_create(const tts_bb_dac_weights* w, void* stream, tts_b
 /* features device fp32 [B][T][1024] (the RVQ decode output); audio device fp32
  * [B][960 T]. Asynchronous on the handle's stream (38 kernel launches); three
  * activation buffers of 30720 T floats per item are allocated on the first
- * call that needs more. TTS_BB_E_INVALID for bad sizes or NULL buffers. */
+ * call that needs more. TTS_BB_E_INVALID for NULL buffers, B < 1 or B > 65535,
+ * T < 1, or B x 960 T above 2^31 - 1 samples. */
 tts_bb_status tts_bb_dac_decode(tts_bb_dac* d, int B, int T, const float* features, float* audio);
 /* Wait and free. NULL is a no-op. */
 void tts_bb_dac_free(tts_bb_dac* d);

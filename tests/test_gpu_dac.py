@@ -75,5 +75,8 @@ def test_dac_rejects_bad_arguments():
         assert m.tts_bb_dac_decode(d, 0, 1, x, a, check=False) == m.E_INVALID
         assert m.tts_bb_dac_decode(d, 1, 0, x, a, check=False) == m.E_INVALID
         assert m.tts_bb_dac_decode(d, 1, 1, None, a, check=False) == m.E_INVALID
+        # rejected on the host before anything is allocated or launched
+        assert m.tts_bb_dac_decode(d, 65536, 1, x, a, check=False) == m.E_INVALID
+        assert m.tts_bb_dac_decode(d, 1, 2_300_000, x, a, check=False) == m.E_INVALID
     finally:
         m.tts_bb_dac_free(d)
