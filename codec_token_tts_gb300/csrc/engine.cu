@@ -1349,9 +1349,10 @@ TTS_API tts_bb_status tts_bb_maskgit_update(tts_bb* h, int n_items, int T, const
         return fail(h, TTS_BB_E_INVALID, "maskgit_update needs audio heads of 2..%d ids", mg_max_vocab());
     if (n_items < 1 || T < 1 || n_unmask < 0 || !logits || !ids)
         return fail(h, TTS_BB_E_INVALID, "maskgit_update: bad sizes or NULL buffers");
-    if (cond_pos0 < 0 || uncond_pos0 < 0 || cond_pos0 + T > S_logits || uncond_pos0 + T > S_logits)
+    if (cond_pos0 < 0 || uncond_pos0 < 0 || (long long)cond_pos0 + T > S_logits || (long long)uncond_pos0 + T > S_logits)
         return fail(h, TTS_BB_E_INVALID, "maskgit_update: logits windows outside S_logits=%d", S_logits);
-    if (cond_ids_pos0 < 0 || uncond_ids_pos0 < 0 || cond_ids_pos0 + T > S_ids || uncond_ids_pos0 + T > S_ids)
+    if (cond_ids_pos0 < 0 || uncond_ids_pos0 < 0 || (long long)cond_ids_pos0 + T > S_ids ||
+        (long long)uncond_ids_pos0 + T > S_ids)
         return fail(h, TTS_BB_E_INVALID, "maskgit_update: id windows outside S_ids=%d", S_ids);
     const size_t cells = (size_t)n_items * c.n_heads * T;
     if (cells > (size_t)INT32_MAX / 2) return fail(h, TTS_BB_E_INVALID, "maskgit_update: too many cells");
@@ -1392,7 +1393,7 @@ TTS_API tts_bb_status tts_bb_maskgit_schedule(int num_step, int n_total, double 
 TTS_API tts_bb_status tts_bb_debug_kv_read(tts_bb* h, int layer, int slot, int pos0, int n, void* k_out, void* v_out) {
     if (!h) return TTS_BB_E_INVALID;
     if (h->cfg.max_slots <= 0 || layer < 0 || layer >= h->cfg.n_layers || slot < 0 || slot >= h->cfg.max_slots ||
-        pos0 < 0 || n < 0 || pos0 + n > h->slot_len[slot] || !k_out || !v_out)
+        pos0 < 0 || n < 0 || (long long)pos0 + n > h->slot_len[slot] || !k_out || !v_out)
         return fail(h, TTS_BB_E_INVALID, "debug_kv_read: bad arguments");
     if (n == 0) return TTS_BB_OK;
     {
@@ -1409,7 +1410,7 @@ TTS_API tts_bb_status tts_bb_debug_kv_write(tts_bb* h, int layer, int slot, int 
                                            const void* v) {
     if (!h) return TTS_BB_E_INVALID;
     if (h->cfg.max_slots <= 0 || layer < 0 || layer >= h->cfg.n_layers || slot < 0 || slot >= h->cfg.max_slots ||
-        pos0 < 0 || n < 0 || pos0 > h->slot_len[slot] || pos0 + n > h->cfg.max_ctx || !k || !v)
+        pos0 < 0 || n < 0 || pos0 > h->slot_len[slot] || (long long)pos0 + n > h->cfg.max_ctx || !k || !v)
         return fail(h, TTS_BB_E_INVALID, "debug_kv_write: bad arguments");
     if (n == 0) return TTS_BB_OK;
     const int new_len = std::max(h->slot_len[slot], pos0 + n);

@@ -138,7 +138,9 @@ def test_update_rejects_bad_windows(eng):
     lg = f32_zeros(2, K, 10, V)
     ids = torch.zeros(2, K, 10, dtype=torch.int32, device="cuda")
     for args in ((1, 10, lg, 10, 1, 0, ids, 10, 0, 0, 5), (1, 10, lg, 10, 0, 0, ids, 10, 0, 1, 5),
-                 (0, 10, lg, 10, 0, 0, ids, 10, 0, 0, 5), (1, 10, lg, 10, 0, 0, ids, 10, 0, 0, -1)):
+                 (0, 10, lg, 10, 0, 0, ids, 10, 0, 0, 5), (1, 10, lg, 10, 0, 0, ids, 10, 0, 0, -1),
+                 # window starts whose end would wrap around a 32-bit int
+                 (1, 10, lg, 10, 2**31 - 5, 0, ids, 10, 0, 0, 5), (1, 10, lg, 10, 0, 0, ids, 10, 0, 2**31 - 5, 5)):
         assert m.tts_bb_maskgit_update(eng.h, *args, check=False) == m.E_INVALID
 
 
