@@ -2,11 +2,13 @@
 // block pool and page tables, per-call validation, and the layer schedule of
 // the backbone step (Talker / Code-Predictor prefill and decode, MaskGIT pass).
 #include <algorithm>
+#include <climits>
 #include <cstdarg>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <new>
 #include <string>
 #include <vector>
 
@@ -323,6 +325,8 @@ cudaError_t dalloc(tts_bb* h, T** p, size_t n) {
     return e;
 }
 
+constexpr int MAX_CFG_LEN = 1 << 20;
+
 bool cfg_supported(const tts_bb_config& c, std::string& why) {
     if (c.hidden != HID || c.n_q_heads != NQ || c.n_kv_heads != NKV || c.head_dim != HD) {
         why = "kernels are built for hidden 1024, 16 q / 8 kv heads of 128";
@@ -330,6 +334,10 @@ bool cfg_supported(const tts_bb_config& c, std::string& why) {
     }
     if (c.ffn % 256 != 0 || c.ffn <= 0 || c.ffn > 3072) {
         why = "ffn must be a positive multiple of 256, at most 3072";
+        return false;
+    }
+    if (c.max_ctx > MAX_CFG_LEN || c.max_tokens > MAX_CFG_LEN || c.max_slots > MAX_CFG_LEN) {
+        why = "max_ctx, max_tokens and max_slots are limited to 2^20";  // host tables scale with them
         return false;
     }
     return true;
@@ -713,7 +721,10 @@ TTS_API void tts_bb_free(tts_bb* h) {
     delete h;
 }
 
-TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weights* w, void* stream, tts_bb** out) {
+// The body of tts_bb_create; `made` holds the handle once it exists, so a
+// host allocation failure (std::bad_alloc) can free it at the C boundary.
+static tts_bb_status create_impl(const tts_bb_config* cfg, const tts_bb_weights* w, void* stream, tts_bb** out,
+                                 tts_bb*& made) {
     if (out) *out = nullptr;
     if (!cfg || !w || !out) return TTS_BB_E_INVALID;
     const tts_bb_config& c = *cfg;
@@ -739,6 +750,7 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
             if (!w->layer[l * TTS_BB_LAYER_TENSORS + r]) return TTS_BB_E_INVALID;
 
     tts_bb* h = new tts_bb();
+    made = h;
     h->cfg = c;
     h->st = reinterpret_cast<cudaStream_t>(stream);
     cudaGetDevice(&h->dev);
@@ -828,8 +840,13 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
     // KV pool [layer][block][K|V][8][64][128]
     if (c.max_slots > 0) {
         h->mbps = (c.max_ctx + KVB - 1) / KVB;
-        h->kv_blocks = c.kv_blocks > 0 ? c.kv_blocks : c.max_slots * h->mbps;
-        if (const char* cap = std::getenv("TTS_BB_MAX_BLOCKS")) h->kv_blocks = std::min(h->kv_blocks, std::atoi(cap));
+        long long nblk = c.kv_blocks > 0 ? (long long)c.kv_blocks : (long long)c.max_slots * h->mbps;
+        if (const char* cap = std::getenv("TTS_BB_MAX_BLOCKS")) {
+            const long long v = std::atoll(cap);
+            if (v > 0) nblk = std::min(nblk, v);
+        }
+        if (nblk > INT32_MAX) return bail(TTS_BB_E_UNSUPPORTED);  // physical block ids are int32
+        h->kv_blocks = (int)nblk;
         h->layer_elems = (size_t)h->kv_blocks * 2 * NKV * KVB * HD;
         if ((e = dalloc(h, &h->pool, h->layer_elems * c.n_layers)) != cudaSuccess) return bail(TTS_BB_E_OOM);
         if ((e = dalloc(h, &h->d_page_table, (size_t)c.max_slots * h->mbps)) != cudaSuccess) return bail(TTS_BB_E_OOM);
@@ -930,6 +947,17 @@ TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weigh
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return bail(cuda_fail(h, e, "create"));
     *out = h;
     return TTS_BB_OK;
+}
+
+TTS_API tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weights* w, void* stream, tts_bb** out) {
+    tts_bb* made = nullptr;
+    try {
+        return create_impl(cfg, w, stream, out, made);
+    } catch (const std::bad_alloc&) {  // no exception crosses the C boundary
+        if (made) tts_bb_free(made);
+        if (out) *out = nullptr;
+        return TTS_BB_E_OOM;
+    }
 }
 
 TTS_API int tts_bb_slot_len(const tts_bb* h, int slot) {

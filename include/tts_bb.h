@@ -87,11 +87,11 @@ typedef struct {
     int n_heads;
     int head_rows;
     /* KV cache: paged, TTS_BB_KV_BLOCK tokens per block. */
-    int max_slots;         /* concurrent sequences (stream slots) */
-    int max_ctx;           /* longest sequence, tokens */
+    int max_slots;         /* concurrent sequences (stream slots), at most 2^20 */
+    int max_ctx;           /* longest sequence, tokens, at most 2^20 */
     int kv_blocks;         /* physical blocks; 0 = max_slots * ceil(max_ctx / 64) */
     int max_batch;         /* largest B of one call (scratch sizing) */
-    int max_tokens;        /* largest B*S of one prefill / MaskGIT call */
+    int max_tokens;        /* largest B*S of one prefill / MaskGIT call, at most 2^20 */
     int sync_errors;       /* 1 = each call synchronises to report device errors */
 } tts_bb_config;
 
@@ -146,7 +146,9 @@ void tts_bb_default_config(tts_bb_config* cfg);
  * (NULL = the legacy default stream) on which every call of the handle runs.
  * Allocates the weights, the KV block pool and scratch. Returns
  * TTS_BB_E_INVALID for a bad config, TTS_BB_E_UNSUPPORTED for a shape the
- * kernels are not built for, TTS_BB_E_OOM when device memory runs out. */
+ * kernels are not built for (or max_slots, max_ctx, max_tokens above 2^20),
+ * TTS_BB_E_OOM when device or host memory runs out. No exception leaves the
+ * call. */
 tts_bb_status tts_bb_create(const tts_bb_config* cfg, const tts_bb_weights* w,
                             void* stream, tts_bb** out);
 

@@ -61,6 +61,11 @@ def test_create_rejects_bad_and_unsupported_configs_before_touching_the_device()
     c.ffn = 4096  # the kernels are built for SwiGLU widths up to 3072
     st, h = _create_status(m, c, wref)
     assert st == m.E_UNSUPPORTED and not h
+    for field in ("max_ctx", "max_tokens", "max_slots"):  # host tables scale with these: capped at 2^20
+        c = config_for(shape)
+        setattr(c, field, (1 << 20) + 1)
+        st, h = _create_status(m, c, wref)
+        assert st == m.E_UNSUPPORTED and not h, field
     c = config_for(shape)
     st, h = _create_status(m, c, m.Weights(1, [dict(w.layers[0], wk=None)], w.codebooks, w.final_norm, w.heads))
     assert st == m.E_INVALID and not h
