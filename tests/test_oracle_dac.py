@@ -123,6 +123,29 @@ def test_dac_pins():
     assert check_snake()
 
 
+def test_convolutions_match_pytorch_cpu_ops():
+    """The page's layers are PyTorch's Conv1d and ConvTranspose1d: the library's own
+    float64 CPU ops give the same result for the five upsampling blocks (k 2r, stride r,
+    padding ceil(r/2), output padding r mod 2) and the dilated k = 7 convolutions."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    rng = np.random.default_rng(6)
+    for r in O.DAC_RATIOS:
+        x, w, b = rng.normal(size=(4, 9)), rng.normal(size=(4, 3, 2 * r)), rng.normal(size=3)
+        want = F.conv_transpose1d(torch.from_numpy(x)[None], torch.from_numpy(w), torch.from_numpy(b), stride=r,
+                                  padding=math.ceil(r / 2), output_padding=r % 2)[0].numpy()
+        got = O.conv_transpose1d(x, w, b, r, math.ceil(r / 2), r % 2)
+        assert got.shape == want.shape == (3, 9 * r)
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+    for dil in O.DAC_DILATIONS:
+        x, w, b = rng.normal(size=(4, 40)), rng.normal(size=(3, 4, 7)), rng.normal(size=3)
+        want = F.conv1d(torch.from_numpy(x)[None], torch.from_numpy(w), torch.from_numpy(b), padding=3 * dil,
+                        dilation=dil)[0].numpy()
+        got = O.conv1d(x, w, b, dil, 3 * dil)
+        assert got.shape == want.shape == (3, 40)
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
 def test_dac_chain_with_identity_residual_units():
     """Zero residual weights make every residual unit the identity: the decode is
     fc2, conv1, then per block ConvTranspose(snake(x)), then snake + conv2; 960 T samples."""
