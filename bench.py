@@ -76,14 +76,21 @@ def dist_max(ws, x: float) -> float:
 
 
 # ---------------------------------------------------------------- clocks
+def this_rank_gpu() -> str:
+    """The physical GPU of this rank (cuda:LOCAL_RANK) as nvidia-smi names it."""
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    vis = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    return vis[local] if local < len(vis) else str(local)
+
+
 class ClockSampler:
     """Samples nvidia-smi clocks and throttle reasons during the timed region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.idx = gpu_index
+    def __init__(self, gpu: str):
+        self.idx = gpu  # nvidia-smi -i: index or UUID
         self.proc = None
         self.lines = []
 
@@ -223,7 +230,7 @@ def run_talker_b1(args, ws, rank):
     steps(args.warmup)
     m.tts_bb_sync(h)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or 0))
+    clocks = ClockSampler(this_rank_gpu())
     n0 = m.tts_bb_launch_count(h)
     dist_barrier(ws)
     torch.cuda.synchronize()

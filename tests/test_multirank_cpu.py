@@ -65,3 +65,18 @@ def test_reference_arm_under_torchrun_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_clock_sampler_watches_this_ranks_gpu(monkeypatch):
+    """Each rank samples the clocks of its own device (cuda:LOCAL_RANK), named as nvidia-smi names it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "4,5,6,7")
+    monkeypatch.setenv("LOCAL_RANK", "2")
+    assert bench.this_rank_gpu() == "6"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "GPU-aaa, GPU-bbb")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+    assert bench.this_rank_gpu() == "GPU-bbb"
+    monkeypatch.delenv("CUDA_VISIBLE_DEVICES")
+    monkeypatch.setenv("LOCAL_RANK", "3")
+    assert bench.this_rank_gpu() == "3"
