@@ -410,8 +410,7 @@ const char* tts_bb_profile_report(tts_bb* h);
 
 /* Decode attention that allocates nothing (the pages have no counterpart: it
  * exists for callers of this library that may not call cudaMalloc — a plug-in
- * whose host framework owns every device allocation, work recorded during
- * CUDA stream capture where cudaMalloc is not allowed, or a real-time audio
+ * whose host framework owns every device allocation, or a real-time audio
  * thread that must not block in the allocator).
  *
  * It runs the same split-K GQA flash-decode kernels as tts_bb_decode_step on
@@ -427,13 +426,17 @@ const char* tts_bb_profile_report(tts_bb* h);
  *               64-token block of sequence b
  *   positions   device int32 [B]: position of the query token of sequence b;
  *               its K/V must already be in the pool, attention covers
- *               positions 0..positions[b]
+ *               positions 0..positions[b]. Values outside 0..max_position
+ *               are clamped into that range on the device before any read
+ *               (so no access leaves the caller's page-table rows); the
+ *               output of such a sequence is then not meaningful
  *   max_position the largest value in positions (host int)
  *   out         device bf16 [B][16][128]
  *   stream      cudaStream_t (NULL = legacy default stream)
  * Returns TTS_BB_E_INVALID for NULL pointers, B outside
  * 1..TTS_BB_STATIC_ATTN_MAX_B or a max_position the page table cannot hold;
- * TTS_BB_E_CUDA if a launch fails. The first call on a device looks up the
+ * TTS_BB_E_CUDA if a CUDA error is already pending when the call starts (it
+ * is left pending, not cleared) or a launch fails. The first call on a device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current:
  * make that first call before any stream capture. Every call shares the
  * array and overwrites all the partials it reads, so nothing needs clearing
