@@ -1,4 +1,6 @@
-"""Oracle of the RVQ codec's decode (codes -> 1024-d frame features).
+"""Oracles of the codec quantizer lookups: the OmniVoice RVQ decode (codes ->
+1024-d frame features) and the Qwen3-TTS split quantizer (codes -> the
+512-channel hidden of its codec body).
 
 TEST INFRASTRUCTURE ONLY: see the package docstring.
 
@@ -18,7 +20,7 @@ from typing import Sequence
 
 import numpy as np
 
-__all__ = ["rvq_decode"]
+__all__ = ["rvq_decode", "split_quantizer_decode"]
 
 
 def rvq_decode(codes: np.ndarray, embed: Sequence[np.ndarray], proj_w: Sequence[np.ndarray],
@@ -36,3 +38,31 @@ def rvq_decode(codes: np.ndarray, embed: Sequence[np.ndarray], proj_w: Sequence[
         p_k = e_k @ np.asarray(proj_w[k], np.float64).T + np.asarray(proj_b[k], np.float64)
         out += p_k
     return out
+
+
+def split_quantizer_decode(codes: np.ndarray, codebooks: Sequence[np.ndarray], proj_semantic: np.ndarray,
+                           proj_acoustic: np.ndarray) -> np.ndarray:
+    """The Qwen3-TTS codec's quantizer lookup: codes -> the [B, out, T] float hidden.
+
+    Source: "Qwen3-TTS ncnn port", Codec Decoder split, steps 1-4: the 16
+    codebooks and two projection weights are read; each frame looks up one
+    row per codebook; the first (semantic) codebook and the other 15
+    (acoustic) codebooks are projected separately and the two projections
+    are summed; the result [B, 512, T] feeds the codec body.
+
+    Readings (the page prints neither the codebook width nor the projection
+    form): each projection is a bias-free linear map [out, d] (a 1x1
+    convolution), the acoustic group's rows are summed before its projection
+    (the same as projecting each row and summing, by linearity), and the
+    codebook width d is a parameter.
+
+    codes [B, K, T] int; codebooks[k] [n_k, d]; proj_semantic, proj_acoustic [out, d].
+    """
+    codes = np.asarray(codes)
+    B, K, T = codes.shape
+    semantic = np.asarray(codebooks[0], np.float64)[codes[:, 0, :]]                 # (B, T, d)
+    acoustic = np.zeros_like(semantic)
+    for k in range(1, K):
+        acoustic += np.asarray(codebooks[k], np.float64)[codes[:, k, :]]
+    y = semantic @ np.asarray(proj_semantic, np.float64).T + acoustic @ np.asarray(proj_acoustic, np.float64).T
+    return np.ascontiguousarray(y.transpose(0, 2, 1))                                # (B, out, T)
