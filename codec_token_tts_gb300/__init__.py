@@ -99,6 +99,10 @@ def _load() -> C.CDLL:
         "tts_bb_rvq_decode": (I, [P, I, I, P, P]),
         "tts_bb_rvq_sync": (I, [P]),
         "tts_bb_rvq_free": (V, [P]),
+        "tts_bb_quantizer_create": (I, [I, I, I, I, C.POINTER(P), P, P, P, C.POINTER(P)]),
+        "tts_bb_quantizer_decode": (I, [P, I, I, P, P]),
+        "tts_bb_quantizer_sync": (I, [P]),
+        "tts_bb_quantizer_free": (V, [P]),
         "tts_bb_dac_create": (I, [C.POINTER(tts_bb_dac_weights), P, C.POINTER(P)]),
         "tts_bb_dac_decode": (I, [P, I, I, P, P]),
         "tts_bb_dac_free": (V, [P]),
@@ -118,7 +122,8 @@ EXPORTED = ("tts_bb_default_config", "tts_bb_create", "tts_bb_free", "tts_bb_pre
             "tts_bb_gqa_decode_attention_static", "tts_bb_debug_fault", "tts_bb_maskgit_update",
             "tts_bb_maskgit_schedule", "tts_bb_frame_step", "tts_bb_rvq_create", "tts_bb_rvq_decode",
             "tts_bb_rvq_sync", "tts_bb_rvq_free", "tts_bb_dac_create", "tts_bb_dac_decode", "tts_bb_dac_free",
-            "tts_bb_decode_step_host")
+            "tts_bb_decode_step_host", "tts_bb_quantizer_create", "tts_bb_quantizer_decode",
+            "tts_bb_quantizer_sync", "tts_bb_quantizer_free")
 
 
 def _ptr(x) -> Optional[int]:
@@ -269,6 +274,35 @@ def tts_bb_rvq_sync(r) -> int:
 
 def tts_bb_rvq_free(r) -> None:
     lib.tts_bb_rvq_free(r)
+
+
+def tts_bb_quantizer_create(codebooks, proj_semantic, proj_acoustic, stream=None):
+    """codebooks: list (one per codebook) of device bf16 tensors [n][d]; projections device bf16 [out][d]."""
+    K = len(codebooks)
+    n, d = int(codebooks[0].shape[0]), int(codebooks[0].shape[1])
+    out_dim = int(proj_semantic.shape[0])
+    books = (C.c_void_p * K)(*[_ptr(x) for x in codebooks])
+    h = C.c_void_p()
+    st = lib.tts_bb_quantizer_create(K, n, d, out_dim, books, _ptr(proj_semantic), _ptr(proj_acoustic), stream,
+                                     C.byref(h))
+    if st != OK:
+        raise TtsBbError(st, "tts_bb_quantizer_create")
+    return h.value
+
+
+def tts_bb_quantizer_decode(q, B: int, T: int, codes, out, check: bool = True) -> int:
+    st = lib.tts_bb_quantizer_decode(q, B, T, _ptr(codes), _ptr(out))
+    if check and st != OK:
+        raise TtsBbError(st, "tts_bb_quantizer_decode")
+    return st
+
+
+def tts_bb_quantizer_sync(q) -> int:
+    return lib.tts_bb_quantizer_sync(q)
+
+
+def tts_bb_quantizer_free(q) -> None:
+    lib.tts_bb_quantizer_free(q)
 
 
 def tts_bb_dac_create(w: dict, stream=None):

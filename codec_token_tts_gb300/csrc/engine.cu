@@ -232,7 +232,7 @@ struct tts_bb {
     unsigned long long* mg_keys = nullptr;  // MaskGIT update scratch: a key and a prediction per cell
     int32_t* mg_pred = nullptr;
     size_t mg_cells = 0;
-    int l2_prefetch = 1;         // persistent step: next-layer weight rows prefetched into L2  // bidirectional attention on tcgen05 (else the mma.sync flash kernel)
+    int l2_prefetch = 3;         // persistent step, L2 prefetch one layer ahead: bit 0 weight rows, bit 1 attention K/V
     size_t mg_pool_blocks = 0;
     int* err = nullptr;
     int* h_err = nullptr;
@@ -902,7 +902,7 @@ static tts_bb_status create_impl(const tts_bb_config* cfg, const tts_bb_weights*
         // so no CTA carries an extra row pair into the critical path: measured faster than all 152 SMs
         // (2040 vs 1911 tokens/s at batch 1) and than every grid from 96 to 144 tried.
         if (h->mega_grid >= 128) h->mega_grid = 128;
-        if (const char* pf = std::getenv("TTS_BB_L2_PREFETCH")) h->l2_prefetch = std::atoi(pf) != 0;
+        if (const char* pf = std::getenv("TTS_BB_L2_PREFETCH")) h->l2_prefetch = std::atoi(pf) & 3;
         if (const char* g = std::getenv("TTS_BB_DECODE_CTAS"))  // tuning knob: CTAs of the persistent step
             h->mega_grid = std::max(std::min(ll_max_grid(), LL_MIN_GRID), std::min(ll_max_grid(), std::atoi(g)));
         if (h->mega_grid > 0) {
@@ -1088,13 +1088,13 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
                     h->phase_us[i] += sum / G;
                     h->phase_max_us[i] += mx;
                 }
-            // ring waits inside gate/up (stamps 6 -> 10) and down (8 -> 11)
+            // ring waits inside gate/up (stamps 6 -> 20) and down (8 -> 30)
             for (int l = 0; l < NL; ++l)
                 for (int g = 0; g < G; ++g) {
                     const unsigned long long* r = &st[((size_t)g * NL + l) * NS];
-                    if (!r[10] || !r[11]) continue;
-                    h->ring_wait[0] += (r[10] - r[6]) * 1e-3;
-                    h->ring_wait[1] += (r[11] - r[8]) * 1e-3;
+                    if (!r[20] || !r[30]) continue;
+                    h->ring_wait[0] += (r[20] - r[6]) * 1e-3;
+                    h->ring_wait[1] += (r[30] - r[8]) * 1e-3;
                     h->ring_wait_n++;
                 }
             // attention-unit phase (stamps 2 -> 3) split by whether the CTA ran a unit

@@ -285,6 +285,9 @@ template <int B>
 __device__ __forceinline__ void l_stage_norm(const MegaArgs& a, const unsigned long long* hx, uint32_t ep,
                                              const bf16* gamma, bf16* xf, float* red) {
     const int t = threadIdx.x;
+    // the gains do not depend on the exchange: their loads go first
+    const uint32_t g0 = __ldg(reinterpret_cast<const unsigned int*>(gamma + 2 * t));
+    const uint32_t g1 = __ldg(reinterpret_cast<const unsigned int*>(gamma + 512 + 2 * t));
     // thread t: elements 2t, 2t+1 and 512+2t, 512+2t+1 of each token row, so
     // a warp's 16-byte loads cover 512 contiguous bytes (all loads issued before any check)
     unsigned long long w[B * 4];
@@ -294,8 +297,6 @@ __device__ __forceinline__ void l_stage_norm(const MegaArgs& a, const unsigned l
         ll_ld2(hx + (size_t)b * HID + 512 + 2 * t, w[b * 4 + 2], w[b * 4 + 3]);
     }
     ll_settle_f(w, [&](int i) { return hx + (size_t)(i >> 2) * HID + ((i & 2) ? 512 : 0) + 2 * t + (i & 1); }, ep, a);
-    const uint32_t g0 = *reinterpret_cast<const uint32_t*>(gamma + 2 * t);
-    const uint32_t g1 = *reinterpret_cast<const uint32_t*>(gamma + 512 + 2 * t);
     const float g4[4] = {__uint_as_float(g0 << 16), __uint_as_float(g0 & 0xFFFF0000u),
                          __uint_as_float(g1 << 16), __uint_as_float(g1 & 0xFFFF0000u)};
     float v[B][4];
@@ -418,6 +419,7 @@ __device__ __forceinline__ void l_consume(const MegaArgs& a, int l, int2 rows, L
             ra[tt][h] = (int)(base + (uint32_t)rin * RS) + (warp * NK * 16 + tq * 4) * 2;
         }
     for (int c = 0; c < nc; ++c) l_mbar_wait(full + (slot0 + c) % ll::NSLOT, ((slot0 + c) / ll::NSLOT) & 1, a);
+    // profiling stamps of this op (slot base `stamp`): +0 ring waits done, +1+w warp w's products done, +9 sink done
     if (stamp >= 0 && a.trace && threadIdx.x == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + stamp] = l_time();
     // two accumulator sets per tile (even / odd column steps) halve the mma dependency chain
     float d[MAXT][2][4];
@@ -442,8 +444,8 @@ __device__ __forceinline__ void l_consume(const MegaArgs& a, int l, int2 rows, L
         }
     }
     __syncwarp();
-    if (stamp >= 0 && a.trace && lane == 0)  // per-warp finish: slots 16 + 8 * (stamp - 10) + warp
-        a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + 16 + 8 * (stamp - 10) + warp] = l_time();
+    if (stamp >= 0 && a.trace && lane == 0)
+        a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + stamp + 1 + warp] = l_time();
     if (lane == 0)
         for (int c = 0; c < nc; ++c)
             asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(l_su32(empty + (slot0 + c) % ll::NSLOT)) : "memory");
@@ -458,6 +460,7 @@ __device__ __forceinline__ void l_consume(const MegaArgs& a, int l, int2 rows, L
         }
         sink(b, r0 + row, v0, true, v1, r0);
     }
+    if (stamp >= 0 && a.trace && threadIdx.x == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + stamp + 9] = l_time();
 }
 
 // q/k RMSNorm + RoPE of one head, 4 elements per lane (RoPE partner lane ^ 16);
@@ -481,11 +484,29 @@ __device__ __forceinline__ void l_gain4(const bf16* gamma, int lane, float* g4) 
     g4[2] = __uint_as_float(u.y << 16); g4[3] = __uint_as_float(u.y & 0xFFFF0000u);
 }
 
+// Request the K and V tiles of this CTA's attention units (unit u = (b, g, block j),
+// CTA c runs u = c, c + G, ...) at layer l into L2, ahead of the layer that reads them.
+__device__ __forceinline__ void l_prefetch_kv(const MegaArgs& a, int l, int B, int nblk0, int nblk1) {
+    const int units_b0 = NKV * nblk0, n_units = units_b0 + NKV * nblk1;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        int b = 0, r = u;
+        if (B > 1 && r >= units_b0) { b = 1; r -= units_b0; }
+        const int nblk = b == 0 ? nblk0 : nblk1;
+        const int g = r / nblk, j = r - g * nblk;
+        const int phys = j == nblk - 1 ? a.last_phys[b] : __ldcg(a.page_table + (size_t)a.slot[b] * a.mbps + j);
+        const bf16* kb = a.pool + (size_t)l * a.layer_elems + ((size_t)phys * 2 * NKV + g) * KVB * HD;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(kb), "r"(KVB * HD * 2) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(kb + (size_t)NKV * KVB * HD), "r"(KVB * HD * 2)
+                     : "memory");
+    }
+}
+
 // Attention unit (b, g, block j): K/V of the block's old keys are loaded
 // before the q/k/v words are polled; the owner of the last block also appends
 // the new token. Writes the block's softmax partial words for heads 2g, 2g+1.
 __device__ __forceinline__ void l_attn_unit(const MegaArgs& a, const XBufs& X, int l, int b, int g, int j, float* att) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (a.trace && threadIdx.x == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + 62] = l_time();
     const int pos = a.pos[b], L = pos + 1;
     const int nblk = (L + KVB - 1) / KVB;
     const bool last = (j == nblk - 1);
@@ -547,7 +568,7 @@ __device__ __forceinline__ void l_attn_unit(const MegaArgs& a, const XBufs& X, i
         newv[lane] = o;
     }
     l_named_sync();
-    if (a.trace && threadIdx.x == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + 36] = l_time();
+    if (a.trace && threadIdx.x == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + 60] = l_time();
     if (last && key0 <= pos && pos < key0 + 8) {  // this warp holds the new token's slot
         kr[pos - key0] = newk[lane];
         vr[pos - key0] = newv[lane];
@@ -615,7 +636,7 @@ __device__ __forceinline__ void l_attn_unit(const MegaArgs& a, const XBufs& X, i
             lsum += ww[2 * HD + 2 * h2 + 1] * f;
             acc += ww[h2 * HD + e] * f;
         }
-        if (a.trace && threadIdx.x == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + 37] = l_time();
+        if (a.trace && threadIdx.x == 0) a.trace[((size_t)blockIdx.x * a.n_layers + l) * TRACE_STRIDE + 61] = l_time();
         unsigned long long* dst = xp_base(a, X, l) + (((size_t)b * NQ + 2 * g + h2) * a.nblk_max + j) * PART_STRIDE;
         const uint32_t ep = ep_p(a, l);
         const size_t rs = xp_rep(a);
@@ -724,7 +745,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
                     l_rows(d.N, blockIdx.x, gridDim.x, r0, r1);
                     // this CTA's rows of the same op one layer ahead (the head after the last layer)
                     // -> L2, so HBM keeps streaming while the ring is full and ring copies hit L2
-                    if (a.l2_prefetch && (l + 1 < a.n_layers || (l + 1 == a.n_layers && a.head && o == 0))) {
+                    if ((a.l2_prefetch & 1) && (l + 1 < a.n_layers || (l + 1 == a.n_layers && a.head && o == 0))) {
                         const LOp nx = l_op(a, l + 1, o);
                         int p0, p1;
                         l_rows(nx.N, blockIdx.x, gridDim.x, p0, p1);
@@ -805,6 +826,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
 
     // page-table entries of blocks opened by this step (read by later launches)
     if (blockIdx.x == 0 && t < a.n_upd) const_cast<int32_t*>(a.page_table)[a.upd_idx[t]] = a.upd_val[t];
+    if (t == 0 && (a.l2_prefetch & 2) && n_units > (int)blockIdx.x) l_prefetch_kv(a, 0, B, nblk0, nblk1);
     // layer-0 input: every CTA sums the embeddings itself (fp32 in the attention
     // scratch); own rows are kept
     float* xs = att;
@@ -861,6 +883,8 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
 
     for (int l = 0; l < a.n_layers; ++l) {
         LSTAMP(0);
+        if (t == 0 && (a.l2_prefetch & 2) && l + 1 < a.n_layers && n_units > (int)blockIdx.x)
+            l_prefetch_kv(a, l + 1, B, nblk0, nblk1);
         if (a.trace && t == 0 && l == 0) {
             uint32_t smid;
             asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
@@ -875,7 +899,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
         {
             unsigned long long* qx = X.q + (size_t)(l & 1) * mk::MAXB * QKV;
             const uint32_t eq = ep_q(a, l);
-            l_consume<B, HID, (QKV + LL_MIN_GRID - 1) / LL_MIN_GRID / 16 + 1>(a, l, rows_qkv, ring, ring_mem, full, empty, xf, part, -1,
+            l_consume<B, HID, (QKV + LL_MIN_GRID - 1) / LL_MIN_GRID / 16 + 1>(a, l, rows_qkv, ring, ring_mem, full, empty, xf, part, 40,
                          [&](int b, int row, float v0, bool two, float v1, int) {
                              ll_put(qx + (size_t)b * QKV + row, v0, eq);
                              if (two) ll_put(qx + (size_t)b * QKV + row + 1, v1, eq);
@@ -896,7 +920,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
         l_stage_attn<B>(a, X, l, xf);
         l_named_sync();
         LSTAMP(4);
-        l_consume<B, NQ * HD, 1>(a, l, rows_o, ring, ring_mem, full, empty, xf, part, -1,
+        l_consume<B, NQ * HD, 1>(a, l, rows_o, ring, ring_mem, full, empty, xf, part, 50,
                      [&](int b, int row, float v0, bool two, float v1, int r0) {
                          hown[b * ll::OWN_MAX + row - r0] += v0;
                          if (two) hown[b * ll::OWN_MAX + row + 1 - r0] += v1;
@@ -919,7 +943,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
         {
             unsigned long long* mx = xm_base(X, l);
             const uint32_t em = ep_m(a, l);
-            l_consume<B, HID, 4>(a, l, rows_gu, ring, ring_mem, full, empty, xf, part, 10,
+            l_consume<B, HID, 4>(a, l, rows_gu, ring, ring_mem, full, empty, xf, part, 20,
                          [&](int b, int row, float g, bool, float u, int) {
                              const float m = g / (1.f + __expf(-g)) * u;
 #pragma unroll
@@ -947,7 +971,7 @@ __global__ void __launch_bounds__(ll::NT, 1) k_decode_ll(const __grid_constant__
         }
         l_named_sync();
         LSTAMP(8);
-        l_consume<B, 3072, 1>(a, l, rows_d, ring, ring_mem, full, empty, xf, part, 11,
+        l_consume<B, 3072, 1>(a, l, rows_d, ring, ring_mem, full, empty, xf, part, 30,
                      [&](int b, int row, float v0, bool two, float v1, int r0) {
                          hown[b * ll::OWN_MAX + row - r0] += v0;
                          if (two) hown[b * ll::OWN_MAX + row + 1 - r0] += v1;

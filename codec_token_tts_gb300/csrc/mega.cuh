@@ -48,7 +48,7 @@ struct MegaArgs {
     const float* sin_t;
     float eps;
     int B, n_layers, ffn;
-    unsigned long long* trace; // optional: [grid][n_layers][16] globaltimer stamps of CTA phases
+    unsigned long long* trace; // optional: [grid][n_layers][TRACE_STRIDE] globaltimer stamps of CTA phases
     // flag-in-data exchange (k_decode_ll.cu)
     unsigned long long* xbuf;  // exchange words (value | epoch << 32), zero-initialised
     uint32_t ep_base;          // first epoch of this launch (grows by ll_epochs_per_launch)
@@ -56,14 +56,14 @@ struct MegaArgs {
     unsigned int* done;        // CTAs finished with the head (last one publishes the argmax)
     unsigned long long timeout_ns;  // bound of every wait (exchange polls, ring slots)
     int debug_stall;           // test hook: CTA 0 withholds one exchange, so every wait runs out
-    int l2_prefetch;           // producer prefetches its next-layer weight rows into L2
+    int l2_prefetch;           // bit 0: next-layer weight rows into L2 (producer); bit 1: next-layer K/V of the attention units
 };
 
 // Launch one decode step on `grid` CTAs (cooperative: all co-resident or an error).
 cudaError_t launch_decode_ll(const MegaArgs& a, int grid, cudaStream_t st);
 int ll_max_grid();
 constexpr int LL_MIN_GRID = 96;   // smallest grid whose per-CTA op slices fit the weight ring
-constexpr int TRACE_STRIDE = 40;  // profiling stamps per (CTA, layer)
+constexpr int TRACE_STRIDE = 64;  // profiling stamps per (CTA, layer)
 // Replicas of the h and SwiGLU exchange vectors and of the attention partials (readers spread over
 // them, writers store every copy). Measured at batch 1 on 128 CTAs (tokens/s, h/SwiGLU : partials):
 // 1:1 2001, 2:2 2072, 4:4 2091, 4:2 2092, 8:8 2027, 16:8 2036, 16:16 1994.

@@ -305,6 +305,37 @@ tts_bb_status tts_bb_rvq_sync(tts_bb_rvq* r);
 /* Wait and free. NULL is a no-op. */
 void tts_bb_rvq_free(tts_bb_rvq* r);
 
+/* Qwen3-TTS codec quantizer lookup (Qwen3-TTS ncnn port, Codec Decoder split,
+ * steps 1-4): the frame's 16 codes -> the 512-channel float hidden that the
+ * codec body reads,
+ *   out[b][o][t] = P_sem[o] . C_0[codes[b][0][t]]
+ *                + P_ac[o] . sum_{k=1..K-1} C_k[codes[b][k][t]]
+ * i.e. the first (semantic) codebook through its own projection and the
+ * other K-1 (acoustic) codebooks summed through the second projection.
+ *   codebooks     K device bf16 pointers, each [codebook_size][dim]
+ *   proj_semantic device bf16 [out_dim][dim]; proj_acoustic the same
+ * (the page: 16 codebooks of 2048 entries, out_dim 512; it does not print the
+ * codebook width, so dim is a parameter; the projections are bias-free).
+ * tts_bb_quantizer_create copies them (the caller may free its copies) and
+ * returns TTS_BB_E_INVALID for NULL pointers or sizes outside 2 <= K <= 32,
+ * dim a multiple of 64 in 64..1024, 1 <= out_dim <= 8192; TTS_BB_E_OOM. */
+typedef struct tts_bb_quantizer tts_bb_quantizer;
+tts_bb_status tts_bb_quantizer_create(int n_codebooks, int codebook_size, int dim, int out_dim,
+                                      const void* const* codebooks, const void* proj_semantic,
+                                      const void* proj_acoustic, void* stream, tts_bb_quantizer** out);
+/* codes device int32 [B][K][T]; out device fp32 [B][out_dim][T] (channel-major,
+ * the [1, 512, T] layout the page feeds to the codec body). Asynchronous on the
+ * handle's stream (a gather kernel and one GEMM); the acoustic sum is carried
+ * as bf16 high + low parts, so the result keeps fp32-level accuracy over the
+ * bf16 tables. A code outside 0..codebook_size-1 contributes nothing and is
+ * reported by tts_bb_quantizer_sync as TTS_BB_E_BAD_ID. Scratch (3 * dim bf16
+ * per frame, rounded up to 256) grows on the first call that needs more. */
+tts_bb_status tts_bb_quantizer_decode(tts_bb_quantizer* q, int B, int T, const int32_t* codes, float* out);
+/* Wait for the handle's work; returns (and clears) a latched device error. */
+tts_bb_status tts_bb_quantizer_sync(tts_bb_quantizer* q);
+/* Wait and free. NULL is a no-op. */
+void tts_bb_quantizer_free(tts_bb_quantizer* q);
+
 /* DAC decoder: frame features -> 24 kHz audio (omnivoice-cpp, Audio tokenizer
  * pipeline, Decode; DAC decoder block channels; Snake activation;
  * ConvTranspose1d): fc2 Linear 1024 -> 256, conv1 (256 -> 1024, k 7, pad 3),

@@ -59,6 +59,11 @@ int main(void) {
         EXPECT(tts_bb_rvq_decode(NULL, 1, 1, NULL, NULL) == TTS_BB_E_INVALID);
         EXPECT(tts_bb_rvq_sync(NULL) == TTS_BB_E_INVALID);
         tts_bb_rvq_free(NULL);
+        tts_bb_quantizer* qz = NULL;
+        EXPECT(tts_bb_quantizer_create(16, 2048, 256, 512, NULL, NULL, NULL, NULL, &qz) == TTS_BB_E_INVALID && qz == NULL);
+        EXPECT(tts_bb_quantizer_decode(NULL, 1, 1, NULL, NULL) == TTS_BB_E_INVALID);
+        EXPECT(tts_bb_quantizer_sync(NULL) == TTS_BB_E_INVALID);
+        tts_bb_quantizer_free(NULL);
     }
     {
         tts_bb_dac* d = NULL;
