@@ -108,6 +108,12 @@ class ClockSampler:
         for ln in self.proc.stdout:
             self.lines.append(ln.strip())
 
+    def wait_first(self, limit_s: float = 3.0):
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < limit_s:
+            time.sleep(0.01)
+        self.skip = len(self.lines)  # samples taken before the timed region are not counted
+
     def stop(self) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
@@ -119,7 +125,8 @@ class ClockSampler:
         self.t.join(timeout=2)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines = self.lines[getattr(self, "skip", 0):] or self.lines[-1:]  # at least the latest sample
+        for ln in lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -232,9 +239,10 @@ def run_talker_b1(args, ws, rank):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(this_rank_gpu())
     n0 = m.tts_bb_launch_count(h)
+    clocks.start()
+    clocks.wait_first()  # the sampler is live before the timed region starts
     dist_barrier(ws)
     torch.cuda.synchronize()
-    clocks.start()
     ev0.record(stream)
     steps(args.steps)
     ev1.record(stream)
@@ -282,13 +290,16 @@ def run_talker_b1(args, ws, rank):
 
     tokens = args.steps * ws
     value = tokens / (ms_max / 1e3)
-    pos_bytes = np.mean([wl.algorithmic_bytes_per_step(P_PREFILL + (t % N_DECODE)) for t in range(N_DECODE)])
+    pos_bytes = np.mean([wl.algorithmic_bytes_per_step(P_PREFILL + (t % N_DECODE)) for t in range(args.steps)])
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic", "config": dict(wl.config(), parallelism="replicas" if ws > 1 else "single"),
         "hbm_step_roofline": {"algorithmic_bytes_per_step": pos_bytes,
-                              "achieved_gbs": pos_bytes / (ms_max / args.steps) / 1e6},
+                              "achieved_gbs": pos_bytes / (ms_max / args.steps) / 1e6,
+                              "frac_of_measured": pos_bytes / (ms_max / args.steps) / 1e6 / peaks()[0]["hbm_gbs"],
+                              "frac_of_8tbs": pos_bytes / (ms_max / args.steps) / 1e6 / 8000.0,
+                              "target_frac": 0.70},
         "clocks": clk, "gpu_launches": int(launches),
         "e2e": {"value": n_e2e * ws / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 16 * 4, "d2h_bytes_per_step": 4 + 4,
                 "path": "tts_bb_decode_step_host: ids H2D, step, argmax + error word D2H, one sync per step"},
@@ -402,6 +413,7 @@ def run_maskgit(steps, warmup):
     refine = run_maskgit_refinement(m, h, seed, stream)
     m.tts_bb_free(h)
     refine["rvq_decode"] = run_rvq_decode(m, stream)
+    refine["quantizer_decode"] = run_quantizer_decode(m, stream)
     refine["dac_decode"] = run_dac_decode(m, stream)
     flops = 2 * 8192 * 15_728_640 * 28 + 4 * 8 * 16 * 1024 ** 2 * 128 * 28 + 2 * 8 * 768 * 8200 * 1024
     pk = peaks()[0]
@@ -441,6 +453,39 @@ def run_rvq_decode(m, stream, B=4, T=768, reps=20):
     # codes read, gathered 64-d rows, packed weights read once, output written
     nbytes = B * K * T * 4 + B * T * K * D * 2 + OUT * K * D * 2 + B * T * OUT * 4
     return {"workload": f"RVQ decode: {B} x {T} frames x {K} codebooks (1024 x 64) -> {OUT}-d fp32",
+            "us_per_decode": us, "frames_per_s": B * T / (us / 1e6), "status": st,
+            "algorithmic_bytes": nbytes, "hbm_frac_of_measured": nbytes / (us / 1e6) / 1e9 / peaks()[0]["hbm_gbs"]}
+
+
+def run_quantizer_decode(m, stream, B=4, T=768, reps=20):
+    """Qwen3-TTS quantizer lookup: 4 x 768 frames x 16 codebooks (2048 x 256, seeded bf16 tables; the
+    pages do not print the codebook width), semantic + acoustic projections -> [4][512][768] fp32."""
+    import torch
+    from tests.gpu_util import dev_bf16_bits, dev_i32
+    K, N, D, OUT = 16, 2048, 256, 512
+    r = synth.rng_for(7, "quant_tables")
+    books = [dev_bf16_bits(synth.normal_bf16(r, (N, D), 1.0)) for _ in range(K)]
+    ps = dev_bf16_bits(synth.normal_bf16(r, (OUT, D), 0.02))
+    pa = dev_bf16_bits(synth.normal_bf16(r, (OUT, D), 0.02))
+    q = m.tts_bb_quantizer_create(books, ps, pa, stream.cuda_stream)
+    codes = dev_i32(synth.rng_for(7, "quant_codes").integers(0, N, (B, K, T)))
+    out = torch.zeros(B, OUT, T, dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        m.tts_bb_quantizer_decode(q, B, T, codes, out)
+    st = m.tts_bb_quantizer_sync(q)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(reps):
+        m.tts_bb_quantizer_decode(q, B, T, codes, out)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    m.tts_bb_quantizer_free(q)
+    us = ev0.elapsed_time(ev1) / reps * 1e3
+    kp = (3 * D + 255) // 256 * 256
+    # codes read, 16 gathered rows per frame, packed rows written and read back, packed weights, output
+    nbytes = B * K * T * 4 + B * T * K * D * 2 + 2 * B * T * kp * 2 + OUT * kp * 2 + B * T * OUT * 4
+    return {"workload": f"Qwen3-TTS quantizer lookup: {B} x {T} frames x {K} codebooks ({N} x {D}) -> {OUT} channels fp32",
             "us_per_decode": us, "frames_per_s": B * T / (us / 1e6), "status": st,
             "algorithmic_bytes": nbytes, "hbm_frac_of_measured": nbytes / (us / 1e6) / 1e9 / peaks()[0]["hbm_gbs"]}
 
@@ -700,7 +745,7 @@ def roofline_from_profile(rep, traffic=None):
     ach = top["bytes"] / (top["ms"] / 1e3) / 1e9
     peak = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     return {"kernel": top["kind"], "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
-            "frac": ach / peak, "traffic": traffic, "peak_source": f"{src} hbm_gbs",
+            "frac": ach / peak, "frac_of_8tbs": ach / 8000.0, "traffic": traffic, "peak_source": f"{src} hbm_gbs",
             "bytes_per_launch": top["bytes"] / top["launches"], "share": top["ms"] / total,
             "launches": top["launches"]}
 

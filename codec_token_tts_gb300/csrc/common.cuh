@@ -171,16 +171,22 @@ struct KVView {
     const int32_t* seq_slot;
     int mbps;              // blocks per slot row of the page table
 };
+// qout_f (optional): the queries as fp32 [T][16][128] instead of bf16 in qout.
 int launch_qk_norm_rope_append(const float* qkv, const bf16* qn, const bf16* kn, const float* cos_t,
                                 const float* sin_t, float eps, bf16* qout, KVView kv, const int32_t* seq_start,
-                                const int32_t* seq_len, int tok_per_seq, int T, int* err, cudaStream_t st);
+                                const int32_t* seq_len, int tok_per_seq, int T, int* err, cudaStream_t st,
+                                float* qout_f = nullptr);
 // Decode attention, one query per sequence: split-K flash decode + combine.
+// qf (optional): fp32 queries [B][16][128], read instead of the bf16 q.
 int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B, int max_len,
-                        float* part, bf16* out, int max_splits, cudaStream_t st, bf16* out_lo = nullptr);
+                        float* part, bf16* out, int max_splits, cudaStream_t st, bf16* out_lo = nullptr,
+                        const float* qf = nullptr);
 // Prefill / bidirectional attention over the paged view, tensor cores.
 // causal: query at position p sees keys <= p; else keys < key_len[seq].
+// out_lo (optional): low bf16 parts of the output, value - bf16(value).
 int launch_attn_prefill(const bf16* q, KVView kv, const int32_t* seq_start, const int32_t* seq_len,
-                         const int32_t* key_len, int causal, int B, int S, bf16* out, cudaStream_t st);
+                         const int32_t* key_len, int causal, int B, int S, bf16* out, cudaStream_t st,
+                         bf16* out_lo = nullptr);
 // out[b * stride] = unpacked argmax
 int launch_argmax_finalize(const unsigned long long* amax, int32_t* out, int stride, int B, cudaStream_t st);
 

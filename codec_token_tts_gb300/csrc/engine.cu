@@ -209,6 +209,7 @@ struct tts_bb {
     bf16* y = nullptr;
     float* qkv = nullptr;
     bf16* q = nullptr;
+    float* qf = nullptr;                // decode: fp32 queries for the decode attention
     bf16* ao = nullptr;
     bf16* m = nullptr;
     bf16 *y_lo = nullptr, *ao_lo = nullptr, *m_lo = nullptr;  // low bf16 parts (decode)
@@ -427,7 +428,7 @@ tts_bb_status ensure_scratch(tts_bb* h, int T) {
     if (T <= h->T_cap) return TTS_BB_OK;
     if (h->h) {
         cudaStreamSynchronize(h->st);
-        void* olds[] = {h->h, h->y, h->qkv, h->q, h->ao, h->m, h->y_lo, h->ao_lo, h->m_lo};
+        void* olds[] = {h->h, h->y, h->qkv, h->q, h->qf, h->ao, h->m, h->y_lo, h->ao_lo, h->m_lo};
         for (void* p : olds) {
             cudaFree(p);
             h->allocs.erase(std::remove(h->allocs.begin(), h->allocs.end(), p), h->allocs.end());
@@ -438,6 +439,7 @@ tts_bb_status ensure_scratch(tts_bb* h, int T) {
         (e = dalloc(h, &h->y, (size_t)T * HID)) != cudaSuccess ||
         (e = dalloc(h, &h->qkv, (size_t)T * QKV)) != cudaSuccess ||
         (e = dalloc(h, &h->q, (size_t)T * NQ * HD)) != cudaSuccess ||
+        (e = dalloc(h, &h->qf, (size_t)T * NQ * HD)) != cudaSuccess ||
         (e = dalloc(h, &h->ao, (size_t)T * NQ * HD)) != cudaSuccess ||
         (e = dalloc(h, &h->m, (size_t)T * h->cfg.ffn)) != cudaSuccess ||
         (e = dalloc(h, &h->y_lo, (size_t)T * HID)) != cudaSuccess ||
@@ -470,10 +472,11 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         const LayerW& w = h->L[l];
         KVView kv = kv_base;
         kv.pool = kv_base.pool + (size_t)l * layer_stride;
-        const int gk = T <= 8 ? K_GEMV : (mode == 0 ? (T <= 256 ? K_GEMM_TCD : K_GEMM) : K_GEMM_TC);
-        // decode carries GEMM inputs as bf16 high + low parts (weights are read
-        // once either way); prefill / bidirectional passes use plain bf16
-        const bool split = mode == 0;
+        // decode and causal prefill carry GEMM inputs as bf16 high + low parts (the
+        // prefill writes the K/V that every later step reads); the bidirectional
+        // pass, tensor-bound, uses plain bf16
+        const bool split = mode != 2;
+        const int gk = T <= 8 ? K_GEMV : (split ? K_GEMM_TCD : K_GEMM_TC);
         bf16* ylo = split ? h->y_lo : nullptr;
         bf16* aolo = split ? h->ao_lo : nullptr;
         bf16* mlo = split ? h->m_lo : nullptr;
@@ -485,16 +488,18 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         { Launch L(h, gk, gemm_bytes(T, QKV, HID, 4), 2.0 * T * QKV * HID); L += launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st, ylo, h->err, skp); }
         { Launch L(h, K_QKROPE, T * (4.0 * QKV + 2.0 * QKV));
           L += launch_qk_norm_rope_append(h->qkv, w.qn, w.kn, h->cos_t, h->sin_t, c.rms_eps, h->q, kv,
-                                          h->seq_start, h->seq_len, tok_per_seq, T, h->err, h->st); }
+                                          h->seq_start, h->seq_len, tok_per_seq, T, h->err, h->st,
+                                          mode == 0 ? h->qf : nullptr); }
         if (bidir_tc) {
             Launch L(h, K_ATTN_BIDIR_TC, 0, attn_flops);
             L += launch_attn_bidir_tc(h->q, kv.pool, h->mg_pool_blocks, kv.mbps, h->key_len, B, tok_per_seq, h->ao, h->err, h->st);
         } else if (mode == 0) {
             Launch L(h, K_ATTN_DECODE, kv_read_bytes + T * (2.0 * NQ * HD * 2), 4.0 * NQ * HD * (kv_read_bytes / (2.0 * NKV * HD * 2)));
-            L += launch_attn_decode(h->q, kv, h->seq_start, B, max_len, h->part, h->ao, MAX_SPLITS, h->st, aolo);
+            L += launch_attn_decode(h->q, kv, h->seq_start, B, max_len, h->part, h->ao, MAX_SPLITS, h->st, aolo, h->qf);
         } else {
             Launch L(h, K_ATTN_PREFILL, 0, attn_flops);
-            L += launch_attn_prefill(h->q, kv, h->seq_start, h->seq_len, h->key_len, mode == 1, B, tok_per_seq, h->ao, h->st);
+            L += launch_attn_prefill(h->q, kv, h->seq_start, h->seq_len, h->key_len, mode == 1, B, tok_per_seq, h->ao, h->st,
+                                     aolo);
         }
         e = Epi{};
         e.mode = EPI_ADD_F32; e.out = h->h; e.ldo = HID;
@@ -1191,7 +1196,7 @@ TTS_API tts_bb_status tts_bb_prefill(tts_bb* h, int B, int S, const int32_t* slo
     if (opts && opts->hidden_out)
         cudaMemcpyAsync(opts->hidden_out, h->h, (size_t)T * HID * sizeof(float), cudaMemcpyDeviceToDevice, h->st);
     if (head_idx >= 0 && (logits_out || argmax_out))
-        run_head(h, B, S, head_idx, true, logits_out, argmax_out, opts && opts->argmax_stride ? opts->argmax_stride : 1);
+        run_head(h, B, S, head_idx, true, logits_out, argmax_out, opts && opts->argmax_stride ? opts->argmax_stride : 1, true);
     return finish(h);
 }
 

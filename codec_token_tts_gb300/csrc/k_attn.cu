@@ -27,7 +27,8 @@ __device__ __forceinline__ const bf16* kv_tile(const KVView& kv, int seq, int j,
 __global__ void __launch_bounds__(128) k_attn_decode(const bf16* __restrict__ q, KVView kv,
                                                      const int32_t* __restrict__ seq_start, int bps,
                                                      int n_splits, float* __restrict__ part,
-                                                     bf16* __restrict__ out, bf16* __restrict__ out_lo) {
+                                                     bf16* __restrict__ out, bf16* __restrict__ out_lo,
+                                                     const float* __restrict__ qf) {
     pdl_wait();  // upstream results are read below
     pdl_trigger();
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -38,7 +39,12 @@ __global__ void __launch_bounds__(128) k_attn_decode(const bf16* __restrict__ q,
 
     const float sc = rsqrtf((float)HD) * LOG2E;
     float q0[4], q1[4];
-    {
+    if (qf) {
+        const float4 a = *reinterpret_cast<const float4*>(qf + ((size_t)b * NQ + 2 * g) * HD + lane * 4);
+        const float4 c = *reinterpret_cast<const float4*>(qf + ((size_t)b * NQ + 2 * g + 1) * HD + lane * 4);
+        q0[0] = a.x * sc; q0[1] = a.y * sc; q0[2] = a.z * sc; q0[3] = a.w * sc;
+        q1[0] = c.x * sc; q1[1] = c.y * sc; q1[2] = c.z * sc; q1[3] = c.w * sc;
+    } else {
         const bf16* qp = q + ((size_t)b * NQ + 2 * g) * HD + lane * 4;
         const uint2 a = *reinterpret_cast<const uint2*>(qp);
         const uint2 c = *reinterpret_cast<const uint2*>(qp + HD);
@@ -174,7 +180,7 @@ __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ 
 }
 
 int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B, int max_len, float* part,
-                        bf16* out, int max_splits, cudaStream_t st, bf16* out_lo) {
+                        bf16* out, int max_splits, cudaStream_t st, bf16* out_lo, const float* qf) {
     if (B <= 0) return 0;
     const int nblk = (max_len + KVB - 1) / KVB;
     // ~32 CTAs per SM (several waves): the block scheduler balances ragged sequence lengths
@@ -183,7 +189,7 @@ int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B
     splits = max(1, min(splits, min(nblk, max_splits)));
     const int bps = (nblk + splits - 1) / splits;
     splits = (nblk + bps - 1) / bps;
-    launch_pdl(k_attn_decode, dim3(splits, NKV, B), 128, 0, st, q, kv, seq_start, bps, splits, part, out, out_lo);
+    launch_pdl(k_attn_decode, dim3(splits, NKV, B), 128, 0, st, q, kv, seq_start, bps, splits, part, out, out_lo, qf);
     if (splits == 1) return 1;
     launch_pdl(k_attn_combine, B * NQ, 128, 0, st, part, splits, out, out_lo);
     return 2;
@@ -228,7 +234,7 @@ __global__ void __launch_bounds__(256) k_attn_prefill(const bf16* __restrict__ q
                                                       const int32_t* __restrict__ seq_start,
                                                       const int32_t* __restrict__ seq_len,
                                                       const int32_t* __restrict__ key_len, int causal, int S,
-                                                      bf16* __restrict__ out) {
+                                                      bf16* __restrict__ out, bf16* __restrict__ out_lo) {
     pdl_wait();  // upstream results are read below
     pdl_trigger();
     using namespace fa;
@@ -380,18 +386,25 @@ __global__ void __launch_bounds__(256) k_attn_prefill(const bf16* __restrict__ q
     for (int r = 0; r < 2; ++r) {
         const int s_idx = row_a + r * 8;
         if (s_idx >= S) continue;
-        bf16* dst = out + ((size_t)(b * S + s_idx) * NQ + h) * HD;
+        const size_t off = ((size_t)(b * S + s_idx) * NQ + h) * HD;
         const float inv = r ? inv1 : inv0;
 #pragma unroll
         for (int d8 = 0; d8 < 16; ++d8) {
             const int d = d8 * 8 + (lane & 3) * 2;
-            *reinterpret_cast<uint32_t*>(dst + d) = pack_bf2(o[d8][2 * r] * inv, o[d8][2 * r + 1] * inv);
+            const float v0 = o[d8][2 * r] * inv, v1 = o[d8][2 * r + 1] * inv;
+            const uint32_t hi = pack_bf2(v0, v1);
+            *reinterpret_cast<uint32_t*>(out + off + d) = hi;
+            if (out_lo) {  // low parts: value - bf16(value)
+                const float2 hf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi));
+                *reinterpret_cast<uint32_t*>(out_lo + off + d) = pack_bf2(v0 - hf.x, v1 - hf.y);
+            }
         }
     }
 }
 
 int launch_attn_prefill(const bf16* q, KVView kv, const int32_t* seq_start, const int32_t* seq_len,
-                         const int32_t* key_len, int causal, int B, int S, bf16* out, cudaStream_t st) {
+                         const int32_t* key_len, int causal, int B, int S, bf16* out, cudaStream_t st,
+                         bf16* out_lo) {
     if (B <= 0 || S <= 0) return 0;
     static bool attr_set = false;
     if (!attr_set) {
@@ -399,7 +412,7 @@ int launch_attn_prefill(const bf16* q, KVView kv, const int32_t* seq_start, cons
         attr_set = true;
     }
     dim3 grid((S + fa::BQ - 1) / fa::BQ, NKV, B);
-    launch_pdl(k_attn_prefill, grid, 256, fa::SMEM, st, q, kv, seq_start, seq_len, key_len, causal, S, out);
+    launch_pdl(k_attn_prefill, grid, 256, fa::SMEM, st, q, kv, seq_start, seq_len, key_len, causal, S, out, out_lo);
     return 1;
 }
 

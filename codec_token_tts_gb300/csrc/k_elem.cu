@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(256) k_qk_norm_rope_append(
     const float* __restrict__ qkv, const bf16* __restrict__ qn, const bf16* __restrict__ kn,
     const float* __restrict__ cos_t, const float* __restrict__ sin_t, float eps, bf16* __restrict__ qout,
     KVView kv, const int32_t* __restrict__ seq_start, const int32_t* __restrict__ seq_len, int tok_per_seq,
-    int* err) {
+    int* err, float* __restrict__ qout_f) {
     pdl_wait();  // upstream results are read below
     pdl_trigger();
     const int t = blockIdx.x;
@@ -225,7 +225,10 @@ __global__ void __launch_bounds__(256) k_qk_norm_rope_append(
         uint2 w;
         w.x = *reinterpret_cast<uint32_t*>(&a);
         w.y = *reinterpret_cast<uint32_t*>(&b);
-        if (isq) {
+        if (isq && qout_f) {  // fp32 queries (the decode attention reads them unrounded)
+            const float4 f4 = valid ? make_float4(o[0], o[1], o[2], o[3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(qout_f + (size_t)t * NQ * HD + hh * HD + lane * 4) = f4;
+        } else if (isq) {
             if (!valid) w = make_uint2(0u, 0u);
             *reinterpret_cast<uint2*>(qout + (size_t)t * NQ * HD + hh * HD + lane * 4) = w;
         } else {
@@ -236,10 +239,11 @@ __global__ void __launch_bounds__(256) k_qk_norm_rope_append(
 
 int launch_qk_norm_rope_append(const float* qkv, const bf16* qn, const bf16* kn, const float* cos_t,
                                 const float* sin_t, float eps, bf16* qout, KVView kv, const int32_t* seq_start,
-                                const int32_t* seq_len, int tok_per_seq, int T, int* err, cudaStream_t st) {
+                                const int32_t* seq_len, int tok_per_seq, int T, int* err, cudaStream_t st,
+                                float* qout_f) {
     if (T <= 0) return 0;
     launch_pdl(k_qk_norm_rope_append, T, 256, 0, st, qkv, qn, kn, cos_t, sin_t, eps, qout, kv, seq_start, seq_len,
-                                             tok_per_seq, err);
+                                             tok_per_seq, err, qout_f);
     return 1;
 }
 

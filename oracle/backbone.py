@@ -14,7 +14,7 @@ __all__ = [
     "bf16_to_f64", "rms_norm", "rope_inv_freq", "rope_half_rotate",
     "mrope_interleaved", "attention_gqa", "silu", "swiglu_mlp",
     "codebook_embed_sum", "omnivoice_embed", "Backbone", "KVCache",
-    "argmax_first", "causal_allowed", "keylen_allowed",
+    "argmax_first", "causal_allowed", "keylen_allowed", "round_bf16",
 ]
 
 
@@ -172,6 +172,14 @@ def omnivoice_embed(ids: np.ndarray, audio_mask: np.ndarray, text_table: np.ndar
     return np.where(m[:, :, None], audio_emb, text_emb)
 
 
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Values as stored in bf16: rounded to float32, then to the nearest bf16
+    (ties to even on the 16 dropped bits), returned as float64."""
+    u = np.ascontiguousarray(np.asarray(x, dtype=np.float32)).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 def argmax_first(x: np.ndarray) -> np.ndarray:
     """Greedy pick along the last axis, lowest index on ties, taken on the
     float32 logits (the precision in which the GPU decides)."""
@@ -205,8 +213,13 @@ class Backbone:
     Weights are float64 copies of the bf16 tensors, PyTorch (out, in) layout.
     """
 
-    def __init__(self, w, shape):
+    def __init__(self, w, shape, kv_storage: Optional[str] = None):
+        """kv_storage: None keeps the cache in float64 (the plain definition);
+        "bf16" stores every appended key and value rounded to bf16, the cache
+        format the GPU path is specified to use, so that its effect on the
+        logits and the greedy picks can be measured apart from everything else."""
         self.s = shape
+        self.kv_storage = kv_storage
         f = bf16_to_f64
         self.layers = [{k: f(v) for k, v in lw.items()} for lw in w.layers]
         self.codebooks = [f(t) for t in w.codebooks]
@@ -252,6 +265,8 @@ class Backbone:
             qi = rope_half_rotate(q[a:b], pos, s.rope_theta)
             ki = rope_half_rotate(k[a:b], pos, s.rope_theta)
             vi = v[a:b]
+            if self.kv_storage == "bf16":
+                ki, vi = round_bf16(ki), round_bf16(vi)
             if cache is not None:
                 cache.k[l] = np.concatenate([cache.k[l], ki], axis=0)
                 cache.v[l] = np.concatenate([cache.v[l], vi], axis=0)

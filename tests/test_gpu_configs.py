@@ -12,8 +12,8 @@ import pytest
 
 import oracle as O
 import synth
-from tests.gpu_util import (HIDDEN_TOL, LOGIT_TOL, Engine, check_logits_and_argmax, dev_bf16_bits, dev_i32,
-                            dev_u8, f32_zeros, i32_full, rel_err_rows)
+from tests.gpu_util import (ARGMAX_AGREE, HIDDEN_TOL, LOGIT_TOL, Engine, check_logits_and_argmax, dev_bf16_bits,
+                            dev_i32, dev_u8, f32_zeros, i32_full, rel_err_rows)
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -29,7 +29,13 @@ def report(name, **kw):
 
 # ---------------------------------------------------------------- Talker batch 1: 128 prefill + 256 decode (seed 1)
 def test_talker_batch1_full():
-    """Whole workload: 28 layers, 128-position prefill, 256 decode steps, every step compared."""
+    """Whole workload: 28 layers, 128-position prefill, 256 decode steps, every step compared.
+
+    The greedy picks must agree with the float64 oracle's on at least 99.5 % of
+    the steps (and on every pick that is unique under the logits tolerance). They
+    are also compared with the oracle whose cache stores K/V in bf16, the storage
+    format the GPU path is specified to use: a disagreement with it may only sit
+    at a near-tie of its logits."""
     seed = 1
     w = synth.model_weights(synth.TALKER, seed)
     m0 = O.Backbone(w, synth.TALKER)
@@ -38,6 +44,10 @@ def test_talker_batch1_full():
     cache = m0.new_cache()
     hp, lg0, a0 = O.talker_prefill(m0, ids, cache)
     hid_o, lg_o, am_o, fed = O.talker_decode_steps(m0, cache, a0, rest)
+    mk = O.Backbone(w, synth.TALKER, kv_storage="bf16")   # same teacher-forced id stream
+    cache_k = mk.new_cache()
+    O.talker_prefill(mk, ids, cache_k)
+    _, lg_k, am_k, _ = O.talker_decode_steps(mk, cache_k, a0, rest, forced_id0=fed[:, 0])
     with Engine(w, max_slots=1, max_ctx=384, max_batch=1, max_tokens=128) as e:
         m = e.m
         logits = f32_zeros(1, 3072)
@@ -54,10 +64,18 @@ def test_talker_batch1_full():
             m.tts_bb_decode_step(e.h, 1, [0], [128 + t], fed_d[t:t + 1], 0, L[t:t + 1], A[t:t + 1],
                                  hidden_out=H[t:t + 1])
         herr = rel_err_rows(H.cpu().numpy(), hid_o)
-        err, agree, agree_u = check_logits_and_argmax(L.cpu().numpy(), lg_o, A.cpu().numpy(), am_o)
+        err, agree, agree_u = check_logits_and_argmax(L.cpu().numpy(), lg_o, A.cpu().numpy(), am_o,
+                                                      min_agree=ARGMAX_AGREE)
         assert herr <= HIDDEN_TOL
+        gl, ga = L.cpu().numpy(), A.cpu().numpy()
+        flips = np.nonzero(ga != am_k)[0]
+        top2 = np.sort(lg_k, axis=1)[:, -2:]
         report("talker_b1", hidden_rel=f"{herr:.2e}", logit_abs=f"{err:.2e}", argmax_raw=agree,
-               argmax_unique=agree_u)
+               argmax_unique=agree_u, logit_abs_bf16_kv=f"{np.abs(gl - lg_k).max():.2e}",
+               logit_mean_bf16_kv=f"{np.abs(gl - lg_k).mean():.2e}", argmax_raw_bf16_kv=float(np.mean(ga == am_k)),
+               flips_bf16_kv=flips.tolist(), flip_gaps=(top2[flips, 1] - top2[flips, 0]).tolist(),
+               oracle_fp64_vs_bf16_kv=float(np.mean(am_o == am_k)))
+        check_logits_and_argmax(gl, lg_k, ga, am_k)
         # free-running on the device: argmax written straight into the next id row
         m.tts_bb_truncate(e.h, 0, 128)
         ids_d = dev_i32(np.concatenate([np.zeros((257, 1), np.int32), np.vstack([rest, rest[:1]])], axis=1))
@@ -117,7 +135,7 @@ def test_serving_batch64_full():
             g = hid.cpu().numpy()[sample]
             worst_h = max(worst_h, rel_err_rows(g, ho))
             err, agree, _ = check_logits_and_argmax(logits.cpu().numpy()[sample], lo, am.cpu().numpy()[sample], ao,
-                                                    min_agree=0.0)
+                                                    min_agree=0.0)  # per step; the whole run is checked below
             worst_l = max(worst_l, err)
             agrees.append(agree)
             if t + 1 < steps:                 # teacher forcing for the followed streams
@@ -127,6 +145,7 @@ def test_serving_batch64_full():
         assert worst_h <= HIDDEN_TOL
         report("serving_b64", sample=sample, hidden_rel=f"{worst_h:.2e}", logit_abs=f"{worst_l:.2e}",
                argmax_raw=float(np.mean(agrees)))
+        assert float(np.mean(agrees)) >= ARGMAX_AGREE
         # paging: the appended tokens sit behind the synthetic prefix, which is unchanged
         b = sample[0]
         n = int(L0[b]) + steps
@@ -176,7 +195,7 @@ def test_code_predictor_256_frames_full():
         gl = np.stack(gl, axis=1)                             # [16, 15, 2048]
         got = codes.cpu().numpy()[sample][:, 1:16]
         err, agree, agree_u = check_logits_and_argmax(gl.reshape(-1, 2048), logits_o.reshape(-1, 2048),
-                                                      got.reshape(-1), codes_o.reshape(-1))
+                                                      got.reshape(-1), codes_o.reshape(-1), min_agree=ARGMAX_AGREE)
         report("code_predictor", frames=F, followed=len(sample), logit_abs=f"{err:.2e}", argmax_raw=agree,
                argmax_unique=agree_u)
 

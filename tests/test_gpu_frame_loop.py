@@ -13,7 +13,7 @@ import pytest
 
 import oracle as O
 import synth
-from tests.gpu_util import LOGIT_TOL, Engine, check_logits_and_argmax, dev_i32, f32_zeros
+from tests.gpu_util import ARGMAX_AGREE, LOGIT_TOL, Engine, check_logits_and_argmax, dev_i32, f32_zeros
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -67,7 +67,7 @@ def test_frame_loop_matches_oracle(B):
         O.talker_prefill(talker, prompt[b][:P], cache)
         o_codes, t_lg, c_lg, _ = O.talker_cp_frames(talker, cp, cache, prompt[b][P], n_frames,
                                                     forced=got_codes[:, b])
-        check_logits_and_argmax(got_logits[:, b], t_lg, got_codes[:, b, 0], o_codes[:, 0], min_agree=0.0)
+        check_logits_and_argmax(got_logits[:, b], t_lg, got_codes[:, b, 0], o_codes[:, 0], min_agree=ARGMAX_AGREE)
         for f in range(n_frames):
             _check_cp_codes(got_codes[f, b, 1:], c_lg[f])
         assert np.all(got_codes[:, b, 0] < 3072) and np.all(got_codes[:, b, 1:] < 2048)
@@ -109,6 +109,6 @@ def test_frame_loop_full_size():
     cache = talker.new_cache()
     O.talker_prefill(talker, pre[:P], cache)
     o_codes, t_lg, c_lg, _ = O.talker_cp_frames(talker, cp, cache, pre[P], n_frames, forced=got_codes)
-    check_logits_and_argmax(got_logits, t_lg, got_codes[:, 0], o_codes[:, 0], min_agree=0.0)
+    check_logits_and_argmax(got_logits, t_lg, got_codes[:, 0], o_codes[:, 0], min_agree=ARGMAX_AGREE)
     for f in range(n_frames):
         _check_cp_codes(got_codes[f, 1:], c_lg[f])
