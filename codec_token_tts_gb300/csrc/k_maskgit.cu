@@ -20,6 +20,10 @@ namespace ttsbb {
 namespace mg {
 constexpr int MAXV_LANE = 33;  // vocabulary up to 32 * 33 = 1056 ids
 constexpr int SELECT_NT = 1024;
+// a logits row staged in shared memory: the 16-byte chunks covering it, up to 3 floats of lead-in
+constexpr int ROWF = 32 * MAXV_LANE + 4;       // floats per staged row (a multiple of 4)
+constexpr int MAXQ = (ROWF / 4 + 31) / 32;     // 16-byte chunks per lane
+constexpr int SCORE_SMEM = 8 * 2 * ROWF * 4;   // 8 warps x (cond, uncond) rows
 }  // namespace mg
 
 __device__ __forceinline__ unsigned long long mg_key(float score, int flat) {
@@ -29,7 +33,12 @@ __device__ __forceinline__ unsigned long long mg_key(float score, int flat) {
     return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)flat);
 }
 
-// grid ceil(n_items K T / 8), 256 threads
+// grid ceil(n_items K T / 8), 256 threads, mg::SCORE_SMEM bytes of shared memory.
+// A row of V floats starts at any 4-byte boundary (V = 1025): the warp reads
+// the 16-byte chunks that cover its two rows (aligned asynchronous copies, all
+// in flight at once) into shared memory and takes element v at v + lead-in.
+// A chunk that holds a byte of the row lies in the row's own memory page, so
+// the few floats read past either end of a row are never out of a mapping.
 __global__ void __launch_bounds__(256) k_mg_score(const float* __restrict__ logits, int n_items, int K, int T, int V,
                                                   int S_log, int cond_pos0, int uncond_pos0,
                                                   const int32_t* __restrict__ ids, int S_ids, int cond_ids_pos0,
@@ -44,23 +53,40 @@ __global__ void __launch_bounds__(256) k_mg_score(const float* __restrict__ logi
     const int i = (int)(cell / KT), r = (int)(cell % KT), k = r / T, t = r % T;
     const float* c = logits + (((size_t)i * K + k) * S_log + cond_pos0 + t) * V;
     const float* u = logits + (((size_t)(n_items + i) * K + k) * S_log + uncond_pos0 + t) * V;
-    // every load of the lane first (predicated, no branch between them), then the arithmetic
-    float z[mg::MAXV_LANE], uu[mg::MAXV_LANE];
+    extern __shared__ float4 mg_smem[];
+    float* sc = reinterpret_cast<float*>(mg_smem) + warp * 2 * mg::ROWF;
+    float* su = sc + mg::ROWF;
+    const float4* c4 = reinterpret_cast<const float4*>(reinterpret_cast<uintptr_t>(c) & ~(uintptr_t)15);
+    const float4* u4 = reinterpret_cast<const float4*>(reinterpret_cast<uintptr_t>(u) & ~(uintptr_t)15);
+    const int shc = (int)((reinterpret_cast<uintptr_t>(c) & 15) >> 2), shu = (int)((reinterpret_cast<uintptr_t>(u) & 15) >> 2);
+    const int nqc = (shc + V + 3) >> 2, nqu = (shu + V + 3) >> 2;
+    // global -> shared without registers: every 16-byte copy of the lane in flight at once
 #pragma unroll
-    for (int j = 0; j < mg::MAXV_LANE; ++j) {
-        const int v = lane + 32 * j;
-        z[j] = v < V ? __ldg(c + v) : 0.f;
-        uu[j] = v < V ? __ldg(u + v) : 0.f;
+    for (int j = 0; j < mg::MAXQ; ++j) {
+        const int q = lane + 32 * j;
+        if (q < nqc)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(sc + 4 * q)),
+                         "l"(c4 + q)
+                         : "memory");
+        if (q < nqu)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(su + 4 * q)),
+                         "l"(u4 + q)
+                         : "memory");
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();
+    // z = c + s (c - u), one rounding per operation; pass 1: max and argmax, pass 2: sum of exp
     float mx = -INFINITY, best = -INFINITY;
     int bi = 0x7FFFFFFF;
-#pragma unroll
+#pragma unroll 4
     for (int j = 0; j < mg::MAXV_LANE; ++j) {
         const int v = lane + 32 * j;
-        z[j] = v < V ? __fadd_rn(z[j], __fmul_rn(cfg, __fsub_rn(z[j], uu[j]))) : -INFINITY;
-        mx = fmaxf(mx, z[j]);
-        const bool better = v < V && v != mask_id && (z[j] > best || bi == 0x7FFFFFFF);  // v grows with j
-        best = better ? z[j] : best;
+        if (v >= V) break;
+        const float cz = sc[v + shc];
+        const float z = __fadd_rn(cz, __fmul_rn(cfg, __fsub_rn(cz, su[v + shu])));
+        mx = fmaxf(mx, z);
+        const bool better = v != mask_id && (z > best || bi == 0x7FFFFFFF);  // v grows with j
+        best = better ? z : best;
         bi = better ? v : bi;
     }
 #pragma unroll
@@ -74,9 +100,13 @@ __global__ void __launch_bounds__(256) k_mg_score(const float* __restrict__ logi
         }
     }
     float sum = 0.f;
-#pragma unroll
-    for (int j = 0; j < mg::MAXV_LANE; ++j)
-        if (lane + 32 * j < V) sum += expf(z[j] - mx);
+#pragma unroll 4
+    for (int j = 0; j < mg::MAXV_LANE; ++j) {
+        const int v = lane + 32 * j;
+        if (v >= V) break;
+        const float cz = sc[v + shc];
+        sum += expf(__fadd_rn(cz, __fmul_rn(cfg, __fsub_rn(cz, su[v + shu]))) - mx);
+    }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (lane == 0) {
@@ -187,7 +217,12 @@ int launch_maskgit_update(const float* logits, int n_items, int K, int T, int V,
                           cudaStream_t st) {
     const long cells = (long)n_items * K * T;
     if (cells <= 0) return 0;
-    launch_pdl(k_mg_score, (unsigned)((cells + 7) / 8), 256, 0, st, logits, n_items, K, T, V, S_log, cond_pos0,
+    static const bool attr = [] {
+        cudaFuncSetAttribute(k_mg_score, cudaFuncAttributeMaxDynamicSharedMemorySize, mg::SCORE_SMEM);
+        return true;
+    }();
+    (void)attr;
+    launch_pdl(k_mg_score, (unsigned)((cells + 7) / 8), 256, mg::SCORE_SMEM, st, logits, n_items, K, T, V, S_log, cond_pos0,
                uncond_pos0, (const int32_t*)ids, S_ids, cond_ids_pos0, mask_id, cfg, penalty, keys, pred);
     launch_pdl(k_mg_select, n_items, mg::SELECT_NT, 0, st, (const unsigned long long*)keys, (const int32_t*)pred,
                n_items, K, T, n_unmask, ids, S_ids, cond_ids_pos0, uncond_ids_pos0);
