@@ -187,6 +187,11 @@ int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B
 int launch_attn_prefill(const bf16* q, KVView kv, const int32_t* seq_start, const int32_t* seq_len,
                          const int32_t* key_len, int causal, int B, int S, bf16* out, cudaStream_t st,
                          bf16* out_lo = nullptr);
+// Causal prefill attention on tcgen05 over one layer's paged pool (pool_blocks blocks): query s of
+// sequence b at position seq_start[b] + s sees keys 0 .. that position; out_lo (optional) low parts.
+// With fp32 queries qf (non-null) Q and P enter the products as bf16 high + low parts; else bf16 q.
+int launch_attn_causal_tc(const bf16* q, const float* qf, KVView kv, size_t pool_blocks, const int32_t* seq_start,
+                          int B, int S, bf16* out, bf16* out_lo, int* err, cudaStream_t st);
 // out[b * stride] = unpacked argmax
 int launch_argmax_finalize(const unsigned long long* amax, int32_t* out, int stride, int B, cudaStream_t st);
 

@@ -6,11 +6,14 @@
 // add), snake, conv2 (32 -> 1, k 7): 960 samples per frame.
 //
 // Activations are fp32 [B][C][T]. k_dac_conv computes a 64-channel x
-// 128-sample output tile per CTA (a thread 4 channels x 8 samples): input
-// channels in chunks of 16, their snake'd input window (128 + (K - 1) d
-// samples, zero outside the sequence: the snake of 0 is 0) and the weight
-// slice staged in shared memory; bias and an optional residual (read and
-// written by the same thread, so the add can be in place) in the epilogue.
+// 128-sample output tile per CTA: input channels in chunks of 16, their
+// snake'd input window (128 + (K - 1) d samples, zero outside the sequence:
+// the snake of 0 is 0) and the weight slice staged in shared memory. A thread
+// owns 4 output channels x two runs of 4 contiguous samples (64 apart); per
+// input channel it reads each run's window of 4 + (K - 1) d samples once, as
+// 16-byte loads that are contiguous across the warp, and applies every tap
+// from registers. Bias and an optional residual (read and written by the same
+// thread, so the add can be in place) in the epilogue.
 // k_dac_convT is output-stationary: with K = 2 s, output sample o takes input
 // samples q / s and q / s - 1 (q = o + p) through taps q mod s and q mod s + s.
 #include <algorithm>
@@ -28,7 +31,7 @@ namespace dac {
 constexpr int RATIOS[5] = {8, 5, 4, 2, 3};
 constexpr int CH[6] = {1024, 512, 256, 128, 64, 32};
 constexpr int DIL[3] = {1, 3, 9};
-constexpr int TO = 128, TOC = 64, ICC = 16, NT = 256, MAXW = TO + 6 * 9;
+constexpr int TO = 128, TOC = 64, ICC = 16, NT = 256, MAXW = TO + 6 * 9 + 2;  // + the last window's 16-byte tail
 constexpr int ICC_T = 8, MAXK_T = 16, MAXW_T = TO / 2 + 3;
 }  // namespace dac
 
@@ -56,17 +59,21 @@ __device__ __forceinline__ float dac_snake(float x, float a) {
 
 // y[b][oc][t] = bias[oc] + sum_ic sum_k w[oc][ic][k] snake(x[b][ic][t + k dil - pad]) (+ res[b][oc][t])
 // x element (b, ic, t) at x + b xb + ic xc + t xt. grid (ceil(T_out / 128), ceil(OC / 64), B), 256 threads.
-template <int K>
+// Thread (ty, tx): channels oc0 + 4 ty + q, samples t0 + 4 tx + 64 h + j (q, j < 4, h < 2).
+template <int K, int DIL>
 __global__ void __launch_bounds__(dac::NT) k_dac_conv(const float* __restrict__ x, long xb, long xc, long xt,
                                                       const float* __restrict__ alpha, const float* __restrict__ w,
                                                       const float* __restrict__ bias, const float* res, float* y, int IC,
-                                                      int OC, int T_in, int T_out, int dil, int pad) {
+                                                      int OC, int T_in, int T_out, int pad) {
     using namespace dac;
-    __shared__ float xs[ICC][MAXW];
-    __shared__ float ws[TOC][ICC][K];
+    constexpr int KP = (K + 3) & ~3;                    // taps padded to whole 16-byte rows
+    constexpr int NWIN = (4 + (K - 1) * DIL + 3) / 4;   // 16-byte pieces of one run's window
+    __shared__ __align__(16) float xs[ICC][MAXW];
+    __shared__ __align__(16) float ws[TOC][ICC][KP];
+    static_assert(4 * 15 + 64 + 4 * NWIN <= MAXW, "window past the staged row");
     const int t0 = blockIdx.x * TO, oc0 = blockIdx.y * TOC, b = blockIdx.z;
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    const int W = TO + (K - 1) * dil;
+    const int W = TO + (K - 1) * DIL;
     const float* xbp = x + (size_t)b * xb;
     float acc[4][8];
 #pragma unroll
@@ -74,34 +81,45 @@ __global__ void __launch_bounds__(dac::NT) k_dac_conv(const float* __restrict__ 
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[q][j] = 0.f;
     for (int ic0 = 0; ic0 < IC; ic0 += ICC) {
-        for (int i = tid; i < ICC * W; i += NT) {
-            const int c = i / W, tt = i - c * W, ic = ic0 + c, ti = t0 + tt - pad;
+        for (int i = tid; i < ICC * MAXW; i += NT) {
+            const int c = i / MAXW, tt = i - c * MAXW, ic = ic0 + c, ti = t0 + tt - pad;
             float v = 0.f;
-            if (ic < IC && ti >= 0 && ti < T_in) {
+            if (tt < W && ic < IC && ti >= 0 && ti < T_in) {
                 v = xbp[(size_t)ic * xc + (size_t)ti * xt];
                 if (alpha) v = dac_snake(v, alpha[ic]);
             }
             xs[c][tt] = v;
         }
-        for (int i = tid; i < TOC * ICC * K; i += NT) {
-            const int o = i / (ICC * K), r = i - o * (ICC * K), c = r / K, k = r - c * K;
+        for (int i = tid; i < TOC * ICC * KP; i += NT) {
+            const int o = i / (ICC * KP), r = i - o * (ICC * KP), c = r / KP, k = r - c * KP;
             const int oc = oc0 + o, ic = ic0 + c;
-            ws[o][c][k] = (oc < OC && ic < IC) ? w[((size_t)oc * IC + ic) * K + k] : 0.f;
+            ws[o][c][k] = (k < K && oc < OC && ic < IC) ? w[((size_t)oc * IC + ic) * K + k] : 0.f;
         }
         __syncthreads();
-#pragma unroll 4
+#pragma unroll 2
         for (int c = 0; c < ICC; ++c) {
+            float wv[4][KP];
 #pragma unroll
-            for (int k = 0; k < K; ++k) {
-                float xv[8], wv[4];
+            for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) xv[j] = xs[c][tx + 16 * j + k * dil];
+                for (int k4 = 0; k4 < KP; k4 += 4) {
+                    const float4 f = *reinterpret_cast<const float4*>(&ws[ty * 4 + q][c][k4]);
+                    wv[q][k4] = f.x; wv[q][k4 + 1] = f.y; wv[q][k4 + 2] = f.z; wv[q][k4 + 3] = f.w;
+                }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) wv[q] = ws[ty * 4 + q][c][k];
+            for (int h = 0; h < 2; ++h) {
+                float xv[4 * NWIN];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
+                for (int p4 = 0; p4 < NWIN; ++p4) {
+                    const float4 f = *reinterpret_cast<const float4*>(&xs[c][4 * tx + 64 * h + 4 * p4]);
+                    xv[4 * p4] = f.x; xv[4 * p4 + 1] = f.y; xv[4 * p4 + 2] = f.z; xv[4 * p4 + 3] = f.w;
+                }
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[q][j] = fmaf(wv[q], xv[j], acc[q][j]);
+                for (int k = 0; k < K; ++k)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) acc[q][4 * h + j] = fmaf(wv[q][k], xv[j + k * DIL], acc[q][4 * h + j]);
             }
         }
         __syncthreads();
@@ -113,7 +131,7 @@ __global__ void __launch_bounds__(dac::NT) k_dac_conv(const float* __restrict__ 
         const float bv = bias[oc];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int t = t0 + tx + 16 * j;
+            const int t = t0 + 4 * tx + 64 * (j >> 2) + (j & 3);
             if (t >= T_out) continue;
             const size_t o = ((size_t)b * OC + oc) * T_out + t;
             float v = acc[q][j] + bv;
@@ -199,9 +217,13 @@ void conv(tts_bb_dac* d, const float* x, long xb, long xc, long xt, const float*
           int pad) {
     dim3 grid((T_out + dac::TO - 1) / dac::TO, (OC + dac::TOC - 1) / dac::TOC, B);
     if (K == 1)
-        k_dac_conv<1><<<grid, dac::NT, 0, d->st>>>(x, xb, xc, xt, alpha, w, bias, res, y, IC, OC, T_in, T_out, dil, pad);
+        k_dac_conv<1, 1><<<grid, dac::NT, 0, d->st>>>(x, xb, xc, xt, alpha, w, bias, res, y, IC, OC, T_in, T_out, pad);
+    else if (dil == 1)
+        k_dac_conv<7, 1><<<grid, dac::NT, 0, d->st>>>(x, xb, xc, xt, alpha, w, bias, res, y, IC, OC, T_in, T_out, pad);
+    else if (dil == 3)
+        k_dac_conv<7, 3><<<grid, dac::NT, 0, d->st>>>(x, xb, xc, xt, alpha, w, bias, res, y, IC, OC, T_in, T_out, pad);
     else
-        k_dac_conv<7><<<grid, dac::NT, 0, d->st>>>(x, xb, xc, xt, alpha, w, bias, res, y, IC, OC, T_in, T_out, dil, pad);
+        k_dac_conv<7, 9><<<grid, dac::NT, 0, d->st>>>(x, xb, xc, xt, alpha, w, bias, res, y, IC, OC, T_in, T_out, pad);
 }
 
 }  // namespace

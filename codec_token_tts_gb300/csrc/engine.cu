@@ -219,6 +219,7 @@ struct tts_bb {
     int32_t *seq_slot = nullptr, *seq_start = nullptr, *seq_len = nullptr, *key_len = nullptr;
     bf16* mg_pool = nullptr;
     bool attn_bidir_tc = false;
+    bool attn_causal_tc = false;        // causal prefill of 64 or more positions per sequence on tcgen05
     int32_t* hx_ids = nullptr;  // tts_bb_decode_step_host: device copies of the caller's host ids and argmax
     int32_t* hx_am = nullptr;
     float* hx_logits = nullptr;
@@ -380,10 +381,11 @@ tts_bb_status finish(tts_bb* h) {
 }
 
 enum Kind { K_SETUP, K_EMBED, K_RMSNORM, K_GEMV, K_GEMM, K_QKROPE, K_ATTN_DECODE, K_ATTN_PREFILL, K_ARGMAX,
-            K_KVCOPY, K_MEGA, K_GEMM_TC, K_GEMM_TCD, K_ATTN_BIDIR_TC, K_MG_UPDATE, K_FRAME, K_NKINDS };
+            K_KVCOPY, K_MEGA, K_GEMM_TC, K_GEMM_TCD, K_ATTN_BIDIR_TC, K_MG_UPDATE, K_FRAME, K_ATTN_CAUSAL_TC, K_NKINDS };
 const char* kind_name[K_NKINDS] = {"setup", "embed_gather", "rmsnorm", "gemv", "gemm_mma_split", "qk_norm_rope_append",
                                    "attn_decode", "attn_prefill", "argmax", "kv_copy", "decode_step_persistent",
-                                   "gemm_tcgen05", "gemm_tcgen05_decode", "attn_bidir_tcgen05", "maskgit_update", "frame_glue"};
+                                   "gemm_tcgen05", "gemm_tcgen05_decode", "attn_bidir_tcgen05", "maskgit_update", "frame_glue",
+                                   "attn_causal_tcgen05"};
 
 cudaEvent_t prof_event(tts_bb* h) {
     if (!h->ev_pool.empty()) {
@@ -468,6 +470,9 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
     const int T = B * tok_per_seq;
     // the bidirectional pass keeps K / V in its own pool (no page table), which the tcgen05 kernel reads by TMA
     const bool bidir_tc = mode == 2 && h->attn_bidir_tc;
+    // a causal prefill of a full 64-query tile per sequence or more runs on tcgen05 from fp32
+    // queries (shorter ones stay on the mma.sync kernel)
+    const bool causal_tc = mode == 1 && h->attn_causal_tc && tok_per_seq >= 64;
     for (int l = 0; l < c.n_layers; ++l) {
         const LayerW& w = h->L[l];
         KVView kv = kv_base;
@@ -489,13 +494,17 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         { Launch L(h, K_QKROPE, T * (4.0 * QKV + 2.0 * QKV));
           L += launch_qk_norm_rope_append(h->qkv, w.qn, w.kn, h->cos_t, h->sin_t, c.rms_eps, h->q, kv,
                                           h->seq_start, h->seq_len, tok_per_seq, T, h->err, h->st,
-                                          mode == 0 ? h->qf : nullptr); }
+                                          mode == 0 || causal_tc ? h->qf : nullptr); }
         if (bidir_tc) {
             Launch L(h, K_ATTN_BIDIR_TC, 0, attn_flops);
             L += launch_attn_bidir_tc(h->q, kv.pool, h->mg_pool_blocks, kv.mbps, h->key_len, B, tok_per_seq, h->ao, h->err, h->st);
         } else if (mode == 0) {
             Launch L(h, K_ATTN_DECODE, kv_read_bytes + T * (2.0 * NQ * HD * 2), 4.0 * NQ * HD * (kv_read_bytes / (2.0 * NKV * HD * 2)));
             L += launch_attn_decode(h->q, kv, h->seq_start, B, max_len, h->part, h->ao, MAX_SPLITS, h->st, aolo, h->qf);
+        } else if (causal_tc) {
+            Launch L(h, K_ATTN_CAUSAL_TC, 0, attn_flops);
+            L += launch_attn_causal_tc(h->q, h->qf, kv, (size_t)h->kv_blocks, h->seq_start, B, tok_per_seq, h->ao, aolo,
+                                       h->err, h->st);
         } else {
             Launch L(h, K_ATTN_PREFILL, 0, attn_flops);
             L += launch_attn_prefill(h->q, kv, h->seq_start, h->seq_len, h->key_len, mode == 1, B, tok_per_seq, h->ao, h->st,
@@ -883,6 +892,8 @@ static tts_bb_status create_impl(const tts_bb_config* cfg, const tts_bb_weights*
     {
         const char* av = std::getenv("TTS_BB_BIDIR_ATTN");  // "mma": the mma.sync flash kernel for the bidirectional pass
         h->attn_bidir_tc = gemm_tc_available() && !(av && std::strcmp(av, "mma") == 0);
+        const char* pv = std::getenv("TTS_BB_PREFILL_ATTN");  // "mma": the mma.sync flash kernel for the causal prefill
+        h->attn_causal_tc = gemm_tc_available() && !(pv && std::strcmp(pv, "mma") == 0);
     }
     if (c.max_slots > 0) {  // graph-replayed decode steps: step block, staging ring, fixed input / output buffers
         const char* gv = std::getenv("TTS_BB_GRAPHS");

@@ -344,7 +344,8 @@ __global__ void __launch_bounds__(256) k_attn_prefill(const bf16* __restrict__ q
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float m = mrow[e >> 1];
-                const float p = (m == -INFINITY) ? 0.f : exp2f(s[n][e] - m);
+                // rounded to bf16 here, as P V will use it: the row sum then matches the weights applied
+                const float p = bf2f(f2bf((m == -INFINITY) ? 0.f : exp2f(s[n][e] - m)));
                 s[n][e] = p;
                 ls[e >> 1] += p;
             }

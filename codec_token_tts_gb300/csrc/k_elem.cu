@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(256) k_qk_norm_rope_append(
         uint2 w;
         w.x = *reinterpret_cast<uint32_t*>(&a);
         w.y = *reinterpret_cast<uint32_t*>(&b);
-        if (isq && qout_f) {  // fp32 queries (the decode attention reads them unrounded)
+        if (isq && qout_f) {  // fp32 queries (decode and tcgen05 causal prefill attention read them unrounded)
             const float4 f4 = valid ? make_float4(o[0], o[1], o[2], o[3]) : make_float4(0.f, 0.f, 0.f, 0.f);
             *reinterpret_cast<float4*>(qout_f + (size_t)t * NQ * HD + hh * HD + lane * 4) = f4;
         } else if (isq) {

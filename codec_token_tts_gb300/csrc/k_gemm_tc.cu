@@ -667,13 +667,26 @@ __global__ void __launch_bounds__(tcd::NT, 1)
 // are rescaled, so P stays <= 2^8 and the result is exact up to rounding;
 // with P double-buffered the softmax of tile j + 1 runs while the tensor
 // cores do P V of tile j. Every wait is bounded.
+// The precise variant (causal prefill, whose K / V feed every later step)
+// carries Q and P as bf16 high + low parts (x = hi + lo to ~2^-17): S = Q_hi
+// K^T + Q_lo K^T and O += P_hi V + P_lo V, from fp32 queries. Its tiles fit
+// the same 224 KB with one K stage and one (hi + lo) P buffer: the K copy of
+// tile j + 1 and its S product overlap the softmax of tile j, which is the
+// longer part of a tile.
 namespace at {
-constexpr int BQ = 64, ROWS = 128, BKV = 128, NT = 320, STAGES = 2;
+constexpr int BQ = 64, ROWS = 128, BKV = 128, NT = 320;
 constexpr int CHUNK = ROWS * 128;                 // 128 rows x 128 B, 128-byte swizzled
-constexpr int Q_OFF = 0, K_OFF = 2 * CHUNK, V_OFF = K_OFF + STAGES * 2 * CHUNK, P_OFF = V_OFF + STAGES * 2 * CHUNK;
-constexpr int BAR_OFF = P_OFF + 2 * 2 * CHUNK;    // 224 KB of tiles, then barriers
-constexpr int PM_OFF = BAR_OFF + 256;             // [2 tile parities][2 halves][128 rows] fp32 row maxima
-constexpr int SMEM = PM_OFF + 2 * 2 * ROWS * 4;   // the tiles start the (1 KB-aligned) dynamic shared memory
+constexpr int TILE = 2 * CHUNK;                   // 128 rows x 128 bf16: two 64-column chunks
+template <bool PRECISE>
+struct Lay {
+    static constexpr int KST = PRECISE ? 1 : 2, VST = 2, NPB = PRECISE ? 1 : 2;  // K, V stages; P buffers
+    static constexpr int Q_OFF = 0, QL_OFF = TILE;                               // QL: precise only
+    static constexpr int K_OFF = (PRECISE ? 2 : 1) * TILE, V_OFF = K_OFF + KST * TILE, P_OFF = V_OFF + VST * TILE;
+    static constexpr int PL_OFF = P_OFF + TILE;                                  // precise only
+    static constexpr int BAR_OFF = P_OFF + (PRECISE ? 2 : NPB) * TILE;          // 224 KB of tiles, then barriers
+    static constexpr int PM_OFF = BAR_OFF + 256;  // [2 tile parities][2 halves][128 rows] fp32 row maxima
+    static constexpr int SMEM = PM_OFF + 2 * 2 * ROWS * 4;  // the tiles start the (1 KB-aligned) dynamic shared memory
+};
 constexpr int TMEM_COLS = 512;                    // S buffers at 0, 128; O at 256
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 constexpr uint32_t IDESC_PV = IDESC | (1u << 16);  // B (V) MN-major
@@ -682,7 +695,7 @@ constexpr uint32_t IDESC_PV = IDESC | (1u << 16);  // B (V) MN-major
 constexpr uint32_t V_LBO = 8192, V_SBO = 1024;
 constexpr unsigned long long TIMEOUT_NS = 1000000000ull;
 }  // namespace at
-static_assert(at::SMEM <= 232448, "shared memory per CTA");
+static_assert(at::Lay<false>::SMEM <= 232448 && at::Lay<true>::SMEM <= 232448, "shared memory per CTA");
 
 // byte offset of 16-byte piece c of row r in a 128-byte-swizzled chunk
 __device__ __forceinline__ uint32_t sw128_off(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
@@ -735,33 +748,57 @@ __device__ __forceinline__ float at_ex2(float x) {
     return y;
 }
 
-// grid (ceil(S / 64), 8, B), 320 threads. q [B*S][16][128] bf16; pool: K and V tiles [64][128] per
-// (block, KV head), [blocks][K, V][8][64][128], blocks of sequence b at b * bps; out [B*S][16][128] bf16.
+// Flash attention on tcgen05 for the dense passes: the bidirectional MaskGIT pass (every query sees
+// keys < key_len[b]) and the causal prefill (query at position seq_start[b] + s sees keys up to its
+// own position, cached keys included).
+// grid (ceil(S / 64), 8, B), 320 threads. q [B*S][16][128] bf16 (precise: qf, the same in fp32); pool: K and V tiles [64][128] per
+// (block, KV head), [blocks][K, V][8][64][128]; cache block j of sequence b is
+// page_table[seq_slot[b] * mbps + j] (j < mbps; an entry below 0 reads as zeros), or b * mbps + j
+// without a page table; out [B*S][16][128] bf16 (+ low parts out_lo, value - bf16(value), if given).
+struct AttnTcArgs {
+    const bf16* q;
+    const float* qf;            // precise variant: fp32 queries
+    const int32_t* key_len;     // bidirectional: keys per sequence
+    const int32_t* seq_start;   // causal: position of query 0 of each sequence (null: 0)
+    const int32_t* page_table;  // null: blocks of sequence b at b * mbps
+    const int32_t* seq_slot;
+    int mbps;
+    int causal;
+    int S;
+    bf16* out;
+    bf16* out_lo;
+    int* err;
+};
+template <bool PRECISE>
 __global__ void __launch_bounds__(at::NT, 1)
-    k_attn_bidir_tc(const __grid_constant__ CUtensorMap tmKV, const bf16* __restrict__ q,
-                    const int32_t* __restrict__ key_len, int S, int bps, bf16* __restrict__ out, int* err) {
+    k_attn_tc(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ AttnTcArgs A) {
+    const int S = A.S;
+    bf16* __restrict__ out = A.out;
+    int* err = A.err;
     using namespace at;
+    using Ly = Lay<PRECISE>;
+    constexpr int KST = Ly::KST, VST = Ly::VST, NPB = Ly::NPB;
     extern __shared__ __align__(1024) unsigned char smem[];
     if (s_addr(smem) & 1023u) {  // the swizzled tiles need a 1 KB-aligned base
         if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) set_err(err, ERR_LAYOUT);
         return;
     }
-    uint64_t* k_full = reinterpret_cast<uint64_t*>(smem + BAR_OFF);  // [STAGES] K of a tile landed
-    uint64_t* k_empty = k_full + STAGES;   // [STAGES] S of the tile done (K stage free)
-    uint64_t* v_full = k_empty + STAGES;   // [STAGES] V of a tile landed
-    uint64_t* v_empty = v_full + STAGES;   // [STAGES] P V of the tile done (V stage free)
-    uint64_t* s_full = v_empty + STAGES;   // [2] S buffer j & 1 written
+    uint64_t* k_full = reinterpret_cast<uint64_t*>(smem + Ly::BAR_OFF);  // [KST] K of a tile landed
+    uint64_t* k_empty = k_full + 2;        // [KST] S of the tile done (K stage free)
+    uint64_t* v_full = k_empty + 2;        // [VST] V of a tile landed
+    uint64_t* v_empty = v_full + 2;        // [VST] P V of the tile done (V stage free)
+    uint64_t* s_full = v_empty + 2;        // [2] S buffer j & 1 written
     uint64_t* p_full = s_full + 2;         // [2] P buffer j & 1 written (8 softmax-warp arrivals)
-    uint64_t* o_done = p_full + 2;         // [2] P V of a tile using P buffer j & 1 complete
+    uint64_t* o_done = p_full + 2;         // [2] P V of tile j complete, by j & 1
     uint64_t* fin = o_done + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
     volatile int* abort_s = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    float* pm = reinterpret_cast<float*>(smem + PM_OFF);
+    float* pm = reinterpret_cast<float*>(smem + Ly::PM_OFF);
     const int qt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < STAGES; ++i) {
+        for (int i = 0; i < 2; ++i) {
             tc_mbar_init(k_full + i, 1);
             tc_mbar_init(k_empty + i, 1);
             tc_mbar_init(v_full + i, 1);
@@ -783,48 +820,88 @@ __global__ void __launch_bounds__(at::NT, 1)
     }
     pdl_wait();  // q and the K / V tiles come from upstream kernels
     pdl_trigger();
-    const int L = key_len[b];
+    // keys this CTA's queries may see: causal, up to the position of its last query
+    const int start = A.causal && A.seq_start ? A.seq_start[b] : 0;
+    const int L = A.causal ? start + min(S, (qt + 1) * BQ) : A.key_len[b];
     const int nt = (L + BKV - 1) / BKV;
+    const int32_t* pt = A.page_table ? A.page_table + (size_t)A.seq_slot[b] * A.mbps : nullptr;
     // K and V tiles j of one stage: 2 cache blocks x 2 dims chunks of 64 x 64 each
     auto issue_tile = [&](int which, int j) {
-        const int st = j % STAGES;
+        const int st = j % (which ? VST : KST);
         uint64_t* full = which ? v_full : k_full;
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(full + st)),
                      "r"((uint32_t)(2 * CHUNK))
                      : "memory");
         for (int i = 0; i < 2; ++i) {
-            const int phys = b * bps + 2 * j + i;  // past the sequence: masked keys (or zero fill)
+            // blocks past the sequence hold masked keys; a block past the table reads as zeros
+            const int blk = 2 * j + i;
+            const int phys = blk >= A.mbps ? -1 : pt ? pt[blk] : b * A.mbps + blk;
             const int row = ((phys * 2 + which) * NKV + g) * KVB;
             for (int c = 0; c < 2; ++c) {
                 // K stage: [dims chunk c][keys 64i ..]; V stage: [cache block i][dims chunk c]
                 const int off = which ? i * CHUNK + c * (CHUNK / 2) : c * CHUNK + i * (CHUNK / 2);
-                tma_load_2d(smem + (which ? V_OFF : K_OFF) + st * 2 * CHUNK + off, &tmKV, c * 64, row, full + st);
+                tma_load_2d(smem + (which ? Ly::V_OFF : Ly::K_OFF) + st * TILE + off, &tmKV, c * 64, row, full + st);
             }
         }
     };
     // the first stages are requested by the thread that initialised the barriers, before Q is staged
-    const int pre = nt < STAGES ? nt : STAGES;
-    if (threadIdx.x == 0)
-        for (int j = 0; j < pre; ++j) {
-            issue_tile(0, j);
-            issue_tile(1, j);
-        }
+    const int preK = nt < KST ? nt : KST, preV = nt < VST ? nt : VST;
+    if (threadIdx.x == 0) {
+        for (int j = 0; j < preK; ++j) issue_tile(0, j);
+        for (int j = 0; j < preV; ++j) issue_tile(1, j);
+    }
     // Q rows -> shared memory, swizzled (rows past the sequence are zero); all loads first
     {
         constexpr int NQL = (ROWS * 16 + NT - 1) / NT;
-        uint4 qv[NQL];
+        if constexpr (PRECISE) {  // fp32 queries -> high and low bf16 parts
+            float4 qv[NQL][2];
 #pragma unroll
-        for (int k = 0; k < NQL; ++k) {
-            const int i = threadIdx.x + k * NT, r = (i >> 4) & (ROWS - 1), pc = i & 15;
-            const int sq = qt * BQ + (r & 63), head = 2 * g + (r >> 6);
-            qv[k] = make_uint4(0u, 0u, 0u, 0u);
-            if (i < ROWS * 16 && sq < S)
-                qv[k] = *reinterpret_cast<const uint4*>(q + (((size_t)b * S + sq) * NQ + head) * HD + pc * 8);
-        }
+            for (int k = 0; k < NQL; ++k) {
+                const int i = threadIdx.x + k * NT, r = (i >> 4) & (ROWS - 1), pc = i & 15;
+                const int sq = qt * BQ + (r & 63), head = 2 * g + (r >> 6);
+                qv[k][0] = qv[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (i < ROWS * 16 && sq < S) {
+                    const float4* src = reinterpret_cast<const float4*>(A.qf + (((size_t)b * S + sq) * NQ + head) * HD + pc * 8);
+                    qv[k][0] = src[0];
+                    qv[k][1] = src[1];
+                }
+            }
 #pragma unroll
-        for (int k = 0; k < NQL; ++k) {
-            const int i = threadIdx.x + k * NT, r = (i >> 4) & (ROWS - 1), pc = i & 15;
-            if (i < ROWS * 16) *reinterpret_cast<uint4*>(smem + Q_OFF + (pc >> 3) * CHUNK + sw128_off(r, pc & 7)) = qv[k];
+            for (int k = 0; k < NQL; ++k) {
+                const int i = threadIdx.x + k * NT, r = (i >> 4) & (ROWS - 1), pc = i & 15;
+                if (i < ROWS * 16) {
+                    const float f[8] = {qv[k][0].x, qv[k][0].y, qv[k][0].z, qv[k][0].w,
+                                        qv[k][1].x, qv[k][1].y, qv[k][1].z, qv[k][1].w};
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(f[2 * u], f[2 * u + 1]);
+                        const float2 hf = __bfloat1622float2(h2);
+                        __nv_bfloat162 l2 = __floats2bfloat162_rn(f[2 * u] - hf.x, f[2 * u + 1] - hf.y);
+                        hi[u] = *reinterpret_cast<uint32_t*>(&h2);
+                        lo[u] = *reinterpret_cast<uint32_t*>(&l2);
+                    }
+                    const uint32_t o = (pc >> 3) * CHUNK + sw128_off(r, pc & 7);
+                    *reinterpret_cast<uint4*>(smem + Ly::Q_OFF + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(smem + Ly::QL_OFF + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+            }
+        } else {
+            uint4 qv[NQL];
+#pragma unroll
+            for (int k = 0; k < NQL; ++k) {
+                const int i = threadIdx.x + k * NT, r = (i >> 4) & (ROWS - 1), pc = i & 15;
+                const int sq = qt * BQ + (r & 63), head = 2 * g + (r >> 6);
+                qv[k] = make_uint4(0u, 0u, 0u, 0u);
+                if (i < ROWS * 16 && sq < S)
+                    qv[k] = *reinterpret_cast<const uint4*>(A.q + (((size_t)b * S + sq) * NQ + head) * HD + pc * 8);
+            }
+#pragma unroll
+            for (int k = 0; k < NQL; ++k) {
+                const int i = threadIdx.x + k * NT, r = (i >> 4) & (ROWS - 1), pc = i & 15;
+                if (i < ROWS * 16)
+                    *reinterpret_cast<uint4*>(smem + Ly::Q_OFF + (pc >> 3) * CHUNK + sw128_off(r, pc & 7)) = qv[k];
+            }
         }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q (generic writes) -> tensor core reads
@@ -835,13 +912,13 @@ __global__ void __launch_bounds__(at::NT, 1)
 
     if (warp == 0) {
         if (lane < 2) {  // ---------------- TMA producers: lane 0 K, lane 1 V of each 128-key tile
-            const int which = lane;
+            const int which = lane, ST = which ? VST : KST;
             uint64_t* full = which ? v_full : k_full;
             uint64_t* empty = which ? v_empty : k_empty;
-            int issued = pre;
-            for (int j = pre; j < nt; ++j) {
-                const int st = j % STAGES;
-                if (!tc_wait(empty + st, ((j / STAGES) - 1) & 1, abort_s)) {
+            int issued = which ? preV : preK;
+            for (int j = issued; j < nt; ++j) {
+                const int st = j % ST;
+                if (!tc_wait(empty + st, ((j / ST) - 1) & 1, abort_s)) {
                     *abort_s = 1;
                     break;
                 }
@@ -849,22 +926,29 @@ __global__ void __launch_bounds__(at::NT, 1)
                 ++issued;
             }
             if (*abort_s)
-                for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j) {
+                for (int j = issued > ST ? issued - ST : 0; j < issued; ++j) {
                     const unsigned long long t0 = g_time();
-                    while (!tc_mbar_try(full + j % STAGES, (j / STAGES) & 1) && g_time() - t0 < TIMEOUT_NS) {
+                    while (!tc_mbar_try(full + j % ST, (j / ST) & 1) && g_time() - t0 < TIMEOUT_NS) {
                     }
                 }
         }
     } else if (warp == 1) {
         if (lane == 0) {  // ---------------- MMA issuer
-            const uint32_t q0 = s_addr(smem + Q_OFF);
-            auto issue_s = [&](int j) {  // S_j = Q K_j^T into buffer j & 1
-                const int st = j % STAGES;
-                const uint32_t k0 = s_addr(smem + K_OFF + st * 2 * CHUNK), d = tmem + (uint32_t)((j & 1) * 128);
+            const uint32_t q0 = s_addr(smem + Ly::Q_OFF), ql0 = s_addr(smem + Ly::QL_OFF);
+            auto issue_s = [&](int j) {  // S_j = Q K_j^T into buffer j & 1 (precise: + Q_lo K_j^T)
+                const int st = j % KST;
+                const uint32_t k0 = s_addr(smem + Ly::K_OFF + st * TILE), d = tmem + (uint32_t)((j & 1) * 128);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = (uint32_t)((kk >> 2) * CHUNK + (kk & 3) * 32);
                     at_mma(d, sw128_desc(q0 + off), sw128_desc(k0 + off), IDESC, kk ? 1u : 0u);
+                }
+                if constexpr (PRECISE) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (uint32_t)((kk >> 2) * CHUNK + (kk & 3) * 32);
+                        at_mma(d, sw128_desc(ql0 + off), sw128_desc(k0 + off), IDESC, 1u);
+                    }
                 }
                 at_commit(s_full + (j & 1));
                 at_commit(k_empty + st);
@@ -876,20 +960,29 @@ __global__ void __launch_bounds__(at::NT, 1)
             }
             for (int j = 0; j < nt && ok; ++j) {
                 if (j + 1 < nt) {  // S buffer (j+1) & 1 was read by the softmax of tile j - 1 (p_full waited)
-                    if (!tc_wait(k_full + (j + 1) % STAGES, ((j + 1) / STAGES) & 1, abort_s)) { ok = false; break; }
+                    if (!tc_wait(k_full + (j + 1) % KST, ((j + 1) / KST) & 1, abort_s)) { ok = false; break; }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                     issue_s(j + 1);
                 }
                 if (!tc_wait(p_full + (j & 1), (j >> 1) & 1, abort_s)) { ok = false; break; }
-                if (!tc_wait(v_full + j % STAGES, (j / STAGES) & 1, abort_s)) { ok = false; break; }
+                if (!tc_wait(v_full + j % VST, (j / VST) & 1, abort_s)) { ok = false; break; }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const int st = j % STAGES;
-                const uint32_t p0 = s_addr(smem + P_OFF + (j & 1) * 2 * CHUNK), v0 = s_addr(smem + V_OFF + st * 2 * CHUNK);
+                const int st = j % VST;
+                const uint32_t p0 = s_addr(smem + Ly::P_OFF + (j % NPB) * TILE), v0 = s_addr(smem + Ly::V_OFF + st * TILE);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step: P chunk kk >> 2, V block kk >> 2, 8-key groups 2 (kk & 3)
                     const uint64_t ad = sw128_desc(p0 + (uint32_t)((kk >> 2) * CHUNK + (kk & 3) * 32));
                     const uint64_t bd = sw128_desc_mn(v0 + (uint32_t)((kk >> 2) * CHUNK + (kk & 3) * 2048), V_LBO, V_SBO);
                     at_mma(tmem + 256, ad, bd, IDESC_PV, (j | kk) ? 1u : 0u);
+                }
+                if constexpr (PRECISE) {
+                    const uint32_t pl0 = s_addr(smem + Ly::PL_OFF);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t ad = sw128_desc(pl0 + (uint32_t)((kk >> 2) * CHUNK + (kk & 3) * 32));
+                        const uint64_t bd = sw128_desc_mn(v0 + (uint32_t)((kk >> 2) * CHUNK + (kk & 3) * 2048), V_LBO, V_SBO);
+                        at_mma(tmem + 256, ad, bd, IDESC_PV, 1u);
+                    }
                 }
                 at_commit(o_done + (j & 1));
                 at_commit(v_empty + st);
@@ -907,6 +1000,8 @@ __global__ void __launch_bounds__(at::NT, 1)
         const uint32_t cbase = (uint32_t)(half * 64);
         const float sc = rsqrtf((float)HD) * 1.4426950408889634f;
         float m_used = -INFINITY, l = 0.f;
+        // keys this row sees: causal, up to its own position
+        const int row_lim = A.causal ? start + qt * BQ + (r & 63) + 1 : L;
         // the two warps of a row quarter meet at a named barrier once per tile and twice after the
         // loop; after a failed wait a warp keeps meeting them (skipping the work), so neither can hang
         bool ok = true;
@@ -917,7 +1012,7 @@ __global__ void __launch_bounds__(at::NT, 1)
         for (int j = 0; j < nt; ++j) {
             uint32_t v[64];
             float mh = -INFINITY;
-            const int kvalid = L - j * BKV - half * 64;  // keys of this half below the sequence's key length
+            const int kvalid = row_lim - j * BKV - half * 64;  // keys of this half the row may see
             wait_u(s_full + (j & 1), (j >> 1) & 1);
             if (ok) {
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -947,8 +1042,8 @@ __global__ void __launch_bounds__(at::NT, 1)
                 alpha = (m_used == -INFINITY) ? 0.f : at_ex2(m_used - mx);
                 m_used = mx;
             }
-            // P buffer j & 1 was read by P V of tile j - 2
-            if (j >= 2) wait_u(o_done + (j & 1), ((j - 2) >> 1) & 1);
+            // the P buffer of tile j was read by P V of tile j - NPB
+            if (j >= NPB) wait_u(o_done + ((j - NPB) & 1), ((j - NPB) >> 1) & 1);
             if (ok && move && j >= 1) {  // rescale this half of O once P V of tile j - 1 is in it
                 wait_u(o_done + ((j - 1) & 1), ((j - 1) >> 1) & 1);
                 if (ok) {
@@ -968,22 +1063,35 @@ __global__ void __launch_bounds__(at::NT, 1)
             l *= alpha;
             float l4[4] = {0.f, 0.f, 0.f, 0.f};
             // this half's keys are key chunk `half` of the P buffer (64 keys = one 128-byte row)
-            unsigned char* prow = smem + P_OFF + (j & 1) * 2 * CHUNK + half * CHUNK;
+            unsigned char* prow = smem + Ly::P_OFF + (j % NPB) * TILE + half * CHUNK;
+            unsigned char* plrow = smem + Ly::PL_OFF + half * CHUNK;  // precise only
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {
-                uint32_t pk[16];
+                uint32_t pk[16], pl[16];
 #pragma unroll
                 for (int x = 0; x < 32; x += 2) {
                     const float p0 = at_ex2(fmaf(__uint_as_float(v[ch * 32 + x]), sc, -m_used));
                     const float p1 = at_ex2(fmaf(__uint_as_float(v[ch * 32 + x + 1]), sc, -m_used));
-                    l4[(x >> 1) & 3] += p0 + p1;
                     __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
                     pk[x >> 1] = *reinterpret_cast<uint32_t*>(&h2);
+                    const float2 pr = __bfloat1622float2(h2);  // the row sum takes the weights P V applies
+                    if constexpr (PRECISE) {
+                        __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - pr.x, p1 - pr.y);
+                        pl[x >> 1] = *reinterpret_cast<uint32_t*>(&l2);
+                        const float2 lr = __bfloat1622float2(l2);
+                        l4[(x >> 1) & 3] += (pr.x + lr.x) + (pr.y + lr.y);
+                    } else {
+                        l4[(x >> 1) & 3] += pr.x + pr.y;
+                    }
                 }
 #pragma unroll
-                for (int pp = 0; pp < 4; ++pp)
+                for (int pp = 0; pp < 4; ++pp) {
                     *reinterpret_cast<uint4*>(prow + sw128_off(r, ch * 4 + pp)) =
                         make_uint4(pk[4 * pp], pk[4 * pp + 1], pk[4 * pp + 2], pk[4 * pp + 3]);
+                    if constexpr (PRECISE)
+                        *reinterpret_cast<uint4*>(plrow + sw128_off(r, ch * 4 + pp)) =
+                            make_uint4(pl[4 * pp], pl[4 * pp + 1], pl[4 * pp + 2], pl[4 * pp + 3]);
+                }
             }
             l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P (generic writes) -> tensor core reads
@@ -1007,17 +1115,21 @@ __global__ void __launch_bounds__(at::NT, 1)
                 tm_ld32_nw(lane_base + 256 + cbase + ch * 32, o);
                 tm_wait_ld();
                 if (sq < S) {
-                    bf16* dst = out + (((size_t)b * S + sq) * NQ + head) * HD + cbase + ch * 32;
+                    const size_t off = (((size_t)b * S + sq) * NQ + head) * HD + cbase + ch * 32;
 #pragma unroll
                     for (int x = 0; x < 32; x += 8) {
-                        uint32_t w[4];
+                        uint32_t w[4], wl[4];
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
-                            __nv_bfloat162 a2 = __floats2bfloat162_rn(__uint_as_float(o[x + 2 * u]) * inv,
-                                                                      __uint_as_float(o[x + 2 * u + 1]) * inv);
+                            const float f0 = __uint_as_float(o[x + 2 * u]) * inv, f1 = __uint_as_float(o[x + 2 * u + 1]) * inv;
+                            __nv_bfloat162 a2 = __floats2bfloat162_rn(f0, f1);
                             w[u] = *reinterpret_cast<uint32_t*>(&a2);
+                            const float2 hf = __bfloat1622float2(a2);
+                            __nv_bfloat162 l2 = __floats2bfloat162_rn(f0 - hf.x, f1 - hf.y);
+                            wl[u] = *reinterpret_cast<uint32_t*>(&l2);
                         }
-                        *reinterpret_cast<uint4*>(dst + x) = make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4*>(out + off + x) = make_uint4(w[0], w[1], w[2], w[3]);
+                        if (A.out_lo) *reinterpret_cast<uint4*>(A.out_lo + off + x) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
                     }
                 }
             }
@@ -1098,6 +1210,18 @@ static bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_
 
 bool gemm_tc_available() { return encode_fn() != nullptr; }
 
+template <bool PRECISE>
+static int launch_attn_tc(const CUtensorMap& mkv, const AttnTcArgs& A, int B, cudaStream_t st) {
+    constexpr int SMEM = at::Lay<PRECISE>::SMEM;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_attn_tc<PRECISE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        attr = true;
+    }
+    dim3 grid((A.S + at::BQ - 1) / at::BQ, NKV, B);
+    return launch_pdl(k_attn_tc<PRECISE>, grid, at::NT, SMEM, st, mkv, A) == cudaSuccess ? 1 : 0;
+}
+
 // Bidirectional attention of the MaskGIT pass on tcgen05 (no page table: sequence b's blocks at
 // b * bps). Returns launches (0 = not available).
 int launch_attn_bidir_tc(const bf16* q, const bf16* pool, size_t pool_blocks, int bps, const int32_t* key_len, int B,
@@ -1107,13 +1231,22 @@ int launch_attn_bidir_tc(const bf16* q, const bf16* pool, size_t pool_blocks, in
     if (rows > (size_t)INT32_MAX) return 0;
     CUtensorMap mkv;
     if (!make_map(&mkv, pool, (int)rows, HD, KVB)) return 0;
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_attn_bidir_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, at::SMEM);
-        attr = true;
-    }
-    dim3 grid((S + at::BQ - 1) / at::BQ, NKV, B);
-    return launch_pdl(k_attn_bidir_tc, grid, at::NT, at::SMEM, st, mkv, q, key_len, S, bps, out, err) == cudaSuccess ? 1 : 0;
+    AttnTcArgs A{q, nullptr, key_len, nullptr, nullptr, nullptr, bps, 0, S, out, nullptr, err};
+    return launch_attn_tc<false>(mkv, A, B, st);
+}
+
+// Causal prefill attention on tcgen05 over the paged cache (one layer's pool of pool_blocks
+// blocks): query s of sequence b sits at position seq_start[b] + s. With fp32 queries qf the
+// precise variant runs (Q and P as high + low parts), else bf16 q. Returns launches (0 = not available).
+int launch_attn_causal_tc(const bf16* q, const float* qf, KVView kv, size_t pool_blocks, const int32_t* seq_start,
+                          int B, int S, bf16* out, bf16* out_lo, int* err, cudaStream_t st) {
+    if (B <= 0 || S <= 0 || !gemm_tc_available()) return 0;
+    const size_t rows = pool_blocks * 2 * NKV * KVB;
+    if (rows > (size_t)INT32_MAX) return 0;
+    CUtensorMap mkv;
+    if (!make_map(&mkv, kv.pool, (int)rows, HD, KVB)) return 0;
+    AttnTcArgs A{q, qf, nullptr, seq_start, kv.page_table, kv.seq_slot, kv.mbps, 1, S, out, out_lo, err};
+    return qf ? launch_attn_tc<true>(mkv, A, B, st) : launch_attn_tc<false>(mkv, A, B, st);
 }
 
 int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N, int K, const Epi& e, int* err,

@@ -64,6 +64,11 @@ def test_talker_batch1_full():
             m.tts_bb_decode_step(e.h, 1, [0], [128 + t], fed_d[t:t + 1], 0, L[t:t + 1], A[t:t + 1],
                                  hidden_out=H[t:t + 1])
         herr = rel_err_rows(H.cpu().numpy(), hid_o)
+        _f = np.nonzero(A.cpu().numpy() != am_o)[0]
+        _t2 = np.sort(lg_o, axis=1)[:, -2:]
+        report("talker_b1_vs_fp64", argmax_raw=float(np.mean(A.cpu().numpy() == am_o)), flips=_f.tolist(),
+               gaps=(_t2[_f, 1] - _t2[_f, 0]).tolist(), logit_abs=f"{np.abs(L.cpu().numpy() - lg_o).max():.2e}",
+               mean_vs_bf16kv=f"{np.abs(L.cpu().numpy() - lg_k).mean():.3e}")
         err, agree, agree_u = check_logits_and_argmax(L.cpu().numpy(), lg_o, A.cpu().numpy(), am_o,
                                                       min_agree=ARGMAX_AGREE)
         assert herr <= HIDDEN_TOL
