@@ -105,6 +105,7 @@ def _load() -> C.CDLL:
         "tts_bb_quantizer_free": (V, [P]),
         "tts_bb_dac_create": (I, [C.POINTER(tts_bb_dac_weights), P, C.POINTER(P)]),
         "tts_bb_dac_decode": (I, [P, I, I, P, P]),
+        "tts_bb_dac_sync": (I, [P]),
         "tts_bb_dac_free": (V, [P]),
     }
     for name, (res, args) in sig.items():
@@ -121,7 +122,7 @@ EXPORTED = ("tts_bb_default_config", "tts_bb_create", "tts_bb_free", "tts_bb_pre
             "tts_bb_launch_count", "tts_bb_profile", "tts_bb_profile_report",
             "tts_bb_gqa_decode_attention_static", "tts_bb_debug_fault", "tts_bb_maskgit_update",
             "tts_bb_maskgit_schedule", "tts_bb_frame_step", "tts_bb_rvq_create", "tts_bb_rvq_decode",
-            "tts_bb_rvq_sync", "tts_bb_rvq_free", "tts_bb_dac_create", "tts_bb_dac_decode", "tts_bb_dac_free",
+            "tts_bb_rvq_sync", "tts_bb_rvq_free", "tts_bb_dac_create", "tts_bb_dac_decode", "tts_bb_dac_sync", "tts_bb_dac_free",
             "tts_bb_decode_step_host", "tts_bb_quantizer_create", "tts_bb_quantizer_decode",
             "tts_bb_quantizer_sync", "tts_bb_quantizer_free")
 
@@ -329,6 +330,10 @@ def tts_bb_dac_decode(d, B: int, T: int, features, audio, check: bool = True) ->
     if check and st != OK:
         raise TtsBbError(st, "tts_bb_dac_decode")
     return st
+
+
+def tts_bb_dac_sync(d) -> int:
+    return lib.tts_bb_dac_sync(d)
 
 
 def tts_bb_dac_free(d) -> None:

@@ -24,6 +24,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace ttsbb {
 
@@ -35,66 +36,12 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 constexpr int NT = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-5 epilogue
-constexpr unsigned long long TIMEOUT_NS = 1000000000ull;
+constexpr unsigned long long TIMEOUT_NS = TC_TIMEOUT_NS;
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (7-9 = 1),
 // B bf16 (10-12 = 1), both K-major (15, 16 = 0), N >> 3 at 17-22, M >> 4 at 24-28.
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                            ((uint32_t)(BM >> 4) << 24);
 }  // namespace tc
-
-__device__ __forceinline__ uint32_t s_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ unsigned long long g_time() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Shared-memory matrix descriptor for a K-major operand stored as 128-byte
-// rows in 128-byte-swizzle atoms of 8 rows (1024 B apart): start address >> 4
-// at bits 0-13, leading offset 16 B (unused for swizzled K-major), stride
-// offset 1024 B >> 4 at bits 32-45, descriptor version 1 at bit 46, layout
-// SWIZZLE_128B (2) at bits 61-63.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)1 << 16;
-    d |= (uint64_t)(1024 >> 4) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
-__device__ __forceinline__ void tc_mbar_init(uint64_t* b, int n) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(s_addr(b)), "r"(n));
-}
-__device__ __forceinline__ bool tc_mbar_try(uint64_t* b, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(s_addr(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait: false after TIMEOUT_NS or when *abort is set.
-__device__ __forceinline__ bool tc_wait(uint64_t* b, uint32_t parity, volatile int* abort) {
-    if (tc_mbar_try(b, parity)) return true;
-    const unsigned long long t0 = g_time();
-    for (uint32_t i = 0;; ++i) {
-        if (tc_mbar_try(b, parity)) return true;
-        if ((i & 63) == 63) {
-            if (*abort) return false;
-            if (g_time() - t0 > tc::TIMEOUT_NS) return false;
-        }
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            s_addr(dst)),
-        "l"(map), "r"(x), "r"(y), "r"(s_addr(bar))
-        : "memory");
-}
 
 __device__ __forceinline__ float silu_tc(float x) { return x / (1.f + __expf(-x)); }
 
@@ -693,60 +640,9 @@ constexpr uint32_t IDESC_PV = IDESC | (1u << 16);  // B (V) MN-major
 // V stage: [cache block i][dims 64c .. 64c+63][64 keys x 128 B]: MN-major atoms of 64 dims x 8 keys,
 // 1024 B apart along the keys (stride offset), 8 KB apart along the dims (leading offset)
 constexpr uint32_t V_LBO = 8192, V_SBO = 1024;
-constexpr unsigned long long TIMEOUT_NS = 1000000000ull;
+constexpr unsigned long long TIMEOUT_NS = TC_TIMEOUT_NS;
 }  // namespace at
 static_assert(at::Lay<false>::SMEM <= 232448 && at::Lay<true>::SMEM <= 232448, "shared memory per CTA");
-
-// byte offset of 16-byte piece c of row r in a 128-byte-swizzled chunk
-__device__ __forceinline__ uint32_t sw128_off(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
-
-// MN-major 128-byte-swizzled operand descriptor with explicit leading / stride offsets
-__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
-// 32 lanes x 32 columns of 32 bit from TMEM (no wait: tm_wait_ld before use)
-__device__ __forceinline__ void tm_ld32_nw(uint32_t taddr, uint32_t* r) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tm_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tm_st32(uint32_t taddr, const uint32_t* r) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
-        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
-        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-__device__ __forceinline__ void at_mma(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
-        "l"(ad), "l"(bd), "r"(idesc), "r"(acc));
-}
-__device__ __forceinline__ void at_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(s_addr(bar)) : "memory");
-}
-// hardware base-2 exponential (approximate, flushes denormals); ex2(-inf) = 0
-__device__ __forceinline__ float at_ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 // Flash attention on tcgen05 for the dense passes: the bidirectional MaskGIT pass (every query sees
 // keys < key_len[b]) and the causal prefill (query at position seq_start[b] + s sees keys up to its
@@ -1177,7 +1073,7 @@ static bool encode_map(CUtensorMap* m, const void* base, int rows, int K, int bo
 // the engine's activation buffers are fixed, so a decode step re-encodes
 // nothing. The cache is per process and guarded by a mutex; a full cache
 // is cleared (maps are cheap to re-encode).
-static bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
+bool tc_make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
     struct Key {
         const void* base;
         int rows, K, box;
@@ -1210,6 +1106,20 @@ static bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_
 
 bool gemm_tc_available() { return encode_fn() != nullptr; }
 
+// 4-D bf16 tensor [parts][B][T][C] (C contiguous), box 64 channels x 128 rows of one (part, item),
+// 128-byte swizzle; rows and channels outside the tensor read as zeros. Not cached.
+bool tc_make_map_rows(CUtensorMap* m, const void* base, int C, int T, int B, int parts) {
+    auto fn = encode_fn();
+    if (!fn || C % 8 != 0 || C <= 0 || T <= 0 || B <= 0 || parts <= 0) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)T, (cuuint64_t)B, (cuuint64_t)parts};
+    const cuuint64_t strides[3] = {(cuuint64_t)C * 2, (cuuint64_t)T * C * 2, (cuuint64_t)B * T * C * 2};
+    const cuuint32_t box[4] = {64, 128, 1, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool PRECISE>
 static int launch_attn_tc(const CUtensorMap& mkv, const AttnTcArgs& A, int B, cudaStream_t st) {
     constexpr int SMEM = at::Lay<PRECISE>::SMEM;
@@ -1230,7 +1140,7 @@ int launch_attn_bidir_tc(const bf16* q, const bf16* pool, size_t pool_blocks, in
     const size_t rows = pool_blocks * 2 * NKV * KVB;  // [rows][128]: K and V tiles of every (block, KV head)
     if (rows > (size_t)INT32_MAX) return 0;
     CUtensorMap mkv;
-    if (!make_map(&mkv, pool, (int)rows, HD, KVB)) return 0;
+    if (!tc_make_map(&mkv, pool, (int)rows, HD, KVB)) return 0;
     AttnTcArgs A{q, nullptr, key_len, nullptr, nullptr, nullptr, bps, 0, S, out, nullptr, err};
     return launch_attn_tc<false>(mkv, A, B, st);
 }
@@ -1244,7 +1154,7 @@ int launch_attn_causal_tc(const bf16* q, const float* qf, KVView kv, size_t pool
     const size_t rows = pool_blocks * 2 * NKV * KVB;
     if (rows > (size_t)INT32_MAX) return 0;
     CUtensorMap mkv;
-    if (!make_map(&mkv, kv.pool, (int)rows, HD, KVB)) return 0;
+    if (!tc_make_map(&mkv, kv.pool, (int)rows, HD, KVB)) return 0;
     AttnTcArgs A{q, qf, nullptr, seq_start, kv.page_table, kv.seq_slot, kv.mbps, 1, S, out, out_lo, err};
     return qf ? launch_attn_tc<true>(mkv, A, B, st) : launch_attn_tc<false>(mkv, A, B, st);
 }
@@ -1256,7 +1166,7 @@ int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N
     const int blocks = (T + tcd::MAXTB - 1) / tcd::MAXTB;  // token blocks of up to 128
     const int TB = blocks > 1 ? tcd::MAXTB : (T + 15) / 16 * 16;
     CUtensorMap mw, mh, ml;
-    if (!make_map(&mw, W, N, K, tcd::BM) || !make_map(&mh, X, T, K, TB) || !make_map(&ml, X_lo, T, K, TB)) return 0;
+    if (!tc_make_map(&mw, W, N, K, tcd::BM) || !tc_make_map(&mh, X, T, K, TB) || !tc_make_map(&ml, X_lo, T, K, TB)) return 0;
     // clusters of each size that fit at once (1 CTA per SM): S is chosen so all clusters run in one wave
     static const int cand[] = {1, 2, 3, 4, 6, 8, 12, 16};
     static int fit[8] = {-1};
@@ -1330,7 +1240,7 @@ int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N
 int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, int* err, cudaStream_t st) {
     if (T <= 0 || N <= 0 || K % tc::BK != 0) return 0;
     CUtensorMap ma, mb;
-    if (!make_map(&ma, X, T, K, tc::BM) || !make_map(&mb, W, N, K, tc::BN)) return 0;
+    if (!tc_make_map(&ma, X, T, K, tc::BM) || !tc_make_map(&mb, W, N, K, tc::BN)) return 0;
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM);

@@ -371,11 +371,19 @@ typedef struct tts_bb_dac tts_bb_dac;
 /* TTS_BB_E_INVALID for a NULL pointer, TTS_BB_E_OOM when memory runs out. */
 tts_bb_status tts_bb_dac_create(const tts_bb_dac_weights* w, void* stream, tts_bb_dac** out);
 /* features device fp32 [B][T][1024] (the RVQ decode output); audio device fp32
- * [B][960 T]. Asynchronous on the handle's stream (38 kernel launches); three
- * activation buffers of 30720 T floats per item are allocated on the first
- * call that needs more. TTS_BB_E_INVALID for NULL buffers, B < 1 or B > 65535,
- * T < 1, or B x 960 T above 2^31 - 1 samples. */
+ * [B][960 T]. Asynchronous on the handle's stream; three activation buffers of
+ * 30720 T floats per item are allocated on the first call that needs more.
+ * fc2, conv1 and every convolution of the five blocks run on the tensor cores
+ * (39 launches) with fp32 operands split into bf16 high + low parts (three
+ * products per pair, fp32 accumulation) and time-major activations; conv2 runs
+ * in fp32 on the CUDA cores. Environment TTS_BB_DAC=fp32 at create: every
+ * convolution in fp32 on the CUDA cores, channel-major (38 launches).
+ * TTS_BB_E_INVALID for NULL buffers, B < 1 or B > 65535, T < 1, or B x 960 T
+ * above 2^31 - 1 samples. */
 tts_bb_status tts_bb_dac_decode(tts_bb_dac* d, int B, int T, const float* features, float* audio);
+/* Wait for the handle's work; returns (and clears) a latched device error
+ * (TTS_BB_E_DEVICE_TIMEOUT: a bounded wait of a tensor-core kernel ran out). */
+tts_bb_status tts_bb_dac_sync(tts_bb_dac* d);
 /* Wait and free. NULL is a no-op. */
 void tts_bb_dac_free(tts_bb_dac* d);
 

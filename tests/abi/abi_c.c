@@ -71,6 +71,7 @@ int main(void) {
         memset(&dw, 0, sizeof(dw));
         EXPECT(tts_bb_dac_create(&dw, NULL, &d) == TTS_BB_E_INVALID && d == NULL);
         EXPECT(tts_bb_dac_decode(NULL, 1, 1, NULL, NULL) == TTS_BB_E_INVALID);
+        EXPECT(tts_bb_dac_sync(NULL) == TTS_BB_E_INVALID);
         tts_bb_dac_free(NULL);
     }
     EXPECT(tts_bb_maskgit_update(NULL, 1, 1, NULL, 1, 0, 0, NULL, 1, 0, 0, 1, 2.0f, 5.0f) == TTS_BB_E_INVALID);

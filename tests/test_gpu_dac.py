@@ -1,13 +1,19 @@
 """GPU parity of the DAC decoder (tts_bb_dac_decode) with the fp64 oracle.
 
-The decoder computes in fp32 (weights and activations); the oracle in fp64
-from the same fp32 weights. Tolerance: max |gpu - oracle| / max |oracle| at
-most 1e-4 over the whole waveform — fp32 rounding (2^-24) of sums of up to
-1024 x 7 products through 38 layers grows like sqrt(terms x layers) in the
-typical case, ~1e-5 relative here, with an order of magnitude of margin.
-Seeded weights are scaled by their fan-in so activations stay O(1).
+The decoder keeps weights and activations in fp32; the oracle computes in
+fp64 from the same fp32 weights. Two paths: the tensor-core convolutions
+(default: conv1 and every block convolution as implicit GEMMs on tcgen05 with
+each fp32 operand split into bf16 high + low parts, so each product is exact
+to ~2^-17 and sums accumulate in fp32) and the CUDA-core fp32 kernels
+(TTS_BB_DAC=fp32 at create). Tolerance for both: max |gpu - oracle| /
+max |oracle| at most 1e-4 over the whole waveform — rounding of ~2^-17 (split
+operands) or 2^-24 (fp32) per product in sums of up to 1024 x 7 products
+through 38 layers grows like sqrt(terms x layers) in the typical case, ~1e-5
+relative here, with an order of magnitude of margin. Seeded weights are
+scaled by their fan-in so activations stay O(1).
 """
 import math
+import os
 
 import numpy as np
 import pytest
@@ -44,18 +50,25 @@ def to_device(w):
     return torch.from_numpy(np.ascontiguousarray(w)).cuda()
 
 
-@pytest.mark.parametrize("B,T", [(1, 1), (2, 5), (1, 7), (1, 768)])
-def test_dac_matches_oracle(B, T):
-    """(1, 768) is one item of the bench's decode: 30.7 s of audio, every sample compared."""
+@pytest.mark.parametrize("path", ["tensor", "fp32"])
+@pytest.mark.parametrize("B,T", [(1, 1), (2, 5), (1, 7), (3, 130), (1, 768)])
+def test_dac_matches_oracle(B, T, path):
+    """(1, 768) is one item of the bench's decode: 30.7 s of audio, every sample compared;
+    (3, 130) spans several row tiles with a ragged tail in every block, over three items."""
     import codec_token_tts_gb300 as m
     w = dac_weights(71)
     feat = np.random.default_rng(72).normal(0, 1, (B, T, 1024)).astype(np.float32)
     wd = to_device(w)
-    d = m.tts_bb_dac_create(wd, torch.cuda.current_stream().cuda_stream)
+    if path == "fp32":
+        os.environ["TTS_BB_DAC"] = "fp32"
     try:
-        audio = torch.zeros(B, 960 * T, dtype=torch.float32, device="cuda")
+        d = m.tts_bb_dac_create(wd, torch.cuda.current_stream().cuda_stream)
+    finally:
+        os.environ.pop("TTS_BB_DAC", None)
+    try:
+        audio = torch.full((B, 960 * T), float("nan"), dtype=torch.float32, device="cuda")
         m.tts_bb_dac_decode(d, B, T, torch.from_numpy(feat).cuda(), audio)
-        torch.cuda.synchronize()
+        assert m.tts_bb_dac_sync(d) == m.OK
         got = audio.cpu().numpy().astype(np.float64)
     finally:
         m.tts_bb_dac_free(d)
