@@ -557,6 +557,64 @@ def run_dac_decode(m, stream, B=4, T=768, reps=3):
                          "tensor_flop_per_decode": tensor_flops}}
 
 
+def run_dac(steps, warmup):
+    """The DAC decode alone (4 items x 768 frames); steps decodes timed after warmup."""
+    import torch
+    import codec_token_tts_gb300 as m
+    torch.cuda.set_stream(torch.cuda.Stream())
+    return run_dac_decode(m, torch.cuda.current_stream(), reps=max(1, steps))
+
+
+def run_prefill(steps, warmup, B=16, S=2048):
+    """Batched causal prefill on the 28-layer Talker-shaped model: B sequences of S positions from
+    position 0 (bf16 N(0, 1) input rows); one step = one prefill call over all B x S tokens."""
+    import torch
+    import codec_token_tts_gb300 as m
+    from tests.gpu_util import dev_bf16_bits
+    wl = TalkerB1()
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    h = make_engine(wl, m, stream.cuda_stream, S, B, B * S, B)
+    x = dev_bf16_bits(synth.normal_bf16(synth.rng_for(11, "prefill_rows"), (B, S, 1024), 1.0))
+    slots = list(range(B))
+
+    def one():
+        m.tts_bb_prefill(h, B, S, slots, [S] * B, embeds=x)
+        for sl in slots:
+            m.tts_bb_release(h, sl)
+
+    for _ in range(warmup):
+        one()
+    m.tts_bb_sync(h)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(steps):
+        one()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    m.tts_bb_profile(h, True)
+    one()
+    rep = m.tts_bb_profile_report(h)
+    m.tts_bb_profile(h, False)
+    st = m.tts_bb_sync(h)
+    m.tts_bb_free(h)
+    ks = {k["kind"]: k for k in rep["kernels"]}
+    tot = sum(k["ms"] for k in rep["kernels"])
+    pk, _ = peaks()
+    att = ks.get("attn_causal_tcgen05") or ks.get("attn_prefill")
+    out = {"metric": "prefill tokens/s (28 layers, causal)", "workload": f"prefill: {B} sequences x {S} positions, "
+           "28-layer Talker-shaped model, bf16 N(0,1) input rows", "value": B * S / (ms / 1e3), "unit": "tokens/s",
+           "ms_per_prefill": ms, "status": st,
+           "kernel_share": {k: round(v["ms"] / tot, 4) for k, v in ks.items()}}
+    if att:
+        tf = att["flops"] / (att["ms"] / 1e3) / 1e12
+        out["attention"] = {"kind": att["kind"], "ms": att["ms"], "tflops": tf,
+                            "frac_of_measured_sustained": tf / pk["bf16_tflops_sustained"]}
+    return out
+
+
 def run_maskgit_refinement(m, h, seed, stream, n_step=32):
     """32 greedy refinement steps (pass + device update) of 4 items with CFG: rows 0-3 hold the
     conditional prompts (256 text + 768 masked target frames), rows 4-7 the unconditional ones
@@ -842,7 +900,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--no-secondary", action="store_true", help="skip the batch-64 serving, MaskGIT and Code Predictor lines")
-    ap.add_argument("--only", choices=["serving_b64", "maskgit", "code_predictor", "frame_loop"],
+    ap.add_argument("--prefill-batch", type=int, default=16, help="sequences of the --only prefill workload")
+    ap.add_argument("--only", choices=["serving_b64", "maskgit", "code_predictor", "frame_loop", "dac", "prefill"],
                     help="run one secondary workload alone (--steps / --warmup apply) and print its line; a profiling aid")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -853,8 +912,8 @@ def main():
         torch.cuda.set_device(0)
         build_lib()
         fn = {"serving_b64": run_serving_b64, "maskgit": run_maskgit, "code_predictor": run_code_predictor,
-              "frame_loop": run_frame_loop}[args.only]
-        r = fn(args.steps, args.warmup)
+              "frame_loop": run_frame_loop, "dac": run_dac, "prefill": run_prefill}[args.only]
+        r = fn(args.steps, args.warmup, B=args.prefill_batch) if args.only == "prefill" else fn(args.steps, args.warmup)
         print(json.dumps({k: v for k, v in r.items() if k != "kernel_profile"}), flush=True)
         return
 

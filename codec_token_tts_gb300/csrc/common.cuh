@@ -148,7 +148,9 @@ struct SplitK {
 // MMA per k-step.
 int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st,
                 const bf16* X_lo = nullptr, int* err = nullptr, const SplitK* sk = nullptr);
-int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, int* err, cudaStream_t st);
+// Dense persistent tcgen05 GEMM; with X_lo the activations are bf16 high + low parts (two passes over K).
+int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, int* err, cudaStream_t st,
+                   const bf16* X_lo = nullptr);
 int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N, int K, const Epi& e, int* err,
                     cudaStream_t st);
 bool gemm_tc_available();

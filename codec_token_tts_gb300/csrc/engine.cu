@@ -481,7 +481,7 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         // prefill writes the K/V that every later step reads); the bidirectional
         // pass, tensor-bound, uses plain bf16
         const bool split = mode != 2;
-        const int gk = T <= 8 ? K_GEMV : (split ? K_GEMM_TCD : K_GEMM_TC);
+        const int gk = T <= 8 ? K_GEMV : (split && T <= 256 ? K_GEMM_TCD : K_GEMM_TC);  // the kernel launch_gemm picks
         bf16* ylo = split ? h->y_lo : nullptr;
         bf16* aolo = split ? h->ao_lo : nullptr;
         bf16* mlo = split ? h->m_lo : nullptr;

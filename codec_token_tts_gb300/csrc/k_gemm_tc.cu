@@ -120,9 +120,12 @@ __device__ __forceinline__ void tc_epilogue16(const Epi& e, int t, int n0, int N
     }
 }
 
+// With split = 1 the activations come as bf16 high + low parts (tmA, tmAl): the k-loop runs over
+// K twice, Y = X_hi W^T + X_lo W^T, the second pass reading the same weight tiles (from L2).
 __global__ void __launch_bounds__(tc::NT, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int T, int N, int K,
-              const __grid_constant__ Epi e, int* err) {
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAl,
+              const __grid_constant__ CUtensorMap tmB, int split, int T, int N, int K, const __grid_constant__ Epi e,
+              int* err) {
     using namespace tc;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -136,7 +139,7 @@ __global__ void __launch_bounds__(tc::NT, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
     volatile int* abort_s = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int MT = (T + BM - 1) / BM, NTL = (N + BN - 1) / BN, tiles = MT * NTL, KT = K / BK;
+    const int MT = (T + BM - 1) / BM, NTL = (N + BN - 1) / BN, tiles = MT * NTL, KT = K / BK, KT2 = split ? 2 * KT : KT;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -168,8 +171,8 @@ __global__ void __launch_bounds__(tc::NT, 1)
             uint32_t g = 0;  // k-blocks issued
             for (int tile = blockIdx.x; tile < tiles && !*abort_s; tile += gridDim.x) {
                 const int m0 = (tile % MT) * BM, n0 = (tile / MT) * BN;
-                for (int kt = 0; kt < KT; ++kt, ++g) {
-                    const int s = g % STAGES;
+                for (int kt = 0; kt < KT2; ++kt, ++g) {
+                    const int s = g % STAGES, kx = (kt < KT ? kt : kt - KT) * BK;
                     if (g >= STAGES && !tc_wait(empty + s, ((g / STAGES) - 1) & 1, abort_s)) {
                         *abort_s = 1;
                         break;
@@ -177,8 +180,8 @@ __global__ void __launch_bounds__(tc::NT, 1)
                     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(full + s)),
                                  "r"(STAGE_BYTES)
                                  : "memory");
-                    tma_load_2d(sA + s * A_BYTES, &tmA, kt * BK, m0, full + s);
-                    tma_load_2d(sB + s * B_BYTES, &tmB, kt * BK, n0, full + s);
+                    tma_load_2d(sA + s * A_BYTES, kt < KT ? &tmA : &tmAl, kx, m0, full + s);
+                    tma_load_2d(sB + s * B_BYTES, &tmB, kx, n0, full + s);
                 }
             }
             if (*abort_s) {  // let the copies in flight (the last STAGES issued) land before the CTA can exit
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(tc::NT, 1)
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t d = tmem + (uint32_t)(buf * BN);
-                for (int kt = 0; kt < KT; ++kt, ++g) {
+                for (int kt = 0; kt < KT2; ++kt, ++g) {
                     const int s = g % STAGES;
                     if (!tc_wait(full + s, (g / STAGES) & 1, abort_s)) {
                         *abort_s = 1;
@@ -1237,10 +1240,13 @@ int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N
 
 // Y = X W^T on tcgen05. Requires K % 64 == 0, 16-byte aligned X and W rows.
 // Returns the number of kernels launched (0 if the shape is not supported).
-int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, int* err, cudaStream_t st) {
+int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, int* err, cudaStream_t st,
+                   const bf16* X_lo) {
     if (T <= 0 || N <= 0 || K % tc::BK != 0) return 0;
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mal, mb;
     if (!tc_make_map(&ma, X, T, K, tc::BM) || !tc_make_map(&mb, W, N, K, tc::BN)) return 0;
+    if (X_lo && !tc_make_map(&mal, X_lo, T, K, tc::BM)) return 0;
+    if (!X_lo) mal = ma;
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM);
@@ -1253,7 +1259,7 @@ int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi&
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     }
     const int tiles = ((N + tc::BN - 1) / tc::BN) * ((T + tc::BM - 1) / tc::BM);
-    launch_pdl(k_gemm_tc, std::min(tiles, sms), tc::NT, tc::SMEM, st, ma, mb, T, N, K, e, err);
+    launch_pdl(k_gemm_tc, std::min(tiles, sms), tc::NT, tc::SMEM, st, ma, mal, mb, X_lo ? 1 : 0, T, N, K, e, err);
     return 1;
 }
 

@@ -512,27 +512,6 @@ static int launch_splitk(const bf16* X, const bf16* X_lo, const bf16* W, int T, 
     return 1;
 }
 
-// The epilogue of token rows t0.. of a GEMM (row-wise modes only).
-static Epi epi_rows_from(const Epi& e, int t0) {
-    Epi r = e;
-    switch (e.mode) {
-        case EPI_STORE_F32:
-        case EPI_ADD_F32:
-        case EPI_LOGITS:
-            if (r.out) r.out = reinterpret_cast<float*>(r.out) + (size_t)t0 * e.ldo;
-            if (r.amax) r.amax += t0;
-            break;
-        case EPI_STORE_BF16:
-        case EPI_SWIGLU:
-            r.out = reinterpret_cast<bf16*>(r.out) + (size_t)t0 * e.ldo;
-            if (r.out_lo) r.out_lo = reinterpret_cast<bf16*>(r.out_lo) + (size_t)t0 * e.ldo;
-            break;
-        default:
-            break;
-    }
-    return r;
-}
-
 int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st, const bf16* X_lo,
                 int* err, const SplitK* skw) {
     if (T <= 0) return 0;
@@ -542,16 +521,11 @@ int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e,
         const int n = launch_gemm_tcd(X, X_lo, W, T, N, K, e, err, st);
         if (n) return n;
     }
-    if (X_lo && T > 256 && e.mode != EPI_LOGITS_PERM && gemm_tc_available()) {
-        // split activations beyond 256 tokens (a long causal prefill): 256-token slices on
-        // tcgen05 (the slices differ only in their row offset, so if the first launches all do)
-        int n = launch_gemm_tcd(X, X_lo, W, 256, N, K, e, err, st);
-        if (n) {
-            for (int t0 = 256; t0 < T; t0 += 256)
-                n += launch_gemm_tcd(X + (size_t)t0 * K, X_lo + (size_t)t0 * K, W, T - t0 < 256 ? T - t0 : 256, N, K,
-                                     epi_rows_from(e, t0), err, st);
-            return n;
-        }
+    if (X_lo && T > 256 && gemm_tc_available()) {
+        // split activations beyond 256 tokens (a causal prefill): the dense persistent kernel, two
+        // passes over K (high parts, then low parts) into the same accumulator
+        const int n = launch_gemm_tc(X, W, T, N, K, e, err, st, X_lo);
+        if (n) return n;
     }
     if (X_lo && skw) {
         const int n = launch_splitk(X, X_lo, W, T, N, K, e, *skw, st);
