@@ -49,6 +49,7 @@ struct DacTcConv {
     bf16* wp = nullptr;
     CUtensorMap map;
     int IC = 0, OC = 0, taps = 0, dil = 1, pad = 0, s = 1, po = 0, N = 0, NTL = 0, Npad = 0;
+    int bk = 64;  // channels per K chunk (32 when IC is 32)
 };
 
 struct tts_bb_dac {
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(dac::NT) k_dac_convT(const float* __restrict__
 // absolute error there is ~2^-21. Every wait is bounded.
 namespace dig {
 constexpr int BM = 128, BK = 64, MAXN = 128, NT = 320, STAGES = 3;  // warps 2-9: epilogue
-constexpr int A_BYTES = BM * BK * 2;                   // one part of an A tile
+constexpr int A_BYTES = BM * BK * 2;                   // one part of an A tile (of 64 channels at most)
 constexpr int W_BYTES = MAXN * BK * 2;                 // one part of a W tile (NTL rows used)
 constexpr int STAGE = 2 * A_BYTES + 2 * W_BYTES;       // A hi, A lo, W hi, W lo
 constexpr int BAR_OFF = STAGES * STAGE;
@@ -269,8 +270,20 @@ __device__ __forceinline__ float dac_snake_fast(float x, float a, float inv) {
 }
 static_assert(dig::SMEM <= 232448, "shared memory per CTA");
 
+// K-major operand with 64-byte rows (32 bf16) in 64-byte-swizzle atoms of 8 rows (512 B apart):
+// layout SWIZZLE_64B (4) at bits 61-63, otherwise as the 128-byte form
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(512 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)4 << 61;
+    return d;
+}
+
 struct DacIgArgs {
     int IC, OC, T_in, T_out, B;
+    int bk;               // channels per K chunk: 64 (128-byte rows) or 32 (64-byte rows, for IC = 32)
     int taps, dil, pad;   // tap k of row u reads input row u + k dil - pad
     int s, po;            // column n: channel n mod OC, output sample u s + n / OC - po
     int U, N, NTL, Npad;  // rows, columns (s OC), columns per tile, rows of one (part, tap) weight block
@@ -301,7 +314,7 @@ __global__ void __launch_bounds__(dig::NT, 1)
     float* p_inv = p_alpha + MAXOC;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int MT = (a.U + BM - 1) / BM, NTT = a.Npad / a.NTL, tiles = MT * NTT * a.B;
-    const int nch = (a.IC + BK - 1) / BK, KT = nch * a.taps;
+    const int bk = a.bk, nch = (a.IC + bk - 1) / bk, KT = nch * a.taps;
     for (int i = threadIdx.x; i < a.OC; i += blockDim.x) {  // OC <= MAXOC (checked on the host)
         p_bias[i] = a.bias[i];
         p_alpha[i] = a.alpha_out ? a.alpha_out[i] : 0.f;
@@ -334,7 +347,7 @@ __global__ void __launch_bounds__(dig::NT, 1)
     if (warp == 0) {
         if (lane == 0) {  // ---------------- TMA producer: the stage ring runs on across tiles
             uint32_t g = 0;
-            const uint32_t bytes = (uint32_t)(2 * A_BYTES + 2 * a.NTL * BK * 2);
+            const uint32_t bytes = (uint32_t)(2 * BM * bk * 2 + 2 * a.NTL * bk * 2);
             for (int tile = blockIdx.x; tile < tiles && !*abort_s; tile += gridDim.x) {
                 const int mt = tile % MT, rest = tile / MT, n0 = (rest % NTT) * a.NTL, b = rest / NTT;
                 const int u0 = mt * BM;
@@ -349,10 +362,10 @@ __global__ void __launch_bounds__(dig::NT, 1)
                                  : "memory");
                     unsigned char* sp = smem + st * STAGE;
                     const int row = u0 + k * a.dil - a.pad;
-                    tma_load_4d(sp, &tmA, c * BK, row, b, 0, full + st);
-                    tma_load_4d(sp + A_BYTES, &tmA, c * BK, row, b, 1, full + st);
-                    tma_load_2d(sp + 2 * A_BYTES, &tmW, c * BK, k * a.Npad + n0, full + st);
-                    tma_load_2d(sp + 2 * A_BYTES + W_BYTES, &tmW, c * BK, (a.taps + k) * a.Npad + n0, full + st);
+                    tma_load_4d(sp, &tmA, c * bk, row, b, 0, full + st);
+                    tma_load_4d(sp + A_BYTES, &tmA, c * bk, row, b, 1, full + st);
+                    tma_load_2d(sp + 2 * A_BYTES, &tmW, c * bk, k * a.Npad + n0, full + st);
+                    tma_load_2d(sp + 2 * A_BYTES + W_BYTES, &tmW, c * bk, (a.taps + k) * a.Npad + n0, full + st);
                 }
             }
             if (*abort_s)  // let the copies in flight land before the CTA can exit
@@ -386,12 +399,22 @@ __global__ void __launch_bounds__(dig::NT, 1)
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                     const uint32_t ah = s_addr(smem + st * STAGE), al = ah + A_BYTES;
                     const uint32_t wh = ah + 2 * A_BYTES, wl = wh + W_BYTES;
+                    if (bk == 64) {
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint32_t off = (uint32_t)(kk * 32);
-                        at_mma(d, sw128_desc(ah + off), sw128_desc(wh + off), idesc, (kt | kk) ? 1u : 0u);
-                        at_mma(d, sw128_desc(ah + off), sw128_desc(wl + off), idesc, 1u);
-                        at_mma(d, sw128_desc(al + off), sw128_desc(wh + off), idesc, 1u);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t off = (uint32_t)(kk * 32);
+                            at_mma(d, sw128_desc(ah + off), sw128_desc(wh + off), idesc, (kt | kk) ? 1u : 0u);
+                            at_mma(d, sw128_desc(ah + off), sw128_desc(wl + off), idesc, 1u);
+                            at_mma(d, sw128_desc(al + off), sw128_desc(wh + off), idesc, 1u);
+                        }
+                    } else {  // 32 channels: two K steps in 64-byte rows
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const uint32_t off = (uint32_t)(kk * 32);
+                            at_mma(d, sw64_desc(ah + off), sw64_desc(wh + off), idesc, (kt | kk) ? 1u : 0u);
+                            at_mma(d, sw64_desc(ah + off), sw64_desc(wl + off), idesc, 1u);
+                            at_mma(d, sw64_desc(al + off), sw64_desc(wh + off), idesc, 1u);
+                        }
                     }
                     at_commit(empty + st);
                 }
@@ -586,12 +609,13 @@ bool tc_prepare(tts_bb_dac* d, DacTcConv& c, const float* w, bool transposed, in
     c.NTL = c.N < dig::MAXN ? c.N : dig::MAXN;
     if (c.NTL % 32 != 0 || c.N % c.NTL != 0 || IC % 8 != 0 || OC % 16 != 0 || OC > dig::MAXOC) return false;
     c.Npad = c.N;
-    const int ICpad = (IC + dig::BK - 1) / dig::BK * dig::BK;
+    c.bk = IC == 32 ? 32 : dig::BK;
+    const int ICpad = (IC + c.bk - 1) / c.bk * c.bk;
     const size_t n = (size_t)2 * c.taps * c.Npad * ICpad;
     if (dalloc_copy(d, &c.wp, nullptr, n) != cudaSuccess) return false;
     k_dac_pack<<<1024, 256, 0, d->st>>>(w, transposed ? 1 : 0, IC, OC, c.taps, c.s, c.Npad, ICpad, c.wp);
     if (cudaGetLastError() != cudaSuccess) return false;
-    return tc_make_map(&c.map, c.wp, 2 * c.taps * c.Npad, ICpad, c.NTL);
+    return tc_make_map_k(&c.map, c.wp, 2 * c.taps * c.Npad, ICpad, c.NTL, c.bk);
 }
 
 // One convolution on the tensor-core path. s_in: its input (after its snake) as [2][B][T_in][IC]
@@ -606,8 +630,8 @@ bool tc_conv(tts_bb_dac* d, const DacTcConv& c, const bf16* s_in, int B, int T_i
         attr = true;
     }
     CUtensorMap ma;
-    if (!tc_make_map_rows(&ma, s_in, c.IC, T_in, B, 2)) return false;
-    DacIgArgs a{c.IC, c.OC, T_in, T_out, B, c.taps, c.dil, c.pad, c.s, c.po, c.s > 1 ? T_in + 1 : T_out,
+    if (!tc_make_map_rows(&ma, s_in, c.IC, T_in, B, 2, c.bk)) return false;
+    DacIgArgs a{c.IC, c.OC, T_in, T_out, B, c.bk, c.taps, c.dil, c.pad, c.s, c.po, c.s > 1 ? T_in + 1 : T_out,
                 c.N, c.NTL, c.Npad, bias, res, y, s_out, alpha_out, alpha_inv, d->err};
     const long tiles = (long)((a.U + dig::BM - 1) / dig::BM) * (c.Npad / c.NTL) * B;
     const int grid = (int)std::min<long>(tiles, d->n_sm);

@@ -1109,18 +1109,33 @@ bool tc_make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows
 
 bool gemm_tc_available() { return encode_fn() != nullptr; }
 
-// 4-D bf16 tensor [parts][B][T][C] (C contiguous), box 64 channels x 128 rows of one (part, item),
-// 128-byte swizzle; rows and channels outside the tensor read as zeros. Not cached.
-bool tc_make_map_rows(CUtensorMap* m, const void* base, int C, int T, int B, int parts) {
+// 4-D bf16 tensor [parts][B][T][C] (C contiguous), box box_c (64 or 32) channels x 128 rows of one
+// (part, item), 128- or 64-byte swizzle (rows of box_c x 2 bytes); rows and channels outside the
+// tensor read as zeros. Not cached.
+bool tc_make_map_rows(CUtensorMap* m, const void* base, int C, int T, int B, int parts, int box_c) {
     auto fn = encode_fn();
-    if (!fn || C % 8 != 0 || C <= 0 || T <= 0 || B <= 0 || parts <= 0) return false;
+    if (!fn || C % 8 != 0 || C <= 0 || T <= 0 || B <= 0 || parts <= 0 || (box_c != 64 && box_c != 32)) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)T, (cuuint64_t)B, (cuuint64_t)parts};
     const cuuint64_t strides[3] = {(cuuint64_t)C * 2, (cuuint64_t)T * C * 2, (cuuint64_t)B * T * C * 2};
-    const cuuint32_t box[4] = {64, 128, 1, 1};
+    const cuuint32_t box[4] = {(cuuint32_t)box_c, 128, 1, 1};
     const cuuint32_t es[4] = {1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_INTERLEAVE_NONE, box_c == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D bf16 tensor [rows][K] (K contiguous), box [box_rows][box_k] with box_k 64 (128-byte swizzle)
+// or 32 (64-byte swizzle). Not cached.
+bool tc_make_map_k(CUtensorMap* m, const void* base, int rows, int K, int box_rows, int box_k) {
+    auto fn = encode_fn();
+    if (!fn || (box_k != 64 && box_k != 32) || K % 8 != 0) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)box_k, (cuuint32_t)box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, box_k == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <bool PRECISE>

@@ -126,8 +126,12 @@ __device__ __forceinline__ float at_ex2(float x) {
 // Host: 2-D bf16 tensor map [rows][K] (K contiguous), box [box_rows][64], 128-byte swizzle,
 // cached by (base, rows, K, box rows). False when the driver entry point is missing.
 bool tc_make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows);
-// Host: 4-D bf16 tensor map [parts][B][T][C] (C contiguous, C a multiple of 8), box 64 channels x
-// 128 rows of one (part, item), 128-byte swizzle; out-of-range rows and channels read as zeros.
-bool tc_make_map_rows(CUtensorMap* m, const void* base, int C, int T, int B, int parts);
+// Host: 4-D bf16 tensor map [parts][B][T][C] (C contiguous, C a multiple of 8), box box_c (64 or 32)
+// channels x 128 rows of one (part, item), 128- or 64-byte swizzle; out-of-range rows and channels
+// read as zeros.
+bool tc_make_map_rows(CUtensorMap* m, const void* base, int C, int T, int B, int parts, int box_c);
+// Host: 2-D bf16 tensor map [rows][K], box [box_rows][box_k], box_k 64 (128-byte swizzle) or 32
+// (64-byte swizzle).
+bool tc_make_map_k(CUtensorMap* m, const void* base, int rows, int K, int box_rows, int box_k);
 
 }  // namespace ttsbb
