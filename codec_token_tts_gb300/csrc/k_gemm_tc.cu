@@ -973,14 +973,14 @@ __global__ void __launch_bounds__(at::NT, 1)
                     const float p1 = at_ex2(fmaf(__uint_as_float(v[ch * 32 + x + 1]), sc, -m_used));
                     __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
                     pk[x >> 1] = *reinterpret_cast<uint32_t*>(&h2);
-                    const float2 pr = __bfloat1622float2(h2);  // the row sum takes the weights P V applies
-                    if constexpr (PRECISE) {
+                    if constexpr (PRECISE) {  // the row sum takes the weights P V applies (hi + lo)
+                        const float2 pr = __bfloat1622float2(h2);
                         __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - pr.x, p1 - pr.y);
                         pl[x >> 1] = *reinterpret_cast<uint32_t*>(&l2);
                         const float2 lr = __bfloat1622float2(l2);
                         l4[(x >> 1) & 3] += (pr.x + lr.x) + (pr.y + lr.y);
                     } else {
-                        l4[(x >> 1) & 3] += pr.x + pr.y;
+                        l4[(x >> 1) & 3] += p0 + p1;
                     }
                 }
 #pragma unroll
