@@ -6,12 +6,12 @@
 // 4-stage shared-memory ring that runs on across tiles; one thread issues
 // tcgen05.mma (M=128, N=256, K=16, bf16 in, fp32 accumulate) into one of two
 // TMEM accumulators (2 x 256 columns) and commits each stage back to the
-// producer through an mbarrier; four epilogue warps drain the other
-// accumulator with tcgen05.ld (each warp owns its 32-lane quarter of TMEM =
-// 32 token rows) while the next tile accumulates, applying the same fused
-// epilogues as the other linear kernels (fp32 store, residual add, SwiGLU
-// over interleaved gate/up columns, logits + argmax, permuted audio-head
-// logits).
+// producer through an mbarrier; eight epilogue warps drain the other
+// accumulator with tcgen05.ld (two per 32-lane quarter of TMEM = 32 token
+// rows, 128 columns each) while the next tile accumulates, applying the same
+// fused epilogues as the other linear kernels (fp32 store, residual add,
+// SwiGLU over interleaved gate/up columns, logits + argmax, permuted
+// audio-head logits).
 //
 // Every mbarrier wait is bounded; on timeout the CTA raises the error word,
 // stops issuing work, waits (bounded) for its copies and MMAs in flight,
@@ -35,7 +35,7 @@ constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr int TMEM_COLS = 2 * BN;  // two accumulators
-constexpr int NT = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-5 epilogue
+constexpr int NT = 320;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-9 epilogue (2 per lane quarter)
 constexpr unsigned long long TIMEOUT_NS = TC_TIMEOUT_NS;
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (7-9 = 1),
 // B bf16 (10-12 = 1), both K-major (15, 16 = 0), N >> 3 at 17-22, M >> 4 at 24-28.
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(tc::NT, 1)
         }
         for (int i = 0; i < 2; ++i) {
             tc_mbar_init(accf + i, 1);
-            tc_mbar_init(acce + i, 4);
+            tc_mbar_init(acce + i, 8);
         }
         tc_mbar_init(fin, 1);
         *abort_s = 0;
@@ -241,8 +241,9 @@ __global__ void __launch_bounds__(tc::NT, 1)
             }
         }
     } else {
-        // ---------------- epilogue: warp w reads TMEM lanes 32 * (w % 4) .. of the tile's accumulator
-        const int q = warp & 3;
+        // ---------------- epilogue: warp w reads TMEM lanes 32 * (w % 4) .. of the tile's accumulator,
+        // columns [128 h, 128 h + 128) with h = (w - 2) / 4
+        const int q = warp & 3, h = (warp - 2) >> 2;
         int it = 0;
         for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++it) {
             const int buf = it & 1;
@@ -255,7 +256,7 @@ __global__ void __launch_bounds__(tc::NT, 1)
             const int m0 = (tile % MT) * BM, n0 = (tile / MT) * BN;
             const int t = m0 + q * 32 + lane;
             unsigned long long best = 0ull;
-            for (int c = 0; c < BN; c += 16) {
+            for (int c = h * (BN / 2); c < (h + 1) * (BN / 2); c += 16) {
                 uint32_t r[16];
                 const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c);
                 asm volatile(
