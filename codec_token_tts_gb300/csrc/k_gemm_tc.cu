@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(tc::NT, 1)
 // adds the S partials in rank order (deterministic) and applies the epilogue,
 // one thread per output feature.
 namespace tcd {
-constexpr int BM = 128, BK = 64, STAGES = 4, NT = 192;
+constexpr int BM = 128, BK = 64, STAGES = 4, NT = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr int MAXTB = 128;                          // padded tokens per launch
 constexpr int A_BYTES = BM * BK * 2;                // 16 KB
 constexpr int STAGE = A_BYTES + 2 * MAXTB * BK * 2; // 48 KB
@@ -335,14 +335,14 @@ struct TcdOut {
 
 // Sum, in rank order, the S partials of tokens [t0, t1) (this CTA's own
 // partial in `red`, the peers' in `recv`) and apply the epilogue. Epilogue
-// warp w takes tokens t0 + w, t0 + w + 4, ...; lane l takes the four features
+// warp w (of 8) takes tokens t0 + w, t0 + w + 8, ...; lane l takes the four features
 // n0 + 4l .. 4l + 3 (vector loads and stores; a gate/up pair stays in one lane).
 template <int MODE>
 __device__ __forceinline__ void tcd_reduce(const TcdOut o, const float* __restrict__ red, const float* __restrict__ recv,
                                            int t0, int t1, uint32_t S, uint32_t r, int n0, int N, int w, int lane) {
     constexpr int BM = tcd::BM;
     const int nt_all = t1 - t0, f = lane * 4, n = n0 + f;
-    for (int t = t0 + w; t < t1; t += 4) {
+    for (int t = t0 + w; t < t1; t += 8) {
         const int tl = t - t0;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int p0 = 0; p0 < (int)S; p0 += 4) {
@@ -521,12 +521,13 @@ __global__ void __launch_bounds__(tcd::NT, 1)
                          : "memory");
         }
     } else {
-        // partial sums: thread = feature q * 32 + lane; column c < TB is token c's high part, TB + c its low part
-        const int q = warp & 3, f = q * 32 + lane;
+        // partial sums: thread = feature q * 32 + lane; column c < TB is token c's high part, TB + c its low
+        // part; the two warps of a lane quarter take alternate 16-column chunks
+        const int q = warp & 3, hf = (warp - 2) >> 2, f = q * 32 + lane;
         const bool ok = tc_wait(accf, 0, abort_s) && !*abort_s;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (ok) {
-            for (int c = 0; c < TB; c += 16) {
+            for (int c = 16 * hf; c < TB; c += 32) {
                 uint32_t hi[16], lo[16];
                 const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c;
                 asm volatile(
