@@ -6,9 +6,9 @@
 // 4-stage shared-memory ring that runs on across tiles; one thread issues
 // tcgen05.mma (M=128, N=256, K=16, bf16 in, fp32 accumulate) into one of two
 // TMEM accumulators (2 x 256 columns) and commits each stage back to the
-// producer through an mbarrier; eight epilogue warps drain the other
-// accumulator with tcgen05.ld (two per 32-lane quarter of TMEM = 32 token
-// rows, 128 columns each) while the next tile accumulates, applying the same
+// producer through an mbarrier; sixteen epilogue warps drain the other
+// accumulator with tcgen05.ld (four per 32-lane quarter of TMEM = 32 token
+// rows, 64 columns each) while the next tile accumulates, applying the same
 // fused epilogues as the other linear kernels (fp32 store, residual add,
 // SwiGLU over interleaved gate/up columns, logits + argmax, permuted
 // audio-head logits).
@@ -35,7 +35,8 @@ constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr int TMEM_COLS = 2 * BN;  // two accumulators
-constexpr int NT = 320;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-9 epilogue (2 per lane quarter)
+constexpr int EPW = 16;  // epilogue warps: EPW / 4 per TMEM lane quarter, BN / (EPW / 4) columns each
+constexpr int NT = 64 + 32 * EPW;  // warp 0 TMA, warp 1 MMA + TMEM owner, then the epilogue warps
 constexpr unsigned long long TIMEOUT_NS = TC_TIMEOUT_NS;
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (7-9 = 1),
 // B bf16 (10-12 = 1), both K-major (15, 16 = 0), N >> 3 at 17-22, M >> 4 at 24-28.
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(tc::NT, 1)
         }
         for (int i = 0; i < 2; ++i) {
             tc_mbar_init(accf + i, 1);
-            tc_mbar_init(acce + i, 8);
+            tc_mbar_init(acce + i, EPW);
         }
         tc_mbar_init(fin, 1);
         *abort_s = 0;
@@ -242,7 +243,8 @@ __global__ void __launch_bounds__(tc::NT, 1)
         }
     } else {
         // ---------------- epilogue: warp w reads TMEM lanes 32 * (w % 4) .. of the tile's accumulator,
-        // columns [128 h, 128 h + 128) with h = (w - 2) / 4
+        // columns [h CW, (h + 1) CW) with h = (w - 2) / 4
+        constexpr int CW = BN / (EPW / 4);
         const int q = warp & 3, h = (warp - 2) >> 2;
         int it = 0;
         for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++it) {
@@ -256,7 +258,7 @@ __global__ void __launch_bounds__(tc::NT, 1)
             const int m0 = (tile % MT) * BM, n0 = (tile / MT) * BN;
             const int t = m0 + q * 32 + lane;
             unsigned long long best = 0ull;
-            for (int c = h * (BN / 2); c < (h + 1) * (BN / 2); c += 16) {
+            for (int c = h * CW; c < (h + 1) * CW; c += 16) {
                 uint32_t r[16];
                 const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c);
                 asm volatile(
@@ -303,7 +305,8 @@ __global__ void __launch_bounds__(tc::NT, 1)
 // adds the S partials in rank order (deterministic) and applies the epilogue,
 // one thread per output feature.
 namespace tcd {
-constexpr int BM = 128, BK = 64, STAGES = 4, NT = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+constexpr int EPW = 16;  // epilogue warps (EPW / 4 per TMEM lane quarter)
+constexpr int BM = 128, BK = 64, STAGES = 4, NT = 64 + 32 * EPW;  // warp 0 TMA, warp 1 MMA, then the epilogue
 constexpr int MAXTB = 128;                          // padded tokens per launch
 constexpr int A_BYTES = BM * BK * 2;                // 16 KB
 constexpr int STAGE = A_BYTES + 2 * MAXTB * BK * 2; // 48 KB
@@ -335,14 +338,14 @@ struct TcdOut {
 
 // Sum, in rank order, the S partials of tokens [t0, t1) (this CTA's own
 // partial in `red`, the peers' in `recv`) and apply the epilogue. Epilogue
-// warp w (of 8) takes tokens t0 + w, t0 + w + 8, ...; lane l takes the four features
+// warp w (of EPW) takes tokens t0 + w, t0 + w + EPW, ...; lane l takes the four features
 // n0 + 4l .. 4l + 3 (vector loads and stores; a gate/up pair stays in one lane).
 template <int MODE>
 __device__ __forceinline__ void tcd_reduce(const TcdOut o, const float* __restrict__ red, const float* __restrict__ recv,
                                            int t0, int t1, uint32_t S, uint32_t r, int n0, int N, int w, int lane) {
     constexpr int BM = tcd::BM;
     const int nt_all = t1 - t0, f = lane * 4, n = n0 + f;
-    for (int t = t0 + w; t < t1; t += 8) {
+    for (int t = t0 + w; t < t1; t += tcd::EPW) {
         const int tl = t - t0;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int p0 = 0; p0 < (int)S; p0 += 4) {
@@ -522,12 +525,12 @@ __global__ void __launch_bounds__(tcd::NT, 1)
         }
     } else {
         // partial sums: thread = feature q * 32 + lane; column c < TB is token c's high part, TB + c its low
-        // part; the two warps of a lane quarter take alternate 16-column chunks
+        // part; the EPW / 4 warps of a lane quarter take 16-column chunks in turn
         const int q = warp & 3, hf = (warp - 2) >> 2, f = q * 32 + lane;
         const bool ok = tc_wait(accf, 0, abort_s) && !*abort_s;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (ok) {
-            for (int c = 16 * hf; c < TB; c += 32) {
+            for (int c = 16 * hf; c < TB; c += 16 * (EPW / 4)) {
                 uint32_t hi[16], lo[16];
                 const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c;
                 asm volatile(
