@@ -816,13 +816,14 @@ def roofline_from_profile(rep, traffic=None):
             "launches": top["launches"]}
 
 
-# DRAM bytes (read + write) per launch of a kernel, from the ncu capture summarised under
-# profiles/ (decode_ll_talker_b1.md). Valid only while the kernel's sources are the ones that
-# were captured: the sha256 of the listed files must match, else the bench reports null.
+# DRAM bytes (read + write) per launch of a kernel, from an ncu capture of this bench's own
+# command (dram__bytes_read.sum + dram__bytes_write.sum of a launch after the warm-up steps).
+# Valid only while the kernel's sources are the ones that were captured: the sha256 of the listed
+# files must match, else the bench reports null.
 MEASURED_TRAFFIC = {
     "decode_step_persistent": {"files": ("k_decode_ll.cu", "mega.cuh", "common.cuh"),
-                               "sha256": "c384dd941621c16fb9578b2dd317c6acf0d49326afd6db4d315d068dcbb99fee",
-                               "bytes_per_launch": 918.552576e6},
+                               "sha256": "f673dc802c8b63796966d6b15ff0faee0015cb2a57a6a1f7a50adc4c16464cac",
+                               "bytes_per_launch": 926.365184e6},
 }
 
 
