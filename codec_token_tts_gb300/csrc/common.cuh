@@ -70,7 +70,35 @@ enum EpiMode : int {
     EPI_ADD_F32 = 2,     // out_f32[t*ldo + n] += acc (residual)
     EPI_SWIGLU = 3,      // rows interleaved gate/up: out_bf16[t*ldo + n/2] = silu(g)*u
     EPI_LOGITS = 4,      // out_f32 (optional) + packed argmax per row (optional)
-    EPI_LOGITS_PERM = 5  // OmniVoice audio heads: out[((b*G + k)*R + s)*V + v]
+    EPI_LOGITS_PERM = 5, // OmniVoice audio heads: out[((b*G + k)*R + s)*V + v]
+    EPI_QKROPE = 6       // the QKV product: q/k RMSNorm + RoPE, q out, k and v appended (decode GEMM only)
+};
+
+// Paged KV cache of one layer. Block of (seq, j): page_table[seq_slot[seq]*mbps + j] or, when
+// page_table is null, seq*mbps + j.
+struct KVView {
+    bf16* pool;            // layer base: [blocks][2][8][64][128]
+    const int32_t* page_table;
+    const int32_t* seq_slot;
+    int mbps;              // blocks per slot row of the page table
+};
+
+// EPI_QKROPE arguments: token t belongs to sequence t / tok_per_seq at position seq_start[seq] +
+// t % tok_per_seq, valid when t % tok_per_seq < seq_len[seq]; q -> q (bf16) or qf (fp32, when
+// non-null) [T][16][128], k and v -> the paged cache kv.
+struct EpiQk {
+    const bf16* qn;
+    const bf16* kn;
+    const float* cos_t;
+    const float* sin_t;
+    float eps;
+    bf16* q;
+    float* qf;
+    KVView kv;
+    const int32_t* seq_start;
+    const int32_t* seq_len;
+    int tok_per_seq;
+    int* err;
 };
 
 struct Epi {
@@ -82,6 +110,7 @@ struct Epi {
     int perm_vocab;            // V
     int perm_groups;           // G
     void* out_lo;              // EPI_SWIGLU: optional bf16 low part (value - bf16(value))
+    EpiQk qk;                  // EPI_QKROPE
 };
 
 // ---------------------------------------------------------------- programmatic dependent launch
@@ -165,14 +194,7 @@ int launch_attn_bidir_tc(const bf16* q, const bf16* pool, size_t pool_blocks, in
 
 // Per-token q/k RMSNorm + RoPE; q -> qout [T][16][128] bf16; k, v -> paged pool.
 // Token t belongs to sequence t / tok_per_seq at position seq_start[seq] + t % tok_per_seq,
-// valid when t % tok_per_seq < seq_len[seq]. Block of (seq, j): page_table[seq_slot[seq]*mbps + j]
-// or, when page_table is null, seq*mbps + j.
-struct KVView {
-    bf16* pool;            // layer base: [blocks][2][8][64][128]
-    const int32_t* page_table;
-    const int32_t* seq_slot;
-    int mbps;              // blocks per slot row of the page table
-};
+// valid when t % tok_per_seq < seq_len[seq].
 // qout_f (optional): the queries as fp32 [T][16][128] instead of bf16 in qout.
 int launch_qk_norm_rope_append(const float* qkv, const bf16* qn, const bf16* kn, const float* cos_t,
                                 const float* sin_t, float eps, bf16* qout, KVView kv, const int32_t* seq_start,

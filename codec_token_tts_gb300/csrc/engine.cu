@@ -220,6 +220,7 @@ struct tts_bb {
     bf16* mg_pool = nullptr;
     bool attn_bidir_tc = false;
     bool attn_causal_tc = false;        // causal prefill of 64 or more positions per sequence on tcgen05
+    bool fuse_qk = false;               // q/k norm + RoPE + KV append in the decode GEMM's QKV epilogue
     int32_t* hx_ids = nullptr;  // tts_bb_decode_step_host: device copies of the caller's host ids and argmax
     int32_t* hx_am = nullptr;
     float* hx_logits = nullptr;
@@ -489,12 +490,25 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         const double norm_bytes = T * (4.0 + 2.0) * HID + 2.0 * HID;
         { Launch L(h, K_RMSNORM, norm_bytes); L += launch_rmsnorm(h->h, w.in_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st, ylo); }
         Epi e{};
-        e.mode = EPI_STORE_F32; e.out = h->qkv; e.ldo = QKV;
-        { Launch L(h, gk, gemm_bytes(T, QKV, HID, 4), 2.0 * T * QKV * HID); L += launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st, ylo, h->err, skp); }
-        { Launch L(h, K_QKROPE, T * (4.0 * QKV + 2.0 * QKV));
-          L += launch_qk_norm_rope_append(h->qkv, w.qn, w.kn, h->cos_t, h->sin_t, c.rms_eps, h->q, kv,
-                                          h->seq_start, h->seq_len, tok_per_seq, T, h->err, h->st,
-                                          mode == 0 || causal_tc ? h->qf : nullptr); }
+        float* qf_out = mode == 0 || causal_tc ? h->qf : nullptr;
+        int fused = 0;
+        if (gk == K_GEMM_TCD && h->fuse_qk) {
+            // the split-K decode GEMM applies q/k norm + RoPE and appends k, v in its epilogue
+            e.mode = EPI_QKROPE;
+            e.qk = EpiQk{w.qn, w.kn, h->cos_t, h->sin_t, c.rms_eps, h->q, qf_out, kv, h->seq_start, h->seq_len,
+                         tok_per_seq, h->err};
+            Launch L(h, gk, gemm_bytes(T, QKV, HID, 2), 2.0 * T * QKV * HID);
+            fused = launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st, ylo, h->err, skp);
+            L += fused;
+            e = Epi{};
+        }
+        if (!fused) {
+            e.mode = EPI_STORE_F32; e.out = h->qkv; e.ldo = QKV;
+            { Launch L(h, gk, gemm_bytes(T, QKV, HID, 4), 2.0 * T * QKV * HID); L += launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st, ylo, h->err, skp); }
+            { Launch L(h, K_QKROPE, T * (4.0 * QKV + 2.0 * QKV));
+              L += launch_qk_norm_rope_append(h->qkv, w.qn, w.kn, h->cos_t, h->sin_t, c.rms_eps, h->q, kv,
+                                              h->seq_start, h->seq_len, tok_per_seq, T, h->err, h->st, qf_out); }
+        }
         if (bidir_tc) {
             Launch L(h, K_ATTN_BIDIR_TC, 0, attn_flops);
             L += launch_attn_bidir_tc(h->q, kv.pool, h->mg_pool_blocks, kv.mbps, h->key_len, B, tok_per_seq, h->ao, h->err, h->st);
@@ -894,6 +908,8 @@ static tts_bb_status create_impl(const tts_bb_config* cfg, const tts_bb_weights*
         h->attn_bidir_tc = gemm_tc_available() && !(av && std::strcmp(av, "mma") == 0);
         const char* pv = std::getenv("TTS_BB_PREFILL_ATTN");  // "mma": the mma.sync flash kernel for the causal prefill
         h->attn_causal_tc = gemm_tc_available() && !(pv && std::strcmp(pv, "mma") == 0);
+        const char* fq = std::getenv("TTS_BB_QKV_EPILOGUE");  // "separate": the q/k norm + RoPE + append kernel
+        h->fuse_qk = gemm_tc_available() && !(fq && std::strcmp(fq, "separate") == 0);
     }
     if (c.max_slots > 0) {  // graph-replayed decode steps: step block, staging ring, fixed input / output buffers
         const char* gv = std::getenv("TTS_BB_GRAPHS");

@@ -404,6 +404,94 @@ __device__ __forceinline__ void tcd_reduce(const TcdOut o, const float* __restri
     }
 }
 
+// EPI_QKROPE on the decode GEMM: this CTA's 128 features are one head (n0 / 128: q 0..15, k 16..23,
+// v 24..31). Per token (warp w takes tokens t0 + w, t0 + w + EPW, ..., lane l features 4l .. 4l + 3)
+// the rank-order sum of the partials, then the same arithmetic as the separate q/k norm + RoPE +
+// append kernel: the head's RMSNorm (warp sum of squares) and gain, the rotation of dims (i, i + 64)
+// by pos * theta^(-2i/128) with the partner dims in lane l ^ 16 (omnivoice-cpp, Qwen3 specifics:
+// per-head RMSNorm before RoPE; Qwen3-TTS ncnn port: 1-D half-rotate RoPE); q to q / qf, k and v
+// appended to the paged cache. tb0: the block's first token in the launch.
+__device__ __forceinline__ void tcd_qkrope(const EpiQk& k, const float* __restrict__ red,
+                                           const float* __restrict__ recv, int t0, int t1, uint32_t S, uint32_t r,
+                                           int n0, int w, int lane, int tb0) {
+    constexpr int BM = tcd::BM;
+    const int nt_all = t1 - t0, f = lane * 4, u = n0 / HD;
+    for (int t = t0 + w; t < t1; t += tcd::EPW) {
+        const int tl = t - t0;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int p0 = 0; p0 < (int)S; p0 += 4) {
+            float4 xs[4];
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                const int p = min(p0 + pp, (int)S - 1);
+                const float* src = p == (int)r ? red + (size_t)t * BM + f : recv + ((size_t)p * nt_all + tl) * BM + f;
+                xs[pp] = *reinterpret_cast<const float4*>(src);
+            }
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp)
+                if (p0 + pp < (int)S) { x.x += xs[pp].x; x.y += xs[pp].y; x.z += xs[pp].z; x.w += xs[pp].w; }
+        }
+        const int tg = tb0 + t, seq = tg / k.tok_per_seq, s = tg - seq * k.tok_per_seq;
+        const bool valid = s < k.seq_len[seq];
+        const int pos = k.seq_start[seq] + s;
+        bf16* kdst = nullptr;
+        if (valid && u >= NQ) {
+            const int j = pos / KVB;
+            const int phys = k.kv.page_table ? k.kv.page_table[(size_t)k.kv.seq_slot[seq] * k.kv.mbps + j]
+                                             : seq * k.kv.mbps + j;
+            if (phys < 0) {
+                if (lane == 0) set_err(k.err, ERR_KV_RANGE);
+            } else {
+                kdst = k.kv.pool + (size_t)phys * 2 * NKV * KVB * HD + (size_t)(pos % KVB) * HD;
+            }
+        }
+        if (u >= NQ + NKV) {  // v head: copied into the cache
+            if (kdst) {
+                __nv_bfloat162 a2 = __floats2bfloat162_rn(x.x, x.y), b2 = __floats2bfloat162_rn(x.z, x.w);
+                uint2 o;
+                o.x = *reinterpret_cast<uint32_t*>(&a2);
+                o.y = *reinterpret_cast<uint32_t*>(&b2);
+                *reinterpret_cast<uint2*>(kdst + (size_t)NKV * KVB * HD + (size_t)(u - NQ - NKV) * KVB * HD + f) = o;
+            }
+            continue;
+        }
+        const bool isq = u < NQ;
+        const int hh = isq ? u : u - NQ;
+        if (!isq && !kdst) continue;
+        const float ss = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w);
+        const float rn = rsqrtf(ss * (1.f / HD) + k.eps);
+        const bf16* gm = isq ? k.qn : k.kn;
+        float v[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = v[e] * rn * bf2f(gm[lane * 4 + e]);
+        float pv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pv[e] = __shfl_xor_sync(0xffffffffu, v[e], 16);
+        const int i0 = (lane & 15) * 4;
+        const float* ct = k.cos_t + (size_t)pos * (HD / 2) + i0;
+        const float* st = k.sin_t + (size_t)pos * (HD / 2) + i0;
+        float o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float c = valid ? ct[e] : 1.f, sn = valid ? st[e] : 0.f;
+            o[e] = (lane < 16) ? (v[e] * c - pv[e] * sn) : (v[e] * c + pv[e] * sn);
+        }
+        __nv_bfloat162 a2 = __floats2bfloat162_rn(o[0], o[1]), b2 = __floats2bfloat162_rn(o[2], o[3]);
+        uint2 wv;
+        wv.x = *reinterpret_cast<uint32_t*>(&a2);
+        wv.y = *reinterpret_cast<uint32_t*>(&b2);
+        if (isq && k.qf) {
+            const float4 f4 = valid ? make_float4(o[0], o[1], o[2], o[3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(k.qf + (size_t)tg * NQ * HD + hh * HD + f) = f4;
+        } else if (isq) {
+            if (!valid) wv = make_uint2(0u, 0u);
+            *reinterpret_cast<uint2*>(k.q + (size_t)tg * NQ * HD + hh * HD + f) = wv;
+        } else {
+            *reinterpret_cast<uint2*>(kdst + (size_t)hh * KVB * HD + f) = wv;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(tcd::NT, 1)
     k_gemm_tcd(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmXh,
                const __grid_constant__ CUtensorMap tmXl, int T, int TB, int tb_base, int N, int K,
@@ -590,6 +678,7 @@ __global__ void __launch_bounds__(tcd::NT, 1)
         o.ldo = e.ldo;
         const int w = warp - 2;
         switch (e.mode) {
+            case EPI_QKROPE: tcd_qkrope(e.qk, red, recv, t0, t1, S, r, n0, w, lane, tb0); break;
             case EPI_STORE_F32: tcd_reduce<EPI_STORE_F32>(o, red, recv, t0, t1, S, r, n0, N, w, lane); break;
             case EPI_ADD_F32: tcd_reduce<EPI_ADD_F32>(o, red, recv, t0, t1, S, r, n0, N, w, lane); break;
             case EPI_SWIGLU: tcd_reduce<EPI_SWIGLU>(o, red, recv, t0, t1, S, r, n0, N, w, lane); break;
@@ -1185,7 +1274,10 @@ int launch_attn_causal_tc(const bf16* q, const float* qf, KVView kv, size_t pool
 int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N, int K, const Epi& e, int* err,
                     cudaStream_t st) {
     if (T <= 0 || T > 2 * tcd::MAXTB || N <= 0 || K % tcd::BK != 0 || !X_lo) return 0;
-    if (e.mode != EPI_STORE_F32 && e.mode != EPI_ADD_F32 && e.mode != EPI_SWIGLU && e.mode != EPI_LOGITS) return 0;
+    if (e.mode != EPI_STORE_F32 && e.mode != EPI_ADD_F32 && e.mode != EPI_SWIGLU && e.mode != EPI_LOGITS &&
+        e.mode != EPI_QKROPE)
+        return 0;
+    if (e.mode == EPI_QKROPE && N != QKV) return 0;
     const int blocks = (T + tcd::MAXTB - 1) / tcd::MAXTB;  // token blocks of up to 128
     const int TB = blocks > 1 ? tcd::MAXTB : (T + 15) / 16 * 16;
     CUtensorMap mw, mh, ml;
