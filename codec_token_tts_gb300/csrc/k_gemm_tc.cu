@@ -33,9 +33,12 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
-constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 constexpr int EPW = 16;  // epilogue warps: EPW / 4 per TMEM lane quarter, BN / (EPW / 4) columns each
+constexpr int OST = 32 * 16 * 4;                       // per epilogue warp: [32 rows][16 fp32] store staging
+constexpr int OST_OFF = STAGES * STAGE_BYTES;          // staging buffers, then the barriers
+constexpr int BAR_OFF = OST_OFF + EPW * OST;
+constexpr int SMEM = BAR_OFF + 256 + 1024;             // + alignment of the dynamic base
+constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 constexpr int NT = 64 + 32 * EPW;  // warp 0 TMA, warp 1 MMA + TMEM owner, then the epilogue warps
 constexpr unsigned long long TIMEOUT_NS = TC_TIMEOUT_NS;
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (7-9 = 1),
@@ -43,6 +46,7 @@ constexpr unsigned long long TIMEOUT_NS = TC_TIMEOUT_NS;
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                            ((uint32_t)(BM >> 4) << 24);
 }  // namespace tc
+static_assert(tc::SMEM <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ float silu_tc(float x) { return x / (1.f + __expf(-x)); }
 
@@ -121,18 +125,50 @@ __device__ __forceinline__ void tc_epilogue16(const Epi& e, int t, int n0, int N
     }
 }
 
+// 16 consecutive fp32 accumulator columns of this thread's TMEM lane (warp-collective)
+__device__ __forceinline__ void tc_ld16(uint32_t ta, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(ta));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// Bulk tensor store / reduce-add of a shared-memory box (async proxy), and their group waits.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, const void* src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x), "r"(y),
+                 "r"(s_addr(src))
+                 : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, int x, int y, const void* src) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
+                 "r"(x), "r"(y), "r"(s_addr(src))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // With split = 1 the activations come as bf16 high + low parts (tmA, tmAl): the k-loop runs over
 // K twice, Y = X_hi W^T + X_lo W^T, the second pass reading the same weight tiles (from L2).
+// EPI_STORE_F32 / EPI_ADD_F32 leave through tmO (the fp32 output [T][ldo], boxes of 32 rows x 16
+// columns, 64-byte swizzle): each epilogue warp stages its 32 rows x 16 columns in shared memory and
+// one lane issues a bulk tensor store (or reduce-add, for the residual), so the stores are full
+// coalesced boxes instead of one 16-byte piece per row per instruction.
 __global__ void __launch_bounds__(tc::NT, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAl,
-              const __grid_constant__ CUtensorMap tmB, int split, int T, int N, int K, const __grid_constant__ Epi e,
-              int* err) {
+              const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmO, int split, int T,
+              int N, int K, const __grid_constant__ Epi e, int* err) {
     using namespace tc;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     unsigned char* sA = smem;
     unsigned char* sB = smem + STAGES * A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
     uint64_t* empty = full + STAGES;
     uint64_t* accf = empty + STAGES;  // [2] accumulator ready (MMA -> epilogue)
     uint64_t* acce = accf + 2;        // [2] accumulator drained (epilogue -> MMA), 4 warp arrivals
@@ -246,6 +282,8 @@ __global__ void __launch_bounds__(tc::NT, 1)
         // columns [h CW, (h + 1) CW) with h = (w - 2) / 4
         constexpr int CW = BN / (EPW / 4);
         const int q = warp & 3, h = (warp - 2) >> 2;
+        const bool tma_out = e.mode == EPI_STORE_F32 || e.mode == EPI_ADD_F32;
+        unsigned char* ost = smem + OST_OFF + (warp - 2) * OST;
         int it = 0;
         for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++it) {
             const int buf = it & 1;
@@ -258,7 +296,28 @@ __global__ void __launch_bounds__(tc::NT, 1)
             const int m0 = (tile % MT) * BM, n0 = (tile / MT) * BN;
             const int t = m0 + q * 32 + lane;
             unsigned long long best = 0ull;
-            for (int c = h * CW; c < (h + 1) * CW; c += 16) {
+            if (tma_out) {  // fp32 store / residual add through the staged boxes
+                for (int c = h * CW; c < (h + 1) * CW; c += 16) {
+                    float v[16];
+                    tc_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c), v);
+                    if (lane == 0) bulk_wait_read0();  // the previous box has been read out of the staging buffer
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)  // 16-byte piece k of row `lane`, 64-byte swizzle
+                        *reinterpret_cast<float4*>(ost + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+                            make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0 && n0 + c < N && m0 + q * 32 < T) {
+                        if (e.mode == EPI_ADD_F32)
+                            tma_reduce_add_2d(&tmO, n0 + c, m0 + q * 32, ost);
+                        else
+                            tma_store_2d(&tmO, n0 + c, m0 + q * 32, ost);
+                        bulk_commit();
+                    }
+                }
+            }
+            for (int c = h * CW; c < (h + 1) * CW && !tma_out; c += 16) {
                 uint32_t r[16];
                 const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c);
                 asm volatile(
@@ -281,6 +340,7 @@ __global__ void __launch_bounds__(tc::NT, 1)
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(s_addr(acce + buf)) : "memory");
         }
+        if (tma_out && lane == 0) bulk_wait0();  // every bulk store of this warp has completed
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -1203,6 +1263,46 @@ bool tc_make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows
 
 bool gemm_tc_available() { return encode_fn() != nullptr; }
 
+// fp32 output [rows][ld] (first `cols` columns), box 16 columns x 32 rows, 64-byte swizzle: the
+// dense GEMM's bulk-store epilogue. Cached by (base, rows, cols, ld) like the operand maps.
+static bool make_out_map(CUtensorMap* m, const void* base, int rows, int cols, int ld) {
+    struct Key {
+        const void* base;
+        int rows, cols, ld;
+        bool operator==(const Key& o) const { return base == o.base && rows == o.rows && cols == o.cols && ld == o.ld; }
+    };
+    struct KeyHash {
+        size_t operator()(const Key& k) const {
+            return std::hash<const void*>()(k.base) ^ ((size_t)k.rows * 0x9E3779B97F4A7C15ull + (size_t)k.cols * 131 + (size_t)k.ld);
+        }
+    };
+    static std::mutex mu;
+    static std::unordered_map<Key, CUtensorMap, KeyHash> cache;
+    const Key key{base, rows, cols, ld};
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            *m = it->second;
+            return true;
+        }
+    }
+    auto fn = encode_fn();
+    if (!fn || ld % 4 != 0 || cols > ld) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
+    const cuuint32_t box[2] = {16, 32};
+    const cuuint32_t es[2] = {1, 1};
+    if (fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::lock_guard<std::mutex> g(mu);
+    if (cache.size() > 4096) cache.clear();
+    cache.emplace(key, *m);
+    return true;
+}
+
 // 4-D bf16 tensor [parts][B][T][C] (C contiguous), box box_c (64 or 32) channels x 128 rows of one
 // (part, item), 128- or 64-byte swizzle (rows of box_c x 2 bytes); rows and channels outside the
 // tensor read as zeros. Not cached.
@@ -1355,10 +1455,15 @@ int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N
 int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, int* err, cudaStream_t st,
                    const bf16* X_lo) {
     if (T <= 0 || N <= 0 || K % tc::BK != 0) return 0;
-    CUtensorMap ma, mal, mb;
+    CUtensorMap ma, mal, mb, mo;
     if (!tc_make_map(&ma, X, T, K, tc::BM) || !tc_make_map(&mb, W, N, K, tc::BN)) return 0;
     if (X_lo && !tc_make_map(&mal, X_lo, T, K, tc::BM)) return 0;
     if (!X_lo) mal = ma;
+    if (e.mode == EPI_STORE_F32 || e.mode == EPI_ADD_F32) {
+        if (!make_out_map(&mo, e.out, T, N, e.ldo)) return 0;
+    } else {
+        mo = ma;  // unused
+    }
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM);
@@ -1371,7 +1476,7 @@ int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi&
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     }
     const int tiles = ((N + tc::BN - 1) / tc::BN) * ((T + tc::BM - 1) / tc::BM);
-    launch_pdl(k_gemm_tc, std::min(tiles, sms), tc::NT, tc::SMEM, st, ma, mal, mb, X_lo ? 1 : 0, T, N, K, e, err);
+    launch_pdl(k_gemm_tc, std::min(tiles, sms), tc::NT, tc::SMEM, st, ma, mal, mb, mo, X_lo ? 1 : 0, T, N, K, e, err);
     return 1;
 }
 
