@@ -158,11 +158,14 @@ __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_
 // EPI_STORE_F32 / EPI_ADD_F32 leave through tmO (the fp32 output [T][ldo], boxes of 32 rows x 16
 // columns, 64-byte swizzle): each epilogue warp stages its 32 rows x 16 columns in shared memory and
 // one lane issues a bulk tensor store (or reduce-add, for the residual), so the stores are full
-// coalesced boxes instead of one 16-byte piece per row per instruction.
+// coalesced boxes instead of one 16-byte piece per row per instruction. EPI_SWIGLU does the same
+// with its 32 rows x 32 bf16 outputs (64 columns of gate/up pairs) through tmO, and the low parts
+// through tmOl when the output has them.
 __global__ void __launch_bounds__(tc::NT, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAl,
-              const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmO, int split, int T,
-              int N, int K, const __grid_constant__ Epi e, int* err) {
+              const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmO,
+              const __grid_constant__ CUtensorMap tmOl, int split, int T, int N, int K, const __grid_constant__ Epi e,
+              int* err) {
     using namespace tc;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -283,6 +286,7 @@ __global__ void __launch_bounds__(tc::NT, 1)
         constexpr int CW = BN / (EPW / 4);
         const int q = warp & 3, h = (warp - 2) >> 2;
         const bool tma_out = e.mode == EPI_STORE_F32 || e.mode == EPI_ADD_F32;
+        const bool tma_swiglu = e.mode == EPI_SWIGLU;
         unsigned char* ost = smem + OST_OFF + (warp - 2) * OST;
         int it = 0;
         for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++it) {
@@ -317,7 +321,51 @@ __global__ void __launch_bounds__(tc::NT, 1)
                     }
                 }
             }
-            for (int c = h * CW; c < (h + 1) * CW && !tma_out; c += 16) {
+            if (tma_swiglu) {  // 64 gate/up columns -> 32 bf16 outputs per row, staged as one 64-byte row
+                uint32_t lo_pk[4][4];
+                if (lane == 0) bulk_wait_read0();
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < CW / 16; ++k) {
+                    float v[16];
+                    tc_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * CW + 16 * k), v);
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const float m0v = silu_tc(v[4 * jj]) * v[4 * jj + 1];
+                        const float m1v = silu_tc(v[4 * jj + 2]) * v[4 * jj + 3];
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(m0v, m1v);
+                        pk[jj] = *reinterpret_cast<uint32_t*>(&h2);
+                        __nv_bfloat162 l2 = __halves2bfloat162(f2bf_lo(m0v), f2bf_lo(m1v));
+                        lo_pk[k][jj] = *reinterpret_cast<uint32_t*>(&l2);
+                    }
+                    *reinterpret_cast<uint4*>(ost + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                const int xo = (n0 + h * CW) / 2, yo = m0 + q * 32;
+                const bool in = n0 + h * CW < N && yo < T;
+                if (lane == 0 && in) {
+                    tma_store_2d(&tmO, xo, yo, ost);
+                    bulk_commit();
+                }
+                if (e.out_lo) {
+                    if (lane == 0) bulk_wait_read0();
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < CW / 16; ++k)
+                        *reinterpret_cast<uint4*>(ost + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+                            make_uint4(lo_pk[k][0], lo_pk[k][1], lo_pk[k][2], lo_pk[k][3]);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0 && in) {
+                        tma_store_2d(&tmOl, xo, yo, ost);
+                        bulk_commit();
+                    }
+                }
+            }
+            for (int c = h * CW; c < (h + 1) * CW && !tma_out && !tma_swiglu; c += 16) {
                 uint32_t r[16];
                 const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c);
                 asm volatile(
@@ -340,7 +388,7 @@ __global__ void __launch_bounds__(tc::NT, 1)
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(s_addr(acce + buf)) : "memory");
         }
-        if (tma_out && lane == 0) bulk_wait0();  // every bulk store of this warp has completed
+        if ((tma_out || tma_swiglu) && lane == 0) bulk_wait0();  // every bulk store of this warp has completed
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -1263,13 +1311,15 @@ bool tc_make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows
 
 bool gemm_tc_available() { return encode_fn() != nullptr; }
 
-// fp32 output [rows][ld] (first `cols` columns), box 16 columns x 32 rows, 64-byte swizzle: the
-// dense GEMM's bulk-store epilogue. Cached by (base, rows, cols, ld) like the operand maps.
-static bool make_out_map(CUtensorMap* m, const void* base, int rows, int cols, int ld) {
+// fp32 (or bf16) output [rows][ld] (first `cols` columns), box of 64-byte rows (16 fp32 / 32 bf16) x
+// 32 rows, 64-byte swizzle: the dense GEMM's bulk-store epilogue. Cached like the operand maps.
+static bool make_out_map(CUtensorMap* m, const void* base, int rows, int cols, int ld, bool bf16_out = false) {
     struct Key {
         const void* base;
-        int rows, cols, ld;
-        bool operator==(const Key& o) const { return base == o.base && rows == o.rows && cols == o.cols && ld == o.ld; }
+        int rows, cols, ld, bf;
+        bool operator==(const Key& o) const {
+            return base == o.base && rows == o.rows && cols == o.cols && ld == o.ld && bf == o.bf;
+        }
     };
     struct KeyHash {
         size_t operator()(const Key& k) const {
@@ -1278,7 +1328,7 @@ static bool make_out_map(CUtensorMap* m, const void* base, int rows, int cols, i
     };
     static std::mutex mu;
     static std::unordered_map<Key, CUtensorMap, KeyHash> cache;
-    const Key key{base, rows, cols, ld};
+    const Key key{base, rows, cols, ld, bf16_out ? 1 : 0};
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
@@ -1288,12 +1338,14 @@ static bool make_out_map(CUtensorMap* m, const void* base, int rows, int cols, i
         }
     }
     auto fn = encode_fn();
-    if (!fn || ld % 4 != 0 || cols > ld) return false;
+    const int esz = bf16_out ? 2 : 4;
+    if (!fn || (ld * esz) % 16 != 0 || cols > ld || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
-    const cuuint32_t box[2] = {16, 32};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * esz};
+    const cuuint32_t box[2] = {(cuuint32_t)(64 / esz), 32};  // 64-byte rows of the box
     const cuuint32_t es[2] = {1, 1};
-    if (fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+    if (fn(m, bf16_out ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base),
+           dims, strides, box, es,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
@@ -1455,14 +1507,16 @@ int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N
 int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, int* err, cudaStream_t st,
                    const bf16* X_lo) {
     if (T <= 0 || N <= 0 || K % tc::BK != 0) return 0;
-    CUtensorMap ma, mal, mb, mo;
+    CUtensorMap ma, mal, mb, mo, mol;
     if (!tc_make_map(&ma, X, T, K, tc::BM) || !tc_make_map(&mb, W, N, K, tc::BN)) return 0;
     if (X_lo && !tc_make_map(&mal, X_lo, T, K, tc::BM)) return 0;
     if (!X_lo) mal = ma;
+    mo = mol = ma;  // unused unless set below
     if (e.mode == EPI_STORE_F32 || e.mode == EPI_ADD_F32) {
         if (!make_out_map(&mo, e.out, T, N, e.ldo)) return 0;
-    } else {
-        mo = ma;  // unused
+    } else if (e.mode == EPI_SWIGLU) {
+        if (N % 2 != 0 || !make_out_map(&mo, e.out, T, N / 2, e.ldo, true)) return 0;
+        if (e.out_lo && !make_out_map(&mol, e.out_lo, T, N / 2, e.ldo, true)) return 0;
     }
     static bool attr = false;
     if (!attr) {
@@ -1476,7 +1530,8 @@ int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi&
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     }
     const int tiles = ((N + tc::BN - 1) / tc::BN) * ((T + tc::BM - 1) / tc::BM);
-    launch_pdl(k_gemm_tc, std::min(tiles, sms), tc::NT, tc::SMEM, st, ma, mal, mb, mo, X_lo ? 1 : 0, T, N, K, e, err);
+    launch_pdl(k_gemm_tc, std::min(tiles, sms), tc::NT, tc::SMEM, st, ma, mal, mb, mo, mol, X_lo ? 1 : 0, T, N, K, e,
+               err);
     return 1;
 }
 
