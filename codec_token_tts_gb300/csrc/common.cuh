@@ -111,6 +111,17 @@ struct Epi {
     int perm_groups;           // G
     void* out_lo;              // EPI_SWIGLU: optional bf16 low part (value - bf16(value))
     EpiQk qk;                  // EPI_QKROPE
+    // RMSNorm folded into the decode GEMM (split-K kernel only). Producer (EPI_ADD_F32): besides h,
+    // write the next norm's input h * gamma as bf16 high + low parts (nrm_y, nrm_ylo, [T][1024]) and
+    // this 128-feature tile's sum of squares of h per token (nrm_ss[tile][T]). Consumer: scale each
+    // token row of the product by rsqrt(sum over the 8 tiles of nrm_scale_ss[tile][T] / 1024 + eps).
+    const bf16* nrm_gamma;
+    bf16* nrm_y;
+    bf16* nrm_ylo;
+    float* nrm_ss;
+    const float* nrm_scale_ss;
+    float nrm_eps;
+    int nrm_T;
 };
 
 // ---------------------------------------------------------------- programmatic dependent launch

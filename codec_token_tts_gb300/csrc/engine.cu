@@ -210,6 +210,8 @@ struct tts_bb {
     float* qkv = nullptr;
     bf16* q = nullptr;
     float* qf = nullptr;                // decode: fp32 queries for the decode attention
+    float* nss = nullptr;               // decode: per-tile sums of squares of the folded RMSNorms [8][T]
+    bool launch_missing = false;        // a fused GEMM epilogue had no kernel to run on
     bf16* ao = nullptr;
     bf16* m = nullptr;
     bf16 *y_lo = nullptr, *ao_lo = nullptr, *m_lo = nullptr;  // low bf16 parts (decode)
@@ -221,6 +223,7 @@ struct tts_bb {
     bool attn_bidir_tc = false;
     bool attn_causal_tc = false;        // causal prefill of 64 or more positions per sequence on tcgen05
     bool fuse_qk = false;               // q/k norm + RoPE + KV append in the decode GEMM's QKV epilogue
+    bool fold_norm = false;             // decode batches: the RMSNorms folded into the decode GEMMs' epilogues
     int32_t* hx_ids = nullptr;  // tts_bb_decode_step_host: device copies of the caller's host ids and argmax
     int32_t* hx_am = nullptr;
     float* hx_logits = nullptr;
@@ -377,6 +380,10 @@ tts_bb_status read_err(tts_bb* h) {
 tts_bb_status finish(tts_bb* h) {
     tts_bb_status s = check_launch(h, "kernel launch");
     if (s != TTS_BB_OK) return s;
+    if (h->launch_missing) {
+        h->launch_missing = false;
+        return fail(h, TTS_BB_E_CUDA, "a fused decode-GEMM epilogue could not be launched");
+    }
     if (h->cfg.sync_errors) return read_err(h);
     return TTS_BB_OK;
 }
@@ -431,7 +438,7 @@ tts_bb_status ensure_scratch(tts_bb* h, int T) {
     if (T <= h->T_cap) return TTS_BB_OK;
     if (h->h) {
         cudaStreamSynchronize(h->st);
-        void* olds[] = {h->h, h->y, h->qkv, h->q, h->qf, h->ao, h->m, h->y_lo, h->ao_lo, h->m_lo};
+        void* olds[] = {h->h, h->y, h->qkv, h->q, h->qf, h->ao, h->m, h->y_lo, h->ao_lo, h->m_lo, h->nss};
         for (void* p : olds) {
             cudaFree(p);
             h->allocs.erase(std::remove(h->allocs.begin(), h->allocs.end(), p), h->allocs.end());
@@ -447,7 +454,8 @@ tts_bb_status ensure_scratch(tts_bb* h, int T) {
         (e = dalloc(h, &h->m, (size_t)T * h->cfg.ffn)) != cudaSuccess ||
         (e = dalloc(h, &h->y_lo, (size_t)T * HID)) != cudaSuccess ||
         (e = dalloc(h, &h->ao_lo, (size_t)T * NQ * HD)) != cudaSuccess ||
-        (e = dalloc(h, &h->m_lo, (size_t)T * h->cfg.ffn)) != cudaSuccess) {
+        (e = dalloc(h, &h->m_lo, (size_t)T * h->cfg.ffn)) != cudaSuccess ||
+        (e = dalloc(h, &h->nss, (size_t)8 * T)) != cudaSuccess) {
         h->T_cap = 0;
         h->h = nullptr;
         return cuda_fail(h, e, "scratch allocation");
@@ -465,10 +473,16 @@ void launch_setup(tts_bb* h, SetupArgs& a) {
 // The layer schedule shared by every mode. T tokens laid out as B sequences x
 // tok_per_seq positions; mode: 0 decode (query length 1), 1 causal prefill,
 // 2 bidirectional pass.
-void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView kv_base, size_t layer_stride,
+// Returns true when the decode step folded its RMSNorms into the GEMM epilogues: the final norm's
+// input (h * gamma, high + low parts) and sums of squares are then in y / y_lo / nss for run_head.
+bool run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView kv_base, size_t layer_stride,
                 double kv_read_bytes = 0, double attn_flops = 0) {
     const tts_bb_config& c = h->cfg;
     const int T = B * tok_per_seq;
+    // decode batches on the split-K decode GEMM: each RMSNorm after the first is folded into the
+    // GEMMs around it (the residual-add epilogue writes h * gamma and per-tile sums of squares; the
+    // next product scales its rows by the inverse RMS)
+    const bool fold = mode == 0 && h->fold_norm && T > 8 && T <= 256;
     // the bidirectional pass keeps K / V in its own pool (no page table), which the tcgen05 kernel reads by TMA
     const bool bidir_tc = mode == 2 && h->attn_bidir_tc;
     // a causal prefill of a full 64-query tile per sequence or more runs on tcgen05 from fp32
@@ -488,7 +502,27 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         bf16* mlo = split ? h->m_lo : nullptr;
         const SplitK* skp = split && h->sk.part ? &h->sk : nullptr;
         const double norm_bytes = T * (4.0 + 2.0) * HID + 2.0 * HID;
-        { Launch L(h, K_RMSNORM, norm_bytes); L += launch_rmsnorm(h->h, w.in_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st, ylo); }
+        auto need = [&](int n) {  // a folded epilogue must run on the decode GEMM
+            if (fold && !n) h->launch_missing = true;
+            return n;
+        };
+        auto scale_in = [&](Epi& ee) {  // consumer of a folded norm
+            ee.nrm_scale_ss = h->nss;
+            ee.nrm_eps = c.rms_eps;
+            ee.nrm_T = T;
+        };
+        auto norm_out = [&](Epi& ee, const bf16* gamma) {  // producer of the next folded norm's input
+            ee.nrm_gamma = gamma;
+            ee.nrm_y = h->y;
+            ee.nrm_ylo = h->y_lo;
+            ee.nrm_ss = h->nss;
+            ee.nrm_eps = c.rms_eps;
+            ee.nrm_T = T;
+        };
+        if (!fold || l == 0) {
+            Launch L(h, K_RMSNORM, norm_bytes);
+            L += launch_rmsnorm(h->h, w.in_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st, ylo);
+        }
         Epi e{};
         float* qf_out = mode == 0 || causal_tc ? h->qf : nullptr;
         int fused = 0;
@@ -497,6 +531,7 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
             e.mode = EPI_QKROPE;
             e.qk = EpiQk{w.qn, w.kn, h->cos_t, h->sin_t, c.rms_eps, h->q, qf_out, kv, h->seq_start, h->seq_len,
                          tok_per_seq, h->err};
+            if (fold && l > 0) scale_in(e);
             Launch L(h, gk, gemm_bytes(T, QKV, HID, 2), 2.0 * T * QKV * HID);
             fused = launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st, ylo, h->err, skp);
             L += fused;
@@ -504,7 +539,8 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         }
         if (!fused) {
             e.mode = EPI_STORE_F32; e.out = h->qkv; e.ldo = QKV;
-            { Launch L(h, gk, gemm_bytes(T, QKV, HID, 4), 2.0 * T * QKV * HID); L += launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st, ylo, h->err, skp); }
+            if (fold && l > 0) scale_in(e);
+            { Launch L(h, gk, gemm_bytes(T, QKV, HID, 4), 2.0 * T * QKV * HID); L += need(launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st, ylo, h->err, skp)); }
             { Launch L(h, K_QKROPE, T * (4.0 * QKV + 2.0 * QKV));
               L += launch_qk_norm_rope_append(h->qkv, w.qn, w.kn, h->cos_t, h->sin_t, c.rms_eps, h->q, kv,
                                               h->seq_start, h->seq_len, tok_per_seq, T, h->err, h->st, qf_out); }
@@ -526,29 +562,44 @@ void run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         }
         e = Epi{};
         e.mode = EPI_ADD_F32; e.out = h->h; e.ldo = HID;
-        { Launch L(h, gk, gemm_bytes(T, HID, NQ * HD, 8), 2.0 * T * HID * NQ * HD); L += launch_gemm(h->ao, w.wo, T, HID, NQ * HD, e, h->st, aolo, h->err, skp); }
-        { Launch L(h, K_RMSNORM, norm_bytes); L += launch_rmsnorm(h->h, w.post_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st, ylo); }
+        if (fold) norm_out(e, w.post_norm);
+        { Launch L(h, gk, gemm_bytes(T, HID, NQ * HD, 8), 2.0 * T * HID * NQ * HD); L += need(launch_gemm(h->ao, w.wo, T, HID, NQ * HD, e, h->st, aolo, h->err, skp)); }
+        if (!fold) { Launch L(h, K_RMSNORM, norm_bytes); L += launch_rmsnorm(h->h, w.post_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st, ylo); }
         e = Epi{};
         e.mode = EPI_SWIGLU; e.out = h->m; e.ldo = c.ffn; e.out_lo = mlo;
-        { Launch L(h, gk, gemm_bytes(T, 2 * c.ffn, HID, 1), 2.0 * T * 2 * c.ffn * HID); L += launch_gemm(h->y, w.wgu, T, 2 * c.ffn, HID, e, h->st, ylo, h->err, skp); }
+        if (fold) scale_in(e);
+        { Launch L(h, gk, gemm_bytes(T, 2 * c.ffn, HID, 1), 2.0 * T * 2 * c.ffn * HID); L += need(launch_gemm(h->y, w.wgu, T, 2 * c.ffn, HID, e, h->st, ylo, h->err, skp)); }
         e = Epi{};
         e.mode = EPI_ADD_F32; e.out = h->h; e.ldo = HID;
-        { Launch L(h, gk, gemm_bytes(T, HID, c.ffn, 8), 2.0 * T * HID * c.ffn); L += launch_gemm(h->m, w.wd, T, HID, c.ffn, e, h->st, mlo, h->err, skp); }
+        if (fold) norm_out(e, l + 1 < c.n_layers ? h->L[l + 1].in_norm : h->final_norm);
+        { Launch L(h, gk, gemm_bytes(T, HID, c.ffn, 8), 2.0 * T * HID * c.ffn); L += need(launch_gemm(h->m, w.wd, T, HID, c.ffn, e, h->st, mlo, h->err, skp)); }
     }
+    return fold;
 }
 
 // Final norm of B selected rows + head GEMM with logits / argmax.
+// folded: the decode layers left the final norm's input (h * gamma, high + low parts) and sums of
+// squares in y / y_lo / nss, so the head scales its rows instead of running the norm.
 void run_head(tts_bb* h, int B, int per_seq, int head_idx, bool last_of_seq, float* logits_out, int32_t* argmax_out,
-              int argmax_stride, bool split = false, bool finalize = true) {
+              int argmax_stride, bool split = false, bool finalize = true, bool folded = false) {
     const tts_bb_config& c = h->cfg;
     bf16* ylo = split ? h->y_lo : nullptr;
-    { Launch L(h, K_RMSNORM, B * 6.0 * HID + 2.0 * HID);
-      L += launch_rmsnorm(h->h, h->final_norm, h->y, B, c.rms_eps, 1, per_seq, 0, last_of_seq ? h->seq_len : nullptr, h->st, ylo); }
+    if (!folded) {
+        Launch L(h, K_RMSNORM, B * 6.0 * HID + 2.0 * HID);
+        L += launch_rmsnorm(h->h, h->final_norm, h->y, B, c.rms_eps, 1, per_seq, 0, last_of_seq ? h->seq_len : nullptr, h->st, ylo);
+    }
     Epi e{};
     e.mode = EPI_LOGITS; e.out = logits_out; e.ldo = c.head_rows; e.amax = argmax_out ? h->amax : nullptr;
+    if (folded) {
+        e.nrm_scale_ss = h->nss;
+        e.nrm_eps = c.rms_eps;
+        e.nrm_T = B;
+    }
     { Launch L(h, B <= 8 ? K_GEMV : (split ? (B <= 256 ? K_GEMM_TCD : K_GEMM) : K_GEMM_TC), gemm_bytes(B, c.head_rows, HID, logits_out ? 4 : 0), 2.0 * B * c.head_rows * HID);
-      L += launch_gemm(h->y, h->heads[head_idx], B, c.head_rows, HID, e, h->st, ylo, h->err,
-                        split && h->sk.part ? &h->sk : nullptr); }
+      const int n = launch_gemm(h->y, h->heads[head_idx], B, c.head_rows, HID, e, h->st, ylo, h->err,
+                                split && h->sk.part ? &h->sk : nullptr);
+      if (folded && !n) h->launch_missing = true;
+      L += n; }
     if (argmax_out && finalize) { Launch L(h, K_ARGMAX); L += launch_argmax_finalize(h->amax, argmax_out, argmax_stride, B, h->st); }
 }
 
@@ -647,9 +698,10 @@ bool decode_step_graph(tts_bb* h, int B, int head_idx, const int32_t* ids, const
             h->launches += launch_embed_codebooks(h->tabs, ids ? h->ids_buf : nullptr, embeds ? h->emb_buf : nullptr,
                                                   h->h, B, h->err, h->st);
             KVView kv{h->pool, h->d_page_table, h->seq_slot, h->mbps};
-            run_layers(h, B, 1, 0, c.max_ctx, kv, h->layer_elems, 0);  // attention grid sized for max_ctx
+            const bool folded = run_layers(h, B, 1, 0, c.max_ctx, kv, h->layer_elems, 0);  // attention grid sized for max_ctx
             if (want_head)
-                run_head(h, B, 1, head_idx, false, logits_out ? h->logits_buf : nullptr, argmax_out, 1, true, false);
+                run_head(h, B, 1, head_idx, false, logits_out ? h->logits_buf : nullptr, argmax_out, 1, true, false,
+                         folded);
             launch_pdl(k_step_publish, B, 256, 0, h->st, h->d_step, want_head && logits_out ? h->logits_buf : nullptr,
                                                   c.head_rows, want_head && argmax_out ? h->amax : nullptr,
                                                   hidden_out ? h->h : nullptr);
@@ -910,6 +962,8 @@ static tts_bb_status create_impl(const tts_bb_config* cfg, const tts_bb_weights*
         h->attn_causal_tc = gemm_tc_available() && !(pv && std::strcmp(pv, "mma") == 0);
         const char* fq = std::getenv("TTS_BB_QKV_EPILOGUE");  // "separate": the q/k norm + RoPE + append kernel
         h->fuse_qk = gemm_tc_available() && !(fq && std::strcmp(fq, "separate") == 0);
+        const char* fnm = std::getenv("TTS_BB_NORM_FOLD");  // "off": the RMSNorm kernels in decode batches
+        h->fold_norm = gemm_tc_available() && !(fnm && std::strcmp(fnm, "off") == 0);
     }
     if (c.max_slots > 0) {  // graph-replayed decode steps: step block, staging ring, fixed input / output buffers
         const char* gv = std::getenv("TTS_BB_GRAPHS");
@@ -1167,12 +1221,12 @@ TTS_API tts_bb_status tts_bb_decode_step(tts_bb* h, int B, const int32_t* slots,
     for (int b = 0; b < B; ++b) kv_bytes += (double)nl[b] * 2 * NKV * HD * 2;
     // attention splits are sized for max_ctx here as in the graph-replayed step, so a step's
     // summation order (and result) does not depend on which of the two ran
-    run_layers(h, B, 1, 0, c.max_ctx, kv, h->layer_elems, kv_bytes);
+    const bool folded = run_layers(h, B, 1, 0, c.max_ctx, kv, h->layer_elems, kv_bytes);
     if (opts && opts->hidden_out)
         cudaMemcpyAsync(opts->hidden_out, h->h, (size_t)B * HID * sizeof(float), cudaMemcpyDeviceToDevice, h->st);
     if (head_idx >= 0 && (logits_out || argmax_out))
         run_head(h, B, 1, head_idx, false, logits_out, argmax_out, opts && opts->argmax_stride ? opts->argmax_stride : 1,
-                 true);
+                 true, true, folded);
     return finish(h);
 }
 

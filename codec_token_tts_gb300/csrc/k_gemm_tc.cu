@@ -442,7 +442,23 @@ struct TcdOut {
     bf16* __restrict__ lo;            // SWIGLU low part (may be null)
     unsigned long long* __restrict__ amax;
     int ldo;
+    // folded RMSNorm (see Epi): producer outputs (rows of this token block) and consumer scale
+    const bf16* __restrict__ ng;
+    bf16* __restrict__ ny;
+    bf16* __restrict__ nylo;
+    float* __restrict__ nss;          // [8][Ttot], absolute token index
+    const float* __restrict__ css;    // [8][Ttot]
+    float eps;
+    int Ttot, tb0;
 };
+
+// 1 / RMS of token tg from the 8 per-tile sums of squares of its 1024 features (fixed order)
+__device__ __forceinline__ float tcd_norm_scale(const float* __restrict__ ss, int Ttot, int tg, float eps) {
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += ss[(size_t)i * Ttot + tg];
+    return rsqrtf(s * (1.f / 1024.f) + eps);
+}
 
 // Sum, in rank order, the S partials of tokens [t0, t1) (this CTA's own
 // partial in `red`, the peers' in `recv`) and apply the epilogue. Epilogue
@@ -469,6 +485,10 @@ __device__ __forceinline__ void tcd_reduce(const TcdOut o, const float* __restri
                 if (p0 + pp < (int)S) { v.x += x[pp].x; v.y += x[pp].y; v.z += x[pp].z; v.w += x[pp].w; }
         }
         const size_t row = (size_t)t * o.ldo;
+        if (MODE != EPI_ADD_F32 && o.css) {  // the folded RMSNorm of this product's input rows
+            const float rs = tcd_norm_scale(o.css, o.Ttot, o.tb0 + t, o.eps);
+            v.x *= rs; v.y *= rs; v.z *= rs; v.w *= rs;
+        }
         if (MODE == EPI_STORE_F32 || MODE == EPI_ADD_F32) {
             float* dst = o.f32 + row + n;
             if (n + 4 <= N) {
@@ -477,6 +497,24 @@ __device__ __forceinline__ void tcd_reduce(const TcdOut o, const float* __restri
                     v.x += h.x; v.y += h.y; v.z += h.z; v.w += h.w;
                 }
                 *reinterpret_cast<float4*>(dst) = v;
+                if (MODE == EPI_ADD_F32 && o.ng) {  // the next norm's input: h * gamma, and this tile's sum of squares
+                    const uint2 gr = *reinterpret_cast<const uint2*>(o.ng + n);
+                    const float g0 = __uint_as_float(gr.x << 16), g1 = __uint_as_float(gr.x & 0xFFFF0000u);
+                    const float g2 = __uint_as_float(gr.y << 16), g3 = __uint_as_float(gr.y & 0xFFFF0000u);
+                    const float f0 = v.x * g0, f1 = v.y * g1, f2 = v.z * g2, f3 = v.w * g3;
+                    __nv_bfloat162 a2 = __floats2bfloat162_rn(f0, f1), b2 = __floats2bfloat162_rn(f2, f3);
+                    uint2 hv;
+                    hv.x = *reinterpret_cast<uint32_t*>(&a2);
+                    hv.y = *reinterpret_cast<uint32_t*>(&b2);
+                    *reinterpret_cast<uint2*>(o.ny + (size_t)t * 1024 + n) = hv;
+                    __nv_bfloat162 al = __halves2bfloat162(f2bf_lo(f0), f2bf_lo(f1));
+                    __nv_bfloat162 bl = __halves2bfloat162(f2bf_lo(f2), f2bf_lo(f3));
+                    hv.x = *reinterpret_cast<uint32_t*>(&al);
+                    hv.y = *reinterpret_cast<uint32_t*>(&bl);
+                    *reinterpret_cast<uint2*>(o.nylo + (size_t)t * 1024 + n) = hv;
+                    const float ssp = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
+                    if (lane == 0) o.nss[(size_t)(n0 / 128) * o.Ttot + o.tb0 + t] = ssp;
+                }
             } else {
                 const float vv[4] = {v.x, v.y, v.z, v.w};
                 for (int j = 0; j < 4 && n + j < N; ++j) dst[j] = (MODE == EPI_ADD_F32 ? dst[j] : 0.f) + vv[j];
@@ -521,7 +559,8 @@ __device__ __forceinline__ void tcd_reduce(const TcdOut o, const float* __restri
 // appended to the paged cache. tb0: the block's first token in the launch.
 __device__ __forceinline__ void tcd_qkrope(const EpiQk& k, const float* __restrict__ red,
                                            const float* __restrict__ recv, int t0, int t1, uint32_t S, uint32_t r,
-                                           int n0, int w, int lane, int tb0) {
+                                           int n0, int w, int lane, int tb0, const float* __restrict__ css, float ceps,
+                                           int Ttot) {
     constexpr int BM = tcd::BM;
     const int nt_all = t1 - t0, f = lane * 4, u = n0 / HD;
     for (int t = t0 + w; t < t1; t += tcd::EPW) {
@@ -540,6 +579,10 @@ __device__ __forceinline__ void tcd_qkrope(const EpiQk& k, const float* __restri
                 if (p0 + pp < (int)S) { x.x += xs[pp].x; x.y += xs[pp].y; x.z += xs[pp].z; x.w += xs[pp].w; }
         }
         const int tg = tb0 + t, seq = tg / k.tok_per_seq, s = tg - seq * k.tok_per_seq;
+        if (css) {  // the folded input RMSNorm of this token
+            const float rs = tcd_norm_scale(css, Ttot, tg, ceps);
+            x.x *= rs; x.y *= rs; x.z *= rs; x.w *= rs;
+        }
         const bool valid = s < k.seq_len[seq];
         const int pos = k.seq_start[seq] + s;
         bf16* kdst = nullptr;
@@ -784,9 +827,18 @@ __global__ void __launch_bounds__(tcd::NT, 1)
         o.lo = e.out_lo ? reinterpret_cast<bf16*>(e.out_lo) + orow : nullptr;
         o.amax = e.amax ? e.amax + tb0 : nullptr;
         o.ldo = e.ldo;
+        o.ng = e.nrm_gamma;
+        o.ny = e.nrm_y ? e.nrm_y + (size_t)tb0 * 1024 : nullptr;
+        o.nylo = e.nrm_ylo ? e.nrm_ylo + (size_t)tb0 * 1024 : nullptr;
+        o.nss = e.nrm_ss;
+        o.css = e.nrm_scale_ss;
+        o.eps = e.nrm_eps;
+        o.Ttot = e.nrm_T;
+        o.tb0 = tb0;
         const int w = warp - 2;
         switch (e.mode) {
-            case EPI_QKROPE: tcd_qkrope(e.qk, red, recv, t0, t1, S, r, n0, w, lane, tb0); break;
+            case EPI_QKROPE: tcd_qkrope(e.qk, red, recv, t0, t1, S, r, n0, w, lane, tb0, e.nrm_scale_ss, e.nrm_eps, e.nrm_T);
+                break;
             case EPI_STORE_F32: tcd_reduce<EPI_STORE_F32>(o, red, recv, t0, t1, S, r, n0, N, w, lane); break;
             case EPI_ADD_F32: tcd_reduce<EPI_ADD_F32>(o, red, recv, t0, t1, S, r, n0, N, w, lane); break;
             case EPI_SWIGLU: tcd_reduce<EPI_SWIGLU>(o, red, recv, t0, t1, S, r, n0, N, w, lane); break;

@@ -515,7 +515,7 @@ static int launch_splitk(const bf16* X, const bf16* X_lo, const bf16* W, int T, 
 int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st, const bf16* X_lo,
                 int* err, const SplitK* skw) {
     if (T <= 0) return 0;
-    if (e.mode == EPI_QKROPE)  // fused q/k norm + RoPE + KV append: the split-K decode GEMM only (else 0)
+    if (e.mode == EPI_QKROPE || e.nrm_gamma || e.nrm_scale_ss)  // fused epilogues: the split-K decode GEMM only (else 0)
         return X_lo && T > 8 && T <= 256 && gemm_tc_available() ? launch_gemm_tcd(X, X_lo, W, T, N, K, e, err, st) : 0;
     if (T <= 8) return launch_gemv(X, W, T, N, K, e, st, X_lo);
     if (X_lo && T <= 256 && gemm_tc_available()) {
