@@ -206,11 +206,12 @@ int launch_attn_bidir_tc(const bf16* q, const bf16* pool, size_t pool_blocks, in
 // Per-token q/k RMSNorm + RoPE; q -> qout [T][16][128] bf16; k, v -> paged pool.
 // Token t belongs to sequence t / tok_per_seq at position seq_start[seq] + t % tok_per_seq,
 // valid when t % tok_per_seq < seq_len[seq].
-// qout_f (optional): the queries as fp32 [T][16][128] instead of bf16 in qout.
+// qout_f (optional): the queries as fp32 [T][16][128] instead of bf16 in qout. qkv_bf (optional):
+// the QKV rows as bf16 [T][4096], read instead of the fp32 qkv.
 int launch_qk_norm_rope_append(const float* qkv, const bf16* qn, const bf16* kn, const float* cos_t,
                                 const float* sin_t, float eps, bf16* qout, KVView kv, const int32_t* seq_start,
                                 const int32_t* seq_len, int tok_per_seq, int T, int* err, cudaStream_t st,
-                                float* qout_f = nullptr);
+                                float* qout_f = nullptr, const bf16* qkv_bf = nullptr);
 // Decode attention, one query per sequence: split-K flash decode + combine.
 // qf (optional): fp32 queries [B][16][128], read instead of the bf16 q.
 int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B, int max_len,

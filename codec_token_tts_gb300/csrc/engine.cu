@@ -538,12 +538,14 @@ bool run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
             e = Epi{};
         }
         if (!fused) {
-            e.mode = EPI_STORE_F32; e.out = h->qkv; e.ldo = QKV;
+            // the bidirectional pass (bf16 operands throughout) keeps its QKV rows in bf16
+            bf16* qkv_bf = mode == 2 && gk == K_GEMM_TC ? reinterpret_cast<bf16*>(h->qkv) : nullptr;
+            e.mode = qkv_bf ? EPI_STORE_BF16 : EPI_STORE_F32; e.out = h->qkv; e.ldo = QKV;
             if (fold && l > 0) scale_in(e);
-            { Launch L(h, gk, gemm_bytes(T, QKV, HID, 4), 2.0 * T * QKV * HID); L += need(launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st, ylo, h->err, skp)); }
-            { Launch L(h, K_QKROPE, T * (4.0 * QKV + 2.0 * QKV));
+            { Launch L(h, gk, gemm_bytes(T, QKV, HID, qkv_bf ? 2 : 4), 2.0 * T * QKV * HID); L += need(launch_gemm(h->y, w.wqkv, T, QKV, HID, e, h->st, ylo, h->err, skp)); }
+            { Launch L(h, K_QKROPE, T * ((qkv_bf ? 2.0 : 4.0) * QKV + 2.0 * QKV));
               L += launch_qk_norm_rope_append(h->qkv, w.qn, w.kn, h->cos_t, h->sin_t, c.rms_eps, h->q, kv,
-                                              h->seq_start, h->seq_len, tok_per_seq, T, h->err, h->st, qf_out); }
+                                              h->seq_start, h->seq_len, tok_per_seq, T, h->err, h->st, qf_out, qkv_bf); }
         }
         if (bidir_tc) {
             Launch L(h, K_ATTN_BIDIR_TC, 0, attn_flops);

@@ -160,8 +160,18 @@ int launch_rmsnorm(const float* h, const bf16* gamma, bf16* y, int T, float eps,
 // rotate pairs (i, i+64) by pos * theta^(-2i/128) (omnivoice-cpp, Qwen3
 // specifics: per-head RMSNorm before RoPE; Qwen3-TTS ncnn port, mRoPE
 // conclusion: 1-D half-rotate RoPE). The cos/sin table is computed on the host.
+// 4 consecutive QKV values from fp32 or bf16 rows
+__device__ __forceinline__ float4 qkv_load4(const float* __restrict__ f, const bf16* __restrict__ b, size_t i) {
+    if (b) {
+        const uint2 u = *reinterpret_cast<const uint2*>(b + i);
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                           __uint_as_float(u.y & 0xFFFF0000u));
+    }
+    return *reinterpret_cast<const float4*>(f + i);
+}
+
 __global__ void __launch_bounds__(256) k_qk_norm_rope_append(
-    const float* __restrict__ qkv, const bf16* __restrict__ qn, const bf16* __restrict__ kn,
+    const float* __restrict__ qkv, const bf16* __restrict__ qkv_bf, const bf16* __restrict__ qn, const bf16* __restrict__ kn,
     const float* __restrict__ cos_t, const float* __restrict__ sin_t, float eps, bf16* __restrict__ qout,
     KVView kv, const int32_t* __restrict__ seq_start, const int32_t* __restrict__ seq_len, int tok_per_seq,
     int* err, float* __restrict__ qout_f) {
@@ -185,13 +195,13 @@ __global__ void __launch_bounds__(256) k_qk_norm_rope_append(
             vdst = kdst + (size_t)NKV * KVB * HD;
         }
     }
-    const float* row = qkv + (size_t)t * QKV;
+    const size_t row = (size_t)t * QKV;
     const int i0 = (lane & 15) * 4;  // frequency index of this lane's first element
     for (int u = warp; u < 32; u += 8) {
         if (u >= 24) {  // v head: copy
             const int g = u - 24;
             if (!kdst) continue;
-            const float4 x = *reinterpret_cast<const float4*>(row + NQ * HD + NKV * HD + g * HD + lane * 4);
+            const float4 x = qkv_load4(qkv, qkv_bf, row + NQ * HD + NKV * HD + g * HD + lane * 4);
             __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y), b = __floats2bfloat162_rn(x.z, x.w);
             uint2 o;
             o.x = *reinterpret_cast<uint32_t*>(&a);
@@ -202,8 +212,8 @@ __global__ void __launch_bounds__(256) k_qk_norm_rope_append(
         const bool isq = u < 16;
         const int hh = isq ? u : u - 16;
         if (!isq && !kdst) continue;
-        const float* src = row + (isq ? hh * HD : NQ * HD + hh * HD);
-        float4 x = *reinterpret_cast<const float4*>(src + lane * 4);
+        const size_t src = row + (isq ? hh * HD : NQ * HD + hh * HD);
+        float4 x = qkv_load4(qkv, qkv_bf, src + lane * 4);
         float ss = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w);
         const float r = rsqrtf(ss * (1.f / HD) + eps);
         const bf16* gm = isq ? qn : kn;
@@ -240,9 +250,9 @@ __global__ void __launch_bounds__(256) k_qk_norm_rope_append(
 int launch_qk_norm_rope_append(const float* qkv, const bf16* qn, const bf16* kn, const float* cos_t,
                                 const float* sin_t, float eps, bf16* qout, KVView kv, const int32_t* seq_start,
                                 const int32_t* seq_len, int tok_per_seq, int T, int* err, cudaStream_t st,
-                                float* qout_f) {
+                                float* qout_f, const bf16* qkv_bf) {
     if (T <= 0) return 0;
-    launch_pdl(k_qk_norm_rope_append, T, 256, 0, st, qkv, qn, kn, cos_t, sin_t, eps, qout, kv, seq_start, seq_len,
+    launch_pdl(k_qk_norm_rope_append, T, 256, 0, st, qkv, qkv_bf, qn, kn, cos_t, sin_t, eps, qout, kv, seq_start, seq_len,
                                              tok_per_seq, err, qout_f);
     return 1;
 }

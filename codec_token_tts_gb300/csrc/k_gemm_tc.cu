@@ -287,6 +287,7 @@ __global__ void __launch_bounds__(tc::NT, 1)
         const int q = warp & 3, h = (warp - 2) >> 2;
         const bool tma_out = e.mode == EPI_STORE_F32 || e.mode == EPI_ADD_F32;
         const bool tma_swiglu = e.mode == EPI_SWIGLU;
+        const bool tma_bf16 = e.mode == EPI_STORE_BF16;
         unsigned char* ost = smem + OST_OFF + (warp - 2) * OST;
         int it = 0;
         for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++it) {
@@ -365,7 +366,33 @@ __global__ void __launch_bounds__(tc::NT, 1)
                     }
                 }
             }
-            for (int c = h * CW; c < (h + 1) * CW && !tma_out && !tma_swiglu; c += 16) {
+            if (tma_bf16) {  // bf16 store: two 16-column chunks per staged 64-byte row, one box per pair
+                for (int c = h * CW; c < (h + 1) * CW; c += 32) {
+                    float v[32];
+                    tc_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c), v);
+                    tc_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c + 16), v + 16);
+                    if (lane == 0) bulk_wait_read0();
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * k + 2 * jj], v[8 * k + 2 * jj + 1]);
+                            pk[jj] = *reinterpret_cast<uint32_t*>(&h2);
+                        }
+                        *reinterpret_cast<uint4*>(ost + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0 && n0 + c < N && m0 + q * 32 < T) {
+                        tma_store_2d(&tmO, n0 + c, m0 + q * 32, ost);
+                        bulk_commit();
+                    }
+                }
+            }
+            for (int c = h * CW; c < (h + 1) * CW && !tma_out && !tma_swiglu && !tma_bf16; c += 16) {
                 uint32_t r[16];
                 const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c);
                 asm volatile(
@@ -388,7 +415,7 @@ __global__ void __launch_bounds__(tc::NT, 1)
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(s_addr(acce + buf)) : "memory");
         }
-        if ((tma_out || tma_swiglu) && lane == 0) bulk_wait0();  // every bulk store of this warp has completed
+        if ((tma_out || tma_swiglu || tma_bf16) && lane == 0) bulk_wait0();  // every bulk store of this warp has completed
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -1566,6 +1593,8 @@ int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi&
     mo = mol = ma;  // unused unless set below
     if (e.mode == EPI_STORE_F32 || e.mode == EPI_ADD_F32) {
         if (!make_out_map(&mo, e.out, T, N, e.ldo)) return 0;
+    } else if (e.mode == EPI_STORE_BF16) {
+        if (!make_out_map(&mo, e.out, T, N, e.ldo, true)) return 0;
     } else if (e.mode == EPI_SWIGLU) {
         if (N % 2 != 0 || !make_out_map(&mo, e.out, T, N / 2, e.ldo, true)) return 0;
         if (e.out_lo && !make_out_map(&mol, e.out_lo, T, N / 2, e.ldo, true)) return 0;
