@@ -62,13 +62,15 @@ __global__ void __launch_bounds__(128) k_attn_decode(const bf16* __restrict__ q,
         const int key0 = j * KVB + warp * 16;
         float d[32];  // d[h*16 + kk]
         uint2 kr[16], vr[16];
-        // K and V of the warp's 16 keys are independent of the scores: issue all loads at once
+        // K of the warp's 16 keys now; their V rows (16 x 256 B: one 128-byte line per lane) are
+        // prefetched into L2 and read after the scores, so fewer registers are live across the loads
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
             const bool ok = key0 + kk < L;
             kr[kk] = ok ? *reinterpret_cast<const uint2*>(kb + (size_t)(warp * 16 + kk) * HD + lane * 4) : make_uint2(0u, 0u);
-            vr[kk] = ok ? *reinterpret_cast<const uint2*>(vb + (size_t)(warp * 16 + kk) * HD + lane * 4) : make_uint2(0u, 0u);
         }
+        if (key0 + (lane >> 1) < L)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(vb + (size_t)(warp * 16 + (lane >> 1)) * HD + (lane & 1) * 64));
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
             const float k0 = __uint_as_float(kr[kk].x << 16), k1 = __uint_as_float(kr[kk].x & 0xFFFF0000u);
@@ -108,6 +110,11 @@ __global__ void __launch_bounds__(128) k_attn_decode(const bf16* __restrict__ q,
         m1 = mn1;
 #pragma unroll
         for (int e = 0; e < 4; ++e) { o0[e] *= a0; o1[e] *= a1; }
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            const bool ok = key0 + kk < L;
+            vr[kk] = ok ? *reinterpret_cast<const uint2*>(vb + (size_t)(warp * 16 + kk) * HD + lane * 4) : make_uint2(0u, 0u);
+        }
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
             const float p0 = __shfl_sync(0xffffffffu, p, kk), p1 = __shfl_sync(0xffffffffu, p, 16 + kk);
