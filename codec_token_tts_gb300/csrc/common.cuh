@@ -214,9 +214,11 @@ int launch_qk_norm_rope_append(const float* qkv, const bf16* qn, const bf16* kn,
                                 float* qout_f = nullptr, const bf16* qkv_bf = nullptr);
 // Decode attention, one query per sequence: split-K flash decode + combine.
 // qf (optional): fp32 queries [B][16][128], read instead of the bf16 q.
+// tps > 1: B = sequences x tps queries of a short causal prefill (query b is token b % tps of
+// sequence b / tps, seq_len gives each sequence's valid tokens).
 int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B, int max_len,
                         float* part, bf16* out, int max_splits, cudaStream_t st, bf16* out_lo = nullptr,
-                        const float* qf = nullptr);
+                        const float* qf = nullptr, int tps = 1, const int32_t* seq_len = nullptr);
 // Prefill / bidirectional attention over the paged view, tensor cores.
 // causal: query at position p sees keys <= p; else keys < key_len[seq].
 // out_lo (optional): low bf16 parts of the output, value - bf16(value).

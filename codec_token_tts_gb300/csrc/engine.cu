@@ -224,6 +224,7 @@ struct tts_bb {
     bool attn_causal_tc = false;        // causal prefill of 64 or more positions per sequence on tcgen05
     bool fuse_qk = false;               // q/k norm + RoPE + KV append in the decode GEMM's QKV epilogue
     bool fold_norm = false;             // decode batches: the RMSNorms folded into the decode GEMMs' epilogues
+    bool short_prefill_attn = false;    // causal prefills of <= 8 positions per sequence on the decode attention
     int32_t* hx_ids = nullptr;  // tts_bb_decode_step_host: device copies of the caller's host ids and argmax
     int32_t* hx_am = nullptr;
     float* hx_logits = nullptr;
@@ -488,6 +489,9 @@ bool run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
     // a causal prefill of a full 64-query tile per sequence or more runs on tcgen05 from fp32
     // queries (shorter ones stay on the mma.sync kernel)
     const bool causal_tc = mode == 1 && h->attn_causal_tc && tok_per_seq >= 64;
+    // a causal prefill of at most 8 positions per sequence (the Code Predictor's 2-token call) runs
+    // on the decode attention kernel, one query per token, from fp32 queries
+    const bool short_prefill = mode == 1 && !causal_tc && tok_per_seq <= 8 && h->short_prefill_attn;
     for (int l = 0; l < c.n_layers; ++l) {
         const LayerW& w = h->L[l];
         KVView kv = kv_base;
@@ -524,7 +528,7 @@ bool run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
             L += launch_rmsnorm(h->h, w.in_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st, ylo);
         }
         Epi e{};
-        float* qf_out = mode == 0 || causal_tc ? h->qf : nullptr;
+        float* qf_out = mode == 0 || causal_tc || short_prefill ? h->qf : nullptr;
         int fused = 0;
         if (gk == K_GEMM_TCD && h->fuse_qk) {
             // the split-K decode GEMM applies q/k norm + RoPE and appends k, v in its epilogue
@@ -553,6 +557,11 @@ bool run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         } else if (mode == 0) {
             Launch L(h, K_ATTN_DECODE, kv_read_bytes + T * (2.0 * NQ * HD * 2), 4.0 * NQ * HD * (kv_read_bytes / (2.0 * NKV * HD * 2)));
             L += launch_attn_decode(h->q, kv, h->seq_start, B, max_len, h->part, h->ao, MAX_SPLITS, h->st, aolo, h->qf);
+        } else if (short_prefill) {
+            Launch L(h, K_ATTN_DECODE, 0, attn_flops);
+            const int nb = std::max(c.max_batch, 1);
+            L += launch_attn_decode(h->q, kv, h->seq_start, T, c.max_ctx, h->part, h->ao, std::max(1, nb * MAX_SPLITS / T),
+                                    h->st, aolo, h->qf, tok_per_seq, h->seq_len);
         } else if (causal_tc) {
             Launch L(h, K_ATTN_CAUSAL_TC, 0, attn_flops);
             L += launch_attn_causal_tc(h->q, h->qf, kv, (size_t)h->kv_blocks, h->seq_start, B, tok_per_seq, h->ao, aolo,
@@ -966,6 +975,7 @@ static tts_bb_status create_impl(const tts_bb_config* cfg, const tts_bb_weights*
         h->fuse_qk = gemm_tc_available() && !(fq && std::strcmp(fq, "separate") == 0);
         const char* fnm = std::getenv("TTS_BB_NORM_FOLD");  // "off": the RMSNorm kernels in decode batches
         h->fold_norm = gemm_tc_available() && !(fnm && std::strcmp(fnm, "off") == 0);
+        h->short_prefill_attn = !(pv && std::strcmp(pv, "mma") == 0);  // TTS_BB_PREFILL_ATTN=mma: every prefill on mma.sync
     }
     if (c.max_slots > 0) {  // graph-replayed decode steps: step block, staging ring, fixed input / output buffers
         const char* gv = std::getenv("TTS_BB_GRAPHS");

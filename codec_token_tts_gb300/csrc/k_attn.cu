@@ -24,16 +24,22 @@ __device__ __forceinline__ const bf16* kv_tile(const KVView& kv, int seq, int j,
 // block of the split; lane l holds head elements 4l..4l+3 of both query heads.
 // With one split the CTA writes the normalised output itself (what the
 // combine would compute: its weight for a single split is exactly 1).
+// Query b (grid z) is token b % tps of sequence b / tps: with tps = 1 one decode token per
+// sequence; with tps > 1 a short causal prefill, query s at position seq_start + s seeing keys up
+// to its own position (a padding token, s >= seq_len, sees the sequence's valid keys only).
 __global__ void __launch_bounds__(128) k_attn_decode(const bf16* __restrict__ q, KVView kv,
                                                      const int32_t* __restrict__ seq_start, int bps,
                                                      int n_splits, float* __restrict__ part,
                                                      bf16* __restrict__ out, bf16* __restrict__ out_lo,
-                                                     const float* __restrict__ qf) {
+                                                     const float* __restrict__ qf, int tps,
+                                                     const int32_t* __restrict__ seq_len) {
     pdl_wait();  // upstream results are read below
     pdl_trigger();
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L = seq_start[b] + 1;                 // keys incl. the token just appended
+    const int seq = b / tps, s_tok = b - seq * tps;
+    // keys incl. the token just appended (decode), or up to this query's position (short prefill)
+    const int L = tps == 1 ? seq_start[seq] + 1 : seq_start[seq] + min(s_tok + 1, seq_len[seq]);
     const int nblk = (L + KVB - 1) / KVB;
     const int blk0 = split * bps, blk1 = min(nblk, blk0 + bps);
 
@@ -57,8 +63,8 @@ __global__ void __launch_bounds__(128) k_attn_decode(const bf16* __restrict__ q,
     float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};
 
     for (int j = blk0; j < blk1; ++j) {
-        const bf16* kb = kv_tile(kv, b, j, 0, g);
-        const bf16* vb = kv_tile(kv, b, j, 1, g);
+        const bf16* kb = kv_tile(kv, seq, j, 0, g);
+        const bf16* vb = kv_tile(kv, seq, j, 1, g);
         const int key0 = j * KVB + warp * 16;
         float d[32];  // d[h*16 + kk]
         uint2 kr[16], vr[16];
@@ -187,7 +193,9 @@ __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ 
 }
 
 int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B, int max_len, float* part,
-                        bf16* out, int max_splits, cudaStream_t st, bf16* out_lo, const float* qf) {
+                        bf16* out, int max_splits, cudaStream_t st, bf16* out_lo, const float* qf, int tps,
+                        const int32_t* seq_len) {
+    if (tps < 1 || (tps > 1 && !seq_len)) return 0;
     if (B <= 0) return 0;
     const int nblk = (max_len + KVB - 1) / KVB;
     // ~32 CTAs per SM (several waves): the block scheduler balances ragged sequence lengths
@@ -196,7 +204,8 @@ int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B
     splits = max(1, min(splits, min(nblk, max_splits)));
     const int bps = (nblk + splits - 1) / splits;
     splits = (nblk + bps - 1) / bps;
-    launch_pdl(k_attn_decode, dim3(splits, NKV, B), 128, 0, st, q, kv, seq_start, bps, splits, part, out, out_lo, qf);
+    launch_pdl(k_attn_decode, dim3(splits, NKV, B), 128, 0, st, q, kv, seq_start, bps, splits, part, out, out_lo, qf,
+               tps, seq_len);
     if (splits == 1) return 1;
     launch_pdl(k_attn_combine, B * NQ, 128, 0, st, part, splits, out, out_lo);
     return 2;

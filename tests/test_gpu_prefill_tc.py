@@ -1,13 +1,15 @@
-"""Causal prefill attention on tcgen05 (GPU), against the fp64 oracle.
+"""Causal prefill attention on tcgen05 and on the decode kernel (GPU), against the fp64 oracle.
 
 A causal prefill of 64 or more positions per sequence runs its attention on
 the tcgen05 flash kernel over the paged cache: query s of sequence b sits at
 position start_b + s and sees every key up to its own position, the keys of
 earlier chunks included. Cases: three ragged sequences prefilled in two
 chunks (the second chunk attends to cached keys of the first, its positions
-crossing cache blocks), and the 28-layer Talker's 128-position prompt. The
-engine's profile must show the tcgen05 kernel, and an engine that keeps the
-prefill on the mma.sync kernel must agree with it.
+crossing cache blocks), and the 28-layer Talker's 128-position prompt. A
+prefill of at most 8 positions per sequence runs on the decode attention
+kernel with one query per token (ragged chunks of up to 8, padding tokens
+included). The engine's profile must show the expected kernel, and an engine
+that keeps every prefill on the mma.sync kernel must agree with it.
 """
 import os
 
@@ -85,3 +87,28 @@ def test_talker_prompt_prefill_on_tcgen05():
         m.tts_bb_profile(e.h, False)
     assert "attn_causal_tcgen05" in kinds, kinds
     assert rel_err_rows(hid.cpu().numpy(), hp) <= HIDDEN_TOL
+
+
+def test_short_ragged_prefill_on_the_decode_kernel():
+    w = synth.model_weights(SHAPE, 93)
+    lens1, lens2 = [5, 2, 8], [3, 8, 1]
+    X = synth.normal_bf16(synth.rng_for(93, "prefill_short"), (3, 16, 1024), 1.0)
+    (h1, h2), kinds = _chunked_prefill(w, X, lens1, lens2, 8, 8)
+    assert "attn_decode" in kinds and "attn_prefill" not in kinds, kinds
+    m0 = O.Backbone(w, SHAPE)
+    for b in range(3):
+        cache = m0.new_cache()
+        n1, n2 = lens1[b], lens2[b]
+        o1 = m0.forward_cached(O.bf16_to_f64(X[b, :n1]), np.arange(n1), cache)
+        o2 = m0.forward_cached(O.bf16_to_f64(X[b, n1:n1 + n2]), np.arange(n1, n1 + n2), cache)
+        assert rel_err_rows(h1[b, :n1], o1) <= HIDDEN_TOL
+        assert rel_err_rows(h2[b, :n2], o2) <= HIDDEN_TOL
+    os.environ["TTS_BB_PREFILL_ATTN"] = "mma"
+    try:
+        (g1, g2), kinds_mma = _chunked_prefill(w, X, lens1, lens2, 8, 8)
+    finally:
+        del os.environ["TTS_BB_PREFILL_ATTN"]
+    assert "attn_prefill" in kinds_mma and "attn_decode" not in kinds_mma
+    for b in range(3):
+        assert rel_err_rows(h1[b, :lens1[b]], g1[b, :lens1[b]]) <= HIDDEN_TOL
+        assert rel_err_rows(h2[b, :lens2[b]], g2[b, :lens2[b]]) <= HIDDEN_TOL
