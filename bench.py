@@ -822,8 +822,8 @@ def roofline_from_profile(rep, traffic=None):
 # files must match, else the bench reports null.
 MEASURED_TRAFFIC = {
     "decode_step_persistent": {"files": ("k_decode_ll.cu", "mega.cuh", "common.cuh"),
-                               "sha256": "f673dc802c8b63796966d6b15ff0faee0015cb2a57a6a1f7a50adc4c16464cac",
-                               "bytes_per_launch": 926.365184e6},
+                               "sha256": "f03e56e5657bc4fa4f3fc573827fd540cbfdca263eb1db6bf22a67e1868a3644",
+                               "bytes_per_launch": 926.815232e6},
 }
 
 
