@@ -677,7 +677,10 @@ __global__ void __launch_bounds__(tcd::NT, 1)
     using namespace tcd;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE);
+    // a stage holds one weight tile and the token block's high and low tiles: sized by TB, so a
+    // small token block leaves room for a second CTA (of the next kernel) on the SM
+    const int STG = A_BYTES + 2 * TB * BK * 2;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STG);
     uint64_t* empty = full + STAGES;
     uint64_t* accf = empty + STAGES;
     uint64_t* recvb = accf + 1;  // peers' slices of this CTA's tokens have landed
@@ -686,7 +689,7 @@ __global__ void __launch_bounds__(tcd::NT, 1)
     // over the stages once the MMAs are done: this CTA's partial sums [TB][128], then the
     // receive buffer [S][tokens of this CTA][128]
     float* red = reinterpret_cast<float*>(smem);
-    float* recv = red + MAXTB * BM;
+    float* recv = red + TB * BM;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint32_t S, r;
     asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(S));
@@ -731,7 +734,7 @@ __global__ void __launch_bounds__(tcd::NT, 1)
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(full + i)),
                              "r"((uint32_t)A_BYTES + b_bytes)
                              : "memory");
-                tma_load_2d(smem + i * STAGE, &tmW, (kb0 + i) * BK, n0, full + i);
+                tma_load_2d(smem + i * STG, &tmW, (kb0 + i) * BK, n0, full + i);
             }
             pdl_wait();
             int issued = 0;
@@ -741,7 +744,7 @@ __global__ void __launch_bounds__(tcd::NT, 1)
                     *abort_s = 1;
                     break;
                 }
-                unsigned char* st = smem + s * STAGE;
+                unsigned char* st = smem + s * STG;
                 const int kx = (kb0 + i) * BK;
                 if (i >= pre) {
                     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(full + s)),
@@ -771,7 +774,7 @@ __global__ void __launch_bounds__(tcd::NT, 1)
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t a0 = s_addr(smem + s * STAGE), b0 = a0 + A_BYTES;
+                const uint32_t a0 = s_addr(smem + s * STG), b0 = a0 + A_BYTES;
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k) {
                     const uint64_t ad = sw128_desc(a0 + k * 32), bd = sw128_desc(b0 + k * 32);
@@ -1558,7 +1561,7 @@ int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(tiles * S, rows);
         cfg.blockDim = dim3(tcd::NT);
-        cfg.dynamicSmemBytes = tcd::SMEM;
+        cfg.dynamicSmemBytes = tcd::STAGES * (tcd::A_BYTES + 2 * TB * tcd::BK * 2) + 1024 + 256;
         cfg.stream = st;
         cudaLaunchAttribute at[2];
         at[0].id = cudaLaunchAttributeClusterDimension;
