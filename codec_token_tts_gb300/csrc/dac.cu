@@ -539,14 +539,20 @@ __global__ void __launch_bounds__(256) k_dac_conv2(const bf16* __restrict__ s_in
     const int t0 = blockIdx.x * 256, b = blockIdx.y;
     const size_t lo_off = (size_t)B * T * 32;
     for (int i = threadIdx.x; i < 224; i += 256) ws[i % 7][i / 7] = w[i];  // w [1][32][7]
-    for (int i = threadIdx.x; i < 262 * 32; i += 256) {
-        const int r = i >> 5, c = i & 31, t = t0 - 3 + r;
-        float v = 0.f;
+    for (int i = threadIdx.x; i < 262 * 4; i += 256) {  // 16-byte pieces: 8 channels of one row, both parts
+        const int r = i >> 2, pc = i & 3, t = t0 - 3 + r;
+        uint4 hv = make_uint4(0u, 0u, 0u, 0u), lv = hv;
         if (t >= 0 && t < T) {
-            const size_t si = ((size_t)b * T + t) * 32 + c;
-            v = __bfloat162float(s_in[si]) + __bfloat162float(s_in[si + lo_off]);
+            const size_t si = ((size_t)b * T + t) * 32 + pc * 8;
+            hv = *reinterpret_cast<const uint4*>(s_in + si);
+            lv = *reinterpret_cast<const uint4*>(s_in + si + lo_off);
         }
-        xs[r][c] = v;
+        const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w}, lw[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            xs[r][pc * 8 + 2 * j] = __uint_as_float(hw[j] << 16) + __uint_as_float(lw[j] << 16);
+            xs[r][pc * 8 + 2 * j + 1] = __uint_as_float(hw[j] & 0xFFFF0000u) + __uint_as_float(lw[j] & 0xFFFF0000u);
+        }
     }
     __syncthreads();
     const int t = t0 + threadIdx.x;
