@@ -212,10 +212,12 @@ int launch_qk_norm_rope_append(const float* qkv, const bf16* qn, const bf16* kn,
                                 const float* sin_t, float eps, bf16* qout, KVView kv, const int32_t* seq_start,
                                 const int32_t* seq_len, int tok_per_seq, int T, int* err, cudaStream_t st,
                                 float* qout_f = nullptr, const bf16* qkv_bf = nullptr);
-// Decode attention, one query per sequence: split-K flash decode + combine.
+// Decode attention, one query per sequence: split-K flash decode + combine; for max_len <=
+// ATTN_SHORT_CTX one warp per (query, KV head) over the whole context, no combine.
 // qf (optional): fp32 queries [B][16][128], read instead of the bf16 q.
 // tps > 1: B = sequences x tps queries of a short causal prefill (query b is token b % tps of
 // sequence b / tps, seq_len gives each sequence's valid tokens).
+constexpr int ATTN_SHORT_CTX = 32;
 int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B, int max_len,
                         float* part, bf16* out, int max_splits, cudaStream_t st, bf16* out_lo = nullptr,
                         const float* qf = nullptr, int tps = 1, const int32_t* seq_len = nullptr);

@@ -390,11 +390,12 @@ tts_bb_status finish(tts_bb* h) {
 }
 
 enum Kind { K_SETUP, K_EMBED, K_RMSNORM, K_GEMV, K_GEMM, K_QKROPE, K_ATTN_DECODE, K_ATTN_PREFILL, K_ARGMAX,
-            K_KVCOPY, K_MEGA, K_GEMM_TC, K_GEMM_TCD, K_ATTN_BIDIR_TC, K_MG_UPDATE, K_FRAME, K_ATTN_CAUSAL_TC, K_NKINDS };
+            K_KVCOPY, K_MEGA, K_GEMM_TC, K_GEMM_TCD, K_ATTN_BIDIR_TC, K_MG_UPDATE, K_FRAME, K_ATTN_CAUSAL_TC,
+            K_ATTN_DECODE_SHORT, K_NKINDS };
 const char* kind_name[K_NKINDS] = {"setup", "embed_gather", "rmsnorm", "gemv", "gemm_mma_split", "qk_norm_rope_append",
                                    "attn_decode", "attn_prefill", "argmax", "kv_copy", "decode_step_persistent",
                                    "gemm_tcgen05", "gemm_tcgen05_decode", "attn_bidir_tcgen05", "maskgit_update", "frame_glue",
-                                   "attn_causal_tcgen05"};
+                                   "attn_causal_tcgen05", "attn_decode_short"};
 
 cudaEvent_t prof_event(tts_bb* h) {
     if (!h->ev_pool.empty()) {
@@ -555,10 +556,11 @@ bool run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
             Launch L(h, K_ATTN_BIDIR_TC, 0, attn_flops);
             L += launch_attn_bidir_tc(h->q, kv.pool, h->mg_pool_blocks, kv.mbps, h->key_len, B, tok_per_seq, h->ao, h->err, h->st);
         } else if (mode == 0) {
-            Launch L(h, K_ATTN_DECODE, kv_read_bytes + T * (2.0 * NQ * HD * 2), 4.0 * NQ * HD * (kv_read_bytes / (2.0 * NKV * HD * 2)));
+            Launch L(h, max_len <= ATTN_SHORT_CTX ? K_ATTN_DECODE_SHORT : K_ATTN_DECODE, kv_read_bytes + T * (2.0 * NQ * HD * 2),
+                     4.0 * NQ * HD * (kv_read_bytes / (2.0 * NKV * HD * 2)));
             L += launch_attn_decode(h->q, kv, h->seq_start, B, max_len, h->part, h->ao, MAX_SPLITS, h->st, aolo, h->qf);
         } else if (short_prefill) {
-            Launch L(h, K_ATTN_DECODE, 0, attn_flops);
+            Launch L(h, c.max_ctx <= ATTN_SHORT_CTX ? K_ATTN_DECODE_SHORT : K_ATTN_DECODE, 0, attn_flops);
             const int nb = std::max(c.max_batch, 1);
             L += launch_attn_decode(h->q, kv, h->seq_start, T, c.max_ctx, h->part, h->ao, std::max(1, nb * MAX_SPLITS / T),
                                     h->st, aolo, h->qf, tok_per_seq, h->seq_len);

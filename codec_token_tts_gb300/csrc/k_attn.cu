@@ -20,6 +20,101 @@ __device__ __forceinline__ const bf16* kv_tile(const KVView& kv, int seq, int j,
 }
 
 // ---------------------------------------------------------------- decode
+// One warp's 16 keys, rows row0 .. row0 + 15 of a cache block whose first key is kbase (K tile kb,
+// V tile vb): the scores of both query heads (lane l holds head elements 4l .. 4l + 3), then the
+// online-softmax update of each head's running max m, sum l and output o. Keys >= L are masked.
+__device__ __forceinline__ void attn_warp_keys16(const float (&q0)[4], const float (&q1)[4], const bf16* kb, const bf16* vb,
+                                                 int kbase, int row0, int L, int lane, float& m0, float& m1, float& l0,
+                                                 float& l1, float (&o0)[4], float (&o1)[4]) {
+    const int key0 = kbase + row0;
+    float d[32];  // d[h*16 + kk]
+    uint2 kr[16], vr[16];
+    // K of the 16 keys now; their V rows (16 x 256 B: one 128-byte line per lane) are
+    // prefetched into L2 and read after the scores, so fewer registers are live across the loads
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+        const bool ok = key0 + kk < L;
+        kr[kk] = ok ? *reinterpret_cast<const uint2*>(kb + (size_t)(row0 + kk) * HD + lane * 4) : make_uint2(0u, 0u);
+    }
+    if (key0 + (lane >> 1) < L)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(vb + (size_t)(row0 + (lane >> 1)) * HD + (lane & 1) * 64));
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+        const float k0 = __uint_as_float(kr[kk].x << 16), k1 = __uint_as_float(kr[kk].x & 0xFFFF0000u);
+        const float k2 = __uint_as_float(kr[kk].y << 16), k3 = __uint_as_float(kr[kk].y & 0xFFFF0000u);
+        d[kk] = q0[0] * k0 + q0[1] * k1 + q0[2] * k2 + q0[3] * k3;
+        d[16 + kk] = q1[0] * k0 + q1[1] * k1 + q1[2] * k2 + q1[3] * k3;
+    }
+    // transpose-reduce: afterwards lane i holds the full dot of index i (head i/16, key i%16)
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = upper ? d[i] : d[i + s];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, s);
+            d[i] = (upper ? d[i + s] : d[i]) + recv;
+        }
+    }
+    const int mykey = key0 + (lane & 15);
+    const float score = (mykey < L) ? d[0] : -INFINITY;
+    float mx = score;
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float mx0 = __shfl_sync(0xffffffffu, mx, 0), mx1 = __shfl_sync(0xffffffffu, mx, 16);
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float mine_m = (lane < 16) ? mn0 : mn1;
+    const float p = (mine_m == -INFINITY) ? 0.f : exp2f(score - mine_m);
+    float ps = p;
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+    const float ps0 = __shfl_sync(0xffffffffu, ps, 0), ps1 = __shfl_sync(0xffffffffu, ps, 16);
+    const float a0 = (mn0 == -INFINITY) ? 1.f : exp2f(m0 - mn0);
+    const float a1 = (mn1 == -INFINITY) ? 1.f : exp2f(m1 - mn1);
+    l0 = l0 * a0 + ps0;
+    l1 = l1 * a1 + ps1;
+    m0 = mn0;
+    m1 = mn1;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) { o0[e] *= a0; o1[e] *= a1; }
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+        const bool ok = key0 + kk < L;
+        vr[kk] = ok ? *reinterpret_cast<const uint2*>(vb + (size_t)(row0 + kk) * HD + lane * 4) : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+        const float p0 = __shfl_sync(0xffffffffu, p, kk), p1 = __shfl_sync(0xffffffffu, p, 16 + kk);
+        {
+            const float v0 = __uint_as_float(vr[kk].x << 16), v1 = __uint_as_float(vr[kk].x & 0xFFFF0000u);
+            const float v2 = __uint_as_float(vr[kk].y << 16), v3 = __uint_as_float(vr[kk].y & 0xFFFF0000u);
+            o0[0] += p0 * v0; o0[1] += p0 * v1; o0[2] += p0 * v2; o0[3] += p0 * v3;
+            o1[0] += p1 * v0; o1[1] += p1 * v1; o1[2] += p1 * v2; o1[3] += p1 * v3;
+        }
+    }
+}
+
+// Query heads 2g and 2g + 1 of query b, elements 4 lane .. 4 lane + 3, scaled by log2(e) / sqrt(128)
+// (fp32 queries qf if given, else the bf16 rows of q).
+__device__ __forceinline__ void attn_load_q(const bf16* __restrict__ q, const float* __restrict__ qf, int b, int g, int lane,
+                                            float (&q0)[4], float (&q1)[4]) {
+    const float sc = rsqrtf((float)HD) * LOG2E;
+    if (qf) {
+        const float4 a = *reinterpret_cast<const float4*>(qf + ((size_t)b * NQ + 2 * g) * HD + lane * 4);
+        const float4 c = *reinterpret_cast<const float4*>(qf + ((size_t)b * NQ + 2 * g + 1) * HD + lane * 4);
+        q0[0] = a.x * sc; q0[1] = a.y * sc; q0[2] = a.z * sc; q0[3] = a.w * sc;
+        q1[0] = c.x * sc; q1[1] = c.y * sc; q1[2] = c.z * sc; q1[3] = c.w * sc;
+    } else {
+        const bf16* qp = q + ((size_t)b * NQ + 2 * g) * HD + lane * 4;
+        const uint2 a = *reinterpret_cast<const uint2*>(qp);
+        const uint2 c = *reinterpret_cast<const uint2*>(qp + HD);
+        q0[0] = __uint_as_float(a.x << 16) * sc; q0[1] = __uint_as_float(a.x & 0xFFFF0000u) * sc;
+        q0[2] = __uint_as_float(a.y << 16) * sc; q0[3] = __uint_as_float(a.y & 0xFFFF0000u) * sc;
+        q1[0] = __uint_as_float(c.x << 16) * sc; q1[1] = __uint_as_float(c.x & 0xFFFF0000u) * sc;
+        q1[2] = __uint_as_float(c.y << 16) * sc; q1[3] = __uint_as_float(c.y & 0xFFFF0000u) * sc;
+    }
+}
+
 // grid (n_splits, 8, B), 128 threads. Warp w takes keys 16w..16w+15 of every
 // block of the split; lane l holds head elements 4l..4l+3 of both query heads.
 // With one split the CTA writes the normalised output itself (what the
@@ -43,94 +138,15 @@ __global__ void __launch_bounds__(128) k_attn_decode(const bf16* __restrict__ q,
     const int nblk = (L + KVB - 1) / KVB;
     const int blk0 = split * bps, blk1 = min(nblk, blk0 + bps);
 
-    const float sc = rsqrtf((float)HD) * LOG2E;
     float q0[4], q1[4];
-    if (qf) {
-        const float4 a = *reinterpret_cast<const float4*>(qf + ((size_t)b * NQ + 2 * g) * HD + lane * 4);
-        const float4 c = *reinterpret_cast<const float4*>(qf + ((size_t)b * NQ + 2 * g + 1) * HD + lane * 4);
-        q0[0] = a.x * sc; q0[1] = a.y * sc; q0[2] = a.z * sc; q0[3] = a.w * sc;
-        q1[0] = c.x * sc; q1[1] = c.y * sc; q1[2] = c.z * sc; q1[3] = c.w * sc;
-    } else {
-        const bf16* qp = q + ((size_t)b * NQ + 2 * g) * HD + lane * 4;
-        const uint2 a = *reinterpret_cast<const uint2*>(qp);
-        const uint2 c = *reinterpret_cast<const uint2*>(qp + HD);
-        q0[0] = __uint_as_float(a.x << 16) * sc; q0[1] = __uint_as_float(a.x & 0xFFFF0000u) * sc;
-        q0[2] = __uint_as_float(a.y << 16) * sc; q0[3] = __uint_as_float(a.y & 0xFFFF0000u) * sc;
-        q1[0] = __uint_as_float(c.x << 16) * sc; q1[1] = __uint_as_float(c.x & 0xFFFF0000u) * sc;
-        q1[2] = __uint_as_float(c.y << 16) * sc; q1[3] = __uint_as_float(c.y & 0xFFFF0000u) * sc;
-    }
+    attn_load_q(q, qf, b, g, lane, q0, q1);
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};
 
     for (int j = blk0; j < blk1; ++j) {
         const bf16* kb = kv_tile(kv, seq, j, 0, g);
         const bf16* vb = kv_tile(kv, seq, j, 1, g);
-        const int key0 = j * KVB + warp * 16;
-        float d[32];  // d[h*16 + kk]
-        uint2 kr[16], vr[16];
-        // K of the warp's 16 keys now; their V rows (16 x 256 B: one 128-byte line per lane) are
-        // prefetched into L2 and read after the scores, so fewer registers are live across the loads
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-            const bool ok = key0 + kk < L;
-            kr[kk] = ok ? *reinterpret_cast<const uint2*>(kb + (size_t)(warp * 16 + kk) * HD + lane * 4) : make_uint2(0u, 0u);
-        }
-        if (key0 + (lane >> 1) < L)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(vb + (size_t)(warp * 16 + (lane >> 1)) * HD + (lane & 1) * 64));
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-            const float k0 = __uint_as_float(kr[kk].x << 16), k1 = __uint_as_float(kr[kk].x & 0xFFFF0000u);
-            const float k2 = __uint_as_float(kr[kk].y << 16), k3 = __uint_as_float(kr[kk].y & 0xFFFF0000u);
-            d[kk] = q0[0] * k0 + q0[1] * k1 + q0[2] * k2 + q0[3] * k3;
-            d[16 + kk] = q1[0] * k0 + q1[1] * k1 + q1[2] * k2 + q1[3] * k3;
-        }
-        // transpose-reduce: afterwards lane i holds the full dot of index i (head i/16, key i%16)
-#pragma unroll
-        for (int s = 16; s >= 1; s >>= 1) {
-            const bool upper = (lane & s) != 0;
-#pragma unroll
-            for (int i = 0; i < s; ++i) {
-                const float send = upper ? d[i] : d[i + s];
-                const float recv = __shfl_xor_sync(0xffffffffu, send, s);
-                d[i] = (upper ? d[i + s] : d[i]) + recv;
-            }
-        }
-        const int mykey = key0 + (lane & 15);
-        const float score = (mykey < L) ? d[0] : -INFINITY;
-        float mx = score;
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const float mx0 = __shfl_sync(0xffffffffu, mx, 0), mx1 = __shfl_sync(0xffffffffu, mx, 16);
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float mine_m = (lane < 16) ? mn0 : mn1;
-        const float p = (mine_m == -INFINITY) ? 0.f : exp2f(score - mine_m);
-        float ps = p;
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-        const float ps0 = __shfl_sync(0xffffffffu, ps, 0), ps1 = __shfl_sync(0xffffffffu, ps, 16);
-        const float a0 = (mn0 == -INFINITY) ? 1.f : exp2f(m0 - mn0);
-        const float a1 = (mn1 == -INFINITY) ? 1.f : exp2f(m1 - mn1);
-        l0 = l0 * a0 + ps0;
-        l1 = l1 * a1 + ps1;
-        m0 = mn0;
-        m1 = mn1;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) { o0[e] *= a0; o1[e] *= a1; }
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-            const bool ok = key0 + kk < L;
-            vr[kk] = ok ? *reinterpret_cast<const uint2*>(vb + (size_t)(warp * 16 + kk) * HD + lane * 4) : make_uint2(0u, 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-            const float p0 = __shfl_sync(0xffffffffu, p, kk), p1 = __shfl_sync(0xffffffffu, p, 16 + kk);
-            {
-                const float v0 = __uint_as_float(vr[kk].x << 16), v1 = __uint_as_float(vr[kk].x & 0xFFFF0000u);
-                const float v2 = __uint_as_float(vr[kk].y << 16), v3 = __uint_as_float(vr[kk].y & 0xFFFF0000u);
-                o0[0] += p0 * v0; o0[1] += p0 * v1; o0[2] += p0 * v2; o0[3] += p0 * v3;
-                o1[0] += p1 * v0; o1[1] += p1 * v1; o1[2] += p1 * v2; o1[3] += p1 * v3;
-            }
-        }
+        attn_warp_keys16(q0, q1, kb, vb, j * KVB, warp * 16, L, lane, m0, m1, l0, l1, o0, o1);
     }
     // merge the 4 warps of the CTA
     __shared__ float sm_ml[4][4];
@@ -171,6 +187,47 @@ __global__ void __launch_bounds__(128) k_attn_decode(const bf16* __restrict__ q,
     if ((threadIdx.x & 63) == 0) { dst[HD] = M; dst[HD + 1] = l; }
 }
 
+// Decode attention for contexts that fit two 16-key rounds (max_len <= ATTN_SHORT_CTX, e.g. the
+// Code Predictor's 16 positions): one warp per (query, KV head) pair takes the keys in rounds of
+// 16 (the split kernel's per-warp step, continued with the online softmax) and writes the
+// normalised output; no warp idles on keys past the end. Queries as in k_attn_decode.
+// grid ceil(B * 8 / 4), 128 threads; warp w of CTA c takes pair 4c + w = b * 8 + g.
+__global__ void __launch_bounds__(128) k_attn_decode_short(const bf16* __restrict__ q, KVView kv,
+                                                           const int32_t* __restrict__ seq_start, int npairs,
+                                                           bf16* __restrict__ out, bf16* __restrict__ out_lo,
+                                                           const float* __restrict__ qf, int tps,
+                                                           const int32_t* __restrict__ seq_len) {
+    pdl_wait();  // upstream results are read below
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pair = blockIdx.x * 4 + warp;
+    if (pair >= npairs) return;
+    const int b = pair / NKV, g = pair - b * NKV;
+    const int seq = b / tps, s_tok = b - seq * tps;
+    const int L = tps == 1 ? seq_start[seq] + 1 : seq_start[seq] + min(s_tok + 1, seq_len[seq]);
+    float q0[4], q1[4];
+    attn_load_q(q, qf, b, g, lane, q0, q1);
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};
+    if (L > 0) {
+        const bf16* kb = kv_tile(kv, seq, 0, 0, g);
+        const bf16* vb = kv_tile(kv, seq, 0, 1, g);
+        for (int row0 = 0; row0 < L && row0 < KVB; row0 += 16)
+            attn_warp_keys16(q0, q1, kb, vb, 0, row0, L, lane, m0, m1, l0, l1, o0, o1);
+    }
+    const size_t o = ((size_t)b * NQ + 2 * g) * HD + lane * 4;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float r0 = l0 > 0.f ? o0[e] / l0 : 0.f, r1 = l1 > 0.f ? o1[e] / l1 : 0.f;
+        out[o + e] = f2bf(r0);
+        out[o + HD + e] = f2bf(r1);
+        if (out_lo) {
+            out_lo[o + e] = f2bf_lo(r0);
+            out_lo[o + HD + e] = f2bf_lo(r1);
+        }
+    }
+}
+
 // grid B*16, 128 threads: merge the splits of one (sequence, head) in split order.
 __global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ part, int n_splits,
                                                       bf16* __restrict__ out, bf16* __restrict__ out_lo) {
@@ -197,6 +254,12 @@ int launch_attn_decode(const bf16* q, KVView kv, const int32_t* seq_start, int B
                         const int32_t* seq_len) {
     if (tps < 1 || (tps > 1 && !seq_len)) return 0;
     if (B <= 0) return 0;
+    if (max_len <= ATTN_SHORT_CTX) {
+        const int npairs = B * NKV;
+        launch_pdl(k_attn_decode_short, (npairs + 3) / 4, 128, 0, st, q, kv, seq_start, npairs, out, out_lo, qf, tps,
+                   seq_len);
+        return 1;
+    }
     const int nblk = (max_len + KVB - 1) / KVB;
     // ~32 CTAs per SM (several waves): the block scheduler balances ragged sequence lengths
     // (splits past a sequence's end exit at once); measured better than one wave of 8 per SM

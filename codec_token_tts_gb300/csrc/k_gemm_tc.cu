@@ -474,8 +474,7 @@ struct TcdOut {
     bf16* __restrict__ ny;
     bf16* __restrict__ nylo;
     float* __restrict__ nss;          // [8][Ttot], absolute token index
-    const float* __restrict__ css;    // [8][Ttot]
-    float eps;
+    const float* __restrict__ css;    // [8][Ttot] (the scales themselves are preloaded: TcdPre)
     int Ttot, tb0;
 };
 
@@ -487,16 +486,68 @@ __device__ __forceinline__ float tcd_norm_scale(const float* __restrict__ ss, in
     return rsqrtf(s * (1.f / 1024.f) + eps);
 }
 
+// Per-token epilogue inputs that do not depend on the product, read by the epilogue warps while
+// the MMAs run (one round trip for all of a warp's tokens instead of one or more per token): the
+// folded norm's inverse RMS (consumers), the residual slice h[t][n .. n + 3] and the gains
+// (EPI_ADD_F32), or the token's position and cache block (EPI_QKROPE). Entry i is token
+// t0 + w + i * EPW of the warp; lane i < 8 computes the per-token scalars and broadcasts them.
+constexpr int TCD_TPW = tcd::MAXTB / tcd::EPW;  // tokens per epilogue warp at most (one split)
+static_assert(TCD_TPW <= 32, "per-token scalars are computed one per lane");
+struct TcdPre {
+    float rs[TCD_TPW];   // folded-norm scale (1 without a folded norm)
+    uint4 pv[TCD_TPW];   // EPI_ADD_F32: the residual float4; EPI_QKROPE: {pos, cache block or -1, valid, 0}
+    uint2 gam;           // EPI_ADD_F32 with a norm output: the gains of features n .. n + 3 (bf16)
+};
+__device__ __forceinline__ void tcd_preload(TcdPre& P, const Epi& e, int t0, int t1, int tb0, int n0, int N, int w,
+                                            int lane) {
+    const int n = n0 + lane * 4;
+    const int ti = t0 + w + lane * tcd::EPW;  // this lane's token (lanes < TCD_TPW)
+    float my_rs = 1.f;
+    int my_pos = 0, my_phys = -1, my_valid = 0;
+    if (lane < TCD_TPW && ti < t1) {
+        const int tg = tb0 + ti;
+        if (e.nrm_scale_ss) my_rs = tcd_norm_scale(e.nrm_scale_ss, e.nrm_T, tg, e.nrm_eps);
+        if (e.mode == EPI_QKROPE) {
+            const EpiQk& k = e.qk;
+            const int seq = tg / k.tok_per_seq, s = tg - seq * k.tok_per_seq;
+            my_valid = s < k.seq_len[seq];
+            my_pos = k.seq_start[seq] + s;
+            if (my_valid && n0 / HD >= NQ) {  // k / v head: the cache block that receives this token
+                const int j = my_pos / KVB;
+                my_phys = k.kv.page_table ? k.kv.page_table[(size_t)k.kv.seq_slot[seq] * k.kv.mbps + j] : seq * k.kv.mbps + j;
+                if (my_phys < 0) {
+                    set_err(k.err, ERR_KV_RANGE);
+                    my_phys = -1;
+                }
+            }
+        }
+    }
+    const bool add = e.mode == EPI_ADD_F32 && n + 4 <= N;
+#pragma unroll
+    for (int i = 0; i < TCD_TPW; ++i) {
+        P.rs[i] = __shfl_sync(0xffffffffu, my_rs, i);
+        P.pv[i] = make_uint4((uint32_t)__shfl_sync(0xffffffffu, my_pos, i), (uint32_t)__shfl_sync(0xffffffffu, my_phys, i),
+                             (uint32_t)__shfl_sync(0xffffffffu, my_valid, i), 0u);
+        const int t = t0 + w + i * tcd::EPW;
+        if (add && t < t1) P.pv[i] = *reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(e.out) + (size_t)(tb0 + t) * e.ldo + n);
+    }
+    P.gam = add && e.nrm_gamma ? *reinterpret_cast<const uint2*>(e.nrm_gamma + n) : make_uint2(0u, 0u);
+}
+
 // Sum, in rank order, the S partials of tokens [t0, t1) (this CTA's own
 // partial in `red`, the peers' in `recv`) and apply the epilogue. Epilogue
 // warp w (of EPW) takes tokens t0 + w, t0 + w + EPW, ...; lane l takes the four features
 // n0 + 4l .. 4l + 3 (vector loads and stores; a gate/up pair stays in one lane).
 template <int MODE>
-__device__ __forceinline__ void tcd_reduce(const TcdOut o, const float* __restrict__ red, const float* __restrict__ recv,
-                                           int t0, int t1, uint32_t S, uint32_t r, int n0, int N, int w, int lane) {
+__device__ __forceinline__ void tcd_reduce(const TcdOut o, const TcdPre& P, const float* __restrict__ red,
+                                           const float* __restrict__ recv, int t0, int t1, uint32_t S, uint32_t r,
+                                           int n0, int N, int w, int lane) {
     constexpr int BM = tcd::BM;
     const int nt_all = t1 - t0, f = lane * 4, n = n0 + f;
-    for (int t = t0 + w; t < t1; t += tcd::EPW) {
+#pragma unroll
+    for (int i = 0; i < TCD_TPW; ++i) {
+        const int t = t0 + w + i * tcd::EPW;
+        if (t >= t1) break;
         const int tl = t - t0;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int p0 = 0; p0 < (int)S; p0 += 4) {
@@ -513,19 +564,19 @@ __device__ __forceinline__ void tcd_reduce(const TcdOut o, const float* __restri
         }
         const size_t row = (size_t)t * o.ldo;
         if (MODE != EPI_ADD_F32 && o.css) {  // the folded RMSNorm of this product's input rows
-            const float rs = tcd_norm_scale(o.css, o.Ttot, o.tb0 + t, o.eps);
+            const float rs = P.rs[i];
             v.x *= rs; v.y *= rs; v.z *= rs; v.w *= rs;
         }
         if (MODE == EPI_STORE_F32 || MODE == EPI_ADD_F32) {
             float* dst = o.f32 + row + n;
             if (n + 4 <= N) {
                 if (MODE == EPI_ADD_F32) {
-                    const float4 h = *reinterpret_cast<const float4*>(dst);
-                    v.x += h.x; v.y += h.y; v.z += h.z; v.w += h.w;
+                    v.x += __uint_as_float(P.pv[i].x); v.y += __uint_as_float(P.pv[i].y);
+                    v.z += __uint_as_float(P.pv[i].z); v.w += __uint_as_float(P.pv[i].w);
                 }
                 *reinterpret_cast<float4*>(dst) = v;
                 if (MODE == EPI_ADD_F32 && o.ng) {  // the next norm's input: h * gamma, and this tile's sum of squares
-                    const uint2 gr = *reinterpret_cast<const uint2*>(o.ng + n);
+                    const uint2 gr = P.gam;
                     const float g0 = __uint_as_float(gr.x << 16), g1 = __uint_as_float(gr.x & 0xFFFF0000u);
                     const float g2 = __uint_as_float(gr.y << 16), g3 = __uint_as_float(gr.y & 0xFFFF0000u);
                     const float f0 = v.x * g0, f1 = v.y * g1, f2 = v.z * g2, f3 = v.w * g3;
@@ -584,13 +635,20 @@ __device__ __forceinline__ void tcd_reduce(const TcdOut o, const float* __restri
 // by pos * theta^(-2i/128) with the partner dims in lane l ^ 16 (omnivoice-cpp, Qwen3 specifics:
 // per-head RMSNorm before RoPE; Qwen3-TTS ncnn port: 1-D half-rotate RoPE); q to q / qf, k and v
 // appended to the paged cache. tb0: the block's first token in the launch.
-__device__ __forceinline__ void tcd_qkrope(const EpiQk& k, const float* __restrict__ red,
+__device__ __forceinline__ void tcd_qkrope(const EpiQk& k, const TcdPre& P, const float* __restrict__ red,
                                            const float* __restrict__ recv, int t0, int t1, uint32_t S, uint32_t r,
-                                           int n0, int w, int lane, int tb0, const float* __restrict__ css, float ceps,
-                                           int Ttot) {
+                                           int n0, int w, int lane, int tb0, bool scaled) {
     constexpr int BM = tcd::BM;
     const int nt_all = t1 - t0, f = lane * 4, u = n0 / HD;
-    for (int t = t0 + w; t < t1; t += tcd::EPW) {
+    const bool isq = u < NQ;
+    const int hh = isq ? u : u - NQ;
+    float gmv[4];  // this lane's q or k norm gains
+#pragma unroll
+    for (int e = 0; e < 4; ++e) gmv[e] = bf2f((isq ? k.qn : k.kn)[lane * 4 + e]);
+#pragma unroll
+    for (int i = 0; i < TCD_TPW; ++i) {
+        const int t = t0 + w + i * tcd::EPW;
+        if (t >= t1) break;
         const int tl = t - t0;
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int p0 = 0; p0 < (int)S; p0 += 4) {
@@ -605,24 +663,15 @@ __device__ __forceinline__ void tcd_qkrope(const EpiQk& k, const float* __restri
             for (int pp = 0; pp < 4; ++pp)
                 if (p0 + pp < (int)S) { x.x += xs[pp].x; x.y += xs[pp].y; x.z += xs[pp].z; x.w += xs[pp].w; }
         }
-        const int tg = tb0 + t, seq = tg / k.tok_per_seq, s = tg - seq * k.tok_per_seq;
-        if (css) {  // the folded input RMSNorm of this token
-            const float rs = tcd_norm_scale(css, Ttot, tg, ceps);
+        const int tg = tb0 + t;
+        if (scaled) {  // the folded input RMSNorm of this token
+            const float rs = P.rs[i];
             x.x *= rs; x.y *= rs; x.z *= rs; x.w *= rs;
         }
-        const bool valid = s < k.seq_len[seq];
-        const int pos = k.seq_start[seq] + s;
-        bf16* kdst = nullptr;
-        if (valid && u >= NQ) {
-            const int j = pos / KVB;
-            const int phys = k.kv.page_table ? k.kv.page_table[(size_t)k.kv.seq_slot[seq] * k.kv.mbps + j]
-                                             : seq * k.kv.mbps + j;
-            if (phys < 0) {
-                if (lane == 0) set_err(k.err, ERR_KV_RANGE);
-            } else {
-                kdst = k.kv.pool + (size_t)phys * 2 * NKV * KVB * HD + (size_t)(pos % KVB) * HD;
-            }
-        }
+        const int pos = (int)P.pv[i].x, phys = (int)P.pv[i].y;
+        const bool valid = P.pv[i].z != 0u;
+        // the cache row of a k / v head's valid token (phys < 0: no append)
+        bf16* kdst = phys >= 0 ? k.kv.pool + (size_t)phys * 2 * NKV * KVB * HD + (size_t)(pos % KVB) * HD : nullptr;
         if (u >= NQ + NKV) {  // v head: copied into the cache
             if (kdst) {
                 __nv_bfloat162 a2 = __floats2bfloat162_rn(x.x, x.y), b2 = __floats2bfloat162_rn(x.z, x.w);
@@ -633,15 +682,12 @@ __device__ __forceinline__ void tcd_qkrope(const EpiQk& k, const float* __restri
             }
             continue;
         }
-        const bool isq = u < NQ;
-        const int hh = isq ? u : u - NQ;
         if (!isq && !kdst) continue;
         const float ss = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w);
         const float rn = rsqrtf(ss * (1.f / HD) + k.eps);
-        const bf16* gm = isq ? k.qn : k.kn;
         float v[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = v[e] * rn * bf2f(gm[lane * 4 + e]);
+        for (int e = 0; e < 4; ++e) v[e] = v[e] * rn * gmv[e];
         float pv[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) pv[e] = __shfl_xor_sync(0xffffffffu, v[e], 16);
@@ -724,6 +770,10 @@ __global__ void __launch_bounds__(tcd::NT, 1)
     const uint32_t tmem = *tmem_slot;
     pdl_trigger();
     if (!(warp == 0 && lane == 0)) pdl_wait();  // activations (and the output) come from upstream kernels
+    // tokens owned by CTA q: [tok(q), tok(q + 1))
+    auto tok = [&](uint32_t q) { return (int)(q * (uint32_t)Th / S); };
+    const int t0 = tok(r), t1 = tok(r + 1);
+    TcdPre pre;
 
     if (warp == 0) {
         if (lane == 0) {  // TMA producer
@@ -796,6 +846,7 @@ __global__ void __launch_bounds__(tcd::NT, 1)
         // partial sums: thread = feature q * 32 + lane; column c < TB is token c's high part, TB + c its low
         // part; the EPW / 4 warps of a lane quarter take 16-column chunks in turn
         const int q = warp & 3, hf = (warp - 2) >> 2, f = q * 32 + lane;
+        tcd_preload(pre, e, t0, t1, tb0, n0, N, warp - 2, lane);  // overlaps the MMAs
         const bool ok = tc_wait(accf, 0, abort_s) && !*abort_s;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (ok) {
@@ -824,9 +875,6 @@ __global__ void __launch_bounds__(tcd::NT, 1)
             set_err(err, ERR_TIMEOUT);
         }
     }
-    // tokens owned by CTA q: [tok(q), tok(q + 1))
-    auto tok = [&](uint32_t q) { return (int)(q * (uint32_t)Th / S); };
-    const int t0 = tok(r), t1 = tok(r + 1);
     if (threadIdx.x == 0)  // expect the S - 1 peers' slices of this CTA's tokens
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s_addr(recvb)),
                      "r"((uint32_t)((S - 1) * (t1 - t0) * BM * 4))
@@ -862,17 +910,16 @@ __global__ void __launch_bounds__(tcd::NT, 1)
         o.nylo = e.nrm_ylo ? e.nrm_ylo + (size_t)tb0 * 1024 : nullptr;
         o.nss = e.nrm_ss;
         o.css = e.nrm_scale_ss;
-        o.eps = e.nrm_eps;
         o.Ttot = e.nrm_T;
         o.tb0 = tb0;
         const int w = warp - 2;
         switch (e.mode) {
-            case EPI_QKROPE: tcd_qkrope(e.qk, red, recv, t0, t1, S, r, n0, w, lane, tb0, e.nrm_scale_ss, e.nrm_eps, e.nrm_T);
+            case EPI_QKROPE: tcd_qkrope(e.qk, pre, red, recv, t0, t1, S, r, n0, w, lane, tb0, e.nrm_scale_ss != nullptr);
                 break;
-            case EPI_STORE_F32: tcd_reduce<EPI_STORE_F32>(o, red, recv, t0, t1, S, r, n0, N, w, lane); break;
-            case EPI_ADD_F32: tcd_reduce<EPI_ADD_F32>(o, red, recv, t0, t1, S, r, n0, N, w, lane); break;
-            case EPI_SWIGLU: tcd_reduce<EPI_SWIGLU>(o, red, recv, t0, t1, S, r, n0, N, w, lane); break;
-            default: tcd_reduce<EPI_LOGITS>(o, red, recv, t0, t1, S, r, n0, N, w, lane); break;
+            case EPI_STORE_F32: tcd_reduce<EPI_STORE_F32>(o, pre, red, recv, t0, t1, S, r, n0, N, w, lane); break;
+            case EPI_ADD_F32: tcd_reduce<EPI_ADD_F32>(o, pre, red, recv, t0, t1, S, r, n0, N, w, lane); break;
+            case EPI_SWIGLU: tcd_reduce<EPI_SWIGLU>(o, pre, red, recv, t0, t1, S, r, n0, N, w, lane); break;
+            default: tcd_reduce<EPI_LOGITS>(o, pre, red, recv, t0, t1, S, r, n0, N, w, lane); break;
         }
     }
     cluster_sync_all();  // peers are done reading this CTA's partials

@@ -9,7 +9,9 @@ crossing cache blocks), and the 28-layer Talker's 128-position prompt. A
 prefill of at most 8 positions per sequence runs on the decode attention
 kernel with one query per token (ragged chunks of up to 8, padding tokens
 included). The engine's profile must show the expected kernel, and an engine
-that keeps every prefill on the mma.sync kernel must agree with it.
+that keeps every prefill on the mma.sync kernel must agree with it. Contexts
+of at most 32 keys (the Code Predictor's) run decode attention and the short
+prefill one warp per (query, KV head) in 16-key rounds.
 """
 import os
 
@@ -112,3 +114,40 @@ def test_short_ragged_prefill_on_the_decode_kernel():
     for b in range(3):
         assert rel_err_rows(h1[b, :lens1[b]], g1[b, :lens1[b]]) <= HIDDEN_TOL
         assert rel_err_rows(h2[b, :lens2[b]], g2[b, :lens2[b]]) <= HIDDEN_TOL
+
+
+def test_short_context_attention_one_warp_per_head():
+    """12 sequences, ragged 1..8-token prefills, then decode steps up to 32 keys (max_ctx 32)."""
+    w = synth.model_weights(SHAPE, 95)
+    B, S, CTX = 12, 8, 32
+    r = synth.rng_for(95, "short_ctx")
+    lens = [int(x) for x in r.integers(1, S + 1, B)]
+    n_dec = CTX - max(lens)
+    X = synth.normal_bf16(r, (B, S, 1024), 1.0)
+    D = synth.normal_bf16(r, (n_dec, B, 1024), 1.0)
+    emb = np.zeros((B, S, 1024), np.uint16)
+    for b in range(B):
+        emb[b, :lens[b]] = X[b, :lens[b]]
+    with Engine(w, max_slots=B, max_ctx=CTX, max_batch=B, max_tokens=B * S) as e:
+        m = e.m
+        m.tts_bb_profile(e.h, True)
+        hid = f32_zeros(B * S, 1024)
+        m.tts_bb_prefill(e.h, B, S, list(range(B)), lens, embeds=dev_bf16_bits(emb), hidden_out=hid)
+        hp = hid.cpu().numpy().reshape(B, S, 1024)
+        kv, hd = list(lens), []
+        for t in range(n_dec):
+            ho = f32_zeros(B, 1024)
+            m.tts_bb_decode_step(e.h, B, list(range(B)), kv, None, embeds=dev_bf16_bits(D[t]), hidden_out=ho)
+            hd.append(ho.cpu().numpy())
+            kv = [x + 1 for x in kv]
+        kinds = {k["kind"] for k in m.tts_bb_profile_report(e.h)["kernels"]}
+        m.tts_bb_profile(e.h, False)
+    assert "attn_decode_short" in kinds and "attn_decode" not in kinds, kinds
+    m0 = O.Backbone(w, SHAPE)
+    for b in range(B):
+        cache = m0.new_cache()
+        n = lens[b]
+        o1 = m0.forward_cached(O.bf16_to_f64(X[b, :n]), np.arange(n), cache)
+        assert rel_err_rows(hp[b, :n], o1) <= HIDDEN_TOL
+        od = np.stack([m0.forward_cached(O.bf16_to_f64(D[t, b:b + 1]), [n + t], cache)[0] for t in range(n_dec)])
+        assert rel_err_rows(np.stack([x[b] for x in hd]), od) <= HIDDEN_TOL
