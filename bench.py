@@ -822,8 +822,8 @@ def roofline_from_profile(rep, traffic=None):
 # files must match, else the bench reports null.
 MEASURED_TRAFFIC = {
     "decode_step_persistent": {"files": ("k_decode_ll.cu", "mega.cuh", "common.cuh"),
-                               "sha256": "f03e56e5657bc4fa4f3fc573827fd540cbfdca263eb1db6bf22a67e1868a3644",
-                               "bytes_per_launch": 926.815232e6},
+                               "sha256": "0c156b34053d153f0edfe7ddbe9640f9411301c399b3d573fb0681e91854144c",
+                               "bytes_per_launch": 926.577664e6},
 }
 
 

@@ -534,6 +534,28 @@ __device__ __forceinline__ void tcd_preload(TcdPre& P, const Epi& e, int t0, int
     P.gam = add && e.nrm_gamma ? *reinterpret_cast<const uint2*>(e.nrm_gamma + n) : make_uint2(0u, 0u);
 }
 
+// Rank-order sum of the S partials of token t (local index tl of nt_all), features f .. f + 3:
+// this CTA's own (rank r) in red, the peers' in recv.
+__device__ __forceinline__ float4 tcd_sum(const float* __restrict__ red, const float* __restrict__ recv, int t, int tl,
+                                          int nt_all, uint32_t S, uint32_t r, int f) {
+    constexpr int BM = tcd::BM;
+    if (S == 1) return *reinterpret_cast<const float4*>(red + (size_t)t * BM + f);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p0 = 0; p0 < (int)S; p0 += 4) {
+        float4 x[4];
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+            const int p = min(p0 + pp, (int)S - 1);
+            const float* src = p == (int)r ? red + (size_t)t * BM + f : recv + ((size_t)p * nt_all + tl) * BM + f;
+            x[pp] = *reinterpret_cast<const float4*>(src);
+        }
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp)
+            if (p0 + pp < (int)S) { v.x += x[pp].x; v.y += x[pp].y; v.z += x[pp].z; v.w += x[pp].w; }
+    }
+    return v;
+}
+
 // Sum, in rank order, the S partials of tokens [t0, t1) (this CTA's own
 // partial in `red`, the peers' in `recv`) and apply the epilogue. Epilogue
 // warp w (of EPW) takes tokens t0 + w, t0 + w + EPW, ...; lane l takes the four features
@@ -542,26 +564,13 @@ template <int MODE>
 __device__ __forceinline__ void tcd_reduce(const TcdOut o, const TcdPre& P, const float* __restrict__ red,
                                            const float* __restrict__ recv, int t0, int t1, uint32_t S, uint32_t r,
                                            int n0, int N, int w, int lane) {
-    constexpr int BM = tcd::BM;
     const int nt_all = t1 - t0, f = lane * 4, n = n0 + f;
 #pragma unroll
     for (int i = 0; i < TCD_TPW; ++i) {
         const int t = t0 + w + i * tcd::EPW;
         if (t >= t1) break;
         const int tl = t - t0;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int p0 = 0; p0 < (int)S; p0 += 4) {
-            float4 x[4];
-#pragma unroll
-            for (int pp = 0; pp < 4; ++pp) {
-                const int p = min(p0 + pp, (int)S - 1);
-                const float* src = p == (int)r ? red + (size_t)t * BM + f : recv + ((size_t)p * nt_all + tl) * BM + f;
-                x[pp] = *reinterpret_cast<const float4*>(src);
-            }
-#pragma unroll
-            for (int pp = 0; pp < 4; ++pp)
-                if (p0 + pp < (int)S) { v.x += x[pp].x; v.y += x[pp].y; v.z += x[pp].z; v.w += x[pp].w; }
-        }
+        float4 v = tcd_sum(red, recv, t, tl, nt_all, S, r, f);
         const size_t row = (size_t)t * o.ldo;
         if (MODE != EPI_ADD_F32 && o.css) {  // the folded RMSNorm of this product's input rows
             const float rs = P.rs[i];
@@ -638,7 +647,6 @@ __device__ __forceinline__ void tcd_reduce(const TcdOut o, const TcdPre& P, cons
 __device__ __forceinline__ void tcd_qkrope(const EpiQk& k, const TcdPre& P, const float* __restrict__ red,
                                            const float* __restrict__ recv, int t0, int t1, uint32_t S, uint32_t r,
                                            int n0, int w, int lane, int tb0, bool scaled) {
-    constexpr int BM = tcd::BM;
     const int nt_all = t1 - t0, f = lane * 4, u = n0 / HD;
     const bool isq = u < NQ;
     const int hh = isq ? u : u - NQ;
@@ -650,19 +658,7 @@ __device__ __forceinline__ void tcd_qkrope(const EpiQk& k, const TcdPre& P, cons
         const int t = t0 + w + i * tcd::EPW;
         if (t >= t1) break;
         const int tl = t - t0;
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int p0 = 0; p0 < (int)S; p0 += 4) {
-            float4 xs[4];
-#pragma unroll
-            for (int pp = 0; pp < 4; ++pp) {
-                const int p = min(p0 + pp, (int)S - 1);
-                const float* src = p == (int)r ? red + (size_t)t * BM + f : recv + ((size_t)p * nt_all + tl) * BM + f;
-                xs[pp] = *reinterpret_cast<const float4*>(src);
-            }
-#pragma unroll
-            for (int pp = 0; pp < 4; ++pp)
-                if (p0 + pp < (int)S) { x.x += xs[pp].x; x.y += xs[pp].y; x.z += xs[pp].z; x.w += xs[pp].w; }
-        }
+        float4 x = tcd_sum(red, recv, t, tl, nt_all, S, r, f);
         const int tg = tb0 + t;
         if (scaled) {  // the folded input RMSNorm of this token
             const float rs = P.rs[i];
