@@ -894,6 +894,8 @@ __global__ void __launch_bounds__(tcd::NT, 1)
     if (warp >= 2) {
         const bool got = t1 == t0 || S == 1 || tc_wait(recvb, 0, abort_s);
         if (!got && lane == 0 && warp == 2) set_err(err, ERR_TIMEOUT);
+        // this CTA's incoming partials have landed: the peers' copies out of their shared memory are done
+        asm volatile("barrier.cluster.arrive;" ::: "memory");
         TcdOut o;
         const size_t orow = (size_t)tb0 * e.ldo;
         o.f32 = e.out ? reinterpret_cast<float*>(e.out) + orow : nullptr;
@@ -918,7 +920,10 @@ __global__ void __launch_bounds__(tcd::NT, 1)
             default: tcd_reduce<EPI_LOGITS>(o, pre, red, recv, t0, t1, S, r, n0, N, w, lane); break;
         }
     }
-    cluster_sync_all();  // peers are done reading this CTA's partials
+    // exit (and free the SM for the next launch) once every peer has received this CTA's partials,
+    // without waiting for the peers' reductions
+    if (warp < 2) asm volatile("barrier.cluster.arrive;" ::: "memory");
+    asm volatile("barrier.cluster.wait;" ::: "memory");
     if (warp == 1) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tcols));
