@@ -933,8 +933,13 @@ def main():
     res, wl = run_talker_b1(args, ws, rank)
     res["roofline"] = roofline_from_profile(res["kernel_profile"], measured_traffic(res["kernel_profile"]))
     if not args.no_secondary:
-        res["also"] = {"serving_b64": run_serving_b64(64, 4), "maskgit": run_maskgit(8, 3),
-                       "code_predictor": run_code_predictor(16, 3), "frame_loop": run_frame_loop(64, 4)}
+        sv = run_serving_b64(64, 4)
+        # the batch-64 half of the metric at the top level of the line (the "also" block holds the details)
+        res["batch64"] = {"value": sv["value"], "unit": sv["unit"], "ms_per_step": sv["ms_per_step"],
+                          "workload": sv["workload"], "roofline": sv.get("roofline")}
+        res["also"] = {"serving_b64": {k: v for k, v in sv.items() if k != "kernel_profile"},
+                       "maskgit": run_maskgit(8, 3), "code_predictor": run_code_predictor(16, 3),
+                       "frame_loop": run_frame_loop(64, 4)}
     if rank == 0 and not args.no_cpu_baseline:
         v, n, el, setup_s = oracle_talker_tokens_per_s(args.cpu_budget_s, 10_000)
         ci = cpu_info()

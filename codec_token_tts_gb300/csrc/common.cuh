@@ -181,11 +181,12 @@ struct SplitK {
     int* ctr;
     int n_ctr;
 };
-// Plain bf16 activations with T > 8 run on tcgen05 (k_gemm_tc.cu); split
-// activations (X_lo) with 8 < T <= 128 run on the swap-AB cluster split-K
-// tcgen05 kernel (k_gemm_tc.cu), with T <= 256 on the split-K mma.sync kernel
-// when a workspace is given, else on the tiled mma.sync kernel with a second
-// MMA per k-step.
+// T <= 8: the matrix-vector kernel. Split activations (X_lo): the swap-AB cluster split-K tcgen05
+// kernel (k_gemm_tc.cu) for up to two 128-token blocks, and for three or four when one launch of
+// them fits one wave (gemm_tcd_takes); beyond that the dense persistent tcgen05 kernel with two
+// passes over K. Plain bf16 activations with T > 8: the dense tcgen05 kernel. Without tcgen05
+// the mma.sync kernels (split-K with a workspace, else tiled with a second MMA per k-step).
+// Fused epilogues (q/k norm + RoPE + append, folded norms) run on the split-K tcgen05 kernel only.
 int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e, cudaStream_t st,
                 const bf16* X_lo = nullptr, int* err = nullptr, const SplitK* sk = nullptr);
 // Dense persistent tcgen05 GEMM; with X_lo the activations are bf16 high + low parts (two passes over K).
@@ -193,6 +194,8 @@ int launch_gemm_tc(const bf16* X, const bf16* W, int T, int N, int K, const Epi&
                    const bf16* X_lo = nullptr);
 int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N, int K, const Epi& e, int* err,
                     cudaStream_t st);
+// Whether launch_gemm_tcd takes a [T x K] x [N x K]^T product (up to four 128-token blocks).
+bool gemm_tcd_takes(int T, int N, int K);
 bool gemm_tc_available();
 // MaskGIT greedy update (k_maskgit.cu): two launches
 int launch_maskgit_update(const float* logits, int n_items, int K, int T, int V, int S_log, int cond_pos0,

@@ -501,7 +501,11 @@ bool run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         // prefill writes the K/V that every later step reads); the bidirectional
         // pass, tensor-bound, uses plain bf16
         const bool split = mode != 2;
-        const int gk = T <= 8 ? K_GEMV : (split && T <= 256 ? K_GEMM_TCD : K_GEMM_TC);  // the kernel launch_gemm picks
+        // the kernel launch_gemm picks for an N x K product
+        auto gk_of = [&](int N, int K) {
+            return T <= 8 ? K_GEMV : (split && (T <= 256 || gemm_tcd_takes(T, N, K)) ? K_GEMM_TCD : K_GEMM_TC);
+        };
+        const int gk = gk_of(QKV, HID), gk_o = gk_of(HID, NQ * HD), gk_gu = gk_of(2 * c.ffn, HID), gk_d = gk_of(HID, c.ffn);
         bf16* ylo = split ? h->y_lo : nullptr;
         bf16* aolo = split ? h->ao_lo : nullptr;
         bf16* mlo = split ? h->m_lo : nullptr;
@@ -576,16 +580,16 @@ bool run_layers(tts_bb* h, int B, int tok_per_seq, int mode, int max_len, KVView
         e = Epi{};
         e.mode = EPI_ADD_F32; e.out = h->h; e.ldo = HID;
         if (fold) norm_out(e, w.post_norm);
-        { Launch L(h, gk, gemm_bytes(T, HID, NQ * HD, 8), 2.0 * T * HID * NQ * HD); L += need(launch_gemm(h->ao, w.wo, T, HID, NQ * HD, e, h->st, aolo, h->err, skp)); }
+        { Launch L(h, gk_o, gemm_bytes(T, HID, NQ * HD, 8), 2.0 * T * HID * NQ * HD); L += need(launch_gemm(h->ao, w.wo, T, HID, NQ * HD, e, h->st, aolo, h->err, skp)); }
         if (!fold) { Launch L(h, K_RMSNORM, norm_bytes); L += launch_rmsnorm(h->h, w.post_norm, h->y, T, c.rms_eps, 1, 1, 0, nullptr, h->st, ylo); }
         e = Epi{};
         e.mode = EPI_SWIGLU; e.out = h->m; e.ldo = c.ffn; e.out_lo = mlo;
         if (fold) scale_in(e);
-        { Launch L(h, gk, gemm_bytes(T, 2 * c.ffn, HID, 1), 2.0 * T * 2 * c.ffn * HID); L += need(launch_gemm(h->y, w.wgu, T, 2 * c.ffn, HID, e, h->st, ylo, h->err, skp)); }
+        { Launch L(h, gk_gu, gemm_bytes(T, 2 * c.ffn, HID, 1), 2.0 * T * 2 * c.ffn * HID); L += need(launch_gemm(h->y, w.wgu, T, 2 * c.ffn, HID, e, h->st, ylo, h->err, skp)); }
         e = Epi{};
         e.mode = EPI_ADD_F32; e.out = h->h; e.ldo = HID;
         if (fold) norm_out(e, l + 1 < c.n_layers ? h->L[l + 1].in_norm : h->final_norm);
-        { Launch L(h, gk, gemm_bytes(T, HID, c.ffn, 8), 2.0 * T * HID * c.ffn); L += need(launch_gemm(h->m, w.wd, T, HID, c.ffn, e, h->st, mlo, h->err, skp)); }
+        { Launch L(h, gk_d, gemm_bytes(T, HID, c.ffn, 8), 2.0 * T * HID * c.ffn); L += need(launch_gemm(h->m, w.wd, T, HID, c.ffn, e, h->st, mlo, h->err, skp)); }
     }
     return fold;
 }
@@ -608,7 +612,8 @@ void run_head(tts_bb* h, int B, int per_seq, int head_idx, bool last_of_seq, flo
         e.nrm_eps = c.rms_eps;
         e.nrm_T = B;
     }
-    { Launch L(h, B <= 8 ? K_GEMV : (split ? (B <= 256 ? K_GEMM_TCD : K_GEMM) : K_GEMM_TC), gemm_bytes(B, c.head_rows, HID, logits_out ? 4 : 0), 2.0 * B * c.head_rows * HID);
+    const int gk = B <= 8 ? K_GEMV : (split && (B <= 256 || gemm_tcd_takes(B, c.head_rows, HID)) ? K_GEMM_TCD : K_GEMM_TC);
+    { Launch L(h, gk, gemm_bytes(B, c.head_rows, HID, logits_out ? 4 : 0), 2.0 * B * c.head_rows * HID);
       const int n = launch_gemm(h->y, h->heads[head_idx], B, c.head_rows, HID, e, h->st, ylo, h->err,
                                 split && h->sk.part ? &h->sk : nullptr);
       if (folded && !n) h->launch_missing = true;

@@ -24,6 +24,8 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+
+#include <array>
 #include "tcgen05.cuh"
 
 namespace ttsbb {
@@ -442,7 +444,8 @@ __global__ void __launch_bounds__(tc::NT, 1)
 namespace tcd {
 constexpr int EPW = 16;  // epilogue warps (EPW / 4 per TMEM lane quarter)
 constexpr int BM = 128, BK = 64, STAGES = 4, NT = 64 + 32 * EPW;  // warp 0 TMA, warp 1 MMA, then the epilogue
-constexpr int MAXTB = 128;                          // padded tokens per launch
+constexpr int MAXTB = 128;                          // tokens per CTA (one token block)
+constexpr int MAXBLK = 4;                           // token blocks per launch (grid y)
 constexpr int A_BYTES = BM * BK * 2;                // 16 KB
 constexpr int STAGE = A_BYTES + 2 * MAXTB * BK * 2; // 48 KB
 constexpr int SMEM = STAGES * STAGE + 1024 + 256;
@@ -1553,9 +1556,61 @@ int launch_attn_causal_tc(const bf16* q, const float* qf, KVView kv, size_t pool
     return qf ? launch_attn_tc<true>(mkv, A, B, st) : launch_attn_tc<false>(mkv, A, B, st);
 }
 
+namespace {
+constexpr int TCD_CAND[8] = {1, 2, 3, 4, 6, 8, 12, 16};  // cluster sizes (split-K ways)
+// Clusters of each candidate size that fit at once (1 CTA per SM), found once per process.
+const int* tcd_fit() {
+    static const std::array<int, 8> fit = [] {
+        std::array<int, 8> f{};
+        cudaFuncSetAttribute(k_gemm_tcd, cudaFuncAttributeMaxDynamicSharedMemorySize, tcd::SMEM);
+        const bool nonport = cudaFuncSetAttribute(k_gemm_tcd, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+        for (int i = 0; i < 8; ++i) {
+            if (TCD_CAND[i] > 8 && !nonport) continue;
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(TCD_CAND[i]);
+            q.blockDim = dim3(tcd::NT);
+            q.dynamicSmemBytes = tcd::SMEM;
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = TCD_CAND[i];
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            q.attrs = qa;
+            q.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tcd, &q) == cudaSuccess) f[i] = n;
+        }
+        cudaGetLastError();
+        return f;
+    }();
+    return fit.data();
+}
+// The most CTAs with which `clusters` clusters (one per weight tile and token block) all run in
+// one wave, and the cluster size S that gives it; 0 if no size fits.
+int tcd_pick(int clusters, int KT, int& S) {
+    const int* fit = tcd_fit();
+    int best = 0;
+    S = 1;
+    for (int i = 0; i < 8; ++i)
+        if (TCD_CAND[i] <= KT && clusters <= fit[i] && clusters * TCD_CAND[i] > best) {
+            best = clusters * TCD_CAND[i];
+            S = TCD_CAND[i];
+        }
+    return best;
+}
+}  // namespace
+
+bool gemm_tcd_takes(int T, int N, int K) {
+    if (T <= 0 || T > tcd::MAXBLK * tcd::MAXTB || N <= 0 || K <= 0 || K % tcd::BK != 0) return false;
+    const int blocks = (T + tcd::MAXTB - 1) / tcd::MAXTB;
+    if (blocks <= 2) return true;  // one launch over both blocks, or one launch per block
+    int S = 1;
+    return tcd_pick(((N + tcd::BM - 1) / tcd::BM) * blocks, K / tcd::BK, S) > 0;  // more blocks: one wave, one launch
+}
+
 int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N, int K, const Epi& e, int* err,
                     cudaStream_t st) {
-    if (T <= 0 || T > 2 * tcd::MAXTB || N <= 0 || K % tcd::BK != 0 || !X_lo) return 0;
+    if (!X_lo || !gemm_tcd_takes(T, N, K)) return 0;
     if (e.mode != EPI_STORE_F32 && e.mode != EPI_ADD_F32 && e.mode != EPI_SWIGLU && e.mode != EPI_LOGITS &&
         e.mode != EPI_QKROPE)
         return 0;
@@ -1564,47 +1619,13 @@ int launch_gemm_tcd(const bf16* X, const bf16* X_lo, const bf16* W, int T, int N
     const int TB = blocks > 1 ? tcd::MAXTB : (T + 15) / 16 * 16;
     CUtensorMap mw, mh, ml;
     if (!tc_make_map(&mw, W, N, K, tcd::BM) || !tc_make_map(&mh, X, T, K, TB) || !tc_make_map(&ml, X_lo, T, K, TB)) return 0;
-    // clusters of each size that fit at once (1 CTA per SM): S is chosen so all clusters run in one wave
-    static const int cand[] = {1, 2, 3, 4, 6, 8, 12, 16};
-    static int fit[8] = {-1};
-    if (fit[0] < 0) {
-        cudaFuncSetAttribute(k_gemm_tcd, cudaFuncAttributeMaxDynamicSharedMemorySize, tcd::SMEM);
-        const bool nonport = cudaFuncSetAttribute(k_gemm_tcd, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
-        for (int i = 0; i < 8; ++i) {
-            fit[i] = 0;
-            if (cand[i] > 8 && !nonport) continue;
-            cudaLaunchConfig_t q = {};
-            q.gridDim = dim3(cand[i]);
-            q.blockDim = dim3(tcd::NT);
-            q.dynamicSmemBytes = tcd::SMEM;
-            cudaLaunchAttribute qa[1];
-            qa[0].id = cudaLaunchAttributeClusterDimension;
-            qa[0].val.clusterDim.x = cand[i];
-            qa[0].val.clusterDim.y = 1;
-            qa[0].val.clusterDim.z = 1;
-            q.attrs = qa;
-            q.numAttrs = 1;
-            int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tcd, &q) == cudaSuccess) fit[i] = n;
-        }
-        cudaGetLastError();
-    }
     const int tiles = (N + tcd::BM - 1) / tcd::BM, KT = K / tcd::BK;
-    // the most CTAs whose clusters (one per weight tile and token block) all fit in one wave
-    auto pick = [&](int clusters, int& S) {
-        int best = 0;
-        S = 1;
-        for (int i = 0; i < 8; ++i)
-            if (cand[i] <= KT && clusters <= fit[i] && clusters * cand[i] > best) {
-                best = clusters * cand[i];
-                S = cand[i];
-            }
-        return best;
-    };
     int S1 = 1, S2 = 1;
-    const int one = pick(tiles, S1);
-    // both token blocks in one launch when that keeps as many CTAs busy as a launch per block
-    const bool joint = blocks > 1 && pick(tiles * blocks, S2) >= one;
+    const int one = tcd_pick(tiles, KT, S1);
+    // every token block in one launch when that keeps as many CTAs busy as a launch per block (more
+    // than two blocks: whenever it fits one wave, which gemm_tcd_takes checked)
+    const bool joint = blocks > 2 || (blocks > 1 && tcd_pick(tiles * blocks, KT, S2) >= one);
+    if (blocks > 2) tcd_pick(tiles * blocks, KT, S2);
     auto go = [&](int S, int rows, int tb_base) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(tiles * S, rows);

@@ -516,10 +516,10 @@ int launch_gemm(const bf16* X, const bf16* W, int T, int N, int K, const Epi& e,
                 int* err, const SplitK* skw) {
     if (T <= 0) return 0;
     if (e.mode == EPI_QKROPE || e.nrm_gamma || e.nrm_scale_ss)  // fused epilogues: the split-K decode GEMM only (else 0)
-        return X_lo && T > 8 && T <= 256 && gemm_tc_available() ? launch_gemm_tcd(X, X_lo, W, T, N, K, e, err, st) : 0;
+        return X_lo && T > 8 && gemm_tc_available() ? launch_gemm_tcd(X, X_lo, W, T, N, K, e, err, st) : 0;
     if (T <= 8) return launch_gemv(X, W, T, N, K, e, st, X_lo);
-    if (X_lo && T <= 256 && gemm_tc_available()) {
-        // up to 256 tokens as one or two 128-token blocks (N = 2 x block <= 256 per MMA)
+    if (X_lo && gemm_tc_available()) {
+        // 128-token blocks (N = 2 x block <= 256 per MMA); 0 if the product does not fit the kernel
         const int n = launch_gemm_tcd(X, X_lo, W, T, N, K, e, err, st);
         if (n) return n;
     }
