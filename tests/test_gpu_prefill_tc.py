@@ -8,7 +8,8 @@ chunks (the second chunk attends to cached keys of the first, its positions
 crossing cache blocks), and the 28-layer Talker's 128-position prompt. A
 prefill of at most 8 positions per sequence runs on the decode attention
 kernel with one query per token (ragged chunks of up to 8, padding tokens
-included). The engine's profile must show the expected kernel, and an engine
+included). Chunks of 257–512 tokens run their products on the split-K GEMM over three or four
+token blocks when one launch fits a wave. The engine's profile must show the expected kernel, and an engine
 that keeps every prefill on the mma.sync kernel must agree with it. Contexts
 of at most 32 keys (the Code Predictor's) run decode attention and the short
 prefill one warp per (query, KV head) in 16-key rounds.
@@ -54,6 +55,9 @@ def test_chunked_ragged_prefill_on_tcgen05():
     X = synth.normal_bf16(synth.rng_for(91, "prefill_tc"), (3, 220, 1024), 1.0)
     (h1, h2), kinds = _chunked_prefill(w, X, lens1, lens2, S1, S2)
     assert "attn_causal_tcgen05" in kinds, kinds
+    # 390 and 270 tokens: the split-K GEMM over three or four 128-token blocks where one launch fits
+    # a wave (QKV with the fused q/k norm + RoPE + append), the dense GEMM for gate/up at 390
+    assert {"gemm_tcgen05_decode", "gemm_tcgen05"} <= kinds and "qk_norm_rope_append" not in kinds, kinds
     m0 = O.Backbone(w, SHAPE)
     for b in range(3):
         cache = m0.new_cache()
