@@ -452,9 +452,10 @@ const char* tts_bb_profile_report(tts_bb* h);
  * whose host framework owns every device allocation, or a real-time audio
  * thread that must not block in the allocator).
  *
- * It runs the same split-K GQA flash-decode kernels as tts_bb_decode_step on
- * the caller's own buffers; the split partials go to a fixed array in device
- * memory that is part of the library (TTS_BB_STATIC_ATTN_MAX_B x 16 heads x
+ * It runs the same GQA decode attention kernels as tts_bb_decode_step on the
+ * caller's own buffers (split-K flash decode; for max_position < 32 one warp
+ * per query and KV head, which writes no partials); the split partials go to
+ * a fixed array in device memory that is part of the library (TTS_BB_STATIC_ATTN_MAX_B x 16 heads x
  * TTS_BB_STATIC_ATTN_MAX_SPLITS x 130 floats = 4.26 MB, held by every GPU that
  * loads the library until the process exits). No cudaMalloc or cudaFree, no
  * allocating library call.
@@ -476,8 +477,7 @@ const char* tts_bb_profile_report(tts_bb* h);
  * 1..TTS_BB_STATIC_ATTN_MAX_B or a max_position the page table cannot hold;
  * TTS_BB_E_CUDA if a CUDA error is already pending when the call starts (it
  * is left pending, not cleared) or a launch fails. The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current:
- * make that first call before any stream capture. Every call shares the
+ * array's device address (cudaGetSymbolAddress) with that device current. Every call shares the
  * array and overwrites all the partials it reads, so nothing needs clearing
  * between calls; calls that overlap on the GPU (other streams, other host
  * threads) race on it and must be serialised by the caller. */
